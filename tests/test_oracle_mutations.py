@@ -1,0 +1,148 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check that the pins catch them.
+
+Each mutant replaces one oracle function with a subtly wrong variant (a wrong
+sign, a swapped index, a dropped term, another rounding rule); at least one
+pin must then fail.  This shows the pins constrain every part of the oracle.
+"""
+
+import numpy as np
+import pytest
+
+from oracle import kvq_oracle as ko
+import test_oracle_pins as pins
+
+F32 = np.float32
+
+
+_orig = {"fwht": ko.fwht, "pack_q4_0": ko.pack_q4_0, "quantize_q4_0": ko.quantize_q4_0,
+         "quantize_q8_0": ko.quantize_q8_0, "bf16_bits": ko.bf16_bits,
+         "signed_max_magnitude": ko.signed_max_magnitude, "rotation_matrix": ko.rotation_matrix,
+         "sylvester_hadamard": ko.sylvester_hadamard, "pack_q5_0": ko.pack_q5_0,
+         "dequantize": ko.dequantize, "softmax_attention": ko.softmax_attention}
+
+
+def _fwht_transposed_pairs(x, group):
+    # butterfly with (a-b, a+b): a sign/ordering slip
+    y = np.array(x, dtype=np.float64, copy=True)
+    shape, d, h = y.shape, y.shape[-1], 1
+    while h < group:
+        v = y.reshape(-1, d // group, group // (2 * h), 2, h)
+        a, b = v[:, :, :, 0, :].copy(), v[:, :, :, 1, :].copy()
+        v[:, :, :, 0, :], v[:, :, :, 1, :] = a - b, a + b
+        y = v.reshape(shape)
+        h *= 2
+    return y / np.sqrt(group)
+
+
+def _pack_q4_swapped(codes):
+    c = np.asarray(codes, dtype=np.uint8)
+    return (c[..., 16:] | (c[..., :16] << 4)).astype(np.uint8)
+
+
+def _pack_q4_interleaved(codes):
+    c = np.asarray(codes, dtype=np.uint8)
+    return (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
+
+
+def _q4_rounding(y):
+    b = ko._blocks(y)
+    m, _ = ko.signed_max_magnitude(b)
+    d = (m / F32(-8)).astype(F32)
+    inv = ko._inverse(d)
+    v = (b * inv[..., None]).astype(F32) + F32(8.0)
+    codes = np.clip(np.rint(v), 0, 15)   # round-half-even instead of trunc(x + 8.5)
+    return ko.f16_bits(d), codes.astype(np.uint8)
+
+
+def _q4_amax_scale(y):
+    b = ko._blocks(y)
+    _, amax = ko.signed_max_magnitude(b)
+    d = (amax / F32(-8)).astype(F32)       # sign of the max dropped
+    inv = ko._inverse(d)
+    v = ((b * inv[..., None]).astype(F32) + F32(8.5)).astype(F32)
+    return ko.f16_bits(d), np.minimum(15, np.trunc(v)).astype(np.uint8)
+
+
+def _q8_half_even(y):
+    b = ko._blocks(y)
+    amax = np.max(np.abs(b), axis=-1).astype(F32)
+    d = (amax / F32(127)).astype(F32)
+    v = (b * ko._inverse(d)[..., None]).astype(F32)
+    return ko.f16_bits(d), np.rint(v).astype(np.int8)
+
+
+def _bf16_truncate(x):
+    u = np.asarray(x, dtype=F32).view(np.uint32)
+    return (u >> 16).astype(np.uint16)
+
+
+def _signed_max_last_tie(blocks):
+    a = np.abs(blocks)
+    idx = blocks.shape[-1] - 1 - np.argmax(a[..., ::-1], axis=-1)
+    amax = np.take_along_axis(a, idx[..., None], axis=-1)[..., 0]
+    m = np.take_along_axis(blocks, idx[..., None], axis=-1)[..., 0]
+    return np.where(amax > 0, m, F32(0)).astype(F32), amax.astype(F32)
+
+
+def _rotation_unnormalized(d):
+    return _orig["rotation_matrix"](d) * np.sqrt(ko.rotation_group(d))
+
+
+def _rotation_natural_blocks(d):
+    # block-diagonal built with the wrong block size for non-power-of-two d
+    if ko.is_power_of_two(d):
+        return _orig["rotation_matrix"](d)
+    g = 32
+    hg = ko.sylvester_hadamard(g) / np.sqrt(g)
+    r = np.zeros((d, d))
+    for i in range(d // g):
+        r[i * g:(i + 1) * g, i * g:(i + 1) * g] = hg
+    return r
+
+
+def _pack_q5_high_bits_reversed(codes):
+    qs, qh = _orig["pack_q5_0"](codes)
+    rev = np.zeros_like(qh)
+    for j in range(32):
+        rev |= ((qh >> np.uint32(j)) & np.uint32(1)) << np.uint32(31 - j)
+    return qs, rev
+
+
+def _dequant_no_offset(qtype, d_bits, codes):
+    dv = ko.f16_value(d_bits)[..., None]
+    x = np.asarray(codes).astype(np.float64) * dv
+    return x.reshape(x.shape[:-2] + (x.shape[-2] * 32,))
+
+
+def _softmax_no_max_shift_scale(q, K, V, scale):
+    return _orig["softmax_attention"](q, K, V, scale * 1.01)
+
+
+MUTANTS = [
+    ("fwht", _fwht_transposed_pairs, [pins.test_rotate_golden_vectors]),
+    ("pack_q4_0", _pack_q4_swapped, [pins.test_packing_golden]),
+    ("pack_q4_0", _pack_q4_interleaved, [pins.test_packing_golden]),
+    ("quantize_q4_0", _q4_rounding, [pins.test_golden_blocks]),
+    ("quantize_q4_0", _q4_amax_scale, [pins.test_golden_blocks]),
+    ("quantize_q8_0", _q8_half_even, [pins.test_golden_blocks]),
+    ("bf16_bits", _bf16_truncate, [pins.test_bf16_rounding_matches_torch]),
+    ("signed_max_magnitude", _signed_max_last_tie, [pins.test_signed_max_first_index_on_ties, pins.test_golden_blocks]),
+    ("rotation_matrix", _rotation_unnormalized, [lambda: pins.test_rotation_orthonormal_symmetric(128)]),
+    ("rotation_matrix", _rotation_natural_blocks, [lambda: pins.test_rotation_orthonormal_symmetric(192)]),
+    ("pack_q5_0", _pack_q5_high_bits_reversed, [pins.test_packing_golden]),
+    ("dequantize", _dequant_no_offset, [lambda: pins.test_quantizer_error_bounds("q4_0")]),
+    ("softmax_attention", _softmax_no_max_shift_scale, [pins.test_decode_gqa_bruteforce]),
+]
+
+
+@pytest.mark.parametrize("i", range(len(MUTANTS)))
+def test_pins_catch_planted_mistake(monkeypatch, i):
+    name, fn, checks = MUTANTS[i]
+    monkeypatch.setattr(ko, name, fn)
+    failed = 0
+    for chk in checks:
+        try:
+            chk()
+        except (AssertionError, ValueError):
+            failed += 1
+    assert failed >= 1, f"mutant of {name} ({fn.__name__}) passed every pin"
