@@ -1,0 +1,429 @@
+#!/usr/bin/env python
+"""Throughput of the rotated, block-quantized KV-cache hot path on GB300.
+
+A step = one decode step of the 64k-context workload (4 sequences x 65,536
+tokens, 24 query / 4 KV heads, head_dim 256, K q8_0 / V q4_0, bf16 tail of
+1024 tokens): rotate + quantize + append one new token per sequence, then
+decode attention over body + tail for all 24 heads.  The value is achieved
+HBM bandwidth in GB/s: algorithmic bytes (packed body + bf16 tail + q/out of
+the decode, plus the append's input, packed output and tail writes) divided by
+the measured step time.  Inputs are larger than L2 (446 MB per step), so no
+flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs under torch.distributed.run: every rank holds its own replica of
+the workload (the path shards over (sequence, KV head) with no exchange), and
+the value is the bytes of all ranks over the slowest rank's time.
+--impl reference times the CPU oracle (numpy, float64) on a bounded sample of
+the same workload on the host cores; it is test infrastructure, not a product
+path.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from rotated_bit_kv_kvq_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "quantized-KV decode attention: achieved HBM GB/s vs 8 TB/s; append tokens/s"
+BLOCK_BYTES = {"q4_0": 18, "q5_0": 22, "q8_0": 34}
+
+
+# ---------------------------------------------------------------------------
+# byte accounting (algorithmic bytes)
+# ---------------------------------------------------------------------------
+def token_bytes(w: wl.Workload) -> int:
+    """Packed body bytes of one token of one KV head, K + V."""
+    nb = w.head_dim // 32
+    return nb * (BLOCK_BYTES[w.k_type] + BLOCK_BYTES[w.v_type])
+
+
+def decode_bytes(w: wl.Workload, lengths, q_bytes=2, out_bytes=2) -> int:
+    tot = 0
+    for n in lengths:
+        body = max(0, int(n) - w.tail_len)
+        tail = min(int(n), w.tail_len)
+        tot += w.n_kv_heads * (body * token_bytes(w) + tail * 2 * w.head_dim * 2)
+    tot += len(lengths) * w.n_q_heads * w.head_dim * (q_bytes + out_bytes)
+    return tot
+
+
+def append_bytes(w: wl.Workload, n_new: int, in_bytes=2) -> int:
+    per = w.n_kv_heads * n_new * w.batch
+    return per * (2 * w.head_dim * in_bytes + token_bytes(w) + (2 * w.head_dim * 2 if w.tail_len else 0))
+
+
+# ---------------------------------------------------------------------------
+# environment helpers
+# ---------------------------------------------------------------------------
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def recorded_traffic(kernel_file: str):
+    """ncu DRAM bytes per launch recorded in profiles/, valid only while the
+    kernel source is unchanged (its hash is stored beside the number)."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "decode_b4_ctx64k_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    src = os.path.join(ROOT, "rotated_bit_kv_kvq_gb300", "csrc", kernel_file)
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    return d.get("bytes_per_launch") if d.get("source_sha256") == h else None
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        self.path = os.path.join("/tmp", f"kvq_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu), "-lms", "100"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def fill_cache(torch, kvq, cache, w: wl.Workload, n_fill: int, seed: int = 0):
+    """Seeded synthetic history (N(0,1), outlier channels x20, bf16), appended
+    through the library's own write path in chunks."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    k_chan = wl.outlier_channels(rng, w.n_kv_heads, w.head_dim, w.n_outliers)
+    v_chan = wl.outlier_channels(rng, w.n_kv_heads, w.head_dim, w.n_outliers)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    kmask = torch.ones(w.n_kv_heads, w.head_dim, device="cuda")
+    vmask = torch.ones(w.n_kv_heads, w.head_dim, device="cuda")
+    for h in range(w.n_kv_heads):
+        kmask[h, torch.tensor(k_chan[h])] = 20.0
+        vmask[h, torch.tensor(v_chan[h])] = 20.0
+    chunk = 8192
+    done = 0
+    while done < n_fill:
+        n = min(chunk, n_fill - done)
+        k = (torch.randn(w.batch, n, w.n_kv_heads, w.head_dim, generator=gen, device="cuda") * kmask).to(torch.bfloat16)
+        v = (torch.randn(w.batch, n, w.n_kv_heads, w.head_dim, generator=gen, device="cuda") * vmask).to(torch.bfloat16)
+        kvq.kvq_rotate_quantize_append(cache.desc, k, v)
+        done += n
+    torch.cuda.synchronize()
+    st, bits = kvq.kvq_sync_status(cache.desc)
+    assert st == 0, (st, bits)
+    return kmask, vmask, gen
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from rotated_bit_kv_kvq_gb300 import kvq
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    w = wl.WORKLOADS[args.workload]
+    K, W = args.steps, args.warmup
+    n_new = max(1, w.append_per_step)
+    extra = (W + K) * n_new
+    n_start = w.ctx - n_new                       # first timed step decodes at exactly ctx tokens
+    n_fill = n_start - W * n_new
+    cache = kvq.KVCache(w.batch, w.n_kv_heads, w.head_dim, w.max_ctx(extra + 64), w.tail_len, w.k_type, w.v_type)
+    kmask, vmask, gen = fill_cache(torch, kvq, cache, w, n_fill, seed=rank)
+
+    # per-step inputs, generated ahead of the timed region
+    P = 8
+    ks = [(torch.randn(w.batch, n_new, w.n_kv_heads, w.head_dim, generator=gen, device="cuda") * kmask).to(torch.bfloat16)
+          for _ in range(P)]
+    vs = [(torch.randn(w.batch, n_new, w.n_kv_heads, w.head_dim, generator=gen, device="cuda") * vmask).to(torch.bfloat16)
+          for _ in range(P)]
+    qs = [torch.randn(w.batch, w.n_q_heads, w.head_dim, generator=gen, device="cuda").to(torch.bfloat16) for _ in range(P)]
+    out = torch.empty(w.batch, w.n_q_heads, w.head_dim, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(kvq.kvq_decode_workspace_bytes(cache.desc, w.n_q_heads), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    seq0 = cache.seq_len.clone()
+
+    def step(i):
+        kvq.kvq_rotate_quantize_append(cache.desc, ks[i % P], vs[i % P], stream=stream)
+        kvq.kvq_decode_attention(cache.desc, qs[i % P], out, ws, stream=stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # ---- device-resident timed region: W warm-up steps, then K steps --------------
+    for i in range(W):
+        step(i)
+    torch.cuda.synchronize()
+    lens_first = cache.seq_len.cpu().numpy() + n_new
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(K):
+        step(W + i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    step_ms = e0.elapsed_time(e1) / K
+    st, bits = kvq.kvq_sync_status(cache.desc)
+    assert st == 0, (st, bits)
+    total_bytes = 0
+    for i in range(K):
+        lens = lens_first + i * n_new
+        total_bytes += decode_bytes(w, lens) + append_bytes(w, n_new)
+
+    # ---- decode kernel alone (the dominant kernel), same context --------------------
+    dec_lens = cache.seq_len.cpu().numpy()
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(3):
+        kvq.kvq_decode_attention(cache.desc, qs[i % P], out, ws, stream=stream)
+    torch.cuda.synchronize()
+    d0.record(stream)
+    for i in range(K):
+        kvq.kvq_decode_attention(cache.desc, qs[i % P], out, ws, stream=stream)
+    d1.record(stream)
+    torch.cuda.synchronize()
+    dec_ms = d0.elapsed_time(d1) / K
+    dec_bytes = decode_bytes(w, dec_lens)
+
+    # ---- append alone (one token per sequence) ----------------------------------------
+    cache.seq_len.copy_(seq0)
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a0.record(stream)
+    for i in range(K):
+        kvq.kvq_rotate_quantize_append(cache.desc, ks[i % P], vs[i % P], stream=stream)
+    a1.record(stream)
+    torch.cuda.synchronize()
+    app_ms = a0.elapsed_time(a1) / K
+
+    # ---- end to end through the public API, host buffers -----------------------------
+    cache.seq_len.copy_(seq0)
+    hk = [t.cpu().pin_memory() for t in ks]
+    hv = [t.cpu().pin_memory() for t in vs]
+    hq = [t.cpu().pin_memory() for t in qs]
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dk = torch.empty_like(ks[0]); dv = torch.empty_like(vs[0]); dq = torch.empty_like(qs[0])
+
+    def e2e_step(i):
+        dk.copy_(hk[i % P], non_blocking=True)
+        dv.copy_(hv[i % P], non_blocking=True)
+        dq.copy_(hq[i % P], non_blocking=True)
+        kvq.kvq_rotate_quantize_append(cache.desc, dk, dv, stream=stream)
+        kvq.kvq_decode_attention(cache.desc, dq, out, ws, stream=stream)
+        hout.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    for i in range(W):
+        e2e_step(i)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(K):
+        e2e_step(W + i)
+    t1 = time.perf_counter()
+    barrier()
+    e2e_ms = (t1 - t0) * 1e3 / K
+    h2d = sum(t.numel() * t.element_size() for t in (ks[0], vs[0], qs[0]))
+    d2h = out.numel() * out.element_size()
+
+    # ---- max over ranks -----------------------------------------------------------------
+    vals = torch.tensor([step_ms, dec_ms, app_ms, e2e_ms], dtype=torch.float64, device="cuda")
+    if world > 1:
+        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+    step_ms, dec_ms, app_ms, e2e_ms = [float(x) for x in vals.cpu()]
+
+    if rank == 0:
+        peak, peak_kind = measured_peaks()
+        achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
+        per_step_bytes = total_bytes / K
+        line = {
+            "metric": METRIC,
+            "value": round(world * per_step_bytes / (step_ms * 1e-3) / 1e9, 2),
+            "unit": "GB/s",
+            "n_gpus": world, "steps": K, "warmup": W,
+            "ms_per_step": round(step_ms, 5),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "q8_0/q4_0 codes -> fp16 mma, fp32 accumulate",
+            "data": "synthetic (seeded N(0,1), 4 outlier channels x20 per KV head, bf16)",
+            "config": {"workload": w.name, "batch": w.batch, "ctx": w.ctx, "q_heads": w.n_q_heads,
+                       "kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "k_type": w.k_type, "v_type": w.v_type,
+                       "tail_len": w.tail_len, "append_per_step": n_new,
+                       "l2": f"inputs larger than L2 ({per_step_bytes / 1e6:.1f} MB per step), no flush",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "roofline": {"bound": "hbm", "kernel": "decode (split-K + combine) at ctx "
+                         f"{int(dec_lens.max())}", "achieved": round(achieved, 1), "peak": peak,
+                         "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "bytes_per_launch": int(dec_bytes), "ms_per_launch": round(dec_ms, 5),
+                         "traffic": recorded_traffic("kvq_decode.cu")},
+            "append": {"tokens_per_s": round(w.batch * n_new / (app_ms * 1e-3), 1), "ms_per_call": round(app_ms, 5)},
+            "e2e": {"value": round(world * per_step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                    "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 3 * K,
+            "clocks": clk,
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle (cpu_baseline leg and --impl reference)
+# ---------------------------------------------------------------------------
+def oracle_pair_sample(w: wl.Workload, seed: int = 0):
+    """One (sequence, KV head) pair of the workload at full context, in the oracle."""
+    from oracle import kvq_oracle as ko
+    rng = np.random.Generator(np.random.PCG64(seed))
+    n = w.ctx
+    k = rng.standard_normal((1, n, 1, w.head_dim), dtype=np.float32)
+    v = rng.standard_normal((1, n, 1, w.head_dim), dtype=np.float32)
+    k[..., rng.choice(w.head_dim, w.n_outliers, replace=False)] *= 20
+    v[..., rng.choice(w.head_dim, w.n_outliers, replace=False)] *= 20
+    k = wl.round_bf16(k) if w.dtype == "bf16" else k
+    v = wl.round_bf16(v) if w.dtype == "bf16" else v
+    rot = ko.rotation_enabled(w.head_dim)
+    oc = ko.OracleCache(1, 1, w.head_dim, w.max_ctx(), w.tail_len, w.k_type, w.v_type, rot, rot)
+    oc.append(k, v)
+    q = rng.standard_normal((1, w.group, w.head_dim)).astype(np.float32)
+    # one KV head's share: packed body + bf16 tail + q/out (bf16) of its query heads
+    nbytes = (max(0, n - w.tail_len) * token_bytes(w) + min(n, w.tail_len) * 4 * w.head_dim
+              + w.group * w.head_dim * 4)
+    return oc, q, nbytes
+
+
+def cpu_baseline(w: wl.Workload, budget_s: float = 15.0):
+    from oracle import kvq_oracle as ko
+    oc, q, nbytes = oracle_pair_sample(w)
+    times = []
+    t_all = time.perf_counter()
+    while True:
+        t0 = time.perf_counter()
+        ko.decode_attention(oc, q)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_all > budget_s or len(times) >= 30:
+            break
+    per = statistics.median(times)
+    return {"value": round(nbytes / per / 1e9, 4), "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"decode attention of 1 of {w.batch * w.n_kv_heads} (sequence, KV head) pairs at "
+                      f"{w.ctx} tokens ({w.group} query heads), float64 numpy, {len(times)} repetitions, "
+                      f"median {per:.3f} s",
+            "threads_note": "numpy elementwise work is single-threaded; its BLAS products may use all cores"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from oracle import kvq_oracle as ko
+    w = wl.WORKLOADS[args.workload]
+    oc, q, nbytes = oracle_pair_sample(w)
+    for _ in range(args.warmup):
+        ko.decode_attention(oc, q)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        ko.decode_attention(oc, q)
+    dt = (time.perf_counter() - t0) / args.steps
+    val = round(nbytes / dt / 1e9, 4)
+    sample = (f"each step: decode attention of 1 of {w.batch * w.n_kv_heads} (sequence, KV head) pairs at "
+              f"{w.ctx} tokens, float64 numpy oracle")
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name, "batch": w.batch, "ctx": w.ctx,
+                                            "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads,
+                                            "head_dim": w.head_dim, "k_type": w.k_type, "v_type": w.v_type,
+                                            "tail_len": w.tail_len},
+            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=wl.HEADLINE,
+                    choices=sorted(k for k, v in wl.WORKLOADS.items() if not v.prefill))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

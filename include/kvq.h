@@ -1,0 +1,244 @@
+/*
+ * kvq.h -- C ABI of the rotated, block-quantized KV-cache attention library.
+ *
+ * What it computes.  Per attention head, K and V vectors are multiplied by a
+ * normalized Walsh-Hadamard matrix H/sqrt(G) and stored rotated; queries are
+ * rotated the same way, so q.k -- and the attention scores -- are unchanged,
+ * and the attention output is rotated back at the end (velog post
+ * "fix-kv-cache-quantization-outliers", section 아다마르 회전).  Rotation is
+ * used when head_dim >= 64 and a multiple of 64, and K / V rotation can each
+ * be switched off (same post, section 적용 및 배경 기술).  The rotated vectors
+ * are stored in the GGUF q4_0 / q5_0 / q8_0 block formats, which the same
+ * section says stay unchanged: 32 values per block with an fp16 scale.  A
+ * BF16 "precision tail" keeps the most recent tokens unquantized (aitrends.kr
+ * "KV 캐시 양자화 벤치마크: KVarN과 Precision Tail", section 용어 해설).
+ *
+ * Conventions for every entry point.
+ *  - Ownership: the library never allocates, frees or synchronizes (except
+ *    kvq_sync_status).  Every pointer in kvq_cache and every q / k / v / out /
+ *    workspace pointer is caller-owned DEVICE memory on the current CUDA
+ *    device; host pointers are marked as such.  `stream` is a cudaStream_t
+ *    (NULL = legacy default stream); all work is enqueued on it and the call
+ *    returns without waiting.
+ *  - Errors: argument errors are detected on the host before any launch and
+ *    returned synchronously; nothing is launched then.  Errors that depend on
+ *    device-resident values (sequence lengths) set bits in the cache's status
+ *    words; kvq_sync_status reports them.  KVQ_ERR_CUDA reports a launch
+ *    error (or an earlier asynchronous error surfacing at launch).
+ *  - Calls that touch the same cache must be ordered on one stream.
+ *  - Layouts are row-major; [a][b] means b varies fastest.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define KVQ_API __attribute__((visibility("default")))
+#else
+#define KVQ_API
+#endif
+
+#define KVQ_VERSION 1
+
+/* ---- status codes ------------------------------------------------------ */
+typedef int32_t kvq_status;
+#define KVQ_OK                 0
+#define KVQ_ERR_INVALID_ARG   -1  /* null pointer, bad size, bad alignment, bad enum  */
+#define KVQ_ERR_UNSUPPORTED   -2  /* valid but not built: head_dim, type pair, rotation on an ineligible head_dim */
+#define KVQ_ERR_WORKSPACE     -3  /* workspace pointer NULL or ws_bytes too small      */
+#define KVQ_ERR_CUDA          -4  /* a CUDA runtime call or launch failed              */
+#define KVQ_ERR_TIMEOUT       -5  /* a bounded on-device wait gave up (see status bit) */
+#define KVQ_ERR_DEVICE_RANGE  -6  /* device-side range check failed (see status bits)  */
+
+/* ---- block formats (GGUF, unchanged) ----------------------------------- */
+#define KVQ_TYPE_Q4_0 0   /* fp16 d = m/-8,  code = min(15, trunc(x/d + 8.5)),  x = (code-8)*d  */
+#define KVQ_TYPE_Q5_0 1   /* fp16 d = m/-16, code = min(31, trunc(x/d + 16.5)), x = (code-16)*d */
+#define KVQ_TYPE_Q8_0 2   /* fp16 d = amax/127, code = roundf(x/d) in [-127,127], x = code*d     */
+/* m = the value of largest magnitude in the 32-value block (first on ties). */
+
+/* ---- element types of q / k / v / out ----------------------------------- */
+#define KVQ_F32  0
+#define KVQ_BF16 1
+#define KVQ_F16  2
+
+/* ---- cache flags (kvq_cache.flags) ------------------------------------- */
+#define KVQ_ROT_AUTO   1u  /* rotate K and V when head_dim >= 64 and %64 == 0, else silently off */
+#define KVQ_ROT_K_OFF  2u  /* no K rotation (queries are then not rotated either)             */
+#define KVQ_ROT_V_OFF  4u  /* no V rotation (the output is then not rotated back)             */
+/* flags == 0 (no KVQ_ROT_AUTO): rotation is requested explicitly; an
+ * ineligible head_dim then gives KVQ_ERR_UNSUPPORTED unless both _OFF bits
+ * are set. */
+
+/* ---- append flags -------------------------------------------------------- */
+#define KVQ_INPUT_PREROTATED 1u  /* k / v are already rotated: store them as given */
+
+/* ---- planes of a cache (kvq_plane_bytes) --------------------------------- */
+#define KVQ_PLANE_K_QS    0  /* uint8 [batch][kv_heads][max_ctx][qs_row]    qs_row = d/2 (q4_0, q5_0) or d (q8_0) */
+#define KVQ_PLANE_K_QH    1  /* uint32 [batch][kv_heads][max_ctx][d/32]     q5_0 only (0 bytes otherwise)        */
+#define KVQ_PLANE_K_D     2  /* fp16 [batch][kv_heads][max_ctx][d/32]       block scales                         */
+#define KVQ_PLANE_V_QS    3
+#define KVQ_PLANE_V_QH    4
+#define KVQ_PLANE_V_D     5
+#define KVQ_PLANE_K_TAIL  6  /* bf16 [batch][kv_heads][tail_len][d]          rotated values, slot = pos % tail_len */
+#define KVQ_PLANE_V_TAIL  7
+#define KVQ_PLANE_SEQ_LEN 8  /* int32 [batch]                               tokens stored per sequence           */
+#define KVQ_PLANE_STATUS  9  /* uint32 [4]                                  device status words; zero before use */
+#define KVQ_NUM_PLANES   10
+
+/* device status word 0 bits (read by kvq_sync_status) */
+#define KVQ_DEV_ERR_APPEND_RANGE  1u  /* an append would pass max_ctx, or n_new_per_seq[b] not in [0, n_new] */
+#define KVQ_DEV_ERR_PREFILL_RANGE 2u  /* a prefill query position is negative                              */
+#define KVQ_DEV_ERR_TIMEOUT       4u  /* a bounded wait on a shared-memory barrier gave up                 */
+
+/*
+ * The cache descriptor.  Body planes hold the packed payload of every block:
+ * block j of token t of (seq b, kv head h) has its qs bytes at
+ * qs + ((b*kv_heads + h)*max_ctx + t)*qs_row + j*(16 or 32), its high-bit
+ * word (q5_0) at qh[((b*kv_heads + h)*max_ctx + t)*(d/32) + j] and its scale
+ * at d[same index].  The bytes of one block are exactly the GGUF block
+ * payload; kvq_dequant_debug can export them in GGUF array-of-structs order.
+ *
+ * Requirements (checked by every call): head_dim % 32 == 0 and
+ * 32 <= head_dim <= 256; max_ctx % 64 == 0; tail_len >= 0; every non-NULL
+ * plane 16-byte aligned; k_qh / v_qh non-NULL only for q5_0 (required then);
+ * k_tail / v_tail non-NULL iff tail_len > 0.  Decode and prefill support
+ * head_dim in {64, 128, 256} (plus 192 for q4_0/q4_0); append and debug
+ * support every multiple of 32 up to 256.
+ */
+typedef struct kvq_cache {
+  int32_t batch;        /* sequences                                   */
+  int32_t n_kv_heads;   /* KV heads per sequence                       */
+  int32_t head_dim;     /* d                                           */
+  int32_t max_ctx;      /* token capacity per sequence (multiple of 64)*/
+  int32_t tail_len;     /* T: recent tokens also kept in bf16 (0 = off)*/
+  int32_t k_type;       /* KVQ_TYPE_*                                  */
+  int32_t v_type;       /* KVQ_TYPE_*                                  */
+  uint32_t flags;       /* KVQ_ROT_*                                   */
+  void* k_qs; void* k_qh; void* k_d;
+  void* v_qs; void* v_qh; void* v_d;
+  void* k_tail; void* v_tail;
+  int32_t* seq_len;     /* device int32 [batch]                        */
+  uint32_t* status;     /* device uint32 [4], zero-initialised         */
+} kvq_cache;
+
+/* Library version (KVQ_VERSION). */
+KVQ_API int32_t kvq_version(void);
+
+/* Human-readable name of a status code (static string). */
+KVQ_API const char* kvq_status_string(kvq_status s);
+
+/* Bytes the caller must allocate for plane `plane` (KVQ_PLANE_*) of a cache
+ * with the given sizes and types; pointers in `c` are ignored.  Returns 0 for
+ * an absent plane (qh of a non-q5_0 type, tail of tail_len 0) or an invalid
+ * descriptor. */
+KVQ_API size_t kvq_plane_bytes(const kvq_cache* c, int32_t plane);
+
+/* Host-side check of a descriptor (sizes, types, pointers, alignment). */
+KVQ_API kvq_status kvq_cache_check(const kvq_cache* c);
+
+/* The enable rule (velog 적용 및 배경 기술): writes 1/0 to *rot_k and *rot_v
+ * (host pointers).  KVQ_ROT_AUTO turns rotation on iff head_dim >= 64 and
+ * head_dim % 64 == 0; the _OFF bits switch each side off; an explicit request
+ * (no AUTO bit) on an ineligible head_dim returns KVQ_ERR_UNSUPPORTED. */
+KVQ_API kvq_status kvq_resolve_rotation(const kvq_cache* c, int32_t* rot_k, int32_t* rot_v);
+
+/*
+ * Rotate, quantize and append new tokens (write path).
+ *   k, v          device [batch][n_new][n_kv_heads][head_dim] of in_dtype
+ *   n_new         rows per sequence in k / v (>= 0; 0 is a no-op)
+ *   n_new_per_seq device int32 [batch] or NULL: tokens actually appended for
+ *                 sequence b (0 <= n_new_per_seq[b] <= n_new); rows past it
+ *                 are ignored.  NULL means n_new for every sequence.
+ *   append_flags  KVQ_INPUT_PREROTATED or 0
+ * Token i of sequence b goes to position p = seq_len[b] + i: its rotated
+ * values are quantized into the body planes at p, and if p is among the last
+ * tail_len positions written by this call its rotated values (bf16, round to
+ * nearest even) also go to tail slot p % tail_len.  Afterwards seq_len[b] has
+ * grown by the tokens appended.  A sequence whose append would pass max_ctx
+ * (or whose count is out of range) is left untouched and sets
+ * KVQ_DEV_ERR_APPEND_RANGE.  Uses status word 1 as a completion counter.
+ */
+KVQ_API kvq_status kvq_rotate_quantize_append(const kvq_cache* c, const void* k, const void* v,
+                                      int32_t in_dtype, int32_t n_new,
+                                      const int32_t* n_new_per_seq, uint32_t append_flags,
+                                      void* stream);
+
+/* Workspace bytes kvq_decode_attention needs for this cache and n_q_heads on
+ * the current device (0 on an invalid descriptor). */
+KVQ_API size_t kvq_decode_workspace_bytes(const kvq_cache* c, int32_t n_q_heads);
+
+/*
+ * One decode step of attention for every sequence (read path).
+ *   q      device [batch][n_q_heads][head_dim] of q_dtype (unrotated)
+ *   out    device [batch][n_q_heads][head_dim] of out_dtype (original basis)
+ *   scale  softmax scale; 0 means 1/sqrt(head_dim)
+ * Query head h uses KV head h / (n_q_heads / n_kv_heads).  Scores are taken
+ * in the rotated basis (q rotated when K rotation is on); keys at positions
+ * [n - tail_len, n) come from the bf16 tail, older ones from the quantized
+ * body (n = seq_len[b]); the softmax-weighted sum of values is rotated back
+ * when V rotation is on.  A sequence with n == 0 yields zeros.
+ * n_q_heads must be a multiple of n_kv_heads.  workspace: device memory of at
+ * least kvq_decode_workspace_bytes(c, n_q_heads) bytes, 16-byte aligned.
+ */
+KVQ_API kvq_status kvq_decode_attention(const kvq_cache* c, const void* q, int32_t q_dtype,
+                                int32_t n_q_heads, float scale, void* out, int32_t out_dtype,
+                                void* workspace, size_t ws_bytes, void* stream);
+
+/* Workspace bytes kvq_prefill_attention needs (0 on an invalid descriptor). */
+KVQ_API size_t kvq_prefill_workspace_bytes(const kvq_cache* c, int32_t n_q_heads, int32_t n_tokens);
+
+/*
+ * Chunked attention of a block of queries per sequence over the cache
+ * (prompt processing), after their K/V have been appended.
+ *   q       device [batch][n_tokens][n_q_heads][head_dim] of q_dtype
+ *   q_pos0  device int32 [batch] or NULL: absolute position of query 0 of
+ *           sequence b; NULL means seq_len[b] - n_tokens (the just-appended
+ *           prompt).  A negative position sets KVQ_DEV_ERR_PREFILL_RANGE and
+ *           that sequence's rows are written as zeros.
+ *   causal  non-zero: query at position p sees keys t <= p; always t < seq_len[b]
+ *   chunk   queries per processing chunk (multiple of 64, or 0 for 512); it
+ *           orders the work and does not change the result
+ *   out     device [batch][n_tokens][n_q_heads][head_dim] of out_dtype
+ * Body / tail selection, rotation and scale are as in kvq_decode_attention.
+ */
+KVQ_API kvq_status kvq_prefill_attention(const kvq_cache* c, const void* q, int32_t q_dtype,
+                                 int32_t n_q_heads, int32_t n_tokens, const int32_t* q_pos0,
+                                 int32_t causal, int32_t chunk, float scale, void* out,
+                                 int32_t out_dtype, void* workspace, size_t ws_bytes,
+                                 void* stream);
+
+/*
+ * Inspection of stored tokens (test aid).
+ *   which          0 = K body, 1 = V body, 2 = K tail, 3 = V tail
+ *   t0, count      positions [t0, t0+count) of (seq, kv_head); body positions
+ *                  must lie below max_ctx; tail reads slot p % tail_len
+ *   original_basis non-zero: rotate the values back when that side is rotated
+ *   out            device float [count][head_dim] (NULL allowed)
+ *   blocks_ggml    device bytes [count][head_dim/32][18|22|34] or NULL: the
+ *                  body blocks in GGUF array-of-structs byte order (body only)
+ * No range check against seq_len: positions that were never written return
+ * whatever the planes hold.
+ */
+KVQ_API kvq_status kvq_dequant_debug(const kvq_cache* c, int32_t seq, int32_t kv_head, int32_t which,
+                             int32_t t0, int32_t count, int32_t original_basis, float* out,
+                             void* blocks_ggml, void* stream);
+
+/*
+ * Synchronizes `stream`, reads and clears the cache's device status word 0
+ * (raw bits to *device_bits, a host pointer, if non-NULL) and reports:
+ * KVQ_ERR_CUDA for a pending CUDA error, KVQ_ERR_TIMEOUT or
+ * KVQ_ERR_DEVICE_RANGE for status bits, else KVQ_OK.
+ */
+KVQ_API kvq_status kvq_sync_status(const kvq_cache* c, void* stream, uint32_t* device_bits);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

@@ -1,0 +1,218 @@
+// Device helpers shared by the kvq kernels (sm_103a).
+//
+//  * warp Walsh-Hadamard transform of one head vector held in registers
+//  * shared-memory barrier (mbarrier) + bulk / tensor copy wrappers with
+//    bounded waits
+//  * warp tensor-core fragments: ldmatrix, movmatrix, mma.m16n8k16 (f16)
+//  * byte -> fp16 code conversions used by the dequantizing loaders
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "kvq.h"
+
+namespace kvq {
+
+constexpr int kQK = 32;  // values per quantization block
+
+// ---------------------------------------------------------------------------
+// Format traits (GGUF q4_0 / q5_0 / q8_0 payloads split into planes)
+// ---------------------------------------------------------------------------
+template <int QT> struct Fmt;
+template <> struct Fmt<KVQ_TYPE_Q4_0> { static constexpr int qs_per_block = 16; static constexpr bool has_qh = false; };
+template <> struct Fmt<KVQ_TYPE_Q5_0> { static constexpr int qs_per_block = 16; static constexpr bool has_qh = true; };
+template <> struct Fmt<KVQ_TYPE_Q8_0> { static constexpr int qs_per_block = 32; static constexpr bool has_qh = false; };
+
+__host__ __device__ inline int qs_row_bytes(int qt, int d) { return qt == KVQ_TYPE_Q8_0 ? d : d / 2; }
+
+// ---------------------------------------------------------------------------
+// small utilities
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b16) { return __uint_as_float(b16 << 16); }
+
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+// fp16x2 subtraction of a constant pair given as raw bits.
+__device__ __forceinline__ uint32_t hsub2_bits(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// pack two floats into fp16x2 (round to nearest even); lo goes to bits 0..15.
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// Code conversions to fp16 pairs.  A byte value u placed in the low byte of a
+// 0x64XX half is the fp16 number 1024 + u exactly, so one subtraction gives
+// the signed code, exactly.
+// ---------------------------------------------------------------------------
+// Nibbles at bit offsets s and s+16 of r (codes 0..15) plus optional high
+// bits already placed at bit 4 / bit 20 in `hb` -> fp16 pair (code - off).
+__device__ __forceinline__ uint32_t nib_pair(uint32_t r, int s, uint32_t hb_or_magic, uint32_t off_bits) {
+  uint32_t t = ((r >> s) & 0x000F000Fu) | hb_or_magic;
+  return hsub2_bits(t, off_bits);
+}
+// Signed bytes i0, i1 (0..3) of r -> fp16 pair (code).  `ru` = r ^ 0x80808080.
+template <int I0, int I1>
+__device__ __forceinline__ uint32_t i8_pair(uint32_t ru) {
+  uint32_t t = __byte_perm(ru, 0x64646464u, I0 | (4 << 4) | (I1 << 8) | (4 << 12));
+  return hsub2_bits(t, 0x64806480u);  // 1152 = 1024 + 128
+}
+// bf16 pair -> fp16 pair scaled by 2^-8 (keeps |x| < 1.6e7 finite in fp16).
+__device__ __forceinline__ uint32_t bf16x2_to_h2_scaled(uint32_t b) {
+  float lo = __uint_as_float(b << 16) * 0.00390625f;
+  float hi = __uint_as_float(b & 0xFFFF0000u) * 0.00390625f;
+  return pack_h2(lo, hi);
+}
+
+// ---------------------------------------------------------------------------
+// Warp tensor-core fragments
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ uint32_t movm_t(uint32_t a) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(a));
+  return r;
+}
+// D = A(16x16, row) * B(16x8, col) + C, fp16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// ---------------------------------------------------------------------------
+// Shared-memory barriers and bulk copies (TMA)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+// Bounded wait: gives up after ~`limit_cycles` SM cycles and returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, long long limit_cycles) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > limit_cycles) return false;
+  }
+  return true;
+}
+
+// 1-D bulk copy global -> shared, completion counted on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+// 2-D tiled tensor copy global -> shared (coordinates: x = inner element, y = row).
+__device__ __forceinline__ void tma_2d_g2s(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Byte offset of (row r, byte x) inside a tile that a TMA box copy wrote with
+// the swizzle matching its box width W (128, 64 or 32 bytes; 16-byte chunks
+// XORed with address bits 7..9).  Boxes of `rows` x W are stored one after
+// another along x.  The tile base must be 1024-byte aligned.
+template <int W>
+__device__ __forceinline__ uint32_t swz_off(int r, int x, int rows) {
+  const int box = x / W, xi = x % W;
+  int chunk = xi >> 4;
+  if (W == 128) chunk ^= (r & 7);
+  else if (W == 64) chunk ^= ((r >> 1) & 3);
+  else chunk ^= ((r >> 2) & 1);
+  return box * rows * W + r * W + (chunk << 4) + (xi & 15);
+}
+
+// ---------------------------------------------------------------------------
+// Warp FWHT: a head vector of D values, lane l holding E = D/32 of them.
+// Channel of value j in lane l:  c = (j / P) * G + l * P + (j % P), P = G/32,
+// i.e. G-wide Hadamard groups, each spread over the warp with P consecutive
+// channels per lane.  Computes the unnormalized Sylvester-order transform of
+// every group (callers scale by 1/sqrt(G)).
+// ---------------------------------------------------------------------------
+template <int D, int G>
+__device__ __forceinline__ void warp_fwht(float (&v)[D / 32], int lane) {
+  constexpr int P = G / 32;      // consecutive channels per lane per group
+  constexpr int NG = D / G;      // groups
+  static_assert(P >= 1 && D % G == 0, "bad FWHT layout");
+#pragma unroll
+  for (int h = 1; h < P; h <<= 1) {          // partners inside the lane
+#pragma unroll
+    for (int gi = 0; gi < NG; ++gi)
+#pragma unroll
+      for (int j = 0; j < P; ++j)
+        if ((j & h) == 0) {
+          const float a = v[gi * P + j], b = v[gi * P + j + h];
+          v[gi * P + j] = a + b;
+          v[gi * P + j + h] = a - b;
+        }
+  }
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {         // partners across lanes (stride m*P)
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int j = 0; j < D / 32; ++j) {
+      const float o = __shfl_xor_sync(0xffffffffu, v[j], m);
+      v[j] = upper ? (o - v[j]) : (v[j] + o);
+    }
+  }
+}
+
+// 1/sqrt(G) correctly rounded to fp32.
+template <int G>
+__host__ __device__ constexpr float inv_sqrt_group() {
+  return G == 32 ? 0.17677669529663688f : G == 64 ? 0.125f : G == 128 ? 0.088388347648318440f : 0.0625f;
+}
+static_assert(inv_sqrt_group<256>() == 0.0625f, "");
+
+// Channel held in slot j of lane l for the FWHT layout above.
+template <int D, int G>
+__device__ __forceinline__ int fwht_channel(int lane, int j) {
+  constexpr int P = G / 32;
+  return (j / P) * G + lane * P + (j % P);
+}
+
+}  // namespace kvq

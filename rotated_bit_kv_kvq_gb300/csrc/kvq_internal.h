@@ -1,0 +1,49 @@
+// Host-side declarations shared by the kvq translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "kvq.h"
+
+namespace kvq {
+
+struct Rot {
+  int k;  // K (and query) rotation on
+  int v;  // V rotation on (output rotated back)
+};
+
+// Hadamard group width used for a head: head_dim when it is a power of two,
+// 64 for other multiples of 64, 32 when rotation is impossible (layout only).
+inline int rotation_group(int d) {
+  if (d >= 64 && d % 64 == 0) return (d & (d - 1)) == 0 ? d : 64;
+  return 32;
+}
+
+size_t qs_row_bytes_host(int qt, int d);
+
+// Launchers (arguments already validated by the API layer).
+cudaError_t launch_append(const kvq_cache& c, Rot rot, const void* k, const void* v, int in_dtype,
+                          int n_new, const int32_t* n_new_per_seq, uint32_t flags, cudaStream_t st);
+cudaError_t launch_debug(const kvq_cache& c, Rot rot, int seq, int kv_head, int which, int t0,
+                         int count, int original_basis, float* out, void* blocks, cudaStream_t st);
+
+// Decode: split plan shared by the workspace query and the launch.
+struct DecodePlan {
+  int heads_per_cta;   // query heads handled by one CTA (<= 8)
+  int head_groups;     // CTAs along the head axis per KV head
+  int chunk;           // body tokens per CTA (multiple of 64)
+  int splits_body;     // CTAs per (seq, head group) over the body
+  int tail_chunk;      // tail slots per CTA
+  int splits_tail;     // CTAs per (seq, head group) over the tail
+  int splits;          // splits_body + splits_tail
+  size_t ws_bytes;     // workspace bytes
+};
+bool decode_supported(int d, int kt, int vt);
+DecodePlan plan_decode(const kvq_cache& c, int n_q_heads, int sm_count);
+cudaError_t launch_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, const void* q,
+                          int q_dtype, int n_q_heads, float scale, void* out, int out_dtype,
+                          void* ws, cudaStream_t st);
+
+}  // namespace kvq

@@ -1,0 +1,157 @@
+"""Host-only checks of the C ABI: the library builds for sm_103a, loads without a
+GPU, exports every symbol include/kvq.h declares, and rejects bad arguments on
+the host before any launch.  No compute call is made."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from rotated_bit_kv_kvq_gb300 import kvq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvq_[a-z_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol(built_lib_path):
+    names = _declared_functions()
+    assert len(names) >= 12
+    assert set(names) == set(kvq.SIGNATURES), "binding signatures out of sync with include/kvq.h"
+    handle = ctypes.CDLL(built_lib_path)
+    for n in names:
+        assert hasattr(handle, n), n
+    assert kvq.lib().kvq_version() == 1
+
+
+def test_status_strings(built_lib_path):
+    for s in (0, -1, -2, -3, -4, -5, -6):
+        assert kvq.lib().kvq_status_string(s)
+    assert kvq.lib().kvq_status_string(-99) == b"unknown status"
+
+
+def _desc(**kw):
+    base = dict(batch=2, n_kv_heads=4, head_dim=128, max_ctx=256, tail_len=32, k_type="q8_0", v_type="q4_0")
+    base.update(kw)
+    return kvq.descriptor(**base)
+
+
+def test_plane_bytes(built_lib_path):
+    c = _desc()
+    rows = 2 * 4 * 256
+    assert kvq.kvq_plane_bytes(c, kvq.KVQ_PLANE_K_QS) == rows * 128
+    assert kvq.kvq_plane_bytes(c, kvq.KVQ_PLANE_V_QS) == rows * 64
+    assert kvq.kvq_plane_bytes(c, kvq.KVQ_PLANE_K_QH) == 0
+    assert kvq.kvq_plane_bytes(c, kvq.KVQ_PLANE_K_D) == rows * 4 * 2
+    assert kvq.kvq_plane_bytes(c, kvq.KVQ_PLANE_K_TAIL) == 2 * 4 * 32 * 128 * 2
+    assert kvq.kvq_plane_bytes(c, kvq.KVQ_PLANE_SEQ_LEN) == 8
+    assert kvq.kvq_plane_bytes(c, kvq.KVQ_PLANE_STATUS) == 16
+    c5 = _desc(k_type="q5_0", v_type="q5_0")
+    assert kvq.kvq_plane_bytes(c5, kvq.KVQ_PLANE_V_QH) == rows * 4 * 4
+    # packed bytes per token-head equal the GGUF block sizes (18 / 22 / 34 per 32 values)
+    for qt, blk in (("q4_0", 18), ("q5_0", 22), ("q8_0", 34)):
+        c = _desc(k_type=qt, v_type=qt)
+        per = sum(kvq.kvq_plane_bytes(c, p) for p in (kvq.KVQ_PLANE_K_QS, kvq.KVQ_PLANE_K_QH, kvq.KVQ_PLANE_K_D))
+        assert per == rows * (128 // 32) * blk
+    assert kvq.kvq_plane_bytes(_desc(head_dim=100), 0) == 0
+    assert kvq.kvq_plane_bytes(_desc(max_ctx=100), 0) == 0
+
+
+@pytest.mark.parametrize("d,flags,expect", [
+    (64, kvq.KVQ_ROT_AUTO, (0, 1, 1)),
+    (128, kvq.KVQ_ROT_AUTO, (0, 1, 1)),
+    (192, kvq.KVQ_ROT_AUTO, (0, 1, 1)),
+    (96, kvq.KVQ_ROT_AUTO, (0, 0, 0)),
+    (32, kvq.KVQ_ROT_AUTO, (0, 0, 0)),
+    (96, 0, (kvq.KVQ_ERR_UNSUPPORTED, 0, 0)),
+    (96, kvq.KVQ_ROT_K_OFF | kvq.KVQ_ROT_V_OFF, (0, 0, 0)),
+    (128, 0, (0, 1, 1)),
+    (128, kvq.KVQ_ROT_AUTO | kvq.KVQ_ROT_K_OFF, (0, 0, 1)),
+    (128, kvq.KVQ_ROT_AUTO | kvq.KVQ_ROT_V_OFF, (0, 1, 0)),
+])
+def test_enable_rule(built_lib_path, d, flags, expect):
+    """velog 적용 및 배경 기술: automatic for head_dim >= 64 and %64 == 0; K / V switches."""
+    st, rk, rv = kvq.kvq_resolve_rotation(_desc(head_dim=d, flags=flags))
+    assert (st, rk, rv) == expect
+
+
+FAKE = 0x7f0000000000  # an aligned address; never dereferenced by the rejected calls
+
+
+def _full_desc(**kw):
+    c = _desc(**kw)
+    for name in ("k_qs", "k_d", "v_qs", "v_d", "seq_len", "status", "k_tail", "v_tail"):
+        setattr(c, name, FAKE)
+    if c.k_type == kvq.KVQ_TYPE_Q5_0:
+        c.k_qh = FAKE
+    if c.v_type == kvq.KVQ_TYPE_Q5_0:
+        c.v_qh = FAKE
+    if c.tail_len == 0:
+        c.k_tail = None
+        c.v_tail = None
+    return c
+
+
+def test_cache_check_rejections(built_lib_path):
+    L = kvq.lib()
+    assert L.kvq_cache_check(ctypes.byref(_full_desc())) == 0
+    assert L.kvq_cache_check(None) == kvq.KVQ_ERR_INVALID_ARG
+    c = _full_desc(); c.k_qs = None
+    assert L.kvq_cache_check(ctypes.byref(c)) == kvq.KVQ_ERR_INVALID_ARG
+    c = _full_desc(); c.v_d = FAKE + 8
+    assert L.kvq_cache_check(ctypes.byref(c)) == kvq.KVQ_ERR_INVALID_ARG
+    c = _full_desc(); c.k_qh = FAKE                      # qh given for a q8_0 plane
+    assert L.kvq_cache_check(ctypes.byref(c)) == kvq.KVQ_ERR_INVALID_ARG
+    c = _full_desc(k_type="q5_0"); c.k_qh = None          # q5_0 without its qh plane
+    assert L.kvq_cache_check(ctypes.byref(c)) == kvq.KVQ_ERR_INVALID_ARG
+    c = _full_desc(tail_len=0); c.k_tail = FAKE
+    assert L.kvq_cache_check(ctypes.byref(c)) == kvq.KVQ_ERR_INVALID_ARG
+    for bad in (dict(head_dim=48), dict(head_dim=512), dict(max_ctx=100), dict(batch=0), dict(tail_len=-1),
+                dict(k_type=7), dict(flags=8)):
+        assert L.kvq_cache_check(ctypes.byref(_full_desc(**bad))) == kvq.KVQ_ERR_INVALID_ARG, bad
+
+
+def test_call_rejections_before_launch(built_lib_path):
+    L = kvq.lib()
+    c = _full_desc()
+    ref = ctypes.byref(c)
+    # append: bad dtype, negative count, null / misaligned inputs, unknown flag
+    assert L.kvq_rotate_quantize_append(ref, FAKE, FAKE, 7, 1, None, 0, None) == kvq.KVQ_ERR_INVALID_ARG
+    assert L.kvq_rotate_quantize_append(ref, FAKE, FAKE, 0, -1, None, 0, None) == kvq.KVQ_ERR_INVALID_ARG
+    assert L.kvq_rotate_quantize_append(ref, None, FAKE, 0, 1, None, 0, None) == kvq.KVQ_ERR_INVALID_ARG
+    assert L.kvq_rotate_quantize_append(ref, FAKE + 4, FAKE, 0, 1, None, 0, None) == kvq.KVQ_ERR_INVALID_ARG
+    assert L.kvq_rotate_quantize_append(ref, FAKE, FAKE, 0, 1, None, 2, None) == kvq.KVQ_ERR_INVALID_ARG
+    assert L.kvq_rotate_quantize_append(ref, FAKE, FAKE, 0, 0, None, 0, None) == 0   # n_new = 0: no-op
+    # explicit rotation on an ineligible head_dim
+    c96 = _full_desc(head_dim=96, flags=0)
+    assert L.kvq_rotate_quantize_append(ctypes.byref(c96), FAKE, FAKE, 0, 1, None, 0, None) == kvq.KVQ_ERR_UNSUPPORTED
+    # decode: heads not a multiple of kv heads, bad dtype, null out, workspace
+    assert L.kvq_decode_attention(ref, FAKE, 0, 6, 0.0, FAKE, 0, FAKE, 1 << 30, None) == kvq.KVQ_ERR_INVALID_ARG
+    assert L.kvq_decode_attention(ref, FAKE, 5, 8, 0.0, FAKE, 0, FAKE, 1 << 30, None) == kvq.KVQ_ERR_INVALID_ARG
+    assert L.kvq_decode_attention(ref, FAKE, 0, 8, 0.0, None, 0, FAKE, 1 << 30, None) == kvq.KVQ_ERR_INVALID_ARG
+    assert L.kvq_decode_attention(ref, FAKE, 0, 8, -1.0, FAKE, 0, FAKE, 1 << 30, None) == kvq.KVQ_ERR_INVALID_ARG
+    assert L.kvq_decode_attention(ref, FAKE, 0, 8, 0.0, FAKE, 0, None, 1 << 30, None) == kvq.KVQ_ERR_WORKSPACE
+    assert L.kvq_decode_attention(ref, FAKE, 0, 8, 0.0, FAKE, 0, FAKE, 16, None) == kvq.KVQ_ERR_WORKSPACE
+    c160 = _full_desc(head_dim=160)
+    assert L.kvq_decode_attention(ctypes.byref(c160), FAKE, 0, 8, 0.0, FAKE, 0, FAKE, 1 << 30, None) == \
+        kvq.KVQ_ERR_UNSUPPORTED
+    # debug: out-of-range sequence / head / which / positions
+    assert L.kvq_dequant_debug(ref, 2, 0, 0, 0, 1, 0, FAKE, None, None) == kvq.KVQ_ERR_INVALID_ARG
+    assert L.kvq_dequant_debug(ref, 0, 4, 0, 0, 1, 0, FAKE, None, None) == kvq.KVQ_ERR_INVALID_ARG
+    assert L.kvq_dequant_debug(ref, 0, 0, 4, 0, 1, 0, FAKE, None, None) == kvq.KVQ_ERR_INVALID_ARG
+    assert L.kvq_dequant_debug(ref, 0, 0, 0, 250, 10, 0, FAKE, None, None) == kvq.KVQ_ERR_INVALID_ARG
+    assert L.kvq_dequant_debug(ref, 0, 0, 2, 0, 1, 0, FAKE, FAKE, None) == kvq.KVQ_ERR_INVALID_ARG
+    assert L.kvq_dequant_debug(ref, 0, 0, 0, 0, 1, 0, None, None, None) == kvq.KVQ_ERR_INVALID_ARG
+    assert L.kvq_sync_status(None, None, None) == kvq.KVQ_ERR_INVALID_ARG
+
+
+def test_decode_workspace_bytes_is_a_pure_size_query(built_lib_path):
+    c = _desc()
+    n = kvq.kvq_decode_workspace_bytes(c, 8)
+    assert n > 0 and n % 4 == 0
+    assert kvq.kvq_decode_workspace_bytes(c, 6) == 0     # not a multiple of kv heads

@@ -1,0 +1,171 @@
+"""GPU write path vs the oracle: packed blocks bit-exact, tail bf16 exact, seq_len,
+ragged counts, ring wrap-around, range errors, and the GPU's own rotation."""
+
+import json
+
+import numpy as np
+import pytest
+
+from oracle import kvq_oracle as ko
+from conftest import golden_path
+from kvq_testlib import append_both, gpu_blocks, gpu_values, prerotate, require_gpu, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _edge_blocks():
+    """The hand-worked golden blocks (ties, halves, clamp, zeros, subnormal scale)."""
+    g = json.load(open(golden_path("quant_blocks.json")))
+    out = []
+    for blk in g["blocks"]:
+        x = np.zeros(32, np.float32)
+        for k, v in blk["x"].items():
+            x[int(k)] = v
+        out.append(x)
+    return out
+
+
+def _inputs(rng, B, n, H, d, scale=1.0):
+    x = rng.standard_normal((B, n, H, d)).astype(np.float32) * scale
+    x[:, :, :, 3 % d] *= 20
+    x[:, ::5] *= np.float32(1e-3)
+    edges = _edge_blocks()
+    # plant the golden blocks in the first positions of sequence 0, head 0
+    for i, blk in enumerate(edges):
+        t, j = divmod(i, d // 32)
+        if t < n:
+            x[0, t, 0, 32 * j:32 * j + 32] = blk
+    x[1 % B, 0, 0, :] = 0.0                        # an all-zero vector
+    x[0, n - 1, H - 1, :] = -0.0
+    return x
+
+
+@pytest.mark.parametrize("qt", ["q4_0", "q5_0", "q8_0"])
+@pytest.mark.parametrize("d", [32, 64, 96, 128, 192, 256])
+def test_blocks_bit_exact_prerotated(qt, d):
+    torch = require_gpu()
+    from rotated_bit_kv_kvq_gb300 import kvq
+    rng = np.random.default_rng(100 + d)
+    B, H, n, T = 2, 3, 37, 8
+    other = {"q4_0": "q8_0", "q5_0": "q4_0", "q8_0": "q5_0"}[qt]
+    gc = kvq.KVCache(B, H, d, 64, T, qt, other)
+    oc = ko.OracleCache(B, H, d, 64, T, qt, other, ko.rotation_enabled(d), ko.rotation_enabled(d))
+    k = _inputs(rng, B, n, H, d)
+    v = _inputs(rng, B, n, H, d, scale=3.0)
+    append_both(gc, oc, k, v, torch=torch)
+    assert np.array_equal(gc.seq_len.cpu().numpy(), [n, n])
+    for b in range(B):
+        for h in range(H):
+            for which, w, t in ((0, "k", qt), (1, "v", other)):
+                got = gpu_blocks(gc, b, h, which, 0, n, t, d, torch)
+                exp = oc.ggml_blocks(w, b, h, 0, n)
+                assert np.array_equal(got, exp), (qt, d, b, h, w)
+                # the values the body holds equal the oracle's dequantization exactly
+                vals = gpu_values(gc, b, h, which, 0, n, d, torch)
+                assert np.array_equal(vals, oc.body_values(w, b, h, 0, n))
+            for which, w in ((2, "k"), (3, "v")):
+                pos = np.arange(n - T, n)
+                got = gpu_values(gc, b, h, which, n - T, T, d, torch)
+                assert np.array_equal(got, oc.tail_values(w, b, h, pos))
+
+
+def test_ragged_counts_ring_wrap_and_many_appends():
+    torch = require_gpu()
+    from rotated_bit_kv_kvq_gb300 import kvq
+    rng = np.random.default_rng(7)
+    B, H, d, T = 3, 2, 128, 16
+    gc = kvq.KVCache(B, H, d, 256, T, "q5_0", "q8_0")
+    oc = ko.OracleCache(B, H, d, 256, T, "q5_0", "q8_0", True, True)
+    for step in range(30):
+        nn = [int(x) for x in rng.integers(0, 9, B)]
+        k = _inputs(rng, B, 8, H, d)
+        v = _inputs(rng, B, 8, H, d)
+        append_both(gc, oc, k, v, n_new_per_seq=nn, torch=torch)
+    lens = gc.seq_len.cpu().numpy()
+    assert np.array_equal(lens, oc.seq_len)
+    for b in range(B):
+        n = int(lens[b])
+        for h in range(H):
+            assert np.array_equal(gpu_blocks(gc, b, h, 0, 0, n, "q5_0", d, torch), oc.ggml_blocks("k", b, h, 0, n))
+            assert np.array_equal(gpu_blocks(gc, b, h, 1, 0, n, "q8_0", d, torch), oc.ggml_blocks("v", b, h, 0, n))
+            lo = max(0, n - T)
+            got = gpu_values(gc, b, h, 2, lo, n - lo, d, torch)
+            assert np.array_equal(got, oc.tail_values("k", b, h, np.arange(lo, n)))
+
+
+def test_single_call_longer_than_tail_keeps_last_tokens():
+    torch = require_gpu()
+    from rotated_bit_kv_kvq_gb300 import kvq
+    rng = np.random.default_rng(8)
+    B, H, d, T, n = 2, 2, 64, 16, 150
+    gc = kvq.KVCache(B, H, d, 192, T, "q4_0", "q4_0")
+    oc = ko.OracleCache(B, H, d, 192, T, "q4_0", "q4_0", True, True)
+    append_both(gc, oc, _inputs(rng, B, n, H, d), _inputs(rng, B, n, H, d), torch=torch)
+    for b in range(B):
+        for h in range(H):
+            got = gpu_values(gc, b, h, 3, n - T, T, d, torch)
+            assert np.array_equal(got, oc.tail_values("v", b, h, np.arange(n - T, n)))
+
+
+def test_overflow_sets_status_and_leaves_sequence_untouched():
+    torch = require_gpu()
+    from rotated_bit_kv_kvq_gb300 import kvq
+    rng = np.random.default_rng(9)
+    gc = kvq.KVCache(2, 1, 64, 64, 0, "q8_0", "q8_0")
+    k = to_dev(rng.standard_normal((2, 40, 1, 64)).astype(np.float32), "f32", torch)
+    kvq.kvq_rotate_quantize_append(gc.desc, k, k)
+    st, bits = kvq.kvq_sync_status(gc.desc)
+    assert st == 0 and bits == 0
+    nps = torch.tensor([30, 10], dtype=torch.int32, device="cuda")   # sequence 0 would pass 64
+    kvq.kvq_rotate_quantize_append(gc.desc, k, k, n_new_per_seq=nps)
+    st, bits = kvq.kvq_sync_status(gc.desc)
+    assert st == kvq.KVQ_ERR_DEVICE_RANGE and bits == kvq.KVQ_DEV_ERR_APPEND_RANGE
+    assert gc.seq_len.cpu().numpy().tolist() == [40, 50]
+    st, bits = kvq.kvq_sync_status(gc.desc)            # cleared after being reported
+    assert st == 0 and bits == 0
+
+
+@pytest.mark.parametrize("in_dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("d", [64, 128, 256, 192])
+def test_gpu_rotation_against_oracle(in_dtype, d):
+    """The GPU rotates in fp32 (warp FWHT); the oracle in fp64.  Codes may flip
+    only where the rotated value sits within float rounding of a code boundary:
+    at most 1 in 1000 elements, each by one level, and bf16 tail values agree
+    to one bf16 unit."""
+    torch = require_gpu()
+    from rotated_bit_kv_kvq_gb300 import kvq
+    rng = np.random.default_rng(11)
+    B, H, n, T = 2, 4, 64, 16
+    x = rng.standard_normal((B, n, H, d)).astype(np.float32)
+    x[..., 5] *= 20
+    xd = to_dev(x, in_dtype, torch)
+    xin = xd.float().cpu().numpy()            # the values the GPU actually received
+    for qt in ("q4_0", "q5_0", "q8_0"):
+        gc = kvq.KVCache(B, H, d, 64, T, qt, qt)
+        oc = ko.OracleCache(B, H, d, 64, T, qt, qt, True, True)
+        kvq.kvq_rotate_quantize_append(gc.desc, xd, xd)
+        oc.append(xin, xin)
+        flips = 0
+        total = 0
+        for b in range(B):
+            for h in range(H):
+                got = gpu_values(gc, b, h, 0, 0, n, d, torch)
+                exp = oc.body_values("k", b, h, 0, n)
+                dq = ko.f16_value(oc.dbits["k"][b, h, :n]).repeat(32, axis=-1).reshape(n, d)
+                diff = got != exp
+                flips += int(diff.sum())
+                total += got.size
+                # a flipped element moves by one quantization level of its block
+                # (the block scale itself can differ in its last fp16 bit)
+                lvl = np.abs(dq[diff]) * 1.01 + 1e-30
+                assert np.all(np.abs(got[diff] - exp[diff]) <= lvl)
+                tg = gpu_values(gc, b, h, 2, n - T, T, d, torch)
+                te = oc.tail_values("k", b, h, np.arange(n - T, n))
+                assert np.all(np.abs(tg - te) <= np.abs(te) * 2.0 ** -7 + 1e-30)
+        assert flips <= total // 1000 + 2, (qt, flips, total)
+        # back in the original basis the values are x up to the quantization error
+        back = gpu_values(gc, 0, 0, 0, 0, n, d, torch, original_basis=True)
+        amax = np.abs(ko.rotate(xin[0, :, 0])).reshape(n, d // 32, 32).max(-1)
+        step = {"q4_0": 1 / 8, "q5_0": 1 / 16, "q8_0": 1 / 127}[qt]
+        err = np.linalg.norm(back - xin[0, :, 0], axis=-1)
+        assert np.all(err <= np.sqrt(d) * (amax.max(-1) * step) * 1.01 + 1e-6)
