@@ -181,6 +181,8 @@ def run_ours(args):
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     torch.cuda.set_device(local)
     w = wl.WORKLOADS[args.workload]
+    if args.ctx:
+        w = w.scaled(ctx=args.ctx)
     K, W = args.steps, args.warmup
     n_new = max(1, w.append_per_step)
     extra = (W + K) * n_new
@@ -414,6 +416,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=wl.HEADLINE,
                     choices=sorted(k for k, v in wl.WORKLOADS.items() if not v.prefill))
+    ap.add_argument("--ctx", type=int, default=0,
+                    help="context length override (a smaller case of the same workload, e.g. for ncu captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     args = ap.parse_args()

@@ -36,7 +36,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kMaxHeads = 8;                 // query heads per CTA (mma N)
 constexpr long long kWaitCycles = 1000000000LL;  // ~0.5 s at 2 GHz; a TMA tile lands in microseconds
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kTailChunk = 256;
+constexpr int kTailChunkMax = 4096;  // tail slots per CTA
 constexpr int kSmemBudget = 104 * 1024;      // stages; leaves room for 2 CTAs per SM
 
 constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
@@ -85,10 +85,17 @@ struct Params {
   int q_dtype, n_q_heads, group, heads_per_cta, head_groups;
   int rot_k;
   float scale_log2;                 // softmax scale * log2(e)
-  int chunk, splits_body, splits_tail, splits;
+  int chunk, tail_chunk, splits_body, splits_tail, splits;
 };
 
 __device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
+
+// a, b -> fp16 pairs hi = fp16(a, b) and lo = fp16(a - hi, b - hi): hi + lo keeps ~22 bits.
+__device__ __forceinline__ void split_h2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  hi = pack_h2(a, b);
+  const float2 f = __half22float2(u32_as_h2(hi));
+  lo = pack_h2(a - f.x, b - f.y);
+}
 
 // q5_0 high bits of a K row word h = qh >> (4*tig), placed at bits 4 / 20 (with the 0x6400 magic).
 __device__ __forceinline__ uint32_t khb(uint32_t h, int which) {
@@ -126,8 +133,8 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
   const bool is_tail = split < p.splits_tail;
   int t_begin, t_end;
   if (is_tail) {
-    t_begin = split * kTailChunk;
-    t_end = min(ntail, t_begin + kTailChunk);
+    t_begin = split * p.tail_chunk;
+    t_end = min(ntail, t_begin + p.tail_chunk);
   } else {
     t_begin = (split - p.splits_tail) * p.chunk;
     t_end = min(nbody, t_begin + p.chunk);
@@ -264,19 +271,15 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     const bool v0 = t0 + g < t_end, v8 = (TR == 16) && (t0 + g + 8 < t_end);
 
     float S[4] = {0.f, 0.f, 0.f, 0.f};
-    float dvg[NB], dvg8[NB];
     if (!is_tail) {
       // ------------------------------- body: scores
       float dkg[NB], dkg8[NB];
       {
         const __half* kd = reinterpret_cast<const __half*>(st + C::off_kd);
-        const __half* vd = reinterpret_cast<const __half*>(st + C::off_vd);
 #pragma unroll
         for (int blk = 0; blk < NB; ++blk) {
           dkg[blk] = __half2float(kd[g * NB + blk]);
           dkg8[blk] = __half2float(kd[(g + 8) * NB + blk]);
-          dvg[blk] = v0 ? __half2float(vd[g * NB + blk]) : 0.0f;
-          dvg8[blk] = v8 ? __half2float(vd[(g + 8) * NB + blk]) : 0.0f;
         }
       }
       const uint32_t kbase = smem_u32(st + C::off_kqs);
@@ -331,8 +334,6 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
       }
     } else {
       // ------------------------------- tail (bf16, stored as fp16 * 2^-8): scores
-#pragma unroll
-      for (int blk = 0; blk < NB; ++blk) { dvg[blk] = v0 ? 256.0f : 0.0f; dvg8[blk] = v8 ? 256.0f : 0.0f; }
       const uint8_t* kt = st + C::off_kt;
       float cc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -381,22 +382,50 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     const float p2 = fast_exp2(S[2] - ms0), p3 = fast_exp2(S[3] - ms1);
     l0 += p0 + p2; l1 += p1 + p3;
 
-    // ---- P.V: per block, P scaled by the block's V scale, transposed to a B fragment
+    // ---- P.V.  P is transposed once per tile (movmatrix on fp16 hi + lo parts)
+    // into the B-fragment layout: tokens 2tig, 2tig+1, 2tig+8, 2tig+9 of head g.
+    // Each block then scales it by its V scale (fp32) and splits it again into
+    // fp16 hi + lo, so the products keep ~22 bits; the codes are exact.
+    float pt[4];
+    {
+      const uint32_t h0 = pack_h2(p0, p1), h1 = pack_h2(p2, p3);
+      const float2 f0 = __half22float2(u32_as_h2(h0)), f1 = __half22float2(u32_as_h2(h1));
+      const uint32_t r0 = pack_h2(p0 - f0.x, p1 - f0.y), r1 = pack_h2(p2 - f1.x, p3 - f1.y);
+      const float2 th0 = __half22float2(u32_as_h2(movm_t(h0))), tr0 = __half22float2(u32_as_h2(movm_t(r0)));
+      const float2 th1 = __half22float2(u32_as_h2(movm_t(h1))), tr1 = __half22float2(u32_as_h2(movm_t(r1)));
+      pt[0] = th0.x + tr0.x; pt[1] = th0.y + tr0.y; pt[2] = th1.x + tr1.x; pt[3] = th1.y + tr1.y;
+    }
+    const int tt = t0 + 2 * tig;  // first token of this lane's transposed rows
+    const bool vt0 = tt < t_end, vt1 = tt + 1 < t_end;
+    const bool vt8 = TR == 16 && tt + 8 < t_end, vt9 = TR == 16 && tt + 9 < t_end;
     if (!is_tail) {
+      float dvt[4][NB];  // V scales of the transposed tokens (0 for rows past the end)
+      {
+        const __half* vd = reinterpret_cast<const __half*>(st + C::off_vd);
+        const int rows[4] = {2 * tig, 2 * tig + 1, 2 * tig + 8, 2 * tig + 9};
+        const bool ok[4] = {vt0, vt1, vt8, vt9};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int blk = 0; blk < NB; ++blk) dvt[i][blk] = ok[i] ? __half2float(vd[rows[i] * NB + blk]) : 0.0f;
+      }
       const uint32_t vbase = smem_u32(st + C::off_vqs);
       const int mi = lane >> 3, rr = (lane & 7) + 8 * (mi & 1);
       if constexpr (VT == KVQ_TYPE_Q8_0) {
 #pragma unroll
         for (int blk = 0; blk < NB; ++blk) {
-          const uint32_t b0 = movm_t(pack_h2(p0 * dvg[blk], p1 * dvg[blk]));
-          const uint32_t b1 = movm_t(pack_h2(p2 * dvg8[blk], p3 * dvg8[blk]));
+          uint32_t bh0, bl0, bh1, bl1;
+          split_h2(pt[0] * dvt[0][blk], pt[1] * dvt[1][blk], bh0, bl0);
+          split_h2(pt[2] * dvt[2][blk], pt[3] * dvt[3][blk], bh1, bl1);
           uint32_t r0, r1, r2, r3;
           ldsm_x4_t(vbase + swz_off<C::WV>(rr, 32 * blk + 16 * (mi >> 1), 16), r0, r1, r2, r3);
           r0 ^= 0x80808080u; r1 ^= 0x80808080u; r2 ^= 0x80808080u; r3 ^= 0x80808080u;
           const uint32_t a0[4] = {i8_pair<0, 2>(r0), i8_pair<1, 3>(r0), i8_pair<0, 2>(r1), i8_pair<1, 3>(r1)};
           const uint32_t a1[4] = {i8_pair<0, 2>(r2), i8_pair<1, 3>(r2), i8_pair<0, 2>(r3), i8_pair<1, 3>(r3)};
-          mma16816(acc[blk][0], a0, b0, b1);
-          mma16816(acc[blk][1], a1, b0, b1);
+          mma16816(acc[blk][0], a0, bh0, bh1);
+          mma16816(acc[blk][0], a0, bl0, bl1);
+          mma16816(acc[blk][1], a1, bh0, bh1);
+          mma16816(acc[blk][1], a1, bl0, bl1);
         }
       } else {
         constexpr uint32_t OFF = VT == KVQ_TYPE_Q5_0 ? 0x64106410u : 0x64086408u;
@@ -407,8 +436,9 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int blk = bp + e;
-            const uint32_t b0 = movm_t(pack_h2(p0 * dvg[blk], p1 * dvg[blk]));
-            const uint32_t b1 = movm_t(pack_h2(p2 * dvg8[blk], p3 * dvg8[blk]));
+            uint32_t bh0, bl0, bh1, bl1;
+            split_h2(pt[0] * dvt[0][blk], pt[1] * dvt[1][blk], bh0, bl0);
+            split_h2(pt[2] * dvt[2][blk], pt[3] * dvt[3][blk], bh1, bl1);
             const uint32_t ra = rr4[2 * e], rb = rr4[2 * e + 1];  // tokens 0-7, 8-15
             uint32_t ma0 = 0x64006400u, ma1 = 0x64006400u, ma2 = 0x64006400u, ma3 = 0x64006400u;
             uint32_t mb0 = 0x64006400u, mb1 = 0x64006400u, mb2 = 0x64006400u, mb3 = 0x64006400u;
@@ -428,18 +458,21 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
                                     nib_pair(rb, 0, mb0, OFF), nib_pair(rb, 8, mb1, OFF)};
             const uint32_t a1[4] = {nib_pair(ra, 4, ma2, OFF), nib_pair(ra, 12, ma3, OFF),
                                     nib_pair(rb, 4, mb2, OFF), nib_pair(rb, 12, mb3, OFF)};
-            mma16816(acc[blk][0], a0, b0, b1);
-            mma16816(acc[blk][1], a1, b0, b1);
+            mma16816(acc[blk][0], a0, bh0, bh1);
+            mma16816(acc[blk][0], a0, bl0, bl1);
+            mma16816(acc[blk][1], a1, bh0, bh1);
+            mma16816(acc[blk][1], a1, bl0, bl1);
           }
         }
       }
     } else {
-      const uint32_t b0 = movm_t(pack_h2(p0 * 256.0f, p1 * 256.0f));
-      const uint32_t b1 = movm_t(pack_h2(p2 * 256.0f, p3 * 256.0f));
+      // tail values are stored as fp16 * 2^-8, so P carries the factor 256
+      uint32_t bh0, bl0, bh1, bl1;
+      split_h2(pt[0] * 256.0f, pt[1] * 256.0f, bh0, bl0);
+      split_h2(pt[2] * 256.0f, pt[3] * 256.0f, bh1, bl1);
       // token validity of the rows this lane reads from the transposed tile
-      const int tt = t0 + 2 * tig;
-      const uint32_t mlo = (tt < t_end ? 0x0000FFFFu : 0u) | (tt + 1 < t_end ? 0xFFFF0000u : 0u);
-      const uint32_t mhi = C::TT == 16 ? ((tt + 8 < t_end ? 0x0000FFFFu : 0u) | (tt + 9 < t_end ? 0xFFFF0000u : 0u)) : 0u;
+      const uint32_t mlo = (vt0 ? 0x0000FFFFu : 0u) | (vt1 ? 0xFFFF0000u : 0u);
+      const uint32_t mhi = (vt8 ? 0x0000FFFFu : 0u) | (vt9 ? 0xFFFF0000u : 0u);
       const uint32_t vbase = smem_u32(st + C::off_vt);
       const int mi = lane >> 3;
       const int rr = (lane & 7) + (C::TT == 16 ? 8 * (mi >> 1) : 0);
@@ -452,7 +485,8 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
           ldsm_x4_t(vbase + swz_off<C::WT>(rr, 2 * (16 * mt + 8 * (mi & 1)), C::TT), r0, r1, r2, r3);
           const uint32_t a[4] = {bf16x2_to_h2_scaled(r0) & mlo, bf16x2_to_h2_scaled(r1) & mlo,
                                  bf16x2_to_h2_scaled(r2) & mhi, bf16x2_to_h2_scaled(r3) & mhi};
-          mma16816(acc[blk][cc2], a, b0, b1);
+          mma16816(acc[blk][cc2], a, bh0, bh1);
+          mma16816(acc[blk][cc2], a, bl0, bl1);
         }
     }
     __syncwarp();
@@ -627,7 +661,7 @@ cudaError_t run_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, cons
   p.heads_per_cta = plan.heads_per_cta; p.head_groups = plan.head_groups;
   p.rot_k = rot.k;
   p.scale_log2 = scale * kLog2e;
-  p.chunk = plan.chunk; p.splits_body = plan.splits_body; p.splits_tail = plan.splits_tail; p.splits = plan.splits;
+  p.chunk = plan.chunk; p.tail_chunk = plan.tail_chunk; p.splits_body = plan.splits_body; p.splits_tail = plan.splits_tail; p.splits = plan.splits;
 
   alignas(64) CUtensorMap mk, mv, mkt, mvt;
   memset(&mk, 0, sizeof(mk)); memset(&mv, 0, sizeof(mv)); memset(&mkt, 0, sizeof(mkt)); memset(&mvt, 0, sizeof(mvt));
@@ -678,16 +712,18 @@ DecodePlan plan_decode(const kvq_cache& c, int n_q_heads, int sm_count) {
   pl.head_groups = (g + kMaxHeads - 1) / kMaxHeads;
   pl.heads_per_cta = (g + pl.head_groups - 1) / pl.head_groups;
   const long long pairs = (long long)c.batch * c.n_kv_heads * pl.head_groups;
-  const int body_max = c.max_ctx;
+  // tail: one CTA per (sequence, head group) for tails up to 4096 slots
+  pl.tail_chunk = c.tail_len > 0 ? (c.tail_len < kTailChunkMax ? (c.tail_len + 63) / 64 * 64 : kTailChunkMax) : 64;
+  pl.splits_tail = c.tail_len > 0 ? (c.tail_len + pl.tail_chunk - 1) / pl.tail_chunk : 0;
+  // body: size the chunks so that all CTAs of a full cache fit in one wave of
+  // two CTAs per SM (shorter sequences leave their last splits empty)
   const long long slots = 2LL * (sm_count > 0 ? sm_count : 148);
-  long long per_pair = (slots + pairs - 1) / pairs;
+  long long per_pair = slots / pairs - pl.splits_tail;
   if (per_pair < 1) per_pair = 1;
-  int chunk = int(((body_max + per_pair - 1) / per_pair + 63) / 64 * 64);
-  if (chunk < 256) chunk = 256;
+  int chunk = int(((c.max_ctx + per_pair - 1) / per_pair + 63) / 64 * 64);
+  if (chunk < 512) chunk = 512;
   pl.chunk = chunk;
-  pl.splits_body = (body_max + chunk - 1) / chunk;
-  pl.tail_chunk = kTailChunk;
-  pl.splits_tail = c.tail_len > 0 ? (c.tail_len + kTailChunk - 1) / kTailChunk : 0;
+  pl.splits_body = (c.max_ctx + chunk - 1) / chunk;
   pl.splits = pl.splits_body + pl.splits_tail;
   pl.ws_bytes = (size_t)c.batch * n_q_heads * pl.splits * (c.head_dim + 2) * sizeof(float);
   return pl;

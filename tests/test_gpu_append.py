@@ -161,7 +161,10 @@ def test_gpu_rotation_against_oracle(in_dtype, d):
                 assert np.all(np.abs(got[diff] - exp[diff]) <= lvl)
                 tg = gpu_values(gc, b, h, 2, n - T, T, d, torch)
                 te = oc.tail_values("k", b, h, np.arange(n - T, n))
-                assert np.all(np.abs(tg - te) <= np.abs(te) * 2.0 ** -7 + 1e-30)
+                # one bf16 unit, plus the fp32 rounding of the transform itself for
+                # values that nearly cancel (absolute, relative to the row's largest)
+                tol = np.abs(te) * 2.0 ** -7 + np.abs(te).max(axis=-1, keepdims=True) * 2.0 ** -16
+                assert np.all(np.abs(tg - te) <= tol)
         assert flips <= total // 1000 + 2, (qt, flips, total)
         # back in the original basis the values are x up to the quantization error
         back = gpu_values(gc, 0, 0, 0, 0, n, d, torch, original_basis=True)
