@@ -190,6 +190,33 @@ KVQ_API kvq_status kvq_decode_attention(const kvq_cache* c, const void* q, int32
                                 int32_t n_q_heads, float scale, void* out, int32_t out_dtype,
                                 void* workspace, size_t ws_bytes, void* stream);
 
+/*
+ * kvq_decode_attention without a caller-provided workspace.  The pages have
+ * no counterpart to this entry point; it exists for callers that cannot
+ * allocate device memory themselves -- for example a plugin inside a host
+ * application that owns every device allocation, or a runtime that works
+ * within a fixed memory budget reserved up front -- and therefore cannot
+ * supply the workspace kvq_decode_attention needs.
+ *
+ * The split partials go to one scratch array of KVQ_NOALLOC_SCRATCH_BYTES
+ * that the library defines statically in device memory: every GPU that loads
+ * the library holds it until the process exits.  The call allocates nothing
+ * (no cudaMalloc, no allocating library routine).  The first call on each
+ * device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.
+ * Arguments, results and errors are those of kvq_decode_attention, except:
+ * KVQ_ERR_WORKSPACE when kvq_decode_workspace_bytes(c, n_q_heads) exceeds
+ * KVQ_NOALLOC_SCRATCH_BYTES (nothing is launched then).  All calls share the
+ * one array and it keeps the last call's contents; every call writes all
+ * scratch it reads, so nothing needs clearing.  Calls that overlap on the
+ * GPU (for example on two streams at once) race on the array and must not
+ * be issued.
+ */
+#define KVQ_NOALLOC_SCRATCH_BYTES (16u << 20)
+KVQ_API kvq_status kvq_decode_attention_noalloc(const kvq_cache* c, const void* q, int32_t q_dtype,
+                                                int32_t n_q_heads, float scale, void* out,
+                                                int32_t out_dtype, void* stream);
+
 /* Workspace bytes kvq_prefill_attention needs (0 on an invalid descriptor). */
 KVQ_API size_t kvq_prefill_workspace_bytes(const kvq_cache* c, int32_t n_q_heads, int32_t n_tokens);
 

@@ -169,6 +169,28 @@ kvq_status kvq_decode_attention(const kvq_cache* c, const void* q, int32_t q_dty
                                       static_cast<cudaStream_t>(stream)));
 }
 
+kvq_status kvq_decode_attention_noalloc(const kvq_cache* c, const void* q, int32_t q_dtype, int32_t n_q_heads,
+                                        float scale, void* out, int32_t out_dtype, void* stream) {
+  kvq_status s = check_cache(c);
+  if (s != KVQ_OK) return s;
+  kvq::Rot r{};
+  if ((s = resolve(c, &r)) != KVQ_OK) return s;
+  if (!valid_dtype(q_dtype) || !valid_dtype(out_dtype)) return KVQ_ERR_INVALID_ARG;
+  if (n_q_heads <= 0 || n_q_heads % c->n_kv_heads || n_q_heads / c->n_kv_heads > 4096) return KVQ_ERR_INVALID_ARG;
+  if (!q || !out || !aligned16(q) || !aligned16(out)) return KVQ_ERR_INVALID_ARG;
+  if (!(scale >= 0.0f) || scale > 1e30f) return KVQ_ERR_INVALID_ARG;
+  if (!kvq::decode_supported(c->head_dim, c->k_type, c->v_type)) return KVQ_ERR_UNSUPPORTED;
+  const kvq::DecodePlan plan = kvq::plan_decode(*c, n_q_heads, sm_count());
+  if (plan.ws_bytes > KVQ_NOALLOC_SCRATCH_BYTES) return KVQ_ERR_WORKSPACE;
+  if (plan.splits > 0x7fffffff || (long long)c->n_kv_heads * plan.head_groups > 65535) return KVQ_ERR_UNSUPPORTED;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  if (kvq::decode_noalloc_scratch(&ws, &ws_bytes) != cudaSuccess || ws_bytes < plan.ws_bytes) return KVQ_ERR_CUDA;
+  const float sc = scale == 0.0f ? 1.0f / sqrtf(float(c->head_dim)) : scale;
+  return from_cuda(kvq::launch_decode(*c, r, plan, q, q_dtype, n_q_heads, sc, out, out_dtype, ws,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
 size_t kvq_prefill_workspace_bytes(const kvq_cache* c, int32_t n_q_heads, int32_t n_tokens) {
   if (!shape_ok(c) || n_q_heads <= 0 || n_q_heads % c->n_kv_heads || n_tokens <= 0) return 0;
   return 16;

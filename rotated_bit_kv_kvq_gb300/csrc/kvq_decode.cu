@@ -25,6 +25,8 @@
 #include <cuda_fp16.h>
 #include <math.h>
 
+#include <mutex>
+
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
 
@@ -699,7 +701,33 @@ cudaError_t run_decode_d(const kvq_cache& c, Rot rot, const DecodePlan& plan, co
   return cudaErrorInvalidValue;
 }
 
+// Scratch of kvq_decode_attention_noalloc: a fixed device array, so that
+// callers who cannot allocate still get split partials somewhere.  Every GPU
+// that loads the library holds it until exit.  Host code only sees a host-side
+// stand-in for the name; the device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_decode_scratch[KVQ_NOALLOC_SCRATCH_BYTES];
+
 }  // namespace
+
+cudaError_t decode_noalloc_scratch(void** ptr, size_t* bytes) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {  // once per device, with that device current
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *ptr = addr[dev];
+  *bytes = sizeof(g_decode_scratch);
+  return cudaSuccess;
+}
 
 bool decode_supported(int d, int kt, int vt) {
   if (d == 64 || d == 128 || d == 256) return true;

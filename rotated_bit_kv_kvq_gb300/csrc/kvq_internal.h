@@ -42,6 +42,9 @@ struct DecodePlan {
 };
 bool decode_supported(int d, int kt, int vt);
 DecodePlan plan_decode(const kvq_cache& c, int n_q_heads, int sm_count);
+// Address of the fixed decode scratch array on the current device (looked up
+// once per device); size in *bytes.
+cudaError_t decode_noalloc_scratch(void** ptr, size_t* bytes);
 cudaError_t launch_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, const void* q,
                           int q_dtype, int n_q_heads, float scale, void* out, int out_dtype,
                           void* ws, cudaStream_t st);

@@ -61,6 +61,9 @@ SIGNATURES = {
     "kvq_decode_attention": (ctypes.c_int32, [_P, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
                                               ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t,
                                               ctypes.c_void_p]),
+    "kvq_decode_attention_noalloc": (ctypes.c_int32, [_P, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                                      ctypes.c_float, ctypes.c_void_p, ctypes.c_int32,
+                                                      ctypes.c_void_p]),
     "kvq_prefill_workspace_bytes": (ctypes.c_size_t, [_P, ctypes.c_int32, ctypes.c_int32]),
     "kvq_prefill_attention": (ctypes.c_int32, [_P, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                                ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
@@ -150,6 +153,16 @@ def kvq_decode_attention(cache: kvq_cache, q, out, workspace, scale: float = 0.0
                                       _dtype_id(out) if out_dtype is None else out_dtype,
                                       _ptr(workspace), wsb, _stream(stream)),
            "kvq_decode_attention")
+
+
+KVQ_NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def kvq_decode_attention_noalloc(cache: kvq_cache, q, out, scale: float = 0.0, stream=None):
+    """Decode attention with the library's fixed device scratch instead of a caller workspace."""
+    _check(lib().kvq_decode_attention_noalloc(ctypes.byref(cache), _ptr(q), _dtype_id(q), q.shape[1], float(scale),
+                                              _ptr(out), _dtype_id(out), _stream(stream)),
+           "kvq_decode_attention_noalloc")
 
 
 def kvq_prefill_workspace_bytes(cache: kvq_cache, n_q_heads: int, n_tokens: int) -> int:
