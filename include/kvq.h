@@ -107,9 +107,11 @@ typedef int32_t kvq_status;
  * Requirements (checked by every call): head_dim % 32 == 0 and
  * 32 <= head_dim <= 256; max_ctx % 64 == 0; tail_len >= 0; every non-NULL
  * plane 16-byte aligned; k_qh / v_qh non-NULL only for q5_0 (required then);
- * k_tail / v_tail non-NULL iff tail_len > 0.  Decode and prefill support
- * head_dim in {64, 128, 256} (plus 192 for q4_0/q4_0); append and debug
- * support every multiple of 32 up to 256.
+ * k_tail / v_tail non-NULL iff tail_len > 0.  Decode supports head_dim in
+ * {64, 128, 256} (plus 192 for q4_0/q4_0); prefill supports head_dim 64 and
+ * 128 with up to 128 query heads per KV head; append and debug support every
+ * multiple of 32 up to 256.  Prefill stores keys and values internally as
+ * fp16 x 2^-8, so it needs |rotated value| < 1.6e7.
  */
 typedef struct kvq_cache {
   int32_t batch;        /* sequences                                   */
@@ -217,7 +219,8 @@ KVQ_API kvq_status kvq_decode_attention_noalloc(const kvq_cache* c, const void* 
                                                 int32_t n_q_heads, float scale, void* out,
                                                 int32_t out_dtype, void* stream);
 
-/* Workspace bytes kvq_prefill_attention needs (0 on an invalid descriptor). */
+/* Workspace bytes kvq_prefill_attention needs: 0 (it writes its output rows
+ * directly; the workspace arguments are accepted and ignored). */
 KVQ_API size_t kvq_prefill_workspace_bytes(const kvq_cache* c, int32_t n_q_heads, int32_t n_tokens);
 
 /*

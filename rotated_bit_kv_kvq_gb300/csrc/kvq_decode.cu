@@ -565,27 +565,30 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
 }
 
 // ---------------------------------------------------------------------------
-// Split merge + inverse rotation: one warp per (sequence, query head).
+// Split merge + inverse rotation: one CTA of 8 warps per (sequence, query
+// head); warp w merges splits w, w+8, ... and warp 0 combines the 8 results.
 // ---------------------------------------------------------------------------
+constexpr int kCombineWarps = 8;
+
 template <int D>
-__global__ void __launch_bounds__(128)
-decode_combine_kernel(const float* __restrict__ ws_acc, const float* __restrict__ ws_ml, int splits, int total,
+__global__ void __launch_bounds__(kCombineWarps * 32)
+decode_combine_kernel(const float* __restrict__ ws_acc, const float* __restrict__ ws_ml, int splits,
                       int rot_v, void* __restrict__ out, int out_dtype) {
   constexpr int G = (D >= 64 && D % 64 == 0) ? (((D & (D - 1)) == 0) ? D : 64) : 32;
   constexpr int E = D / 32;
-  const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * 4 + (threadIdx.x >> 5);  // b * Hq + h
-  if (row >= total) return;
+  __shared__ float s_acc[kCombineWarps][D];
+  __shared__ float s_m[kCombineWarps], s_l[kCombineWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int row = blockIdx.x;  // b * Hq + h
   const float* ml = ws_ml + (size_t)row * splits * 2;
   float M = -INFINITY;
-  for (int s = lane; s < splits; s += 32) if (ml[2 * s + 1] > 0.0f) M = fmaxf(M, ml[2 * s]);
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  for (int s = warp; s < splits; s += kCombineWarps)
+    if (ml[2 * s + 1] > 0.0f) M = fmaxf(M, ml[2 * s]);
   float v[E];
 #pragma unroll
   for (int j = 0; j < E; ++j) v[j] = 0.0f;
   float L = 0.0f;
-  for (int s = 0; s < splits; ++s) {
+  for (int s = warp; s < splits; s += kCombineWarps) {
     const float l = ml[2 * s + 1];
     if (!(l > 0.0f)) continue;
     const float f = exp2f(ml[2 * s] - M);
@@ -594,9 +597,30 @@ decode_combine_kernel(const float* __restrict__ ws_acc, const float* __restrict_
 #pragma unroll
     for (int j = 0; j < E; ++j) v[j] += f * a[fwht_channel<D, G>(lane, j)];
   }
-  const float inv = L > 0.0f ? 1.0f / L : 0.0f;
 #pragma unroll
-  for (int j = 0; j < E; ++j) v[j] *= inv;
+  for (int j = 0; j < E; ++j) s_acc[warp][fwht_channel<D, G>(lane, j)] = v[j];
+  if (lane == 0) { s_m[warp] = M; s_l[warp] = L; }
+  __syncthreads();
+  if (warp != 0) return;
+  float Mt = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kCombineWarps; ++w) Mt = fmaxf(Mt, s_m[w]);
+  float f[kCombineWarps];
+  float Lt = 0.0f;
+#pragma unroll
+  for (int w = 0; w < kCombineWarps; ++w) {
+    f[w] = s_m[w] == -INFINITY ? 0.0f : exp2f(s_m[w] - Mt);
+    Lt += s_l[w] * f[w];
+  }
+  const float inv = Lt > 0.0f ? 1.0f / Lt : 0.0f;
+#pragma unroll
+  for (int j = 0; j < E; ++j) {
+    const int c = fwht_channel<D, G>(lane, j);
+    float t = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kCombineWarps; ++w) t += f[w] * s_acc[w][c];
+    v[j] = t * inv;
+  }
   if (rot_v) {
     warp_fwht<D, G>(v, lane);
 #pragma unroll
@@ -684,7 +708,7 @@ cudaError_t run_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, cons
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int total = c.batch * n_q_heads;
-  decode_combine_kernel<D><<<(total + 3) / 4, 128, 0, st>>>(p.ws_acc, p.ws_ml, plan.splits, total, rot.v, out, out_dtype);
+  decode_combine_kernel<D><<<total, kCombineWarps * 32, 0, st>>>(p.ws_acc, p.ws_ml, plan.splits, rot.v, out, out_dtype);
   return cudaGetLastError();
 }
 

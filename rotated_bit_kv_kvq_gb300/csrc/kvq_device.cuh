@@ -116,13 +116,15 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+// One wait attempt; the thread may sleep up to ~suspend_ns inside it while the
+// phase is incomplete (so waiting does not spin through issue slots).
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity, uint32_t suspend_ns = 100000u) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(suspend_ns) : "memory");
   return ok != 0;
 }
 // Bounded wait: gives up after ~`limit_cycles` SM cycles and returns false.
@@ -153,8 +155,8 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
 }
 
 // Byte offset of (row r, byte x) inside a tile that a TMA box copy wrote with
-// the swizzle matching its box width W (128, 64 or 32 bytes; 16-byte chunks
-// XORed with address bits 7..9).  Boxes of `rows` x W are stored one after
+// the swizzle matching its box width W (128, 64 or 32 bytes: 16-byte chunks
+// XORed with address bits 7..9; 16 bytes: no swizzle).  Boxes of `rows` x W are stored one after
 // another along x.  The tile base must be 1024-byte aligned.
 template <int W>
 __device__ __forceinline__ uint32_t swz_off(int r, int x, int rows) {
@@ -162,7 +164,7 @@ __device__ __forceinline__ uint32_t swz_off(int r, int x, int rows) {
   int chunk = xi >> 4;
   if (W == 128) chunk ^= (r & 7);
   else if (W == 64) chunk ^= ((r >> 1) & 3);
-  else chunk ^= ((r >> 2) & 1);
+  else if (W == 32) chunk ^= ((r >> 2) & 1);  // W == 16: no swizzle
   return box * rows * W + r * W + (chunk << 4) + (xi & 15);
 }
 
