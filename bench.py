@@ -329,11 +329,85 @@ def run_ours(args):
             "gpu_launches": 3 * K,
             "clocks": clk,
         }
+        if not args.no_prefill:
+            line["prefill"] = run_prefill_bench(torch, kvq, max(5, K // 5), 3)
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# prompt workload: bulk append of the prompt + causal prefill attention
+# ---------------------------------------------------------------------------
+def prefill_flops(w: wl.Workload) -> float:
+    """Useful flops of causal attention: 4 * head_dim per visible (query, key) pair."""
+    n = w.ctx
+    return 4.0 * w.head_dim * (n * (n + 1) / 2) * w.n_q_heads * w.batch
+
+
+def run_prefill_bench(torch, kvq, steps: int, warmup: int, seed: int = 0):
+    w = wl.WORKLOADS["prefill_b2_4k"]
+    cache = kvq.KVCache(w.batch, w.n_kv_heads, w.head_dim, w.max_ctx(), w.tail_len, w.k_type, w.v_type)
+    rng = np.random.Generator(np.random.PCG64(seed))
+    k_chan = wl.outlier_channels(rng, w.n_kv_heads, w.head_dim, w.n_outliers)
+    v_chan = wl.outlier_channels(rng, w.n_kv_heads, w.head_dim, w.n_outliers)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed + 1)
+    kmask = torch.ones(w.n_kv_heads, w.head_dim, device="cuda")
+    vmask = torch.ones(w.n_kv_heads, w.head_dim, device="cuda")
+    for h in range(w.n_kv_heads):
+        kmask[h, torch.tensor(k_chan[h])] = 20.0
+        vmask[h, torch.tensor(v_chan[h])] = 20.0
+    shape = (w.batch, w.ctx, w.n_kv_heads, w.head_dim)
+    k = (torch.randn(shape, generator=gen, device="cuda") * kmask).to(torch.bfloat16)
+    v = (torch.randn(shape, generator=gen, device="cuda") * vmask).to(torch.bfloat16)
+    q = torch.randn((w.batch, w.ctx, w.n_q_heads, w.head_dim), generator=gen, device="cuda").to(torch.bfloat16)
+    out = torch.empty_like(q)
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    # append: the whole prompt of both sequences per call, into an emptied cache
+    app = []
+    for i in range(warmup + steps):
+        cache.seq_len.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        kvq.kvq_rotate_quantize_append(cache.desc, k, v, stream=stream)
+        e1.record(stream)
+        app.append((e0, e1))
+    torch.cuda.synchronize()
+    app_ms = statistics.median(a.elapsed_time(b) for a, b in app[warmup:])
+    for i in range(warmup):
+        kvq.kvq_prefill_attention(cache.desc, q, out, ws, chunk=w.chunk, stream=stream)
+    torch.cuda.synchronize()
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0.record(stream)
+    for i in range(steps):
+        kvq.kvq_prefill_attention(cache.desc, q, out, ws, chunk=w.chunk, stream=stream)
+    p1.record(stream)
+    torch.cuda.synchronize()
+    st, bits = kvq.kvq_sync_status(cache.desc)
+    assert st == 0, (st, bits)
+    att_ms = p0.elapsed_time(p1) / steps
+    tokens = w.batch * w.ctx
+    app_bytes = append_bytes(w, w.ctx)
+    flops = prefill_flops(w)
+    peak = None
+    pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk):
+        peak = float(json.load(open(pk))["bf16_tflops"])
+    tflops = flops / (att_ms * 1e-3) / 1e12
+    return {"workload": w.name, "batch": w.batch, "prompt": w.ctx, "q_heads": w.n_q_heads,
+            "kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "k_type": w.k_type, "v_type": w.v_type,
+            "tail_len": w.tail_len, "causal": True,
+            "append": {"ms_per_call": round(app_ms, 4), "tokens_per_s": round(tokens / (app_ms * 1e-3), 1),
+                       "gbs": round(app_bytes / (app_ms * 1e-3) / 1e9, 1)},
+            "attention": {"ms_per_call": round(att_ms, 4), "useful_flops": flops,
+                          "tflops": round(tflops, 1), "bound": "tensor", "peak_tflops": peak,
+                          "peak_kind": "measured bf16 burst (the fp16 dense rate is the same)" if peak else None,
+                          "frac": round(tflops / peak, 4) if peak else None,
+                          "note": "fp16 UMMA, three products per contraction (hi/lo splits); useful flops only"}}
 
 
 # ---------------------------------------------------------------------------
@@ -419,6 +493,7 @@ def main():
     ap.add_argument("--ctx", type=int, default=0,
                     help="context length override (a smaller case of the same workload, e.g. for ncu captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the prompt-workload measurement")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     args = ap.parse_args()
     if args.warmup < 3:
