@@ -365,7 +365,8 @@ def run_prefill_bench(torch, kvq, steps: int, warmup: int, seed: int = 0):
     v = (torch.randn(shape, generator=gen, device="cuda") * vmask).to(torch.bfloat16)
     q = torch.randn((w.batch, w.ctx, w.n_q_heads, w.head_dim), generator=gen, device="cuda").to(torch.bfloat16)
     out = torch.empty_like(q)
-    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    ws = torch.empty(kvq.kvq_prefill_workspace_bytes(cache.desc, w.n_q_heads, w.ctx), dtype=torch.uint8,
+                     device="cuda")
     stream = torch.cuda.current_stream()
     # append: the whole prompt of both sequences per call, into an emptied cache
     app = []

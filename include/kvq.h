@@ -219,8 +219,14 @@ KVQ_API kvq_status kvq_decode_attention_noalloc(const kvq_cache* c, const void* 
                                                 int32_t n_q_heads, float scale, void* out,
                                                 int32_t out_dtype, void* stream);
 
-/* Workspace bytes kvq_prefill_attention needs: 0 (it writes its output rows
- * directly; the workspace arguments are accepted and ignored). */
+/* Workspace bytes kvq_prefill_attention needs (a pure size query: no
+ * pointer in *c is read): batch * n_kv_heads * (max_ctx / 64) tiles of
+ * 512 * head_dim bytes each, i.e. 8 bytes per cached K+V element of the
+ * capacity.  Every 64-key tile a call's queries can see is dequantized once
+ * into it (fp16 hi + lo operand tiles) before the attention kernel streams
+ * it.  0 when the shape is invalid or prefill does not support it.  The
+ * library-level staging has no counterpart in the method's description; it
+ * is how this implementation avoids dequantizing a key once per query tile. */
 KVQ_API size_t kvq_prefill_workspace_bytes(const kvq_cache* c, int32_t n_q_heads, int32_t n_tokens);
 
 /*
@@ -235,6 +241,10 @@ KVQ_API size_t kvq_prefill_workspace_bytes(const kvq_cache* c, int32_t n_q_heads
  *   chunk   queries per processing chunk (multiple of 64, or 0 for 512); it
  *           orders the work and does not change the result
  *   out     device [batch][n_tokens][n_q_heads][head_dim] of out_dtype
+ *   workspace, ws_bytes  device scratch, 16-byte aligned, at least
+ *           kvq_prefill_workspace_bytes(c, n_q_heads, n_tokens) bytes, else
+ *           KVQ_ERR_WORKSPACE; owned by the caller, overwritten by the call,
+ *           and must not be shared with a call running concurrently
  * Body / tail selection, rotation and scale are as in kvq_decode_attention.
  */
 KVQ_API kvq_status kvq_prefill_attention(const kvq_cache* c, const void* q, int32_t q_dtype,

@@ -192,14 +192,14 @@ kvq_status kvq_decode_attention_noalloc(const kvq_cache* c, const void* q, int32
 }
 
 size_t kvq_prefill_workspace_bytes(const kvq_cache* c, int32_t n_q_heads, int32_t n_tokens) {
-  (void)c; (void)n_q_heads; (void)n_tokens;
-  return 0;  // every CTA writes its own output rows; no partials
+  if (!shape_ok(c) || n_tokens < 0 || n_q_heads <= 0 || n_q_heads % c->n_kv_heads) return 0;
+  if (!kvq::prefill_supported(c->head_dim, n_q_heads / c->n_kv_heads)) return 0;
+  return kvq::prefill_workspace_bytes(*c);
 }
 
 kvq_status kvq_prefill_attention(const kvq_cache* c, const void* q, int32_t q_dtype, int32_t n_q_heads,
                                  int32_t n_tokens, const int32_t* q_pos0, int32_t causal, int32_t chunk, float scale,
                                  void* out, int32_t out_dtype, void* workspace, size_t ws_bytes, void* stream) {
-  (void)workspace; (void)ws_bytes;
   kvq_status s = check_cache(c);
   if (s != KVQ_OK) return s;
   kvq::Rot r{};
@@ -211,9 +211,10 @@ kvq_status kvq_prefill_attention(const kvq_cache* c, const void* q, int32_t q_dt
   if (n_tokens == 0) return KVQ_OK;
   if (!q || !out || !aligned16(q) || !aligned16(out)) return KVQ_ERR_INVALID_ARG;
   if (!kvq::prefill_supported(c->head_dim, n_q_heads / c->n_kv_heads)) return KVQ_ERR_UNSUPPORTED;
+  if (!workspace || !aligned16(workspace) || ws_bytes < kvq::prefill_workspace_bytes(*c)) return KVQ_ERR_WORKSPACE;
   const float sc = scale == 0.0f ? 1.0f / sqrtf(float(c->head_dim)) : scale;
   return from_cuda(kvq::launch_prefill(*c, r, q, q_dtype, n_q_heads, n_tokens, q_pos0, causal, sc, out, out_dtype,
-                                       static_cast<cudaStream_t>(stream)));
+                                       workspace, static_cast<cudaStream_t>(stream)));
 }
 
 kvq_status kvq_dequant_debug(const kvq_cache* c, int32_t seq, int32_t kv_head, int32_t which, int32_t t0,

@@ -49,10 +49,13 @@ cudaError_t launch_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, c
                           int q_dtype, int n_q_heads, float scale, void* out, int out_dtype,
                           void* ws, cudaStream_t st);
 
-// Prefill (tcgen05): head_dim 64 or 128, GQA group up to 128.
+// Prefill (tcgen05): head_dim 64 or 128, GQA group up to 128.  The workspace
+// holds every 64-key tile of every (sequence, KV head) up to max_ctx, staged
+// once as fp16 hi / lo operand tiles (512 * head_dim bytes per tile).
 bool prefill_supported(int d, int group);
+size_t prefill_workspace_bytes(const kvq_cache& c);
 cudaError_t launch_prefill(const kvq_cache& c, Rot rot, const void* q, int q_dtype, int n_q_heads, int n_tokens,
                            const int32_t* q_pos0, int causal, float scale, void* out, int out_dtype,
-                           cudaStream_t st);
+                           void* ws, cudaStream_t st);
 
 }  // namespace kvq

@@ -9,19 +9,32 @@
 // >= n - tail_len are read from the bf16 tail (aitrends.kr "KVarN과 Precision
 // Tail", section 용어 해설), older ones from the q4_0 / q5_0 / q8_0 body.
 //
-// CTA = 128 query rows (positions x the query heads of one KV head) x one KV
-// head x one sequence; 4 warps, one row per thread.  Per 64-key tile:
-//   1. all threads dequantize K (rows = keys) and V^T (rows = channels) into
-//      shared memory as fp16 hi + lo pairs that are exact (code * scale needs
-//      15 bits), scaled by 2^-8 so every stored value stays in fp16 range;
-//   2. one thread issues S = Q_hi K_hi^T + Q_hi K_lo^T + Q_lo K_hi^T
-//      (tcgen05.mma kind::f16, M=128, N=64) into TMEM;
-//   3. each thread loads its row of S, masks, runs the online softmax, writes
-//      P (fp16 hi + lo) to shared memory and rescales its O row in TMEM when
-//      its running maximum moved;
-//   4. one thread issues O += P_hi V_hi + P_hi V_lo + P_lo V_hi (N = head_dim).
-// The three-term products keep ~22 bits, so the result matches fp32 math.
-// Operands are K-major with the 128-byte swizzle (8-row atoms of 1 KB).
+// Two kernels per call:
+//
+// stage_kernel   one CTA per 64-key tile of a (sequence, KV head): every key
+//                the prompt can see is dequantized ONCE (code * scale, or the
+//                bf16 tail value), scaled by 2^-8 and split into exact fp16
+//                hi + lo parts, laid out exactly as the tensor cores read them
+//                (K: rows = keys; V^T: rows = channels; 128-byte swizzle) and
+//                written to the workspace with one bulk copy.  Keys past the
+//                sequence are zeros.
+// attn_kernel    one CTA per 128 query rows (positions x the query heads of
+//                one KV head), warp-specialized:
+//                  warp 4   streams K and V tiles (1-D bulk copies, two-slot
+//                           rings each, released by the MMAs that read them);
+//                  warp 5   issues S_j = Q K_j^T into one of two TMEM score
+//                           buffers and O += P_j V_j, each as three fp16
+//                           products (hi.hi + hi.lo + lo.hi: ~22 bits, so the
+//                           result matches fp32 arithmetic);
+//                  warps 0-3 (one query row per thread = TMEM lane) prepare
+//                           Q (rotate, scale, split), run the online softmax
+//                           on S_j while the tensor cores work on PV_{j-1} and
+//                           S_{j+1}, rescale O in TMEM when a row's maximum
+//                           grew by more than 2^4, write P_j, and finish with
+//                           O / l, the inverse rotation and the output cast.
+// Every wait is bounded: a wait that gives up sets the status word's timeout
+// bit and a shared abort flag that ends the other roles' loops; the CTA then
+// lets its copies and MMAs in flight finish (bounded) before it releases TMEM.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -35,43 +48,52 @@
 namespace kvq {
 namespace {
 
-constexpr int kPThreads = 128;   // one query row per thread
-constexpr int kPM = 128;         // query rows per CTA (UMMA M)
-constexpr int kPN = 64;          // keys per tile (UMMA N of Q K^T, K of P V)
-constexpr long long kPWait = 2000000000LL;  // ~1 s at 2 GHz per MMA group
+constexpr int kPM = 128;               // query rows per CTA (UMMA M)
+constexpr int kPN = 64;                // keys per tile
+constexpr int kAttnThreads = 192;      // warps 0-3 softmax, 4 producer, 5 MMA
+constexpr int kStageThreads = 256;
+constexpr long long kPWait = 2000000000LL;  // ~1 s at 2 GHz per wait
 constexpr float kPLog2e = 1.4426950408889634f;
-constexpr float kInvScale = 0.00390625f;    // stored K/V values are x * 2^-8
-constexpr float kLazyRescale = 4.0f;        // log2: P stays <= 16 * 256 in fp16
+constexpr float kInvScale = 0.00390625f;    // staged K/V values are x * 2^-8
+constexpr float kLazyRescale = 4.0f;        // log2 units: P*256 stays <= 2^12
 
 template <int D>
-struct PCfg {
-  static constexpr int KA = D / 64;                 // 128-byte atoms along head_dim
-  static constexpr int NB = D / 32;
-  static constexpr int q_bytes = KA * kPM * 128;    // [KA][128 rows][128 B]
-  static constexpr int k_bytes = KA * kPN * 128;    // [KA][64 keys][128 B]
-  static constexpr int v_bytes = D * 128;           // V^T: [D channels][64 keys * 2 B]
-  static constexpr int p_bytes = kPM * 128;         // [128 rows][64 keys * 2 B]
-  static constexpr int off_qh = 0, off_ql = q_bytes;
-  static constexpr int off_kh = 2 * q_bytes, off_kl = off_kh + k_bytes;
-  static constexpr int off_vh = off_kl + k_bytes, off_vl = off_vh + v_bytes;
-  static constexpr int off_ph = off_vl + v_bytes, off_pl = off_ph + p_bytes;
-  static constexpr int off_bar = off_pl + p_bytes;  // 2 mbarriers + TMEM address
-  static constexpr int smem = off_bar + 64 + 1024;
-  static constexpr int stage_stride = D + 1;        // epilogue fp32 rows (reuses Q and K)
-  static_assert(kPM * stage_stride * 4 <= off_vh, "epilogue staging must fit in the Q and K tiles");
+struct PL {
+  static constexpr int KA = D / 64;             // 128-byte atoms along head_dim
+  static constexpr int kt = KA * kPN * 128;     // K tile, hi or lo: [KA][64 keys][128 B]
+  static constexpr int vt = D * 128;            // V^T tile, hi or lo: [D channels][64 keys * 2 B]
+  static constexpr int tile = 2 * kt + 2 * vt;  // workspace bytes per tile: K hi, K lo, V hi, V lo
+  static constexpr int q = KA * kPM * 128;      // Q, hi or lo: [KA][128 rows][128 B]
+  static constexpr int p = kPM * 128;           // P, hi or lo: [128 rows][64 keys * 2 B]
+  static constexpr int off_qh = 0, off_ql = q;
+  static constexpr int off_k = 2 * q;           // two slots of [hi | lo]
+  static constexpr int off_v = off_k + 4 * kt;  // two slots of [hi | lo]
+  static constexpr int off_ph = off_v + 4 * vt, off_pl = off_ph + p;
+  static constexpr int off_bar = off_pl + p;
+  static constexpr int smem = off_bar + 256 + 1024;
+  static constexpr int stage_stride = D + 1;    // epilogue fp32 rows (reuse Q and K slots)
+  static_assert(kPM * stage_stride * 4 <= off_v, "epilogue staging must fit below the V slots");
   static constexpr uint32_t idesc_qk = tc::idesc_f16_f32(kPM, kPN);
   static constexpr uint32_t idesc_pv = tc::idesc_f16_f32(kPM, D);
-  static constexpr uint32_t tmem_cols = 256;        // S: columns 0..63, O: columns 128..128+D
+  static constexpr uint32_t tmem_cols = 256;    // S: columns 0..63 and 64..127, O: 128..128+D
   static constexpr uint32_t o_col = 128;
 };
+static_assert(PL<128>::smem <= 232448, "prefill shared memory over the per-CTA limit");
 
-struct PParams {
+struct SParams {
   const uint8_t* k_qs; const uint8_t* v_qs;
   const __half* k_d; const __half* v_d;
   const uint32_t* k_qh; const uint32_t* v_qh;
   const uint16_t* k_tail; const uint16_t* v_tail;
+  const int32_t* seq_len; const int32_t* q_pos0;
+  int n_kv_heads, max_ctx, tail_len, k_type, v_type, n_tokens, causal, max_tiles;
+  uint8_t* ws;
+};
+
+struct AParams {
+  const uint8_t* ws;
   const int32_t* seq_len; uint32_t* status;
-  int n_kv_heads, max_ctx, tail_len, k_type, v_type;
+  int n_kv_heads, max_tiles;
   const void* q; void* out;
   int q_dtype, out_dtype, n_q_heads, n_tokens, group, ppt, ntiles;
   const int32_t* q_pos0;
@@ -79,95 +101,271 @@ struct PParams {
   float scale_log2;
 };
 
-// 8 channels of one stored key/value -> fp16 hi and lo (4 + 4 pairs), value scaled by 2^-8.
-__device__ __forceinline__ void split8(const float (&v)[8], uint4& hi, uint4& lo) {
-  uint32_t h[4], l[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    h[i] = pack_h2(v[2 * i], v[2 * i + 1]);
-    const float2 f = __half22float2(u32_as_h2(h[i]));
-    l[i] = pack_h2(v[2 * i] - f.x, v[2 * i + 1] - f.y);
-  }
-  hi = make_uint4(h[0], h[1], h[2], h[3]);
-  lo = make_uint4(l[0], l[1], l[2], l[3]);
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-// The 32 stored body values of block `blk` of the key at plane row `row`, x 2^-8.
+// Keys of sequence b that any of the call's queries can see: [0, kv_end).
+__device__ __forceinline__ int visible_keys(int n, int p0, int n_queries, int causal) {
+  if (p0 < 0) return 0;
+  return causal ? min(n, p0 + n_queries) : n;
+}
+
+// fp16 hi / lo split of two values (hi = RN(x), lo = RN(x - hi); exact when x has <= 22 bits)
+__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  hi = pack_h2(a, b);
+  const float2 f = __half22float2(u32_as_h2(hi));
+  lo = pack_h2(a - f.x, b - f.y);
+}
+
+// 8 stored values (channels 8*ch .. 8*ch+7) of one key, times 2^-8.
 template <int D>
-__device__ __forceinline__ void load_body_block(const PParams& p, bool is_v, size_t row, int blk, float (&x)[32]) {
+__device__ __forceinline__ void load8(const SParams& p, bool is_v, int qt, bool valid, bool tail, size_t body_row,
+                                      size_t tail_row, int ch, float (&x)[8]) {
   constexpr int NB = D / 32;
-  const int qt = is_v ? p.v_type : p.k_type;
-  const float sc = __half2float((is_v ? p.v_d : p.k_d)[row * NB + blk]) * kInvScale;
+  if (!valid) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = 0.0f;
+    return;
+  }
+  if (tail) {
+    const uint4 w = *reinterpret_cast<const uint4*>((is_v ? p.v_tail : p.k_tail) + tail_row * D + ch * 8);
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      x[2 * e] = __uint_as_float(ww[e] << 16) * kInvScale;
+      x[2 * e + 1] = __uint_as_float(ww[e] & 0xFFFF0000u) * kInvScale;
+    }
+    return;
+  }
+  const int c0 = ch * 8, blk = c0 / 32, w = c0 % 32;
+  const float sc = __half2float((is_v ? p.v_d : p.k_d)[body_row * NB + blk]) * kInvScale;
   const uint8_t* qs = is_v ? p.v_qs : p.k_qs;
   if (qt == KVQ_TYPE_Q8_0) {
-    const uint4* src = reinterpret_cast<const uint4*>(qs + row * D + blk * 32);
-    const uint4 a = src[0], b = src[1];
-    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    const uint2 a = *reinterpret_cast<const uint2*>(qs + body_row * D + c0);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) x[i] = float(int8_t(w[i >> 2] >> (8 * (i & 3)))) * sc;
+    for (int e = 0; e < 8; ++e) x[e] = float(int8_t((e < 4 ? a.x : a.y) >> (8 * (e & 3)))) * sc;
   } else {
-    const uint4 a = *reinterpret_cast<const uint4*>(qs + row * (D / 2) + blk * 16);
-    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+    // byte i of a block holds element i (low nibble) and element i + 16 (high nibble)
+    const uint2 a = *reinterpret_cast<const uint2*>(qs + body_row * (D / 2) + blk * 16 + (w & 15));
+    const int shift = w < 16 ? 0 : 4;
     uint32_t qh = 0;
     int off = 8;
     if (qt == KVQ_TYPE_Q5_0) {
-      qh = (is_v ? p.v_qh : p.k_qh)[row * NB + blk];
+      qh = (is_v ? p.v_qh : p.k_qh)[body_row * NB + blk];
       off = 16;
     }
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t byte = (w[i >> 2] >> (8 * (i & 3))) & 0xFFu;
-      const int lo = int(byte & 15u) | int(((qh >> i) & 1u) << 4);
-      const int hi = int(byte >> 4) | int(((qh >> (i + 16)) & 1u) << 4);
-      x[i] = float(lo - off) * sc;
-      x[i + 16] = float(hi - off) * sc;
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t byte = ((e < 4 ? a.x : a.y) >> (8 * (e & 3))) & 0xFFu;
+      const int code = int((byte >> shift) & 15u) | int(((qh >> (w + e)) & 1u) << 4);
+      x[e] = float(code - off) * sc;
     }
   }
 }
 
+// ---------------------------------------------------------------------------
+// stage_kernel: one 64-key tile of one (sequence, KV head) -> workspace
+// ---------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(PParams p) {
-  using C = PCfg<D>;
-  constexpr int NB = C::NB;
-  constexpr int G = (D & (D - 1)) == 0 ? D : 64;
+__global__ void __launch_bounds__(kStageThreads) stage_kernel(SParams p) {
+  using L = PL<D>;
+  constexpr int NCH = D / 8;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bar_s = reinterpret_cast<uint64_t*>(smem + C::off_bar);
-  uint64_t* bar_o = bar_s + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::off_bar + 16);
+  uint8_t* sm = align1024(smem_raw);
+  const int j = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int n = min(max(p.seq_len[b], 0), p.max_ctx);  // reads stay inside the planes
+  const int p0 = p.q_pos0 ? p.q_pos0[b] : n - p.n_tokens;
+  if (j * kPN >= visible_keys(n, p0, p.n_tokens, p.causal)) return;
+  const int T = p.tail_len;
+  const size_t bh = (size_t)b * p.n_kv_heads + kvh;
+  const int key = threadIdx.x & (kPN - 1);   // a warp covers 32 consecutive keys
+  const int t = j * kPN + key;
+  const bool valid = t < n;
+  const bool tail = valid && T > 0 && t >= n - T;
+  const size_t body_row = bh * p.max_ctx + (valid ? t : 0);
+  const size_t tail_row = tail ? bh * T + t % T : 0;
+#pragma unroll 1
+  for (int ch = threadIdx.x / kPN; ch < NCH; ch += kStageThreads / kPN) {
+    // K: row = key, 16-byte chunks of 8 channels
+    float x[8];
+    load8<D>(p, false, p.k_type, valid, tail, body_row, tail_row, ch, x);
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) split2(x[2 * e], x[2 * e + 1], h[e], l[e]);
+    const uint32_t off = (ch / 8) * (kPN * 128) + tc::sw128_chunk(key, ch % 8);
+    *reinterpret_cast<uint4*>(sm + off) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(sm + L::kt + off) = make_uint4(l[0], l[1], l[2], l[3]);
+    // V^T: row = channel, this key's 2-byte element in it
+    load8<D>(p, true, p.v_type, valid, tail, body_row, tail_row, ch, x);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) split2(x[2 * e], x[2 * e + 1], h[e], l[e]);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t o = tc::sw128_chunk(ch * 8 + e, key / 8) + (key % 8) * 2;
+      *reinterpret_cast<uint16_t*>(sm + 2 * L::kt + o) = uint16_t(h[e / 2] >> (16 * (e & 1)));
+      *reinterpret_cast<uint16_t*>(sm + 2 * L::kt + L::vt + o) = uint16_t(l[e / 2] >> (16 * (e & 1)));
+    }
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    bulk_s2g(p.ws + (bh * p.max_tiles + j) * (size_t)L::tile, sm, L::tile);
+    bulk_commit();
+    bulk_wait_all();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// attn_kernel
+// ---------------------------------------------------------------------------
+struct Sync {
+  uint64_t kfull[2], kempty[2], vfull[2], vempty[2], sfull[2], sfree[2];
+  uint64_t pfull, odone, qready, fin;
+  uint32_t tmem;
+  int abort;
+};
+
+// Bounded wait that also gives up when another role has aborted.
+__device__ __forceinline__ bool role_wait(uint64_t* bar, uint32_t parity, Sync* sy, uint32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity, 20000u)) {
+    if (*reinterpret_cast<volatile int*>(&sy->abort)) return false;
+    if (clock64() - t0 > kPWait) {
+      *reinterpret_cast<volatile int*>(&sy->abort) = 1;
+      atomicOr(status, KVQ_DEV_ERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
+  using L = PL<D>;
+  constexpr int G = D;  // head_dim 64 and 128 rotate as one Hadamard group
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  Sync* sy = reinterpret_cast<Sync*>(sm + L::off_bar);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int tile = p.ntiles - 1 - blockIdx.x;  // the longest (latest) query tiles first
   const int kvh = blockIdx.y, b = blockIdx.z;
   const int g = p.group;
-  const int n = p.seq_len[b];
-  const int T = p.tail_len;
+  const int n = min(max(p.seq_len[b], 0), p.max_tiles * kPN);  // as the stage kernel
   const int p0 = p.q_pos0 ? p.q_pos0[b] : n - p.n_tokens;
-
-  // this thread's query row
-  const int li = tid / g, hh = tid % g;
-  const int qi = tile * p.ppt + li;
-  const bool row_ok = li < p.ppt && qi < p.n_tokens && p0 >= 0;
-  const int pos = p0 + qi;
-  const int head = kvh * g + hh;
-  const int kv_end_row = row_ok ? (p.causal ? min(n, pos + 1) : n) : 0;
-  // keys any row of the CTA can see
   const int last_q = min(p.n_tokens, (tile + 1) * p.ppt) - 1;
-  const int kv_end = p0 < 0 ? 0 : (p.causal ? min(n, p0 + last_q + 1) : n);
+  const int kv_end = visible_keys(n, p0, last_q + 1, p.causal);
   const int nkv = (kv_end + kPN - 1) / kPN;
   if (p0 < 0 && tid == 0 && blockIdx.x == 0 && kvh == 0) atomicOr(p.status, KVQ_DEV_ERR_PREFILL_RANGE);
 
   if (warp == 0) {
-    tc::tmem_alloc(tmem_slot, C::tmem_cols);
+    tc::tmem_alloc(&sy->tmem, L::tmem_cols);
     tc::tmem_relinquish();
   }
-  if (tid == 0) {
-    mbar_init(bar_s, 1);
-    mbar_init(bar_o, 1);
+  if (tid == 32) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sy->kfull[i], 1); mbar_init(&sy->kempty[i], 1);
+      mbar_init(&sy->vfull[i], 1); mbar_init(&sy->vempty[i], 1);
+      mbar_init(&sy->sfull[i], 1); mbar_init(&sy->sfree[i], kPM);
+    }
+    mbar_init(&sy->pfull, kPM);
+    mbar_init(&sy->odone, 1);
+    mbar_init(&sy->qready, kPM);
+    mbar_init(&sy->fin, 1);
+    sy->abort = 0;
     fence_barrier_init();
   }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = sy->tmem;
 
-  // ---- Q rows: load, rotate, scale, split into hi / lo tiles ---------------
+  if (warp == 4) {
+    // ---- producer: K and V tiles of this (sequence, KV head) ----------------
+    if (lane == 0 && nkv > 0) {
+      const uint8_t* base = p.ws + ((size_t)b * p.n_kv_heads + kvh) * p.max_tiles * (size_t)L::tile;
+      int kiss = 0, viss = 0;
+      for (int j = 0; j < nkv; ++j) {
+        const int s = j & 1;
+        const uint32_t u = j >> 1;
+        const uint8_t* src = base + (size_t)j * L::tile;
+        if (u > 0 && !role_wait(&sy->kempty[s], (u - 1) & 1, sy, p.status)) break;
+        mbar_arrive_expect_tx(&sy->kfull[s], 2 * L::kt);
+        bulk_g2s(sm + L::off_k + s * 2 * L::kt, src, 2 * L::kt, &sy->kfull[s]);
+        ++kiss;
+        if (u > 0 && !role_wait(&sy->vempty[s], (u - 1) & 1, sy, p.status)) break;
+        mbar_arrive_expect_tx(&sy->vfull[s], 2 * L::vt);
+        bulk_g2s(sm + L::off_v + s * 2 * L::vt, src + 2 * L::kt, 2 * L::vt, &sy->vfull[s]);
+        ++viss;
+      }
+      // copies still landing (abort path): let them finish before the CTA can exit
+      for (int j = max(0, kiss - 2); j < kiss; ++j) mbar_wait_bounded(&sy->kfull[j & 1], (j >> 1) & 1, kPWait);
+      for (int j = max(0, viss - 2); j < viss; ++j) mbar_wait_bounded(&sy->vfull[j & 1], (j >> 1) & 1, kPWait);
+    }
+    return;
+  }
+
+  if (warp == 5) {
+    // ---- MMA issue (one thread) -------------------------------------------
+    if (lane == 0 && nkv > 0) {
+      const uint32_t sb = smem_u32(sm);
+      auto issue_s = [&](int j) {
+        const int s = j & 1;
+        const uint32_t kb = sb + L::off_k + s * 2 * L::kt;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t qa = sb + (ks / 4) * (kPM * 128) + (ks % 4) * 32;
+          const uint32_t ka = kb + (ks / 4) * (kPN * 128) + (ks % 4) * 32;
+          const uint64_t aqh = tc::sdesc_sw128(qa + L::off_qh), aql = tc::sdesc_sw128(qa + L::off_ql);
+          const uint64_t bkh = tc::sdesc_sw128(ka), bkl = tc::sdesc_sw128(ka + L::kt);
+          const uint32_t d = tmem + s * kPN;
+          tc::mma_f16(d, aqh, bkh, L::idesc_qk, ks > 0 ? 1u : 0u);
+          tc::mma_f16(d, aqh, bkl, L::idesc_qk, 1u);
+          tc::mma_f16(d, aql, bkh, L::idesc_qk, 1u);
+        }
+        tc::commit(&sy->sfull[s]);
+        tc::commit(&sy->kempty[s]);
+      };
+      bool ok = role_wait(&sy->qready, 0, sy, p.status) && role_wait(&sy->kfull[0], 0, sy, p.status);
+      if (ok) {
+        tc::fence_after_sync();
+        issue_s(0);
+      }
+      for (int j = 0; ok && j < nkv; ++j) {
+        if (j + 1 < nkv) {
+          const int s = (j + 1) & 1;
+          const uint32_t u = (j + 1) >> 1;
+          ok = role_wait(&sy->kfull[s], u & 1, sy, p.status) &&
+               (u == 0 || role_wait(&sy->sfree[s], (u - 1) & 1, sy, p.status));
+          if (!ok) break;
+          tc::fence_after_sync();
+          issue_s(j + 1);
+        }
+        ok = role_wait(&sy->pfull, j & 1, sy, p.status) &&
+             role_wait(&sy->vfull[j & 1], (j >> 1) & 1, sy, p.status);
+        if (!ok) break;
+        tc::fence_after_sync();
+        const uint32_t vb = sb + L::off_v + (j & 1) * 2 * L::vt;
+#pragma unroll
+        for (int ks = 0; ks < kPN / 16; ++ks) {
+          const uint32_t pa = sb + ks * 32;
+          const uint64_t aph = tc::sdesc_sw128(pa + L::off_ph), apl = tc::sdesc_sw128(pa + L::off_pl);
+          const uint64_t bvh = tc::sdesc_sw128(vb + ks * 32), bvl = tc::sdesc_sw128(vb + L::vt + ks * 32);
+          tc::mma_f16(tmem + L::o_col, aph, bvh, L::idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
+          tc::mma_f16(tmem + L::o_col, aph, bvl, L::idesc_pv, 1u);
+          tc::mma_f16(tmem + L::o_col, apl, bvh, L::idesc_pv, 1u);
+        }
+        tc::commit(&sy->odone);
+        tc::commit(&sy->vempty[j & 1]);
+      }
+      tc::commit(&sy->fin);  // arrives once every MMA issued above has completed
+    }
+    return;
+  }
+
+  // ---- warps 0-3: Q rows: load, rotate, scale, split into hi / lo tiles -----
   {
     constexpr int P = G / 32;
     for (int rr = 0; rr < 32; ++rr) {
@@ -192,239 +390,144 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(PParams p) {
         warp_fwht<D, G>(v, lane);
         s *= inv_sqrt_group<G>();
       }
-      // lane holds P consecutive channels per G-group: write them as fp16 hi / lo
+      // lane holds P consecutive channels: write them as fp16 hi / lo pairs
 #pragma unroll
-      for (int gi = 0; gi < D / G; ++gi) {
-#pragma unroll
-        for (int j0 = 0; j0 < P; j0 += 2) {
-          const int c = gi * G + lane * P + j0;
-          const float a = v[gi * P + j0] * s, bq = v[gi * P + j0 + 1] * s;
-          uint32_t hi, lo;
-          hi = pack_h2(a, bq);
-          const float2 f = __half22float2(u32_as_h2(hi));
-          lo = pack_h2(a - f.x, bq - f.y);
-          const uint32_t off = (c / 64) * (kPM * 128) + tc::sw128_chunk(r, (c % 64) / 8) + (c % 8) * 2;
-          *reinterpret_cast<uint32_t*>(smem + C::off_qh + off) = hi;
-          *reinterpret_cast<uint32_t*>(smem + C::off_ql + off) = lo;
-        }
+      for (int j0 = 0; j0 < P; j0 += 2) {
+        const int c = lane * P + j0;
+        uint32_t hi, lo;
+        split2(v[j0] * s, v[j0 + 1] * s, hi, lo);
+        const uint32_t off = (c / 64) * (kPM * 128) + tc::sw128_chunk(r, (c % 64) / 8) + (c % 8) * 2;
+        *reinterpret_cast<uint32_t*>(sm + L::off_qh + off) = hi;
+        *reinterpret_cast<uint32_t*>(sm + L::off_ql + off) = lo;
       }
     }
   }
   fence_proxy_async_smem();
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = *tmem_slot;
+  mbar_arrive(&sy->qready);
 
-  // ---- main loop over 64-key tiles -------------------------------------------
-  float m_used = -INFINITY, l = 0.0f;
-  bool timed_out = false;
-  uint64_t* pend_bar = bar_s;
-  uint32_t pend_phase = 0;
-  const size_t bh = (size_t)b * p.n_kv_heads + kvh;
-  const int kk_key = tid & 63, khalf = tid >> 6;  // dequant role: key, channel half
-  const uint32_t s_taddr = tmem + ((uint32_t)(warp * 32) << 16);
-  const uint32_t o_taddr = s_taddr + C::o_col;
-
+  // ---- softmax: this thread's query row = TMEM lane tid --------------------
+  const int li = tid / g, hh = tid % g;
+  const int qi = tile * p.ppt + li;
+  const bool row_ok = li < p.ppt && qi < p.n_tokens && p0 >= 0;
+  const int kv_end_row = row_ok ? (p.causal ? min(n, p0 + qi + 1) : n) : 0;
+  const uint32_t lane_taddr = tmem + ((uint32_t)(warp * 32) << 16);
+  float m_used = -INFINITY;  // reference maximum of the row, log2 units
+  float l = 0.0f;            // sum of the row's P * 256
+  bool ok = true;
   for (int j = 0; j < nkv; ++j) {
-    // 1. dequantize K and V^T of keys [64j, 64j+64) into shared memory
-    {
-      const int t = j * kPN + kk_key;
-      const bool valid = t < kv_end;
-      const bool tail = valid && t >= n - T;
-      const size_t body_row = bh * p.max_ctx + (valid ? t : 0);
-      const size_t tail_row = T > 0 ? (bh * T + (tail ? t % T : 0)) * D : 0;
-#pragma unroll
-      for (int which = 0; which < 2; ++which) {
-#pragma unroll
-        for (int bb = 0; bb < NB / 2; ++bb) {
-          const int blk = khalf * (NB / 2) + bb;
-          float x[32];
-          if (!valid) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) x[i] = 0.0f;
-          } else if (tail) {
-            const uint16_t* src = (which ? p.v_tail : p.k_tail) + tail_row + blk * 32;
-#pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-              const uint4 w = *reinterpret_cast<const uint4*>(src + i);
-              const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                x[i + 2 * e] = __uint_as_float(ww[e] << 16) * kInvScale;
-                x[i + 2 * e + 1] = __uint_as_float(ww[e] & 0xFFFF0000u) * kInvScale;
-              }
-            }
-          } else {
-            load_body_block<D>(p, which == 1, body_row, blk, x);
-          }
-          if (which == 0) {
-            // K tile: row = key, 16-byte chunks of 8 channels
-#pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8) {
-              const int c = blk * 32 + c8 * 8;
-              float v8[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) v8[e] = x[c8 * 8 + e];
-              uint4 hi, lo;
-              split8(v8, hi, lo);
-              const uint32_t off = (c / 64) * (kPN * 128) + tc::sw128_chunk(kk_key, (c % 64) / 8);
-              *reinterpret_cast<uint4*>(smem + C::off_kh + off) = hi;
-              *reinterpret_cast<uint4*>(smem + C::off_kl + off) = lo;
-            }
-          } else {
-            // V^T tile: row = channel, this key's 2-byte element in it
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              const int c = blk * 32 + e;
-              const uint32_t h2 = pack_h2(x[e], x[e + 1]);
-              const float2 f = __half22float2(u32_as_h2(h2));
-              const uint32_t l2 = pack_h2(x[e] - f.x, x[e + 1] - f.y);
-              const uint32_t o0 = tc::sw128_chunk(c, kk_key / 8) + (kk_key % 8) * 2;
-              const uint32_t o1 = tc::sw128_chunk(c + 1, kk_key / 8) + (kk_key % 8) * 2;
-              *reinterpret_cast<uint16_t*>(smem + C::off_vh + o0) = uint16_t(h2 & 0xFFFFu);
-              *reinterpret_cast<uint16_t*>(smem + C::off_vh + o1) = uint16_t(h2 >> 16);
-              *reinterpret_cast<uint16_t*>(smem + C::off_vl + o0) = uint16_t(l2 & 0xFFFFu);
-              *reinterpret_cast<uint16_t*>(smem + C::off_vl + o1) = uint16_t(l2 >> 16);
-            }
-          }
-        }
-      }
-    }
-    fence_proxy_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-
-    // 2. S = Q K^T (three fp16 products)
-    if (tid == 0) {
-      tc::fence_after_sync();
-#pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        const uint32_t qa = smem_u32(smem) + (ks / 4) * (kPM * 128) + (ks % 4) * 32;
-        const uint32_t ka = smem_u32(smem) + (ks / 4) * (kPN * 128) + (ks % 4) * 32;
-        const uint64_t aqh = tc::sdesc_sw128(qa + C::off_qh), aql = tc::sdesc_sw128(qa + C::off_ql);
-        const uint64_t bkh = tc::sdesc_sw128(ka + C::off_kh), bkl = tc::sdesc_sw128(ka + C::off_kl);
-        tc::mma_f16(tmem, aqh, bkh, C::idesc_qk, ks > 0 ? 1u : 0u);
-        tc::mma_f16(tmem, aqh, bkl, C::idesc_qk, 1u);
-        tc::mma_f16(tmem, aql, bkh, C::idesc_qk, 1u);
-      }
-      tc::commit(bar_s);
-    }
-    if (!mbar_wait_bounded(bar_s, j & 1, kPWait)) { timed_out = true; }
-    if (__syncthreads_or(timed_out)) { timed_out = true; pend_bar = bar_s; pend_phase = j & 1; break; }
+    const int s = j & 1;
+    ok = __all_sync(0xffffffffu, role_wait(&sy->sfull[s], (j >> 1) & 1, sy, p.status));
+    if (!ok) break;
     tc::fence_after_sync();
-
-    // 3. softmax of this thread's row; P -> shared memory; O rescale in TMEM
     float sv[kPN];
 #pragma unroll
     for (int c = 0; c < kPN; c += 16) {
       float t16[16];
-      tc::ld_x16(s_taddr + c, t16);
+      tc::ld_x16(lane_taddr + s * kPN + c, t16);
 #pragma unroll
       for (int e = 0; e < 16; ++e) sv[c + e] = t16[e];
     }
     tc::wait_ld();
-    float mt = -INFINITY;
+    tc::fence_before_sync();
+    mbar_arrive(&sy->sfree[s]);
+    // mask keys past this row's end (partial tiles only)
+    if (j * kPN + kPN > kv_end_row) {
 #pragma unroll
-    for (int c = 0; c < kPN; ++c) {
-      const int t = j * kPN + c;
-      sv[c] = (t < kv_end_row) ? sv[c] * 256.0f : -INFINITY;  // keys were stored x 2^-8
-      mt = fmaxf(mt, sv[c]);
+      for (int c = 0; c < kPN; ++c)
+        if (j * kPN + c >= kv_end_row) sv[c] = -INFINITY;
     }
-    // lazy rescale: move the row's reference maximum only when it grew by more
-    // than 2^4, so P stays <= 16 (x 256) in fp16
+    float mx[4] = {sv[0], sv[1], sv[2], sv[3]};
+#pragma unroll
+    for (int c = 4; c < kPN; ++c) mx[c & 3] = fmaxf(mx[c & 3], sv[c]);
+    const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * 256.0f;  // keys were staged x 2^-8
+    // lazy rescale: move the reference maximum only when it grew by more than 2^4
     float alpha = 1.0f;
     const bool move = mt > m_used + kLazyRescale || (m_used == -INFINITY && mt > -INFINITY);
     if (move) {
-      alpha = m_used == -INFINITY ? 0.0f : exp2f(m_used - mt);
+      alpha = m_used == -INFINITY ? 0.0f : ex2_approx(m_used - mt);
       l *= alpha;
       m_used = mt;
     }
-    if (j > 0 && __any_sync(0xffffffffu, move)) {  // TMEM access is warp-collective
+    // P * 256 (values were staged x 2^-8): 2^(s*256 - (m - 8))
+    const float mb = m_used == -INFINITY ? 0.0f : m_used - 8.0f;
+    uint32_t ph[kPN / 2], pl[kPN / 2];
+    float ls[2] = {0.0f, 0.0f};
 #pragma unroll
-      for (int c = 0; c < D; c += 16) {
-        float t16[16];
-        tc::ld_x16(o_taddr + c, t16);
-        tc::wait_ld();
-#pragma unroll
-        for (int e = 0; e < 16; ++e) t16[e] *= alpha;
-        tc::st_x16(o_taddr + c, t16);
-      }
-      tc::wait_st();
+    for (int c = 0; c < kPN; c += 2) {
+      const float e0 = ex2_approx(fmaf(sv[c], 256.0f, -mb));
+      const float e1 = ex2_approx(fmaf(sv[c + 1], 256.0f, -mb));
+      ls[0] += e0;
+      ls[1] += e1;
+      split2(e0, e1, ph[c / 2], pl[c / 2]);
     }
-    const float ms = m_used == -INFINITY ? 0.0f : m_used;
+    l += ls[0] + ls[1];
+    // PV_{j-1} must be complete: O is stable and the P buffer is free
+    if (j > 0) {
+      ok = __all_sync(0xffffffffu, role_wait(&sy->odone, (j - 1) & 1, sy, p.status));
+      if (!ok) break;
+      tc::fence_after_sync();
+      if (__any_sync(0xffffffffu, move)) {  // TMEM access is warp-collective
+#pragma unroll
+        for (int c = 0; c < D; c += 16) {
+          float t16[16];
+          tc::ld_x16(lane_taddr + L::o_col + c, t16);
+          tc::wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) t16[e] *= alpha;
+          tc::st_x16(lane_taddr + L::o_col + c, t16);
+        }
+        tc::wait_st();
+      }
+    }
 #pragma unroll
     for (int c8 = 0; c8 < kPN / 8; ++c8) {
-      float v8[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float pe = exp2f(sv[c8 * 8 + e] - ms);  // 0 for masked keys
-        l += pe;
-        v8[e] = pe * 256.0f;                            // values were stored x 2^-8
-      }
-      uint4 hi, lo;
-      split8(v8, hi, lo);
       const uint32_t off = tc::sw128_chunk(tid, c8);
-      *reinterpret_cast<uint4*>(smem + C::off_ph + off) = hi;
-      *reinterpret_cast<uint4*>(smem + C::off_pl + off) = lo;
+      *reinterpret_cast<uint4*>(sm + L::off_ph + off) =
+          make_uint4(ph[4 * c8], ph[4 * c8 + 1], ph[4 * c8 + 2], ph[4 * c8 + 3]);
+      *reinterpret_cast<uint4*>(sm + L::off_pl + off) =
+          make_uint4(pl[4 * c8], pl[4 * c8 + 1], pl[4 * c8 + 2], pl[4 * c8 + 3]);
     }
     fence_proxy_async_smem();
     tc::fence_before_sync();
-    __syncthreads();
-
-    // 4. O += P V (three fp16 products)
-    if (tid == 0) {
-      tc::fence_after_sync();
-#pragma unroll
-      for (int ks = 0; ks < kPN / 16; ++ks) {
-        const uint32_t pa = smem_u32(smem) + ks * 32;
-        const uint64_t aph = tc::sdesc_sw128(pa + C::off_ph), apl = tc::sdesc_sw128(pa + C::off_pl);
-        const uint64_t bvh = tc::sdesc_sw128(pa + C::off_vh), bvl = tc::sdesc_sw128(pa + C::off_vl);
-        tc::mma_f16(tmem + C::o_col, aph, bvh, C::idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
-        tc::mma_f16(tmem + C::o_col, aph, bvl, C::idesc_pv, 1u);
-        tc::mma_f16(tmem + C::o_col, apl, bvh, C::idesc_pv, 1u);
-      }
-      tc::commit(bar_o);
-    }
-    if (!mbar_wait_bounded(bar_o, j & 1, kPWait)) { timed_out = true; }
-    if (__syncthreads_or(timed_out)) { timed_out = true; pend_bar = bar_o; pend_phase = j & 1; break; }
-    tc::fence_after_sync();
+    mbar_arrive(&sy->pfull);
   }
-
-  if (timed_out) {
-    if (tid == 0) atomicOr(p.status, KVQ_DEV_ERR_TIMEOUT);
-    // let the MMA group still in flight finish (bounded) before the TMEM is released
-    mbar_wait_bounded(pend_bar, pend_phase, kPWait);
-  }
+  // every MMA of the CTA has completed once `fin` arrives (also on the abort path)
+  if (nkv > 0 && !mbar_wait_bounded(&sy->fin, 0, kPWait)) ok = false;
+  ok = ok && !*reinterpret_cast<volatile int*>(&sy->abort);
+  tc::fence_after_sync();
 
   // ---- epilogue: O / l -> staging -> inverse rotation -> output -------------
-  float* stage = reinterpret_cast<float*>(smem);  // [128][D + 1], reuses Q and K
+  float* stage = reinterpret_cast<float*>(sm);  // [128][D + 1], reuses the Q and K slots
   {
-    const float inv = (l > 0.0f && nkv > 0 && !timed_out) ? 1.0f / l : 0.0f;
+    const float inv = (l > 0.0f && nkv > 0 && ok) ? 256.0f / l : 0.0f;
+    const bool ld = __any_sync(0xffffffffu, nkv > 0 && ok);
 #pragma unroll
     for (int c = 0; c < D; c += 16) {
       float t16[16];
-      if (nkv > 0) {
-        tc::ld_x16(o_taddr + c, t16);
+      if (ld) {
+        tc::ld_x16(lane_taddr + L::o_col + c, t16);
         tc::wait_ld();
       } else {
 #pragma unroll
         for (int e = 0; e < 16; ++e) t16[e] = 0.0f;
       }
 #pragma unroll
-      for (int e = 0; e < 16; ++e) stage[tid * C::stage_stride + c + e] = t16[e] * inv;
+      for (int e = 0; e < 16; ++e) stage[tid * L::stage_stride + c + e] = t16[e] * inv;
     }
   }
   tc::fence_before_sync();
-  __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem, C::tmem_cols);
+  named_sync(1, kPM);
+  if (warp == 0) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, L::tmem_cols);
+  }
   for (int rr = 0; rr < 32; ++rr) {
     const int r = warp * 32 + rr;
     const int rli = r / g, rhh = r % g, rqi = tile * p.ppt + rli;
     if (!(rli < p.ppt && rqi < p.n_tokens)) continue;
     float v[D / 32];
 #pragma unroll
-    for (int j = 0; j < D / 32; ++j) v[j] = stage[r * C::stage_stride + fwht_channel<D, G>(lane, j)];
+    for (int j = 0; j < D / 32; ++j) v[j] = stage[r * L::stage_stride + fwht_channel<D, G>(lane, j)];
     if (p.rot_v) {
       warp_fwht<D, G>(v, lane);
 #pragma unroll
@@ -439,34 +542,45 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(PParams p) {
       else static_cast<__half*>(p.out)[e] = __float2half_rn(v[j]);
     }
   }
-  (void)row_ok; (void)head;
+  (void)hh;
 }
 
 template <int D>
 cudaError_t run_prefill(const kvq_cache& c, Rot rot, const void* q, int q_dtype, int n_q_heads, int n_tokens,
-                        const int32_t* q_pos0, int causal, float scale, void* out, int out_dtype, cudaStream_t st) {
-  using Cf = PCfg<D>;
-  PParams p{};
-  p.k_qs = static_cast<const uint8_t*>(c.k_qs); p.v_qs = static_cast<const uint8_t*>(c.v_qs);
-  p.k_d = static_cast<const __half*>(c.k_d); p.v_d = static_cast<const __half*>(c.v_d);
-  p.k_qh = static_cast<const uint32_t*>(c.k_qh); p.v_qh = static_cast<const uint32_t*>(c.v_qh);
-  p.k_tail = static_cast<const uint16_t*>(c.k_tail); p.v_tail = static_cast<const uint16_t*>(c.v_tail);
+                        const int32_t* q_pos0, int causal, float scale, void* out, int out_dtype, void* ws,
+                        cudaStream_t st) {
+  using L = PL<D>;
+  const int max_tiles = c.max_ctx / kPN;
+  SParams sp{};
+  sp.k_qs = static_cast<const uint8_t*>(c.k_qs); sp.v_qs = static_cast<const uint8_t*>(c.v_qs);
+  sp.k_d = static_cast<const __half*>(c.k_d); sp.v_d = static_cast<const __half*>(c.v_d);
+  sp.k_qh = static_cast<const uint32_t*>(c.k_qh); sp.v_qh = static_cast<const uint32_t*>(c.v_qh);
+  sp.k_tail = static_cast<const uint16_t*>(c.k_tail); sp.v_tail = static_cast<const uint16_t*>(c.v_tail);
+  sp.seq_len = c.seq_len; sp.q_pos0 = q_pos0;
+  sp.n_kv_heads = c.n_kv_heads; sp.max_ctx = c.max_ctx; sp.tail_len = c.tail_len;
+  sp.k_type = c.k_type; sp.v_type = c.v_type; sp.n_tokens = n_tokens; sp.causal = causal ? 1 : 0;
+  sp.max_tiles = max_tiles; sp.ws = static_cast<uint8_t*>(ws);
+  AParams p{};
+  p.ws = static_cast<const uint8_t*>(ws);
   p.seq_len = c.seq_len; p.status = c.status;
-  p.n_kv_heads = c.n_kv_heads; p.max_ctx = c.max_ctx; p.tail_len = c.tail_len;
-  p.k_type = c.k_type; p.v_type = c.v_type;
+  p.n_kv_heads = c.n_kv_heads; p.max_tiles = max_tiles;
   p.q = q; p.out = out; p.q_dtype = q_dtype; p.out_dtype = out_dtype;
   p.n_q_heads = n_q_heads; p.n_tokens = n_tokens;
   p.group = n_q_heads / c.n_kv_heads;
   p.ppt = kPM / p.group;
   p.ntiles = (n_tokens + p.ppt - 1) / p.ppt;
-  p.q_pos0 = q_pos0; p.causal = causal ? 1 : 0;
+  p.q_pos0 = q_pos0; p.causal = sp.causal;
   p.rot_k = rot.k; p.rot_v = rot.v;
   p.scale_log2 = scale * kPLog2e;
-  auto kern = prefill_kernel<D>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::smem);
+  constexpr int stage_smem = L::tile + 1024;
+  cudaError_t e = cudaFuncSetAttribute(stage_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, stage_smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.ntiles, c.n_kv_heads, c.batch);
-  kern<<<grid, kPThreads, Cf::smem, st>>>(p);
+  e = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::smem);
+  if (e != cudaSuccess) return e;
+  stage_kernel<D><<<dim3(max_tiles, c.n_kv_heads, c.batch), kStageThreads, stage_smem, st>>>(sp);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  attn_kernel<D><<<dim3(p.ntiles, c.n_kv_heads, c.batch), kAttnThreads, L::smem, st>>>(p);
   return cudaGetLastError();
 }
 
@@ -474,12 +588,19 @@ cudaError_t run_prefill(const kvq_cache& c, Rot rot, const void* q, int q_dtype,
 
 bool prefill_supported(int d, int group) { return (d == 64 || d == 128) && group >= 1 && group <= kPM; }
 
+size_t prefill_workspace_bytes(const kvq_cache& c) {
+  if (c.head_dim != 64 && c.head_dim != 128) return 0;
+  return (size_t)c.batch * c.n_kv_heads * (c.max_ctx / kPN) * (size_t)(512 * c.head_dim);
+}
+
 cudaError_t launch_prefill(const kvq_cache& c, Rot rot, const void* q, int q_dtype, int n_q_heads, int n_tokens,
-                           const int32_t* q_pos0, int causal, float scale, void* out, int out_dtype,
+                           const int32_t* q_pos0, int causal, float scale, void* out, int out_dtype, void* ws,
                            cudaStream_t st) {
   switch (c.head_dim) {
-    case 64: return run_prefill<64>(c, rot, q, q_dtype, n_q_heads, n_tokens, q_pos0, causal, scale, out, out_dtype, st);
-    case 128: return run_prefill<128>(c, rot, q, q_dtype, n_q_heads, n_tokens, q_pos0, causal, scale, out, out_dtype, st);
+    case 64:
+      return run_prefill<64>(c, rot, q, q_dtype, n_q_heads, n_tokens, q_pos0, causal, scale, out, out_dtype, ws, st);
+    case 128:
+      return run_prefill<128>(c, rot, q, q_dtype, n_q_heads, n_tokens, q_pos0, causal, scale, out, out_dtype, ws, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -20,7 +20,9 @@ def gpu_prefill(gc, q_np, q_dtype, torch, causal=True, q_pos0=None, out_dtype="f
     q = to_dev(q_np, q_dtype, torch)
     tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[out_dtype]
     out = torch.full(q.shape, float("nan"), dtype=tdt, device="cuda")
-    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    wsb = kvq.kvq_prefill_workspace_bytes(gc.desc, q.shape[2], q.shape[1])
+    assert wsb > 0
+    ws = torch.full((wsb,), 0xFF, dtype=torch.uint8, device="cuda")   # NaN fp16 pattern: stale bytes must not leak
     pos = None if q_pos0 is None else torch.tensor(np.asarray(q_pos0, np.int32)).cuda()
     kvq.kvq_prefill_attention(gc.desc, q, out, ws, q_pos0=pos, causal=causal, chunk=512, scale=scale)
     st, bits = kvq.kvq_sync_status(gc.desc)
@@ -131,7 +133,7 @@ def test_negative_query_position_is_reported():
     kvq.kvq_rotate_quantize_append(gc.desc, k, k)
     q = to_dev(rng.standard_normal((1, 20, 1, 64)).astype(np.float32), "f32", torch)  # 20 > 10 keys
     out = torch.full(q.shape, 7.0, device="cuda")
-    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    ws = torch.empty(kvq.kvq_prefill_workspace_bytes(gc.desc, 1, 20), dtype=torch.uint8, device="cuda")
     kvq.kvq_prefill_attention(gc.desc, q, out, ws)   # q_pos0 = 10 - 20 < 0
     st, bits = kvq.kvq_sync_status(gc.desc)
     assert st == kvq.KVQ_ERR_DEVICE_RANGE and bits == kvq.KVQ_DEV_ERR_PREFILL_RANGE
