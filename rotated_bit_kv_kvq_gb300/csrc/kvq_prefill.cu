@@ -20,18 +20,24 @@
 //                sequence are zeros.
 // attn_kernel    one CTA per 128 query rows (positions x the query heads of
 //                one KV head), warp-specialized:
-//                  warp 4   streams K and V tiles (1-D bulk copies, two-slot
+//                  warp 8   streams K and V tiles (1-D bulk copies, two-slot
 //                           rings each, released by the MMAs that read them);
-//                  warp 5   issues S_j = Q K_j^T into one of two TMEM score
-//                           buffers and O += P_j V_j, each as three fp16
-//                           products (hi.hi + hi.lo + lo.hi: ~22 bits, so the
-//                           result matches fp32 arithmetic);
-//                  warps 0-3 (one query row per thread = TMEM lane) prepare
-//                           Q (rotate, scale, split), run the online softmax
-//                           on S_j while the tensor cores work on PV_{j-1} and
-//                           S_{j+1}, rescale O in TMEM when a row's maximum
-//                           grew by more than 2^4, write P_j, and finish with
-//                           O / l, the inverse rotation and the output cast.
+//                  warp 9   issues S_j = Q K_j^T into one of two TMEM score
+//                           buffers, warp 10 issues O += P_j V_j (two issuing
+//                           warps keep the tensor pipe fed: one thread alone
+//                           issues an MMA only every ~75 cycles); each is
+//                           three fp16 products (hi.hi + hi.lo + lo.hi: ~22
+//                           bits, so the result matches fp32 arithmetic);
+//                  warps 0-7 (two warpgroups; row = TMEM lane, warpgroup h
+//                           owns keys 32h..32h+31 of every tile and output
+//                           channels h*D/2..) prepare Q (rotate, scale,
+//                           split), run the online softmax on S_j while the
+//                           tensor cores work on PV_{j-1} and S_{j+1} (both
+//                           halves take the row maximum over all 64 scores,
+//                           so they agree without exchanging it), rescale O
+//                           in TMEM when a row's maximum grew by more than
+//                           2^4, write P_j, and finish with O / l, the
+//                           inverse rotation and the output cast.
 // Every wait is bounded: a wait that gives up sets the status word's timeout
 // bit and a shared abort flag that ends the other roles' loops; the CTA then
 // lets its copies and MMAs in flight finish (bounded) before it releases TMEM.
@@ -50,7 +56,8 @@ namespace {
 
 constexpr int kPM = 128;               // query rows per CTA (UMMA M)
 constexpr int kPN = 64;                // keys per tile
-constexpr int kAttnThreads = 192;      // warps 0-3 softmax, 4 producer, 5 MMA
+constexpr int kSoftmax = 256;          // two warpgroups, each half of a row's 64 scores
+constexpr int kAttnThreads = kSoftmax + 96;  // + warp 8 producer, 9 S issue, 10 PV issue
 constexpr int kStageThreads = 256;
 constexpr long long kPWait = 2000000000LL;  // ~1 s at 2 GHz per wait
 constexpr float kPLog2e = 1.4426950408889634f;
@@ -71,7 +78,7 @@ struct PL {
   static constexpr int off_ph = off_v + 4 * vt, off_pl = off_ph + p;
   static constexpr int off_bar = off_pl + p;
   static constexpr int smem = off_bar + 256 + 1024;
-  static constexpr int stage_stride = D + 1;    // epilogue fp32 rows (reuse Q and K slots)
+  static constexpr int stage_stride = D + 4;    // epilogue fp32 rows (reuse Q and K slots), 16-byte rows
   static_assert(kPM * stage_stride * 4 <= off_v, "epilogue staging must fit below the V slots");
   static constexpr uint32_t idesc_qk = tc::idesc_f16_f32(kPM, kPN);
   static constexpr uint32_t idesc_pv = tc::idesc_f16_f32(kPM, D);
@@ -221,7 +228,7 @@ __global__ void __launch_bounds__(kStageThreads) stage_kernel(SParams p) {
 // ---------------------------------------------------------------------------
 struct Sync {
   uint64_t kfull[2], kempty[2], vfull[2], vempty[2], sfull[2], sfree[2];
-  uint64_t pfull, odone, qready, fin;
+  uint64_t pfull, odone, qready, fin[2];
   uint32_t tmem;
   int abort;
 };
@@ -264,16 +271,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
     tc::tmem_alloc(&sy->tmem, L::tmem_cols);
     tc::tmem_relinquish();
   }
-  if (tid == 32) {
+  if (tid == kSoftmax) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sy->kfull[i], 1); mbar_init(&sy->kempty[i], 1);
       mbar_init(&sy->vfull[i], 1); mbar_init(&sy->vempty[i], 1);
-      mbar_init(&sy->sfull[i], 1); mbar_init(&sy->sfree[i], kPM);
+      mbar_init(&sy->sfull[i], 1); mbar_init(&sy->sfree[i], kSoftmax);
     }
-    mbar_init(&sy->pfull, kPM);
+    mbar_init(&sy->pfull, kSoftmax);
     mbar_init(&sy->odone, 1);
-    mbar_init(&sy->qready, kPM);
-    mbar_init(&sy->fin, 1);
+    mbar_init(&sy->qready, kSoftmax);
+    mbar_init(&sy->fin[0], 1);
+    mbar_init(&sy->fin[1], 1);
     sy->abort = 0;
     fence_barrier_init();
   }
@@ -282,7 +290,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
   tc::fence_after_sync();
   const uint32_t tmem = sy->tmem;
 
-  if (warp == 4) {
+  if (warp == kSoftmax / 32) {
     // ---- producer: K and V tiles of this (sequence, KV head) ----------------
     if (lane == 0 && nkv > 0) {
       const uint8_t* base = p.ws + ((size_t)b * p.n_kv_heads + kvh) * p.max_tiles * (size_t)L::tile;
@@ -307,69 +315,72 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
     return;
   }
 
-  if (warp == 5) {
-    // ---- MMA issue (one thread) -------------------------------------------
+  // Shared-memory descriptors: the K-step and slot offsets are added to these
+  // bases (the 14-bit start-address field cannot overflow inside the buffer).
+  const uint32_t sb = smem_u32(sm);
+  if (warp == kSoftmax / 32 + 1) {
+    // ---- S_j = Q K_j^T issue (one thread) ----------------------------------
     if (lane == 0 && nkv > 0) {
-      const uint32_t sb = smem_u32(sm);
-      auto issue_s = [&](int j) {
+      const uint64_t dqh = tc::sdesc_sw128(sb + L::off_qh), dql = tc::sdesc_sw128(sb + L::off_ql);
+      const uint64_t dk = tc::sdesc_sw128(sb + L::off_k);
+      bool ok = role_wait(&sy->qready, 0, sy, p.status);
+      for (int j = 0; ok && j < nkv; ++j) {
         const int s = j & 1;
-        const uint32_t kb = sb + L::off_k + s * 2 * L::kt;
+        const uint32_t u = j >> 1;
+        ok = role_wait(&sy->kfull[s], u & 1, sy, p.status) &&
+             (u == 0 || role_wait(&sy->sfree[s], (u - 1) & 1, sy, p.status));
+        if (!ok) break;
+        tc::fence_after_sync();
+        const uint64_t kh = dk + ((s * 2 * L::kt) >> 4), kl = kh + (L::kt >> 4);
+        const uint32_t d = tmem + s * kPN;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t qa = sb + (ks / 4) * (kPM * 128) + (ks % 4) * 32;
-          const uint32_t ka = kb + (ks / 4) * (kPN * 128) + (ks % 4) * 32;
-          const uint64_t aqh = tc::sdesc_sw128(qa + L::off_qh), aql = tc::sdesc_sw128(qa + L::off_ql);
-          const uint64_t bkh = tc::sdesc_sw128(ka), bkl = tc::sdesc_sw128(ka + L::kt);
-          const uint32_t d = tmem + s * kPN;
-          tc::mma_f16(d, aqh, bkh, L::idesc_qk, ks > 0 ? 1u : 0u);
-          tc::mma_f16(d, aqh, bkl, L::idesc_qk, 1u);
-          tc::mma_f16(d, aql, bkh, L::idesc_qk, 1u);
+          const uint32_t qo = ((ks / 4) * (kPM * 128) + (ks % 4) * 32) >> 4;
+          const uint32_t ko = ((ks / 4) * (kPN * 128) + (ks % 4) * 32) >> 4;
+          tc::mma_f16(d, dqh + qo, kh + ko, L::idesc_qk, ks > 0 ? 1u : 0u);
+          tc::mma_f16(d, dqh + qo, kl + ko, L::idesc_qk, 1u);
+          tc::mma_f16(d, dql + qo, kh + ko, L::idesc_qk, 1u);
         }
         tc::commit(&sy->sfull[s]);
         tc::commit(&sy->kempty[s]);
-      };
-      bool ok = role_wait(&sy->qready, 0, sy, p.status) && role_wait(&sy->kfull[0], 0, sy, p.status);
-      if (ok) {
-        tc::fence_after_sync();
-        issue_s(0);
       }
-      for (int j = 0; ok && j < nkv; ++j) {
-        if (j + 1 < nkv) {
-          const int s = (j + 1) & 1;
-          const uint32_t u = (j + 1) >> 1;
-          ok = role_wait(&sy->kfull[s], u & 1, sy, p.status) &&
-               (u == 0 || role_wait(&sy->sfree[s], (u - 1) & 1, sy, p.status));
-          if (!ok) break;
-          tc::fence_after_sync();
-          issue_s(j + 1);
-        }
-        ok = role_wait(&sy->pfull, j & 1, sy, p.status) &&
-             role_wait(&sy->vfull[j & 1], (j >> 1) & 1, sy, p.status);
-        if (!ok) break;
-        tc::fence_after_sync();
-        const uint32_t vb = sb + L::off_v + (j & 1) * 2 * L::vt;
-#pragma unroll
-        for (int ks = 0; ks < kPN / 16; ++ks) {
-          const uint32_t pa = sb + ks * 32;
-          const uint64_t aph = tc::sdesc_sw128(pa + L::off_ph), apl = tc::sdesc_sw128(pa + L::off_pl);
-          const uint64_t bvh = tc::sdesc_sw128(vb + ks * 32), bvl = tc::sdesc_sw128(vb + L::vt + ks * 32);
-          tc::mma_f16(tmem + L::o_col, aph, bvh, L::idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
-          tc::mma_f16(tmem + L::o_col, aph, bvl, L::idesc_pv, 1u);
-          tc::mma_f16(tmem + L::o_col, apl, bvh, L::idesc_pv, 1u);
-        }
-        tc::commit(&sy->odone);
-        tc::commit(&sy->vempty[j & 1]);
-      }
-      tc::commit(&sy->fin);  // arrives once every MMA issued above has completed
+      tc::commit(&sy->fin[0]);  // arrives once every MMA issued above has completed
     }
     return;
   }
 
-  // ---- warps 0-3: Q rows: load, rotate, scale, split into hi / lo tiles -----
+  if (warp == kSoftmax / 32 + 2) {
+    // ---- O += P_j V_j issue (one thread; runs beside the S issue) ------------
+    if (lane == 0 && nkv > 0) {
+      const uint64_t dph = tc::sdesc_sw128(sb + L::off_ph), dpl = tc::sdesc_sw128(sb + L::off_pl);
+      const uint64_t dv = tc::sdesc_sw128(sb + L::off_v);
+      bool ok = true;
+      for (int j = 0; ok && j < nkv; ++j) {
+        ok = role_wait(&sy->pfull, j & 1, sy, p.status) &&
+             role_wait(&sy->vfull[j & 1], (j >> 1) & 1, sy, p.status);
+        if (!ok) break;
+        tc::fence_after_sync();
+        const uint64_t vh = dv + (((j & 1) * 2 * L::vt) >> 4), vl = vh + (L::vt >> 4);
+#pragma unroll
+        for (int ks = 0; ks < kPN / 16; ++ks) {
+          const uint32_t o = (ks * 32) >> 4;
+          tc::mma_f16(tmem + L::o_col, dph + o, vh + o, L::idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
+          tc::mma_f16(tmem + L::o_col, dph + o, vl + o, L::idesc_pv, 1u);
+          tc::mma_f16(tmem + L::o_col, dpl + o, vh + o, L::idesc_pv, 1u);
+        }
+        tc::commit(&sy->odone);
+        tc::commit(&sy->vempty[j & 1]);
+      }
+      tc::commit(&sy->fin[1]);
+    }
+    return;
+  }
+
+  // ---- warps 0-7: Q rows: load, rotate, scale, split into hi / lo tiles -----
   {
     constexpr int P = G / 32;
-    for (int rr = 0; rr < 32; ++rr) {
-      const int r = warp * 32 + rr;
+    for (int rr = 0; rr < kPM / 8; ++rr) {
+      const int r = warp * (kPM / 8) + rr;
       const int rli = r / g, rhh = r % g, rqi = tile * p.ppt + rli;
       const bool ok = rli < p.ppt && rqi < p.n_tokens;
       float v[D / 32];
@@ -405,40 +416,44 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
   fence_proxy_async_smem();
   mbar_arrive(&sy->qready);
 
-  // ---- softmax: this thread's query row = TMEM lane tid --------------------
-  const int li = tid / g, hh = tid % g;
+  // ---- softmax: row = TMEM lane (tid % 128), half h of the 64 keys ---------
+  const int row = tid & (kPM - 1), h = tid / kPM;
+  const int li = row / g;
   const int qi = tile * p.ppt + li;
   const bool row_ok = li < p.ppt && qi < p.n_tokens && p0 >= 0;
   const int kv_end_row = row_ok ? (p.causal ? min(n, p0 + qi + 1) : n) : 0;
-  const uint32_t lane_taddr = tmem + ((uint32_t)(warp * 32) << 16);
-  float m_used = -INFINITY;  // reference maximum of the row, log2 units
-  float l = 0.0f;            // sum of the row's P * 256
+  const uint32_t lane_taddr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+  constexpr int HN = kPN / 2;  // keys of a tile owned by this thread
+  constexpr int HD = D / 2;    // output channels owned by this thread
+  float m_used = -INFINITY;    // reference maximum of the row, log2 units
+  float l = 0.0f;              // sum of this half's P * 256
   bool ok = true;
   for (int j = 0; j < nkv; ++j) {
     const int s = j & 1;
     ok = __all_sync(0xffffffffu, role_wait(&sy->sfull[s], (j >> 1) & 1, sy, p.status));
     if (!ok) break;
     tc::fence_after_sync();
-    float sv[kPN];
-#pragma unroll
-    for (int c = 0; c < kPN; c += 16) {
-      float t16[16];
-      tc::ld_x16(lane_taddr + s * kPN + c, t16);
-#pragma unroll
-      for (int e = 0; e < 16; ++e) sv[c + e] = t16[e];
-    }
+    float sv[HN], so[HN];  // own half, other half
+    const uint32_t sa = lane_taddr + s * kPN;
+    tc::ld_x16(sa + h * HN, *reinterpret_cast<float(*)[16]>(&sv[0]));
+    tc::ld_x16(sa + h * HN + 16, *reinterpret_cast<float(*)[16]>(&sv[16]));
+    tc::ld_x16(sa + (1 - h) * HN, *reinterpret_cast<float(*)[16]>(&so[0]));
+    tc::ld_x16(sa + (1 - h) * HN + 16, *reinterpret_cast<float(*)[16]>(&so[16]));
     tc::wait_ld();
     tc::fence_before_sync();
     mbar_arrive(&sy->sfree[s]);
     // mask keys past this row's end (partial tiles only)
     if (j * kPN + kPN > kv_end_row) {
+      const int own0 = j * kPN + h * HN, oth0 = j * kPN + (1 - h) * HN;
 #pragma unroll
-      for (int c = 0; c < kPN; ++c)
-        if (j * kPN + c >= kv_end_row) sv[c] = -INFINITY;
+      for (int c = 0; c < HN; ++c) {
+        if (own0 + c >= kv_end_row) sv[c] = -INFINITY;
+        if (oth0 + c >= kv_end_row) so[c] = -INFINITY;
+      }
     }
-    float mx[4] = {sv[0], sv[1], sv[2], sv[3]};
+    float mx[4] = {fmaxf(sv[0], so[0]), fmaxf(sv[1], so[1]), fmaxf(sv[2], so[2]), fmaxf(sv[3], so[3])};
 #pragma unroll
-    for (int c = 4; c < kPN; ++c) mx[c & 3] = fmaxf(mx[c & 3], sv[c]);
+    for (int c = 4; c < HN; ++c) mx[c & 3] = fmaxf(mx[c & 3], fmaxf(sv[c], so[c]));
     const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * 256.0f;  // keys were staged x 2^-8
     // lazy rescale: move the reference maximum only when it grew by more than 2^4
     float alpha = 1.0f;
@@ -450,10 +465,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
     }
     // P * 256 (values were staged x 2^-8): 2^(s*256 - (m - 8))
     const float mb = m_used == -INFINITY ? 0.0f : m_used - 8.0f;
-    uint32_t ph[kPN / 2], pl[kPN / 2];
+    uint32_t ph[HN / 2], pl[HN / 2];
     float ls[2] = {0.0f, 0.0f};
 #pragma unroll
-    for (int c = 0; c < kPN; c += 2) {
+    for (int c = 0; c < HN; c += 2) {
       const float e0 = ex2_approx(fmaf(sv[c], 256.0f, -mb));
       const float e1 = ex2_approx(fmaf(sv[c + 1], 256.0f, -mb));
       ls[0] += e0;
@@ -468,20 +483,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
       tc::fence_after_sync();
       if (__any_sync(0xffffffffu, move)) {  // TMEM access is warp-collective
 #pragma unroll
-        for (int c = 0; c < D; c += 16) {
+        for (int c = 0; c < HD; c += 16) {
           float t16[16];
-          tc::ld_x16(lane_taddr + L::o_col + c, t16);
+          tc::ld_x16(lane_taddr + L::o_col + h * HD + c, t16);
           tc::wait_ld();
 #pragma unroll
           for (int e = 0; e < 16; ++e) t16[e] *= alpha;
-          tc::st_x16(lane_taddr + L::o_col + c, t16);
+          tc::st_x16(lane_taddr + L::o_col + h * HD + c, t16);
         }
         tc::wait_st();
       }
     }
 #pragma unroll
-    for (int c8 = 0; c8 < kPN / 8; ++c8) {
-      const uint32_t off = tc::sw128_chunk(tid, c8);
+    for (int c8 = 0; c8 < HN / 8; ++c8) {
+      const uint32_t off = tc::sw128_chunk(row, h * (HN / 8) + c8);
       *reinterpret_cast<uint4*>(sm + L::off_ph + off) =
           make_uint4(ph[4 * c8], ph[4 * c8 + 1], ph[4 * c8 + 2], ph[4 * c8 + 3]);
       *reinterpret_cast<uint4*>(sm + L::off_pl + off) =
@@ -491,58 +506,70 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
     tc::fence_before_sync();
     mbar_arrive(&sy->pfull);
   }
-  // every MMA of the CTA has completed once `fin` arrives (also on the abort path)
-  if (nkv > 0 && !mbar_wait_bounded(&sy->fin, 0, kPWait)) ok = false;
+  // every MMA of the CTA has completed once both `fin` barriers arrive (also on the abort path)
+  if (nkv > 0 && !(mbar_wait_bounded(&sy->fin[0], 0, kPWait) && mbar_wait_bounded(&sy->fin[1], 0, kPWait))) ok = false;
   ok = ok && !*reinterpret_cast<volatile int*>(&sy->abort);
   tc::fence_after_sync();
 
-  // ---- epilogue: O / l -> staging -> inverse rotation -> output -------------
-  float* stage = reinterpret_cast<float*>(sm);  // [128][D + 1], reuses the Q and K slots
+  // ---- epilogue: l of both halves, O / l -> staging -> inverse rotation -----
+  float* xl = reinterpret_cast<float*>(sm + L::off_ph);  // [2][128]; the P tile is free now
+  xl[h * kPM + row] = l;
+  named_sync(1, kSoftmax);
+  const float lt = l + xl[(1 - h) * kPM + row];
+  float* stage = reinterpret_cast<float*>(sm);  // [128][D + 4], reuses the Q and K slots
   {
-    const float inv = (l > 0.0f && nkv > 0 && ok) ? 256.0f / l : 0.0f;
+    const float inv = (lt > 0.0f && nkv > 0 && ok) ? 256.0f / lt : 0.0f;
     const bool ld = __any_sync(0xffffffffu, nkv > 0 && ok);
 #pragma unroll
-    for (int c = 0; c < D; c += 16) {
+    for (int c = 0; c < HD; c += 16) {
       float t16[16];
       if (ld) {
-        tc::ld_x16(lane_taddr + L::o_col + c, t16);
+        tc::ld_x16(lane_taddr + L::o_col + h * HD + c, t16);
         tc::wait_ld();
       } else {
 #pragma unroll
         for (int e = 0; e < 16; ++e) t16[e] = 0.0f;
       }
 #pragma unroll
-      for (int e = 0; e < 16; ++e) stage[tid * L::stage_stride + c + e] = t16[e] * inv;
+      for (int e = 0; e < 16; e += 4)
+        *reinterpret_cast<float4*>(&stage[row * L::stage_stride + h * HD + c + e]) =
+            make_float4(t16[e] * inv, t16[e + 1] * inv, t16[e + 2] * inv, t16[e + 3] * inv);
     }
   }
   tc::fence_before_sync();
-  named_sync(1, kPM);
+  named_sync(1, kSoftmax);
   if (warp == 0) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, L::tmem_cols);
   }
-  for (int rr = 0; rr < 32; ++rr) {
-    const int r = warp * 32 + rr;
+  constexpr int P = D / 32;  // consecutive channels per lane
+  for (int rr = 0; rr < kPM / 8; ++rr) {
+    const int r = warp * (kPM / 8) + rr;
     const int rli = r / g, rhh = r % g, rqi = tile * p.ppt + rli;
     if (!(rli < p.ppt && rqi < p.n_tokens)) continue;
-    float v[D / 32];
-#pragma unroll
-    for (int j = 0; j < D / 32; ++j) v[j] = stage[r * L::stage_stride + fwht_channel<D, G>(lane, j)];
+    float v[P];
+    const float* src = &stage[r * L::stage_stride + lane * P];
+    if constexpr (P == 4) {
+      const float4 t = *reinterpret_cast<const float4*>(src);
+      v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+    } else {
+      const float2 t = *reinterpret_cast<const float2*>(src);
+      v[0] = t.x; v[1] = t.y;
+    }
     if (p.rot_v) {
       warp_fwht<D, G>(v, lane);
 #pragma unroll
-      for (int j = 0; j < D / 32; ++j) v[j] *= inv_sqrt_group<G>();
+      for (int j = 0; j < P; ++j) v[j] *= inv_sqrt_group<G>();
     }
     const size_t base = (((size_t)b * p.n_tokens + rqi) * p.n_q_heads + kvh * g + rhh) * D;
 #pragma unroll
-    for (int j = 0; j < D / 32; ++j) {
+    for (int j = 0; j < P; ++j) {
       const size_t e = base + fwht_channel<D, G>(lane, j);
       if (p.out_dtype == KVQ_F32) static_cast<float*>(p.out)[e] = v[j];
       else if (p.out_dtype == KVQ_BF16) static_cast<__nv_bfloat16*>(p.out)[e] = __float2bfloat16_rn(v[j]);
       else static_cast<__half*>(p.out)[e] = __float2half_rn(v[j]);
     }
   }
-  (void)hh;
 }
 
 template <int D>
