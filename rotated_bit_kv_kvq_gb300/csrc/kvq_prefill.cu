@@ -67,7 +67,7 @@ constexpr float kLazyRescale = 4.0f;        // log2 units: P*256 stays <= 2^12
 template <int D>
 struct PL {
   static constexpr int KA = D / 64;             // 128-byte atoms along head_dim
-  static constexpr int kt = KA * kPN * 128;     // K tile, hi or lo: [KA][64 keys][128 B]
+  static constexpr int kt = KA * kPN * 128;     // K tile, hi or lo (stored [KA][hi, lo][64 keys][128 B])
   static constexpr int vt = D * 128;            // V^T tile, hi or lo: [D channels][64 keys * 2 B]
   static constexpr int tile = 2 * kt + 2 * vt;  // workspace bytes per tile: K hi, K lo, V hi, V lo
   static constexpr int q = KA * kPM * 128;      // Q, hi or lo: [KA][128 rows][128 B]
@@ -80,10 +80,16 @@ struct PL {
   static constexpr int smem = off_bar + 256 + 1024;
   static constexpr int stage_stride = D + 4;    // epilogue fp32 rows (reuse Q and K slots), 16-byte rows
   static_assert(kPM * stage_stride * 4 <= off_v, "epilogue staging must fit below the V slots");
-  static constexpr uint32_t idesc_qk = tc::idesc_f16_f32(kPM, kPN);
-  static constexpr uint32_t idesc_pv = tc::idesc_f16_f32(kPM, D);
-  static constexpr uint32_t tmem_cols = 256;    // S: columns 0..63 and 64..127, O: 128..128+D
-  static constexpr uint32_t o_col = 128;
+  static constexpr uint32_t idesc_qk = tc::idesc_f16_f32(kPM, kPN);        // Q_lo . K_hi
+  static constexpr uint32_t idesc_qk2 = tc::idesc_f16_f32(kPM, 2 * kPN);   // Q_hi . [K_hi; K_lo]
+  static constexpr uint32_t idesc_pv = tc::idesc_f16_f32(kPM, D);         // P_lo . V_hi
+  static constexpr uint32_t idesc_pv2 = tc::idesc_f16_f32(kPM, 2 * D);     // P_hi . [V_hi; V_lo]
+  // TMEM: two score buffers of 128 columns ([hi.hi + lo.hi | hi.lo] of 64 keys) and
+  // O as [hi.hi + lo.hi | hi.lo] over 2 * D columns from 256 (summed in the epilogue)
+  static constexpr uint32_t tmem_cols = 512;
+  static constexpr uint32_t s_cols = 2 * kPN;
+  static constexpr uint32_t o_col = 256;
+  static_assert(o_col + 2 * D <= tmem_cols, "TMEM columns");
 };
 static_assert(PL<128>::smem <= 232448, "prefill shared memory over the per-CTA limit");
 
@@ -200,9 +206,10 @@ __global__ void __launch_bounds__(kStageThreads) stage_kernel(SParams p) {
     uint32_t h[4], l[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) split2(x[2 * e], x[2 * e + 1], h[e], l[e]);
-    const uint32_t off = (ch / 8) * (kPN * 128) + tc::sw128_chunk(key, ch % 8);
+    // per 128-byte atom: 64 hi rows then 64 lo rows, so one N=128 operand holds both
+    const uint32_t off = (ch / 8) * (2 * kPN * 128) + tc::sw128_chunk(key, ch % 8);
     *reinterpret_cast<uint4*>(sm + off) = make_uint4(h[0], h[1], h[2], h[3]);
-    *reinterpret_cast<uint4*>(sm + L::kt + off) = make_uint4(l[0], l[1], l[2], l[3]);
+    *reinterpret_cast<uint4*>(sm + kPN * 128 + off) = make_uint4(l[0], l[1], l[2], l[3]);
     // V^T: row = channel, this key's 2-byte element in it
     load8<D>(p, true, p.v_type, valid, tail, body_row, tail_row, ch, x);
 #pragma unroll
@@ -331,15 +338,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
              (u == 0 || role_wait(&sy->sfree[s], (u - 1) & 1, sy, p.status));
         if (!ok) break;
         tc::fence_after_sync();
-        const uint64_t kh = dk + ((s * 2 * L::kt) >> 4), kl = kh + (L::kt >> 4);
-        const uint32_t d = tmem + s * kPN;
+        const uint64_t kb = dk + ((s * 2 * L::kt) >> 4);
+        const uint32_t d = tmem + s * L::s_cols;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t qo = ((ks / 4) * (kPM * 128) + (ks % 4) * 32) >> 4;
-          const uint32_t ko = ((ks / 4) * (kPN * 128) + (ks % 4) * 32) >> 4;
-          tc::mma_f16(d, dqh + qo, kh + ko, L::idesc_qk, ks > 0 ? 1u : 0u);
-          tc::mma_f16(d, dqh + qo, kl + ko, L::idesc_qk, 1u);
-          tc::mma_f16(d, dql + qo, kh + ko, L::idesc_qk, 1u);
+          const uint32_t ko = ((ks / 4) * (2 * kPN * 128) + (ks % 4) * 32) >> 4;
+          tc::mma_f16(d, dqh + qo, kb + ko, L::idesc_qk2, ks > 0 ? 1u : 0u);  // [hi.hi | hi.lo]
+          tc::mma_f16(d, dql + qo, kb + ko, L::idesc_qk, 1u);                 // + lo.hi
         }
         tc::commit(&sy->sfull[s]);
         tc::commit(&sy->kempty[s]);
@@ -360,12 +366,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
              role_wait(&sy->vfull[j & 1], (j >> 1) & 1, sy, p.status);
         if (!ok) break;
         tc::fence_after_sync();
-        const uint64_t vh = dv + (((j & 1) * 2 * L::vt) >> 4), vl = vh + (L::vt >> 4);
+        // V^T hi rows then lo rows are contiguous: one N = 2D operand holds both
+        const uint64_t vh = dv + (((j & 1) * 2 * L::vt) >> 4);
 #pragma unroll
         for (int ks = 0; ks < kPN / 16; ++ks) {
           const uint32_t o = (ks * 32) >> 4;
-          tc::mma_f16(tmem + L::o_col, dph + o, vh + o, L::idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
-          tc::mma_f16(tmem + L::o_col, dph + o, vl + o, L::idesc_pv, 1u);
+          tc::mma_f16(tmem + L::o_col, dph + o, vh + o, L::idesc_pv2, (j > 0 || ks > 0) ? 1u : 0u);
           tc::mma_f16(tmem + L::o_col, dpl + o, vh + o, L::idesc_pv, 1u);
         }
         tc::commit(&sy->odone);
@@ -434,12 +440,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
     if (!ok) break;
     tc::fence_after_sync();
     float sv[HN], so[HN];  // own half, other half
-    const uint32_t sa = lane_taddr + s * kPN;
-    tc::ld_x16(sa + h * HN, *reinterpret_cast<float(*)[16]>(&sv[0]));
-    tc::ld_x16(sa + h * HN + 16, *reinterpret_cast<float(*)[16]>(&sv[16]));
-    tc::ld_x16(sa + (1 - h) * HN, *reinterpret_cast<float(*)[16]>(&so[0]));
-    tc::ld_x16(sa + (1 - h) * HN + 16, *reinterpret_cast<float(*)[16]>(&so[16]));
-    tc::wait_ld();
+    {
+      float t[HN];
+      const uint32_t sa = lane_taddr + s * L::s_cols;
+      tc::ld_x16(sa + h * HN, *reinterpret_cast<float(*)[16]>(&sv[0]));
+      tc::ld_x16(sa + h * HN + 16, *reinterpret_cast<float(*)[16]>(&sv[16]));
+      tc::ld_x16(sa + kPN + h * HN, *reinterpret_cast<float(*)[16]>(&t[0]));
+      tc::ld_x16(sa + kPN + h * HN + 16, *reinterpret_cast<float(*)[16]>(&t[16]));
+      tc::wait_ld();
+#pragma unroll
+      for (int c = 0; c < HN; ++c) sv[c] += t[c];
+      tc::ld_x16(sa + (1 - h) * HN, *reinterpret_cast<float(*)[16]>(&so[0]));
+      tc::ld_x16(sa + (1 - h) * HN + 16, *reinterpret_cast<float(*)[16]>(&so[16]));
+      tc::ld_x16(sa + kPN + (1 - h) * HN, *reinterpret_cast<float(*)[16]>(&t[0]));
+      tc::ld_x16(sa + kPN + (1 - h) * HN + 16, *reinterpret_cast<float(*)[16]>(&t[16]));
+      tc::wait_ld();
+#pragma unroll
+      for (int c = 0; c < HN; ++c) so[c] += t[c];
+    }
     tc::fence_before_sync();
     mbar_arrive(&sy->sfree[s]);
     // mask keys past this row's end (partial tiles only)
@@ -483,13 +501,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
       tc::fence_after_sync();
       if (__any_sync(0xffffffffu, move)) {  // TMEM access is warp-collective
 #pragma unroll
-        for (int c = 0; c < HD; c += 16) {
+        for (int c = 0; c < D; c += 16) {  // this half's D columns of [O_a | O_b]
           float t16[16];
-          tc::ld_x16(lane_taddr + L::o_col + h * HD + c, t16);
+          const uint32_t col = L::o_col + h * D + c;
+          tc::ld_x16(lane_taddr + col, t16);
           tc::wait_ld();
 #pragma unroll
           for (int e = 0; e < 16; ++e) t16[e] *= alpha;
-          tc::st_x16(lane_taddr + L::o_col + h * HD + c, t16);
+          tc::st_x16(lane_taddr + col, t16);
         }
         tc::wait_st();
       }
@@ -524,8 +543,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
     for (int c = 0; c < HD; c += 16) {
       float t16[16];
       if (ld) {
+        float u16[16];
         tc::ld_x16(lane_taddr + L::o_col + h * HD + c, t16);
+        tc::ld_x16(lane_taddr + L::o_col + D + h * HD + c, u16);
         tc::wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) t16[e] += u16[e];
       } else {
 #pragma unroll
         for (int e = 0; e < 16; ++e) t16[e] = 0.0f;
