@@ -71,25 +71,25 @@ struct PL {
   static constexpr int vt = D * 128;            // V^T tile, hi or lo: [D channels][64 keys * 2 B]
   static constexpr int tile = 2 * kt + 2 * vt;  // workspace bytes per tile: K hi, K lo, V hi, V lo
   static constexpr int q = KA * kPM * 128;      // Q, hi or lo: [KA][128 rows][128 B]
-  static constexpr int p = kPM * 128;           // P, hi or lo: [128 rows][64 keys * 2 B]
   static constexpr int off_qh = 0, off_ql = q;
   static constexpr int off_k = 2 * q;           // two slots of [hi | lo]
   static constexpr int off_v = off_k + 4 * kt;  // two slots of [hi | lo]
-  static constexpr int off_ph = off_v + 4 * vt, off_pl = off_ph + p;
-  static constexpr int off_bar = off_pl + p;
+  static constexpr int off_xl = off_v + 4 * vt;  // [2][128] floats: the halves' row sums
+  static constexpr int off_bar = off_xl + 2 * kPM * 4;
   static constexpr int smem = off_bar + 256 + 1024;
   static constexpr int stage_stride = D + 4;    // epilogue fp32 rows (reuse Q and K slots), 16-byte rows
   static_assert(kPM * stage_stride * 4 <= off_v, "epilogue staging must fit below the V slots");
   static constexpr uint32_t idesc_qk = tc::idesc_f16_f32(kPM, kPN);        // Q_lo . K_hi
   static constexpr uint32_t idesc_qk2 = tc::idesc_f16_f32(kPM, 2 * kPN);   // Q_hi . [K_hi; K_lo]
-  static constexpr uint32_t idesc_pv = tc::idesc_f16_f32(kPM, D);         // P_lo . V_hi
-  static constexpr uint32_t idesc_pv2 = tc::idesc_f16_f32(kPM, 2 * D);     // P_hi . [V_hi; V_lo]
-  // TMEM: two score buffers of 128 columns ([hi.hi + lo.hi | hi.lo] of 64 keys) and
-  // O as [hi.hi + lo.hi | hi.lo] over 2 * D columns from 256 (summed in the epilogue)
+  static constexpr uint32_t idesc_pv = tc::idesc_f16_f32(kPM, D);
+  // TMEM: two score buffers of 128 columns ([hi.hi + lo.hi | hi.lo] of 64 keys) at 0
+  // and 128; two P buffers of 64 columns (P_hi: 32 columns of fp16 pairs, then P_lo)
+  // at 256 and 320, the A operand of P V; O over D columns at 384
   static constexpr uint32_t tmem_cols = 512;
   static constexpr uint32_t s_cols = 2 * kPN;
-  static constexpr uint32_t o_col = 256;
-  static_assert(o_col + 2 * D <= tmem_cols, "TMEM columns");
+  static constexpr uint32_t p_col = 256;
+  static constexpr uint32_t o_col = 384;
+  static_assert(o_col + D <= tmem_cols, "TMEM columns");
 };
 static_assert(PL<128>::smem <= 232448, "prefill shared memory over the per-CTA limit");
 
@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(kStageThreads) stage_kernel(SParams p) {
 // ---------------------------------------------------------------------------
 struct Sync {
   uint64_t kfull[2], kempty[2], vfull[2], vempty[2], sfull[2], sfree[2];
-  uint64_t pfull, odone, qready, fin[2];
+  uint64_t pfull, odone[2], qready, fin[2];
   uint32_t tmem;
   int abort;
 };
@@ -285,7 +285,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
       mbar_init(&sy->sfull[i], 1); mbar_init(&sy->sfree[i], kSoftmax);
     }
     mbar_init(&sy->pfull, kSoftmax);
-    mbar_init(&sy->odone, 1);
+    mbar_init(&sy->odone[0], 1);
+    mbar_init(&sy->odone[1], 1);
     mbar_init(&sy->qready, kSoftmax);
     mbar_init(&sy->fin[0], 1);
     mbar_init(&sy->fin[1], 1);
@@ -358,7 +359,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
   if (warp == kSoftmax / 32 + 2) {
     // ---- O += P_j V_j issue (one thread; runs beside the S issue) ------------
     if (lane == 0 && nkv > 0) {
-      const uint64_t dph = tc::sdesc_sw128(sb + L::off_ph), dpl = tc::sdesc_sw128(sb + L::off_pl);
       const uint64_t dv = tc::sdesc_sw128(sb + L::off_v);
       bool ok = true;
       for (int j = 0; ok && j < nkv; ++j) {
@@ -366,15 +366,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
              role_wait(&sy->vfull[j & 1], (j >> 1) & 1, sy, p.status);
         if (!ok) break;
         tc::fence_after_sync();
-        // V^T hi rows then lo rows are contiguous: one N = 2D operand holds both
-        const uint64_t vh = dv + (((j & 1) * 2 * L::vt) >> 4);
+        const uint64_t vh = dv + (((j & 1) * 2 * L::vt) >> 4), vl = vh + (L::vt >> 4);
+        const uint32_t ph = tmem + L::p_col + (j & 1) * kPN, pl = ph + kPN / 2;
 #pragma unroll
         for (int ks = 0; ks < kPN / 16; ++ks) {
           const uint32_t o = (ks * 32) >> 4;
-          tc::mma_f16(tmem + L::o_col, dph + o, vh + o, L::idesc_pv2, (j > 0 || ks > 0) ? 1u : 0u);
-          tc::mma_f16(tmem + L::o_col, dpl + o, vh + o, L::idesc_pv, 1u);
+          tc::mma_f16_ts(tmem + L::o_col, ph + ks * 8, vh + o, L::idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
+          tc::mma_f16_ts(tmem + L::o_col, ph + ks * 8, vl + o, L::idesc_pv, 1u);
+          tc::mma_f16_ts(tmem + L::o_col, pl + ks * 8, vh + o, L::idesc_pv, 1u);
         }
-        tc::commit(&sy->odone);
+        tc::commit(&sy->odone[j & 1]);
         tc::commit(&sy->vempty[j & 1]);
       }
       tc::commit(&sy->fin[1]);
@@ -494,34 +495,33 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
       split2(e0, e1, ph[c / 2], pl[c / 2]);
     }
     l += ls[0] + ls[1];
-    // PV_{j-1} must be complete: O is stable and the P buffer is free
-    if (j > 0) {
-      ok = __all_sync(0xffffffffu, role_wait(&sy->odone, (j - 1) & 1, sy, p.status));
+    // A rescale needs O stable (PV_{j-1} complete); otherwise only this P buffer's
+    // previous reader (PV_{j-2}) must be complete.  One barrier per P buffer, so a
+    // wait is never more than one phase behind.
+    const bool resc = j > 0 && __any_sync(0xffffffffu, move);  // TMEM access is warp-collective
+    if (resc) {
+      ok = __all_sync(0xffffffffu, role_wait(&sy->odone[(j - 1) & 1], ((j - 1) >> 1) & 1, sy, p.status));
       if (!ok) break;
       tc::fence_after_sync();
-      if (__any_sync(0xffffffffu, move)) {  // TMEM access is warp-collective
 #pragma unroll
-        for (int c = 0; c < D; c += 16) {  // this half's D columns of [O_a | O_b]
-          float t16[16];
-          const uint32_t col = L::o_col + h * D + c;
-          tc::ld_x16(lane_taddr + col, t16);
-          tc::wait_ld();
+      for (int c = 0; c < HD; c += 16) {
+        float t16[16];
+        tc::ld_x16(lane_taddr + L::o_col + h * HD + c, t16);
+        tc::wait_ld();
 #pragma unroll
-          for (int e = 0; e < 16; ++e) t16[e] *= alpha;
-          tc::st_x16(lane_taddr + col, t16);
-        }
-        tc::wait_st();
+        for (int e = 0; e < 16; ++e) t16[e] *= alpha;
+        tc::st_x16(lane_taddr + L::o_col + h * HD + c, t16);
       }
+    } else if (j > 1) {
+      ok = __all_sync(0xffffffffu, role_wait(&sy->odone[j & 1], ((j >> 1) - 1) & 1, sy, p.status));
+      if (!ok) break;
+      tc::fence_after_sync();
     }
-#pragma unroll
-    for (int c8 = 0; c8 < HN / 8; ++c8) {
-      const uint32_t off = tc::sw128_chunk(row, h * (HN / 8) + c8);
-      *reinterpret_cast<uint4*>(sm + L::off_ph + off) =
-          make_uint4(ph[4 * c8], ph[4 * c8 + 1], ph[4 * c8 + 2], ph[4 * c8 + 3]);
-      *reinterpret_cast<uint4*>(sm + L::off_pl + off) =
-          make_uint4(pl[4 * c8], pl[4 * c8 + 1], pl[4 * c8 + 2], pl[4 * c8 + 3]);
-    }
-    fence_proxy_async_smem();
+    // P_j -> TMEM buffer j & 1: this half's 32 keys = 16 columns of fp16 pairs, hi then lo
+    const uint32_t pb = lane_taddr + L::p_col + s * kPN + h * (HN / 2);
+    tc::st_x16(pb, *reinterpret_cast<float(*)[16]>(&ph[0]));
+    tc::st_x16(pb + kPN / 2, *reinterpret_cast<float(*)[16]>(&pl[0]));
+    tc::wait_st();
     tc::fence_before_sync();
     mbar_arrive(&sy->pfull);
   }
@@ -531,7 +531,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
   tc::fence_after_sync();
 
   // ---- epilogue: l of both halves, O / l -> staging -> inverse rotation -----
-  float* xl = reinterpret_cast<float*>(sm + L::off_ph);  // [2][128]; the P tile is free now
+  float* xl = reinterpret_cast<float*>(sm + L::off_xl);
   xl[h * kPM + row] = l;
   named_sync(1, kSoftmax);
   const float lt = l + xl[(1 - h) * kPM + row];
@@ -543,12 +543,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
     for (int c = 0; c < HD; c += 16) {
       float t16[16];
       if (ld) {
-        float u16[16];
         tc::ld_x16(lane_taddr + L::o_col + h * HD + c, t16);
-        tc::ld_x16(lane_taddr + L::o_col + D + h * HD + c, u16);
         tc::wait_ld();
-#pragma unroll
-        for (int e = 0; e < 16; ++e) t16[e] += u16[e];
       } else {
 #pragma unroll
         for (int e = 0; e < 16; ++e) t16[e] = 0.0f;
