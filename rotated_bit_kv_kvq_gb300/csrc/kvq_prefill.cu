@@ -235,7 +235,10 @@ __global__ void __launch_bounds__(kStageThreads) stage_kernel(SParams p) {
 // ---------------------------------------------------------------------------
 struct Sync {
   uint64_t kfull[2], kempty[2], vfull[2], vempty[2], sfull[2], sfree[2];
-  uint64_t pfull, odone[2], qready, fin[2];
+  // One barrier per P buffer for P-ready and PV-done: the softmax may finish P_{j+1}
+  // before the PV issuer has observed P_j, and a single barrier would then pass two
+  // phases under the waiter (same parity: the wait would never see its phase end).
+  uint64_t pfull[2], odone[2], qready, fin[2];
   uint32_t tmem;
   int abort;
 };
@@ -284,7 +287,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
       mbar_init(&sy->vfull[i], 1); mbar_init(&sy->vempty[i], 1);
       mbar_init(&sy->sfull[i], 1); mbar_init(&sy->sfree[i], kSoftmax);
     }
-    mbar_init(&sy->pfull, kSoftmax);
+    mbar_init(&sy->pfull[0], kSoftmax);
+    mbar_init(&sy->pfull[1], kSoftmax);
     mbar_init(&sy->odone[0], 1);
     mbar_init(&sy->odone[1], 1);
     mbar_init(&sy->qready, kSoftmax);
@@ -362,7 +366,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
       const uint64_t dv = tc::sdesc_sw128(sb + L::off_v);
       bool ok = true;
       for (int j = 0; ok && j < nkv; ++j) {
-        ok = role_wait(&sy->pfull, j & 1, sy, p.status) &&
+        ok = role_wait(&sy->pfull[j & 1], (j >> 1) & 1, sy, p.status) &&
              role_wait(&sy->vfull[j & 1], (j >> 1) & 1, sy, p.status);
         if (!ok) break;
         tc::fence_after_sync();
@@ -523,7 +527,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
     tc::st_x16(pb + kPN / 2, *reinterpret_cast<float(*)[16]>(&pl[0]));
     tc::wait_st();
     tc::fence_before_sync();
-    mbar_arrive(&sy->pfull);
+    mbar_arrive(&sy->pfull[s]);
   }
   // every MMA of the CTA has completed once both `fin` barriers arrive (also on the abort path)
   if (nkv > 0 && !(mbar_wait_bounded(&sy->fin[0], 0, kPWait) && mbar_wait_bounded(&sy->fin[1], 0, kPWait))) ok = false;
