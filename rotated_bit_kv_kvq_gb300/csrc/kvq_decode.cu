@@ -39,7 +39,8 @@ constexpr int kMaxHeads = 8;                 // query heads per CTA (mma N)
 constexpr long long kWaitCycles = 1000000000LL;  // ~0.5 s at 2 GHz; a TMA tile lands in microseconds
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kTailChunkMax = 4096;  // tail slots per CTA
-constexpr int kSmemBudget = 104 * 1024;      // stages; leaves room for 2 CTAs per SM
+constexpr int kSmemBudget = 64 * 1024;       // stages; leaves room for 3 CTAs per SM
+constexpr int kCtasPerSm = 3;
 
 constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 // widest TMA swizzle box (128, 64 or 32 bytes) that tiles a row exactly
@@ -110,7 +111,7 @@ __device__ __forceinline__ uint32_t khb(uint32_t h, int which) {
 }
 
 template <int D, int KT, int VT>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
 decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const __grid_constant__ CUtensorMap tmKt, const __grid_constant__ CUtensorMap tmVt) {
   using C = Cfg<D, KT, VT>;
@@ -232,25 +233,35 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     }
   }
   __syncthreads();
-  // B fragments: k-step (blk, half) covers channels 32*blk + 16*half + 4*tig + {0,2 | 1,3}
-  uint32_t qf[NB][2][2][2];  // [blk][half][hi/lo][b0b1, b2b3]
+  // B fragments: k-step (blk, half) covers channels 32*blk + 16*half + 4*tig + {0,2 | 1,3}.
+  // They are the same in every warp: warp 0 builds them once and leaves them in
+  // shared memory over the q staging ([blk][half][lane] x {hi b0b1, hi b2b3, lo b0b1,
+  // lo b2b3}, 32*D bytes = the staging's size), so no warp holds them in registers.
+  const uint4* qfs = reinterpret_cast<const uint4*>(sq);
+  if (warp == 0) {
+    uint4 qf[NB][2];
 #pragma unroll
-  for (int blk = 0; blk < NB; ++blk)
+    for (int blk = 0; blk < NB; ++blk)
 #pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      const float4 q4 = *reinterpret_cast<const float4*>(sq + g * D + 32 * blk + 16 * hf + 4 * tig);
-      const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
-      float hi[4], lo[4];
+      for (int hf = 0; hf < 2; ++hf) {
+        const float4 q4 = *reinterpret_cast<const float4*>(sq + g * D + 32 * blk + 16 * hf + 4 * tig);
+        const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
+        float hi[4], lo[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        hi[j] = __half2float(__float2half_rn(qv[j]));
-        lo[j] = qv[j] - hi[j];
+        for (int j = 0; j < 4; ++j) {
+          hi[j] = __half2float(__float2half_rn(qv[j]));
+          lo[j] = qv[j] - hi[j];
+        }
+        qf[blk][hf] = make_uint4(pack_h2(hi[0], hi[2]), pack_h2(hi[1], hi[3]), pack_h2(lo[0], lo[2]),
+                                 pack_h2(lo[1], lo[3]));
       }
-      qf[blk][hf][0][0] = pack_h2(hi[0], hi[2]);
-      qf[blk][hf][0][1] = pack_h2(hi[1], hi[3]);
-      qf[blk][hf][1][0] = pack_h2(lo[0], lo[2]);
-      qf[blk][hf][1][1] = pack_h2(lo[1], lo[3]);
-    }
+    __syncwarp();
+#pragma unroll
+    for (int blk = 0; blk < NB; ++blk)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) reinterpret_cast<uint4*>(sq)[(blk * 2 + hf) * 32 + lane] = qf[blk][hf];
+  }
+  __syncthreads();
 
   // ---- main loop ------------------------------------------------------------
   float acc[NB][2][4];
@@ -275,15 +286,7 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     float S[4] = {0.f, 0.f, 0.f, 0.f};
     if (!is_tail) {
       // ------------------------------- body: scores
-      float dkg[NB], dkg8[NB];
-      {
-        const __half* kd = reinterpret_cast<const __half*>(st + C::off_kd);
-#pragma unroll
-        for (int blk = 0; blk < NB; ++blk) {
-          dkg[blk] = __half2float(kd[g * NB + blk]);
-          dkg8[blk] = __half2float(kd[(g + 8) * NB + blk]);
-        }
-      }
+      const __half* kd = reinterpret_cast<const __half*>(st + C::off_kd);
       const uint32_t kbase = smem_u32(st + C::off_kqs);
       const int mi = lane >> 3, rr = (lane & 7) + 8 * (mi & 1);
       if constexpr (KT == KVQ_TYPE_Q8_0) {
@@ -294,13 +297,15 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
           r0 ^= 0x80808080u; r1 ^= 0x80808080u; r2 ^= 0x80808080u; r3 ^= 0x80808080u;
           const uint32_t alo[4] = {i8_pair<0, 2>(r0), i8_pair<0, 2>(r1), i8_pair<1, 3>(r0), i8_pair<1, 3>(r1)};
           const uint32_t ahi[4] = {i8_pair<0, 2>(r2), i8_pair<0, 2>(r3), i8_pair<1, 3>(r2), i8_pair<1, 3>(r3)};
+          const uint4 qa = qfs[(blk * 2) * 32 + lane], qb = qfs[(blk * 2 + 1) * 32 + lane];
           float cc[4] = {0.f, 0.f, 0.f, 0.f};
-          mma16816(cc, alo, qf[blk][0][0][0], qf[blk][0][0][1]);
-          mma16816(cc, alo, qf[blk][0][1][0], qf[blk][0][1][1]);
-          mma16816(cc, ahi, qf[blk][1][0][0], qf[blk][1][0][1]);
-          mma16816(cc, ahi, qf[blk][1][1][0], qf[blk][1][1][1]);
-          S[0] += dkg[blk] * cc[0]; S[1] += dkg[blk] * cc[1];
-          S[2] += dkg8[blk] * cc[2]; S[3] += dkg8[blk] * cc[3];
+          mma16816(cc, alo, qa.x, qa.y);
+          mma16816(cc, alo, qa.z, qa.w);
+          mma16816(cc, ahi, qb.x, qb.y);
+          mma16816(cc, ahi, qb.z, qb.w);
+          const float dk0 = __half2float(kd[g * NB + blk]), dk8 = __half2float(kd[(g + 8) * NB + blk]);
+          S[0] += dk0 * cc[0]; S[1] += dk0 * cc[1];
+          S[2] += dk8 * cc[2]; S[3] += dk8 * cc[3];
         }
       } else {
         constexpr uint32_t OFF = KT == KVQ_TYPE_Q5_0 ? 0x64106410u : 0x64086408u;
@@ -324,13 +329,15 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
                                      nib_pair(ra, 8, m01, OFF), nib_pair(rb, 8, m11, OFF)};
             const uint32_t ahi[4] = {nib_pair(ra, 4, m02, OFF), nib_pair(rb, 4, m12, OFF),
                                      nib_pair(ra, 12, m03, OFF), nib_pair(rb, 12, m13, OFF)};
+            const uint4 qa = qfs[(blk * 2) * 32 + lane], qb = qfs[(blk * 2 + 1) * 32 + lane];
             float cc[4] = {0.f, 0.f, 0.f, 0.f};
-            mma16816(cc, alo, qf[blk][0][0][0], qf[blk][0][0][1]);
-            mma16816(cc, alo, qf[blk][0][1][0], qf[blk][0][1][1]);
-            mma16816(cc, ahi, qf[blk][1][0][0], qf[blk][1][0][1]);
-            mma16816(cc, ahi, qf[blk][1][1][0], qf[blk][1][1][1]);
-            S[0] += dkg[blk] * cc[0]; S[1] += dkg[blk] * cc[1];
-            S[2] += dkg8[blk] * cc[2]; S[3] += dkg8[blk] * cc[3];
+            mma16816(cc, alo, qa.x, qa.y);
+            mma16816(cc, alo, qa.z, qa.w);
+            mma16816(cc, ahi, qb.x, qb.y);
+            mma16816(cc, ahi, qb.z, qb.w);
+            const float dk0 = __half2float(kd[g * NB + blk]), dk8 = __half2float(kd[(g + 8) * NB + blk]);
+            S[0] += dk0 * cc[0]; S[1] += dk0 * cc[1];
+            S[2] += dk8 * cc[2]; S[3] += dk8 * cc[3];
           }
         }
       }
@@ -350,8 +357,9 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
                                  C::TT == 16 ? bf16x2_to_h2_scaled(__byte_perm(kb.x, kb.y, 0x5410)) : 0u,
                                  bf16x2_to_h2_scaled(__byte_perm(ka.x, ka.y, 0x7632)),
                                  C::TT == 16 ? bf16x2_to_h2_scaled(__byte_perm(kb.x, kb.y, 0x7632)) : 0u};
-          mma16816(cc, a, qf[blk][hf][0][0], qf[blk][hf][0][1]);
-          mma16816(cc, a, qf[blk][hf][1][0], qf[blk][hf][1][1]);
+          const uint4 qa = qfs[(blk * 2 + hf) * 32 + lane];
+          mma16816(cc, a, qa.x, qa.y);
+          mma16816(cc, a, qa.z, qa.w);
         }
 #pragma unroll
       for (int r = 0; r < 4; ++r) S[r] = 256.0f * cc[r];
@@ -401,24 +409,22 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     const bool vt0 = tt < t_end, vt1 = tt + 1 < t_end;
     const bool vt8 = TR == 16 && tt + 8 < t_end, vt9 = TR == 16 && tt + 9 < t_end;
     if (!is_tail) {
-      float dvt[4][NB];  // V scales of the transposed tokens (0 for rows past the end)
-      {
-        const __half* vd = reinterpret_cast<const __half*>(st + C::off_vd);
-        const int rows[4] = {2 * tig, 2 * tig + 1, 2 * tig + 8, 2 * tig + 9};
-        const bool ok[4] = {vt0, vt1, vt8, vt9};
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int blk = 0; blk < NB; ++blk) dvt[i][blk] = ok[i] ? __half2float(vd[rows[i] * NB + blk]) : 0.0f;
-      }
+      // V scales of the transposed tokens, read per block (0 for rows past the end)
+      const __half* vd = reinterpret_cast<const __half*>(st + C::off_vd);
+      const float pz[4] = {vt0 ? pt[0] : 0.0f, vt1 ? pt[1] : 0.0f, vt8 ? pt[2] : 0.0f, vt9 ? pt[3] : 0.0f};
+      auto pscaled = [&](int blk, uint32_t& bh0, uint32_t& bl0, uint32_t& bh1, uint32_t& bl1) {
+        split_h2(pz[0] * __half2float(vd[(2 * tig) * NB + blk]), pz[1] * __half2float(vd[(2 * tig + 1) * NB + blk]),
+                 bh0, bl0);
+        split_h2(pz[2] * __half2float(vd[(2 * tig + 8) * NB + blk]),
+                 pz[3] * __half2float(vd[(2 * tig + 9) * NB + blk]), bh1, bl1);
+      };
       const uint32_t vbase = smem_u32(st + C::off_vqs);
       const int mi = lane >> 3, rr = (lane & 7) + 8 * (mi & 1);
       if constexpr (VT == KVQ_TYPE_Q8_0) {
 #pragma unroll
         for (int blk = 0; blk < NB; ++blk) {
           uint32_t bh0, bl0, bh1, bl1;
-          split_h2(pt[0] * dvt[0][blk], pt[1] * dvt[1][blk], bh0, bl0);
-          split_h2(pt[2] * dvt[2][blk], pt[3] * dvt[3][blk], bh1, bl1);
+          pscaled(blk, bh0, bl0, bh1, bl1);
           uint32_t r0, r1, r2, r3;
           ldsm_x4_t(vbase + swz_off<C::WV>(rr, 32 * blk + 16 * (mi >> 1), 16), r0, r1, r2, r3);
           r0 ^= 0x80808080u; r1 ^= 0x80808080u; r2 ^= 0x80808080u; r3 ^= 0x80808080u;
@@ -439,8 +445,7 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
           for (int e = 0; e < 2; ++e) {
             const int blk = bp + e;
             uint32_t bh0, bl0, bh1, bl1;
-            split_h2(pt[0] * dvt[0][blk], pt[1] * dvt[1][blk], bh0, bl0);
-            split_h2(pt[2] * dvt[2][blk], pt[3] * dvt[3][blk], bh1, bl1);
+            pscaled(blk, bh0, bl0, bh1, bl1);
             const uint32_t ra = rr4[2 * e], rb = rr4[2 * e + 1];  // tokens 0-7, 8-15
             uint32_t ma0 = 0x64006400u, ma1 = 0x64006400u, ma2 = 0x64006400u, ma3 = 0x64006400u;
             uint32_t mb0 = 0x64006400u, mb1 = 0x64006400u, mb2 = 0x64006400u, mb3 = 0x64006400u;
@@ -768,8 +773,8 @@ DecodePlan plan_decode(const kvq_cache& c, int n_q_heads, int sm_count) {
   pl.tail_chunk = c.tail_len > 0 ? (c.tail_len < kTailChunkMax ? (c.tail_len + 63) / 64 * 64 : kTailChunkMax) : 64;
   pl.splits_tail = c.tail_len > 0 ? (c.tail_len + pl.tail_chunk - 1) / pl.tail_chunk : 0;
   // body: size the chunks so that all CTAs of a full cache fit in one wave of
-  // two CTAs per SM (shorter sequences leave their last splits empty)
-  const long long slots = 2LL * (sm_count > 0 ? sm_count : 148);
+  // kCtasPerSm CTAs per SM (shorter sequences leave their last splits empty)
+  const long long slots = (long long)kCtasPerSm * (sm_count > 0 ? sm_count : 148);
   long long per_pair = slots / pairs - pl.splits_tail;
   if (per_pair < 1) per_pair = 1;
   int chunk = int(((c.max_ctx + per_pair - 1) / per_pair + 63) / 64 * 64);
