@@ -570,73 +570,85 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
 }
 
 // ---------------------------------------------------------------------------
-// Split merge + inverse rotation: one CTA of 8 warps per (sequence, query
-// head); warp w merges splits w, w+8, ... and warp 0 combines the 8 results.
+// Split merge + inverse rotation: one CTA of 256 threads per (sequence, query
+// head).  The split weights 2^(m_s - M) go to shared memory; then every thread
+// owns channels (D <= 256: a group of 256 / D threads shares a channel and takes
+// every (256/D)-th split), so all partial loads of a row are independent and
+// coalesced; warp 0 rotates the merged row back.
 // ---------------------------------------------------------------------------
-constexpr int kCombineWarps = 8;
+constexpr int kCombineThreads = 256;
 
 template <int D>
-__global__ void __launch_bounds__(kCombineWarps * 32)
+__global__ void __launch_bounds__(kCombineThreads)
 decode_combine_kernel(const float* __restrict__ ws_acc, const float* __restrict__ ws_ml, int splits,
                       int rot_v, void* __restrict__ out, int out_dtype) {
   constexpr int G = (D >= 64 && D % 64 == 0) ? (((D & (D - 1)) == 0) ? D : 64) : 32;
   constexpr int E = D / 32;
-  __shared__ float s_acc[kCombineWarps][D];
-  __shared__ float s_m[kCombineWarps], s_l[kCombineWarps];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int TPC = kCombineThreads / D >= 1 ? kCombineThreads / D : 1;  // threads per channel
+  extern __shared__ float s_w[];                 // [splits] weights
+  __shared__ float s_part[kCombineThreads];      // per-thread partial sums, then the merged row
+  __shared__ float s_red[2][kCombineThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int row = blockIdx.x;  // b * Hq + h
   const float* ml = ws_ml + (size_t)row * splits * 2;
+  // 1. M = max over non-empty splits
   float M = -INFINITY;
-  for (int s = warp; s < splits; s += kCombineWarps)
+  for (int s = tid; s < splits; s += kCombineThreads)
     if (ml[2 * s + 1] > 0.0f) M = fmaxf(M, ml[2 * s]);
-  float v[E];
 #pragma unroll
-  for (int j = 0; j < E; ++j) v[j] = 0.0f;
-  float L = 0.0f;
-  for (int s = warp; s < splits; s += kCombineWarps) {
-    const float l = ml[2 * s + 1];
-    if (!(l > 0.0f)) continue;
-    const float f = exp2f(ml[2 * s] - M);
-    L += l * f;
-    const float* a = ws_acc + ((size_t)row * splits + s) * D;
-#pragma unroll
-    for (int j = 0; j < E; ++j) v[j] += f * a[fwht_channel<D, G>(lane, j)];
-  }
-#pragma unroll
-  for (int j = 0; j < E; ++j) s_acc[warp][fwht_channel<D, G>(lane, j)] = v[j];
-  if (lane == 0) { s_m[warp] = M; s_l[warp] = L; }
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (lane == 0) s_red[0][warp] = M;
   __syncthreads();
-  if (warp != 0) return;
-  float Mt = -INFINITY;
+  M = s_red[0][0];
 #pragma unroll
-  for (int w = 0; w < kCombineWarps; ++w) Mt = fmaxf(Mt, s_m[w]);
-  float f[kCombineWarps];
-  float Lt = 0.0f;
-#pragma unroll
-  for (int w = 0; w < kCombineWarps; ++w) {
-    f[w] = s_m[w] == -INFINITY ? 0.0f : exp2f(s_m[w] - Mt);
-    Lt += s_l[w] * f[w];
+  for (int w = 1; w < kCombineThreads / 32; ++w) M = fmaxf(M, s_red[0][w]);
+  // 2. weights and L = sum of l_s * weight
+  float L = 0.0f;
+  for (int s = tid; s < splits; s += kCombineThreads) {
+    const float l = ml[2 * s + 1];
+    const float w = l > 0.0f ? exp2f(ml[2 * s] - M) : 0.0f;
+    s_w[s] = w;
+    L += l * w;
   }
-  const float inv = Lt > 0.0f ? 1.0f / Lt : 0.0f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+  if (lane == 0) s_red[1][warp] = L;
+  __syncthreads();
+  L = 0.0f;
+#pragma unroll
+  for (int w = 0; w < kCombineThreads / 32; ++w) L += s_red[1][w];
+  // 3. channel c of this thread, splits sub, sub + TPC, ...
+  const int c = tid % D, sub = tid / D;
+  float v = 0.0f;
+  if (tid < D * TPC) {
+    const float* a = ws_acc + (size_t)row * splits * D + c;
+    for (int s = sub; s < splits; s += TPC) v += s_w[s] * a[(size_t)s * D];
+  }
+  s_part[tid] = v;
+  __syncthreads();
+  // 4. warp 0: merged row / L, inverse rotation, store
+  if (warp != 0) return;
+  const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+  float x[E];
 #pragma unroll
   for (int j = 0; j < E; ++j) {
-    const int c = fwht_channel<D, G>(lane, j);
+    const int ch = fwht_channel<D, G>(lane, j);
     float t = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kCombineWarps; ++w) t += f[w] * s_acc[w][c];
-    v[j] = t * inv;
+    for (int u = 0; u < TPC; ++u) t += s_part[u * D + ch];
+    x[j] = t * inv;
   }
   if (rot_v) {
-    warp_fwht<D, G>(v, lane);
+    warp_fwht<D, G>(x, lane);
 #pragma unroll
-    for (int j = 0; j < E; ++j) v[j] *= inv_sqrt_group<G>();
+    for (int j = 0; j < E; ++j) x[j] *= inv_sqrt_group<G>();
   }
 #pragma unroll
   for (int j = 0; j < E; ++j) {
     const size_t e = (size_t)row * D + fwht_channel<D, G>(lane, j);
-    if (out_dtype == KVQ_F32) static_cast<float*>(out)[e] = v[j];
-    else if (out_dtype == KVQ_BF16) static_cast<__nv_bfloat16*>(out)[e] = __float2bfloat16_rn(v[j]);
-    else static_cast<__half*>(out)[e] = __float2half_rn(v[j]);
+    if (out_dtype == KVQ_F32) static_cast<float*>(out)[e] = x[j];
+    else if (out_dtype == KVQ_BF16) static_cast<__nv_bfloat16*>(out)[e] = __float2bfloat16_rn(x[j]);
+    else static_cast<__half*>(out)[e] = __float2half_rn(x[j]);
   }
 }
 
@@ -713,7 +725,12 @@ cudaError_t run_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, cons
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int total = c.batch * n_q_heads;
-  decode_combine_kernel<D><<<total, kCombineWarps * 32, 0, st>>>(p.ws_acc, p.ws_ml, plan.splits, rot.v, out, out_dtype);
+  const size_t wbytes = (size_t)plan.splits * sizeof(float);
+  if (wbytes > 48 * 1024) {
+    e = cudaFuncSetAttribute(decode_combine_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wbytes);
+    if (e != cudaSuccess) return e;
+  }
+  decode_combine_kernel<D><<<total, kCombineThreads, wbytes, st>>>(p.ws_acc, p.ws_ml, plan.splits, rot.v, out, out_dtype);
   return cudaGetLastError();
 }
 
