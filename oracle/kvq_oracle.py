@@ -22,6 +22,12 @@ Sources (pages are cited by title and section):
   codes round-half-away-from-zero; q5_0 / q4_0 scale = (signed value of
   largest magnitude) / -16 or -8, codes = trunc(x/scale + 16.5 or 8.5)
   clamped to 31 or 15.
+* q4_1 / q5_1 (scale + minimum), which [P2] benchmarks beside them (its
+  tables of K/V type pairs, e.g. q5_0-q4_1 and q8_0-q5_1, section "섹션별
+  상세"): 32 values, fp16 scale d = (max - min) / 15 or 31 and fp16 minimum;
+  codes = min(top, trunc((x - min) / d + 0.5)); value = code * d + min.  The
+  pages name these types without restating them; the reading is the GGUF
+  definition of the same names, as for the _0 types.
 
 Precision: rotation and attention in float64; quantizer arithmetic in IEEE
 float32 exactly as the block definition states (one rounding per operation,
@@ -46,10 +52,13 @@ QK = 32  # values per quantization block
 TYPE_Q4_0 = "q4_0"
 TYPE_Q5_0 = "q5_0"
 TYPE_Q8_0 = "q8_0"
-TYPES = (TYPE_Q4_0, TYPE_Q5_0, TYPE_Q8_0)
+TYPE_Q4_1 = "q4_1"
+TYPE_Q5_1 = "q5_1"
+TYPES = (TYPE_Q4_0, TYPE_Q5_0, TYPE_Q8_0, TYPE_Q4_1, TYPE_Q5_1)
+MIN_TYPES = (TYPE_Q4_1, TYPE_Q5_1)   # scale + minimum per block
 
-# bytes of one block in the GGUF array-of-structs layout: scale + payload
-GGML_BLOCK_BYTES = {TYPE_Q4_0: 18, TYPE_Q5_0: 22, TYPE_Q8_0: 34}
+# bytes of one block in the GGUF array-of-structs layout: scale (+ minimum) + payload
+GGML_BLOCK_BYTES = {TYPE_Q4_0: 18, TYPE_Q5_0: 22, TYPE_Q8_0: 34, TYPE_Q4_1: 20, TYPE_Q5_1: 24}
 
 
 # ---------------------------------------------------------------------------
@@ -229,15 +238,59 @@ def quantize_q5_0(y):
     return _quantize_offset(y, -16.0, 16.5, 31)
 
 
+def _quantize_min(y, top: int):
+    """Scale + minimum blocks: lo / hi = smallest / largest value (float32),
+    d = (hi - lo) / top, id = 1/d (0 when d == 0), code = min(top, trunc((x - lo)
+    * id + 0.5)) with one float32 rounding per operation.  Returns the scale word
+    (fp16 bits of d in bits 0-15, of lo in bits 16-31) and the codes."""
+    b = _blocks(y)
+    lo = np.min(b, axis=-1).astype(F32)
+    hi = np.max(b, axis=-1).astype(F32)
+    d = ((hi - lo) / F32(top)).astype(F32)
+    inv = _inverse(d)
+    v = (((b - lo[..., None]).astype(F32) * inv[..., None]).astype(F32) + F32(0.5)).astype(F32)
+    codes = np.minimum(top, np.trunc(v.astype(F64)))
+    assert np.all(codes >= 0)
+    word = f16_bits(d).astype(np.uint32) | (f16_bits(lo).astype(np.uint32) << np.uint32(16))
+    return word, codes.astype(np.uint8)
+
+
+def quantize_q4_1(y):
+    """q4_1: d = (max - min)/15, codes = min(15, trunc((x - min)*(1/d) + 0.5)).
+
+    Returns (scale word uint32 [..., nb]: fp16 d | fp16 min << 16, codes uint8 0..15)."""
+    return _quantize_min(y, 15)
+
+
+def quantize_q5_1(y):
+    """q5_1: d = (max - min)/31, codes = min(31, trunc((x - min)*(1/d) + 0.5))."""
+    return _quantize_min(y, 31)
+
+
 def quantize(qtype: str, y):
-    return {TYPE_Q4_0: quantize_q4_0, TYPE_Q5_0: quantize_q5_0,
-            TYPE_Q8_0: quantize_q8_0}[qtype](y)
+    return {TYPE_Q4_0: quantize_q4_0, TYPE_Q5_0: quantize_q5_0, TYPE_Q8_0: quantize_q8_0,
+            TYPE_Q4_1: quantize_q4_1, TYPE_Q5_1: quantize_q5_1}[qtype](y)
+
+
+def scale_and_min(qtype: str, d_bits):
+    """(fp16 scale, fp16 minimum) values of stored blocks, float64 (minimum 0 for the _0 types)."""
+    if qtype in MIN_TYPES:
+        w = np.asarray(d_bits, dtype=np.uint32)
+        return (f16_value((w & np.uint32(0xFFFF)).astype(np.uint16)),
+                f16_value((w >> np.uint32(16)).astype(np.uint16)))
+    dv = f16_value(d_bits)
+    return dv, np.zeros_like(dv)
 
 
 def dequantize(qtype: str, d_bits, codes) -> np.ndarray:
-    """code -> value with the stored fp16 scale, in float64, flattened back to head_dim."""
-    dv = f16_value(d_bits)[..., None]
+    """code -> value with the stored fp16 scale (and minimum), in float64,
+    flattened back to head_dim."""
     c = np.asarray(codes).astype(F64)
+    if qtype in MIN_TYPES:
+        dv, mv = scale_and_min(qtype, d_bits)
+        x = c * dv[..., None] + mv[..., None]
+        return x.reshape(x.shape[:-2] + (x.shape[-2] * QK,))
+    dv = f16_value(d_bits)[..., None]
     if qtype == TYPE_Q8_0:
         x = c * dv
     elif qtype == TYPE_Q4_0:
@@ -283,12 +336,17 @@ def unpack_q5_0(qs, qh) -> np.ndarray:
 
 def to_ggml_bytes(qtype: str, d_bits, codes) -> np.ndarray:
     """Array-of-structs GGUF byte image of blocks [..., nb]:
-    q4_0 = [d:2][qs:16], q5_0 = [d:2][qh:4 LE][qs:16], q8_0 = [d:2][qs:32]."""
-    d = np.asarray(d_bits, dtype=np.uint16)
-    dbytes = d[..., None].view(np.uint8).reshape(d.shape + (2,))
-    if qtype == TYPE_Q4_0:
+    q4_0 = [d:2][qs:16], q5_0 = [d:2][qh:4 LE][qs:16], q8_0 = [d:2][qs:32],
+    q4_1 = [d:2][min:2][qs:16], q5_1 = [d:2][min:2][qh:4 LE][qs:16]."""
+    if qtype in MIN_TYPES:
+        w = np.asarray(d_bits, dtype="<u4")
+        dbytes = w[..., None].view(np.uint8).reshape(w.shape + (4,))   # d then min, little-endian
+    else:
+        d = np.asarray(d_bits, dtype=np.uint16)
+        dbytes = d[..., None].view(np.uint8).reshape(d.shape + (2,))
+    if qtype in (TYPE_Q4_0, TYPE_Q4_1):
         parts = [dbytes, pack_q4_0(codes)]
-    elif qtype == TYPE_Q5_0:
+    elif qtype in (TYPE_Q5_0, TYPE_Q5_1):
         qs, qh = pack_q5_0(codes)
         qhb = qh.astype("<u4")[..., None].view(np.uint8).reshape(qh.shape + (4,))
         parts = [dbytes, qhb, qs]
@@ -327,7 +385,8 @@ class OracleCache:
         nb = head_dim // QK
         self.codes = {w: np.zeros((batch, n_kv_heads, max_ctx, nb, QK), np.uint8 if self.types[w] != TYPE_Q8_0 else np.int8)
                       for w in ("k", "v")}
-        self.dbits = {w: np.zeros((batch, n_kv_heads, max_ctx, nb), np.uint16) for w in ("k", "v")}
+        self.dbits = {w: np.zeros((batch, n_kv_heads, max_ctx, nb),
+                                  np.uint32 if self.types[w] in MIN_TYPES else np.uint16) for w in ("k", "v")}
         self.tail = {w: np.zeros((batch, n_kv_heads, max(tail_len, 1), head_dim), np.uint16)
                      for w in ("k", "v")}
         self.seq_len = np.zeros(batch, dtype=np.int64)

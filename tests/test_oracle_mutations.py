@@ -118,6 +118,36 @@ def _softmax_no_max_shift_scale(q, K, V, scale):
     return _orig["softmax_attention"](q, K, V, scale * 1.01)
 
 
+def _min_no_half(y, top=15):
+    """q4_1 without the +0.5 (codes truncated instead of rounded)."""
+    b = ko._blocks(y)
+    lo = np.min(b, axis=-1).astype(np.float32)
+    d = ((np.max(b, axis=-1) - lo) / np.float32(top)).astype(np.float32)
+    inv = ko._inverse(d)
+    v = ((b - lo[..., None]).astype(np.float32) * inv[..., None]).astype(np.float32)
+    codes = np.minimum(top, np.trunc(v.astype(np.float64)))
+    word = ko.f16_bits(d).astype(np.uint32) | (ko.f16_bits(lo).astype(np.uint32) << np.uint32(16))
+    return word, codes.astype(np.uint8)
+
+
+def _min_word_swapped(y):
+    """q5_1 with d and the minimum swapped in the scale word."""
+    word, codes = ko._quantize_min(y, 31)
+    return ((word >> np.uint32(16)) | (word << np.uint32(16))).astype(np.uint32), codes
+
+
+def _dequant_min_dropped(qtype, d_bits, codes):
+    """Scale + minimum blocks decoded without the minimum."""
+    if qtype in ko.MIN_TYPES:
+        dv, _ = ko.scale_and_min(qtype, d_bits)
+        x = np.asarray(codes).astype(np.float64) * dv[..., None]
+        return x.reshape(x.shape[:-2] + (x.shape[-2] * 32,))
+    return _ORIG_DEQUANT(qtype, d_bits, codes)
+
+
+_ORIG_DEQUANT = ko.dequantize
+
+
 MUTANTS = [
     ("fwht", _fwht_transposed_pairs, [pins.test_rotate_golden_vectors]),
     ("pack_q4_0", _pack_q4_swapped, [pins.test_packing_golden]),
@@ -132,6 +162,9 @@ MUTANTS = [
     ("pack_q5_0", _pack_q5_high_bits_reversed, [pins.test_packing_golden]),
     ("dequantize", _dequant_no_offset, [lambda: pins.test_quantizer_error_bounds("q4_0")]),
     ("softmax_attention", _softmax_no_max_shift_scale, [pins.test_decode_gqa_bruteforce]),
+    ("quantize_q4_1", _min_no_half, [pins.test_golden_blocks]),
+    ("quantize_q5_1", _min_word_swapped, [pins.test_golden_blocks]),
+    ("dequantize", _dequant_min_dropped, [lambda: pins.test_min_quantizer_error_bounds("q4_1")]),
 ]
 
 

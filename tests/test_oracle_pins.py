@@ -232,6 +232,75 @@ def test_all_zero_block(qtype, zero_bits, zero_code):
     assert np.all(ko.dequantize(qtype, dbits, codes) == 0)
 
 
+# ---- scale + minimum formats (q4_1 / q5_1)
+
+def _lo_d_exact(qtype, x):
+    """float32 lo and d = (hi - lo)/top before fp16 rounding, restated from the definition."""
+    xf = x.astype(np.float32)
+    lo = xf.min(axis=-1)
+    top = 15 if qtype == "q4_1" else 31
+    return lo.astype(np.float64), ((xf.max(axis=-1) - lo) / np.float32(top)).astype(np.float64), top
+
+
+@pytest.mark.parametrize("qtype", ["q4_1", "q5_1"])
+def test_min_quantizer_error_bounds(qtype):
+    """|x - (code*D + M)| <= d/2 + code*|d - D| + |lo - M| (+ ulps): every code is the
+    rounded position of x on the grid lo + k*d, and the grid fits the block exactly."""
+    rng = np.random.default_rng(17)
+    x = _random_blocks(rng, 4000)
+    word, codes = ko.quantize(qtype, x)
+    deq = ko.dequantize(qtype, word, codes).reshape(-1, 32)
+    lo, d, top = _lo_d_exact(qtype, x)
+    D, M = ko.scale_and_min(qtype, word)
+    c = codes.reshape(-1, 32).astype(np.float64)
+    assert c.max() <= top
+    slack = c * np.abs(d - D.reshape(-1))[:, None] + np.abs(lo - M.reshape(-1))[:, None] \
+        + (np.abs(d) * 1e-5 + np.abs(lo) * 1e-6)[:, None] + 1e-30
+    err = np.abs(x.astype(np.float64) - deq)
+    assert np.all(err <= (d / 2)[:, None] + slack)
+
+
+@pytest.mark.parametrize("qtype", ["q4_1", "q5_1"])
+def test_min_quantizer_extremes(qtype):
+    """The smallest value gets code 0 and the largest the top code (the grid spans the block)."""
+    rng = np.random.default_rng(18)
+    x = _random_blocks(rng, 2000)
+    word, codes = ko.quantize(qtype, x)
+    c = codes.reshape(-1, 32)
+    top = 15 if qtype == "q4_1" else 31
+    rows = np.arange(len(x))
+    assert np.all(c[rows, np.argmin(x, axis=-1)] == 0)
+    assert np.all(c[rows, np.argmax(x, axis=-1)] == top)
+
+
+@pytest.mark.parametrize("qtype", ["q4_1", "q5_1"])
+def test_min_codes_are_nearest_levels_bruteforce(qtype):
+    """Brute force over every code: the chosen one is a nearest grid level lo + k*d."""
+    rng = np.random.default_rng(19)
+    x = _random_blocks(rng, 600)
+    word, codes = ko.quantize(qtype, x)
+    codes = codes.reshape(-1, 32).astype(np.int64)
+    lo, d, top = _lo_d_exact(qtype, x)
+    levels = np.arange(top + 1)
+    for i in range(len(x)):
+        if d[i] == 0:
+            assert np.all(codes[i] == 0)
+            continue
+        for j in range(32):
+            dist = np.abs(x[i, j] - (lo[i] + levels * d[i]))
+            assert dist[codes[i, j]] <= dist.min() + abs(d[i]) * 1e-5, (qtype, i, j)
+
+
+@pytest.mark.parametrize("qtype", ["q4_1", "q5_1"])
+def test_min_constant_and_zero_blocks(qtype):
+    x = np.zeros((3, 64), np.float32)
+    x[1] = -2.5
+    word, codes = ko.quantize(qtype, x)
+    assert np.all(codes == 0)
+    assert np.all((word & 0xFFFF) == 0)
+    assert np.array_equal(ko.dequantize(qtype, word, codes), x.astype(np.float64))
+
+
 def test_signed_max_first_index_on_ties():
     x = np.zeros((3, 32), np.float32)
     x[0, [4, 9]] = [5, -5]
@@ -253,10 +322,12 @@ def test_packing_golden():
         qs, qh = ko.pack_q5_0(c)
         assert qs.tobytes().hex() == g[key]["qs_hex"]
         assert int(qh) == g[key]["qh"]
-    for key, qt in (("ggml_q4_0_block", "q4_0"), ("ggml_q5_0_block", "q5_0"), ("ggml_q8_0_block", "q8_0")):
+    for key, qt in (("ggml_q4_0_block", "q4_0"), ("ggml_q5_0_block", "q5_0"), ("ggml_q8_0_block", "q8_0"),
+                    ("ggml_q4_1_block", "q4_1"), ("ggml_q5_1_block", "q5_1")):
         e = g[key]
         codes = np.array(e["codes"], np.int64).astype(np.int8 if qt == "q8_0" else np.uint8)[None]
-        b = ko.to_ggml_bytes(qt, np.array([e["d_bits"]], np.uint16), codes)
+        word = np.uint32 if qt in ko.MIN_TYPES else np.uint16
+        b = ko.to_ggml_bytes(qt, np.array([e["d_bits"]], word), codes)
         assert b.tobytes().hex() == e["bytes_hex"], key
         assert b.shape[-1] == ko.GGML_BLOCK_BYTES[qt]
 
