@@ -239,13 +239,14 @@ def quantize_q5_0(y):
 
 
 def _quantize_min(y, top: int):
-    """Scale + minimum blocks: lo / hi = smallest / largest value (float32),
-    d = (hi - lo) / top, id = 1/d (0 when d == 0), code = min(top, trunc((x - lo)
-    * id + 0.5)) with one float32 rounding per operation.  Returns the scale word
-    (fp16 bits of d in bits 0-15, of lo in bits 16-31) and the codes."""
+    """Scale + minimum blocks: lo / hi = smallest / largest value (float32; the
+    first one in block order on ties, which only decides the sign of a zero
+    minimum), d = (hi - lo) / top, id = 1/d (0 when d == 0), code = min(top,
+    trunc((x - lo) * id + 0.5)) with one float32 rounding per operation.  Returns
+    the scale word (fp16 bits of d in bits 0-15, of lo in bits 16-31) and the codes."""
     b = _blocks(y)
-    lo = np.min(b, axis=-1).astype(F32)
-    hi = np.max(b, axis=-1).astype(F32)
+    lo = np.take_along_axis(b, np.argmin(b, axis=-1)[..., None], axis=-1)[..., 0].astype(F32)
+    hi = np.take_along_axis(b, np.argmax(b, axis=-1)[..., None], axis=-1)[..., 0].astype(F32)
     d = ((hi - lo) / F32(top)).astype(F32)
     inv = _inverse(d)
     v = (((b - lo[..., None]).astype(F32) * inv[..., None]).astype(F32) + F32(0.5)).astype(F32)
