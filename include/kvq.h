@@ -9,9 +9,12 @@
  * used when head_dim >= 64 and a multiple of 64, and K / V rotation can each
  * be switched off (same post, section 적용 및 배경 기술).  The rotated vectors
  * are stored in the GGUF q4_0 / q5_0 / q8_0 block formats, which the same
- * section says stay unchanged: 32 values per block with an fp16 scale.  A
- * BF16 "precision tail" keeps the most recent tokens unquantized (aitrends.kr
- * "KV 캐시 양자화 벤치마크: KVarN과 Precision Tail", section 용어 해설).
+ * section says stay unchanged: 32 values per block with an fp16 scale; the
+ * scale + minimum formats q4_1 / q5_1, which the aitrends.kr summary "KV 캐시
+ * 양자화 벤치마크: KVarN과 Precision Tail" (section 섹션별 상세) benchmarks in
+ * K/V type pairs beside them, are stored the same way.  A BF16 "precision
+ * tail" keeps the most recent tokens unquantized (same summary, section
+ * 용어 해설).
  *
  * Conventions for every entry point.
  *  - Ownership: the library never allocates, frees or synchronizes (except
@@ -60,7 +63,12 @@ typedef int32_t kvq_status;
 #define KVQ_TYPE_Q4_0 0   /* fp16 d = m/-8,  code = min(15, trunc(x/d + 8.5)),  x = (code-8)*d  */
 #define KVQ_TYPE_Q5_0 1   /* fp16 d = m/-16, code = min(31, trunc(x/d + 16.5)), x = (code-16)*d */
 #define KVQ_TYPE_Q8_0 2   /* fp16 d = amax/127, code = roundf(x/d) in [-127,127], x = code*d     */
-/* m = the value of largest magnitude in the 32-value block (first on ties). */
+#define KVQ_TYPE_Q4_1 3   /* fp16 d = (hi-lo)/15, fp16 lo, code = min(15, trunc((x-lo)/d + 0.5)), x = code*d + lo */
+#define KVQ_TYPE_Q5_1 4   /* fp16 d = (hi-lo)/31, fp16 lo, code = min(31, trunc((x-lo)/d + 0.5)), x = code*d + lo */
+/* m = the value of largest magnitude in the 32-value block (first on ties);
+ * lo / hi = its smallest / largest value (first on ties).  1/d is taken as 0
+ * when d == 0.  Nibble packing (q4_x, q5_x): byte k = code_k | code_{k+16} << 4;
+ * q5_x high bits: bit j of a 32-bit word = bit 4 of code_j. */
 
 /* ---- element types of q / k / v / out ----------------------------------- */
 #define KVQ_F32  0
@@ -79,9 +87,10 @@ typedef int32_t kvq_status;
 #define KVQ_INPUT_PREROTATED 1u  /* k / v are already rotated: store them as given */
 
 /* ---- planes of a cache (kvq_plane_bytes) --------------------------------- */
-#define KVQ_PLANE_K_QS    0  /* uint8 [batch][kv_heads][max_ctx][qs_row]    qs_row = d/2 (q4_0, q5_0) or d (q8_0) */
-#define KVQ_PLANE_K_QH    1  /* uint32 [batch][kv_heads][max_ctx][d/32]     q5_0 only (0 bytes otherwise)        */
-#define KVQ_PLANE_K_D     2  /* fp16 [batch][kv_heads][max_ctx][d/32]       block scales                         */
+#define KVQ_PLANE_K_QS    0  /* uint8 [batch][kv_heads][max_ctx][qs_row]    qs_row = d (q8_0) or d/2 (the others) */
+#define KVQ_PLANE_K_QH    1  /* uint32 [batch][kv_heads][max_ctx][d/32]     q5_0 / q5_1 only (0 bytes otherwise)  */
+#define KVQ_PLANE_K_D     2  /* fp16 [batch][kv_heads][max_ctx][d/32]       block scales; q4_1 / q5_1: fp16 pairs
+                                (d, lo) [..][d/32][2], i.e. the GGUF block header                                   */
 #define KVQ_PLANE_V_QS    3
 #define KVQ_PLANE_V_QH    4
 #define KVQ_PLANE_V_D     5

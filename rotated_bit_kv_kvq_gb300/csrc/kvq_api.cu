@@ -12,7 +12,9 @@
 namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-bool valid_type(int t) { return t == KVQ_TYPE_Q4_0 || t == KVQ_TYPE_Q5_0 || t == KVQ_TYPE_Q8_0; }
+bool valid_type(int t) { return t >= KVQ_TYPE_Q4_0 && t <= KVQ_TYPE_Q5_1; }
+bool has_qh(int t) { return t == KVQ_TYPE_Q5_0 || t == KVQ_TYPE_Q5_1; }
+bool has_min(int t) { return t == KVQ_TYPE_Q4_1 || t == KVQ_TYPE_Q5_1; }
 bool valid_dtype(int t) { return t == KVQ_F32 || t == KVQ_BF16 || t == KVQ_F16; }
 size_t dtype_bytes(int t) { return t == KVQ_F32 ? 4 : 2; }
 
@@ -38,10 +40,10 @@ size_t plane_bytes(const kvq_cache* c, int plane) {
   switch (plane) {
     case KVQ_PLANE_K_QS: return rows * kvq::qs_row_bytes_host(c->k_type, c->head_dim);
     case KVQ_PLANE_V_QS: return rows * kvq::qs_row_bytes_host(c->v_type, c->head_dim);
-    case KVQ_PLANE_K_QH: return c->k_type == KVQ_TYPE_Q5_0 ? rows * nb * 4 : 0;
-    case KVQ_PLANE_V_QH: return c->v_type == KVQ_TYPE_Q5_0 ? rows * nb * 4 : 0;
-    case KVQ_PLANE_K_D:
-    case KVQ_PLANE_V_D: return rows * nb * 2;
+    case KVQ_PLANE_K_QH: return has_qh(c->k_type) ? rows * nb * 4 : 0;
+    case KVQ_PLANE_V_QH: return has_qh(c->v_type) ? rows * nb * 4 : 0;
+    case KVQ_PLANE_K_D: return rows * nb * (has_min(c->k_type) ? 4 : 2);
+    case KVQ_PLANE_V_D: return rows * nb * (has_min(c->v_type) ? 4 : 2);
     case KVQ_PLANE_K_TAIL:
     case KVQ_PLANE_V_TAIL: return size_t(c->batch) * c->n_kv_heads * size_t(c->tail_len) * d * 2;
     case KVQ_PLANE_SEQ_LEN: return size_t(c->batch) * 4;
@@ -55,8 +57,8 @@ kvq_status check_cache(const kvq_cache* c) {
   const void* must[] = {c->k_qs, c->k_d, c->v_qs, c->v_d, c->seq_len, c->status};
   for (const void* p : must)
     if (!p || !aligned16(p)) return KVQ_ERR_INVALID_ARG;
-  if ((c->k_type == KVQ_TYPE_Q5_0) != (c->k_qh != nullptr)) return KVQ_ERR_INVALID_ARG;
-  if ((c->v_type == KVQ_TYPE_Q5_0) != (c->v_qh != nullptr)) return KVQ_ERR_INVALID_ARG;
+  if (has_qh(c->k_type) != (c->k_qh != nullptr)) return KVQ_ERR_INVALID_ARG;
+  if (has_qh(c->v_type) != (c->v_qh != nullptr)) return KVQ_ERR_INVALID_ARG;
   if (c->k_qh && !aligned16(c->k_qh)) return KVQ_ERR_INVALID_ARG;
   if (c->v_qh && !aligned16(c->v_qh)) return KVQ_ERR_INVALID_ARG;
   const bool has_tail = c->tail_len > 0;

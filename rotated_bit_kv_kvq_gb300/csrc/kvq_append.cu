@@ -89,42 +89,71 @@ __device__ __forceinline__ void store_bf16(uint16_t* dst, const float* v) {
 
 // Quantize and store one 32-value block whose values are spread over L = 32/P
 // lanes (lane r of the block holds channels r*P .. r*P+P-1 in y[0..P-1]).
+// d_ptr: the block's fp16 scale, or for q4_1 / q5_1 its 32-bit (d, lo) word.
 template <int P>
 __device__ __forceinline__ void quantize_block(const float* y, int qt, int r, uint8_t* qs_blk,
-                                               uint32_t* qh_word, __half* d_ptr) {
+                                               uint32_t* qh_word, void* d_ptr) {
   constexpr int L = 32 / P;
-  // signed value of largest magnitude, first channel on ties (strict '>' scan from +0)
-  float best_a = 0.0f, best_m = 0.0f;
-  int best_c = 1 << 30;
-#pragma unroll
-  for (int j = 0; j < P; ++j) {
-    const float a = fabsf(y[j]);
-    if (a > best_a) { best_a = a; best_m = y[j]; best_c = r * P + j; }
-  }
-#pragma unroll
-  for (int m = 1; m < L; m <<= 1) {
-    const float oa = __shfl_xor_sync(0xffffffffu, best_a, m);
-    const float om = __shfl_xor_sync(0xffffffffu, best_m, m);
-    const int oc = __shfl_xor_sync(0xffffffffu, best_c, m);
-    if (oa > best_a || (oa == best_a && oc < best_c)) { best_a = oa; best_m = om; best_c = oc; }
-  }
   uint8_t code[P];
-  float d;
-  if (qt == KVQ_TYPE_Q8_0) {
-    d = best_a / 127.0f;
-    const float id = d != 0.0f ? 1.0f / d : 0.0f;
+  if (type_has_min(qt)) {
+    // scale + minimum: smallest / largest value (first channel on ties), d = (hi - lo) / top,
+    // code = min(top, trunc((x - lo) * (1/d) + 0.5)), one rounding per operation
+    float lo = y[0], hi = y[0];
+    int lc = r * P, hc = r * P;
 #pragma unroll
-    for (int j = 0; j < P; ++j) code[j] = uint8_t(int8_t(int(roundf(__fmul_rn(y[j], id)))));
+    for (int j = 1; j < P; ++j) {
+      if (y[j] < lo) { lo = y[j]; lc = r * P + j; }
+      if (y[j] > hi) { hi = y[j]; hc = r * P + j; }
+    }
+#pragma unroll
+    for (int m = 1; m < L; m <<= 1) {
+      const float ol = __shfl_xor_sync(0xffffffffu, lo, m), oh = __shfl_xor_sync(0xffffffffu, hi, m);
+      const int olc = __shfl_xor_sync(0xffffffffu, lc, m), ohc = __shfl_xor_sync(0xffffffffu, hc, m);
+      if (ol < lo || (ol == lo && olc < lc)) { lo = ol; lc = olc; }
+      if (oh > hi || (oh == hi && ohc < hc)) { hi = oh; hc = ohc; }
+    }
+    const int top = qt == KVQ_TYPE_Q5_1 ? 31 : 15;
+    const float d = __fdiv_rn(__fsub_rn(hi, lo), float(top));
+    const float id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
+#pragma unroll
+    for (int j = 0; j < P; ++j)
+      code[j] = uint8_t(min(top, __float2int_rz(__fadd_rn(__fmul_rn(__fsub_rn(y[j], lo), id), 0.5f))));
+    if (r == 0)
+      *static_cast<uint32_t*>(d_ptr) = uint32_t(__half_as_ushort(__float2half_rn(d))) |
+                                       (uint32_t(__half_as_ushort(__float2half_rn(lo))) << 16);
   } else {
-    const bool q5 = qt == KVQ_TYPE_Q5_0;
-    d = q5 ? best_m / -16.0f : best_m / -8.0f;
-    const float id = d != 0.0f ? 1.0f / d : 0.0f;
-    const float off = q5 ? 16.5f : 8.5f;
-    const int top = q5 ? 31 : 15;
+    // signed value of largest magnitude, first channel on ties (strict '>' scan from +0)
+    float best_a = 0.0f, best_m = 0.0f;
+    int best_c = 1 << 30;
 #pragma unroll
-    for (int j = 0; j < P; ++j) code[j] = uint8_t(min(top, __float2int_rz(__fadd_rn(__fmul_rn(y[j], id), off))));
+    for (int j = 0; j < P; ++j) {
+      const float a = fabsf(y[j]);
+      if (a > best_a) { best_a = a; best_m = y[j]; best_c = r * P + j; }
+    }
+#pragma unroll
+    for (int m = 1; m < L; m <<= 1) {
+      const float oa = __shfl_xor_sync(0xffffffffu, best_a, m);
+      const float om = __shfl_xor_sync(0xffffffffu, best_m, m);
+      const int oc = __shfl_xor_sync(0xffffffffu, best_c, m);
+      if (oa > best_a || (oa == best_a && oc < best_c)) { best_a = oa; best_m = om; best_c = oc; }
+    }
+    float d;
+    if (qt == KVQ_TYPE_Q8_0) {
+      d = best_a / 127.0f;
+      const float id = d != 0.0f ? 1.0f / d : 0.0f;
+#pragma unroll
+      for (int j = 0; j < P; ++j) code[j] = uint8_t(int8_t(int(roundf(__fmul_rn(y[j], id)))));
+    } else {
+      const bool q5 = qt == KVQ_TYPE_Q5_0;
+      d = q5 ? best_m / -16.0f : best_m / -8.0f;
+      const float id = d != 0.0f ? 1.0f / d : 0.0f;
+      const float off = q5 ? 16.5f : 8.5f;
+      const int top = q5 ? 31 : 15;
+#pragma unroll
+      for (int j = 0; j < P; ++j) code[j] = uint8_t(min(top, __float2int_rz(__fadd_rn(__fmul_rn(y[j], id), off))));
+    }
+    if (r == 0) *static_cast<__half*>(d_ptr) = __float2half_rn(d);
   }
-  if (r == 0) *d_ptr = __float2half_rn(d);
   if (qt == KVQ_TYPE_Q8_0) {
     store_bytes<P>(qs_blk + r * P, code);
     return;
@@ -137,7 +166,7 @@ __device__ __forceinline__ void quantize_block(const float* y, int qt, int r, ui
     packed[j] = uint8_t((code[j] & 0x0F) | ((hi & 0x0F) << 4));
   }
   if (r < L / 2) store_bytes<P>(qs_blk + r * P, packed);
-  if (qt == KVQ_TYPE_Q5_0) {
+  if (type_has_qh(qt)) {
     uint32_t w = 0;
 #pragma unroll
     for (int j = 0; j < P; ++j) w |= uint32_t((code[j] >> 4) & 1) << (r * P + j);
@@ -189,14 +218,15 @@ append_kernel(kvq_cache c, int rot_k, int rot_v, const void* __restrict__ kin, c
       const size_t row = ((size_t)b * H + h) * c.max_ctx + pos;
       uint8_t* qs = static_cast<uint8_t*>(which ? c.v_qs : c.k_qs) + row * qs_row_bytes(qt, D);
       uint32_t* qh = static_cast<uint32_t*>(which ? c.v_qh : c.k_qh);
-      __half* dp = static_cast<__half*>(which ? c.v_d : c.k_d) + row * NB;
+      uint8_t* dp = static_cast<uint8_t*>(which ? c.v_d : c.k_d) + row * NB * (type_has_min(qt) ? 4 : 2);
       const int L = 32 / P;
       const int r = lane % L;
 #pragma unroll
       for (int gi = 0; gi < D / G; ++gi) {
         const int blk = gi * P + lane / L;
         const int blk_bytes = qt == KVQ_TYPE_Q8_0 ? 32 : 16;
-        quantize_block<P>(v + gi * P, qt, r, qs + blk * blk_bytes, qh ? qh + row * NB + blk : nullptr, dp + blk);
+        quantize_block<P>(v + gi * P, qt, r, qs + blk * blk_bytes, qh ? qh + row * NB + blk : nullptr,
+                          dp + blk * (type_has_min(qt) ? 4 : 2));
       }
       if (c.tail_len > 0 && i >= nb - c.tail_len) {
         uint16_t* tail = static_cast<uint16_t*>(which ? c.v_tail : c.k_tail) +
@@ -233,7 +263,6 @@ template <int D, int G>
 __global__ void __launch_bounds__(128)
 debug_kernel(kvq_cache c, int rot_side, int seq, int kv_head, int which, int t0, int count,
              int original_basis, float* __restrict__ out, uint8_t* __restrict__ blocks) {
-  constexpr int P = G / 32;
   constexpr int E = D / 32;
   constexpr int NB = D / kQK;
   const int lane = threadIdx.x & 31;
@@ -254,38 +283,41 @@ debug_kernel(kvq_cache c, int rot_side, int seq, int kv_head, int which, int t0,
     const size_t row = ((size_t)seq * H + kv_head) * c.max_ctx + pos;
     const uint8_t* qs = static_cast<const uint8_t*>(is_v ? c.v_qs : c.k_qs) + row * qs_row_bytes(qt, D);
     const uint32_t* qh = static_cast<const uint32_t*>(is_v ? c.v_qh : c.k_qh);
-    const __half* dp = static_cast<const __half*>(is_v ? c.v_d : c.k_d) + row * NB;
+    // block header: fp16 d, or for q4_1 / q5_1 the (d, lo) pair, as bytes
+    const int hb = type_has_min(qt) ? 4 : 2;
+    const uint8_t* dp = static_cast<const uint8_t*>(is_v ? c.v_d : c.k_d) + row * NB * hb;
 #pragma unroll
     for (int j = 0; j < E; ++j) {
       const int ch = fwht_channel<D, G>(lane, j);
       const int blk = ch / kQK, k = ch % kQK;
-      const float dv = __half2float(dp[blk]);
+      const float dv = __half2float(reinterpret_cast<const __half*>(dp + blk * hb)[0]);
+      const float mv = type_has_min(qt) ? __half2float(reinterpret_cast<const __half*>(dp + blk * hb)[1]) : 0.0f;
       int code;
       if (qt == KVQ_TYPE_Q8_0) {
         code = int(int8_t(qs[blk * 32 + k]));
       } else {
         const uint8_t byte = qs[blk * 16 + (k & 15)];
         code = k < 16 ? (byte & 15) : (byte >> 4);
-        if (qt == KVQ_TYPE_Q5_0) code |= int((qh[row * NB + blk] >> k) & 1u) << 4;
-        code -= qt == KVQ_TYPE_Q5_0 ? 16 : 8;
+        if (type_has_qh(qt)) code |= int((qh[row * NB + blk] >> k) & 1u) << 4;
+        code -= type_code_offset(qt);
       }
-      v[j] = float(code) * dv;
+      v[j] = float(code) * dv + mv;
     }
     if (blocks) {
-      // GGUF array-of-structs: [d:2][qh:4 (q5_0)][qs:16|32] per block
-      const int bb = qt == KVQ_TYPE_Q4_0 ? 18 : (qt == KVQ_TYPE_Q5_0 ? 22 : 34);
+      // GGUF array-of-structs: [d:2][lo:2 (_1)][qh:4 (q5_x)][qs:16|32] per block
+      const int bb = type_block_bytes(qt);
       uint8_t* ob = blocks + (size_t)t * NB * bb;
       const int qsb = qt == KVQ_TYPE_Q8_0 ? 32 : 16;
+      const int qhb = type_has_qh(qt) ? 4 : 0;
       for (int idx = lane; idx < NB * bb; idx += 32) {
         const int blk = idx / bb, o = idx % bb;
         uint8_t val;
-        if (o < 2) {
-          val = uint8_t(__half_as_ushort(dp[blk]) >> (8 * o));
-        } else if (qt == KVQ_TYPE_Q5_0 && o < 6) {
-          val = uint8_t(qh[row * NB + blk] >> (8 * (o - 2)));
+        if (o < hb) {
+          val = dp[blk * hb + o];
+        } else if (o < hb + qhb) {
+          val = uint8_t(qh[row * NB + blk] >> (8 * (o - hb)));
         } else {
-          const int k = o - (qt == KVQ_TYPE_Q5_0 ? 6 : 2);
-          val = qs[blk * qsb + k];
+          val = qs[blk * qsb + (o - hb - qhb)];
         }
         ob[idx] = val;
       }

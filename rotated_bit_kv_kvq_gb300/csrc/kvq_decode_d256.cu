@@ -1,0 +1,11 @@
+// Decode kernels for head_dim 256, every K / V format pair.
+#include "kvq_decode_impl.cuh"
+
+namespace kvq {
+
+cudaError_t launch_decode_d256(const kvq_cache& c, Rot rot, const DecodePlan& plan, const void* q, int q_dtype,
+                              int n_q_heads, float scale, void* out, int out_dtype, void* ws, cudaStream_t st) {
+  return run_decode_d<256>(c, rot, plan, q, q_dtype, n_q_heads, scale, out, out_dtype, ws, st);
+}
+
+}  // namespace kvq

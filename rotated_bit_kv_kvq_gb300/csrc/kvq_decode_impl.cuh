@@ -1,0 +1,800 @@
+// Decode kernels and their host-side launch templates, included by one
+// translation unit per head_dim (kvq_decode_d*.cu) so the format pairs compile
+// in parallel.
+#pragma once
+
+// Decode attention over the rotated, block-quantized cache plus its bf16 tail.
+//
+// Scores are dot products in the rotated basis: rotating q and k by the same
+// orthogonal Hadamard matrix leaves q.k unchanged, and the softmax-weighted
+// sum of rotated values is rotated back at the end (velog
+// "fix-kv-cache-quantization-outliers", section 아다마르 회전).  Keys and values
+// of the most recent tail_len positions come from the bf16 tail, older ones
+// from the q4_0 / q5_0 / q8_0 body (aitrends.kr "KVarN과 Precision Tail",
+// section 용어 해설).
+//
+// Kernel 1 (split-K): CTA = (split, KV head x head group, sequence), 4 warps.
+// Every warp streams its own 16-token tiles through a ring of shared-memory
+// stages filled by TMA (2-D tensor copies with hardware swizzle for the packed
+// codes and bf16 rows, 1-D bulk copies for scales and q5_0 high bits).  Codes
+// are turned into exact fp16 integers in registers and multiplied on the
+// tensor cores (mma.m16n8k16, fp32 accumulate):
+//   S[t][h]  = sum_blocks Dk[t][blk] * (codes_K[t][blk] . q[h][blk])   (q as fp16 hi + lo)
+//   O[c][h] += codes_V[t][c] . (P[t][h] * Dv[t][blk(c)])                 (P as fp16)
+// with an online softmax (base 2) per head.  Each CTA writes (m, l, acc).
+// Kernel 2: merges the splits per query head (log-sum-exp), normalizes,
+// rotates back with a warp FWHT and stores the output.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <math.h>
+
+#include "kvq_device.cuh"
+#include "kvq_internal.h"
+
+namespace kvq {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kMaxHeads = 8;                 // query heads per CTA (mma N)
+constexpr long long kWaitCycles = 1000000000LL;  // ~0.5 s at 2 GHz; a TMA tile lands in microseconds
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kTailChunkMax = 4096;  // tail slots per CTA
+constexpr int kSmemBudget = 64 * 1024;       // stages; leaves room for 3 CTAs per SM
+constexpr int kCtasPerSm = 3;
+
+constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
+// widest TMA swizzle box (128, 64 or 32 bytes) that tiles a row exactly
+constexpr int box_w(int row_bytes) { return row_bytes % 128 == 0 ? 128 : (row_bytes % 64 == 0 ? 64 : 32); }
+
+template <int D, int KT, int VT>
+struct Cfg {
+  static constexpr int NB = D / 32;
+  static constexpr int rowK = KT == KVQ_TYPE_Q8_0 ? D : D / 2;
+  static constexpr int rowV = VT == KVQ_TYPE_Q8_0 ? D : D / 2;
+  static constexpr int WK = box_w(rowK), WV = box_w(rowV);
+  static constexpr bool K5 = type_has_qh(KT), V5 = type_has_qh(VT);
+  static constexpr bool K1 = type_has_min(KT), V1 = type_has_min(VT);   // scale + minimum blocks
+  static constexpr int KH = K1 ? 4 : 2, VH = V1 ? 4 : 2;                // block header bytes
+  // body stage: 16 tokens
+  static constexpr int off_kqs = 0;
+  static constexpr int off_vqs = align_up(16 * rowK, 1024);
+  static constexpr int off_kd = off_vqs + align_up(16 * rowV, 16);
+  static constexpr int off_vd = off_kd + 16 * NB * KH;
+  static constexpr int off_kqh = off_vd + 16 * NB * VH;
+  static constexpr int off_vqh = off_kqh + (K5 ? 16 * NB * 4 : 0);
+  static constexpr int body_bytes = off_vqh + (V5 ? 16 * NB * 4 : 0);
+  static constexpr uint32_t body_tx =
+      16 * rowK + 16 * rowV + 16 * NB * (KH + VH) + (K5 ? 64 * NB : 0) + (V5 ? 64 * NB : 0);
+  // tail stage: TT tokens of bf16 K and V
+  static constexpr int TT = D >= 256 ? 8 : 16;
+  static constexpr int WT = box_w(2 * D);
+  static constexpr int off_kt = 0;
+  static constexpr int off_vt = align_up(TT * 2 * D, 1024);
+  static constexpr int tail_bytes = off_vt + TT * 2 * D;
+  static constexpr uint32_t tail_tx = 2 * TT * 2 * D;
+  static constexpr int stage = align_up(body_bytes > tail_bytes ? body_bytes : tail_bytes, 1024);
+  static constexpr int NS_raw = kSmemBudget / (kWarps * stage);
+  static constexpr int NS = NS_raw > 4 ? 4 : (NS_raw < 2 ? 2 : NS_raw);
+  static constexpr int off_q = kWarps * NS * stage;                 // q: [8][D] fp32
+  static constexpr int off_qsum = off_q + kMaxHeads * D * 4;        // [NB][8] per-block sums of q (K minimum)
+  static constexpr int off_bar = off_qsum + NB * kMaxHeads * 4;      // mbarriers [kWarps][NS]
+  static constexpr int off_ml = off_bar + kWarps * NS * 8;          // [kWarps][8] m and l
+  static constexpr int smem = off_ml + 2 * kWarps * kMaxHeads * 4 + 1024;  // + alignment slack
+  static_assert(kWarps * kMaxHeads * D * 4 <= kWarps * NS * stage, "merge buffer must fit in the stages");
+};
+
+struct Params {
+  const uint8_t* k_d; const uint8_t* v_d;   // fp16 d per block, or (d, lo) pairs for q4_1 / q5_1
+  const uint32_t* k_qh; const uint32_t* v_qh;
+  const int32_t* seq_len; uint32_t* status;
+  const void* q; float* ws_acc; float* ws_ml;
+  int n_kv_heads, max_ctx, tail_len;
+  int q_dtype, n_q_heads, group, heads_per_cta, head_groups;
+  int rot_k;
+  float scale_log2;                 // softmax scale * log2(e)
+  int chunk, tail_chunk, splits_body, splits_tail, splits;
+};
+
+__device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
+
+// a, b -> fp16 pairs hi = fp16(a, b) and lo = fp16(a - hi, b - hi): hi + lo keeps ~22 bits.
+__device__ __forceinline__ void split_h2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  hi = pack_h2(a, b);
+  const float2 f = __half22float2(u32_as_h2(hi));
+  lo = pack_h2(a - f.x, b - f.y);
+}
+
+// q5_0 high bits of a K row word h = qh >> (4*tig), placed at bits 4 / 20 (with the 0x6400 magic).
+__device__ __forceinline__ uint32_t khb(uint32_t h, int which) {
+  switch (which) {
+    case 0: return (((h << 4) & 0x10u) | ((h << 18) & 0x100000u)) | 0x64006400u;   // channels +0, +2
+    case 1: return (((h << 3) & 0x10u) | ((h << 17) & 0x100000u)) | 0x64006400u;   // +1, +3
+    case 2: return (((h >> 12) & 0x10u) | ((h << 2) & 0x100000u)) | 0x64006400u;   // 16+0, 16+2
+    default: return (((h >> 13) & 0x10u) | ((h << 1) & 0x100000u)) | 0x64006400u;  // 16+1, 16+3
+  }
+}
+
+template <int D, int KT, int VT>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                    const __grid_constant__ CUtensorMap tmKt, const __grid_constant__ CUtensorMap tmVt) {
+  using C = Cfg<D, KT, VT>;
+  constexpr int NB = C::NB;
+  constexpr int NS = C::NS;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, tig = lane & 3;
+  const int b = blockIdx.z;
+  const int kvh = blockIdx.y / p.head_groups;
+  const int hg = blockIdx.y % p.head_groups;
+  const int head0 = kvh * p.group + hg * p.heads_per_cta;
+  const int nheads = min(p.heads_per_cta, p.group - hg * p.heads_per_cta);
+  const int split = blockIdx.x;
+
+  const int n = p.seq_len[b];
+  const int T = p.tail_len;
+  const int nbody = max(0, n - T);
+  const int ntail = min(n, T);
+  const bool is_tail = split < p.splits_tail;
+  int t_begin, t_end;
+  if (is_tail) {
+    t_begin = split * p.tail_chunk;
+    t_end = min(ntail, t_begin + p.tail_chunk);
+  } else {
+    t_begin = (split - p.splits_tail) * p.chunk;
+    t_end = min(nbody, t_begin + p.chunk);
+  }
+  float* ml = p.ws_ml + (((size_t)b * p.n_q_heads + head0) * p.splits + split) * 2;
+  if (t_begin >= t_end) {  // nothing to read: an empty partial
+    if (tid < nheads) {
+      ml[(size_t)tid * p.splits * 2] = -INFINITY;
+      ml[(size_t)tid * p.splits * 2 + 1] = 0.0f;
+    }
+    return;
+  }
+
+  float* sq = reinterpret_cast<float*>(smem + C::off_q);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::off_bar);
+  float* sm_m = reinterpret_cast<float*>(smem + C::off_ml);
+  float* sm_l = sm_m + kWarps * kMaxHeads;
+
+  if (tid == 0) {
+    for (int i = 0; i < kWarps * NS; ++i) mbar_init(&bars[i], 1);
+    fence_barrier_init();
+    if (is_tail) { prefetch_tmap(&tmKt); prefetch_tmap(&tmVt); }
+    else { prefetch_tmap(&tmK); prefetch_tmap(&tmV); }
+  }
+
+  // ---- this warp's tiles, and the producer (lane 0) --------------------
+  const int TR = is_tail ? C::TT : 16;                       // rows per tile
+  const int ntiles = (t_end - t_begin + TR - 1) / TR;
+  const int my_tiles = ntiles > warp ? (ntiles - warp + kWarps - 1) / kWarps : 0;
+  uint8_t* wstage = smem + warp * NS * C::stage;
+  uint64_t* wbar = bars + warp * NS;
+  const size_t bh = (size_t)b * p.n_kv_heads + kvh;
+
+  auto issue = [&](int k) {  // tile k of this warp -> stage k % NS (lane 0 only)
+    const int s = k % NS;
+    uint8_t* st = wstage + s * C::stage;
+    const int t0 = t_begin + (warp + k * kWarps) * TR;
+    if (is_tail) {
+      const int row = int(bh * T + t0);
+      mbar_arrive_expect_tx(&wbar[s], C::tail_tx);
+#pragma unroll
+      for (int x = 0; x < 2 * D; x += C::WT) {
+        tma_2d_g2s(st + C::off_kt + (x / C::WT) * C::TT * C::WT, &tmKt, x / 2, row, &wbar[s]);
+        tma_2d_g2s(st + C::off_vt + (x / C::WT) * C::TT * C::WT, &tmVt, x / 2, row, &wbar[s]);
+      }
+    } else {
+      const size_t row = bh * p.max_ctx + t0;
+      mbar_arrive_expect_tx(&wbar[s], C::body_tx);
+#pragma unroll
+      for (int x = 0; x < C::rowK; x += C::WK)
+        tma_2d_g2s(st + C::off_kqs + (x / C::WK) * 16 * C::WK, &tmK, x, int(row), &wbar[s]);
+#pragma unroll
+      for (int x = 0; x < C::rowV; x += C::WV)
+        tma_2d_g2s(st + C::off_vqs + (x / C::WV) * 16 * C::WV, &tmV, x, int(row), &wbar[s]);
+      bulk_g2s(st + C::off_kd, p.k_d + row * NB * C::KH, 16 * NB * C::KH, &wbar[s]);
+      bulk_g2s(st + C::off_vd, p.v_d + row * NB * C::VH, 16 * NB * C::VH, &wbar[s]);
+      if constexpr (C::K5) bulk_g2s(st + C::off_kqh, p.k_qh + row * NB, 16 * NB * 4, &wbar[s]);
+      if constexpr (C::V5) bulk_g2s(st + C::off_vqh, p.v_qh + row * NB, 16 * NB * 4, &wbar[s]);
+    }
+  };
+
+  __syncthreads();  // barriers initialised
+  if (lane == 0) {
+    for (int k = 0; k < NS && k < my_tiles; ++k) issue(k);
+  }
+
+  // ---- queries: load, rotate, scale, split into fp16 hi/lo fragments ----
+  for (int i = tid; i < kMaxHeads * D; i += kThreads) {
+    const int hh = i / D, c = i % D;
+    float v = 0.0f;
+    if (hh < nheads) {
+      const size_t e = ((size_t)b * p.n_q_heads + head0 + hh) * D + c;
+      if (p.q_dtype == KVQ_F32) v = static_cast<const float*>(p.q)[e];
+      else if (p.q_dtype == KVQ_BF16) v = bf16_bits_to_f32(static_cast<const uint16_t*>(p.q)[e]);
+      else v = __half2float(static_cast<const __half*>(p.q)[e]);
+    }
+    sq[i] = v;
+  }
+  __syncthreads();
+  {
+    constexpr int G = (D >= 64 && D % 64 == 0) ? (((D & (D - 1)) == 0) ? D : 64) : 32;
+    for (int hh = warp; hh < kMaxHeads; hh += kWarps) {
+      float v[D / 32];
+#pragma unroll
+      for (int j = 0; j < D / 32; ++j) v[j] = sq[hh * D + fwht_channel<D, G>(lane, j)];
+      float s = p.scale_log2;
+      if (p.rot_k) {
+        warp_fwht<D, G>(v, lane);
+        s *= inv_sqrt_group<G>();
+      }
+#pragma unroll
+      for (int j = 0; j < D / 32; ++j) sq[hh * D + fwht_channel<D, G>(lane, j)] = v[j] * s;
+    }
+  }
+  __syncthreads();
+  // B fragments: k-step (blk, half) covers channels 32*blk + 16*half + 4*tig + {0,2 | 1,3}.
+  // They are the same in every warp: warp 0 builds them once and leaves them in
+  // shared memory over the q staging ([blk][half][lane] x {hi b0b1, hi b2b3, lo b0b1,
+  // lo b2b3}, 32*D bytes = the staging's size), so no warp holds them in registers.
+  const uint4* qfs = reinterpret_cast<const uint4*>(sq);
+  float* qsum = reinterpret_cast<float*>(smem + C::off_qsum);  // [blk][head]: sum of the block's q values
+  if (warp == 0) {
+    if constexpr (C::K1) {
+      for (int i = lane; i < NB * kMaxHeads; i += 32) {
+        const int blk = i / kMaxHeads, hh = i % kMaxHeads;
+        float t = 0.0f;
+        for (int c = 0; c < 32; ++c) t += sq[hh * D + blk * 32 + c];
+        qsum[i] = t;
+      }
+    }
+    uint4 qf[NB][2];
+#pragma unroll
+    for (int blk = 0; blk < NB; ++blk)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const float4 q4 = *reinterpret_cast<const float4*>(sq + g * D + 32 * blk + 16 * hf + 4 * tig);
+        const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
+        float hi[4], lo[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          hi[j] = __half2float(__float2half_rn(qv[j]));
+          lo[j] = qv[j] - hi[j];
+        }
+        qf[blk][hf] = make_uint4(pack_h2(hi[0], hi[2]), pack_h2(hi[1], hi[3]), pack_h2(lo[0], lo[2]),
+                                 pack_h2(lo[1], lo[3]));
+      }
+    __syncwarp();
+#pragma unroll
+    for (int blk = 0; blk < NB; ++blk)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) reinterpret_cast<uint4*>(sq)[(blk * 2 + hf) * 32 + lane] = qf[blk][hf];
+  }
+  __syncthreads();
+
+  // ---- main loop ------------------------------------------------------------
+  float acc[NB][2][4];
+#pragma unroll
+  for (int i = 0; i < NB; ++i)
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) acc[i][j][r] = 0.0f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+  bool timed_out = false;
+  int k_stop = my_tiles;
+
+  for (int k = 0; k < my_tiles; ++k) {
+    const int s = k % NS;
+    const bool arrived = mbar_wait_bounded(&wbar[s], (k / NS) & 1, kWaitCycles);
+    if (!__all_sync(0xffffffffu, arrived)) { timed_out = true; k_stop = k; break; }
+    const uint8_t* st = wstage + s * C::stage;
+    const int t0 = t_begin + (warp + k * kWarps) * TR;
+    const bool v0 = t0 + g < t_end, v8 = (TR == 16) && (t0 + g + 8 < t_end);
+
+    float S[4] = {0.f, 0.f, 0.f, 0.f};
+    if (!is_tail) {
+      // ------------------------------- body: scores
+      const __half* kd = reinterpret_cast<const __half*>(st + C::off_kd);
+      const uint32_t kbase = smem_u32(st + C::off_kqs);
+      const int mi = lane >> 3, rr = (lane & 7) + 8 * (mi & 1);
+      if constexpr (KT == KVQ_TYPE_Q8_0) {
+#pragma unroll
+        for (int blk = 0; blk < NB; ++blk) {
+          uint32_t r0, r1, r2, r3;
+          ldsm_x4(kbase + swz_off<C::WK>(rr, 32 * blk + 16 * (mi >> 1), 16), r0, r1, r2, r3);
+          r0 ^= 0x80808080u; r1 ^= 0x80808080u; r2 ^= 0x80808080u; r3 ^= 0x80808080u;
+          const uint32_t alo[4] = {i8_pair<0, 2>(r0), i8_pair<0, 2>(r1), i8_pair<1, 3>(r0), i8_pair<1, 3>(r1)};
+          const uint32_t ahi[4] = {i8_pair<0, 2>(r2), i8_pair<0, 2>(r3), i8_pair<1, 3>(r2), i8_pair<1, 3>(r3)};
+          const uint4 qa = qfs[(blk * 2) * 32 + lane], qb = qfs[(blk * 2 + 1) * 32 + lane];
+          float cc[4] = {0.f, 0.f, 0.f, 0.f};
+          mma16816(cc, alo, qa.x, qa.y);
+          mma16816(cc, alo, qa.z, qa.w);
+          mma16816(cc, ahi, qb.x, qb.y);
+          mma16816(cc, ahi, qb.z, qb.w);
+          const float dk0 = __half2float(kd[g * NB + blk]), dk8 = __half2float(kd[(g + 8) * NB + blk]);
+          S[0] += dk0 * cc[0]; S[1] += dk0 * cc[1];
+          S[2] += dk8 * cc[2]; S[3] += dk8 * cc[3];
+        }
+      } else {
+        // header of token t, block blk: d (and, for q4_1 / q5_1, the minimum right after it)
+        constexpr int KHH = C::KH / 2;
+        constexpr uint32_t OFF = (0x6400u + uint32_t(type_code_offset(KT))) * 0x10001u;
+#pragma unroll
+        for (int bp = 0; bp < NB; bp += 2) {
+          uint32_t rr4[4];
+          ldsm_x4(kbase + swz_off<C::WK>(rr, 16 * (bp + (mi >> 1)), 16), rr4[0], rr4[1], rr4[2], rr4[3]);
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int blk = bp + e;
+            const uint32_t ra = rr4[2 * e], rb = rr4[2 * e + 1];  // token g, token g+8
+            uint32_t m00 = 0x64006400u, m01 = 0x64006400u, m02 = 0x64006400u, m03 = 0x64006400u;
+            uint32_t m10 = 0x64006400u, m11 = 0x64006400u, m12 = 0x64006400u, m13 = 0x64006400u;
+            if constexpr (C::K5) {
+              const uint32_t* kqh = reinterpret_cast<const uint32_t*>(st + C::off_kqh);
+              const uint32_t ha = kqh[g * NB + blk] >> (4 * tig), hb = kqh[(g + 8) * NB + blk] >> (4 * tig);
+              m00 = khb(ha, 0); m01 = khb(ha, 1); m02 = khb(ha, 2); m03 = khb(ha, 3);
+              m10 = khb(hb, 0); m11 = khb(hb, 1); m12 = khb(hb, 2); m13 = khb(hb, 3);
+            }
+            const uint32_t alo[4] = {nib_pair(ra, 0, m00, OFF), nib_pair(rb, 0, m10, OFF),
+                                     nib_pair(ra, 8, m01, OFF), nib_pair(rb, 8, m11, OFF)};
+            const uint32_t ahi[4] = {nib_pair(ra, 4, m02, OFF), nib_pair(rb, 4, m12, OFF),
+                                     nib_pair(ra, 12, m03, OFF), nib_pair(rb, 12, m13, OFF)};
+            const uint4 qa = qfs[(blk * 2) * 32 + lane], qb = qfs[(blk * 2 + 1) * 32 + lane];
+            float cc[4] = {0.f, 0.f, 0.f, 0.f};
+            mma16816(cc, alo, qa.x, qa.y);
+            mma16816(cc, alo, qa.z, qa.w);
+            mma16816(cc, ahi, qb.x, qb.y);
+            mma16816(cc, ahi, qb.z, qb.w);
+            const float dk0 = __half2float(kd[(g * NB + blk) * KHH]);
+            const float dk8 = __half2float(kd[((g + 8) * NB + blk) * KHH]);
+            S[0] += dk0 * cc[0]; S[1] += dk0 * cc[1];
+            S[2] += dk8 * cc[2]; S[3] += dk8 * cc[3];
+            if constexpr (C::K1) {  // + lo * (sum of the block's q), per token and head
+              const float mk0 = __half2float(kd[(g * NB + blk) * KHH + 1]);
+              const float mk8 = __half2float(kd[((g + 8) * NB + blk) * KHH + 1]);
+              const float2 qs2 = *reinterpret_cast<const float2*>(qsum + blk * kMaxHeads + 2 * tig);
+              S[0] += mk0 * qs2.x; S[1] += mk0 * qs2.y;
+              S[2] += mk8 * qs2.x; S[3] += mk8 * qs2.y;
+            }
+          }
+        }
+      }
+    } else {
+      // ------------------------------- tail (bf16, stored as fp16 * 2^-8): scores
+      const uint8_t* kt = st + C::off_kt;
+      float cc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int blk = 0; blk < NB; ++blk)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const int xb = 2 * (32 * blk + 16 * hf + 4 * tig);
+          const uint2 ka = *reinterpret_cast<const uint2*>(kt + swz_off<C::WT>(g, xb, C::TT));
+          uint2 kb = make_uint2(0u, 0u);
+          if (C::TT == 16) kb = *reinterpret_cast<const uint2*>(kt + swz_off<C::WT>(g + 8 < C::TT ? g + 8 : g, xb, C::TT));
+          const uint32_t a[4] = {bf16x2_to_h2_scaled(__byte_perm(ka.x, ka.y, 0x5410)),
+                                 C::TT == 16 ? bf16x2_to_h2_scaled(__byte_perm(kb.x, kb.y, 0x5410)) : 0u,
+                                 bf16x2_to_h2_scaled(__byte_perm(ka.x, ka.y, 0x7632)),
+                                 C::TT == 16 ? bf16x2_to_h2_scaled(__byte_perm(kb.x, kb.y, 0x7632)) : 0u};
+          const uint4 qa = qfs[(blk * 2 + hf) * 32 + lane];
+          mma16816(cc, a, qa.x, qa.y);
+          mma16816(cc, a, qa.z, qa.w);
+        }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) S[r] = 256.0f * cc[r];
+    }
+
+    // ---- online softmax (base 2); rows g, g+8 = tokens, cols 2tig, 2tig+1 = heads
+    if (!v0) { S[0] = -INFINITY; S[1] = -INFINITY; }
+    if (!v8) { S[2] = -INFINITY; S[3] = -INFINITY; }
+    float mx0 = fmaxf(S[0], S[2]), mx1 = fmaxf(S[1], S[3]);
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    const float nm0 = fmaxf(m0, mx0), nm1 = fmaxf(m1, mx1);
+    if (__any_sync(0xffffffffu, nm0 > m0 || nm1 > m1)) {
+      const float a0 = m0 == -INFINITY ? 0.0f : fast_exp2(m0 - nm0);
+      const float a1 = m1 == -INFINITY ? 0.0f : fast_exp2(m1 - nm1);
+      l0 *= a0; l1 *= a1;
+#pragma unroll
+      for (int i = 0; i < NB; ++i)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          acc[i][j][0] *= a0; acc[i][j][1] *= a1; acc[i][j][2] *= a0; acc[i][j][3] *= a1;
+        }
+      m0 = nm0; m1 = nm1;
+    }
+    const float ms0 = m0 == -INFINITY ? 0.0f : m0, ms1 = m1 == -INFINITY ? 0.0f : m1;
+    const float p0 = fast_exp2(S[0] - ms0), p1 = fast_exp2(S[1] - ms1);
+    const float p2 = fast_exp2(S[2] - ms0), p3 = fast_exp2(S[3] - ms1);
+    l0 += p0 + p2; l1 += p1 + p3;
+
+    // ---- P.V.  P is transposed once per tile (movmatrix on fp16 hi + lo parts)
+    // into the B-fragment layout: tokens 2tig, 2tig+1, 2tig+8, 2tig+9 of head g.
+    // Each block then scales it by its V scale (fp32) and splits it again into
+    // fp16 hi + lo, so the products keep ~22 bits; the codes are exact.
+    float pt[4];
+    {
+      const uint32_t h0 = pack_h2(p0, p1), h1 = pack_h2(p2, p3);
+      const float2 f0 = __half22float2(u32_as_h2(h0)), f1 = __half22float2(u32_as_h2(h1));
+      const uint32_t r0 = pack_h2(p0 - f0.x, p1 - f0.y), r1 = pack_h2(p2 - f1.x, p3 - f1.y);
+      const float2 th0 = __half22float2(u32_as_h2(movm_t(h0))), tr0 = __half22float2(u32_as_h2(movm_t(r0)));
+      const float2 th1 = __half22float2(u32_as_h2(movm_t(h1))), tr1 = __half22float2(u32_as_h2(movm_t(r1)));
+      pt[0] = th0.x + tr0.x; pt[1] = th0.y + tr0.y; pt[2] = th1.x + tr1.x; pt[3] = th1.y + tr1.y;
+    }
+    const int tt = t0 + 2 * tig;  // first token of this lane's transposed rows
+    const bool vt0 = tt < t_end, vt1 = tt + 1 < t_end;
+    const bool vt8 = TR == 16 && tt + 8 < t_end, vt9 = TR == 16 && tt + 9 < t_end;
+    if (!is_tail) {
+      // V scales of the transposed tokens, read per block (0 for rows past the end)
+      const __half* vd = reinterpret_cast<const __half*>(st + C::off_vd);
+      const float pz[4] = {vt0 ? pt[0] : 0.0f, vt1 ? pt[1] : 0.0f, vt8 ? pt[2] : 0.0f, vt9 ? pt[3] : 0.0f};
+      constexpr int VHH = C::VH / 2;  // halves per block header
+      // P times the V scale (part 0) or the V minimum (part 1) of block blk, as fp16 hi + lo
+      auto pscaled = [&](int blk, int part, uint32_t& bh0, uint32_t& bl0, uint32_t& bh1, uint32_t& bl1) {
+        const int o = blk * VHH + part;
+        split_h2(pz[0] * __half2float(vd[(2 * tig) * NB * VHH + o]), pz[1] * __half2float(vd[(2 * tig + 1) * NB * VHH + o]),
+                 bh0, bl0);
+        split_h2(pz[2] * __half2float(vd[(2 * tig + 8) * NB * VHH + o]),
+                 pz[3] * __half2float(vd[(2 * tig + 9) * NB * VHH + o]), bh1, bl1);
+      };
+      // the minimum adds sum_t P[t][h] * lo[t][blk] to every channel of the block:
+      // an all-ones A fragment (fp16 1.0) against P * lo
+      auto add_min = [&](int blk) {
+        if constexpr (C::V1) {
+          uint32_t mh0, ml0, mh1, ml1;
+          pscaled(blk, 1, mh0, ml0, mh1, ml1);
+          const uint32_t ones[4] = {0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u};
+          mma16816(acc[blk][0], ones, mh0, mh1);
+          mma16816(acc[blk][0], ones, ml0, ml1);
+          mma16816(acc[blk][1], ones, mh0, mh1);
+          mma16816(acc[blk][1], ones, ml0, ml1);
+        }
+      };
+      const uint32_t vbase = smem_u32(st + C::off_vqs);
+      const int mi = lane >> 3, rr = (lane & 7) + 8 * (mi & 1);
+      if constexpr (VT == KVQ_TYPE_Q8_0) {
+#pragma unroll
+        for (int blk = 0; blk < NB; ++blk) {
+          uint32_t bh0, bl0, bh1, bl1;
+          pscaled(blk, 0, bh0, bl0, bh1, bl1);
+          uint32_t r0, r1, r2, r3;
+          ldsm_x4_t(vbase + swz_off<C::WV>(rr, 32 * blk + 16 * (mi >> 1), 16), r0, r1, r2, r3);
+          r0 ^= 0x80808080u; r1 ^= 0x80808080u; r2 ^= 0x80808080u; r3 ^= 0x80808080u;
+          const uint32_t a0[4] = {i8_pair<0, 2>(r0), i8_pair<1, 3>(r0), i8_pair<0, 2>(r1), i8_pair<1, 3>(r1)};
+          const uint32_t a1[4] = {i8_pair<0, 2>(r2), i8_pair<1, 3>(r2), i8_pair<0, 2>(r3), i8_pair<1, 3>(r3)};
+          mma16816(acc[blk][0], a0, bh0, bh1);
+          mma16816(acc[blk][0], a0, bl0, bl1);
+          mma16816(acc[blk][1], a1, bh0, bh1);
+          mma16816(acc[blk][1], a1, bl0, bl1);
+        }
+      } else {
+        constexpr uint32_t OFF = (0x6400u + uint32_t(type_code_offset(VT))) * 0x10001u;
+#pragma unroll
+        for (int bp = 0; bp < NB; bp += 2) {
+          uint32_t rr4[4];
+          ldsm_x4_t(vbase + swz_off<C::WV>(rr, 16 * (bp + (mi >> 1)), 16), rr4[0], rr4[1], rr4[2], rr4[3]);
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int blk = bp + e;
+            uint32_t bh0, bl0, bh1, bl1;
+            pscaled(blk, 0, bh0, bl0, bh1, bl1);
+            add_min(blk);
+            const uint32_t ra = rr4[2 * e], rb = rr4[2 * e + 1];  // tokens 0-7, 8-15
+            uint32_t ma0 = 0x64006400u, ma1 = 0x64006400u, ma2 = 0x64006400u, ma3 = 0x64006400u;
+            uint32_t mb0 = 0x64006400u, mb1 = 0x64006400u, mb2 = 0x64006400u, mb3 = 0x64006400u;
+            if constexpr (C::V5) {
+              const uint32_t* vqh = reinterpret_cast<const uint32_t*>(st + C::off_vqh);
+              const int t = 2 * tig;
+              const uint32_t h0 = vqh[t * NB + blk] >> (2 * g), h1 = vqh[(t + 1) * NB + blk] >> (2 * g);
+              const uint32_t h8 = vqh[(t + 8) * NB + blk] >> (2 * g), h9 = vqh[(t + 9) * NB + blk] >> (2 * g);
+              const uint32_t wa = __byte_perm(h0, h1, 0x5410), wa2 = __byte_perm(h0, h1, 0x7632);
+              const uint32_t wb = __byte_perm(h8, h9, 0x5410), wb2 = __byte_perm(h8, h9, 0x7632);
+              ma0 = ((wa << 4) & 0x00100010u) | 0x64006400u;  ma1 = ((wa << 3) & 0x00100010u) | 0x64006400u;
+              ma2 = ((wa2 << 4) & 0x00100010u) | 0x64006400u; ma3 = ((wa2 << 3) & 0x00100010u) | 0x64006400u;
+              mb0 = ((wb << 4) & 0x00100010u) | 0x64006400u;  mb1 = ((wb << 3) & 0x00100010u) | 0x64006400u;
+              mb2 = ((wb2 << 4) & 0x00100010u) | 0x64006400u; mb3 = ((wb2 << 3) & 0x00100010u) | 0x64006400u;
+            }
+            const uint32_t a0[4] = {nib_pair(ra, 0, ma0, OFF), nib_pair(ra, 8, ma1, OFF),
+                                    nib_pair(rb, 0, mb0, OFF), nib_pair(rb, 8, mb1, OFF)};
+            const uint32_t a1[4] = {nib_pair(ra, 4, ma2, OFF), nib_pair(ra, 12, ma3, OFF),
+                                    nib_pair(rb, 4, mb2, OFF), nib_pair(rb, 12, mb3, OFF)};
+            mma16816(acc[blk][0], a0, bh0, bh1);
+            mma16816(acc[blk][0], a0, bl0, bl1);
+            mma16816(acc[blk][1], a1, bh0, bh1);
+            mma16816(acc[blk][1], a1, bl0, bl1);
+          }
+        }
+      }
+    } else {
+      // tail values are stored as fp16 * 2^-8, so P carries the factor 256
+      uint32_t bh0, bl0, bh1, bl1;
+      split_h2(pt[0] * 256.0f, pt[1] * 256.0f, bh0, bl0);
+      split_h2(pt[2] * 256.0f, pt[3] * 256.0f, bh1, bl1);
+      // token validity of the rows this lane reads from the transposed tile
+      const uint32_t mlo = (vt0 ? 0x0000FFFFu : 0u) | (vt1 ? 0xFFFF0000u : 0u);
+      const uint32_t mhi = (vt8 ? 0x0000FFFFu : 0u) | (vt9 ? 0xFFFF0000u : 0u);
+      const uint32_t vbase = smem_u32(st + C::off_vt);
+      const int mi = lane >> 3;
+      const int rr = (lane & 7) + (C::TT == 16 ? 8 * (mi >> 1) : 0);
+#pragma unroll
+      for (int blk = 0; blk < NB; ++blk)
+#pragma unroll
+        for (int cc2 = 0; cc2 < 2; ++cc2) {
+          const int mt = 2 * blk + cc2;  // 16 channels
+          uint32_t r0, r1, r2, r3;
+          ldsm_x4_t(vbase + swz_off<C::WT>(rr, 2 * (16 * mt + 8 * (mi & 1)), C::TT), r0, r1, r2, r3);
+          const uint32_t a[4] = {bf16x2_to_h2_scaled(r0) & mlo, bf16x2_to_h2_scaled(r1) & mlo,
+                                 bf16x2_to_h2_scaled(r2) & mhi, bf16x2_to_h2_scaled(r3) & mhi};
+          mma16816(acc[blk][cc2], a, bh0, bh1);
+          mma16816(acc[blk][cc2], a, bl0, bl1);
+        }
+    }
+    __syncwarp();
+    if (lane == 0 && k + NS < my_tiles) {
+      fence_proxy_async_smem();
+      issue(k + NS);
+    }
+  }
+
+  if (timed_out) {
+    if (lane == 0) atomicOr(p.status, KVQ_DEV_ERR_TIMEOUT);
+    // wait (bounded) for this warp's copies still in flight before leaving:
+    // tiles k_stop .. k_stop+NS-1 were issued and not consumed
+    for (int k = k_stop; k < my_tiles && k < k_stop + NS; ++k) {
+      const int s = k % NS;
+      mbar_wait_bounded(&wbar[s], (k / NS) & 1, kWaitCycles);
+    }
+  }
+
+  // ---- merge the 4 warps, write this CTA's partial ---------------------------
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+  }
+  if (g == 0) {
+    sm_m[warp * kMaxHeads + 2 * tig] = m0; sm_m[warp * kMaxHeads + 2 * tig + 1] = m1;
+    sm_l[warp * kMaxHeads + 2 * tig] = l0; sm_l[warp * kMaxHeads + 2 * tig + 1] = l1;
+  }
+  __syncthreads();  // all warps done with their stages; sm_m / sm_l complete
+  float f0, f1;
+  {
+    float M0 = -INFINITY, M1 = -INFINITY;
+    for (int w = 0; w < kWarps; ++w) {
+      M0 = fmaxf(M0, sm_m[w * kMaxHeads + 2 * tig]);
+      M1 = fmaxf(M1, sm_m[w * kMaxHeads + 2 * tig + 1]);
+    }
+    f0 = (m0 == -INFINITY) ? 0.0f : fast_exp2(m0 - M0);
+    f1 = (m1 == -INFINITY) ? 0.0f : fast_exp2(m1 - M1);
+  }
+  float* macc = reinterpret_cast<float*>(smem);  // [kWarps][8][D], reuses the stages
+#pragma unroll
+  for (int blk = 0; blk < NB; ++blk)
+#pragma unroll
+    for (int cc2 = 0; cc2 < 2; ++cc2) {
+      const int mt = 2 * blk + cc2;
+      const int cg = is_tail ? 16 * mt + g : 16 * mt + 2 * g;
+      const int cg8 = is_tail ? 16 * mt + g + 8 : 16 * mt + 2 * g + 1;
+      float* base = macc + (size_t)warp * kMaxHeads * D;
+      base[(2 * tig) * D + cg] = acc[blk][cc2][0] * f0;
+      base[(2 * tig + 1) * D + cg] = acc[blk][cc2][1] * f1;
+      base[(2 * tig) * D + cg8] = acc[blk][cc2][2] * f0;
+      base[(2 * tig + 1) * D + cg8] = acc[blk][cc2][3] * f1;
+    }
+  __syncthreads();
+  for (int i = tid; i < nheads * D; i += kThreads) {
+    const int hh = i / D, c = i % D;
+    float v = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) v += macc[((size_t)w * kMaxHeads + hh) * D + c];
+    p.ws_acc[(((size_t)b * p.n_q_heads + head0 + hh) * p.splits + split) * D + c] = v;
+  }
+  if (tid < nheads) {
+    float M = -INFINITY;
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w * kMaxHeads + tid]);
+    float L = 0.0f;
+    for (int w = 0; w < kWarps; ++w) {
+      const float mw = sm_m[w * kMaxHeads + tid];
+      if (mw != -INFINITY) L += sm_l[w * kMaxHeads + tid] * fast_exp2(mw - M);
+    }
+    ml[(size_t)tid * p.splits * 2] = M;
+    ml[(size_t)tid * p.splits * 2 + 1] = L;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Split merge + inverse rotation: one CTA of 256 threads per (sequence, query
+// head).  The split weights 2^(m_s - M) go to shared memory; then every thread
+// owns channels (D <= 256: a group of 256 / D threads shares a channel and takes
+// every (256/D)-th split), so all partial loads of a row are independent and
+// coalesced; splits with weight 0 (no keys) are skipped, their rows were never
+// written; warp 0 rotates the merged row back.
+// ---------------------------------------------------------------------------
+constexpr int kCombineThreads = 256;
+
+template <int D>
+__global__ void __launch_bounds__(kCombineThreads)
+decode_combine_kernel(const float* __restrict__ ws_acc, const float* __restrict__ ws_ml, int splits,
+                      int rot_v, void* __restrict__ out, int out_dtype) {
+  constexpr int G = (D >= 64 && D % 64 == 0) ? (((D & (D - 1)) == 0) ? D : 64) : 32;
+  constexpr int E = D / 32;
+  constexpr int TPC = kCombineThreads / D >= 1 ? kCombineThreads / D : 1;  // threads per channel
+  extern __shared__ float s_w[];                 // [splits] weights
+  __shared__ float s_part[kCombineThreads];      // per-thread partial sums, then the merged row
+  __shared__ float s_red[2][kCombineThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int row = blockIdx.x;  // b * Hq + h
+  const float* ml = ws_ml + (size_t)row * splits * 2;
+  // 1. M = max over non-empty splits
+  float M = -INFINITY;
+  for (int s = tid; s < splits; s += kCombineThreads)
+    if (ml[2 * s + 1] > 0.0f) M = fmaxf(M, ml[2 * s]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (lane == 0) s_red[0][warp] = M;
+  __syncthreads();
+  M = s_red[0][0];
+#pragma unroll
+  for (int w = 1; w < kCombineThreads / 32; ++w) M = fmaxf(M, s_red[0][w]);
+  // 2. weights and L = sum of l_s * weight
+  float L = 0.0f;
+  for (int s = tid; s < splits; s += kCombineThreads) {
+    const float l = ml[2 * s + 1];
+    const float w = l > 0.0f ? exp2f(ml[2 * s] - M) : 0.0f;
+    s_w[s] = w;
+    L += l * w;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+  if (lane == 0) s_red[1][warp] = L;
+  __syncthreads();
+  L = 0.0f;
+#pragma unroll
+  for (int w = 0; w < kCombineThreads / 32; ++w) L += s_red[1][w];
+  // 3. channel c of this thread, splits sub, sub + TPC, ...
+  const int c = tid % D, sub = tid / D;
+  float v = 0.0f;
+  if (tid < D * TPC) {
+    const float* a = ws_acc + (size_t)row * splits * D + c;
+    for (int s = sub; s < splits; s += TPC) {
+      const float w = s_w[s];
+      if (w != 0.0f) v += w * a[(size_t)s * D];  // empty splits never wrote their row: do not read it
+    }
+  }
+  s_part[tid] = v;
+  __syncthreads();
+  // 4. warp 0: merged row / L, inverse rotation, store
+  if (warp != 0) return;
+  const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+  float x[E];
+#pragma unroll
+  for (int j = 0; j < E; ++j) {
+    const int ch = fwht_channel<D, G>(lane, j);
+    float t = 0.0f;
+#pragma unroll
+    for (int u = 0; u < TPC; ++u) t += s_part[u * D + ch];
+    x[j] = t * inv;
+  }
+  if (rot_v) {
+    warp_fwht<D, G>(x, lane);
+#pragma unroll
+    for (int j = 0; j < E; ++j) x[j] *= inv_sqrt_group<G>();
+  }
+#pragma unroll
+  for (int j = 0; j < E; ++j) {
+    const size_t e = (size_t)row * D + fwht_channel<D, G>(lane, j);
+    if (out_dtype == KVQ_F32) static_cast<float*>(out)[e] = x[j];
+    else if (out_dtype == KVQ_BF16) static_cast<__nv_bfloat16*>(out)[e] = __float2bfloat16_rn(x[j]);
+    else static_cast<__half*>(out)[e] = __float2half_rn(x[j]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+CUtensorMapSwizzle swizzle_for(int w) {
+  return w == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : (w == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+}
+
+// rows x row_bytes plane of `elem` sized elements, boxes of box_w bytes x box_rows.
+bool make_map(CUtensorMap* m, void* base, CUtensorMapDataType dt, int elem, long long rows, int row_bytes,
+              int box_w_bytes, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cuuint64_t(row_bytes / elem), cuuint64_t(rows)};
+  cuuint64_t strides[1] = {cuuint64_t(row_bytes)};
+  cuuint32_t box[2] = {cuuint32_t(box_w_bytes / elem), cuuint32_t(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(box_w_bytes),
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, int KT, int VT>
+cudaError_t run_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, const void* q, int q_dtype,
+                       int n_q_heads, float scale, void* out, int out_dtype, void* ws, cudaStream_t st) {
+  using Cf = Cfg<D, KT, VT>;
+  Params p{};
+  p.k_d = static_cast<const uint8_t*>(c.k_d); p.v_d = static_cast<const uint8_t*>(c.v_d);
+  p.k_qh = static_cast<const uint32_t*>(c.k_qh); p.v_qh = static_cast<const uint32_t*>(c.v_qh);
+  p.seq_len = c.seq_len; p.status = c.status; p.q = q;
+  const size_t nacc = (size_t)c.batch * n_q_heads * plan.splits * D;
+  p.ws_acc = static_cast<float*>(ws);
+  p.ws_ml = p.ws_acc + nacc;
+  p.n_kv_heads = c.n_kv_heads; p.max_ctx = c.max_ctx; p.tail_len = c.tail_len;
+  p.q_dtype = q_dtype; p.n_q_heads = n_q_heads; p.group = n_q_heads / c.n_kv_heads;
+  p.heads_per_cta = plan.heads_per_cta; p.head_groups = plan.head_groups;
+  p.rot_k = rot.k;
+  p.scale_log2 = scale * kLog2e;
+  p.chunk = plan.chunk; p.tail_chunk = plan.tail_chunk; p.splits_body = plan.splits_body; p.splits_tail = plan.splits_tail; p.splits = plan.splits;
+
+  alignas(64) CUtensorMap mk, mv, mkt, mvt;
+  memset(&mk, 0, sizeof(mk)); memset(&mv, 0, sizeof(mv)); memset(&mkt, 0, sizeof(mkt)); memset(&mvt, 0, sizeof(mvt));
+  const long long rows = (long long)c.batch * c.n_kv_heads * c.max_ctx;
+  if (!make_map(&mk, c.k_qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, rows, Cf::rowK, Cf::WK, 16)) return cudaErrorInvalidValue;
+  if (!make_map(&mv, c.v_qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, rows, Cf::rowV, Cf::WV, 16)) return cudaErrorInvalidValue;
+  if (c.tail_len > 0) {
+    const long long trows = (long long)c.batch * c.n_kv_heads * c.tail_len;
+    if (!make_map(&mkt, c.k_tail, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, trows, 2 * D, Cf::WT, Cf::TT) ||
+        !make_map(&mvt, c.v_tail, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, trows, 2 * D, Cf::WT, Cf::TT))
+      return cudaErrorInvalidValue;
+  }
+  auto kern = decode_split_kernel<D, KT, VT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(plan.splits, c.n_kv_heads * plan.head_groups, c.batch);
+  kern<<<grid, kThreads, Cf::smem, st>>>(p, mk, mv, mkt, mvt);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int total = c.batch * n_q_heads;
+  const size_t wbytes = (size_t)plan.splits * sizeof(float);
+  if (wbytes > 48 * 1024) {
+    e = cudaFuncSetAttribute(decode_combine_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wbytes);
+    if (e != cudaSuccess) return e;
+  }
+  decode_combine_kernel<D><<<total, kCombineThreads, wbytes, st>>>(p.ws_acc, p.ws_ml, plan.splits, rot.v, out, out_dtype);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t run_decode_d(const kvq_cache& c, Rot rot, const DecodePlan& plan, const void* q, int q_dtype, int nq,
+                         float scale, void* out, int out_dtype, void* ws, cudaStream_t st) {
+#define KVQ_CASE(KT, VT)                                                                          \
+  if (c.k_type == KT && c.v_type == VT)                                                           \
+    return run_decode<D, KT, VT>(c, rot, plan, q, q_dtype, nq, scale, out, out_dtype, ws, st);
+#define KVQ_CASES_K(KT) KVQ_CASE(KT, KVQ_TYPE_Q4_0) KVQ_CASE(KT, KVQ_TYPE_Q5_0) KVQ_CASE(KT, KVQ_TYPE_Q8_0) \
+                        KVQ_CASE(KT, KVQ_TYPE_Q4_1) KVQ_CASE(KT, KVQ_TYPE_Q5_1)
+  KVQ_CASES_K(KVQ_TYPE_Q4_0) KVQ_CASES_K(KVQ_TYPE_Q5_0) KVQ_CASES_K(KVQ_TYPE_Q8_0)
+  KVQ_CASES_K(KVQ_TYPE_Q4_1) KVQ_CASES_K(KVQ_TYPE_Q5_1)
+#undef KVQ_CASES_K
+#undef KVQ_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+}  // namespace kvq

@@ -26,6 +26,18 @@ template <> struct Fmt<KVQ_TYPE_Q4_0> { static constexpr int qs_per_block = 16; 
 template <> struct Fmt<KVQ_TYPE_Q5_0> { static constexpr int qs_per_block = 16; static constexpr bool has_qh = true; };
 template <> struct Fmt<KVQ_TYPE_Q8_0> { static constexpr int qs_per_block = 32; static constexpr bool has_qh = false; };
 
+// per-type facts used by every kernel
+__host__ __device__ constexpr bool type_has_qh(int qt) { return qt == KVQ_TYPE_Q5_0 || qt == KVQ_TYPE_Q5_1; }
+__host__ __device__ constexpr bool type_has_min(int qt) { return qt == KVQ_TYPE_Q4_1 || qt == KVQ_TYPE_Q5_1; }
+// code offset of the _0 types (value = (code - offset) * d); 0 for q8_0 and the _1 types
+__host__ __device__ constexpr int type_code_offset(int qt) {
+  return qt == KVQ_TYPE_Q4_0 ? 8 : (qt == KVQ_TYPE_Q5_0 ? 16 : 0);
+}
+// bytes of one GGUF array-of-structs block
+__host__ __device__ constexpr int type_block_bytes(int qt) {
+  return qt == KVQ_TYPE_Q4_0 ? 18 : qt == KVQ_TYPE_Q5_0 ? 22 : qt == KVQ_TYPE_Q8_0 ? 34 : qt == KVQ_TYPE_Q4_1 ? 20 : 24;
+}
+
 __host__ __device__ inline int qs_row_bytes(int qt, int d) { return qt == KVQ_TYPE_Q8_0 ? d : d / 2; }
 
 // ---------------------------------------------------------------------------

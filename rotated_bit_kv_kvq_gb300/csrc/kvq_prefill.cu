@@ -95,7 +95,7 @@ static_assert(PL<128>::smem <= 232448, "prefill shared memory over the per-CTA l
 
 struct SParams {
   const uint8_t* k_qs; const uint8_t* v_qs;
-  const __half* k_d; const __half* v_d;
+  const uint8_t* k_d; const uint8_t* v_d;   // fp16 d per block, or (d, lo) pairs for q4_1 / q5_1
   const uint32_t* k_qh; const uint32_t* v_qh;
   const uint16_t* k_tail; const uint16_t* v_tail;
   const int32_t* seq_len; const int32_t* q_pos0;
@@ -152,7 +152,10 @@ __device__ __forceinline__ void load8(const SParams& p, bool is_v, int qt, bool 
     return;
   }
   const int c0 = ch * 8, blk = c0 / 32, w = c0 % 32;
-  const float sc = __half2float((is_v ? p.v_d : p.k_d)[body_row * NB + blk]) * kInvScale;
+  const int hb = type_has_min(qt) ? 2 : 1;  // halves per block header
+  const __half* hdr = reinterpret_cast<const __half*>(is_v ? p.v_d : p.k_d) + (body_row * NB + blk) * hb;
+  const float sc = __half2float(hdr[0]) * kInvScale;
+  const float mn = type_has_min(qt) ? __half2float(hdr[1]) * kInvScale : 0.0f;  // x = code*d + lo
   const uint8_t* qs = is_v ? p.v_qs : p.k_qs;
   if (qt == KVQ_TYPE_Q8_0) {
     const uint2 a = *reinterpret_cast<const uint2*>(qs + body_row * D + c0);
@@ -163,16 +166,13 @@ __device__ __forceinline__ void load8(const SParams& p, bool is_v, int qt, bool 
     const uint2 a = *reinterpret_cast<const uint2*>(qs + body_row * (D / 2) + blk * 16 + (w & 15));
     const int shift = w < 16 ? 0 : 4;
     uint32_t qh = 0;
-    int off = 8;
-    if (qt == KVQ_TYPE_Q5_0) {
-      qh = (is_v ? p.v_qh : p.k_qh)[body_row * NB + blk];
-      off = 16;
-    }
+    const int off = type_code_offset(qt);
+    if (type_has_qh(qt)) qh = (is_v ? p.v_qh : p.k_qh)[body_row * NB + blk];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const uint32_t byte = ((e < 4 ? a.x : a.y) >> (8 * (e & 3))) & 0xFFu;
       const int code = int((byte >> shift) & 15u) | int(((qh >> (w + e)) & 1u) << 4);
-      x[e] = float(code - off) * sc;
+      x[e] = __fadd_rn(__fmul_rn(float(code - off), sc), mn);
     }
   }
 }
@@ -603,7 +603,7 @@ cudaError_t run_prefill(const kvq_cache& c, Rot rot, const void* q, int q_dtype,
   const int max_tiles = c.max_ctx / kPN;
   SParams sp{};
   sp.k_qs = static_cast<const uint8_t*>(c.k_qs); sp.v_qs = static_cast<const uint8_t*>(c.v_qs);
-  sp.k_d = static_cast<const __half*>(c.k_d); sp.v_d = static_cast<const __half*>(c.v_d);
+  sp.k_d = static_cast<const uint8_t*>(c.k_d); sp.v_d = static_cast<const uint8_t*>(c.v_d);
   sp.k_qh = static_cast<const uint32_t*>(c.k_qh); sp.v_qh = static_cast<const uint32_t*>(c.v_qh);
   sp.k_tail = static_cast<const uint16_t*>(c.k_tail); sp.v_tail = static_cast<const uint16_t*>(c.v_tail);
   sp.seq_len = c.seq_len; sp.q_pos0 = q_pos0;

@@ -24,8 +24,9 @@ KVQ_ERR_CUDA = -4
 KVQ_ERR_TIMEOUT = -5
 KVQ_ERR_DEVICE_RANGE = -6
 
-KVQ_TYPE_Q4_0, KVQ_TYPE_Q5_0, KVQ_TYPE_Q8_0 = 0, 1, 2
-TYPE_IDS = {"q4_0": KVQ_TYPE_Q4_0, "q5_0": KVQ_TYPE_Q5_0, "q8_0": KVQ_TYPE_Q8_0}
+KVQ_TYPE_Q4_0, KVQ_TYPE_Q5_0, KVQ_TYPE_Q8_0, KVQ_TYPE_Q4_1, KVQ_TYPE_Q5_1 = 0, 1, 2, 3, 4
+TYPE_IDS = {"q4_0": KVQ_TYPE_Q4_0, "q5_0": KVQ_TYPE_Q5_0, "q8_0": KVQ_TYPE_Q8_0,
+            "q4_1": KVQ_TYPE_Q4_1, "q5_1": KVQ_TYPE_Q5_1}
 KVQ_F32, KVQ_BF16, KVQ_F16 = 0, 1, 2
 KVQ_ROT_AUTO, KVQ_ROT_K_OFF, KVQ_ROT_V_OFF = 1, 2, 4
 KVQ_INPUT_PREROTATED = 1

@@ -54,7 +54,7 @@ def test_plane_bytes(built_lib_path):
     c5 = _desc(k_type="q5_0", v_type="q5_0")
     assert kvq.kvq_plane_bytes(c5, kvq.KVQ_PLANE_V_QH) == rows * 4 * 4
     # packed bytes per token-head equal the GGUF block sizes (18 / 22 / 34 per 32 values)
-    for qt, blk in (("q4_0", 18), ("q5_0", 22), ("q8_0", 34)):
+    for qt, blk in (("q4_0", 18), ("q5_0", 22), ("q8_0", 34), ("q4_1", 20), ("q5_1", 24)):
         c = _desc(k_type=qt, v_type=qt)
         per = sum(kvq.kvq_plane_bytes(c, p) for p in (kvq.KVQ_PLANE_K_QS, kvq.KVQ_PLANE_K_QH, kvq.KVQ_PLANE_K_D))
         assert per == rows * (128 // 32) * blk
@@ -87,9 +87,9 @@ def _full_desc(**kw):
     c = _desc(**kw)
     for name in ("k_qs", "k_d", "v_qs", "v_d", "seq_len", "status", "k_tail", "v_tail"):
         setattr(c, name, FAKE)
-    if c.k_type == kvq.KVQ_TYPE_Q5_0:
+    if c.k_type in (kvq.KVQ_TYPE_Q5_0, kvq.KVQ_TYPE_Q5_1):
         c.k_qh = FAKE
-    if c.v_type == kvq.KVQ_TYPE_Q5_0:
+    if c.v_type in (kvq.KVQ_TYPE_Q5_0, kvq.KVQ_TYPE_Q5_1):
         c.v_qh = FAKE
     if c.tail_len == 0:
         c.k_tail = None
@@ -109,10 +109,14 @@ def test_cache_check_rejections(built_lib_path):
     assert L.kvq_cache_check(ctypes.byref(c)) == kvq.KVQ_ERR_INVALID_ARG
     c = _full_desc(k_type="q5_0"); c.k_qh = None          # q5_0 without its qh plane
     assert L.kvq_cache_check(ctypes.byref(c)) == kvq.KVQ_ERR_INVALID_ARG
+    c = _full_desc(v_type="q5_1"); c.v_qh = None          # q5_1 without its qh plane
+    assert L.kvq_cache_check(ctypes.byref(c)) == kvq.KVQ_ERR_INVALID_ARG
+    c = _full_desc(k_type="q4_1"); c.k_qh = FAKE          # qh given for a q4_1 plane
+    assert L.kvq_cache_check(ctypes.byref(c)) == kvq.KVQ_ERR_INVALID_ARG
     c = _full_desc(tail_len=0); c.k_tail = FAKE
     assert L.kvq_cache_check(ctypes.byref(c)) == kvq.KVQ_ERR_INVALID_ARG
     for bad in (dict(head_dim=48), dict(head_dim=512), dict(max_ctx=100), dict(batch=0), dict(tail_len=-1),
-                dict(k_type=7), dict(flags=8)):
+                dict(k_type=7), dict(v_type=5), dict(flags=8)):
         assert L.kvq_cache_check(ctypes.byref(_full_desc(**bad))) == kvq.KVQ_ERR_INVALID_ARG, bad
 
 

@@ -40,14 +40,14 @@ def _inputs(rng, B, n, H, d, scale=1.0):
     return x
 
 
-@pytest.mark.parametrize("qt", ["q4_0", "q5_0", "q8_0"])
+@pytest.mark.parametrize("qt", ["q4_0", "q5_0", "q8_0", "q4_1", "q5_1"])
 @pytest.mark.parametrize("d", [32, 64, 96, 128, 192, 256])
 def test_blocks_bit_exact_prerotated(qt, d):
     torch = require_gpu()
     from rotated_bit_kv_kvq_gb300 import kvq
     rng = np.random.default_rng(100 + d)
     B, H, n, T = 2, 3, 37, 8
-    other = {"q4_0": "q8_0", "q5_0": "q4_0", "q8_0": "q5_0"}[qt]
+    other = {"q4_0": "q8_0", "q5_0": "q4_1", "q8_0": "q5_1", "q4_1": "q5_0", "q5_1": "q4_0"}[qt]
     gc = kvq.KVCache(B, H, d, 64, T, qt, other)
     oc = ko.OracleCache(B, H, d, 64, T, qt, other, ko.rotation_enabled(d), ko.rotation_enabled(d))
     k = _inputs(rng, B, n, H, d)
@@ -140,7 +140,7 @@ def test_gpu_rotation_against_oracle(in_dtype, d):
     x[..., 5] *= 20
     xd = to_dev(x, in_dtype, torch)
     xin = xd.float().cpu().numpy()            # the values the GPU actually received
-    for qt in ("q4_0", "q5_0", "q8_0"):
+    for qt in ("q4_0", "q5_0", "q8_0", "q4_1", "q5_1"):
         gc = kvq.KVCache(B, H, d, 64, T, qt, qt)
         oc = ko.OracleCache(B, H, d, 64, T, qt, qt, True, True)
         kvq.kvq_rotate_quantize_append(gc.desc, xd, xd)
@@ -151,7 +151,7 @@ def test_gpu_rotation_against_oracle(in_dtype, d):
             for h in range(H):
                 got = gpu_values(gc, b, h, 0, 0, n, d, torch)
                 exp = oc.body_values("k", b, h, 0, n)
-                dq = ko.f16_value(oc.dbits["k"][b, h, :n]).repeat(32, axis=-1).reshape(n, d)
+                dq = ko.scale_and_min(qt, oc.dbits["k"][b, h, :n])[0].repeat(32, axis=-1).reshape(n, d)
                 diff = got != exp
                 flips += int(diff.sum())
                 total += got.size
@@ -169,6 +169,7 @@ def test_gpu_rotation_against_oracle(in_dtype, d):
         # back in the original basis the values are x up to the quantization error
         back = gpu_values(gc, 0, 0, 0, 0, n, d, torch, original_basis=True)
         amax = np.abs(ko.rotate(xin[0, :, 0])).reshape(n, d // 32, 32).max(-1)
-        step = {"q4_0": 1 / 8, "q5_0": 1 / 16, "q8_0": 1 / 127}[qt]
+        # quantization step relative to the block's largest magnitude (range / levels for the _1 types)
+        step = {"q4_0": 1 / 8, "q5_0": 1 / 16, "q8_0": 1 / 127, "q4_1": 2 / 15, "q5_1": 2 / 31}[qt]
         err = np.linalg.norm(back - xin[0, :, 0], axis=-1)
         assert np.all(err <= np.sqrt(d) * (amax.max(-1) * step) * 1.01 + 1e-6)

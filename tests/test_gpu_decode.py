@@ -66,8 +66,8 @@ def _kv(rng, B, n, H, d):
     return k, v
 
 
-@pytest.mark.parametrize("kt", ["q4_0", "q5_0", "q8_0"])
-@pytest.mark.parametrize("vt", ["q4_0", "q5_0", "q8_0"])
+@pytest.mark.parametrize("kt", ["q4_0", "q5_0", "q8_0", "q4_1", "q5_1"])
+@pytest.mark.parametrize("vt", ["q4_0", "q5_0", "q8_0", "q4_1", "q5_1"])
 def test_every_format_pair(kt, vt):
     rng = np.random.default_rng(21)
     B, H, g, d, T = 2, 2, 4, 128, 48
@@ -79,7 +79,9 @@ def test_every_format_pair(kt, vt):
 
 
 @pytest.mark.parametrize("d,kt,vt", [(64, "q8_0", "q4_0"), (64, "q5_0", "q5_0"), (256, "q8_0", "q4_0"),
-                                     (256, "q4_0", "q5_0"), (256, "q8_0", "q8_0"), (192, "q4_0", "q4_0")])
+                                     (256, "q4_0", "q5_0"), (256, "q8_0", "q8_0"), (192, "q4_0", "q4_0"),
+                                     (64, "q4_1", "q5_1"), (256, "q5_1", "q4_1"), (256, "q8_0", "q5_1"),
+                                     (256, "q5_0", "q4_1")])
 def test_head_dims(d, kt, vt):
     rng = np.random.default_rng(22)
     B, H, g, T = 2, 2, 3, 40

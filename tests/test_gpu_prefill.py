@@ -56,8 +56,8 @@ def test_prompt_workload_reduced():
     assert_close(got, ref, what="prompt workload reduced")
 
 
-@pytest.mark.parametrize("kt", ["q4_0", "q5_0", "q8_0"])
-@pytest.mark.parametrize("vt", ["q4_0", "q8_0"])
+@pytest.mark.parametrize("kt", ["q4_0", "q5_0", "q8_0", "q4_1", "q5_1"])
+@pytest.mark.parametrize("vt", ["q4_0", "q8_0", "q4_1", "q5_1"])
 def test_format_pairs_causal(kt, vt):
     rng = np.random.default_rng(31)
     B, H, g, d, T, n = 2, 2, 4, 128, 40, 300
