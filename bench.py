@@ -38,7 +38,7 @@ sys.path.insert(0, ROOT)
 from rotated_bit_kv_kvq_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "quantized-KV decode attention: achieved HBM GB/s vs 8 TB/s; append tokens/s"
-BLOCK_BYTES = {"q4_0": 18, "q5_0": 22, "q8_0": 34}
+BLOCK_BYTES = {"q4_0": 18, "q5_0": 22, "q8_0": 34, "q4_1": 20, "q5_1": 24}
 
 
 # ---------------------------------------------------------------------------
@@ -322,7 +322,7 @@ def run_ours(args):
                          f"{int(dec_lens.max())}", "achieved": round(achieved, 1), "peak": peak,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "bytes_per_launch": int(dec_bytes), "ms_per_launch": round(dec_ms, 5),
-                         "traffic": recorded_traffic("kvq_decode.cu")},
+                         "traffic": recorded_traffic("kvq_decode_impl.cuh")},
             "append": {"tokens_per_s": round(w.batch * n_new / (app_ms * 1e-3), 1), "ms_per_call": round(app_ms, 5)},
             "e2e": {"value": round(world * per_step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                     "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -331,11 +331,55 @@ def run_ours(args):
         }
         if not args.no_prefill:
             line["prefill"] = run_prefill_bench(torch, kvq, max(5, K // 5), 3)
+        if not args.no_format_pairs:
+            del cache, ws
+            torch.cuda.empty_cache()
+            line["format_pairs"] = run_format_pairs(torch, kvq, w, max(5, K // 5), peak)
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# the same decode workload with the scale + minimum formats in the K/V pairs the
+# benchmark summary names (q5_0-q4_1, q8_0-q5_1): decode call alone, same context
+# ---------------------------------------------------------------------------
+FORMAT_PAIRS = (("q5_0", "q4_1"), ("q8_0", "q5_1"))
+
+
+def run_format_pairs(torch, kvq, w: wl.Workload, steps: int, peak: float):
+    import dataclasses
+    res = []
+    for kt, vt in FORMAT_PAIRS:
+        w2 = dataclasses.replace(w, k_type=kt, v_type=vt)
+        cache = kvq.KVCache(w2.batch, w2.n_kv_heads, w2.head_dim, w2.max_ctx(64), w2.tail_len, kt, vt)
+        _, _, gen = fill_cache(torch, kvq, cache, w2, w2.ctx, seed=7)
+        qs = [torch.randn(w2.batch, w2.n_q_heads, w2.head_dim, generator=gen, device="cuda").to(torch.bfloat16)
+              for _ in range(4)]
+        out = torch.empty(w2.batch, w2.n_q_heads, w2.head_dim, dtype=torch.bfloat16, device="cuda")
+        ws = torch.empty(kvq.kvq_decode_workspace_bytes(cache.desc, w2.n_q_heads), dtype=torch.uint8, device="cuda")
+        stream = torch.cuda.current_stream()
+        for i in range(3):
+            kvq.kvq_decode_attention(cache.desc, qs[i % 4], out, ws, stream=stream)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            kvq.kvq_decode_attention(cache.desc, qs[i % 4], out, ws, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        st, bits = kvq.kvq_sync_status(cache.desc)
+        assert st == 0, (st, bits)
+        ms = e0.elapsed_time(e1) / steps
+        nbytes = decode_bytes(w2, cache.seq_len.cpu().numpy())
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res.append({"k_type": kt, "v_type": vt, "ctx": w2.ctx, "ms_per_call": round(ms, 5),
+                    "bytes_per_call": int(nbytes), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)})
+        del cache, ws
+        torch.cuda.empty_cache()
+    return res
 
 
 # ---------------------------------------------------------------------------
@@ -495,6 +539,8 @@ def main():
                     help="context length override (a smaller case of the same workload, e.g. for ncu captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prompt-workload measurement")
+    ap.add_argument("--no-format-pairs", action="store_true",
+                    help="skip the decode measurement with the q4_1 / q5_1 format pairs")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     args = ap.parse_args()
     if args.warmup < 3:
