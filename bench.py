@@ -61,8 +61,11 @@ def decode_bytes(w: wl.Workload, lengths, q_bytes=2, out_bytes=2) -> int:
 
 
 def append_bytes(w: wl.Workload, n_new: int, in_bytes=2) -> int:
-    per = w.n_kv_heads * n_new * w.batch
-    return per * (2 * w.head_dim * in_bytes + token_bytes(w) + (2 * w.head_dim * 2 if w.tail_len else 0))
+    """Input K+V read, packed blocks written, and bf16 tail rows written (only the
+    last min(n_new, tail_len) tokens of a call reach the ring)."""
+    heads = w.n_kv_heads * w.batch
+    tail_tokens = min(n_new, w.tail_len)
+    return heads * (n_new * (2 * w.head_dim * in_bytes + token_bytes(w)) + tail_tokens * 2 * w.head_dim * 2)
 
 
 # ---------------------------------------------------------------------------
