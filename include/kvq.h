@@ -162,7 +162,8 @@ KVQ_API kvq_status kvq_resolve_rotation(const kvq_cache* c, int32_t* rot_k, int3
 /*
  * Rotate, quantize and append new tokens (write path).
  *   k, v          device [batch][n_new][n_kv_heads][head_dim] of in_dtype
- *   n_new         rows per sequence in k / v (>= 0; 0 is a no-op)
+ *   n_new         rows per sequence in k / v (>= 0; 0 is a no-op; batch * n_new *
+ *                 n_kv_heads * 2 must stay below 2^31, else KVQ_ERR_INVALID_ARG)
  *   n_new_per_seq device int32 [batch] or NULL: tokens actually appended for
  *                 sequence b (0 <= n_new_per_seq[b] <= n_new); rows past it
  *                 are ignored.  NULL means n_new for every sequence.

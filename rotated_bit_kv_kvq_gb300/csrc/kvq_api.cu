@@ -142,7 +142,7 @@ kvq_status kvq_rotate_quantize_append(const kvq_cache* c, const void* k, const v
   if (!valid_dtype(in_dtype) || n_new < 0 || (append_flags & ~KVQ_INPUT_PREROTATED)) return KVQ_ERR_INVALID_ARG;
   if (n_new == 0) return KVQ_OK;
   if (!k || !v || !aligned16(k) || !aligned16(v)) return KVQ_ERR_INVALID_ARG;
-  if ((long long)c->batch * n_new * c->n_kv_heads * 2 / 8 >= 0x7fffffffLL) return KVQ_ERR_INVALID_ARG;
+  if ((long long)c->batch * n_new * c->n_kv_heads * 2 > 0x7fffffffLL) return KVQ_ERR_INVALID_ARG;  // vectors < 2^31
   return from_cuda(kvq::launch_append(*c, r, k, v, in_dtype, n_new, n_new_per_seq, append_flags,
                                       static_cast<cudaStream_t>(stream)));
 }

@@ -189,12 +189,14 @@ append_kernel(kvq_cache c, int rot_k, int rot_v, const void* __restrict__ kin, c
   const long long tasks = (long long)c.batch * n_new * H * 2;
 
   if (warp < tasks) {
-    const int which = warp & 1;                       // 0 = K, 1 = V
-    const long long vec = warp >> 1;                  // (b * n_new + i) * H + h
-    const int h = int(vec % H);
-    const long long bi = vec / H;
-    const int i = int(bi % n_new);
-    const int b = int(bi / n_new);
+    // 32-bit index arithmetic (the host keeps the vector count below 2^31)
+    const unsigned wu = unsigned(warp);
+    const int which = int(wu & 1u);                   // 0 = K, 1 = V
+    const unsigned vec = wu >> 1;                     // (b * n_new + i) * H + h
+    const int h = int(vec % unsigned(H));
+    const unsigned bi = vec / unsigned(H);
+    const int i = int(bi % unsigned(n_new));
+    const int b = int(bi / unsigned(n_new));
     const int n0 = c.seq_len[b];
     const int nb = n_new_per_seq ? n_new_per_seq[b] : n_new;
     const bool ok = nb >= 0 && nb <= n_new && n0 >= 0 && (long long)n0 + nb <= c.max_ctx;
@@ -340,7 +342,7 @@ cudaError_t append_d(const kvq_cache& c, Rot rot, const void* k, const void* v, 
                      const int32_t* nps, uint32_t flags, cudaStream_t st) {
   const long long warps = (long long)c.batch * n_new * c.n_kv_heads * 2;
   const long long blocks = (warps + kAppendWarps - 1) / kAppendWarps;
-  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (warps > 0x7fffffffLL) return cudaErrorInvalidValue;
   const int pre = (flags & KVQ_INPUT_PREROTATED) ? 1 : 0;
   constexpr int G = (D >= 64 && D % 64 == 0) ? (((D & (D - 1)) == 0) ? D : 64) : 32;
   append_kernel<D, G><<<unsigned(blocks), kAppendWarps * 32, 0, st>>>(c, rot.k, rot.v, k, v, in_dtype, n_new, nps, pre);
