@@ -206,9 +206,14 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
     seq0 = cache.seq_len.clone()
 
+    # one step = kvq_append_decode: the new token is written inside the decode launch
+    # (split + merge kernels) when the workload allows it (tail present, <= 8 query heads
+    # per KV head, one tail split), else append + decode
+    fused = w.tail_len > 0 and n_new <= w.tail_len and w.group <= 8 and w.tail_len <= 4096
+    launches_per_step = 2 if fused else 3
+
     def step(i):
-        kvq.kvq_rotate_quantize_append(cache.desc, ks[i % P], vs[i % P], stream=stream)
-        kvq.kvq_decode_attention(cache.desc, qs[i % P], out, ws, stream=stream)
+        kvq.kvq_append_decode(cache.desc, ks[i % P], vs[i % P], qs[i % P], out, ws, stream=stream)
 
     def barrier():
         if world > 1:
@@ -277,8 +282,7 @@ def run_ours(args):
         dk.copy_(hk[i % P], non_blocking=True)
         dv.copy_(hv[i % P], non_blocking=True)
         dq.copy_(hq[i % P], non_blocking=True)
-        kvq.kvq_rotate_quantize_append(cache.desc, dk, dv, stream=stream)
-        kvq.kvq_decode_attention(cache.desc, dq, out, ws, stream=stream)
+        kvq.kvq_append_decode(cache.desc, dk, dv, dq, out, ws, stream=stream)
         hout.copy_(out, non_blocking=True)
         stream.synchronize()
 
@@ -329,7 +333,8 @@ def run_ours(args):
             "append": {"tokens_per_s": round(w.batch * n_new / (app_ms * 1e-3), 1), "ms_per_call": round(app_ms, 5)},
             "e2e": {"value": round(world * per_step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                     "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": 3 * K,
+            "gpu_launches": launches_per_step * K,
+            "step_call": "kvq_append_decode" + (" (append fused into the decode launch)" if fused else ""),
             "clocks": clk,
         }
         if not args.no_prefill:

@@ -229,6 +229,24 @@ KVQ_API kvq_status kvq_decode_attention_noalloc(const kvq_cache* c, const void* 
                                                 int32_t n_q_heads, float scale, void* out,
                                                 int32_t out_dtype, void* stream);
 
+/*
+ * One decode step: kvq_rotate_quantize_append(c, k, v, in_dtype, n_new,
+ * n_new_per_seq, append_flags) followed by kvq_decode_attention(c, q, ...),
+ * with the same arguments, results and errors as the two calls in sequence.
+ * When n_new <= tail_len, the query heads of a KV head fit one CTA (up to 8)
+ * and the tail fits one (tail_len <= 4096), the append runs inside the decode
+ * launch: the CTA that reads a (sequence, KV head)'s bf16 tail first writes
+ * the new tokens (body blocks and tail rows), and the merge kernel advances
+ * seq_len after every split has read it -- one launch pair instead of three
+ * kernels.  Otherwise the two calls run in sequence.  The workspace is the
+ * decode's (kvq_decode_workspace_bytes).  Library addition for serving loops:
+ * the pages describe the append and the attention, not this entry point.
+ */
+KVQ_API kvq_status kvq_append_decode(const kvq_cache* c, const void* k, const void* v, int32_t in_dtype,
+                                     int32_t n_new, const int32_t* n_new_per_seq, uint32_t append_flags,
+                                     const void* q, int32_t q_dtype, int32_t n_q_heads, float scale, void* out,
+                                     int32_t out_dtype, void* workspace, size_t ws_bytes, void* stream);
+
 /* Workspace bytes kvq_prefill_attention needs (a pure size query: no
  * pointer in *c is read): batch * n_kv_heads * (max_ctx / 64) tiles of
  * 512 * head_dim bytes each, i.e. 8 bytes per cached K+V element of the

@@ -171,6 +171,41 @@ kvq_status kvq_decode_attention(const kvq_cache* c, const void* q, int32_t q_dty
                                       static_cast<cudaStream_t>(stream)));
 }
 
+kvq_status kvq_append_decode(const kvq_cache* c, const void* k, const void* v, int32_t in_dtype, int32_t n_new,
+                             const int32_t* n_new_per_seq, uint32_t append_flags, const void* q, int32_t q_dtype,
+                             int32_t n_q_heads, float scale, void* out, int32_t out_dtype, void* workspace,
+                             size_t ws_bytes, void* stream) {
+  kvq_status s = check_cache(c);
+  if (s != KVQ_OK) return s;
+  kvq::Rot r{};
+  if ((s = resolve(c, &r)) != KVQ_OK) return s;
+  // the append's arguments
+  if (!valid_dtype(in_dtype) || n_new < 0 || (append_flags & ~KVQ_INPUT_PREROTATED)) return KVQ_ERR_INVALID_ARG;
+  if (n_new > 0 && (!k || !v || !aligned16(k) || !aligned16(v))) return KVQ_ERR_INVALID_ARG;
+  if ((long long)c->batch * n_new * c->n_kv_heads * 2 > 0x7fffffffLL) return KVQ_ERR_INVALID_ARG;
+  // the decode's arguments
+  if (!valid_dtype(q_dtype) || !valid_dtype(out_dtype)) return KVQ_ERR_INVALID_ARG;
+  if (n_q_heads <= 0 || n_q_heads % c->n_kv_heads || n_q_heads / c->n_kv_heads > 4096) return KVQ_ERR_INVALID_ARG;
+  if (!q || !out || !aligned16(q) || !aligned16(out)) return KVQ_ERR_INVALID_ARG;
+  if (!(scale >= 0.0f) || scale > 1e30f) return KVQ_ERR_INVALID_ARG;
+  if (!kvq::decode_supported(c->head_dim, c->k_type, c->v_type)) return KVQ_ERR_UNSUPPORTED;
+  const kvq::DecodePlan plan = kvq::plan_decode(*c, n_q_heads, sm_count());
+  if (!workspace || !aligned16(workspace) || ws_bytes < plan.ws_bytes) return KVQ_ERR_WORKSPACE;
+  if (plan.splits > 0x7fffffff || (long long)c->n_kv_heads * plan.head_groups > 65535) return KVQ_ERR_UNSUPPORTED;
+  const float sc = scale == 0.0f ? 1.0f / sqrtf(float(c->head_dim)) : scale;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (n_new > 0 && kvq::fused_step_ok(*c, plan, n_new)) {
+    const kvq::FusedAppend fa{k, v, in_dtype, n_new, n_new_per_seq, (append_flags & KVQ_INPUT_PREROTATED) ? 1 : 0};
+    return from_cuda(kvq::launch_decode(*c, r, plan, q, q_dtype, n_q_heads, sc, out, out_dtype, workspace, st, &fa));
+  }
+  // not fusable (or nothing to append): the two calls in sequence
+  if (n_new > 0) {
+    s = from_cuda(kvq::launch_append(*c, r, k, v, in_dtype, n_new, n_new_per_seq, append_flags, st));
+    if (s != KVQ_OK) return s;
+  }
+  return from_cuda(kvq::launch_decode(*c, r, plan, q, q_dtype, n_q_heads, sc, out, out_dtype, workspace, st));
+}
+
 kvq_status kvq_decode_attention_noalloc(const kvq_cache* c, const void* q, int32_t q_dtype, int32_t n_q_heads,
                                         float scale, void* out, int32_t out_dtype, void* stream) {
   kvq_status s = check_cache(c);

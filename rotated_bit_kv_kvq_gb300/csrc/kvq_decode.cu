@@ -65,13 +65,18 @@ DecodePlan plan_decode(const kvq_cache& c, int n_q_heads, int sm_count) {
   return pl;
 }
 
+bool fused_step_ok(const kvq_cache& c, const DecodePlan& plan, int n_new) {
+  return c.tail_len > 0 && n_new >= 0 && n_new <= c.tail_len && plan.head_groups == 1 && plan.splits_tail == 1;
+}
+
 cudaError_t launch_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, const void* q, int q_dtype,
-                          int n_q_heads, float scale, void* out, int out_dtype, void* ws, cudaStream_t st) {
+                          int n_q_heads, float scale, void* out, int out_dtype, void* ws, cudaStream_t st,
+                          const FusedAppend* fa) {
   switch (c.head_dim) {
-    case 64: return launch_decode_d64(c, rot, plan, q, q_dtype, n_q_heads, scale, out, out_dtype, ws, st);
-    case 128: return launch_decode_d128(c, rot, plan, q, q_dtype, n_q_heads, scale, out, out_dtype, ws, st);
-    case 256: return launch_decode_d256(c, rot, plan, q, q_dtype, n_q_heads, scale, out, out_dtype, ws, st);
-    case 192: return launch_decode_d192(c, rot, plan, q, q_dtype, n_q_heads, scale, out, out_dtype, ws, st);
+    case 64: return launch_decode_d64(c, rot, plan, q, q_dtype, n_q_heads, scale, out, out_dtype, ws, st, fa);
+    case 128: return launch_decode_d128(c, rot, plan, q, q_dtype, n_q_heads, scale, out, out_dtype, ws, st, fa);
+    case 256: return launch_decode_d256(c, rot, plan, q, q_dtype, n_q_heads, scale, out, out_dtype, ws, st, fa);
+    case 192: return launch_decode_d192(c, rot, plan, q, q_dtype, n_q_heads, scale, out, out_dtype, ws, st, fa);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -32,6 +32,7 @@
 
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
+#include "kvq_quant.cuh"
 
 namespace kvq {
 namespace {
@@ -96,7 +97,18 @@ struct Params {
   int rot_k;
   float scale_log2;                 // softmax scale * log2(e)
   int chunk, tail_chunk, splits_body, splits_tail, splits;
+  // fused step: new tokens written by the tail CTA (fused != 0)
+  int fused, rot_v;
+  FusedAppend fa;
+  kvq_cache cache;
 };
+
+// New tokens of sequence b in a fused step: the requested count if it fits, else 0.
+__device__ __forceinline__ int fused_count(const FusedAppend& fa, int n0, int b, int max_ctx, bool& ok) {
+  const int req = fa.n_new_per_seq ? fa.n_new_per_seq[b] : fa.n_new;
+  ok = req >= 0 && req <= fa.n_new && n0 >= 0 && (long long)n0 + req <= max_ctx;
+  return ok ? req : 0;
+}
 
 __device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
 
@@ -136,7 +148,14 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
   const int nheads = min(p.heads_per_cta, p.group - hg * p.heads_per_cta);
   const int split = blockIdx.x;
 
-  const int n = p.seq_len[b];
+  const int n0 = p.seq_len[b];
+  int nn = 0;  // tokens this launch appends to sequence b (fused step)
+  if (p.fused) {
+    bool ok;
+    nn = fused_count(p.fa, n0, b, p.max_ctx, ok);
+    if (!ok && tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(p.status, KVQ_DEV_ERR_APPEND_RANGE);
+  }
+  const int n = n0 + nn;
   const int T = p.tail_len;
   const int nbody = max(0, n - T);
   const int ntail = min(n, T);
@@ -206,7 +225,21 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     }
   };
 
-  __syncthreads();  // barriers initialised
+  // Fused step: this (sequence, KV head)'s only tail CTA writes the new tokens
+  // (body blocks and bf16 tail rows) before any tail tile is fetched.  Body CTAs
+  // never treat those positions as valid: they are >= n - T.  The proxy fence
+  // makes the stores visible to the tensor copies issued after the barrier.
+  if (p.fused && is_tail && nn > 0) {
+    constexpr int GQ = (D >= 64 && D % 64 == 0) ? (((D & (D - 1)) == 0) ? D : 64) : 32;
+    for (int t = warp; t < 2 * nn; t += kWarps) {
+      const int i = t >> 1, which = t & 1;
+      const bool rot = (which ? p.rot_v : p.rot_k) && !p.fa.prerotated;
+      store_vector<D, GQ>(p.cache, which, b, kvh, n0 + i, true, which ? p.fa.v : p.fa.k,
+                          (((size_t)b * p.fa.n_new + i) * p.n_kv_heads + kvh) * D, p.fa.in_dtype, rot, lane);
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+  }
+  __syncthreads();  // barriers initialised (and the fused step's tokens stored)
   if (lane == 0) {
     for (int k = 0; k < NS && k < my_tiles; ++k) issue(k);
   }
@@ -625,7 +658,8 @@ constexpr int kCombineThreads = 256;
 template <int D>
 __global__ void __launch_bounds__(kCombineThreads)
 decode_combine_kernel(const float* __restrict__ ws_acc, const float* __restrict__ ws_ml, int splits,
-                      int rot_v, void* __restrict__ out, int out_dtype) {
+                      int rot_v, void* __restrict__ out, int out_dtype, int n_q_heads, int fused,
+                      FusedAppend fa, int32_t* __restrict__ seq_len, int max_ctx) {
   constexpr int G = (D >= 64 && D % 64 == 0) ? (((D & (D - 1)) == 0) ? D : 64) : 32;
   constexpr int E = D / 32;
   constexpr int TPC = kCombineThreads / D >= 1 ? kCombineThreads / D : 1;  // threads per channel
@@ -634,6 +668,12 @@ decode_combine_kernel(const float* __restrict__ ws_acc, const float* __restrict_
   __shared__ float s_red[2][kCombineThreads / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int row = blockIdx.x;  // b * Hq + h
+  // fused step: every split CTA has read seq_len; advance it (head 0's CTA of each sequence)
+  if (fused && tid == 0 && row % n_q_heads == 0) {
+    const int b = row / n_q_heads;
+    bool ok;
+    seq_len[b] += fused_count(fa, seq_len[b], b, max_ctx, ok);
+  }
   const float* ml = ws_ml + (size_t)row * splits * 2;
   // 1. M = max over non-empty splits
   float M = -INFINITY;
@@ -737,7 +777,8 @@ bool make_map(CUtensorMap* m, void* base, CUtensorMapDataType dt, int elem, long
 
 template <int D, int KT, int VT>
 cudaError_t run_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, const void* q, int q_dtype,
-                       int n_q_heads, float scale, void* out, int out_dtype, void* ws, cudaStream_t st) {
+                       int n_q_heads, float scale, void* out, int out_dtype, void* ws, cudaStream_t st,
+                       const FusedAppend* fa) {
   using Cf = Cfg<D, KT, VT>;
   Params p{};
   p.k_d = static_cast<const uint8_t*>(c.k_d); p.v_d = static_cast<const uint8_t*>(c.v_d);
@@ -750,6 +791,10 @@ cudaError_t run_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, cons
   p.q_dtype = q_dtype; p.n_q_heads = n_q_heads; p.group = n_q_heads / c.n_kv_heads;
   p.heads_per_cta = plan.heads_per_cta; p.head_groups = plan.head_groups;
   p.rot_k = rot.k;
+  p.rot_v = rot.v;
+  p.fused = fa ? 1 : 0;
+  if (fa) p.fa = *fa;
+  p.cache = c;
   p.scale_log2 = scale * kLog2e;
   p.chunk = plan.chunk; p.tail_chunk = plan.tail_chunk; p.splits_body = plan.splits_body; p.splits_tail = plan.splits_tail; p.splits = plan.splits;
 
@@ -777,16 +822,17 @@ cudaError_t run_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, cons
     e = cudaFuncSetAttribute(decode_combine_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wbytes);
     if (e != cudaSuccess) return e;
   }
-  decode_combine_kernel<D><<<total, kCombineThreads, wbytes, st>>>(p.ws_acc, p.ws_ml, plan.splits, rot.v, out, out_dtype);
+  decode_combine_kernel<D><<<total, kCombineThreads, wbytes, st>>>(p.ws_acc, p.ws_ml, plan.splits, rot.v, out, out_dtype,
+                                                                   n_q_heads, p.fused, p.fa, c.seq_len, c.max_ctx);
   return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t run_decode_d(const kvq_cache& c, Rot rot, const DecodePlan& plan, const void* q, int q_dtype, int nq,
-                         float scale, void* out, int out_dtype, void* ws, cudaStream_t st) {
+                         float scale, void* out, int out_dtype, void* ws, cudaStream_t st, const FusedAppend* fa) {
 #define KVQ_CASE(KT, VT)                                                                          \
   if (c.k_type == KT && c.v_type == VT)                                                           \
-    return run_decode<D, KT, VT>(c, rot, plan, q, q_dtype, nq, scale, out, out_dtype, ws, st);
+    return run_decode<D, KT, VT>(c, rot, plan, q, q_dtype, nq, scale, out, out_dtype, ws, st, fa);
 #define KVQ_CASES_K(KT) KVQ_CASE(KT, KVQ_TYPE_Q4_0) KVQ_CASE(KT, KVQ_TYPE_Q5_0) KVQ_CASE(KT, KVQ_TYPE_Q8_0) \
                         KVQ_CASE(KT, KVQ_TYPE_Q4_1) KVQ_CASE(KT, KVQ_TYPE_Q5_1)
   KVQ_CASES_K(KVQ_TYPE_Q4_0) KVQ_CASES_K(KVQ_TYPE_Q5_0) KVQ_CASES_K(KVQ_TYPE_Q8_0)

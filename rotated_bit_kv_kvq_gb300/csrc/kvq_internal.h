@@ -45,13 +45,27 @@ DecodePlan plan_decode(const kvq_cache& c, int n_q_heads, int sm_count);
 // Address of the fixed decode scratch array on the current device (looked up
 // once per device); size in *bytes.
 cudaError_t decode_noalloc_scratch(void** ptr, size_t* bytes);
+// New tokens appended by the decode launch itself (the fused step): the one
+// tail CTA of each (sequence, KV head) writes them before its tail attention,
+// and the merge kernel advances seq_len.  Requires n_new <= tail_len, one head
+// group and one tail split (fused_step_ok).
+struct FusedAppend {
+  const void* k;
+  const void* v;
+  int in_dtype;
+  int n_new;
+  const int32_t* n_new_per_seq;  // device, may be NULL
+  int prerotated;
+};
+bool fused_step_ok(const kvq_cache& c, const DecodePlan& plan, int n_new);
 cudaError_t launch_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, const void* q,
                           int q_dtype, int n_q_heads, float scale, void* out, int out_dtype,
-                          void* ws, cudaStream_t st);
+                          void* ws, cudaStream_t st, const FusedAppend* fa = nullptr);
 // per-head_dim launchers (one translation unit each); 192 supports q4_0 / q4_0 only
 #define KVQ_DECODE_LAUNCHER(NAME)                                                                     \
   cudaError_t NAME(const kvq_cache& c, Rot rot, const DecodePlan& plan, const void* q, int q_dtype,  \
-                   int n_q_heads, float scale, void* out, int out_dtype, void* ws, cudaStream_t st);
+                   int n_q_heads, float scale, void* out, int out_dtype, void* ws, cudaStream_t st,  \
+                   const FusedAppend* fa);
 KVQ_DECODE_LAUNCHER(launch_decode_d64)
 KVQ_DECODE_LAUNCHER(launch_decode_d128)
 KVQ_DECODE_LAUNCHER(launch_decode_d192)

@@ -65,6 +65,10 @@ SIGNATURES = {
     "kvq_decode_attention_noalloc": (ctypes.c_int32, [_P, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                                                       ctypes.c_float, ctypes.c_void_p, ctypes.c_int32,
                                                       ctypes.c_void_p]),
+    "kvq_append_decode": (ctypes.c_int32, [_P, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                           ctypes.c_void_p, ctypes.c_uint32, ctypes.c_void_p, ctypes.c_int32,
+                                           ctypes.c_int32, ctypes.c_float, ctypes.c_void_p, ctypes.c_int32,
+                                           ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "kvq_prefill_workspace_bytes": (ctypes.c_size_t, [_P, ctypes.c_int32, ctypes.c_int32]),
     "kvq_prefill_attention": (ctypes.c_int32, [_P, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                                ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
@@ -157,6 +161,18 @@ def kvq_decode_attention(cache: kvq_cache, q, out, workspace, scale: float = 0.0
 
 
 KVQ_NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def kvq_append_decode(cache: kvq_cache, k, v, q, out, workspace, n_new_per_seq=None, prerotated=False,
+                      scale: float = 0.0, stream=None):
+    """One decode step: append k, v ([batch][n_new][kv_heads][head_dim]) then decode q
+    ([batch][n_q_heads][head_dim]) into out; fused into the decode launch when possible."""
+    wsb = workspace.numel() * workspace.element_size()
+    _check(lib().kvq_append_decode(ctypes.byref(cache), _ptr(k), _ptr(v), _dtype_id(k), k.shape[1],
+                                   _ptr(n_new_per_seq), KVQ_INPUT_PREROTATED if prerotated else 0,
+                                   _ptr(q), _dtype_id(q), q.shape[1], float(scale), _ptr(out), _dtype_id(out),
+                                   _ptr(workspace), wsb, _stream(stream)),
+           "kvq_append_decode")
 
 
 def kvq_decode_attention_noalloc(cache: kvq_cache, q, out, scale: float = 0.0, stream=None):
