@@ -810,7 +810,7 @@ cudaError_t run_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, cons
       return cudaErrorInvalidValue;
   }
   auto kern = decode_split_kernel<D, KT, VT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::smem);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), Cf::smem);
   if (e != cudaSuccess) return e;
   dim3 grid(plan.splits, c.n_kv_heads * plan.head_groups, c.batch);
   kern<<<grid, kThreads, Cf::smem, st>>>(p, mk, mv, mkt, mvt);
@@ -819,7 +819,7 @@ cudaError_t run_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, cons
   const int total = c.batch * n_q_heads;
   const size_t wbytes = (size_t)plan.splits * sizeof(float);
   if (wbytes > 48 * 1024) {
-    e = cudaFuncSetAttribute(decode_combine_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wbytes);
+    e = ensure_dynamic_smem(reinterpret_cast<const void*>(decode_combine_kernel<D>), (int)wbytes);
     if (e != cudaSuccess) return e;
   }
   decode_combine_kernel<D><<<total, kCombineThreads, wbytes, st>>>(p.ws_acc, p.ws_ml, plan.splits, rot.v, out, out_dtype,

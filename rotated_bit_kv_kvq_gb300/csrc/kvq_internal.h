@@ -5,6 +5,9 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
+#include <unordered_map>
+
 #include "kvq.h"
 
 namespace kvq {
@@ -22,6 +25,25 @@ inline int rotation_group(int d) {
 }
 
 size_t qs_row_bytes_host(int qt, int d);
+
+// Raises a kernel's dynamic shared-memory limit once per device (again only for
+// a larger size), so that steady-state calls make no attribute call and can be
+// captured into a CUDA graph.
+inline cudaError_t ensure_dynamic_smem(const void* kernel, int bytes) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static std::unordered_map<const void*, int[kMaxDevices]> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  std::lock_guard<std::mutex> lock(mu);
+  int& have = done[kernel][dev];
+  if (have >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) have = bytes;
+  return e;
+}
 
 // Launchers (arguments already validated by the API layer).
 cudaError_t launch_append(const kvq_cache& c, Rot rot, const void* k, const void* v, int in_dtype,

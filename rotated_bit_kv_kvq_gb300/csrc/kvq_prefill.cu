@@ -623,9 +623,9 @@ cudaError_t run_prefill(const kvq_cache& c, Rot rot, const void* q, int q_dtype,
   p.rot_k = rot.k; p.rot_v = rot.v;
   p.scale_log2 = scale * kPLog2e;
   constexpr int stage_smem = L::tile + 1024;
-  cudaError_t e = cudaFuncSetAttribute(stage_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, stage_smem);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(stage_kernel<D>), stage_smem);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::smem);
+  e = ensure_dynamic_smem(reinterpret_cast<const void*>(attn_kernel<D>), L::smem);
   if (e != cudaSuccess) return e;
   stage_kernel<D><<<dim3(max_tiles, c.n_kv_heads, c.batch), kStageThreads, stage_smem, st>>>(sp);
   e = cudaGetLastError();
