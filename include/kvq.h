@@ -87,6 +87,7 @@ typedef int32_t kvq_status;
 #define KVQ_INPUT_PREROTATED 1u  /* k / v are already rotated: store them as given */
 
 /* ---- planes of a cache (kvq_plane_bytes) --------------------------------- */
+/* body planes: rows [batch][kv_heads][max_ctx], or [n_pages][kv_heads][page_tokens] when paged */
 #define KVQ_PLANE_K_QS    0  /* uint8 [batch][kv_heads][max_ctx][qs_row]    qs_row = d (q8_0) or d/2 (the others) */
 #define KVQ_PLANE_K_QH    1  /* uint32 [batch][kv_heads][max_ctx][d/32]     q5_0 / q5_1 only (0 bytes otherwise)  */
 #define KVQ_PLANE_K_D     2  /* fp16 [batch][kv_heads][max_ctx][d/32]       block scales; q4_1 / q5_1: fp16 pairs
@@ -104,6 +105,7 @@ typedef int32_t kvq_status;
 #define KVQ_DEV_ERR_APPEND_RANGE  1u  /* an append would pass max_ctx, or n_new_per_seq[b] not in [0, n_new] */
 #define KVQ_DEV_ERR_PREFILL_RANGE 2u  /* a prefill query position is negative                              */
 #define KVQ_DEV_ERR_TIMEOUT       4u  /* a bounded wait on a shared-memory barrier gave up                 */
+#define KVQ_DEV_ERR_PAGE          8u  /* a page_table entry lies outside [0, n_pages) (paged layout)        */
 
 /*
  * The cache descriptor.  Body planes hold the packed payload of every block:
@@ -136,6 +138,19 @@ typedef struct kvq_cache {
   void* k_tail; void* v_tail;
   int32_t* seq_len;     /* device int32 [batch]                        */
   uint32_t* status;     /* device uint32 [4], zero-initialised         */
+  /* Paged layout (optional; page_tokens == 0 keeps the contiguous rows
+   * [batch][kv_heads][max_ctx] above).  Otherwise the body planes are one pool
+   * of n_pages pages shared by all sequences, rows [n_pages][kv_heads]
+   * [page_tokens], and position t of sequence b lives in page
+   * page_table[b * (max_ctx / page_tokens) + t / page_tokens] at row offset
+   * t % page_tokens.  max_ctx stays the logical capacity per sequence; the
+   * bf16 tail stays per sequence.  A page id outside [0, n_pages) met by a
+   * kernel sets KVQ_DEV_ERR_PAGE and that page reads as empty / is not
+   * written.  Library addition for serving batches (block-table allocation);
+   * the pages describe only the contiguous cache. */
+  int32_t page_tokens;        /* 0, or a multiple of 64 that divides max_ctx   */
+  int32_t n_pages;            /* pages in the pool (paged layout)              */
+  const int32_t* page_table;  /* device int32 [batch][max_ctx / page_tokens]   */
 } kvq_cache;
 
 /* Library version (KVQ_VERSION). */

@@ -27,14 +27,20 @@ bool shape_ok(const kvq_cache* c) {
   if (c->tail_len < 0 || c->tail_len > (1 << 24)) return false;
   if (!valid_type(c->k_type) || !valid_type(c->v_type)) return false;
   if (c->flags & ~(KVQ_ROT_AUTO | KVQ_ROT_K_OFF | KVQ_ROT_V_OFF)) return false;
+  // paged layout: pages of a multiple of 64 tokens that divide the capacity
+  if (c->page_tokens < 0 || c->n_pages < 0) return false;
+  if (c->page_tokens && (c->page_tokens % 64 || c->max_ctx % c->page_tokens || c->n_pages == 0)) return false;
+  if (!c->page_tokens && c->n_pages) return false;
   // every plane offset must stay below 2^62 bytes
   const double rows = double(c->batch) * c->n_kv_heads * c->max_ctx;
-  if (rows * c->head_dim * 2 > 4.0e18) return false;
+  const double prow = double(c->n_pages) * c->n_kv_heads * c->page_tokens;
+  if (rows * c->head_dim * 2 > 4.0e18 || prow * c->head_dim * 2 > 4.0e18) return false;
   return true;
 }
 
 size_t plane_bytes(const kvq_cache* c, int plane) {
-  const size_t rows = size_t(c->batch) * c->n_kv_heads * c->max_ctx;
+  const size_t rows = c->page_tokens ? size_t(c->n_pages) * c->n_kv_heads * c->page_tokens
+                                     : size_t(c->batch) * c->n_kv_heads * c->max_ctx;
   const size_t nb = size_t(c->head_dim) / 32;
   const size_t d = size_t(c->head_dim);
   switch (plane) {
@@ -57,6 +63,8 @@ kvq_status check_cache(const kvq_cache* c) {
   const void* must[] = {c->k_qs, c->k_d, c->v_qs, c->v_d, c->seq_len, c->status};
   for (const void* p : must)
     if (!p || !aligned16(p)) return KVQ_ERR_INVALID_ARG;
+  if (c->page_tokens && (!c->page_table || (reinterpret_cast<uintptr_t>(c->page_table) & 3u))) return KVQ_ERR_INVALID_ARG;
+  if (!c->page_tokens && c->page_table) return KVQ_ERR_INVALID_ARG;
   if (has_qh(c->k_type) != (c->k_qh != nullptr)) return KVQ_ERR_INVALID_ARG;
   if (has_qh(c->v_type) != (c->v_qh != nullptr)) return KVQ_ERR_INVALID_ARG;
   if (c->k_qh && !aligned16(c->k_qh)) return KVQ_ERR_INVALID_ARG;

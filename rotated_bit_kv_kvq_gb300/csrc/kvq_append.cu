@@ -98,7 +98,9 @@ debug_kernel(kvq_cache c, int rot_side, int seq, int kv_head, int which, int t0,
     for (int j = 0; j < E; ++j) v[j] = bf16_bits_to_f32(tp[fwht_channel<D, G>(lane, j)]);
   } else {
     const int qt = is_v ? c.v_type : c.k_type;
-    const size_t row = ((size_t)seq * H + kv_head) * c.max_ctx + pos;
+    const long long brow = body_row(row_map(c), seq, kv_head, pos);
+    if (brow < 0 && lane == 0) atomicOr(&c.status[0], KVQ_DEV_ERR_PAGE);
+    const size_t row = brow < 0 ? 0 : size_t(brow);  // an invalid page reads as row 0 (status set)
     const uint8_t* qs = static_cast<const uint8_t*>(is_v ? c.v_qs : c.k_qs) + row * qs_row_bytes(qt, D);
     const uint32_t* qh = static_cast<const uint32_t*>(is_v ? c.v_qh : c.k_qh);
     // block header: fp16 d, or for q4_1 / q5_1 the (d, lo) pair, as bytes

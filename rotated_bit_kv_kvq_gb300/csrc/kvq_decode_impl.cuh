@@ -101,6 +101,7 @@ struct Params {
   int fused, rot_v;
   FusedAppend fa;
   kvq_cache cache;
+  RowMap rows;   // body row of (sequence, KV head, position): contiguous or paged
 };
 
 // New tokens of sequence b in a fused step: the requested count if it fits, else 0.
@@ -210,7 +211,12 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
         tma_2d_g2s(st + C::off_vt + (x / C::WT) * C::TT * C::WT, &tmVt, x / 2, row, &wbar[s]);
       }
     } else {
-      const size_t row = bh * p.max_ctx + t0;
+      long long brow = body_row(p.rows, b, kvh, t0);  // a 16-token tile never crosses a page
+      if (brow < 0) {  // page id outside the pool: fetch row 0, the consumer masks the tile
+        atomicOr(p.status, KVQ_DEV_ERR_PAGE);
+        brow = 0;
+      }
+      const size_t row = size_t(brow);
       mbar_arrive_expect_tx(&wbar[s], C::body_tx);
 #pragma unroll
       for (int x = 0; x < C::rowK; x += C::WK)
@@ -330,7 +336,9 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     if (!__all_sync(0xffffffffu, arrived)) { timed_out = true; k_stop = k; break; }
     const uint8_t* st = wstage + s * C::stage;
     const int t0 = t_begin + (warp + k * kWarps) * TR;
-    const bool v0 = t0 + g < t_end, v8 = (TR == 16) && (t0 + g + 8 < t_end);
+    // positions past the end, or a whole tile whose page id lies outside the pool, are masked
+    const int t_lim = (!is_tail && body_row(p.rows, b, kvh, t0) < 0) ? t0 : t_end;
+    const bool v0 = t0 + g < t_lim, v8 = (TR == 16) && (t0 + g + 8 < t_lim);
 
     float S[4] = {0.f, 0.f, 0.f, 0.f};
     if (!is_tail) {
@@ -465,8 +473,8 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
       pt[0] = th0.x + tr0.x; pt[1] = th0.y + tr0.y; pt[2] = th1.x + tr1.x; pt[3] = th1.y + tr1.y;
     }
     const int tt = t0 + 2 * tig;  // first token of this lane's transposed rows
-    const bool vt0 = tt < t_end, vt1 = tt + 1 < t_end;
-    const bool vt8 = TR == 16 && tt + 8 < t_end, vt9 = TR == 16 && tt + 9 < t_end;
+    const bool vt0 = tt < t_lim, vt1 = tt + 1 < t_lim;
+    const bool vt8 = TR == 16 && tt + 8 < t_lim, vt9 = TR == 16 && tt + 9 < t_lim;
     if (!is_tail) {
       // V scales of the transposed tokens, read per block (0 for rows past the end)
       const __half* vd = reinterpret_cast<const __half*>(st + C::off_vd);
@@ -795,12 +803,13 @@ cudaError_t run_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, cons
   p.fused = fa ? 1 : 0;
   if (fa) p.fa = *fa;
   p.cache = c;
+  p.rows = row_map(c);
   p.scale_log2 = scale * kLog2e;
   p.chunk = plan.chunk; p.tail_chunk = plan.tail_chunk; p.splits_body = plan.splits_body; p.splits_tail = plan.splits_tail; p.splits = plan.splits;
 
   alignas(64) CUtensorMap mk, mv, mkt, mvt;
   memset(&mk, 0, sizeof(mk)); memset(&mv, 0, sizeof(mv)); memset(&mkt, 0, sizeof(mkt)); memset(&mvt, 0, sizeof(mvt));
-  const long long rows = (long long)c.batch * c.n_kv_heads * c.max_ctx;
+  const long long rows = body_rows(c);
   if (!make_map(&mk, c.k_qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, rows, Cf::rowK, Cf::WK, 16)) return cudaErrorInvalidValue;
   if (!make_map(&mv, c.v_qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, rows, Cf::rowV, Cf::WV, 16)) return cudaErrorInvalidValue;
   if (c.tail_len > 0) {

@@ -40,6 +40,29 @@ __host__ __device__ constexpr int type_block_bytes(int qt) {
 
 __host__ __device__ inline int qs_row_bytes(int qt, int d) { return qt == KVQ_TYPE_Q8_0 ? d : d / 2; }
 
+// Where the body row of logical position t of (sequence b, KV head h) lives:
+// contiguous rows [batch][kv_heads][max_ctx], or in the paged layout
+// [page][kv_heads][page_tokens] through the page table.
+struct RowMap {
+  int n_kv_heads, max_ctx, page_tokens, n_pages;
+  const int32_t* page_table;
+};
+__host__ __device__ inline RowMap row_map(const kvq_cache& c) {
+  return RowMap{c.n_kv_heads, c.max_ctx, c.page_tokens, c.n_pages, c.page_table};
+}
+// rows of the body planes (what a tensor map over a plane spans)
+__host__ __device__ inline long long body_rows(const kvq_cache& c) {
+  return c.page_tokens ? (long long)c.n_pages * c.n_kv_heads * c.page_tokens
+                       : (long long)c.batch * c.n_kv_heads * c.max_ctx;
+}
+// -1 when the page id is outside the pool
+__device__ __forceinline__ long long body_row(const RowMap& m, int b, int h, int t) {
+  if (m.page_tokens == 0) return ((long long)b * m.n_kv_heads + h) * m.max_ctx + t;
+  const int pg = m.page_table[(long long)b * (m.max_ctx / m.page_tokens) + t / m.page_tokens];
+  if (pg < 0 || pg >= m.n_pages) return -1;
+  return ((long long)pg * m.n_kv_heads + h) * m.page_tokens + t % m.page_tokens;
+}
+
 // ---------------------------------------------------------------------------
 // small utilities
 // ---------------------------------------------------------------------------

@@ -101,6 +101,8 @@ struct SParams {
   const int32_t* seq_len; const int32_t* q_pos0;
   int n_kv_heads, max_ctx, tail_len, k_type, v_type, n_tokens, causal, max_tiles;
   uint8_t* ws;
+  RowMap rows;   // body row of (sequence, KV head, position): contiguous or paged
+  uint32_t* status;
 };
 
 struct AParams {
@@ -194,9 +196,18 @@ __global__ void __launch_bounds__(kStageThreads) stage_kernel(SParams p) {
   const size_t bh = (size_t)b * p.n_kv_heads + kvh;
   const int key = threadIdx.x & (kPN - 1);   // a warp covers 32 consecutive keys
   const int t = j * kPN + key;
-  const bool valid = t < n;
+  bool valid = t < n;
   const bool tail = valid && T > 0 && t >= n - T;
-  const size_t body_row = bh * p.max_ctx + (valid ? t : 0);
+  long long brow = 0;
+  if (valid && !tail) {
+    brow = kvq::body_row(p.rows, b, kvh, t);
+    if (brow < 0) {  // page id outside the pool: the key reads as empty
+      atomicOr(p.status, KVQ_DEV_ERR_PAGE);
+      valid = false;
+      brow = 0;
+    }
+  }
+  const size_t body_row = size_t(brow);
   const size_t tail_row = tail ? bh * T + t % T : 0;
 #pragma unroll 1
   for (int ch = threadIdx.x / kPN; ch < NCH; ch += kStageThreads / kPN) {
@@ -610,6 +621,7 @@ cudaError_t run_prefill(const kvq_cache& c, Rot rot, const void* q, int q_dtype,
   sp.n_kv_heads = c.n_kv_heads; sp.max_ctx = c.max_ctx; sp.tail_len = c.tail_len;
   sp.k_type = c.k_type; sp.v_type = c.v_type; sp.n_tokens = n_tokens; sp.causal = causal ? 1 : 0;
   sp.max_tiles = max_tiles; sp.ws = static_cast<uint8_t*>(ws);
+  sp.rows = row_map(c); sp.status = c.status;
   AParams p{};
   p.ws = static_cast<const uint8_t*>(ws);
   p.seq_len = c.seq_len; p.status = c.status;

@@ -184,18 +184,23 @@ __device__ __forceinline__ void store_vector(const kvq_cache& c, int which, int 
     for (int j = 0; j < E; ++j) v[j] *= s;
   }
   const int qt = which ? c.v_type : c.k_type;
-  const size_t row = ((size_t)b * c.n_kv_heads + h) * c.max_ctx + pos;
-  uint8_t* qs = static_cast<uint8_t*>(which ? c.v_qs : c.k_qs) + row * qs_row_bytes(qt, D);
-  uint32_t* qh = static_cast<uint32_t*>(which ? c.v_qh : c.k_qh);
-  uint8_t* dp = static_cast<uint8_t*>(which ? c.v_d : c.k_d) + row * NB * (type_has_min(qt) ? 4 : 2);
-  constexpr int L = 32 / P;
-  const int r = lane % L;
+  const long long brow = body_row(row_map(c), b, h, pos);
+  if (brow < 0) {  // page id outside the pool: the body row is not written
+    if (lane == 0) atomicOr(&c.status[0], KVQ_DEV_ERR_PAGE);
+  } else {
+    const size_t row = size_t(brow);
+    uint8_t* qs = static_cast<uint8_t*>(which ? c.v_qs : c.k_qs) + row * qs_row_bytes(qt, D);
+    uint32_t* qh = static_cast<uint32_t*>(which ? c.v_qh : c.k_qh);
+    uint8_t* dp = static_cast<uint8_t*>(which ? c.v_d : c.k_d) + row * NB * (type_has_min(qt) ? 4 : 2);
+    constexpr int L = 32 / P;
+    const int r = lane % L;
 #pragma unroll
-  for (int gi = 0; gi < D / G; ++gi) {
-    const int blk = gi * P + lane / L;
-    const int blk_bytes = qt == KVQ_TYPE_Q8_0 ? 32 : 16;
-    quantize_block<P>(v + gi * P, qt, r, qs + blk * blk_bytes, qh ? qh + row * NB + blk : nullptr,
-                      dp + blk * (type_has_min(qt) ? 4 : 2));
+    for (int gi = 0; gi < D / G; ++gi) {
+      const int blk = gi * P + lane / L;
+      const int blk_bytes = qt == KVQ_TYPE_Q8_0 ? 32 : 16;
+      quantize_block<P>(v + gi * P, qt, r, qs + blk * blk_bytes, qh ? qh + row * NB + blk : nullptr,
+                        dp + blk * (type_has_min(qt) ? 4 : 2));
+    }
   }
   if (to_tail) {
     uint16_t* tail = static_cast<uint16_t*>(which ? c.v_tail : c.k_tail) +

@@ -32,7 +32,7 @@ KVQ_ROT_AUTO, KVQ_ROT_K_OFF, KVQ_ROT_V_OFF = 1, 2, 4
 KVQ_INPUT_PREROTATED = 1
 (KVQ_PLANE_K_QS, KVQ_PLANE_K_QH, KVQ_PLANE_K_D, KVQ_PLANE_V_QS, KVQ_PLANE_V_QH, KVQ_PLANE_V_D,
  KVQ_PLANE_K_TAIL, KVQ_PLANE_V_TAIL, KVQ_PLANE_SEQ_LEN, KVQ_PLANE_STATUS) = range(10)
-KVQ_DEV_ERR_APPEND_RANGE, KVQ_DEV_ERR_PREFILL_RANGE, KVQ_DEV_ERR_TIMEOUT = 1, 2, 4
+KVQ_DEV_ERR_APPEND_RANGE, KVQ_DEV_ERR_PREFILL_RANGE, KVQ_DEV_ERR_TIMEOUT, KVQ_DEV_ERR_PAGE = 1, 2, 4, 8
 
 
 class kvq_cache(ctypes.Structure):
@@ -44,6 +44,7 @@ class kvq_cache(ctypes.Structure):
         ("v_qs", ctypes.c_void_p), ("v_qh", ctypes.c_void_p), ("v_d", ctypes.c_void_p),
         ("k_tail", ctypes.c_void_p), ("v_tail", ctypes.c_void_p),
         ("seq_len", ctypes.c_void_p), ("status", ctypes.c_void_p),
+        ("page_tokens", ctypes.c_int32), ("n_pages", ctypes.c_int32), ("page_table", ctypes.c_void_p),
     ]
 
 
@@ -220,13 +221,15 @@ def kvq_resolve_rotation(cache: kvq_cache):
     return st, rk.value, rv.value
 
 
-def descriptor(batch, n_kv_heads, head_dim, max_ctx, tail_len, k_type, v_type, flags=KVQ_ROT_AUTO) -> kvq_cache:
+def descriptor(batch, n_kv_heads, head_dim, max_ctx, tail_len, k_type, v_type, flags=KVQ_ROT_AUTO,
+               page_tokens=0, n_pages=0) -> kvq_cache:
     """A descriptor with sizes and types only (pointers NULL)."""
     c = kvq_cache()
     c.batch, c.n_kv_heads, c.head_dim, c.max_ctx, c.tail_len = batch, n_kv_heads, head_dim, max_ctx, tail_len
     c.k_type = TYPE_IDS.get(k_type, k_type)
     c.v_type = TYPE_IDS.get(v_type, v_type)
     c.flags = flags
+    c.page_tokens, c.n_pages = page_tokens, n_pages
     return c
 
 
@@ -234,9 +237,21 @@ class KVCache:
     """The planes of one cache, allocated with torch on the current device."""
 
     def __init__(self, batch, n_kv_heads, head_dim, max_ctx, tail_len, k_type, v_type,
-                 flags=KVQ_ROT_AUTO, device="cuda"):
+                 flags=KVQ_ROT_AUTO, device="cuda", page_tokens=0, n_pages=0, page_table=None):
+        """page_tokens > 0: paged body planes, a pool of n_pages pages (default: batch *
+        max_ctx / page_tokens) and a page table (device int32 [batch][max_ctx / page_tokens];
+        default: sequence b owns pages b * per_seq ...)."""
         import torch
-        self.desc = descriptor(batch, n_kv_heads, head_dim, max_ctx, tail_len, k_type, v_type, flags)
+        if page_tokens and not n_pages:
+            n_pages = batch * (max_ctx // page_tokens)
+        self.desc = descriptor(batch, n_kv_heads, head_dim, max_ctx, tail_len, k_type, v_type, flags,
+                               page_tokens, n_pages)
+        if page_tokens:
+            per_seq = max_ctx // page_tokens
+            if page_table is None:
+                page_table = torch.arange(batch * per_seq, dtype=torch.int32, device=device)
+            self.page_table = page_table.to(device=device, dtype=torch.int32).contiguous()
+            self.desc.page_table = self.page_table.data_ptr()
         self.planes = {}
         names = ["k_qs", "k_qh", "k_d", "v_qs", "v_qh", "v_d", "k_tail", "v_tail", "seq_len", "status"]
         for idx, name in enumerate(names):

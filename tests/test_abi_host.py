@@ -58,6 +58,14 @@ def test_plane_bytes(built_lib_path):
         c = _desc(k_type=qt, v_type=qt)
         per = sum(kvq.kvq_plane_bytes(c, p) for p in (kvq.KVQ_PLANE_K_QS, kvq.KVQ_PLANE_K_QH, kvq.KVQ_PLANE_K_D))
         assert per == rows * (128 // 32) * blk
+    # paged: a pool of n_pages pages of page_tokens rows per KV head
+    cp = kvq.descriptor(2, 4, 128, 256, 32, "q8_0", "q4_0", page_tokens=64, n_pages=11)
+    assert kvq.kvq_plane_bytes(cp, kvq.KVQ_PLANE_K_QS) == 11 * 4 * 64 * 128
+    assert kvq.kvq_plane_bytes(cp, kvq.KVQ_PLANE_V_D) == 11 * 4 * 64 * 4 * 2
+    assert kvq.kvq_plane_bytes(cp, kvq.KVQ_PLANE_K_TAIL) == 2 * 4 * 32 * 128 * 2   # the tail is not paged
+    for bad in (dict(page_tokens=32, n_pages=4), dict(page_tokens=192, n_pages=4), dict(page_tokens=64, n_pages=0),
+                dict(page_tokens=0, n_pages=3)):
+        assert kvq.kvq_plane_bytes(kvq.descriptor(2, 4, 128, 256, 32, "q8_0", "q4_0", **bad), 0) == 0, bad
     assert kvq.kvq_plane_bytes(_desc(head_dim=100), 0) == 0
     assert kvq.kvq_plane_bytes(_desc(max_ctx=100), 0) == 0
 
@@ -114,6 +122,12 @@ def test_cache_check_rejections(built_lib_path):
     c = _full_desc(k_type="q4_1"); c.k_qh = FAKE          # qh given for a q4_1 plane
     assert L.kvq_cache_check(ctypes.byref(c)) == kvq.KVQ_ERR_INVALID_ARG
     c = _full_desc(tail_len=0); c.k_tail = FAKE
+    assert L.kvq_cache_check(ctypes.byref(c)) == kvq.KVQ_ERR_INVALID_ARG
+    c = _full_desc(); c.page_tokens, c.n_pages = 64, 8          # paged without a page table
+    assert L.kvq_cache_check(ctypes.byref(c)) == kvq.KVQ_ERR_INVALID_ARG
+    c.page_table = FAKE
+    assert L.kvq_cache_check(ctypes.byref(c)) == 0
+    c = _full_desc(); c.page_table = FAKE                        # a page table without pages
     assert L.kvq_cache_check(ctypes.byref(c)) == kvq.KVQ_ERR_INVALID_ARG
     for bad in (dict(head_dim=48), dict(head_dim=512), dict(max_ctx=100), dict(batch=0), dict(tail_len=-1),
                 dict(k_type=7), dict(v_type=5), dict(flags=8)):
