@@ -372,6 +372,8 @@ def run_ours(args):
             del cache, ws
             torch.cuda.empty_cache()
             line["format_pairs"] = run_format_pairs(torch, kvq, w, max(5, K // 5), peak)
+            line["paged"] = run_format_pairs(torch, kvq, w, max(5, K // 5), peak,
+                                             pairs=((w.k_type, w.v_type),), page_tokens=256)[0]
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
         print(json.dumps(line), flush=True)
@@ -386,12 +388,25 @@ def run_ours(args):
 FORMAT_PAIRS = (("q5_0", "q4_1"), ("q8_0", "q5_1"))
 
 
-def run_format_pairs(torch, kvq, w: wl.Workload, steps: int, peak: float):
+def run_format_pairs(torch, kvq, w: wl.Workload, steps: int, peak: float, pairs=FORMAT_PAIRS, page_tokens=0):
+    """Decode call alone at the workload's context for other K/V format pairs, or
+    (page_tokens > 0) from a paged cache whose pages are handed out in a shuffled
+    order (a pool with 5% spare pages)."""
     import dataclasses
     res = []
-    for kt, vt in FORMAT_PAIRS:
+    for kt, vt in pairs:
         w2 = dataclasses.replace(w, k_type=kt, v_type=vt)
-        cache = kvq.KVCache(w2.batch, w2.n_kv_heads, w2.head_dim, w2.max_ctx(64), w2.tail_len, kt, vt)
+        max_ctx = w2.max_ctx(64)
+        paged = {}
+        if page_tokens:
+            max_ctx = (max_ctx + page_tokens - 1) // page_tokens * page_tokens
+            per_seq = max_ctx // page_tokens
+            n_pages = w2.batch * per_seq + max(1, w2.batch * per_seq // 20)
+            g = torch.Generator()
+            g.manual_seed(5)
+            table = torch.randperm(n_pages, generator=g)[:w2.batch * per_seq].to(torch.int32)
+            paged = dict(page_tokens=page_tokens, n_pages=n_pages, page_table=table)
+        cache = kvq.KVCache(w2.batch, w2.n_kv_heads, w2.head_dim, max_ctx, w2.tail_len, kt, vt, **paged)
         _, _, gen = fill_cache(torch, kvq, cache, w2, w2.ctx, seed=7)
         qs = [torch.randn(w2.batch, w2.n_q_heads, w2.head_dim, generator=gen, device="cuda").to(torch.bfloat16)
               for _ in range(4)]
@@ -412,8 +427,12 @@ def run_format_pairs(torch, kvq, w: wl.Workload, steps: int, peak: float):
         ms = e0.elapsed_time(e1) / steps
         nbytes = decode_bytes(w2, cache.seq_len.cpu().numpy())
         gbs = nbytes / (ms * 1e-3) / 1e9
-        res.append({"k_type": kt, "v_type": vt, "ctx": w2.ctx, "ms_per_call": round(ms, 5),
-                    "bytes_per_call": int(nbytes), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)})
+        r = {"k_type": kt, "v_type": vt, "ctx": w2.ctx, "ms_per_call": round(ms, 5),
+             "bytes_per_call": int(nbytes), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)}
+        if page_tokens:
+            r["page_tokens"] = page_tokens
+            r["layout"] = "paged, shuffled page table"
+        res.append(r)
         del cache, ws
         torch.cuda.empty_cache()
     return res

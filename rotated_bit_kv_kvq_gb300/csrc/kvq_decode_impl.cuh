@@ -197,6 +197,8 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
   uint8_t* wstage = smem + warp * NS * C::stage;
   uint64_t* wbar = bars + warp * NS;
   const size_t bh = (size_t)b * p.n_kv_heads + kvh;
+  const bool paged = p.rows.page_tokens != 0;
+  uint32_t bad_stage = 0;  // lane 0: bit s set when the tile in stage s came from a page outside the pool
 
   auto issue = [&](int k) {  // tile k of this warp -> stage k % NS (lane 0 only)
     const int s = k % NS;
@@ -211,12 +213,18 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
         tma_2d_g2s(st + C::off_vt + (x / C::WT) * C::TT * C::WT, &tmVt, x / 2, row, &wbar[s]);
       }
     } else {
-      long long brow = body_row(p.rows, b, kvh, t0);  // a 16-token tile never crosses a page
-      if (brow < 0) {  // page id outside the pool: fetch row 0, the consumer masks the tile
-        atomicOr(p.status, KVQ_DEV_ERR_PAGE);
-        brow = 0;
+      size_t row = bh * p.max_ctx + t0;
+      if (paged) {  // a 16-token tile never crosses a page
+        const int pg = p.rows.page_table[(size_t)b * (p.max_ctx / p.rows.page_tokens) + t0 / p.rows.page_tokens];
+        const bool bad = pg < 0 || pg >= p.rows.n_pages;
+        bad_stage = (bad_stage & ~(1u << s)) | (bad ? (1u << s) : 0u);
+        if (bad) {  // outside the pool: fetch row 0, the consumer masks the tile
+          atomicOr(p.status, KVQ_DEV_ERR_PAGE);
+          row = 0;
+        } else {
+          row = ((size_t)pg * p.n_kv_heads + kvh) * p.rows.page_tokens + t0 % p.rows.page_tokens;
+        }
       }
-      const size_t row = size_t(brow);
       mbar_arrive_expect_tx(&wbar[s], C::body_tx);
 #pragma unroll
       for (int x = 0; x < C::rowK; x += C::WK)
@@ -337,7 +345,8 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     const uint8_t* st = wstage + s * C::stage;
     const int t0 = t_begin + (warp + k * kWarps) * TR;
     // positions past the end, or a whole tile whose page id lies outside the pool, are masked
-    const int t_lim = (!is_tail && body_row(p.rows, b, kvh, t0) < 0) ? t0 : t_end;
+    int t_lim = t_end;
+    if (paged && ((__shfl_sync(0xffffffffu, bad_stage, 0) >> s) & 1u)) t_lim = t0;
     const bool v0 = t0 + g < t_lim, v8 = (TR == 16) && (t0 + g + 8 < t_lim);
 
     float S[4] = {0.f, 0.f, 0.f, 0.f};
