@@ -269,6 +269,22 @@ __device__ __forceinline__ bool role_wait(uint64_t* bar, uint32_t parity, Sync* 
   return true;
 }
 
+// N consecutive 32-bit words from global memory, as one vector load when the
+// address is 4N-byte aligned (N = 1, 2 or 4).
+template <int N>
+__device__ __forceinline__ void ld_words(const uint32_t* src, uint32_t* dst) {
+  if constexpr (N == 4) {
+    const uint4 t = *reinterpret_cast<const uint4*>(src);
+    dst[0] = t.x; dst[1] = t.y; dst[2] = t.z; dst[3] = t.w;
+  } else if constexpr (N == 2) {
+    const uint2 t = *reinterpret_cast<const uint2*>(src);
+    dst[0] = t.x; dst[1] = t.y;
+  } else {
+    static_assert(N == 1, "1, 2 or 4 words");
+    dst[0] = *src;
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
   using L = PL<D>;
@@ -399,36 +415,53 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
   }
 
   // ---- warps 0-7: Q rows: load, rotate, scale, split into hi / lo tiles -----
+  // The raw words of all of a warp's rows are loaded first, so that their
+  // latencies overlap, then converted and transformed row by row; lane l holds
+  // the P = D/32 consecutive channels l*P .. l*P+P-1 (q is 16-byte aligned, so
+  // each lane's P elements are one aligned vector).
   {
     constexpr int P = G / 32;
-    for (int rr = 0; rr < kPM / 8; ++rr) {
-      const int r = warp * (kPM / 8) + rr;
+    constexpr int RR = kPM / 8;  // rows per warp
+    uint32_t raw[RR][P];
+    const bool wide = p.q_dtype == KVQ_F32;
+#pragma unroll
+    for (int rr = 0; rr < RR; ++rr) {
+      const int r = warp * RR + rr;
       const int rli = r / g, rhh = r % g, rqi = tile * p.ppt + rli;
       const bool ok = rli < p.ppt && rqi < p.n_tokens;
-      float v[D / 32];
-      const size_t base = (((size_t)b * p.n_tokens + (ok ? rqi : 0)) * p.n_q_heads + kvh * g + rhh) * D;
+      const size_t e = (((size_t)b * p.n_tokens + (ok ? rqi : 0)) * p.n_q_heads + kvh * g + rhh) * D + lane * P;
+      if (wide) ld_words<P>(static_cast<const uint32_t*>(p.q) + e, raw[rr]);
+      else ld_words<P / 2>(reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(p.q) + e), raw[rr]);
+    }
+    float v[RR][P];
 #pragma unroll
-      for (int j = 0; j < D / 32; ++j) {
-        const int c = fwht_channel<D, G>(lane, j);
-        float x = 0.0f;
-        if (ok) {
-          if (p.q_dtype == KVQ_F32) x = static_cast<const float*>(p.q)[base + c];
-          else if (p.q_dtype == KVQ_BF16) x = bf16_bits_to_f32(static_cast<const uint16_t*>(p.q)[base + c]);
-          else x = __half2float(static_cast<const __half*>(p.q)[base + c]);
-        }
-        v[j] = x;
+    for (int rr = 0; rr < RR; ++rr) {
+      const int r = warp * RR + rr;
+      const int rli = r / g, rqi = tile * p.ppt + rli;
+      const bool ok = rli < p.ppt && rqi < p.n_tokens;
+#pragma unroll
+      for (int j = 0; j < P; ++j) {
+        const uint32_t w = raw[rr][j / 2];
+        const uint32_t h = (j & 1) ? (w >> 16) : (w & 0xFFFFu);
+        float x;
+        if (wide) x = __uint_as_float(raw[rr][j]);
+        else if (p.q_dtype == KVQ_BF16) x = bf16_bits_to_f32(h);
+        else x = __half2float(__ushort_as_half(uint16_t(h)));
+        v[rr][j] = ok ? x : 0.0f;
       }
-      float s = p.scale_log2;
-      if (p.rot_k) {
-        warp_fwht<D, G>(v, lane);
-        s *= inv_sqrt_group<G>();
-      }
-      // lane holds P consecutive channels: write them as fp16 hi / lo pairs
+    }
+    float s = p.scale_log2;
+    if (p.rot_k) s *= inv_sqrt_group<G>();
+#pragma unroll
+    for (int rr = 0; rr < RR; ++rr) {
+      const int r = warp * RR + rr;
+      if (p.rot_k) warp_fwht<D, G>(v[rr], lane);
+      // write the lane's P consecutive channels as fp16 hi / lo pairs
 #pragma unroll
       for (int j0 = 0; j0 < P; j0 += 2) {
         const int c = lane * P + j0;
         uint32_t hi, lo;
-        split2(v[j0] * s, v[j0 + 1] * s, hi, lo);
+        split2(v[rr][j0] * s, v[rr][j0 + 1] * s, hi, lo);
         const uint32_t off = (c / 64) * (kPM * 128) + tc::sw128_chunk(r, (c % 64) / 8) + (c % 8) * 2;
         *reinterpret_cast<uint32_t*>(sm + L::off_qh + off) = hi;
         *reinterpret_cast<uint32_t*>(sm + L::off_ql + off) = lo;
