@@ -255,11 +255,13 @@ __device__ __forceinline__ void warp_fwht(float (&v)[D / 32], int lane) {
   }
 #pragma unroll
   for (int m = 1; m < 32; m <<= 1) {         // partners across lanes (stride m*P)
-    const bool upper = (lane & m) != 0;
+    // upper lane: o - v, lower lane: v + o; as o + sgn*v (sgn*v is exact, so the
+    // single rounding is that of the plain sum or difference)
+    const float sgn = (lane & m) ? -1.0f : 1.0f;
 #pragma unroll
     for (int j = 0; j < D / 32; ++j) {
       const float o = __shfl_xor_sync(0xffffffffu, v[j], m);
-      v[j] = upper ? (o - v[j]) : (v[j] + o);
+      v[j] = fmaf(sgn, v[j], o);
     }
   }
 }

@@ -269,19 +269,27 @@ __device__ __forceinline__ bool role_wait(uint64_t* bar, uint32_t parity, Sync* 
   return true;
 }
 
-// N consecutive 32-bit words from global memory, as one vector load when the
-// address is 4N-byte aligned (N = 1, 2 or 4).
-template <int N>
-__device__ __forceinline__ void ld_words(const uint32_t* src, uint32_t* dst) {
-  if constexpr (N == 4) {
-    const uint4 t = *reinterpret_cast<const uint4*>(src);
-    dst[0] = t.x; dst[1] = t.y; dst[2] = t.z; dst[3] = t.w;
-  } else if constexpr (N == 2) {
-    const uint2 t = *reinterpret_cast<const uint2*>(src);
-    dst[0] = t.x; dst[1] = t.y;
-  } else {
-    static_assert(N == 1, "1, 2 or 4 words");
-    dst[0] = *src;
+// Unnormalised Sylvester FWHT of D-channel rows, one row per R = D/32
+// consecutive lanes: lane l holds channels 32(l % R) .. 32(l % R) + 31 of row
+// l / R.  The 5 channel bits inside a lane are combined in registers, the
+// remaining log2(R) across lanes (one shuffle per value per bit).
+template <int D>
+__device__ __forceinline__ void row_fwht(float (&v)[32], int lane) {
+  static_assert(D == 64 || D == 128, "rows of 64 or 128 channels");
+#pragma unroll
+  for (int h = 1; h < 32; h <<= 1)
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if ((i & h) == 0) {
+        const float a = v[i], b = v[i + h];
+        v[i] = a + b;
+        v[i + h] = a - b;
+      }
+#pragma unroll
+  for (int m = 1; m < D / 32; m <<= 1) {
+    const float sgn = (lane & m) ? -1.0f : 1.0f;  // upper partner: o - v, lower: v + o
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = fmaf(sgn, v[i], __shfl_xor_sync(0xffffffffu, v[i], m));
   }
 }
 
@@ -297,6 +305,33 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
   const int tile = p.ntiles - 1 - blockIdx.x;  // the longest (latest) query tiles first
   const int kvh = blockIdx.y, b = blockIdx.z;
   const int g = p.group;
+  // Warps 0-7 start loading their query rows before any set-up, so that the
+  // load latency overlaps the TMEM allocation and barrier initialisation.  A
+  // row is held by QR = D/32 consecutive lanes, 32 consecutive channels each
+  // (one aligned 64- or 128-byte run: q is 16-byte aligned); a warp's 16 rows
+  // take QPASS passes of 32/QR rows.
+  constexpr int QR = D / 32, QRP = 32 / QR, QPASS = (kPM / 8) / QRP;
+  const int qsub = lane % QR;
+  uint32_t qraw[QPASS][32];
+  const bool qwide = p.q_dtype == KVQ_F32;
+  if (warp < kSoftmax / 32) {
+#pragma unroll
+    for (int pp = 0; pp < QPASS; ++pp) {
+      const int r = warp * (kPM / 8) + pp * QRP + lane / QR;
+      const int rli = r / g, rhh = r % g, rqi = tile * p.ppt + rli;
+      const bool ok = rli < p.ppt && rqi < p.n_tokens;
+      const size_t e = (((size_t)b * p.n_tokens + (ok ? rqi : 0)) * p.n_q_heads + kvh * g + rhh) * D + qsub * 32;
+      const uint4* src = qwide ? reinterpret_cast<const uint4*>(static_cast<const float*>(p.q) + e)
+                               : reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) + e);
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        if (t >= 4 && !qwide) break;  // 16-bit rows: 64 bytes
+        const uint4 w = src[t];
+        qraw[pp][4 * t] = w.x; qraw[pp][4 * t + 1] = w.y; qraw[pp][4 * t + 2] = w.z; qraw[pp][4 * t + 3] = w.w;
+      }
+    }
+  }
+
   const int n = min(max(p.seq_len[b], 0), p.max_tiles * kPN);  // as the stage kernel
   const int p0 = p.q_pos0 ? p.q_pos0[b] : n - p.n_tokens;
   const int last_q = min(p.n_tokens, (tile + 1) * p.ppt) - 1;
@@ -414,57 +449,37 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
     return;
   }
 
-  // ---- warps 0-7: Q rows: load, rotate, scale, split into hi / lo tiles -----
-  // The raw words of all of a warp's rows are loaded first, so that their
-  // latencies overlap, then converted and transformed row by row; lane l holds
-  // the P = D/32 consecutive channels l*P .. l*P+P-1 (q is 16-byte aligned, so
-  // each lane's P elements are one aligned vector).
+  // ---- warps 0-7: Q rows (loaded above): rotate, scale, split into hi / lo tiles
   {
-    constexpr int P = G / 32;
-    constexpr int RR = kPM / 8;  // rows per warp
-    uint32_t raw[RR][P];
-    const bool wide = p.q_dtype == KVQ_F32;
+    float sc = p.scale_log2;
+    if (p.rot_k) sc *= inv_sqrt_group<G>();
 #pragma unroll
-    for (int rr = 0; rr < RR; ++rr) {
-      const int r = warp * RR + rr;
-      const int rli = r / g, rhh = r % g, rqi = tile * p.ppt + rli;
-      const bool ok = rli < p.ppt && rqi < p.n_tokens;
-      const size_t e = (((size_t)b * p.n_tokens + (ok ? rqi : 0)) * p.n_q_heads + kvh * g + rhh) * D + lane * P;
-      if (wide) ld_words<P>(static_cast<const uint32_t*>(p.q) + e, raw[rr]);
-      else ld_words<P / 2>(reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(p.q) + e), raw[rr]);
-    }
-    float v[RR][P];
-#pragma unroll
-    for (int rr = 0; rr < RR; ++rr) {
-      const int r = warp * RR + rr;
+    for (int pp = 0; pp < QPASS; ++pp) {
+      const int r = warp * (kPM / 8) + pp * QRP + lane / QR;
       const int rli = r / g, rqi = tile * p.ppt + rli;
       const bool ok = rli < p.ppt && rqi < p.n_tokens;
+      float v[32];
 #pragma unroll
-      for (int j = 0; j < P; ++j) {
-        const uint32_t w = raw[rr][j / 2];
-        const uint32_t h = (j & 1) ? (w >> 16) : (w & 0xFFFFu);
+      for (int i = 0; i < 32; ++i) {
+        const uint32_t w = qraw[pp][i / 2];
+        const uint32_t hb = (i & 1) ? (w >> 16) : (w & 0xFFFFu);
         float x;
-        if (wide) x = __uint_as_float(raw[rr][j]);
-        else if (p.q_dtype == KVQ_BF16) x = bf16_bits_to_f32(h);
-        else x = __half2float(__ushort_as_half(uint16_t(h)));
-        v[rr][j] = ok ? x : 0.0f;
+        if (qwide) x = __uint_as_float(qraw[pp][i]);
+        else if (p.q_dtype == KVQ_BF16) x = bf16_bits_to_f32(hb);
+        else x = __half2float(__ushort_as_half(uint16_t(hb)));
+        v[i] = ok ? x : 0.0f;
       }
-    }
-    float s = p.scale_log2;
-    if (p.rot_k) s *= inv_sqrt_group<G>();
+      if (p.rot_k) row_fwht<D>(v, lane);
+      // the lane's 32 channels = four 16-byte chunks of 8 fp16 in each of the hi / lo tiles
 #pragma unroll
-    for (int rr = 0; rr < RR; ++rr) {
-      const int r = warp * RR + rr;
-      if (p.rot_k) warp_fwht<D, G>(v[rr], lane);
-      // write the lane's P consecutive channels as fp16 hi / lo pairs
+      for (int t = 0; t < 4; ++t) {
+        uint32_t hi[4], lo[4];
 #pragma unroll
-      for (int j0 = 0; j0 < P; j0 += 2) {
-        const int c = lane * P + j0;
-        uint32_t hi, lo;
-        split2(v[rr][j0] * s, v[rr][j0 + 1] * s, hi, lo);
-        const uint32_t off = (c / 64) * (kPM * 128) + tc::sw128_chunk(r, (c % 64) / 8) + (c % 8) * 2;
-        *reinterpret_cast<uint32_t*>(sm + L::off_qh + off) = hi;
-        *reinterpret_cast<uint32_t*>(sm + L::off_ql + off) = lo;
+        for (int e = 0; e < 4; ++e) split2(v[8 * t + 2 * e] * sc, v[8 * t + 2 * e + 1] * sc, hi[e], lo[e]);
+        const int c = qsub * 32 + 8 * t;
+        const uint32_t off = (c / 64) * (kPM * 128) + tc::sw128_chunk(r, (c % 64) / 8);
+        *reinterpret_cast<uint4*>(sm + L::off_qh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(sm + L::off_ql + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
     }
   }
@@ -609,32 +624,45 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, L::tmem_cols);
   }
-  constexpr int P = D / 32;  // consecutive channels per lane
-  for (int rr = 0; rr < kPM / 8; ++rr) {
-    const int r = warp * (kPM / 8) + rr;
+  // rows as in the Q prologue: QR lanes per row, 32 consecutive channels per lane
+#pragma unroll
+  for (int pp = 0; pp < QPASS; ++pp) {
+    const int r = warp * (kPM / 8) + pp * QRP + lane / QR;
     const int rli = r / g, rhh = r % g, rqi = tile * p.ppt + rli;
-    if (!(rli < p.ppt && rqi < p.n_tokens)) continue;
-    float v[P];
-    const float* src = &stage[r * L::stage_stride + lane * P];
-    if constexpr (P == 4) {
-      const float4 t = *reinterpret_cast<const float4*>(src);
-      v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
-    } else {
-      const float2 t = *reinterpret_cast<const float2*>(src);
-      v[0] = t.x; v[1] = t.y;
+    float v[32];
+    const float4* src = reinterpret_cast<const float4*>(&stage[r * L::stage_stride + qsub * 32]);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const float4 x = src[t];
+      v[4 * t] = x.x; v[4 * t + 1] = x.y; v[4 * t + 2] = x.z; v[4 * t + 3] = x.w;
     }
     if (p.rot_v) {
-      warp_fwht<D, G>(v, lane);
+      row_fwht<D>(v, lane);
 #pragma unroll
-      for (int j = 0; j < P; ++j) v[j] *= inv_sqrt_group<G>();
+      for (int i = 0; i < 32; ++i) v[i] *= inv_sqrt_group<G>();
     }
-    const size_t base = (((size_t)b * p.n_tokens + rqi) * p.n_q_heads + kvh * g + rhh) * D;
+    if (!(rli < p.ppt && rqi < p.n_tokens)) continue;
+    // 32 consecutive channels: 128 (fp32) or 64 (16-bit) bytes, as 16-byte stores
+    const size_t e = (((size_t)b * p.n_tokens + rqi) * p.n_q_heads + kvh * g + rhh) * D + qsub * 32;
+    if (p.out_dtype == KVQ_F32) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + e);
 #pragma unroll
-    for (int j = 0; j < P; ++j) {
-      const size_t e = base + fwht_channel<D, G>(lane, j);
-      if (p.out_dtype == KVQ_F32) static_cast<float*>(p.out)[e] = v[j];
-      else if (p.out_dtype == KVQ_BF16) static_cast<__nv_bfloat16*>(p.out)[e] = __float2bfloat16_rn(v[j]);
-      else static_cast<__half*>(p.out)[e] = __float2half_rn(v[j]);
+      for (int t = 0; t < 8; ++t) dst[t] = make_float4(v[4 * t], v[4 * t + 1], v[4 * t + 2], v[4 * t + 3]);
+    } else {
+      uint32_t w[16];
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        if (p.out_dtype == KVQ_BF16) {
+          const __nv_bfloat162 t2 = __floats2bfloat162_rn(v[i], v[i + 1]);
+          w[i / 2] = *reinterpret_cast<const uint32_t*>(&t2);
+        } else {
+          const __half2 t2 = __floats2half2_rn(v[i], v[i + 1]);
+          w[i / 2] = *reinterpret_cast<const uint32_t*>(&t2);
+        }
+      }
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + e);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) dst[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
     }
   }
 }
