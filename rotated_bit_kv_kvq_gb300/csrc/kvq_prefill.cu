@@ -269,6 +269,11 @@ __device__ __forceinline__ bool role_wait(uint64_t* bar, uint32_t parity, Sync* 
   return true;
 }
 
+// Hint: bring `bytes` (a multiple of 16) at the 16-byte aligned `src` into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Unnormalised Sylvester FWHT of D-channel rows, one row per R = D/32
 // consecutive lanes: lane l holds channels 32(l % R) .. 32(l % R) + 31 of row
 // l / R.  The 5 channel bits inside a lane are combined in registers, the
@@ -365,6 +370,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
   const uint32_t tmem = sy->tmem;
 
   if (warp == kSoftmax / 32) {
+    // ---- L2 prefetch of the query rows of the CTA one SM-count further in the
+    // launch order (about the one that takes over an SM after this wave) -------
+    {
+      uint32_t nsm;
+      asm("mov.u32 %0, %%nsmid;" : "=r"(nsm));
+      const uint32_t nx = gridDim.x, ny = gridDim.y;
+      const uint32_t lin = blockIdx.x + nx * (blockIdx.y + ny * blockIdx.z) + nsm;
+      if (lin < nx * ny * gridDim.z) {
+        const int t2 = p.ntiles - 1 - int(lin % nx), h2 = int((lin / nx) % ny), b2 = int(lin / (nx * ny));
+        const size_t esz = qwide ? 4 : 2;
+        for (int i = lane; i < p.ppt; i += 32) {
+          const int qi = t2 * p.ppt + i;
+          if (qi >= p.n_tokens) break;
+          const size_t e = (((size_t)b2 * p.n_tokens + qi) * p.n_q_heads + (size_t)h2 * g) * D;
+          bulk_prefetch_l2(static_cast<const uint8_t*>(p.q) + e * esz, uint32_t(g * D * esz));
+        }
+      }
+    }
     // ---- producer: K and V tiles of this (sequence, KV head) ----------------
     if (lane == 0 && nkv > 0) {
       const uint8_t* base = p.ws + ((size_t)b * p.n_kv_heads + kvh) * p.max_tiles * (size_t)L::tile;
