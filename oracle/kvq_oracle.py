@@ -29,12 +29,27 @@ Sources (pages are cited by title and section):
   pages name these types without restating them; the reading is the GGUF
   definition of the same names, as for the _0 types.
 
+* Outlier channels kept at 8 bits ([P1] section "적용 및 배경 기술" names, as a
+  direction of the work the patch comes from, mixed precision that keeps only
+  the outlier channels at 8 bits; it gives no selection rule, count or
+  interplay with the rotation).  Reading used here: per KV head the caller
+  names O channels (O a multiple of 32) of the *original* basis.  On the
+  write path those O values are stored as q8_0 blocks, unrotated, in slot
+  order (increasing channel); they are set to zero in the vector, and the
+  rest is rotated and quantized in the cache's format as before.  The bf16
+  tail keeps the whole rotated vector.  What attention sees for a body
+  position is the rotated, dequantized rest plus the rotated scatter of the
+  dequantized outlier values -- in the original basis,
+  k_hat = R^T deq(R k_rest) + scatter(deq8(k_O)), which is k up to the two
+  quantization errors.
+
 Precision: rotation and attention in float64; quantizer arithmetic in IEEE
 float32 exactly as the block definition states (one rounding per operation,
 no fused multiply-add); fp16 and bf16 round-to-nearest-even.
 
-Parity pins (see tests/test_oracle_pins.py): every function below is pinned
-by closed forms, invariants, brute force or hand-worked golden values.  No
+Parity pins (see tests/test_oracle_pins.py and tests/test_oracle_outliers.py):
+every function below is pinned by closed forms, invariants, brute force or
+hand-worked golden values.  No
 function is "parity unpinned".
 """
 
@@ -359,6 +374,33 @@ def to_ggml_bytes(qtype: str, d_bits, codes) -> np.ndarray:
 
 
 # ---------------------------------------------------------------------------
+# Outlier channels ([P1] 적용 및 배경 기술: 8-bit outlier channels; reading in
+# the module docstring)
+# ---------------------------------------------------------------------------
+
+def split_outliers(x: np.ndarray, oidx: np.ndarray):
+    """x [..., H, d] (float32), oidx [H][O] -> (x_O [..., H, O]: the values of
+    each head's outlier channels in slot order, x_rest: x with those channels
+    set to zero)."""
+    x = np.asarray(x, dtype=F32)
+    xo = np.stack([x[..., h, oidx[h]] for h in range(x.shape[-2])], axis=-2)
+    rest = x.copy()
+    for h in range(x.shape[-2]):
+        rest[..., h, oidx[h]] = 0.0
+    return xo, rest
+
+
+def outlier_values(d_bits, codes, chans, head_dim: int) -> np.ndarray:
+    """q8_0 outlier blocks of one head ([n][O/32], [n][O/32][32]) -> float64
+    [n][head_dim]: slot i's dequantized value at channel chans[i], zeros
+    elsewhere (original basis)."""
+    v = dequantize(TYPE_Q8_0, d_bits, codes)
+    out = np.zeros(v.shape[:-1] + (head_dim,), dtype=F64)
+    out[..., np.asarray(chans)] = v
+    return out
+
+
+# ---------------------------------------------------------------------------
 # The rotated, quantized KV cache with a BF16 precision tail
 # ---------------------------------------------------------------------------
 
@@ -374,9 +416,18 @@ class OracleCache:
     written for every token ("write-through"), so codes never depend on T."""
 
     def __init__(self, batch, n_kv_heads, head_dim, max_ctx, tail_len,
-                 k_type, v_type, rot_k, rot_v):
+                 k_type, v_type, rot_k, rot_v, outliers=None):
         if head_dim % QK:
             raise ValueError("head_dim must be a multiple of 32")
+        # outlier channels: [n_kv_heads][O], strictly increasing, O a multiple of 32
+        self.oidx = None if outliers is None else np.asarray(outliers, dtype=np.int64)
+        self.O = 0 if self.oidx is None else self.oidx.shape[1]
+        if self.O:
+            if (self.oidx.shape[0] != n_kv_heads or self.O % QK or self.O >= head_dim
+                    or np.any(self.oidx < 0) or np.any(self.oidx >= head_dim)
+                    or np.any(np.diff(self.oidx, axis=1) <= 0)):
+                raise ValueError("outlier channels: [n_kv_heads][O], O a multiple of 32 below head_dim, "
+                                 "strictly increasing channels")
         if (rot_k or rot_v) and not rotation_enabled(head_dim):
             raise ValueError("rotation requested on an ineligible head_dim")
         self.B, self.H, self.d = batch, n_kv_heads, head_dim
@@ -390,6 +441,9 @@ class OracleCache:
                                   np.uint32 if self.types[w] in MIN_TYPES else np.uint16) for w in ("k", "v")}
         self.tail = {w: np.zeros((batch, n_kv_heads, max(tail_len, 1), head_dim), np.uint16)
                      for w in ("k", "v")}
+        no = max(self.O, QK) // QK
+        self.ocodes = {w: np.zeros((batch, n_kv_heads, max_ctx, no, QK), np.int8) for w in ("k", "v")}
+        self.odbits = {w: np.zeros((batch, n_kv_heads, max_ctx, no), np.uint16) for w in ("k", "v")}
         self.seq_len = np.zeros(batch, dtype=np.int64)
 
     # -- write path -------------------------------------------------------
@@ -407,6 +461,8 @@ class OracleCache:
         k = np.asarray(k, dtype=F32)
         v = np.asarray(v, dtype=F32)
         n_new = k.shape[1]
+        if self.O and prerotated:
+            raise ValueError("outlier channels are picked in the original basis: no prerotated input")
         for b in range(self.B):
             nb = n_new if n_new_per_seq is None else int(n_new_per_seq[b])
             n0 = int(self.seq_len[b])
@@ -415,8 +471,16 @@ class OracleCache:
             if nb == 0:
                 continue
             for which, x in (("k", k), ("v", v)):
-                y = self.stored_input(which, x[b, :nb], prerotated)  # [nb][H][d]
-                dbits, codes = quantize(self.types[which], y)
+                y = self.stored_input(which, x[b, :nb], prerotated)  # [nb][H][d], the tail's values
+                yb = y
+                if self.O:
+                    # outlier values (unrotated) -> q8_0; the rest, zeroed there, is rotated
+                    xo, rest = split_outliers(x[b, :nb], self.oidx)
+                    od, oc = quantize_q8_0(xo)
+                    self.ocodes[which][b, :, n0:n0 + nb] = oc.transpose(1, 0, 2, 3)
+                    self.odbits[which][b, :, n0:n0 + nb] = od.transpose(1, 0, 2)
+                    yb = self.stored_input(which, rest, False)
+                dbits, codes = quantize(self.types[which], yb)
                 self.codes[which][b, :, n0:n0 + nb] = codes.transpose(1, 0, 2, 3)
                 self.dbits[which][b, :, n0:n0 + nb] = dbits.transpose(1, 0, 2)
                 if self.T > 0:
@@ -427,9 +491,18 @@ class OracleCache:
 
     # -- what attention reads --------------------------------------------
     def body_values(self, which, b, h, t0=0, t1=None) -> np.ndarray:
+        """float64 [t1 - t0][d] in the basis attention works in (rotated when
+        rotation is on): the dequantized body, plus -- with outlier channels --
+        the dequantized q8_0 outlier values scattered to their channels and
+        rotated like the rest."""
         t1 = int(self.seq_len[b]) if t1 is None else t1
-        return dequantize(self.types[which], self.dbits[which][b, h, t0:t1],
-                          self.codes[which][b, h, t0:t1])
+        x = dequantize(self.types[which], self.dbits[which][b, h, t0:t1],
+                       self.codes[which][b, h, t0:t1])
+        if self.O:
+            xo = outlier_values(self.odbits[which][b, h, t0:t1], self.ocodes[which][b, h, t0:t1],
+                                self.oidx[h], self.d)
+            x = x + (rotate(xo) if self.rot[which] else xo)
+        return x
 
     def tail_values(self, which, b, h, positions) -> np.ndarray:
         slots = np.asarray(positions, dtype=np.int64) % self.T

@@ -9,6 +9,7 @@ import numpy as np
 import pytest
 
 from oracle import kvq_oracle as ko
+import test_oracle_outliers as opins
 import test_oracle_pins as pins
 
 F32 = np.float32
@@ -146,6 +147,29 @@ def _dequant_min_dropped(qtype, d_bits, codes):
 
 
 _ORIG_DEQUANT = ko.dequantize
+_ORIG_SPLIT = ko.split_outliers
+_ORIG_OVALS = ko.outlier_values
+
+
+def _split_rest_not_zeroed(x, oidx):
+    """Outlier values taken but left in the vector that gets rotated."""
+    xo, _ = _ORIG_SPLIT(x, oidx)
+    return xo, np.asarray(x, dtype=np.float32).copy()
+
+
+def _split_slots_reversed(x, oidx):
+    """Outlier values stored in decreasing channel order."""
+    xo, rest = _ORIG_SPLIT(x, oidx)
+    return xo[..., ::-1].copy(), rest
+
+
+def _ovals_shifted(d_bits, codes, chans, head_dim):
+    """Outlier values scattered one channel off."""
+    return np.roll(_ORIG_OVALS(d_bits, codes, chans, head_dim), 1, axis=-1)
+
+
+def _ovals_negated(d_bits, codes, chans, head_dim):
+    return -_ORIG_OVALS(d_bits, codes, chans, head_dim)
 
 
 MUTANTS = [
@@ -165,6 +189,10 @@ MUTANTS = [
     ("quantize_q4_1", _min_no_half, [pins.test_golden_blocks]),
     ("quantize_q5_1", _min_word_swapped, [pins.test_golden_blocks]),
     ("dequantize", _dequant_min_dropped, [lambda: pins.test_min_quantizer_error_bounds("q4_1")]),
+    ("split_outliers", _split_rest_not_zeroed, [lambda: opins.test_exact_reconstruction_through_rotation(True)]),
+    ("split_outliers", _split_slots_reversed, [lambda: opins.test_exact_reconstruction_through_rotation(False)]),
+    ("outlier_values", _ovals_shifted, [opins.test_outlier_only_vectors_are_q8_0_alone]),
+    ("outlier_values", _ovals_negated, [lambda: opins.test_reconstruction_error_within_the_two_quantizations("q4_0")]),
 ]
 
 
