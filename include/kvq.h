@@ -99,13 +99,19 @@ typedef int32_t kvq_status;
 #define KVQ_PLANE_V_TAIL  7
 #define KVQ_PLANE_SEQ_LEN 8  /* int32 [batch]                               tokens stored per sequence           */
 #define KVQ_PLANE_STATUS  9  /* uint32 [4]                                  device status words; zero before use */
-#define KVQ_NUM_PLANES   10
+#define KVQ_PLANE_K_OQS  10  /* int8 [rows][n_outlier]                      outlier-channel q8_0 codes (n_outlier > 0) */
+#define KVQ_PLANE_K_OD   11  /* fp16 [rows][n_outlier/32]                   their block scales                     */
+#define KVQ_PLANE_V_OQS  12
+#define KVQ_PLANE_V_OD   13
+#define KVQ_PLANE_OUTLIER_IDX 14  /* int32 [kv_heads][n_outlier]            the caller's outlier channel lists     */
+#define KVQ_NUM_PLANES   15
 
 /* device status word 0 bits (read by kvq_sync_status) */
 #define KVQ_DEV_ERR_APPEND_RANGE  1u  /* an append would pass max_ctx, or n_new_per_seq[b] not in [0, n_new] */
 #define KVQ_DEV_ERR_PREFILL_RANGE 2u  /* a prefill query position is negative                              */
 #define KVQ_DEV_ERR_TIMEOUT       4u  /* a bounded wait on a shared-memory barrier gave up                 */
 #define KVQ_DEV_ERR_PAGE          8u  /* a page_table entry lies outside [0, n_pages) (paged layout)        */
+#define KVQ_DEV_ERR_OUTLIER      16u  /* an outlier_idx row is not strictly increasing inside [0, head_dim) */
 
 /*
  * The cache descriptor.  Body planes hold the packed payload of every block:
@@ -151,6 +157,25 @@ typedef struct kvq_cache {
   int32_t page_tokens;        /* 0, or a multiple of 64 that divides max_ctx   */
   int32_t n_pages;            /* pages in the pool (paged layout)              */
   const int32_t* page_table;  /* device int32 [batch][max_ctx / page_tokens]   */
+  /* Outlier channels kept at 8 bits (optional; n_outlier == 0 turns them off).
+   * The pages (velog "fix-kv-cache-quantization-outliers", section 적용 및
+   * 배경 기술) name this direction without fixing it; the reading implemented
+   * here: per KV head the caller lists n_outlier channels of the original
+   * basis (outlier_idx, strictly increasing).  The write path stores their
+   * values unrotated as q8_0 blocks in slot order (k_oqs / k_od, v_oqs / v_od,
+   * one row per body row, contiguous or paged like the body), sets them to
+   * zero in the vector and rotates / quantizes the rest as usual; the bf16
+   * tail keeps the whole rotated vector.  Attention adds q_O . k_O to every
+   * body score and scatters sum_t p_t v_O,t back to those channels of the
+   * output.  Requires head_dim >= 64 and inputs in the original basis (no
+   * KVQ_INPUT_PREROTATED).  Supported by append, the fused step and decode for
+   * the q4_0 / q5_0 / q8_0 pairs; prefill returns KVQ_ERR_UNSUPPORTED.  A row
+   * of outlier_idx that is not strictly increasing in [0, head_dim) sets
+   * KVQ_DEV_ERR_OUTLIER; its invalid slots are then ignored. */
+  int32_t n_outlier;           /* 0 or 32                                     */
+  const int32_t* outlier_idx;  /* device int32 [kv_heads][n_outlier]          */
+  void* k_oqs; void* k_od;     /* KVQ_PLANE_K_OQS / KVQ_PLANE_K_OD            */
+  void* v_oqs; void* v_od;     /* KVQ_PLANE_V_OQS / KVQ_PLANE_V_OD            */
 } kvq_cache;
 
 /* Library version (KVQ_VERSION). */

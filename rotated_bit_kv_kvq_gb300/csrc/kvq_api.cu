@@ -31,6 +31,8 @@ bool shape_ok(const kvq_cache* c) {
   if (c->page_tokens < 0 || c->n_pages < 0) return false;
   if (c->page_tokens && (c->page_tokens % 64 || c->max_ctx % c->page_tokens || c->n_pages == 0)) return false;
   if (!c->page_tokens && c->n_pages) return false;
+  // outlier channels: 32 per KV head, below head_dim
+  if (c->n_outlier != 0 && (c->n_outlier != 32 || c->head_dim < 64)) return false;
   // every plane offset must stay below 2^62 bytes
   const double rows = double(c->batch) * c->n_kv_heads * c->max_ctx;
   const double prow = double(c->n_pages) * c->n_kv_heads * c->page_tokens;
@@ -54,6 +56,11 @@ size_t plane_bytes(const kvq_cache* c, int plane) {
     case KVQ_PLANE_V_TAIL: return size_t(c->batch) * c->n_kv_heads * size_t(c->tail_len) * d * 2;
     case KVQ_PLANE_SEQ_LEN: return size_t(c->batch) * 4;
     case KVQ_PLANE_STATUS: return 16;
+    case KVQ_PLANE_K_OQS:
+    case KVQ_PLANE_V_OQS: return rows * size_t(c->n_outlier);
+    case KVQ_PLANE_K_OD:
+    case KVQ_PLANE_V_OD: return rows * size_t(c->n_outlier / 32) * 2;
+    case KVQ_PLANE_OUTLIER_IDX: return size_t(c->n_kv_heads) * size_t(c->n_outlier) * 4;
     default: return 0;
   }
 }
@@ -72,6 +79,11 @@ kvq_status check_cache(const kvq_cache* c) {
   const bool has_tail = c->tail_len > 0;
   if (has_tail != (c->k_tail != nullptr) || has_tail != (c->v_tail != nullptr)) return KVQ_ERR_INVALID_ARG;
   if (has_tail && (!aligned16(c->k_tail) || !aligned16(c->v_tail))) return KVQ_ERR_INVALID_ARG;
+  const void* outl[] = {c->outlier_idx, c->k_oqs, c->k_od, c->v_oqs, c->v_od};
+  for (const void* p : outl) {
+    if (c->n_outlier && (!p || !aligned16(p))) return KVQ_ERR_INVALID_ARG;
+    if (!c->n_outlier && p) return KVQ_ERR_INVALID_ARG;
+  }
   return KVQ_OK;
 }
 
@@ -148,6 +160,7 @@ kvq_status kvq_rotate_quantize_append(const kvq_cache* c, const void* k, const v
   kvq::Rot r{};
   if ((s = resolve(c, &r)) != KVQ_OK) return s;
   if (!valid_dtype(in_dtype) || n_new < 0 || (append_flags & ~KVQ_INPUT_PREROTATED)) return KVQ_ERR_INVALID_ARG;
+  if (c->n_outlier && (append_flags & KVQ_INPUT_PREROTATED)) return KVQ_ERR_INVALID_ARG;  // outliers: original basis
   if (n_new == 0) return KVQ_OK;
   if (!k || !v || !aligned16(k) || !aligned16(v)) return KVQ_ERR_INVALID_ARG;
   if ((long long)c->batch * n_new * c->n_kv_heads * 2 > 0x7fffffffLL) return KVQ_ERR_INVALID_ARG;  // vectors < 2^31
@@ -170,7 +183,7 @@ kvq_status kvq_decode_attention(const kvq_cache* c, const void* q, int32_t q_dty
   if (n_q_heads <= 0 || n_q_heads % c->n_kv_heads || n_q_heads / c->n_kv_heads > 4096) return KVQ_ERR_INVALID_ARG;
   if (!q || !out || !aligned16(q) || !aligned16(out)) return KVQ_ERR_INVALID_ARG;
   if (!(scale >= 0.0f) || scale > 1e30f) return KVQ_ERR_INVALID_ARG;
-  if (!kvq::decode_supported(c->head_dim, c->k_type, c->v_type)) return KVQ_ERR_UNSUPPORTED;
+  if (!kvq::decode_supported(c->head_dim, c->k_type, c->v_type, c->n_outlier)) return KVQ_ERR_UNSUPPORTED;
   const kvq::DecodePlan plan = kvq::plan_decode(*c, n_q_heads, sm_count());
   if (!workspace || !aligned16(workspace) || ws_bytes < plan.ws_bytes) return KVQ_ERR_WORKSPACE;
   if (plan.splits > 0x7fffffff || (long long)c->n_kv_heads * plan.head_groups > 65535) return KVQ_ERR_UNSUPPORTED;
@@ -189,6 +202,7 @@ kvq_status kvq_append_decode(const kvq_cache* c, const void* k, const void* v, i
   if ((s = resolve(c, &r)) != KVQ_OK) return s;
   // the append's arguments
   if (!valid_dtype(in_dtype) || n_new < 0 || (append_flags & ~KVQ_INPUT_PREROTATED)) return KVQ_ERR_INVALID_ARG;
+  if (c->n_outlier && (append_flags & KVQ_INPUT_PREROTATED)) return KVQ_ERR_INVALID_ARG;
   if (n_new > 0 && (!k || !v || !aligned16(k) || !aligned16(v))) return KVQ_ERR_INVALID_ARG;
   if ((long long)c->batch * n_new * c->n_kv_heads * 2 > 0x7fffffffLL) return KVQ_ERR_INVALID_ARG;
   // the decode's arguments
@@ -196,7 +210,7 @@ kvq_status kvq_append_decode(const kvq_cache* c, const void* k, const void* v, i
   if (n_q_heads <= 0 || n_q_heads % c->n_kv_heads || n_q_heads / c->n_kv_heads > 4096) return KVQ_ERR_INVALID_ARG;
   if (!q || !out || !aligned16(q) || !aligned16(out)) return KVQ_ERR_INVALID_ARG;
   if (!(scale >= 0.0f) || scale > 1e30f) return KVQ_ERR_INVALID_ARG;
-  if (!kvq::decode_supported(c->head_dim, c->k_type, c->v_type)) return KVQ_ERR_UNSUPPORTED;
+  if (!kvq::decode_supported(c->head_dim, c->k_type, c->v_type, c->n_outlier)) return KVQ_ERR_UNSUPPORTED;
   const kvq::DecodePlan plan = kvq::plan_decode(*c, n_q_heads, sm_count());
   if (!workspace || !aligned16(workspace) || ws_bytes < plan.ws_bytes) return KVQ_ERR_WORKSPACE;
   if (plan.splits > 0x7fffffff || (long long)c->n_kv_heads * plan.head_groups > 65535) return KVQ_ERR_UNSUPPORTED;
@@ -224,7 +238,7 @@ kvq_status kvq_decode_attention_noalloc(const kvq_cache* c, const void* q, int32
   if (n_q_heads <= 0 || n_q_heads % c->n_kv_heads || n_q_heads / c->n_kv_heads > 4096) return KVQ_ERR_INVALID_ARG;
   if (!q || !out || !aligned16(q) || !aligned16(out)) return KVQ_ERR_INVALID_ARG;
   if (!(scale >= 0.0f) || scale > 1e30f) return KVQ_ERR_INVALID_ARG;
-  if (!kvq::decode_supported(c->head_dim, c->k_type, c->v_type)) return KVQ_ERR_UNSUPPORTED;
+  if (!kvq::decode_supported(c->head_dim, c->k_type, c->v_type, c->n_outlier)) return KVQ_ERR_UNSUPPORTED;
   const kvq::DecodePlan plan = kvq::plan_decode(*c, n_q_heads, sm_count());
   if (plan.ws_bytes > KVQ_NOALLOC_SCRATCH_BYTES) return KVQ_ERR_WORKSPACE;
   if (plan.splits > 0x7fffffff || (long long)c->n_kv_heads * plan.head_groups > 65535) return KVQ_ERR_UNSUPPORTED;
@@ -238,7 +252,7 @@ kvq_status kvq_decode_attention_noalloc(const kvq_cache* c, const void* q, int32
 
 size_t kvq_prefill_workspace_bytes(const kvq_cache* c, int32_t n_q_heads, int32_t n_tokens) {
   if (!shape_ok(c) || n_tokens < 0 || n_q_heads <= 0 || n_q_heads % c->n_kv_heads) return 0;
-  if (!kvq::prefill_supported(c->head_dim, n_q_heads / c->n_kv_heads)) return 0;
+  if (c->n_outlier || !kvq::prefill_supported(c->head_dim, n_q_heads / c->n_kv_heads)) return 0;
   return kvq::prefill_workspace_bytes(*c);
 }
 
@@ -255,7 +269,7 @@ kvq_status kvq_prefill_attention(const kvq_cache* c, const void* q, int32_t q_dt
   if (!(scale >= 0.0f) || scale > 1e30f) return KVQ_ERR_INVALID_ARG;
   if (n_tokens == 0) return KVQ_OK;
   if (!q || !out || !aligned16(q) || !aligned16(out)) return KVQ_ERR_INVALID_ARG;
-  if (!kvq::prefill_supported(c->head_dim, n_q_heads / c->n_kv_heads)) return KVQ_ERR_UNSUPPORTED;
+  if (c->n_outlier || !kvq::prefill_supported(c->head_dim, n_q_heads / c->n_kv_heads)) return KVQ_ERR_UNSUPPORTED;
   if (!workspace || !aligned16(workspace) || ws_bytes < kvq::prefill_workspace_bytes(*c)) return KVQ_ERR_WORKSPACE;
   const float sc = scale == 0.0f ? 1.0f / sqrtf(float(c->head_dim)) : scale;
   return from_cuda(kvq::launch_prefill(*c, r, q, q_dtype, n_q_heads, n_tokens, q_pos0, causal, sc, out, out_dtype,

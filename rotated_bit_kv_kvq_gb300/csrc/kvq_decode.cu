@@ -37,7 +37,9 @@ cudaError_t decode_noalloc_scratch(void** ptr, size_t* bytes) {
   return cudaSuccess;
 }
 
-bool decode_supported(int d, int kt, int vt) {
+bool decode_supported(int d, int kt, int vt, int n_outlier) {
+  if (n_outlier)
+    return (d == 64 || d == 128 || d == 256) && kt <= KVQ_TYPE_Q8_0 && vt <= KVQ_TYPE_Q8_0 && n_outlier == 32;
   if (d == 64 || d == 128 || d == 256) return true;  // every K / V format pair
   return d == 192 && kt == KVQ_TYPE_Q4_0 && vt == KVQ_TYPE_Q4_0;
 }
@@ -61,7 +63,7 @@ DecodePlan plan_decode(const kvq_cache& c, int n_q_heads, int sm_count) {
   pl.chunk = chunk;
   pl.splits_body = (c.max_ctx + chunk - 1) / chunk;
   pl.splits = pl.splits_body + pl.splits_tail;
-  pl.ws_bytes = (size_t)c.batch * n_q_heads * pl.splits * (c.head_dim + 2) * sizeof(float);
+  pl.ws_bytes = (size_t)c.batch * n_q_heads * pl.splits * (c.head_dim + 2 + c.n_outlier) * sizeof(float);
   return pl;
 }
 

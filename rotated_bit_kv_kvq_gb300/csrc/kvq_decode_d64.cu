@@ -13,7 +13,7 @@ cudaError_t launch_decode_d192(const kvq_cache& c, Rot rot, const DecodePlan& pl
                                int n_q_heads, float scale, void* out, int out_dtype, void* ws, cudaStream_t st,
                               const FusedAppend* fa) {
   if (c.k_type == KVQ_TYPE_Q4_0 && c.v_type == KVQ_TYPE_Q4_0)
-    return run_decode<192, KVQ_TYPE_Q4_0, KVQ_TYPE_Q4_0>(c, rot, plan, q, q_dtype, n_q_heads, scale, out, out_dtype,
+    return run_decode<192, KVQ_TYPE_Q4_0, KVQ_TYPE_Q4_0, false>(c, rot, plan, q, q_dtype, n_q_heads, scale, out, out_dtype,
                                                          ws, st, fa);
   return cudaErrorInvalidValue;
 }

@@ -50,7 +50,7 @@ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 // widest TMA swizzle box (128, 64 or 32 bytes) that tiles a row exactly
 constexpr int box_w(int row_bytes) { return row_bytes % 128 == 0 ? 128 : (row_bytes % 64 == 0 ? 64 : 32); }
 
-template <int D, int KT, int VT>
+template <int D, int KT, int VT, bool OL = false>
 struct Cfg {
   static constexpr int NB = D / 32;
   static constexpr int rowK = KT == KVQ_TYPE_Q8_0 ? D : D / 2;
@@ -66,9 +66,14 @@ struct Cfg {
   static constexpr int off_vd = off_kd + 16 * NB * KH;
   static constexpr int off_kqh = off_vd + 16 * NB * VH;
   static constexpr int off_vqh = off_kqh + (K5 ? 16 * NB * 4 : 0);
-  static constexpr int body_bytes = off_vqh + (V5 ? 16 * NB * 4 : 0);
+  // outlier channels (OL): 32 int8 codes of K, then of V, per token (plain rows), then their fp16 scales
+  static constexpr int off_ko = align_up(off_vqh + (V5 ? 16 * NB * 4 : 0), 16);
+  static constexpr int off_vo = off_ko + 16 * 32;
+  static constexpr int off_kod = off_vo + 16 * 32;
+  static constexpr int off_vod = off_kod + 16 * 2;
+  static constexpr int body_bytes = OL ? off_vod + 16 * 2 : off_vqh + (V5 ? 16 * NB * 4 : 0);
   static constexpr uint32_t body_tx =
-      16 * rowK + 16 * rowV + 16 * NB * (KH + VH) + (K5 ? 64 * NB : 0) + (V5 ? 64 * NB : 0);
+      16 * rowK + 16 * rowV + 16 * NB * (KH + VH) + (K5 ? 64 * NB : 0) + (V5 ? 64 * NB : 0) + (OL ? 2 * 16 * 34 : 0);
   // tail stage: TT tokens of bf16 K and V
   static constexpr int TT = D >= 256 ? 8 : 16;
   static constexpr int WT = box_w(2 * D);
@@ -81,10 +86,14 @@ struct Cfg {
   static constexpr int NS = NS_raw > 4 ? 4 : (NS_raw < 2 ? 2 : NS_raw);
   static constexpr int off_q = kWarps * NS * stage;                 // q: [8][D] fp32
   static constexpr int off_qsum = off_q + kMaxHeads * D * 4;        // [NB][8] per-block sums of q (K minimum)
-  static constexpr int off_bar = off_qsum + NB * kMaxHeads * 4;      // mbarriers [kWarps][NS]
+  // OL: scaled, unrotated query values of the outlier slots [8][32] fp32, then their B fragments [2][32] x uint4
+  static constexpr int off_qo = align_up(off_qsum + NB * kMaxHeads * 4, 16);
+  static constexpr int off_qof = off_qo + kMaxHeads * 32 * 4;
+  static constexpr int off_bar = OL ? off_qof + 2 * 32 * 16 : off_qsum + NB * kMaxHeads * 4;  // mbarriers [kWarps][NS]
   static constexpr int off_ml = off_bar + kWarps * NS * 8;          // [kWarps][8] m and l
   static constexpr int smem = off_ml + 2 * kWarps * kMaxHeads * 4 + 1024;  // + alignment slack
-  static_assert(kWarps * kMaxHeads * D * 4 <= kWarps * NS * stage, "merge buffer must fit in the stages");
+  static_assert(kWarps * kMaxHeads * (D + (OL ? 32 : 0)) * 4 <= kWarps * NS * stage,
+                "merge buffer must fit in the stages");
 };
 
 struct Params {
@@ -102,6 +111,7 @@ struct Params {
   FusedAppend fa;
   kvq_cache cache;
   RowMap rows;   // body row of (sequence, KV head, position): contiguous or paged
+  float* ws_acco;  // outlier channels: their partial acc [B][Hq][splits][32]
 };
 
 // New tokens of sequence b in a fused step: the requested count if it fits, else 0.
@@ -130,11 +140,11 @@ __device__ __forceinline__ uint32_t khb(uint32_t h, int which) {
   }
 }
 
-template <int D, int KT, int VT>
+template <int D, int KT, int VT, bool OL>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const __grid_constant__ CUtensorMap tmKt, const __grid_constant__ CUtensorMap tmVt) {
-  using C = Cfg<D, KT, VT>;
+  using C = Cfg<D, KT, VT, OL>;
   constexpr int NB = C::NB;
   constexpr int NS = C::NS;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -236,6 +246,12 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
       bulk_g2s(st + C::off_vd, p.v_d + row * NB * C::VH, 16 * NB * C::VH, &wbar[s]);
       if constexpr (C::K5) bulk_g2s(st + C::off_kqh, p.k_qh + row * NB, 16 * NB * 4, &wbar[s]);
       if constexpr (C::V5) bulk_g2s(st + C::off_vqh, p.v_qh + row * NB, 16 * NB * 4, &wbar[s]);
+      if constexpr (OL) {  // outlier rows: 32 codes + one fp16 scale per token, K and V
+        bulk_g2s(st + C::off_ko, static_cast<const uint8_t*>(p.cache.k_oqs) + row * 32, 16 * 32, &wbar[s]);
+        bulk_g2s(st + C::off_vo, static_cast<const uint8_t*>(p.cache.v_oqs) + row * 32, 16 * 32, &wbar[s]);
+        bulk_g2s(st + C::off_kod, static_cast<const uint8_t*>(p.cache.k_od) + row * 2, 16 * 2, &wbar[s]);
+        bulk_g2s(st + C::off_vod, static_cast<const uint8_t*>(p.cache.v_od) + row * 2, 16 * 2, &wbar[s]);
+      }
     }
   };
 
@@ -271,6 +287,15 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     sq[i] = v;
   }
   __syncthreads();
+  float* qo = reinterpret_cast<float*>(smem + C::off_qo);  // OL: [8][32] unrotated, scaled
+  if constexpr (OL) {
+    if (warp == 0) {
+      const int ch = outlier_channel<D>(p.cache, kvh, lane);
+#pragma unroll
+      for (int hh = 0; hh < kMaxHeads; ++hh) qo[hh * 32 + lane] = ch >= 0 ? sq[hh * D + ch] * p.scale_log2 : 0.0f;
+    }
+    __syncthreads();
+  }
   {
     constexpr int G = (D >= 64 && D % 64 == 0) ? (((D & (D - 1)) == 0) ? D : 64) : 32;
     for (int hh = warp; hh < kMaxHeads; hh += kWarps) {
@@ -323,8 +348,24 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     for (int blk = 0; blk < NB; ++blk)
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) reinterpret_cast<uint4*>(sq)[(blk * 2 + hf) * 32 + lane] = qf[blk][hf];
+    if constexpr (OL) {  // the outlier slots' B fragments, same layout as one block of qf
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const float4 q4 = *reinterpret_cast<const float4*>(qo + g * 32 + 16 * hf + 4 * tig);
+        const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
+        float hi[4], lo[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          hi[j] = __half2float(__float2half_rn(qv[j]));
+          lo[j] = qv[j] - hi[j];
+        }
+        reinterpret_cast<uint4*>(smem + C::off_qof)[hf * 32 + lane] =
+            make_uint4(pack_h2(hi[0], hi[2]), pack_h2(hi[1], hi[3]), pack_h2(lo[0], lo[2]), pack_h2(lo[1], lo[3]));
+      }
+    }
   }
   __syncthreads();
+  const uint4* qofs = reinterpret_cast<const uint4*>(smem + C::off_qof);
 
   // ---- main loop ------------------------------------------------------------
   float acc[NB][2][4];
@@ -334,6 +375,11 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     for (int j = 0; j < 2; ++j)
 #pragma unroll
       for (int r = 0; r < 4; ++r) acc[i][j][r] = 0.0f;
+  float acco[OL ? 2 : 1][4];  // OL: outlier slots 0-15 / 16-31 (body tiles only)
+#pragma unroll
+  for (int j = 0; j < (OL ? 2 : 1); ++j)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) acco[j][r] = 0.0f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
   bool timed_out = false;
   int k_stop = my_tiles;
@@ -417,6 +463,23 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
           }
         }
       }
+      if constexpr (OL) {  // + d_O[t] * (codes_O[t] . q_O[h]): one q8_0 block in plain 32-byte rows
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4(smem_u32(st + C::off_ko) + rr * 32 + 16 * (mi >> 1), r0, r1, r2, r3);
+        r0 ^= 0x80808080u; r1 ^= 0x80808080u; r2 ^= 0x80808080u; r3 ^= 0x80808080u;
+        const uint32_t alo[4] = {i8_pair<0, 2>(r0), i8_pair<0, 2>(r1), i8_pair<1, 3>(r0), i8_pair<1, 3>(r1)};
+        const uint32_t ahi[4] = {i8_pair<0, 2>(r2), i8_pair<0, 2>(r3), i8_pair<1, 3>(r2), i8_pair<1, 3>(r3)};
+        const uint4 qa = qofs[lane], qb = qofs[32 + lane];
+        float cc[4] = {0.f, 0.f, 0.f, 0.f};
+        mma16816(cc, alo, qa.x, qa.y);
+        mma16816(cc, alo, qa.z, qa.w);
+        mma16816(cc, ahi, qb.x, qb.y);
+        mma16816(cc, ahi, qb.z, qb.w);
+        const __half* kod = reinterpret_cast<const __half*>(st + C::off_kod);
+        const float dk0 = __half2float(kod[g]), dk8 = __half2float(kod[g + 8]);
+        S[0] += dk0 * cc[0]; S[1] += dk0 * cc[1];
+        S[2] += dk8 * cc[2]; S[3] += dk8 * cc[3];
+      }
     } else {
       // ------------------------------- tail (bf16, stored as fp16 * 2^-8): scores
       const uint8_t* kt = st + C::off_kt;
@@ -461,6 +524,12 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
         for (int j = 0; j < 2; ++j) {
           acc[i][j][0] *= a0; acc[i][j][1] *= a1; acc[i][j][2] *= a0; acc[i][j][3] *= a1;
         }
+      if constexpr (OL) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          acco[j][0] *= a0; acco[j][1] *= a1; acco[j][2] *= a0; acco[j][3] *= a1;
+        }
+      }
       m0 = nm0; m1 = nm1;
     }
     const float ms0 = m0 == -INFINITY ? 0.0f : m0, ms1 = m1 == -INFINITY ? 0.0f : m1;
@@ -565,6 +634,21 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
           }
         }
       }
+      if constexpr (OL) {  // outlier slots += codes_O^T . (P * d_O), as one more q8_0 block
+        const __half* vod = reinterpret_cast<const __half*>(st + C::off_vod);
+        uint32_t bh0, bl0, bh1, bl1;
+        split_h2(pz[0] * __half2float(vod[2 * tig]), pz[1] * __half2float(vod[2 * tig + 1]), bh0, bl0);
+        split_h2(pz[2] * __half2float(vod[2 * tig + 8]), pz[3] * __half2float(vod[2 * tig + 9]), bh1, bl1);
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4_t(smem_u32(st + C::off_vo) + rr * 32 + 16 * (mi >> 1), r0, r1, r2, r3);
+        r0 ^= 0x80808080u; r1 ^= 0x80808080u; r2 ^= 0x80808080u; r3 ^= 0x80808080u;
+        const uint32_t a0[4] = {i8_pair<0, 2>(r0), i8_pair<1, 3>(r0), i8_pair<0, 2>(r1), i8_pair<1, 3>(r1)};
+        const uint32_t a1[4] = {i8_pair<0, 2>(r2), i8_pair<1, 3>(r2), i8_pair<0, 2>(r3), i8_pair<1, 3>(r3)};
+        mma16816(acco[0], a0, bh0, bh1);
+        mma16816(acco[0], a0, bl0, bl1);
+        mma16816(acco[1], a1, bh0, bh1);
+        mma16816(acco[1], a1, bl0, bl1);
+      }
     } else {
       // tail values are stored as fp16 * 2^-8, so P carries the factor 256
       uint32_t bh0, bl0, bh1, bl1;
@@ -641,6 +725,18 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
       base[(2 * tig) * D + cg8] = acc[blk][cc2][2] * f0;
       base[(2 * tig + 1) * D + cg8] = acc[blk][cc2][3] * f1;
     }
+  float* maco = macc + (size_t)kWarps * kMaxHeads * D;  // OL: [kWarps][8][32]
+  if constexpr (OL) {
+#pragma unroll
+    for (int cc2 = 0; cc2 < 2; ++cc2) {
+      const int sl = 16 * cc2 + 2 * g;
+      float* base = maco + (size_t)warp * kMaxHeads * 32;
+      base[(2 * tig) * 32 + sl] = acco[cc2][0] * f0;
+      base[(2 * tig + 1) * 32 + sl] = acco[cc2][1] * f1;
+      base[(2 * tig) * 32 + sl + 1] = acco[cc2][2] * f0;
+      base[(2 * tig + 1) * 32 + sl + 1] = acco[cc2][3] * f1;
+    }
+  }
   __syncthreads();
   for (int i = tid; i < nheads * D; i += kThreads) {
     const int hh = i / D, c = i % D;
@@ -648,6 +744,15 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) v += macc[((size_t)w * kMaxHeads + hh) * D + c];
     p.ws_acc[(((size_t)b * p.n_q_heads + head0 + hh) * p.splits + split) * D + c] = v;
+  }
+  if constexpr (OL) {
+    for (int i = tid; i < nheads * 32; i += kThreads) {
+      const int hh = i / 32, c = i % 32;
+      float v = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) v += maco[((size_t)w * kMaxHeads + hh) * 32 + c];
+      p.ws_acco[(((size_t)b * p.n_q_heads + head0 + hh) * p.splits + split) * 32 + c] = v;
+    }
   }
   if (tid < nheads) {
     float M = -INFINITY;
@@ -676,7 +781,8 @@ template <int D>
 __global__ void __launch_bounds__(kCombineThreads)
 decode_combine_kernel(const float* __restrict__ ws_acc, const float* __restrict__ ws_ml, int splits,
                       int rot_v, void* __restrict__ out, int out_dtype, int n_q_heads, int fused,
-                      FusedAppend fa, int32_t* __restrict__ seq_len, int max_ctx) {
+                      FusedAppend fa, int32_t* __restrict__ seq_len, int max_ctx,
+                      const float* __restrict__ ws_acco, const int32_t* __restrict__ oidx, int group) {
   constexpr int G = (D >= 64 && D % 64 == 0) ? (((D & (D - 1)) == 0) ? D : 64) : 32;
   constexpr int E = D / 32;
   constexpr int TPC = kCombineThreads / D >= 1 ? kCombineThreads / D : 1;  // threads per channel
@@ -729,8 +835,19 @@ decode_combine_kernel(const float* __restrict__ ws_acc, const float* __restrict_
     }
   }
   s_part[tid] = v;
+  // outlier channels: merged partial of slot tid
+  __shared__ float s_o[32];
+  if (ws_acco && tid < 32) {
+    const float* a = ws_acco + (size_t)row * splits * 32 + tid;
+    float t = 0.0f;
+    for (int s = 0; s < splits; ++s) {
+      const float w = s_w[s];
+      if (w != 0.0f) t += w * a[(size_t)s * 32];
+    }
+    s_o[tid] = t;
+  }
   __syncthreads();
-  // 4. warp 0: merged row / L, inverse rotation, store
+  // 4. warp 0: merged row / L, inverse rotation, (+ outlier channels), store
   if (warp != 0) return;
   const float inv = L > 0.0f ? 1.0f / L : 0.0f;
   float x[E];
@@ -746,6 +863,21 @@ decode_combine_kernel(const float* __restrict__ ws_acc, const float* __restrict_
     warp_fwht<D, G>(x, lane);
 #pragma unroll
     for (int j = 0; j < E; ++j) x[j] *= inv_sqrt_group<G>();
+  }
+  if (ws_acco) {  // slot i's merged value goes to its channel, in the original basis
+    const int kvh = (row % n_q_heads) / group;
+    const int ch = oidx[(size_t)kvh * 32 + lane];
+    const int prev = __shfl_up_sync(0xffffffffu, ch, 1);
+    const bool ok = ch >= 0 && ch < D && (lane == 0 || prev < ch);
+    const float val = s_o[lane] * inv;
+#pragma unroll 4
+    for (int sl = 0; sl < 32; ++sl) {
+      const int cs = __shfl_sync(0xffffffffu, ok ? ch : -1, sl);
+      const float vs = __shfl_sync(0xffffffffu, val, sl);
+#pragma unroll
+      for (int j = 0; j < E; ++j)
+        if (fwht_channel<D, G>(lane, j) == cs) x[j] += vs;
+    }
   }
 #pragma unroll
   for (int j = 0; j < E; ++j) {
@@ -792,11 +924,11 @@ bool make_map(CUtensorMap* m, void* base, CUtensorMapDataType dt, int elem, long
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int KT, int VT>
+template <int D, int KT, int VT, bool OL>
 cudaError_t run_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, const void* q, int q_dtype,
                        int n_q_heads, float scale, void* out, int out_dtype, void* ws, cudaStream_t st,
                        const FusedAppend* fa) {
-  using Cf = Cfg<D, KT, VT>;
+  using Cf = Cfg<D, KT, VT, OL>;
   Params p{};
   p.k_d = static_cast<const uint8_t*>(c.k_d); p.v_d = static_cast<const uint8_t*>(c.v_d);
   p.k_qh = static_cast<const uint32_t*>(c.k_qh); p.v_qh = static_cast<const uint32_t*>(c.v_qh);
@@ -804,6 +936,7 @@ cudaError_t run_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, cons
   const size_t nacc = (size_t)c.batch * n_q_heads * plan.splits * D;
   p.ws_acc = static_cast<float*>(ws);
   p.ws_ml = p.ws_acc + nacc;
+  p.ws_acco = OL ? p.ws_ml + (size_t)c.batch * n_q_heads * plan.splits * 2 : nullptr;
   p.n_kv_heads = c.n_kv_heads; p.max_ctx = c.max_ctx; p.tail_len = c.tail_len;
   p.q_dtype = q_dtype; p.n_q_heads = n_q_heads; p.group = n_q_heads / c.n_kv_heads;
   p.heads_per_cta = plan.heads_per_cta; p.head_groups = plan.head_groups;
@@ -827,7 +960,7 @@ cudaError_t run_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, cons
         !make_map(&mvt, c.v_tail, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, trows, 2 * D, Cf::WT, Cf::TT))
       return cudaErrorInvalidValue;
   }
-  auto kern = decode_split_kernel<D, KT, VT>;
+  auto kern = decode_split_kernel<D, KT, VT, OL>;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), Cf::smem);
   if (e != cudaSuccess) return e;
   dim3 grid(plan.splits, c.n_kv_heads * plan.head_groups, c.batch);
@@ -841,20 +974,29 @@ cudaError_t run_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, cons
     if (e != cudaSuccess) return e;
   }
   decode_combine_kernel<D><<<total, kCombineThreads, wbytes, st>>>(p.ws_acc, p.ws_ml, plan.splits, rot.v, out, out_dtype,
-                                                                   n_q_heads, p.fused, p.fa, c.seq_len, c.max_ctx);
+                                                                   n_q_heads, p.fused, p.fa, c.seq_len, c.max_ctx,
+                                                                   p.ws_acco, c.outlier_idx, p.group);
   return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t run_decode_d(const kvq_cache& c, Rot rot, const DecodePlan& plan, const void* q, int q_dtype, int nq,
                          float scale, void* out, int out_dtype, void* ws, cudaStream_t st, const FusedAppend* fa) {
-#define KVQ_CASE(KT, VT)                                                                          \
-  if (c.k_type == KT && c.v_type == VT)                                                           \
-    return run_decode<D, KT, VT>(c, rot, plan, q, q_dtype, nq, scale, out, out_dtype, ws, st, fa);
-#define KVQ_CASES_K(KT) KVQ_CASE(KT, KVQ_TYPE_Q4_0) KVQ_CASE(KT, KVQ_TYPE_Q5_0) KVQ_CASE(KT, KVQ_TYPE_Q8_0) \
-                        KVQ_CASE(KT, KVQ_TYPE_Q4_1) KVQ_CASE(KT, KVQ_TYPE_Q5_1)
+#define KVQ_CASE(KT, VT, OL)                                                                          \
+  if (c.k_type == KT && c.v_type == VT)                                                               \
+    return run_decode<D, KT, VT, OL>(c, rot, plan, q, q_dtype, nq, scale, out, out_dtype, ws, st, fa);
+#define KVQ_CASES_K(KT) KVQ_CASE(KT, KVQ_TYPE_Q4_0, false) KVQ_CASE(KT, KVQ_TYPE_Q5_0, false)         \
+                        KVQ_CASE(KT, KVQ_TYPE_Q8_0, false) KVQ_CASE(KT, KVQ_TYPE_Q4_1, false)         \
+                        KVQ_CASE(KT, KVQ_TYPE_Q5_1, false)
+#define KVQ_CASES_K_OL(KT) KVQ_CASE(KT, KVQ_TYPE_Q4_0, true) KVQ_CASE(KT, KVQ_TYPE_Q5_0, true) \
+                           KVQ_CASE(KT, KVQ_TYPE_Q8_0, true)
+  if (c.n_outlier) {  // outlier channels: the q4_0 / q5_0 / q8_0 pairs
+    KVQ_CASES_K_OL(KVQ_TYPE_Q4_0) KVQ_CASES_K_OL(KVQ_TYPE_Q5_0) KVQ_CASES_K_OL(KVQ_TYPE_Q8_0)
+    return cudaErrorInvalidValue;
+  }
   KVQ_CASES_K(KVQ_TYPE_Q4_0) KVQ_CASES_K(KVQ_TYPE_Q5_0) KVQ_CASES_K(KVQ_TYPE_Q8_0)
   KVQ_CASES_K(KVQ_TYPE_Q4_1) KVQ_CASES_K(KVQ_TYPE_Q5_1)
+#undef KVQ_CASES_K_OL
 #undef KVQ_CASES_K
 #undef KVQ_CASE
   return cudaErrorInvalidValue;

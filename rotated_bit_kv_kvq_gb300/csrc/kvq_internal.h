@@ -60,9 +60,11 @@ struct DecodePlan {
   int tail_chunk;      // tail slots per CTA
   int splits_tail;     // CTAs per (seq, head group) over the tail
   int splits;          // splits_body + splits_tail
-  size_t ws_bytes;     // workspace bytes
+  size_t ws_bytes;     // workspace bytes: acc [B][Hq][splits][D], (m, l) [B][Hq][splits][2],
+                       // then, with outlier channels, their acc [B][Hq][splits][32]
 };
-bool decode_supported(int d, int kt, int vt);
+// n_outlier > 0: the q4_0 / q5_0 / q8_0 pairs at head_dim 64, 128 and 256.
+bool decode_supported(int d, int kt, int vt, int n_outlier);
 DecodePlan plan_decode(const kvq_cache& c, int n_q_heads, int sm_count);
 // Address of the fixed decode scratch array on the current device (looked up
 // once per device); size in *bytes.

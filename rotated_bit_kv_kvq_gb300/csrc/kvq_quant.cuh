@@ -164,10 +164,26 @@ __device__ __forceinline__ void quantize_block(const float* y, int qt, int r, ui
   }
 }
 
+// Outlier channel of slot `lane` of KV head h (n_outlier = 32): the caller's
+// list must be strictly increasing inside [0, D).  Returns the channel, or -1
+// for an invalid slot (and sets KVQ_DEV_ERR_OUTLIER once per warp).
+template <int D>
+__device__ __forceinline__ int outlier_channel(const kvq_cache& c, int h, int lane) {
+  const int ch = c.outlier_idx[(size_t)h * 32 + lane];
+  const int prev = __shfl_up_sync(0xffffffffu, ch, 1);
+  const bool ok = ch >= 0 && ch < D && (lane == 0 || prev < ch);
+  const unsigned bad = __ballot_sync(0xffffffffu, !ok);
+  if (bad && lane == 0) atomicOr(&c.status[0], KVQ_DEV_ERR_OUTLIER);
+  return ok ? ch : -1;
+}
+
 // One warp: rotate (when `rot`), quantize and store one K (which = 0) or V
 // (which = 1) vector of (sequence b, KV head h) at position pos, reading its
 // head_dim values from src[elem0 ..]; also its bf16 tail row (slot pos % T)
 // when `to_tail`.  Lane l holds channels l*P .. l*P+P-1 of every G-wide group.
+// With outlier channels (c.n_outlier = 32) the body gets the vector with those
+// channels zeroed (then rotated and quantized), slot l's value goes to a q8_0
+// block of the outlier plane, unrotated, and the tail keeps the whole vector.
 template <int D, int G>
 __device__ __forceinline__ void store_vector(const kvq_cache& c, int which, int b, int h, int pos, bool to_tail,
                                              const void* src, size_t elem0, int in_dtype, bool rot, int lane) {
@@ -177,11 +193,41 @@ __device__ __forceinline__ void store_vector(const kvq_cache& c, int which, int 
   float v[E];
 #pragma unroll
   for (int gi = 0; gi < D / G; ++gi) load_vals<P>(src, in_dtype, elem0 + gi * G + lane * P, v + gi * P);
+  const bool outl = c.n_outlier != 0;
+  float ov = 0.0f;      // outlier slot `lane`: its value (original basis)
+  float vt[E];          // whole vector for the tail when the body's differs
+  if (outl) {
+    const int ch = outlier_channel<D>(c, h, lane);
+    // slot value: channel ch lives in lane (ch % G) / P, register (ch / G) * P + ch % P
+    const int src_lane = ch < 0 ? 0 : (ch % G) / P, src_reg = ch < 0 ? -1 : (ch / G) * P + ch % P;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const float t = __shfl_sync(0xffffffffu, v[e], src_lane);
+      if (e == src_reg) ov = t;
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) vt[e] = v[e];
+    // zero this lane's channels that are outlier slots
+#pragma unroll 4
+    for (int sl = 0; sl < 32; ++sl) {
+      const int cs = __shfl_sync(0xffffffffu, ch, sl);
+      if (cs >= 0 && (cs % G) / P == lane) {
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+          if (e == (cs / G) * P + cs % P) v[e] = 0.0f;
+      }
+    }
+  }
   if (rot) {
-    warp_fwht<D, G>(v, lane);
     const float s = inv_sqrt_group<G>();
+    warp_fwht<D, G>(v, lane);
 #pragma unroll
     for (int j = 0; j < E; ++j) v[j] *= s;
+    if (outl && to_tail) {
+      warp_fwht<D, G>(vt, lane);
+#pragma unroll
+      for (int j = 0; j < E; ++j) vt[j] *= s;
+    }
   }
   const int qt = which ? c.v_type : c.k_type;
   const long long brow = body_row(row_map(c), b, h, pos);
@@ -201,12 +247,17 @@ __device__ __forceinline__ void store_vector(const kvq_cache& c, int which, int 
       quantize_block<P>(v + gi * P, qt, r, qs + blk * blk_bytes, qh ? qh + row * NB + blk : nullptr,
                         dp + blk * (type_has_min(qt) ? 4 : 2));
     }
+    if (outl) {  // one q8_0 block, slot = lane
+      uint8_t* oqs = static_cast<uint8_t*>(which ? c.v_oqs : c.k_oqs) + row * 32;
+      uint16_t* od = static_cast<uint16_t*>(which ? c.v_od : c.k_od) + row;
+      quantize_block<1>(&ov, KVQ_TYPE_Q8_0, lane, oqs, nullptr, od);
+    }
   }
   if (to_tail) {
     uint16_t* tail = static_cast<uint16_t*>(which ? c.v_tail : c.k_tail) +
                      (((size_t)b * c.n_kv_heads + h) * c.tail_len + pos % c.tail_len) * D;
 #pragma unroll
-    for (int gi = 0; gi < D / G; ++gi) store_bf16<P>(tail + gi * G + lane * P, v + gi * P);
+    for (int gi = 0; gi < D / G; ++gi) store_bf16<P>(tail + gi * G + lane * P, (outl ? vt : v) + gi * P);
   }
 }
 

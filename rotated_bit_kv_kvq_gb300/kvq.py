@@ -31,8 +31,10 @@ KVQ_F32, KVQ_BF16, KVQ_F16 = 0, 1, 2
 KVQ_ROT_AUTO, KVQ_ROT_K_OFF, KVQ_ROT_V_OFF = 1, 2, 4
 KVQ_INPUT_PREROTATED = 1
 (KVQ_PLANE_K_QS, KVQ_PLANE_K_QH, KVQ_PLANE_K_D, KVQ_PLANE_V_QS, KVQ_PLANE_V_QH, KVQ_PLANE_V_D,
- KVQ_PLANE_K_TAIL, KVQ_PLANE_V_TAIL, KVQ_PLANE_SEQ_LEN, KVQ_PLANE_STATUS) = range(10)
+ KVQ_PLANE_K_TAIL, KVQ_PLANE_V_TAIL, KVQ_PLANE_SEQ_LEN, KVQ_PLANE_STATUS, KVQ_PLANE_K_OQS, KVQ_PLANE_K_OD,
+ KVQ_PLANE_V_OQS, KVQ_PLANE_V_OD, KVQ_PLANE_OUTLIER_IDX) = range(15)
 KVQ_DEV_ERR_APPEND_RANGE, KVQ_DEV_ERR_PREFILL_RANGE, KVQ_DEV_ERR_TIMEOUT, KVQ_DEV_ERR_PAGE = 1, 2, 4, 8
+KVQ_DEV_ERR_OUTLIER = 16
 
 
 class kvq_cache(ctypes.Structure):
@@ -45,6 +47,8 @@ class kvq_cache(ctypes.Structure):
         ("k_tail", ctypes.c_void_p), ("v_tail", ctypes.c_void_p),
         ("seq_len", ctypes.c_void_p), ("status", ctypes.c_void_p),
         ("page_tokens", ctypes.c_int32), ("n_pages", ctypes.c_int32), ("page_table", ctypes.c_void_p),
+        ("n_outlier", ctypes.c_int32), ("outlier_idx", ctypes.c_void_p),
+        ("k_oqs", ctypes.c_void_p), ("k_od", ctypes.c_void_p), ("v_oqs", ctypes.c_void_p), ("v_od", ctypes.c_void_p),
     ]
 
 
@@ -222,7 +226,7 @@ def kvq_resolve_rotation(cache: kvq_cache):
 
 
 def descriptor(batch, n_kv_heads, head_dim, max_ctx, tail_len, k_type, v_type, flags=KVQ_ROT_AUTO,
-               page_tokens=0, n_pages=0) -> kvq_cache:
+               page_tokens=0, n_pages=0, n_outlier=0) -> kvq_cache:
     """A descriptor with sizes and types only (pointers NULL)."""
     c = kvq_cache()
     c.batch, c.n_kv_heads, c.head_dim, c.max_ctx, c.tail_len = batch, n_kv_heads, head_dim, max_ctx, tail_len
@@ -230,6 +234,7 @@ def descriptor(batch, n_kv_heads, head_dim, max_ctx, tail_len, k_type, v_type, f
     c.v_type = TYPE_IDS.get(v_type, v_type)
     c.flags = flags
     c.page_tokens, c.n_pages = page_tokens, n_pages
+    c.n_outlier = n_outlier
     return c
 
 
@@ -237,15 +242,18 @@ class KVCache:
     """The planes of one cache, allocated with torch on the current device."""
 
     def __init__(self, batch, n_kv_heads, head_dim, max_ctx, tail_len, k_type, v_type,
-                 flags=KVQ_ROT_AUTO, device="cuda", page_tokens=0, n_pages=0, page_table=None):
+                 flags=KVQ_ROT_AUTO, device="cuda", page_tokens=0, n_pages=0, page_table=None,
+                 outliers=None):
         """page_tokens > 0: paged body planes, a pool of n_pages pages (default: batch *
         max_ctx / page_tokens) and a page table (device int32 [batch][max_ctx / page_tokens];
-        default: sequence b owns pages b * per_seq ...)."""
+        default: sequence b owns pages b * per_seq ...).  outliers: int [n_kv_heads][32],
+        each row the strictly increasing channels kept at 8 bits (None: off)."""
         import torch
         if page_tokens and not n_pages:
             n_pages = batch * (max_ctx // page_tokens)
+        n_outlier = 0 if outliers is None else len(outliers[0])
         self.desc = descriptor(batch, n_kv_heads, head_dim, max_ctx, tail_len, k_type, v_type, flags,
-                               page_tokens, n_pages)
+                               page_tokens, n_pages, n_outlier)
         if page_tokens:
             per_seq = max_ctx // page_tokens
             if page_table is None:
@@ -253,7 +261,13 @@ class KVCache:
             self.page_table = page_table.to(device=device, dtype=torch.int32).contiguous()
             self.desc.page_table = self.page_table.data_ptr()
         self.planes = {}
-        names = ["k_qs", "k_qh", "k_d", "v_qs", "v_qh", "v_d", "k_tail", "v_tail", "seq_len", "status"]
+        names = ["k_qs", "k_qh", "k_d", "v_qs", "v_qh", "v_d", "k_tail", "v_tail", "seq_len", "status",
+                 "k_oqs", "k_od", "v_oqs", "v_od"]
+        if n_outlier:
+            self.outlier_idx = torch.as_tensor(outliers, dtype=torch.int32).to(device).contiguous()
+            if tuple(self.outlier_idx.shape) != (n_kv_heads, n_outlier):
+                raise ValueError("outliers: [n_kv_heads][n_outlier]")
+            self.desc.outlier_idx = self.outlier_idx.data_ptr()
         for idx, name in enumerate(names):
             nbytes = kvq_plane_bytes(self.desc, idx)
             if nbytes == 0:
