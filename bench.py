@@ -374,6 +374,8 @@ def run_ours(args):
             line["format_pairs"] = run_format_pairs(torch, kvq, w, max(5, K // 5), peak)
             line["paged"] = run_format_pairs(torch, kvq, w, max(5, K // 5), peak,
                                              pairs=((w.k_type, w.v_type),), page_tokens=256)[0]
+            line["outliers"] = run_format_pairs(torch, kvq, w, max(5, K // 5), peak,
+                                                pairs=((w.k_type, w.v_type),), outliers=True)[0]
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
         print(json.dumps(line), flush=True)
@@ -388,10 +390,28 @@ def run_ours(args):
 FORMAT_PAIRS = (("q5_0", "q4_1"), ("q8_0", "q5_1"))
 
 
-def run_format_pairs(torch, kvq, w: wl.Workload, steps: int, peak: float, pairs=FORMAT_PAIRS, page_tokens=0):
+def outlier_lists(w: wl.Workload, seed: int) -> np.ndarray:
+    """Per KV head, 32 channels kept at 8 bits: the synthetic history's K and V
+    outlier channels (the draws fill_cache makes with the same seed), then the
+    lowest other channels, sorted."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    k_chan = wl.outlier_channels(rng, w.n_kv_heads, w.head_dim, w.n_outliers)
+    v_chan = wl.outlier_channels(rng, w.n_kv_heads, w.head_dim, w.n_outliers)
+    out = []
+    for h in range(w.n_kv_heads):
+        chosen = sorted(set(k_chan[h].tolist()) | set(v_chan[h].tolist()))[:32]
+        rest = [c for c in range(w.head_dim) if c not in chosen]
+        out.append(sorted(chosen + rest[:32 - len(chosen)]))
+    return np.asarray(out, dtype=np.int64)
+
+
+def run_format_pairs(torch, kvq, w: wl.Workload, steps: int, peak: float, pairs=FORMAT_PAIRS, page_tokens=0,
+                     outliers=False):
     """Decode call alone at the workload's context for other K/V format pairs, or
     (page_tokens > 0) from a paged cache whose pages are handed out in a shuffled
-    order (a pool with 5% spare pages)."""
+    order (a pool with 5% spare pages), or (outliers) with 32 channels per KV head
+    kept as unrotated q8_0 (their codes and scales add 2 x 34 bytes per body token
+    and KV head)."""
     import dataclasses
     res = []
     for kt, vt in pairs:
@@ -406,7 +426,8 @@ def run_format_pairs(torch, kvq, w: wl.Workload, steps: int, peak: float, pairs=
             g.manual_seed(5)
             table = torch.randperm(n_pages, generator=g)[:w2.batch * per_seq].to(torch.int32)
             paged = dict(page_tokens=page_tokens, n_pages=n_pages, page_table=table)
-        cache = kvq.KVCache(w2.batch, w2.n_kv_heads, w2.head_dim, max_ctx, w2.tail_len, kt, vt, **paged)
+        extra = dict(outliers=outlier_lists(w2, 7).tolist()) if outliers else {}
+        cache = kvq.KVCache(w2.batch, w2.n_kv_heads, w2.head_dim, max_ctx, w2.tail_len, kt, vt, **paged, **extra)
         _, _, gen = fill_cache(torch, kvq, cache, w2, w2.ctx, seed=7)
         qs = [torch.randn(w2.batch, w2.n_q_heads, w2.head_dim, generator=gen, device="cuda").to(torch.bfloat16)
               for _ in range(4)]
@@ -425,13 +446,18 @@ def run_format_pairs(torch, kvq, w: wl.Workload, steps: int, peak: float, pairs=
         st, bits = kvq.kvq_sync_status(cache.desc)
         assert st == 0, (st, bits)
         ms = e0.elapsed_time(e1) / steps
-        nbytes = decode_bytes(w2, cache.seq_len.cpu().numpy())
+        lens = cache.seq_len.cpu().numpy()
+        nbytes = decode_bytes(w2, lens)
+        if outliers:
+            nbytes += sum(max(0, int(n) - w2.tail_len) for n in lens) * w2.n_kv_heads * 2 * 34
         gbs = nbytes / (ms * 1e-3) / 1e9
         r = {"k_type": kt, "v_type": vt, "ctx": w2.ctx, "ms_per_call": round(ms, 5),
              "bytes_per_call": int(nbytes), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)}
         if page_tokens:
             r["page_tokens"] = page_tokens
             r["layout"] = "paged, shuffled page table"
+        if outliers:
+            r["n_outlier"] = 32
         res.append(r)
         del cache, ws
         torch.cuda.empty_cache()

@@ -50,8 +50,13 @@ append_kernel(kvq_cache c, int rot_k, int rot_v, const void* __restrict__ kin, c
       if (i == 0 && h == 0 && which == 0 && lane == 0) atomicOr(&c.status[0], KVQ_DEV_ERR_APPEND_RANGE);
     } else if (i < nb) {
       const bool rot = (which ? rot_v : rot_k) && !prerotated;
-      store_vector<D, G>(c, which, b, h, n0 + i, c.tail_len > 0 && i >= nb - c.tail_len, which ? vin : kin,
-                         size_t(vec) * D, in_dtype, rot, lane);
+      const bool to_tail = c.tail_len > 0 && i >= nb - c.tail_len;
+      if (c.n_outlier)
+        store_vector<D, G, true>(c, which, b, h, n0 + i, to_tail, which ? vin : kin, size_t(vec) * D, in_dtype, rot,
+                                 lane);
+      else
+        store_vector<D, G, false>(c, which, b, h, n0 + i, to_tail, which ? vin : kin, size_t(vec) * D, in_dtype, rot,
+                                  lane);
     }
   }
 

@@ -264,7 +264,7 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     for (int t = warp; t < 2 * nn; t += kWarps) {
       const int i = t >> 1, which = t & 1;
       const bool rot = (which ? p.rot_v : p.rot_k) && !p.fa.prerotated;
-      store_vector<D, GQ>(p.cache, which, b, kvh, n0 + i, true, which ? p.fa.v : p.fa.k,
+      store_vector<D, GQ, OL>(p.cache, which, b, kvh, n0 + i, true, which ? p.fa.v : p.fa.k,
                           (((size_t)b * p.fa.n_new + i) * p.n_kv_heads + kvh) * D, p.fa.in_dtype, rot, lane);
     }
     asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -777,7 +777,7 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
 // ---------------------------------------------------------------------------
 constexpr int kCombineThreads = 256;
 
-template <int D>
+template <int D, bool OL>
 __global__ void __launch_bounds__(kCombineThreads)
 decode_combine_kernel(const float* __restrict__ ws_acc, const float* __restrict__ ws_ml, int splits,
                       int rot_v, void* __restrict__ out, int out_dtype, int n_q_heads, int fused,
@@ -837,7 +837,7 @@ decode_combine_kernel(const float* __restrict__ ws_acc, const float* __restrict_
   s_part[tid] = v;
   // outlier channels: merged partial of slot tid
   __shared__ float s_o[32];
-  if (ws_acco && tid < 32) {
+  if (OL && tid < 32) {
     const float* a = ws_acco + (size_t)row * splits * 32 + tid;
     float t = 0.0f;
     for (int s = 0; s < splits; ++s) {
@@ -864,7 +864,7 @@ decode_combine_kernel(const float* __restrict__ ws_acc, const float* __restrict_
 #pragma unroll
     for (int j = 0; j < E; ++j) x[j] *= inv_sqrt_group<G>();
   }
-  if (ws_acco) {  // slot i's merged value goes to its channel, in the original basis
+  if constexpr (OL) {  // slot i's merged value goes to its channel, in the original basis
     const int kvh = (row % n_q_heads) / group;
     const int ch = oidx[(size_t)kvh * 32 + lane];
     const int prev = __shfl_up_sync(0xffffffffu, ch, 1);
@@ -970,10 +970,10 @@ cudaError_t run_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, cons
   const int total = c.batch * n_q_heads;
   const size_t wbytes = (size_t)plan.splits * sizeof(float);
   if (wbytes > 48 * 1024) {
-    e = ensure_dynamic_smem(reinterpret_cast<const void*>(decode_combine_kernel<D>), (int)wbytes);
+    e = ensure_dynamic_smem(reinterpret_cast<const void*>(decode_combine_kernel<D, OL>), (int)wbytes);
     if (e != cudaSuccess) return e;
   }
-  decode_combine_kernel<D><<<total, kCombineThreads, wbytes, st>>>(p.ws_acc, p.ws_ml, plan.splits, rot.v, out, out_dtype,
+  decode_combine_kernel<D, OL><<<total, kCombineThreads, wbytes, st>>>(p.ws_acc, p.ws_ml, plan.splits, rot.v, out, out_dtype,
                                                                    n_q_heads, p.fused, p.fa, c.seq_len, c.max_ctx,
                                                                    p.ws_acco, c.outlier_idx, p.group);
   return cudaGetLastError();

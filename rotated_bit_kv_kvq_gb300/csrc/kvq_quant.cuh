@@ -184,7 +184,9 @@ __device__ __forceinline__ int outlier_channel(const kvq_cache& c, int h, int la
 // With outlier channels (c.n_outlier = 32) the body gets the vector with those
 // channels zeroed (then rotated and quantized), slot l's value goes to a q8_0
 // block of the outlier plane, unrotated, and the tail keeps the whole vector.
-template <int D, int G>
+// OLW: whether that code is compiled in (callers without outlier channels leave
+// it out).
+template <int D, int G, bool OLW>
 __device__ __forceinline__ void store_vector(const kvq_cache& c, int which, int b, int h, int pos, bool to_tail,
                                              const void* src, size_t elem0, int in_dtype, bool rot, int lane) {
   constexpr int P = G / 32;
@@ -193,7 +195,7 @@ __device__ __forceinline__ void store_vector(const kvq_cache& c, int which, int 
   float v[E];
 #pragma unroll
   for (int gi = 0; gi < D / G; ++gi) load_vals<P>(src, in_dtype, elem0 + gi * G + lane * P, v + gi * P);
-  const bool outl = c.n_outlier != 0;
+  const bool outl = OLW && c.n_outlier != 0;
   float ov = 0.0f;      // outlier slot `lane`: its value (original basis)
   float vt[E];          // whole vector for the tail when the body's differs
   if (outl) {
@@ -207,16 +209,16 @@ __device__ __forceinline__ void store_vector(const kvq_cache& c, int which, int 
     }
 #pragma unroll
     for (int e = 0; e < E; ++e) vt[e] = v[e];
-    // zero this lane's channels that are outlier slots
+    // zero this lane's channels that are outlier slots (a register bit mask, so
+    // that v is never indexed by a run-time value)
+    uint32_t zmask = 0;
 #pragma unroll 4
     for (int sl = 0; sl < 32; ++sl) {
       const int cs = __shfl_sync(0xffffffffu, ch, sl);
-      if (cs >= 0 && (cs % G) / P == lane) {
-#pragma unroll
-        for (int e = 0; e < E; ++e)
-          if (e == (cs / G) * P + cs % P) v[e] = 0.0f;
-      }
+      if (cs >= 0 && (cs % G) / P == lane) zmask |= 1u << ((cs / G) * P + cs % P);
     }
+#pragma unroll
+    for (int e = 0; e < E; ++e) v[e] = ((zmask >> e) & 1u) ? 0.0f : v[e];
   }
   if (rot) {
     const float s = inv_sqrt_group<G>();
@@ -257,7 +259,10 @@ __device__ __forceinline__ void store_vector(const kvq_cache& c, int which, int 
     uint16_t* tail = static_cast<uint16_t*>(which ? c.v_tail : c.k_tail) +
                      (((size_t)b * c.n_kv_heads + h) * c.tail_len + pos % c.tail_len) * D;
 #pragma unroll
-    for (int gi = 0; gi < D / G; ++gi) store_bf16<P>(tail + gi * G + lane * P, (outl ? vt : v) + gi * P);
+    for (int gi = 0; gi < D / G; ++gi) {  // (two calls: a selected array pointer would force v into local memory)
+      if (outl) store_bf16<P>(tail + gi * G + lane * P, vt + gi * P);
+      else store_bf16<P>(tail + gi * G + lane * P, v + gi * P);
+    }
   }
 }
 
