@@ -168,8 +168,10 @@ typedef struct kvq_cache {
    * tail keeps the whole rotated vector.  Attention adds q_O . k_O to every
    * body score and scatters sum_t p_t v_O,t back to those channels of the
    * output.  Requires head_dim >= 64 and inputs in the original basis (no
-   * KVQ_INPUT_PREROTATED).  Supported by append, the fused step and decode for
-   * the q4_0 / q5_0 / q8_0 pairs; prefill returns KVQ_ERR_UNSUPPORTED.  A row
+   * KVQ_INPUT_PREROTATED).  Supported by append, the fused step, decode (the
+   * q4_0 / q5_0 / q8_0 pairs) and prefill (its staging adds each key's and
+   * value's rotated outlier part to the dequantized rest); kvq_dequant_debug
+   * reads the low-bit planes only.  A row
    * of outlier_idx that is not strictly increasing in [0, head_dim) sets
    * KVQ_DEV_ERR_OUTLIER; its invalid slots are then ignored. */
   int32_t n_outlier;           /* 0 or 32                                     */

@@ -252,7 +252,7 @@ kvq_status kvq_decode_attention_noalloc(const kvq_cache* c, const void* q, int32
 
 size_t kvq_prefill_workspace_bytes(const kvq_cache* c, int32_t n_q_heads, int32_t n_tokens) {
   if (!shape_ok(c) || n_tokens < 0 || n_q_heads <= 0 || n_q_heads % c->n_kv_heads) return 0;
-  if (c->n_outlier || !kvq::prefill_supported(c->head_dim, n_q_heads / c->n_kv_heads)) return 0;
+  if (!kvq::prefill_supported(c->head_dim, n_q_heads / c->n_kv_heads)) return 0;
   return kvq::prefill_workspace_bytes(*c);
 }
 
@@ -269,7 +269,7 @@ kvq_status kvq_prefill_attention(const kvq_cache* c, const void* q, int32_t q_dt
   if (!(scale >= 0.0f) || scale > 1e30f) return KVQ_ERR_INVALID_ARG;
   if (n_tokens == 0) return KVQ_OK;
   if (!q || !out || !aligned16(q) || !aligned16(out)) return KVQ_ERR_INVALID_ARG;
-  if (c->n_outlier || !kvq::prefill_supported(c->head_dim, n_q_heads / c->n_kv_heads)) return KVQ_ERR_UNSUPPORTED;
+  if (!kvq::prefill_supported(c->head_dim, n_q_heads / c->n_kv_heads)) return KVQ_ERR_UNSUPPORTED;
   if (!workspace || !aligned16(workspace) || ws_bytes < kvq::prefill_workspace_bytes(*c)) return KVQ_ERR_WORKSPACE;
   const float sc = scale == 0.0f ? 1.0f / sqrtf(float(c->head_dim)) : scale;
   return from_cuda(kvq::launch_prefill(*c, r, q, q_dtype, n_q_heads, n_tokens, q_pos0, causal, sc, out, out_dtype,

@@ -103,6 +103,11 @@ struct SParams {
   uint8_t* ws;
   RowMap rows;   // body row of (sequence, KV head, position): contiguous or paged
   uint32_t* status;
+  // outlier channels (n_outlier = 32): unrotated q8_0 slots, added back rotated like the rest
+  int n_outlier, rot_k, rot_v;
+  const int32_t* oidx;
+  const int8_t* k_oqs; const int8_t* v_oqs;
+  const uint16_t* k_od; const uint16_t* v_od;
 };
 
 struct AParams {
@@ -179,6 +184,13 @@ __device__ __forceinline__ void load8(const SParams& p, bool is_v, int qt, bool 
   }
 }
 
+// x[e] += src[e], e < 8 (src 16-byte aligned, shared memory)
+__device__ __forceinline__ void add8(const float* src, float (&x)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(src)[0], c = reinterpret_cast<const float4*>(src)[1];
+  x[0] += a.x; x[1] += a.y; x[2] += a.z; x[3] += a.w;
+  x[4] += c.x; x[5] += c.y; x[6] += c.z; x[7] += c.w;
+}
+
 // ---------------------------------------------------------------------------
 // stage_kernel: one 64-key tile of one (sequence, KV head) -> workspace
 // ---------------------------------------------------------------------------
@@ -209,11 +221,52 @@ __global__ void __launch_bounds__(kStageThreads) stage_kernel(SParams p) {
   }
   const size_t body_row = size_t(brow);
   const size_t tail_row = tail ? bh * T + t % T : 0;
+  // Outlier channels: per body key, the 32 dequantized slot values (x 2^-8) are
+  // scattered to their channels and rotated like the rest (warp FWHT), for K
+  // and V, into [2][64 keys][D] fp32 after the tile in shared memory; the
+  // loop below adds them to the dequantized rest.
+  float* obuf = reinterpret_cast<float*>(sm + L::tile);
+  const bool ol = p.n_outlier != 0;
+  if (ol) {
+    for (int i = threadIdx.x; i < 2 * kPN * D / 4; i += kStageThreads)
+      reinterpret_cast<float4*>(obuf)[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    __syncthreads();
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int chn = p.oidx[(size_t)kvh * 32 + lane];
+    const int prev = __shfl_up_sync(0xffffffffu, chn, 1);
+    const bool ok = chn >= 0 && chn < D && (lane == 0 || prev < chn);
+    if (__ballot_sync(0xffffffffu, !ok) && lane == 0) atomicOr(p.status, KVQ_DEV_ERR_OUTLIER);
+    for (int kk = warp; kk < kPN; kk += kStageThreads / 32) {
+      const int tt = j * kPN + kk;
+      if (tt >= n || (T > 0 && tt >= n - T)) continue;  // past the end, or a tail key (whole vector in bf16)
+      const long long br = kvq::body_row(p.rows, b, kvh, tt);
+      if (br < 0) continue;
+      auto part = [&](const int8_t* oqs, const uint16_t* od, int rot, float* row) {
+        const float dd = __half2float(__ushort_as_half(od[br]));
+        if (ok) row[chn] = float(oqs[(size_t)br * 32 + lane]) * dd * kInvScale;
+        __syncwarp();
+        if (rot) {
+          constexpr int P = D / 32;
+          float v[P];
+#pragma unroll
+          for (int e = 0; e < P; ++e) v[e] = row[lane * P + e];
+          warp_fwht<D, D>(v, lane);
+#pragma unroll
+          for (int e = 0; e < P; ++e) row[lane * P + e] = v[e] * inv_sqrt_group<D>();
+          __syncwarp();
+        }
+      };
+      part(p.k_oqs, p.k_od, p.rot_k, obuf + (size_t)kk * D);
+      part(p.v_oqs, p.v_od, p.rot_v, obuf + (size_t)(kPN + kk) * D);
+    }
+    __syncthreads();
+  }
 #pragma unroll 1
   for (int ch = threadIdx.x / kPN; ch < NCH; ch += kStageThreads / kPN) {
     // K: row = key, 16-byte chunks of 8 channels
     float x[8];
     load8<D>(p, false, p.k_type, valid, tail, body_row, tail_row, ch, x);
+    if (ol) add8(obuf + (size_t)key * D + ch * 8, x);
     uint32_t h[4], l[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) split2(x[2 * e], x[2 * e + 1], h[e], l[e]);
@@ -223,6 +276,7 @@ __global__ void __launch_bounds__(kStageThreads) stage_kernel(SParams p) {
     *reinterpret_cast<uint4*>(sm + kPN * 128 + off) = make_uint4(l[0], l[1], l[2], l[3]);
     // V^T: row = channel, this key's 2-byte element in it
     load8<D>(p, true, p.v_type, valid, tail, body_row, tail_row, ch, x);
+    if (ol) add8(obuf + (size_t)(kPN + key) * D + ch * 8, x);
 #pragma unroll
     for (int e = 0; e < 4; ++e) split2(x[2 * e], x[2 * e + 1], h[e], l[e]);
 #pragma unroll
@@ -706,6 +760,10 @@ cudaError_t run_prefill(const kvq_cache& c, Rot rot, const void* q, int q_dtype,
   sp.k_type = c.k_type; sp.v_type = c.v_type; sp.n_tokens = n_tokens; sp.causal = causal ? 1 : 0;
   sp.max_tiles = max_tiles; sp.ws = static_cast<uint8_t*>(ws);
   sp.rows = row_map(c); sp.status = c.status;
+  sp.n_outlier = c.n_outlier; sp.rot_k = rot.k; sp.rot_v = rot.v;
+  sp.oidx = c.outlier_idx;
+  sp.k_oqs = static_cast<const int8_t*>(c.k_oqs); sp.v_oqs = static_cast<const int8_t*>(c.v_oqs);
+  sp.k_od = static_cast<const uint16_t*>(c.k_od); sp.v_od = static_cast<const uint16_t*>(c.v_od);
   AParams p{};
   p.ws = static_cast<const uint8_t*>(ws);
   p.seq_len = c.seq_len; p.status = c.status;
@@ -718,7 +776,8 @@ cudaError_t run_prefill(const kvq_cache& c, Rot rot, const void* q, int q_dtype,
   p.q_pos0 = q_pos0; p.causal = sp.causal;
   p.rot_k = rot.k; p.rot_v = rot.v;
   p.scale_log2 = scale * kPLog2e;
-  constexpr int stage_smem = L::tile + 1024;
+  // + the rotated outlier parts of the tile's keys and values, [2][64][D] fp32
+  const int stage_smem = L::tile + 1024 + (c.n_outlier ? 2 * kPN * D * 4 : 0);
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(stage_kernel<D>), stage_smem);
   if (e != cudaSuccess) return e;
   e = ensure_dynamic_smem(reinterpret_cast<const void*>(attn_kernel<D>), L::smem);

@@ -177,7 +177,7 @@ def test_decode_workspace_bytes_is_a_pure_size_query(built_lib_path):
 
 def test_outlier_planes_and_checks(built_lib_path):
     """Outlier channels: 32 per KV head, planes sized per body row (paged like the
-    body), every pointer required together; prerotated input and prefill refused."""
+    body), every pointer required together; prerotated input refused."""
     c = kvq.descriptor(2, 4, 128, 256, 16, "q4_0", "q8_0", n_outlier=32)
     assert kvq.kvq_plane_bytes(c, kvq.KVQ_PLANE_K_OQS) == 2 * 4 * 256 * 32
     assert kvq.kvq_plane_bytes(c, kvq.KVQ_PLANE_V_OD) == 2 * 4 * 256 * 2
@@ -202,9 +202,7 @@ def test_outlier_planes_and_checks(built_lib_path):
     ref = ctypes.byref(full)
     assert L.kvq_rotate_quantize_append(ref, FAKE, FAKE, 0, 1, None, kvq.KVQ_INPUT_PREROTATED, None) == \
         kvq.KVQ_ERR_INVALID_ARG
-    assert L.kvq_prefill_workspace_bytes(ref, 8, 64) == 0
-    assert L.kvq_prefill_attention(ref, FAKE, 0, 8, 64, None, 1, 0, 0.0, FAKE, 0, FAKE, 1 << 30, None) == \
-        kvq.KVQ_ERR_UNSUPPORTED
+    assert L.kvq_prefill_workspace_bytes(ref, 8, 64) == L.kvq_prefill_workspace_bytes(ctypes.byref(_full_desc()), 8, 64)
     # decode: the q4_0 / q5_0 / q8_0 pairs only; the workspace holds the outlier partials too
     assert L.kvq_decode_workspace_bytes(ref, 8) > L.kvq_decode_workspace_bytes(ctypes.byref(_full_desc()), 8)
     q41 = _full_desc(k_type=kvq.KVQ_TYPE_Q4_1)

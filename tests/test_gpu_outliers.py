@@ -1,5 +1,6 @@
 """Outlier channels kept at 8 bits (q8_0, original basis) beside the rotated
-low-bit rest: GPU write path and decode against the oracle.
+low-bit rest: GPU write path, decode, the fused step and prefill against the
+oracle.
 
 Outlier caches take inputs in the original basis only, so the GPU rotates
 the rest itself.  To keep both sides' caches identical the inputs are dyadic
@@ -198,3 +199,46 @@ def test_invalid_outlier_list_sets_status():
     st, bits = kvq.kvq_sync_status(gc.desc)
     assert bits & kvq.KVQ_DEV_ERR_OUTLIER
     assert torch.isfinite(out).all()
+
+
+@pytest.mark.parametrize("d,rot,kt,vt,T", [(64, True, "q4_0", "q8_0", 16), (64, True, "q5_0", "q4_0", 0),
+                                           (128, False, "q4_0", "q4_0", 32), (128, False, "q8_0", "q5_0", 0)])
+def test_prefill(d, rot, kt, vt, T):
+    """The staging adds each body key's and value's rotated outlier part to the
+    dequantized rest; causal and non-causal, GQA 4, ragged lengths."""
+    torch = require_gpu()
+    from rotated_bit_kv_kvq_gb300 import kvq
+    from test_gpu_prefill import gpu_prefill
+    rng = np.random.default_rng(87)
+    B, H, g, n = 2, 2, 4, 200
+    oidx = _outliers(rng, H, d)
+    gc, oc = _caches(kvq, B, H, d, 256, T, kt, vt, rot, oidx)
+    if rot:
+        k, v = _dyadic(rng, (B, n, H, d), oidx), _dyadic(rng, (B, n, H, d), oidx)
+    else:
+        k = rng.standard_normal((B, n, H, d)).astype(np.float32)
+        v = rng.standard_normal((B, n, H, d)).astype(np.float32)
+        for h in range(H):
+            k[:, :, h][..., oidx[h][:3]] *= 25
+    _append(kvq, torch, gc, oc, k, v, [n, 150])
+    q = rng.standard_normal((B, 150, H * g, d)).astype(np.float32)
+    for causal in (True, False):
+        assert_close(gpu_prefill(gc, q, "f32", torch, causal=causal),
+                     ko.prefill_attention(oc, q, causal=causal), what=f"d{d} {kt}/{vt} T{T} causal={causal}")
+
+
+def test_prefill_paged():
+    torch = require_gpu()
+    from rotated_bit_kv_kvq_gb300 import kvq
+    from test_gpu_prefill import gpu_prefill
+    rng = np.random.default_rng(88)
+    B, H, g, d, T, P, max_ctx = 2, 2, 2, 64, 8, 64, 256
+    n_pages = B * max_ctx // P + 2
+    table = rng.permutation(n_pages)[:B * max_ctx // P].astype(np.int32)
+    oidx = _outliers(rng, H, d)
+    gc, oc = _caches(kvq, B, H, d, max_ctx, T, "q8_0", "q4_0", True, oidx, page_tokens=P, n_pages=n_pages,
+                     page_table=torch.from_numpy(table))
+    k, v = _dyadic(rng, (B, 180, H, d), oidx), _dyadic(rng, (B, 180, H, d), oidx)
+    _append(kvq, torch, gc, oc, k, v, [180, 77])
+    q = rng.standard_normal((B, 77, H * g, d)).astype(np.float32)
+    assert_close(gpu_prefill(gc, q, "f32", torch), ko.prefill_attention(oc, q), what="paged prefill")
