@@ -99,12 +99,9 @@ typedef int32_t kvq_status;
 #define KVQ_PLANE_V_TAIL  7
 #define KVQ_PLANE_SEQ_LEN 8  /* int32 [batch]                               tokens stored per sequence           */
 #define KVQ_PLANE_STATUS  9  /* uint32 [4]                                  device status words; zero before use */
-#define KVQ_PLANE_K_OQS  10  /* int8 [rows][n_outlier]                      outlier-channel q8_0 codes (n_outlier > 0) */
-#define KVQ_PLANE_K_OD   11  /* fp16 [rows][n_outlier/32]                   their block scales                     */
-#define KVQ_PLANE_V_OQS  12
-#define KVQ_PLANE_V_OD   13
-#define KVQ_PLANE_OUTLIER_IDX 14  /* int32 [kv_heads][n_outlier]            the caller's outlier channel lists     */
-#define KVQ_NUM_PLANES   15
+#define KVQ_PLANE_OUTLIER 10  /* [rows / 16][1088 B]                         outlier-channel q8_0 blocks (n_outlier > 0) */
+#define KVQ_PLANE_OUTLIER_IDX 11  /* int32 [kv_heads][n_outlier]            the caller's outlier channel lists          */
+#define KVQ_NUM_PLANES   12
 
 /* device status word 0 bits (read by kvq_sync_status) */
 #define KVQ_DEV_ERR_APPEND_RANGE  1u  /* an append would pass max_ctx, or n_new_per_seq[b] not in [0, n_new] */
@@ -162,8 +159,10 @@ typedef struct kvq_cache {
    * 배경 기술) name this direction without fixing it; the reading implemented
    * here: per KV head the caller lists n_outlier channels of the original
    * basis (outlier_idx, strictly increasing).  The write path stores their
-   * values unrotated as q8_0 blocks in slot order (k_oqs / k_od, v_oqs / v_od,
-   * one row per body row, contiguous or paged like the body), sets them to
+   * values unrotated as one q8_0 block in slot order (plane `outl`, body rows
+   * contiguous or paged like the body, in groups of 16 rows of 1088 bytes: K
+   * codes int8 [16][32], V codes int8 [16][32], K scales fp16 [16], V scales
+   * fp16 [16], so one copy moves a 16-token tile), sets them to
    * zero in the vector and rotates / quantizes the rest as usual; the bf16
    * tail keeps the whole rotated vector.  Attention adds q_O . k_O to every
    * body score and scatters sum_t p_t v_O,t back to those channels of the
@@ -176,8 +175,7 @@ typedef struct kvq_cache {
    * KVQ_DEV_ERR_OUTLIER; its invalid slots are then ignored. */
   int32_t n_outlier;           /* 0 or 32                                     */
   const int32_t* outlier_idx;  /* device int32 [kv_heads][n_outlier]          */
-  void* k_oqs; void* k_od;     /* KVQ_PLANE_K_OQS / KVQ_PLANE_K_OD            */
-  void* v_oqs; void* v_od;     /* KVQ_PLANE_V_OQS / KVQ_PLANE_V_OD            */
+  void* outl;                  /* KVQ_PLANE_OUTLIER                           */
 } kvq_cache;
 
 /* Library version (KVQ_VERSION). */

@@ -56,10 +56,7 @@ size_t plane_bytes(const kvq_cache* c, int plane) {
     case KVQ_PLANE_V_TAIL: return size_t(c->batch) * c->n_kv_heads * size_t(c->tail_len) * d * 2;
     case KVQ_PLANE_SEQ_LEN: return size_t(c->batch) * 4;
     case KVQ_PLANE_STATUS: return 16;
-    case KVQ_PLANE_K_OQS:
-    case KVQ_PLANE_V_OQS: return rows * size_t(c->n_outlier);
-    case KVQ_PLANE_K_OD:
-    case KVQ_PLANE_V_OD: return rows * size_t(c->n_outlier / 32) * 2;
+    case KVQ_PLANE_OUTLIER: return c->n_outlier ? rows / 16 * 1088 : 0;  // rows is a multiple of 64
     case KVQ_PLANE_OUTLIER_IDX: return size_t(c->n_kv_heads) * size_t(c->n_outlier) * 4;
     default: return 0;
   }
@@ -79,7 +76,7 @@ kvq_status check_cache(const kvq_cache* c) {
   const bool has_tail = c->tail_len > 0;
   if (has_tail != (c->k_tail != nullptr) || has_tail != (c->v_tail != nullptr)) return KVQ_ERR_INVALID_ARG;
   if (has_tail && (!aligned16(c->k_tail) || !aligned16(c->v_tail))) return KVQ_ERR_INVALID_ARG;
-  const void* outl[] = {c->outlier_idx, c->k_oqs, c->k_od, c->v_oqs, c->v_od};
+  const void* outl[] = {c->outlier_idx, c->outl};
   for (const void* p : outl) {
     if (c->n_outlier && (!p || !aligned16(p))) return KVQ_ERR_INVALID_ARG;
     if (!c->n_outlier && p) return KVQ_ERR_INVALID_ARG;

@@ -45,6 +45,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kTailChunkMax = 4096;  // tail slots per CTA
 constexpr int kSmemBudget = 64 * 1024;       // stages; leaves room for 3 CTAs per SM
 constexpr int kCtasPerSm = 3;
+constexpr int kCtasPerSmOutl = 2;  // outlier-channel kernels: the extra block's registers
 
 constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 // widest TMA swizzle box (128, 64 or 32 bytes) that tiles a row exactly
@@ -66,7 +67,7 @@ struct Cfg {
   static constexpr int off_vd = off_kd + 16 * NB * KH;
   static constexpr int off_kqh = off_vd + 16 * NB * VH;
   static constexpr int off_vqh = off_kqh + (K5 ? 16 * NB * 4 : 0);
-  // outlier channels (OL): 32 int8 codes of K, then of V, per token (plain rows), then their fp16 scales
+  // outlier channels (OL): one 16-row group of the outlier plane (K codes, V codes, K scales, V scales)
   static constexpr int off_ko = align_up(off_vqh + (V5 ? 16 * NB * 4 : 0), 16);
   static constexpr int off_vo = off_ko + 16 * 32;
   static constexpr int off_kod = off_vo + 16 * 32;
@@ -141,7 +142,7 @@ __device__ __forceinline__ uint32_t khb(uint32_t h, int which) {
 }
 
 template <int D, int KT, int VT, bool OL>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+__global__ void __launch_bounds__(kThreads, OL ? kCtasPerSmOutl : kCtasPerSm)
 decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const __grid_constant__ CUtensorMap tmKt, const __grid_constant__ CUtensorMap tmVt) {
   using C = Cfg<D, KT, VT, OL>;
@@ -247,10 +248,9 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
       if constexpr (C::K5) bulk_g2s(st + C::off_kqh, p.k_qh + row * NB, 16 * NB * 4, &wbar[s]);
       if constexpr (C::V5) bulk_g2s(st + C::off_vqh, p.v_qh + row * NB, 16 * NB * 4, &wbar[s]);
       if constexpr (OL) {  // outlier rows: 32 codes + one fp16 scale per token, K and V
-        bulk_g2s(st + C::off_ko, static_cast<const uint8_t*>(p.cache.k_oqs) + row * 32, 16 * 32, &wbar[s]);
-        bulk_g2s(st + C::off_vo, static_cast<const uint8_t*>(p.cache.v_oqs) + row * 32, 16 * 32, &wbar[s]);
-        bulk_g2s(st + C::off_kod, static_cast<const uint8_t*>(p.cache.k_od) + row * 2, 16 * 2, &wbar[s]);
-        bulk_g2s(st + C::off_vod, static_cast<const uint8_t*>(p.cache.v_od) + row * 2, 16 * 2, &wbar[s]);
+        // the tile's 16-row group of the outlier plane has the stage's layout: one copy
+        bulk_g2s(st + C::off_ko, static_cast<const uint8_t*>(p.cache.outl) + (row / 16) * kOutlTile, kOutlTile,
+                 &wbar[s]);
       }
     }
   };

@@ -16,6 +16,10 @@
 
 namespace kvq {
 
+// Outlier-channel plane: groups of 16 body rows, 1088 bytes each (K codes
+// int8 [16][32], V codes int8 [16][32], K scales fp16 [16], V scales fp16 [16]).
+constexpr int kOutlTile = 1088;
+
 constexpr int kQK = 32;  // values per quantization block
 
 // ---------------------------------------------------------------------------

@@ -106,8 +106,7 @@ struct SParams {
   // outlier channels (n_outlier = 32): unrotated q8_0 slots, added back rotated like the rest
   int n_outlier, rot_k, rot_v;
   const int32_t* oidx;
-  const int8_t* k_oqs; const int8_t* v_oqs;
-  const uint16_t* k_od; const uint16_t* v_od;
+  const uint8_t* outl;   // [rows / 16][kOutlTile]: K codes, V codes, K scales, V scales of 16 rows
 };
 
 struct AParams {
@@ -241,9 +240,10 @@ __global__ void __launch_bounds__(kStageThreads) stage_kernel(SParams p) {
       if (tt >= n || (T > 0 && tt >= n - T)) continue;  // past the end, or a tail key (whole vector in bf16)
       const long long br = kvq::body_row(p.rows, b, kvh, tt);
       if (br < 0) continue;
-      auto part = [&](const int8_t* oqs, const uint16_t* od, int rot, float* row) {
-        const float dd = __half2float(__ushort_as_half(od[br]));
-        if (ok) row[chn] = float(oqs[(size_t)br * 32 + lane]) * dd * kInvScale;
+      const uint8_t* grp = p.outl + (size_t)(br / 16) * kOutlTile;
+      auto part = [&](int which, int rot, float* row) {
+        const float dd = __half2float(reinterpret_cast<const __half*>(grp + 1024 + which * 32)[br % 16]);
+        if (ok) row[chn] = float(reinterpret_cast<const int8_t*>(grp + which * 512 + (br % 16) * 32)[lane]) * dd * kInvScale;
         __syncwarp();
         if (rot) {
           constexpr int P = D / 32;
@@ -256,8 +256,8 @@ __global__ void __launch_bounds__(kStageThreads) stage_kernel(SParams p) {
           __syncwarp();
         }
       };
-      part(p.k_oqs, p.k_od, p.rot_k, obuf + (size_t)kk * D);
-      part(p.v_oqs, p.v_od, p.rot_v, obuf + (size_t)(kPN + kk) * D);
+      part(0, p.rot_k, obuf + (size_t)kk * D);
+      part(1, p.rot_v, obuf + (size_t)(kPN + kk) * D);
     }
     __syncthreads();
   }
@@ -762,8 +762,7 @@ cudaError_t run_prefill(const kvq_cache& c, Rot rot, const void* q, int q_dtype,
   sp.rows = row_map(c); sp.status = c.status;
   sp.n_outlier = c.n_outlier; sp.rot_k = rot.k; sp.rot_v = rot.v;
   sp.oidx = c.outlier_idx;
-  sp.k_oqs = static_cast<const int8_t*>(c.k_oqs); sp.v_oqs = static_cast<const int8_t*>(c.v_oqs);
-  sp.k_od = static_cast<const uint16_t*>(c.k_od); sp.v_od = static_cast<const uint16_t*>(c.v_od);
+  sp.outl = static_cast<const uint8_t*>(c.outl);
   AParams p{};
   p.ws = static_cast<const uint8_t*>(ws);
   p.seq_len = c.seq_len; p.status = c.status;

@@ -250,8 +250,9 @@ __device__ __forceinline__ void store_vector(const kvq_cache& c, int which, int 
                         dp + blk * (type_has_min(qt) ? 4 : 2));
     }
     if (outl) {  // one q8_0 block, slot = lane
-      uint8_t* oqs = static_cast<uint8_t*>(which ? c.v_oqs : c.k_oqs) + row * 32;
-      uint16_t* od = static_cast<uint16_t*>(which ? c.v_od : c.k_od) + row;
+      uint8_t* grp = static_cast<uint8_t*>(c.outl) + (row / 16) * kOutlTile;
+      uint8_t* oqs = grp + which * 512 + (row % 16) * 32;
+      uint16_t* od = reinterpret_cast<uint16_t*>(grp + 1024 + which * 32) + row % 16;
       quantize_block<1>(&ov, KVQ_TYPE_Q8_0, lane, oqs, nullptr, od);
     }
   }

@@ -31,8 +31,8 @@ KVQ_F32, KVQ_BF16, KVQ_F16 = 0, 1, 2
 KVQ_ROT_AUTO, KVQ_ROT_K_OFF, KVQ_ROT_V_OFF = 1, 2, 4
 KVQ_INPUT_PREROTATED = 1
 (KVQ_PLANE_K_QS, KVQ_PLANE_K_QH, KVQ_PLANE_K_D, KVQ_PLANE_V_QS, KVQ_PLANE_V_QH, KVQ_PLANE_V_D,
- KVQ_PLANE_K_TAIL, KVQ_PLANE_V_TAIL, KVQ_PLANE_SEQ_LEN, KVQ_PLANE_STATUS, KVQ_PLANE_K_OQS, KVQ_PLANE_K_OD,
- KVQ_PLANE_V_OQS, KVQ_PLANE_V_OD, KVQ_PLANE_OUTLIER_IDX) = range(15)
+ KVQ_PLANE_K_TAIL, KVQ_PLANE_V_TAIL, KVQ_PLANE_SEQ_LEN, KVQ_PLANE_STATUS, KVQ_PLANE_OUTLIER,
+ KVQ_PLANE_OUTLIER_IDX) = range(12)
 KVQ_DEV_ERR_APPEND_RANGE, KVQ_DEV_ERR_PREFILL_RANGE, KVQ_DEV_ERR_TIMEOUT, KVQ_DEV_ERR_PAGE = 1, 2, 4, 8
 KVQ_DEV_ERR_OUTLIER = 16
 
@@ -48,7 +48,7 @@ class kvq_cache(ctypes.Structure):
         ("seq_len", ctypes.c_void_p), ("status", ctypes.c_void_p),
         ("page_tokens", ctypes.c_int32), ("n_pages", ctypes.c_int32), ("page_table", ctypes.c_void_p),
         ("n_outlier", ctypes.c_int32), ("outlier_idx", ctypes.c_void_p),
-        ("k_oqs", ctypes.c_void_p), ("k_od", ctypes.c_void_p), ("v_oqs", ctypes.c_void_p), ("v_od", ctypes.c_void_p),
+        ("outl", ctypes.c_void_p),
     ]
 
 
@@ -262,7 +262,7 @@ class KVCache:
             self.desc.page_table = self.page_table.data_ptr()
         self.planes = {}
         names = ["k_qs", "k_qh", "k_d", "v_qs", "v_qh", "v_d", "k_tail", "v_tail", "seq_len", "status",
-                 "k_oqs", "k_od", "v_oqs", "v_od"]
+                 "outl"]
         if n_outlier:
             self.outlier_idx = torch.as_tensor(outliers, dtype=torch.int32).to(device).contiguous()
             if tuple(self.outlier_idx.shape) != (n_kv_heads, n_outlier):

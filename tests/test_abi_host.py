@@ -179,26 +179,25 @@ def test_outlier_planes_and_checks(built_lib_path):
     """Outlier channels: 32 per KV head, planes sized per body row (paged like the
     body), every pointer required together; prerotated input refused."""
     c = kvq.descriptor(2, 4, 128, 256, 16, "q4_0", "q8_0", n_outlier=32)
-    assert kvq.kvq_plane_bytes(c, kvq.KVQ_PLANE_K_OQS) == 2 * 4 * 256 * 32
-    assert kvq.kvq_plane_bytes(c, kvq.KVQ_PLANE_V_OD) == 2 * 4 * 256 * 2
+    assert kvq.kvq_plane_bytes(c, kvq.KVQ_PLANE_OUTLIER) == 2 * 4 * 256 // 16 * 1088   # 2 x 34 B per row
     assert kvq.kvq_plane_bytes(c, kvq.KVQ_PLANE_OUTLIER_IDX) == 4 * 32 * 4
     cp = kvq.descriptor(2, 4, 128, 256, 16, "q4_0", "q8_0", page_tokens=64, n_pages=5, n_outlier=32)
-    assert kvq.kvq_plane_bytes(cp, kvq.KVQ_PLANE_K_OQS) == 5 * 4 * 64 * 32
-    assert kvq.kvq_plane_bytes(_desc(), kvq.KVQ_PLANE_K_OQS) == 0          # off: absent planes
+    assert kvq.kvq_plane_bytes(cp, kvq.KVQ_PLANE_OUTLIER) == 5 * 4 * 64 * 68
+    assert kvq.kvq_plane_bytes(_desc(), kvq.KVQ_PLANE_OUTLIER) == 0        # off: absent plane
     for bad in (dict(n_outlier=16), dict(n_outlier=64), dict(n_outlier=32, head_dim=32)):
         assert kvq.kvq_plane_bytes(_desc(**bad), 0) == 0, bad
     L = kvq.lib()
     full = _full_desc()
     full.n_outlier = 32
     assert L.kvq_cache_check(ctypes.byref(full)) == kvq.KVQ_ERR_INVALID_ARG   # pointers missing
-    full.outlier_idx, full.k_oqs, full.k_od, full.v_oqs, full.v_od = FAKE, FAKE, FAKE, FAKE, FAKE
+    full.outlier_idx, full.outl = FAKE, FAKE
     assert L.kvq_cache_check(ctypes.byref(full)) == 0
-    full.k_od = FAKE + 8
+    full.outl = FAKE + 8
     assert L.kvq_cache_check(ctypes.byref(full)) == kvq.KVQ_ERR_INVALID_ARG   # misaligned
     off = _full_desc()
-    off.k_oqs = FAKE
+    off.outl = FAKE
     assert L.kvq_cache_check(ctypes.byref(off)) == kvq.KVQ_ERR_INVALID_ARG    # plane without n_outlier
-    full.k_od = FAKE
+    full.outl = FAKE
     ref = ctypes.byref(full)
     assert L.kvq_rotate_quantize_append(ref, FAKE, FAKE, 0, 1, None, kvq.KVQ_INPUT_PREROTATED, None) == \
         kvq.KVQ_ERR_INVALID_ARG
@@ -206,6 +205,6 @@ def test_outlier_planes_and_checks(built_lib_path):
     # decode: the q4_0 / q5_0 / q8_0 pairs only; the workspace holds the outlier partials too
     assert L.kvq_decode_workspace_bytes(ref, 8) > L.kvq_decode_workspace_bytes(ctypes.byref(_full_desc()), 8)
     q41 = _full_desc(k_type=kvq.KVQ_TYPE_Q4_1)
-    q41.n_outlier, q41.outlier_idx, q41.k_oqs, q41.k_od, q41.v_oqs, q41.v_od = 32, FAKE, FAKE, FAKE, FAKE, FAKE
+    q41.n_outlier, q41.outlier_idx, q41.outl = 32, FAKE, FAKE
     assert L.kvq_decode_attention(ctypes.byref(q41), FAKE, 0, 8, 0.0, FAKE, 0, FAKE, 1 << 40, None) == \
         kvq.KVQ_ERR_UNSUPPORTED

@@ -47,10 +47,15 @@ def _append(kvq, torch, gc, oc, k, v, nps=None):
 
 
 def _outlier_rows(gc, which, rows, torch):
-    """int8 codes [rows][32] and fp16 scale bits [rows] of the K / V outlier plane."""
-    qs = gc.planes[f"{which}_oqs"].cpu().numpy().view(np.int8).reshape(-1, 32)
-    dd = gc.planes[f"{which}_od"].cpu().numpy().view(np.uint16)
-    return qs[rows], dd[rows]
+    """int8 codes [rows][32] and fp16 scale bits [rows] of K or V in the outlier
+    plane (groups of 16 rows: K codes [16][32], V codes [16][32], K scales [16],
+    V scales [16])."""
+    grp = gc.planes["outl"].cpu().numpy().reshape(-1, 1088)
+    w = 0 if which == "k" else 1
+    g, i = rows // 16, rows % 16
+    codes = grp[:, w * 512:(w + 1) * 512].reshape(-1, 16, 32).view(np.int8)
+    scales = grp[:, 1024 + w * 32:1024 + (w + 1) * 32].copy().view(np.uint16)
+    return codes[g, i], scales[g, i]
 
 
 def _check_cache(torch, gc, oc, kt, vt, d, page_of=None):
