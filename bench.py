@@ -171,6 +171,23 @@ def fill_cache(torch, kvq, cache, w: wl.Workload, n_fill: int, seed: int = 0):
     return kmask, vmask, gen
 
 
+def max_over_ranks(vals, world: int, device: str = "cpu"):
+    """Every rank calls this with its own timings; each comes back as the maximum
+    over the ranks (the slowest replica sets the job's time)."""
+    import torch
+    t = torch.tensor(vals, dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def job_gbs(world: int, bytes_per_rank_step: float, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank moves the same bytes per step (weak scaling,
+    one replica per GPU), over the slowest rank's step time."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -326,10 +343,8 @@ def run_ours(args):
     d2h = out.numel() * out.element_size()
 
     # ---- max over ranks -----------------------------------------------------------------
-    vals = torch.tensor([step_ms, dec_ms, app_ms, e2e_ms, e2e_eager_ms], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    step_ms, dec_ms, app_ms, e2e_ms, e2e_eager_ms = [float(x) for x in vals.cpu()]
+    step_ms, dec_ms, app_ms, e2e_ms, e2e_eager_ms = max_over_ranks(
+        [step_ms, dec_ms, app_ms, e2e_ms, e2e_eager_ms], world, "cuda")
 
     if rank == 0:
         peak, peak_kind = measured_peaks()
@@ -337,7 +352,7 @@ def run_ours(args):
         per_step_bytes = total_bytes / K
         line = {
             "metric": METRIC,
-            "value": round(world * per_step_bytes / (step_ms * 1e-3) / 1e9, 2),
+            "value": round(job_gbs(world, per_step_bytes, step_ms), 2),
             "unit": "GB/s",
             "n_gpus": world, "steps": K, "warmup": W,
             "ms_per_step": round(step_ms, 5),
@@ -357,10 +372,10 @@ def run_ours(args):
                          "bytes_per_launch": int(dec_bytes), "ms_per_launch": round(dec_ms, 5),
                          "traffic": recorded_traffic("kvq_decode_impl.cuh")},
             "append": {"tokens_per_s": round(w.batch * n_new / (app_ms * 1e-3), 1), "ms_per_call": round(app_ms, 5)},
-            "e2e": {"value": round(world * per_step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "e2e": {"value": round(job_gbs(world, per_step_bytes, e2e_ms), 2), "unit": "GB/s",
                     "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "how": "CUDA graph per step: pinned H2D copies + kvq_append_decode + D2H, host sync each step"},
-            "e2e_eager": {"value": round(world * per_step_bytes / (e2e_eager_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "e2e_eager": {"value": round(job_gbs(world, per_step_bytes, e2e_eager_ms), 2), "unit": "GB/s",
                           "ms_per_step": round(e2e_eager_ms, 5)},
             "gpu_launches": launches_per_step * K,
             "step_call": "kvq_append_decode" + (" (append fused into the decode launch)" if fused else ""),
