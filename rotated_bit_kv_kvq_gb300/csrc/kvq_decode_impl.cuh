@@ -380,6 +380,11 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
   for (int j = 0; j < (OL ? 2 : 1); ++j)
 #pragma unroll
     for (int r = 0; r < 4; ++r) acco[j][r] = 0.0f;
+  // V1 (scale + minimum V blocks): sum over this lane's transposed tokens of P * lo per
+  // block, for head g, in the running-max frame; added to the block's channels at the end
+  float vmin[C::V1 ? NB : 1];
+#pragma unroll
+  for (int i = 0; i < (C::V1 ? NB : 1); ++i) vmin[i] = 0.0f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
   bool timed_out = false;
   int k_stop = my_tiles;
@@ -530,6 +535,12 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
           acco[j][0] *= a0; acco[j][1] *= a1; acco[j][2] *= a0; acco[j][3] *= a1;
         }
       }
+      if constexpr (C::V1) {  // head g's factor lives in lane tig = g / 2
+        const float x0 = __shfl_sync(0xffffffffu, a0, g >> 1), x1 = __shfl_sync(0xffffffffu, a1, g >> 1);
+        const float ag = (g & 1) ? x1 : x0;
+#pragma unroll
+        for (int i = 0; i < NB; ++i) vmin[i] *= ag;
+      }
       m0 = nm0; m1 = nm1;
     }
     const float ms0 = m0 == -INFINITY ? 0.0f : m0, ms1 = m1 == -INFINITY ? 0.0f : m1;
@@ -566,17 +577,15 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
         split_h2(pz[2] * __half2float(vd[(2 * tig + 8) * NB * VHH + o]),
                  pz[3] * __half2float(vd[(2 * tig + 9) * NB * VHH + o]), bh1, bl1);
       };
-      // the minimum adds sum_t P[t][h] * lo[t][blk] to every channel of the block:
-      // an all-ones A fragment (fp16 1.0) against P * lo
+      // the minimum adds sum_t P[t][h] * lo[t][blk] to every channel of the block: the
+      // lane's share for head g is summed here in fp32 and spread over the channels at the end
       auto add_min = [&](int blk) {
         if constexpr (C::V1) {
-          uint32_t mh0, ml0, mh1, ml1;
-          pscaled(blk, 1, mh0, ml0, mh1, ml1);
-          const uint32_t ones[4] = {0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u};
-          mma16816(acc[blk][0], ones, mh0, mh1);
-          mma16816(acc[blk][0], ones, ml0, ml1);
-          mma16816(acc[blk][1], ones, mh0, mh1);
-          mma16816(acc[blk][1], ones, ml0, ml1);
+          const int o = blk * VHH + 1;
+          vmin[blk] = fmaf(pz[0], __half2float(vd[(2 * tig) * NB * VHH + o]), vmin[blk]);
+          vmin[blk] = fmaf(pz[1], __half2float(vd[(2 * tig + 1) * NB * VHH + o]), vmin[blk]);
+          vmin[blk] = fmaf(pz[2], __half2float(vd[(2 * tig + 8) * NB * VHH + o]), vmin[blk]);
+          vmin[blk] = fmaf(pz[3], __half2float(vd[(2 * tig + 9) * NB * VHH + o]), vmin[blk]);
         }
       };
       const uint32_t vbase = smem_u32(st + C::off_vqs);
@@ -725,6 +734,20 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
       base[(2 * tig) * D + cg8] = acc[blk][cc2][2] * f0;
       base[(2 * tig + 1) * D + cg8] = acc[blk][cc2][3] * f1;
     }
+  if constexpr (C::V1) {  // head g: the 4 tig lanes' sums, in this warp's merge frame, on every channel
+    const float x0 = __shfl_sync(0xffffffffu, f0, g >> 1), x1 = __shfl_sync(0xffffffffu, f1, g >> 1);
+    const float fg = (g & 1) ? x1 : x0;
+    __syncwarp();
+#pragma unroll
+    for (int blk = 0; blk < NB; ++blk) {
+      float t = vmin[blk];
+      t += __shfl_xor_sync(0xffffffffu, t, 1);
+      t += __shfl_xor_sync(0xffffffffu, t, 2);
+      float* row = macc + ((size_t)warp * kMaxHeads + g) * D + 32 * blk + 8 * tig;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) row[c] += t * fg;
+    }
+  }
   float* maco = macc + (size_t)kWarps * kMaxHeads * D;  // OL: [kWarps][8][32]
   if constexpr (OL) {
 #pragma unroll
