@@ -285,7 +285,23 @@ def run_ours(args):
         kvq.kvq_rotate_quantize_append(cache.desc, ks[i % P], vs[i % P], stream=stream)
     a1.record(stream)
     torch.cuda.synchronize()
+    app_eager_ms = a0.elapsed_time(a1) / K
+    # the same K calls captured in one CUDA graph: the calls' device time without
+    # the host's per-launch cost (a one-token append is a few microseconds of work)
+    cap_a = torch.cuda.Stream()
+    g_app = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_app, stream=cap_a):
+        for i in range(K):
+            kvq.kvq_rotate_quantize_append(cache.desc, ks[i % P], vs[i % P], stream=cap_a)
+    cache.seq_len.copy_(seq0)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(cap_a):
+        a0.record(cap_a)
+        g_app.replay()
+        a1.record(cap_a)
+    torch.cuda.synchronize()
     app_ms = a0.elapsed_time(a1) / K
+    del g_app
 
     # ---- end to end through the public API, host buffers -----------------------------
     # Every step copies the new tokens and the query from pinned host memory, runs
@@ -343,8 +359,8 @@ def run_ours(args):
     d2h = out.numel() * out.element_size()
 
     # ---- max over ranks -----------------------------------------------------------------
-    step_ms, dec_ms, app_ms, e2e_ms, e2e_eager_ms = max_over_ranks(
-        [step_ms, dec_ms, app_ms, e2e_ms, e2e_eager_ms], world, "cuda")
+    step_ms, dec_ms, app_ms, app_eager_ms, e2e_ms, e2e_eager_ms = max_over_ranks(
+        [step_ms, dec_ms, app_ms, app_eager_ms, e2e_ms, e2e_eager_ms], world, "cuda")
 
     if rank == 0:
         peak, peak_kind = measured_peaks()
@@ -371,7 +387,10 @@ def run_ours(args):
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "bytes_per_launch": int(dec_bytes), "ms_per_launch": round(dec_ms, 5),
                          "traffic": recorded_traffic("kvq_decode_impl.cuh")},
-            "append": {"tokens_per_s": round(w.batch * n_new / (app_ms * 1e-3), 1), "ms_per_call": round(app_ms, 5)},
+            "append": {"tokens_per_s": round(world * w.batch * n_new / (app_ms * 1e-3), 1),
+                       "ms_per_call": round(app_ms, 5), "ms_per_call_eager": round(app_eager_ms, 5),
+                       "how": "kvq_rotate_quantize_append, one token per sequence, K calls in one CUDA graph "
+                              "(device time); ms_per_call_eager: the same calls launched one by one"},
             "e2e": {"value": round(job_gbs(world, per_step_bytes, e2e_ms), 2), "unit": "GB/s",
                     "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "how": "CUDA graph per step: pinned H2D copies + kvq_append_decode + D2H, host sync each step"},

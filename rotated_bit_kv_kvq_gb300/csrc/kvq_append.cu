@@ -24,6 +24,27 @@ namespace kvq {
 namespace {
 
 constexpr int kAppendWarps = 8;
+constexpr long long kRowsMinVectors = 2048;  // appends of at least this many vectors use append_rows_kernel
+
+// The last CTA of an append advances seq_len: every CTA has read seq_len before
+// it counts itself in.  Called by all threads of every CTA at its end.
+__device__ __forceinline__ void finish_append(const kvq_cache& c, int n_new, const int32_t* n_new_per_seq) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned done = atomicAdd(&c.status[1], 1u);
+    if (done == gridDim.x - 1) {
+      __threadfence();
+      for (int b = 0; b < c.batch; ++b) {
+        const int n0 = c.seq_len[b];
+        const int nb = n_new_per_seq ? n_new_per_seq[b] : n_new;
+        if (nb >= 0 && nb <= n_new && n0 >= 0 && (long long)n0 + nb <= c.max_ctx) c.seq_len[b] = n0 + nb;
+      }
+      c.status[1] = 0;
+      __threadfence();
+    }
+  }
+}
 
 template <int D, int G>
 __global__ void __launch_bounds__(kAppendWarps * 32)
@@ -60,23 +81,209 @@ append_kernel(kvq_cache c, int rot_k, int rot_v, const void* __restrict__ kin, c
     }
   }
 
-  // The last CTA to finish advances seq_len: every CTA has read seq_len
-  // before it counts itself in.
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const unsigned done = atomicAdd(&c.status[1], 1u);
-    if (done == gridDim.x - 1) {
-      __threadfence();
-      for (int b = 0; b < c.batch; ++b) {
-        const int n0 = c.seq_len[b];
-        const int nb = n_new_per_seq ? n_new_per_seq[b] : n_new;
-        if (nb >= 0 && nb <= n_new && n0 >= 0 && (long long)n0 + nb <= c.max_ctx) c.seq_len[b] = n0 + nb;
+  finish_append(c, n_new, n_new_per_seq);
+}
+
+// ---------------------------------------------------------------------------
+// Block-per-lane variant for power-of-two head_dim 64 / 128 / 256 without
+// outlier channels: a vector is held by R = D/32 consecutive lanes and lane
+// l % R holds exactly block l % R (32 consecutive channels).  The rotation
+// combines the 5 channel bits inside a lane in registers and the log2(R)
+// block bits across lanes (one shuffle per value per bit); each lane then
+// quantizes and stores its own block with no cross-lane reduction, 16-byte
+// loads and stores throughout.  Same arithmetic as quantize_block, operation
+// by operation.
+// ---------------------------------------------------------------------------
+
+// Unnormalised Sylvester FWHT of a vector held by R consecutive lanes, 32
+// consecutive channels each: the 5 in-lane channel bits in registers, the
+// log2(R) lane bits by shuffles (o + sgn*v: the rounding of the plain sum or
+// difference).
+template <int R>
+__device__ __forceinline__ void lane_fwht(float (&r)[32], int lane) {
+#pragma unroll
+  for (int hh = 1; hh < 32; hh <<= 1)
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if ((j & hh) == 0) {
+        const float a = r[j], bq = r[j + hh];
+        r[j] = a + bq;
+        r[j + hh] = a - bq;
       }
-      c.status[1] = 0;
-      __threadfence();
+#pragma unroll
+  for (int m = 1; m < R; m <<= 1) {
+    const float sgn = (lane & m) ? -1.0f : 1.0f;  // upper partner: o - v, lower: v + o
+#pragma unroll
+    for (int j = 0; j < 32; ++j) r[j] = fmaf(sgn, r[j], __shfl_xor_sync(0xffffffffu, r[j], m));
+  }
+}
+
+// One 32-value block held by one lane: quantize and store (qs: the block's
+// bytes; qh_word: q5_x high bits or null; d_ptr: fp16 d or the (d, lo) word).
+__device__ __forceinline__ void quantize_lane_block(const float (&y)[32], int qt, uint8_t* qs_blk,
+                                                    uint32_t* qh_word, void* d_ptr) {
+  uint8_t code[32];
+  if (type_has_min(qt)) {
+    float lo = y[0], hi = y[0];
+#pragma unroll
+    for (int j = 1; j < 32; ++j) {  // first index on ties: strict comparisons in ascending order
+      if (y[j] < lo) lo = y[j];
+      if (y[j] > hi) hi = y[j];
+    }
+    const int top = qt == KVQ_TYPE_Q5_1 ? 31 : 15;
+    const float d = __fdiv_rn(__fsub_rn(hi, lo), float(top));
+    const float id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      code[j] = uint8_t(min(top, __float2int_rz(__fadd_rn(__fmul_rn(__fsub_rn(y[j], lo), id), 0.5f))));
+    *static_cast<uint32_t*>(d_ptr) = uint32_t(__half_as_ushort(__float2half_rn(d))) |
+                                     (uint32_t(__half_as_ushort(__float2half_rn(lo))) << 16);
+  } else {
+    float best_a = 0.0f, best_m = 0.0f;  // strict '>' scan from +0: first index on ties
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float a = fabsf(y[j]);
+      if (a > best_a) { best_a = a; best_m = y[j]; }
+    }
+    float d;
+    if (qt == KVQ_TYPE_Q8_0) {
+      d = best_a / 127.0f;
+      const float id = d != 0.0f ? 1.0f / d : 0.0f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) code[j] = uint8_t(int8_t(int(roundf(__fmul_rn(y[j], id)))));
+    } else {
+      const bool q5 = qt == KVQ_TYPE_Q5_0;
+      d = q5 ? best_m / -16.0f : best_m / -8.0f;
+      const float id = d != 0.0f ? 1.0f / d : 0.0f;
+      const float off = q5 ? 16.5f : 8.5f;
+      const int top = q5 ? 31 : 15;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) code[j] = uint8_t(min(top, __float2int_rz(__fadd_rn(__fmul_rn(y[j], id), off))));
+    }
+    *static_cast<__half*>(d_ptr) = __float2half_rn(d);
+  }
+  uint32_t w[8];
+  if (qt == KVQ_TYPE_Q8_0) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      w[k] = uint32_t(code[4 * k]) | (uint32_t(code[4 * k + 1]) << 8) | (uint32_t(code[4 * k + 2]) << 16) |
+             (uint32_t(code[4 * k + 3]) << 24);
+    reinterpret_cast<uint4*>(qs_blk)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    reinterpret_cast<uint4*>(qs_blk)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    return;
+  }
+  // byte k = code_k | code_{k+16} << 4
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint32_t t = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      t |= uint32_t((code[4 * k + e] & 0x0F) | ((code[4 * k + e + 16] & 0x0F) << 4)) << (8 * e);
+    w[k] = t;
+  }
+  *reinterpret_cast<uint4*>(qs_blk) = make_uint4(w[0], w[1], w[2], w[3]);
+  if (type_has_qh(qt)) {
+    uint32_t h = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) h |= uint32_t((code[j] >> 4) & 1) << j;
+    *qh_word = h;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kAppendWarps * 32)
+append_rows_kernel(kvq_cache c, int rot_k, int rot_v, const void* __restrict__ kin, const void* __restrict__ vin,
+                   int in_dtype, int n_new, const int32_t* __restrict__ n_new_per_seq, int prerotated) {
+  static_assert(D == 64 || D == 128 || D == 256, "power-of-two head_dim of 64 to 256");
+  constexpr int R = D / 32;   // lanes per vector
+  constexpr int NB = D / kQK;
+  const int lane = threadIdx.x & 31, sub = lane % R;
+  const int H = c.n_kv_heads;
+  const unsigned tasks = unsigned(c.batch) * unsigned(n_new) * unsigned(H) * 2u;
+  const unsigned task = (blockIdx.x * unsigned(kAppendWarps) + (threadIdx.x >> 5)) * (32u / R) + unsigned(lane / R);
+  const bool live = task < tasks;
+  const unsigned tu = live ? task : tasks - 1;   // lanes past the end compute a copy and store nothing
+  const int which = int(tu & 1u);
+  const unsigned vec = tu >> 1;                  // (b * n_new + i) * H + h
+  const int h = int(vec % unsigned(H));
+  const unsigned bi = vec / unsigned(H);
+  const int i = int(bi % unsigned(n_new));
+  const int b = int(bi / unsigned(n_new));
+  const int n0 = c.seq_len[b];
+  const int nb = n_new_per_seq ? n_new_per_seq[b] : n_new;
+  const bool ok = nb >= 0 && nb <= n_new && n0 >= 0 && (long long)n0 + nb <= c.max_ctx;
+  if (live && !ok && i == 0 && h == 0 && which == 0 && sub == 0) atomicOr(&c.status[0], KVQ_DEV_ERR_APPEND_RANGE);
+
+  // this lane's block: channels 32*sub .. 32*sub+31
+  float y[32];
+  const size_t e0 = size_t(vec) * D + 32 * sub;
+  if (in_dtype == KVQ_F32) {
+    const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(which ? vin : kin) + e0);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const float4 x = src[t];
+      y[4 * t] = x.x; y[4 * t + 1] = x.y; y[4 * t + 2] = x.z; y[4 * t + 3] = x.w;
+    }
+  } else {
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(which ? vin : kin) + e0);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const uint4 x = src[t];
+      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint16_t l16 = uint16_t(w[e] & 0xFFFFu), h16 = uint16_t(w[e] >> 16);
+        y[8 * t + 2 * e] = in_dtype == KVQ_BF16 ? bf16_bits_to_f32(l16) : __half2float(__ushort_as_half(l16));
+        y[8 * t + 2 * e + 1] = in_dtype == KVQ_BF16 ? bf16_bits_to_f32(h16) : __half2float(__ushort_as_half(h16));
+      }
     }
   }
+  // rotation (a warp mixes K and V vectors: when only one of them rotates, the
+  // butterflies run on a copy so that every lane takes part in the shuffles)
+  const bool rot = (which ? rot_v : rot_k) && !prerotated;
+  if (__all_sync(0xffffffffu, rot)) {
+    lane_fwht<R>(y, lane);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) y[j] *= inv_sqrt_group<D>();
+  } else if (__any_sync(0xffffffffu, rot)) {
+    float r[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) r[j] = y[j];
+    lane_fwht<R>(r, lane);
+    if (rot) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) y[j] = r[j] * inv_sqrt_group<D>();
+    }
+  }
+  const int pos = n0 + i;
+  const int qt = which ? c.v_type : c.k_type;
+  const bool store = live && ok && i < nb;
+  const long long brow = store ? body_row(row_map(c), b, h, pos) : 0;
+  if (!store) {
+  } else if (brow < 0) {  // page id outside the pool: the body row is not written
+    if (sub == 0) atomicOr(&c.status[0], KVQ_DEV_ERR_PAGE);
+  } else {
+    const size_t row = size_t(brow);
+    uint8_t* qs = static_cast<uint8_t*>(which ? c.v_qs : c.k_qs) + row * qs_row_bytes(qt, D) +
+                  sub * (qt == KVQ_TYPE_Q8_0 ? 32 : 16);
+    uint32_t* qh = static_cast<uint32_t*>(which ? c.v_qh : c.k_qh);
+    uint8_t* dp = static_cast<uint8_t*>(which ? c.v_d : c.k_d) + (row * NB + sub) * (type_has_min(qt) ? 4 : 2);
+    quantize_lane_block(y, qt, qs, qh ? qh + row * NB + sub : nullptr, dp);
+  }
+  if (store && c.tail_len > 0 && i >= nb - c.tail_len) {
+    uint16_t* tail = static_cast<uint16_t*>(which ? c.v_tail : c.k_tail) +
+                     (((size_t)b * H + h) * c.tail_len + pos % c.tail_len) * D + 32 * sub;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        w[e] = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(y[8 * t + 2 * e]))) |
+               (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(y[8 * t + 2 * e + 1]))) << 16);
+      reinterpret_cast<uint4*>(tail)[t] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+  finish_append(c, n_new, n_new_per_seq);
 }
 
 // ---------------------------------------------------------------------------
@@ -168,6 +375,16 @@ cudaError_t append_d(const kvq_cache& c, Rot rot, const void* k, const void* v, 
   if (warps > 0x7fffffffLL) return cudaErrorInvalidValue;
   const int pre = (flags & KVQ_INPUT_PREROTATED) ? 1 : 0;
   constexpr int G = (D >= 64 && D % 64 == 0) ? (((D & (D - 1)) == 0) ? D : 64) : 32;
+  if constexpr (D == 64 || D == 128 || D == 256) {
+    // one block per lane (32 / (D/32) vectors per warp) for bulk appends; a few
+    // vectors (a decode step) finish sooner spread one per warp
+    if (!c.n_outlier && warps >= kRowsMinVectors) {
+      const long long per_cta = (long long)kAppendWarps * (32 / (D / 32));
+      append_rows_kernel<D><<<unsigned((warps + per_cta - 1) / per_cta), kAppendWarps * 32, 0, st>>>(
+          c, rot.k, rot.v, k, v, in_dtype, n_new, nps, pre);
+      return cudaGetLastError();
+    }
+  }
   append_kernel<D, G><<<unsigned(blocks), kAppendWarps * 32, 0, st>>>(c, rot.k, rot.v, k, v, in_dtype, n_new, nps, pre);
   return cudaGetLastError();
 }

@@ -126,23 +126,24 @@ def test_overflow_sets_status_and_leaves_sequence_untouched():
 
 
 @pytest.mark.parametrize("in_dtype", ["f32", "bf16", "f16"])
-@pytest.mark.parametrize("d", [64, 128, 256, 192])
-def test_gpu_rotation_against_oracle(in_dtype, d):
+@pytest.mark.parametrize("d,n", [(64, 64), (128, 64), (256, 64), (192, 64), (64, 320), (128, 320), (256, 320)])
+def test_gpu_rotation_against_oracle(in_dtype, d, n):
     """The GPU rotates in fp32 (warp FWHT); the oracle in fp64.  Codes may flip
     only where the rotated value sits within float rounding of a code boundary:
     at most 1 in 1000 elements, each by one level, and bf16 tail values agree
-    to one bf16 unit."""
+    to one bf16 unit.  n = 320 (5,120 vectors) takes the bulk, block-per-lane
+    kernel; n = 64 the vector-per-warp one."""
     torch = require_gpu()
     from rotated_bit_kv_kvq_gb300 import kvq
     rng = np.random.default_rng(11)
-    B, H, n, T = 2, 4, 64, 16
+    B, H, T = 2, 4, 16
     x = rng.standard_normal((B, n, H, d)).astype(np.float32)
     x[..., 5] *= 20
     xd = to_dev(x, in_dtype, torch)
     xin = xd.float().cpu().numpy()            # the values the GPU actually received
     for qt in ("q4_0", "q5_0", "q8_0", "q4_1", "q5_1"):
-        gc = kvq.KVCache(B, H, d, 64, T, qt, qt)
-        oc = ko.OracleCache(B, H, d, 64, T, qt, qt, True, True)
+        gc = kvq.KVCache(B, H, d, n, T, qt, qt)
+        oc = ko.OracleCache(B, H, d, n, T, qt, qt, True, True)
         kvq.kvq_rotate_quantize_append(gc.desc, xd, xd)
         oc.append(xin, xin)
         flips = 0
@@ -173,3 +174,54 @@ def test_gpu_rotation_against_oracle(in_dtype, d):
         step = {"q4_0": 1 / 8, "q5_0": 1 / 16, "q8_0": 1 / 127, "q4_1": 2 / 15, "q5_1": 2 / 31}[qt]
         err = np.linalg.norm(back - xin[0, :, 0], axis=-1)
         assert np.all(err <= np.sqrt(d) * (amax.max(-1) * step) * 1.01 + 1e-6)
+
+
+@pytest.mark.parametrize("qt", ["q4_0", "q5_0", "q8_0", "q4_1", "q5_1"])
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_bulk_blocks_bit_exact_prerotated(qt, d):
+    """Appends of at least 2,048 vectors (the block-per-lane kernel): blocks,
+    dequantized values and tail rows bit-exact, ragged counts, two calls."""
+    torch = require_gpu()
+    from rotated_bit_kv_kvq_gb300 import kvq
+    rng = np.random.default_rng(200 + d)
+    B, H, T = 2, 4, 16
+    other = {"q4_0": "q8_0", "q5_0": "q4_1", "q8_0": "q5_1", "q4_1": "q5_0", "q5_1": "q4_0"}[qt]
+    gc = kvq.KVCache(B, H, d, 640, T, qt, other)
+    oc = ko.OracleCache(B, H, d, 640, T, qt, other, True, True)
+    for n, nps in ((300, [300, 261]), (290, [250, 290])):
+        k = _inputs(rng, B, n, H, d)
+        v = _inputs(rng, B, n, H, d, scale=3.0)
+        append_both(gc, oc, k, v, n_new_per_seq=nps, torch=torch)
+    lens = gc.seq_len.cpu().numpy()
+    assert np.array_equal(lens, oc.seq_len)
+    for b in range(B):
+        n = int(lens[b])
+        for h in range(H):
+            for which, w, t in ((0, "k", qt), (1, "v", other)):
+                assert np.array_equal(gpu_blocks(gc, b, h, which, 0, n, t, d, torch), oc.ggml_blocks(w, b, h, 0, n))
+            for which, w in ((2, "k"), (3, "v")):
+                got = gpu_values(gc, b, h, which, n - T, T, d, torch)
+                assert np.array_equal(got, oc.tail_values(w, b, h, np.arange(n - T, n)))
+
+
+def test_bulk_k_rotated_v_not():
+    """K rotated in the kernel, V stored as given (KVQ_ROT_V_OFF): in the bulk
+    kernel a warp mixes both kinds of vectors.  V blocks are bit-exact; K within
+    the rotation tolerance (exact here: dyadic inputs at head_dim 64)."""
+    torch = require_gpu()
+    from rotated_bit_kv_kvq_gb300 import kvq
+    rng = np.random.default_rng(203)
+    B, H, d, n, T = 2, 4, 64, 300, 8
+    gc = kvq.KVCache(B, H, d, 320, T, "q4_0", "q8_0", flags=kvq.KVQ_ROT_AUTO | kvq.KVQ_ROT_V_OFF)
+    oc = ko.OracleCache(B, H, d, 320, T, "q4_0", "q8_0", True, False)
+    k = rng.integers(-64, 65, (B, n, H, d)).astype(np.float32) * np.float32(0.125)
+    v = rng.standard_normal((B, n, H, d)).astype(np.float32)
+    kvq.kvq_rotate_quantize_append(gc.desc, to_dev(k, "f32", torch), to_dev(v, "f32", torch))
+    oc.append(k, v)
+    for b in range(B):
+        for h in range(H):
+            for which, w, t in ((0, "k", "q4_0"), (1, "v", "q8_0")):
+                assert np.array_equal(gpu_blocks(gc, b, h, which, 0, n, t, d, torch), oc.ggml_blocks(w, b, h, 0, n))
+            for which, w in ((2, "k"), (3, "v")):
+                got = gpu_values(gc, b, h, which, n - T, T, d, torch)
+                assert np.array_equal(got, oc.tail_values(w, b, h, np.arange(n - T, n)))
