@@ -55,7 +55,7 @@ DecodePlan plan_decode(const kvq_cache& c, int n_q_heads, int sm_count) {
   pl.splits_tail = c.tail_len > 0 ? (c.tail_len + pl.tail_chunk - 1) / pl.tail_chunk : 0;
   // body: size the chunks so that all CTAs of a full cache fit in one wave of
   // kCtasPerSm CTAs per SM (shorter sequences leave their last splits empty)
-  const long long slots = (long long)(c.n_outlier ? kCtasPerSmOutl : kCtasPerSm) * (sm_count > 0 ? sm_count : 148);
+  const long long slots = (long long)ctas_per_sm(c.head_dim, c.n_outlier != 0) * (sm_count > 0 ? sm_count : 148);
   long long per_pair = slots / pairs - pl.splits_tail;
   if (per_pair < 1) per_pair = 1;
   int chunk = int(((c.max_ctx + per_pair - 1) / per_pair + 63) / 64 * 64);

@@ -45,7 +45,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kTailChunkMax = 4096;  // tail slots per CTA
 constexpr int kSmemBudget = 64 * 1024;       // stages; leaves room for 3 CTAs per SM
 constexpr int kCtasPerSm = 3;
-constexpr int kCtasPerSmOutl = 2;  // outlier-channel kernels: the extra block's registers
+// Outlier-channel kernels at head_dim 256 run 2 CTAs per SM: at 3 the extra
+// block's registers spill inside the tile loop.
+constexpr int ctas_per_sm(int d, bool outl) { return outl && d >= 256 ? 2 : kCtasPerSm; }
 
 constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 // widest TMA swizzle box (128, 64 or 32 bytes) that tiles a row exactly
@@ -142,7 +144,7 @@ __device__ __forceinline__ uint32_t khb(uint32_t h, int which) {
 }
 
 template <int D, int KT, int VT, bool OL>
-__global__ void __launch_bounds__(kThreads, OL ? kCtasPerSmOutl : kCtasPerSm)
+__global__ void __launch_bounds__(kThreads, ctas_per_sm(D, OL))
 decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const __grid_constant__ CUtensorMap tmKt, const __grid_constant__ CUtensorMap tmVt) {
   using C = Cfg<D, KT, VT, OL>;

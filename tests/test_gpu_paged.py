@@ -81,22 +81,24 @@ def test_paged_prefill_and_fused_steps():
     assert np.array_equal(gc.seq_len.cpu().numpy(), oc.seq_len)
 
 
-def test_page_outside_pool_is_reported():
+@pytest.mark.parametrize("H", [1, 8])
+def test_page_outside_pool_is_reported(H):
     """A page-table entry outside the pool: nothing is written or read through it,
-    and append and decode report KVQ_DEV_ERR_PAGE."""
+    and append and decode report KVQ_DEV_ERR_PAGE (H = 8: 3,200 vectors, the
+    bulk append kernel; H = 1: one warp per vector)."""
     torch = require_gpu()
     from rotated_bit_kv_kvq_gb300 import kvq
     rng = np.random.default_rng(73)
-    B, H, d, max_ctx = 1, 1, 64, 256
+    B, d, max_ctx = 1, 64, 256
     table = torch.tensor([0, 1, 99, 2], dtype=torch.int32)   # page 2 of the sequence points outside 4 pages
     gc = kvq.KVCache(B, H, d, max_ctx, 0, "q8_0", "q8_0", page_tokens=64, n_pages=4, page_table=table)
     k, v = _kv(rng, B, 200, H, d)
     kvq.kvq_rotate_quantize_append(gc.desc, to_dev(k, "f32", torch), to_dev(v, "f32", torch))
     st, bits = kvq.kvq_sync_status(gc.desc)
     assert st == kvq.KVQ_ERR_DEVICE_RANGE and bits == kvq.KVQ_DEV_ERR_PAGE
-    q = to_dev(rng.standard_normal((B, 4, d)).astype(np.float32), "f32", torch)
+    q = to_dev(rng.standard_normal((B, 4 * H, d)).astype(np.float32), "f32", torch)
     out = torch.empty_like(q)
-    ws = torch.empty(kvq.kvq_decode_workspace_bytes(gc.desc, 4), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(kvq.kvq_decode_workspace_bytes(gc.desc, 4 * H), dtype=torch.uint8, device="cuda")
     kvq.kvq_decode_attention(gc.desc, q, out, ws)
     st, bits = kvq.kvq_sync_status(gc.desc)
     assert st == kvq.KVQ_ERR_DEVICE_RANGE and bits == kvq.KVQ_DEV_ERR_PAGE
