@@ -194,7 +194,7 @@ __device__ __forceinline__ void add8(const float* src, float (&x)[8]) {
 // stage_kernel: one 64-key tile of one (sequence, KV head) -> workspace
 // ---------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(kStageThreads) stage_kernel(SParams p) {
+__global__ void __launch_bounds__(kStageThreads, 2) stage_kernel(SParams p) {
   using L = PL<D>;
   constexpr int NCH = D / 8;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -676,6 +676,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
   named_sync(1, kSoftmax);
   const float lt = l + xl[(1 - h) * kPM + row];
   float* stage = reinterpret_cast<float*>(sm);  // [128][D + 4], reuses the Q and K slots
+  // Thread (row, h) holds half a row of O / l.  With V rotated, the row's inverse
+  // rotation is H_D = [[H, H], [H, -H]] with H = H_{D/2}: each half is transformed
+  // in registers, the halves are exchanged through shared memory, and thread h
+  // writes a + b (h = 0) or a - b (h = 1), a and b the transformed halves.
+  float v[HD];
   {
     const float inv = (lt > 0.0f && nkv > 0 && ok) ? 256.0f / lt : 0.0f;
     const bool ld = __any_sync(0xffffffffu, nkv > 0 && ok);
@@ -690,56 +695,66 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
         for (int e = 0; e < 16; ++e) t16[e] = 0.0f;
       }
 #pragma unroll
-      for (int e = 0; e < 16; e += 4)
-        *reinterpret_cast<float4*>(&stage[row * L::stage_stride + h * HD + c + e]) =
-            make_float4(t16[e] * inv, t16[e + 1] * inv, t16[e + 2] * inv, t16[e + 3] * inv);
+      for (int e = 0; e < 16; ++e) v[c + e] = t16[e] * inv;
     }
   }
   tc::fence_before_sync();
+  if (p.rot_v) {
+#pragma unroll
+    for (int hh = 1; hh < HD; hh <<= 1)
+#pragma unroll
+      for (int j = 0; j < HD; ++j)
+        if ((j & hh) == 0) {
+          const float a = v[j], bq = v[j + hh];
+          v[j] = a + bq;
+          v[j + hh] = a - bq;
+        }
+  }
+#pragma unroll
+  for (int e = 0; e < HD; e += 4)
+    *reinterpret_cast<float4*>(&stage[row * L::stage_stride + h * HD + e]) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
   named_sync(1, kSoftmax);
   if (warp == 0) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, L::tmem_cols);
   }
-  // rows as in the Q prologue: QR lanes per row, 32 consecutive channels per lane
+  {
+    const int rli = row / g, rhh = row % g, rqi = tile * p.ppt + rli;
+    if (rli < p.ppt && rqi < p.n_tokens) {
+      const float* part = &stage[row * L::stage_stride + (1 - h) * HD];
+      const float sc = inv_sqrt_group<G>();
+      const size_t e0 = (((size_t)b * p.n_tokens + rqi) * p.n_q_heads + kvh * g + rhh) * D + h * HD;
 #pragma unroll
-  for (int pp = 0; pp < QPASS; ++pp) {
-    const int r = warp * (kPM / 8) + pp * QRP + lane / QR;
-    const int rli = r / g, rhh = r % g, rqi = tile * p.ppt + rli;
-    float v[32];
-    const float4* src = reinterpret_cast<const float4*>(&stage[r * L::stage_stride + qsub * 32]);
+      for (int c = 0; c < HD; c += 8) {
+        float o[8];
+        if (p.rot_v) {
+          const float4 x0 = *reinterpret_cast<const float4*>(part + c), x1 = *reinterpret_cast<const float4*>(part + c + 4);
+          const float pv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      const float4 x = src[t];
-      v[4 * t] = x.x; v[4 * t + 1] = x.y; v[4 * t + 2] = x.z; v[4 * t + 3] = x.w;
-    }
-    if (p.rot_v) {
-      row_fwht<D>(v, lane);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] *= inv_sqrt_group<G>();
-    }
-    if (!(rli < p.ppt && rqi < p.n_tokens)) continue;
-    // 32 consecutive channels: 128 (fp32) or 64 (16-bit) bytes, as 16-byte stores
-    const size_t e = (((size_t)b * p.n_tokens + rqi) * p.n_q_heads + kvh * g + rhh) * D + qsub * 32;
-    if (p.out_dtype == KVQ_F32) {
-      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + e);
-#pragma unroll
-      for (int t = 0; t < 8; ++t) dst[t] = make_float4(v[4 * t], v[4 * t + 1], v[4 * t + 2], v[4 * t + 3]);
-    } else {
-      uint32_t w[16];
-#pragma unroll
-      for (int i = 0; i < 32; i += 2) {
-        if (p.out_dtype == KVQ_BF16) {
-          const __nv_bfloat162 t2 = __floats2bfloat162_rn(v[i], v[i + 1]);
-          w[i / 2] = *reinterpret_cast<const uint32_t*>(&t2);
+          for (int e = 0; e < 8; ++e) o[e] = (h == 0 ? v[c + e] + pv[e] : pv[e] - v[c + e]) * sc;
         } else {
-          const __half2 t2 = __floats2half2_rn(v[i], v[i + 1]);
-          w[i / 2] = *reinterpret_cast<const uint32_t*>(&t2);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[e] = v[c + e];
+        }
+        if (p.out_dtype == KVQ_F32) {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + e0 + c);
+          dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+          dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+        } else {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (p.out_dtype == KVQ_BF16) {
+              const __nv_bfloat162 t2 = __floats2bfloat162_rn(o[2 * e], o[2 * e + 1]);
+              w[e] = *reinterpret_cast<const uint32_t*>(&t2);
+            } else {
+              const __half2 t2 = __floats2half2_rn(o[2 * e], o[2 * e + 1]);
+              w[e] = *reinterpret_cast<const uint32_t*>(&t2);
+            }
+          }
+          *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + e0 + c) = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + e);
-#pragma unroll
-      for (int t = 0; t < 4; ++t) dst[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
     }
   }
 }
