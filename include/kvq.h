@@ -345,6 +345,15 @@ KVQ_API kvq_status kvq_dequant_debug(const kvq_cache* c, int32_t seq, int32_t kv
  */
 KVQ_API kvq_status kvq_sync_status(const kvq_cache* c, void* stream, uint32_t* device_bits);
 
+/*
+ * Test aid for the failure path: launches one CTA that waits on a shared-memory
+ * barrier nothing ever completes, with the same bounded wait the kernels use
+ * (limit_cycles clock cycles, 1 .. 2^31), and sets KVQ_DEV_ERR_TIMEOUT in the
+ * cache's status word when it gives up.  The kernel then exits normally, so the
+ * context stays usable; kvq_sync_status reports KVQ_ERR_TIMEOUT.  Asynchronous.
+ */
+KVQ_API kvq_status kvq_selftest_wait_timeout(const kvq_cache* c, int64_t limit_cycles, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -290,6 +290,12 @@ kvq_status kvq_dequant_debug(const kvq_cache* c, int32_t seq, int32_t kv_head, i
                                      static_cast<cudaStream_t>(stream)));
 }
 
+kvq_status kvq_selftest_wait_timeout(const kvq_cache* c, int64_t limit_cycles, void* stream) {
+  if (!c || !c->status || !aligned16(c->status)) return KVQ_ERR_INVALID_ARG;
+  if (limit_cycles < 1 || limit_cycles > (int64_t(1) << 31)) return KVQ_ERR_INVALID_ARG;
+  return from_cuda(kvq::launch_wait_timeout(c->status, limit_cycles, static_cast<cudaStream_t>(stream)));
+}
+
 kvq_status kvq_sync_status(const kvq_cache* c, void* stream, uint32_t* device_bits) {
   if (!c || !c->status) return KVQ_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

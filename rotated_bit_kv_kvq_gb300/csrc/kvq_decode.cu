@@ -37,6 +37,25 @@ cudaError_t decode_noalloc_scratch(void** ptr, size_t* bytes) {
   return cudaSuccess;
 }
 
+namespace {
+// A fresh barrier expecting one arrival that never comes: the wait gives up
+// after limit_cycles and reports it, as every kernel's bounded waits do.
+__global__ void wait_timeout_kernel(uint32_t* status, long long limit_cycles) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_wait_bounded(&bar, 0, limit_cycles)) atomicOr(status, KVQ_DEV_ERR_TIMEOUT);
+}
+}  // namespace
+
+cudaError_t launch_wait_timeout(uint32_t* status, long long limit_cycles, cudaStream_t st) {
+  wait_timeout_kernel<<<1, 32, 0, st>>>(status, limit_cycles);
+  return cudaGetLastError();
+}
+
 bool decode_supported(int d, int kt, int vt, int n_outlier) {
   if (n_outlier)
     return (d == 64 || d == 128 || d == 256) && kt <= KVQ_TYPE_Q8_0 && vt <= KVQ_TYPE_Q8_0 && n_outlier == 32;

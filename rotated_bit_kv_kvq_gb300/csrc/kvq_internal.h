@@ -51,6 +51,9 @@ cudaError_t launch_append(const kvq_cache& c, Rot rot, const void* k, const void
 cudaError_t launch_debug(const kvq_cache& c, Rot rot, int seq, int kv_head, int which, int t0,
                          int count, int original_basis, float* out, void* blocks, cudaStream_t st);
 
+// One CTA waiting (bounded) on a barrier that never completes: the failure path.
+cudaError_t launch_wait_timeout(uint32_t* status, long long limit_cycles, cudaStream_t st);
+
 // Decode: split plan shared by the workspace query and the launch.
 struct DecodePlan {
   int heads_per_cta;   // query heads handled by one CTA (<= 8)

@@ -83,6 +83,7 @@ SIGNATURES = {
                                            ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
                                            ctypes.c_void_p]),
     "kvq_sync_status": (ctypes.c_int32, [_P, ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]),
+    "kvq_selftest_wait_timeout": (ctypes.c_int32, [_P, ctypes.c_int64, ctypes.c_void_p]),
 }
 
 _lib = None
@@ -206,6 +207,12 @@ def kvq_dequant_debug(cache: kvq_cache, seq, kv_head, which, t0, count, out=None
     _check(lib().kvq_dequant_debug(ctypes.byref(cache), seq, kv_head, which, t0, count, 1 if original_basis else 0,
                                    _ptr(out), _ptr(blocks), _stream(stream)),
            "kvq_dequant_debug")
+
+
+def kvq_selftest_wait_timeout(cache: kvq_cache, limit_cycles: int = 1 << 20, stream=None):
+    """Launches the bounded wait that nothing completes (sets KVQ_DEV_ERR_TIMEOUT)."""
+    _check(lib().kvq_selftest_wait_timeout(ctypes.byref(cache), int(limit_cycles), _stream(stream)),
+           "kvq_selftest_wait_timeout")
 
 
 def kvq_sync_status(cache: kvq_cache, stream=None):

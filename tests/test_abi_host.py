@@ -208,3 +208,13 @@ def test_outlier_planes_and_checks(built_lib_path):
     q41.n_outlier, q41.outlier_idx, q41.outl = 32, FAKE, FAKE
     assert L.kvq_decode_attention(ctypes.byref(q41), FAKE, 0, 8, 0.0, FAKE, 0, FAKE, 1 << 40, None) == \
         kvq.KVQ_ERR_UNSUPPORTED
+
+
+def test_selftest_wait_timeout_argument_checks(built_lib_path):
+    L = kvq.lib()
+    c = _full_desc()
+    assert L.kvq_selftest_wait_timeout(ctypes.byref(c), 0, None) == kvq.KVQ_ERR_INVALID_ARG
+    assert L.kvq_selftest_wait_timeout(ctypes.byref(c), (1 << 31) + 1, None) == kvq.KVQ_ERR_INVALID_ARG
+    assert L.kvq_selftest_wait_timeout(None, 1000, None) == kvq.KVQ_ERR_INVALID_ARG
+    c.status = FAKE + 4
+    assert L.kvq_selftest_wait_timeout(ctypes.byref(c), 1000, None) == kvq.KVQ_ERR_INVALID_ARG
