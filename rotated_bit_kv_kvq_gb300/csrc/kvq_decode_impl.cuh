@@ -701,6 +701,9 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     }
   }
 
+  // the merge kernel may start launching (it waits for this grid's completion)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
   // ---- merge the 4 warps, write this CTA's partial ---------------------------
 #pragma unroll
   for (int o = 4; o < 32; o <<= 1) {
@@ -816,6 +819,9 @@ decode_combine_kernel(const float* __restrict__ ws_acc, const float* __restrict_
   __shared__ float s_red[2][kCombineThreads / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int row = blockIdx.x;  // b * Hq + h
+  // launched as a programmatic dependent of the split kernel: wait for its completion
+  // (and memory) before reading anything it wrote
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // fused step: every split CTA has read seq_len; advance it (head 0's CTA of each sequence)
   if (fused && tid == 0 && row % n_q_heads == 0) {
     const int b = row / n_q_heads;
@@ -998,10 +1004,20 @@ cudaError_t run_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, cons
     e = ensure_dynamic_smem(reinterpret_cast<const void*>(decode_combine_kernel<D, OL>), (int)wbytes);
     if (e != cudaSuccess) return e;
   }
-  decode_combine_kernel<D, OL><<<total, kCombineThreads, wbytes, st>>>(p.ws_acc, p.ws_ml, plan.splits, rot.v, out, out_dtype,
-                                                                   n_q_heads, p.fused, p.fa, c.seq_len, c.max_ctx,
-                                                                   p.ws_acco, c.outlier_idx, p.group);
-  return cudaGetLastError();
+  // programmatic dependent launch: the merge grid's launch overlaps the split grid's end
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(total);
+  cfg.blockDim = dim3(kCombineThreads);
+  cfg.dynamicSmemBytes = wbytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, OL>, (const float*)p.ws_acc, (const float*)p.ws_ml,
+                            (int)plan.splits, (int)rot.v, out, out_dtype, n_q_heads, p.fused, p.fa, c.seq_len,
+                            c.max_ctx, (const float*)p.ws_acco, c.outlier_idx, p.group);
 }
 
 template <int D>
