@@ -859,10 +859,19 @@ decode_combine_kernel(const float* __restrict__ ws_acc, const float* __restrict_
   const int c = tid % D, sub = tid / D;
   float v = 0.0f;
   if (tid < D * TPC) {
+    // 8 partials in flight per thread; rows of empty splits (weight 0) were never
+    // written: whatever they hold is read but selected away, never multiplied
     const float* a = ws_acc + (size_t)row * splits * D + c;
-    for (int s = sub; s < splits; s += TPC) {
-      const float w = s_w[s];
-      if (w != 0.0f) v += w * a[(size_t)s * D];  // empty splits never wrote their row: do not read it
+    for (int s0 = sub; s0 < splits; s0 += 8 * TPC) {
+      float x[8], wv[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int s = s0 + u * TPC;
+        wv[u] = s < splits ? s_w[s] : 0.0f;
+        x[u] = s < splits ? a[(size_t)s * D] : 0.0f;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v += wv[u] != 0.0f ? wv[u] * x[u] : 0.0f;
     }
   }
   s_part[tid] = v;
@@ -871,9 +880,15 @@ decode_combine_kernel(const float* __restrict__ ws_acc, const float* __restrict_
   if (OL && tid < 32) {
     const float* a = ws_acco + (size_t)row * splits * 32 + tid;
     float t = 0.0f;
-    for (int s = 0; s < splits; ++s) {
-      const float w = s_w[s];
-      if (w != 0.0f) t += w * a[(size_t)s * 32];
+    for (int s0 = 0; s0 < splits; s0 += 8) {
+      float x[8], wv[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        wv[u] = s0 + u < splits ? s_w[s0 + u] : 0.0f;
+        x[u] = s0 + u < splits ? a[(size_t)(s0 + u) * 32] : 0.0f;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) t += wv[u] != 0.0f ? wv[u] * x[u] : 0.0f;
     }
     s_o[tid] = t;
   }
