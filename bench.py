@@ -275,6 +275,17 @@ def run_ours(args):
     torch.cuda.synchronize()
     dec_ms = d0.elapsed_time(d1) / K
     dec_bytes = decode_bytes(w, dec_lens)
+    # the same calls timed one by one (an event pair around each) for the spread
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(K):
+        evs[i][0].record(stream)
+        kvq.kvq_decode_attention(cache.desc, qs[i % P], out, ws, stream=stream)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    dec_each = sorted(a.elapsed_time(b) for a, b in evs)
+    dec_spread = {"median": round(statistics.median(dec_each), 5),
+                  "p10": round(dec_each[int(0.1 * (K - 1))], 5), "p90": round(dec_each[int(0.9 * (K - 1))], 5),
+                  "n": K}
 
     # ---- append alone (one token per sequence) ----------------------------------------
     cache.seq_len.copy_(seq0)
@@ -394,7 +405,8 @@ def run_ours(args):
                          f"{int(dec_lens.max())}", "achieved": round(achieved, 1), "peak": peak,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "bytes_per_launch": int(dec_bytes), "ms_per_launch": round(dec_ms, 5),
-                         "traffic": recorded_traffic("kvq_decode_impl.cuh")},
+                         "traffic": recorded_traffic("kvq_decode_impl.cuh"),
+                         "ms_per_launch_each": dec_spread},
             "append": {"tokens_per_s": round(world * w.batch * n_new / (app_ms * 1e-3), 1),
                        "ms_per_call": round(app_ms, 5), "ms_per_call_eager": round(app_eager_ms, 5),
                        "how": "kvq_rotate_quantize_append, one token per sequence, K calls in one CUDA graph "
@@ -616,10 +628,25 @@ def cpu_baseline(w: wl.Workload, budget_s: float = 15.0):
         if time.perf_counter() - t_all > budget_s or len(times) >= 30:
             break
     per = statistics.median(times)
+    # the write path too: the oracle appending one token per sequence to every KV head of the
+    # workload (the decode step's append), rotation in float64 and float32 quantizers
+    rng = np.random.Generator(np.random.PCG64(1))
+    rot = ko.rotation_enabled(w.head_dim)
+    oa = ko.OracleCache(w.batch, w.n_kv_heads, w.head_dim, 64, min(w.tail_len, 64), w.k_type, w.v_type, rot, rot)
+    x = rng.standard_normal((w.batch, 1, w.n_kv_heads, w.head_dim)).astype(np.float32)
+    at = []
+    for _ in range(20):
+        t0 = time.perf_counter()
+        oa.append(x, x)
+        at.append(time.perf_counter() - t0)
+    app = statistics.median(at)
     return {"value": round(nbytes / per / 1e9, 4), "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"decode attention of 1 of {w.batch * w.n_kv_heads} (sequence, KV head) pairs at "
                       f"{w.ctx} tokens ({w.group} query heads), float64 numpy, {len(times)} repetitions, "
                       f"median {per:.3f} s",
+            "append": {"tokens_per_s": round(w.batch / app, 1), "ms_per_call": round(app * 1e3, 3),
+                       "sample": f"oracle append of 1 token to each of {w.batch} sequences x {w.n_kv_heads} KV heads, "
+                                 f"20 repetitions, median"},
             "threads_note": "numpy elementwise work is single-threaded; its BLAS products may use all cores"}
 
 
