@@ -98,9 +98,9 @@ append_kernel(kvq_cache c, int rot_k, int rot_v, const void* __restrict__ kin, c
 // Unnormalised Sylvester FWHT of a vector held by R consecutive lanes, 32
 // consecutive channels each: the 5 in-lane channel bits in registers, the
 // log2(R) lane bits by shuffles (o + sgn*v: the rounding of the plain sum or
-// difference).
+// difference) among the lanes of `mask`, which holds whole R-lane groups.
 template <int R>
-__device__ __forceinline__ void lane_fwht(float (&r)[32], int lane) {
+__device__ __forceinline__ void lane_fwht(float (&r)[32], int lane, unsigned mask) {
 #pragma unroll
   for (int hh = 1; hh < 32; hh <<= 1)
 #pragma unroll
@@ -114,7 +114,7 @@ __device__ __forceinline__ void lane_fwht(float (&r)[32], int lane) {
   for (int m = 1; m < R; m <<= 1) {
     const float sgn = (lane & m) ? -1.0f : 1.0f;  // upper partner: o - v, lower: v + o
 #pragma unroll
-    for (int j = 0; j < 32; ++j) r[j] = fmaf(sgn, r[j], __shfl_xor_sync(0xffffffffu, r[j], m));
+    for (int j = 0; j < 32; ++j) r[j] = fmaf(sgn, r[j], __shfl_xor_sync(mask, r[j], m));
   }
 }
 
@@ -122,20 +122,22 @@ __device__ __forceinline__ void lane_fwht(float (&r)[32], int lane) {
 // bytes; qh_word: q5_x high bits or null; d_ptr: fp16 d or the (d, lo) word).
 __device__ __forceinline__ void quantize_lane_block(const float (&y)[32], int qt, uint8_t* qs_blk,
                                                     uint32_t* qh_word, void* d_ptr) {
-  uint8_t code[32];
-  if (type_has_min(qt)) {
-    float lo = y[0], hi = y[0];
+  // block parameters, then each code computed once straight into its packed byte
+  float lo = 0.0f, id = 0.0f, off = 0.0f;
+  int top = 0;
+  const bool q8 = qt == KVQ_TYPE_Q8_0, mn = type_has_min(qt);
+  if (mn) {
+    float hi = y[0];
+    lo = y[0];
 #pragma unroll
     for (int j = 1; j < 32; ++j) {  // first index on ties: strict comparisons in ascending order
       if (y[j] < lo) lo = y[j];
       if (y[j] > hi) hi = y[j];
     }
-    const int top = qt == KVQ_TYPE_Q5_1 ? 31 : 15;
+    top = qt == KVQ_TYPE_Q5_1 ? 31 : 15;
     const float d = __fdiv_rn(__fsub_rn(hi, lo), float(top));
-    const float id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      code[j] = uint8_t(min(top, __float2int_rz(__fadd_rn(__fmul_rn(__fsub_rn(y[j], lo), id), 0.5f))));
+    id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
+    off = 0.5f;
     *static_cast<uint32_t*>(d_ptr) = uint32_t(__half_as_ushort(__float2half_rn(d))) |
                                      (uint32_t(__half_as_ushort(__float2half_rn(lo))) << 16);
   } else {
@@ -146,48 +148,43 @@ __device__ __forceinline__ void quantize_lane_block(const float (&y)[32], int qt
       if (a > best_a) { best_a = a; best_m = y[j]; }
     }
     float d;
-    if (qt == KVQ_TYPE_Q8_0) {
+    if (q8) {
       d = best_a / 127.0f;
-      const float id = d != 0.0f ? 1.0f / d : 0.0f;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) code[j] = uint8_t(int8_t(int(roundf(__fmul_rn(y[j], id)))));
     } else {
       const bool q5 = qt == KVQ_TYPE_Q5_0;
       d = q5 ? best_m / -16.0f : best_m / -8.0f;
-      const float id = d != 0.0f ? 1.0f / d : 0.0f;
-      const float off = q5 ? 16.5f : 8.5f;
-      const int top = q5 ? 31 : 15;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) code[j] = uint8_t(min(top, __float2int_rz(__fadd_rn(__fmul_rn(y[j], id), off))));
+      off = q5 ? 16.5f : 8.5f;
+      top = q5 ? 31 : 15;
     }
+    id = d != 0.0f ? 1.0f / d : 0.0f;
     *static_cast<__half*>(d_ptr) = __float2half_rn(d);
   }
-  uint32_t w[8];
-  if (qt == KVQ_TYPE_Q8_0) {
+  // code of value j, operation by operation as the block definitions state
+  auto code_of = [&](int j) -> uint32_t {
+    if (q8) return uint32_t(uint8_t(int8_t(int(roundf(__fmul_rn(y[j], id))))));
+    if (mn) return uint32_t(min(top, __float2int_rz(__fadd_rn(__fmul_rn(__fsub_rn(y[j], lo), id), off))));
+    return uint32_t(min(top, __float2int_rz(__fadd_rn(__fmul_rn(y[j], id), off))));
+  };
+  if (q8) {
+    uint32_t w[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k)
-      w[k] = uint32_t(code[4 * k]) | (uint32_t(code[4 * k + 1]) << 8) | (uint32_t(code[4 * k + 2]) << 16) |
-             (uint32_t(code[4 * k + 3]) << 24);
+      w[k] = code_of(4 * k) | (code_of(4 * k + 1) << 8) | (code_of(4 * k + 2) << 16) | (code_of(4 * k + 3) << 24);
     reinterpret_cast<uint4*>(qs_blk)[0] = make_uint4(w[0], w[1], w[2], w[3]);
     reinterpret_cast<uint4*>(qs_blk)[1] = make_uint4(w[4], w[5], w[6], w[7]);
     return;
   }
-  // byte k = code_k | code_{k+16} << 4
+  // byte k = code_k | code_{k+16} << 4; high bits (q5_x) bit j = bit 4 of code_j
+  uint32_t w[4] = {0u, 0u, 0u, 0u}, h = 0;
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    uint32_t t = 0;
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      t |= uint32_t((code[4 * k + e] & 0x0F) | ((code[4 * k + e + 16] & 0x0F) << 4)) << (8 * e);
-    w[k] = t;
+  for (int k = 0; k < 16; ++k) {
+    const uint32_t c0 = code_of(k), c1 = code_of(k + 16);
+    w[k / 4] |= ((c0 & 0x0Fu) | ((c1 & 0x0Fu) << 4)) << (8 * (k % 4));
+    h |= ((c0 >> 4) & 1u) << k;
+    h |= ((c1 >> 4) & 1u) << (k + 16);
   }
   *reinterpret_cast<uint4*>(qs_blk) = make_uint4(w[0], w[1], w[2], w[3]);
-  if (type_has_qh(qt)) {
-    uint32_t h = 0;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) h |= uint32_t((code[j] >> 4) & 1) << j;
-    *qh_word = h;
-  }
+  if (type_has_qh(qt)) *qh_word = h;
 }
 
 template <int D>
@@ -238,22 +235,14 @@ append_rows_kernel(kvq_cache c, int rot_k, int rot_v, const void* __restrict__ k
       }
     }
   }
-  // rotation (a warp mixes K and V vectors: when only one of them rotates, the
-  // butterflies run on a copy so that every lane takes part in the shuffles)
+  // rotation: the R lanes of a vector rotate together (a warp may mix K and V
+  // vectors, which rotate or not); the shuffles name exactly the rotating lanes
   const bool rot = (which ? rot_v : rot_k) && !prerotated;
-  if (__all_sync(0xffffffffu, rot)) {
-    lane_fwht<R>(y, lane);
+  const unsigned rmask = __ballot_sync(0xffffffffu, rot);
+  if (rot) {
+    lane_fwht<R>(y, lane, rmask);
 #pragma unroll
     for (int j = 0; j < 32; ++j) y[j] *= inv_sqrt_group<D>();
-  } else if (__any_sync(0xffffffffu, rot)) {
-    float r[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) r[j] = y[j];
-    lane_fwht<R>(r, lane);
-    if (rot) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) y[j] = r[j] * inv_sqrt_group<D>();
-    }
   }
   const int pos = n0 + i;
   const int qt = which ? c.v_type : c.k_type;
