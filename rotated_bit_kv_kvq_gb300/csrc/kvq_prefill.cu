@@ -137,19 +137,46 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t&
   lo = pack_h2(a - f.x, b - f.y);
 }
 
-// 8 stored values (channels 8*ch .. 8*ch+7) of one key, times 2^-8.
+// The raw stored words behind 8 values (channels 8*ch .. 8*ch+7) of one key:
+// 16 bytes of bf16 tail values, or 8 bytes of codes with the block header
+// (fp16 d, or the (d, lo) pair) and the q5_x high-bit word.  Loaded first for
+// every chunk a thread handles, so that the loads overlap; decoded after.
+struct Raw8 {
+  uint4 w;
+  uint32_t hdr, qh;
+};
+
 template <int D>
-__device__ __forceinline__ void load8(const SParams& p, bool is_v, int qt, bool valid, bool tail, size_t body_row,
-                                      size_t tail_row, int ch, float (&x)[8]) {
+__device__ __forceinline__ Raw8 fetch8(const SParams& p, bool is_v, int qt, bool valid, bool tail, size_t body_row,
+                                       size_t tail_row, int ch) {
   constexpr int NB = D / 32;
+  Raw8 r{make_uint4(0u, 0u, 0u, 0u), 0u, 0u};
+  if (!valid) return r;
+  if (tail) {
+    r.w = *reinterpret_cast<const uint4*>((is_v ? p.v_tail : p.k_tail) + tail_row * D + ch * 8);
+    return r;
+  }
+  const int c0 = ch * 8, blk = c0 / 32, w = c0 % 32;
+  const uint8_t* hd = (is_v ? p.v_d : p.k_d) + (body_row * NB + blk) * (type_has_min(qt) ? 4 : 2);
+  r.hdr = type_has_min(qt) ? *reinterpret_cast<const uint32_t*>(hd) : uint32_t(*reinterpret_cast<const uint16_t*>(hd));
+  const uint8_t* qs = is_v ? p.v_qs : p.k_qs;
+  const uint2 a = qt == KVQ_TYPE_Q8_0 ? *reinterpret_cast<const uint2*>(qs + body_row * D + c0)
+                                      : *reinterpret_cast<const uint2*>(qs + body_row * (D / 2) + blk * 16 + (w & 15));
+  r.w.x = a.x;
+  r.w.y = a.y;
+  if (type_has_qh(qt)) r.qh = (is_v ? p.v_qh : p.k_qh)[body_row * NB + blk];
+  return r;
+}
+
+// 8 stored values (channels 8*ch .. 8*ch+7) of one key, times 2^-8, from their raw words.
+__device__ __forceinline__ void decode8(const Raw8& r, int qt, bool valid, bool tail, int ch, float (&x)[8]) {
   if (!valid) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) x[e] = 0.0f;
     return;
   }
   if (tail) {
-    const uint4 w = *reinterpret_cast<const uint4*>((is_v ? p.v_tail : p.k_tail) + tail_row * D + ch * 8);
-    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+    const uint32_t ww[4] = {r.w.x, r.w.y, r.w.z, r.w.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       x[2 * e] = __uint_as_float(ww[e] << 16) * kInvScale;
@@ -157,28 +184,21 @@ __device__ __forceinline__ void load8(const SParams& p, bool is_v, int qt, bool 
     }
     return;
   }
-  const int c0 = ch * 8, blk = c0 / 32, w = c0 % 32;
-  const int hb = type_has_min(qt) ? 2 : 1;  // halves per block header
-  const __half* hdr = reinterpret_cast<const __half*>(is_v ? p.v_d : p.k_d) + (body_row * NB + blk) * hb;
-  const float sc = __half2float(hdr[0]) * kInvScale;
-  const float mn = type_has_min(qt) ? __half2float(hdr[1]) * kInvScale : 0.0f;  // x = code*d + lo
-  const uint8_t* qs = is_v ? p.v_qs : p.k_qs;
+  const int w = (ch * 8) % 32;
+  const float sc = __half2float(__ushort_as_half(uint16_t(r.hdr & 0xFFFFu))) * kInvScale;
+  const float mn = type_has_min(qt) ? __half2float(__ushort_as_half(uint16_t(r.hdr >> 16))) * kInvScale : 0.0f;
   if (qt == KVQ_TYPE_Q8_0) {
-    const uint2 a = *reinterpret_cast<const uint2*>(qs + body_row * D + c0);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) x[e] = float(int8_t((e < 4 ? a.x : a.y) >> (8 * (e & 3)))) * sc;
+    for (int e = 0; e < 8; ++e) x[e] = float(int8_t((e < 4 ? r.w.x : r.w.y) >> (8 * (e & 3)))) * sc;
   } else {
     // byte i of a block holds element i (low nibble) and element i + 16 (high nibble)
-    const uint2 a = *reinterpret_cast<const uint2*>(qs + body_row * (D / 2) + blk * 16 + (w & 15));
     const int shift = w < 16 ? 0 : 4;
-    uint32_t qh = 0;
     const int off = type_code_offset(qt);
-    if (type_has_qh(qt)) qh = (is_v ? p.v_qh : p.k_qh)[body_row * NB + blk];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      const uint32_t byte = ((e < 4 ? a.x : a.y) >> (8 * (e & 3))) & 0xFFu;
-      const int code = int((byte >> shift) & 15u) | int(((qh >> (w + e)) & 1u) << 4);
-      x[e] = __fadd_rn(__fmul_rn(float(code - off), sc), mn);
+      const uint32_t byte = ((e < 4 ? r.w.x : r.w.y) >> (8 * (e & 3))) & 0xFFu;
+      const int code = int((byte >> shift) & 15u) | int(((r.qh >> (w + e)) & 1u) << 4);
+      x[e] = __fadd_rn(__fmul_rn(float(code - off), sc), mn);  // x = code*d + lo
     }
   }
 }
@@ -194,7 +214,7 @@ __device__ __forceinline__ void add8(const float* src, float (&x)[8]) {
 // stage_kernel: one 64-key tile of one (sequence, KV head) -> workspace
 // ---------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(kStageThreads, 2) stage_kernel(SParams p) {
+__global__ void __launch_bounds__(kStageThreads, 3) stage_kernel(SParams p) {
   using L = PL<D>;
   constexpr int NCH = D / 8;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -261,11 +281,22 @@ __global__ void __launch_bounds__(kStageThreads, 2) stage_kernel(SParams p) {
     }
     __syncthreads();
   }
-#pragma unroll 1
-  for (int ch = threadIdx.x / kPN; ch < NCH; ch += kStageThreads / kPN) {
+  // every chunk's raw words first (K and V), then decode, split and store
+  constexpr int IT = NCH / (kStageThreads / kPN);  // chunks per thread
+  static_assert(NCH % (kStageThreads / kPN) == 0, "chunks per thread");
+  Raw8 rk[IT], rv[IT];
+#pragma unroll
+  for (int it = 0; it < IT; ++it) {
+    const int ch = threadIdx.x / kPN + it * (kStageThreads / kPN);
+    rk[it] = fetch8<D>(p, false, p.k_type, valid, tail, body_row, tail_row, ch);
+    rv[it] = fetch8<D>(p, true, p.v_type, valid, tail, body_row, tail_row, ch);
+  }
+#pragma unroll
+  for (int it = 0; it < IT; ++it) {
+    const int ch = threadIdx.x / kPN + it * (kStageThreads / kPN);
     // K: row = key, 16-byte chunks of 8 channels
     float x[8];
-    load8<D>(p, false, p.k_type, valid, tail, body_row, tail_row, ch, x);
+    decode8(rk[it], p.k_type, valid, tail, ch, x);
     if (ol) add8(obuf + (size_t)key * D + ch * 8, x);
     uint32_t h[4], l[4];
 #pragma unroll
@@ -275,7 +306,7 @@ __global__ void __launch_bounds__(kStageThreads, 2) stage_kernel(SParams p) {
     *reinterpret_cast<uint4*>(sm + off) = make_uint4(h[0], h[1], h[2], h[3]);
     *reinterpret_cast<uint4*>(sm + kPN * 128 + off) = make_uint4(l[0], l[1], l[2], l[3]);
     // V^T: row = channel, this key's 2-byte element in it
-    load8<D>(p, true, p.v_type, valid, tail, body_row, tail_row, ch, x);
+    decode8(rv[it], p.v_type, valid, tail, ch, x);
     if (ol) add8(obuf + (size_t)(kPN + key) * D + ch * 8, x);
 #pragma unroll
     for (int e = 0; e < 4; ++e) split2(x[2 * e], x[2 * e + 1], h[e], l[e]);
