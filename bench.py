@@ -513,6 +513,17 @@ def run_format_pairs(torch, kvq, w: wl.Workload, steps: int, peak: float, pairs=
             r["layout"] = "paged, shuffled page table"
         if outliers:
             r["n_outlier"] = 32
+            # the write path of this cache: one 8,192-token append of the workload's sequences and heads
+            kb = (torch.randn(w2.batch, 8192, w2.n_kv_heads, w2.head_dim, generator=gen, device="cuda")).to(torch.bfloat16)
+            cache.seq_len.zero_()
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            kvq.kvq_rotate_quantize_append(cache.desc, kb, kb, stream=stream)
+            cache.seq_len.zero_()
+            a0.record(stream)
+            kvq.kvq_rotate_quantize_append(cache.desc, kb, kb, stream=stream)
+            a1.record(stream)
+            torch.cuda.synchronize()
+            r["append_8192_ms"] = round(a0.elapsed_time(a1), 4)
         res.append(r)
         del cache, ws
         torch.cuda.empty_cache()

@@ -187,7 +187,7 @@ __device__ __forceinline__ void quantize_lane_block(const float (&y)[32], int qt
   if (type_has_qh(qt)) *qh_word = h;
 }
 
-template <int D>
+template <int D, bool OUTL>
 __global__ void __launch_bounds__(kAppendWarps * 32)
 append_rows_kernel(kvq_cache c, int rot_k, int rot_v, const void* __restrict__ kin, const void* __restrict__ vin,
                    int in_dtype, int n_new, const int32_t* __restrict__ n_new_per_seq, int prerotated) {
@@ -235,6 +235,43 @@ append_rows_kernel(kvq_cache c, int rot_k, int rot_v, const void* __restrict__ k
       }
     }
   }
+  // Outlier channels (OUTL): the raw vector is staged in shared memory; lane sub
+  // takes slots sub*SL .. sub*SL+SL-1 of the head's list (their unrotated values
+  // become one q8_0 block, written below), and zeroes its own block's channels
+  // that are slots before the rest is rotated and quantized.
+  constexpr int SL = 32 / R;  // outlier slots per lane
+  float ov[OUTL ? SL : 1];
+  float* raw = nullptr;
+  if constexpr (OUTL) {
+    __shared__ __align__(16) float s_raw[kAppendWarps][32 * 32];
+    raw = &s_raw[threadIdx.x >> 5][(lane / R) * D];
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+      *reinterpret_cast<float4*>(raw + 32 * sub + 4 * t) = make_float4(y[4 * t], y[4 * t + 1], y[4 * t + 2], y[4 * t + 3]);
+    __syncwarp();
+    const int32_t* idx = c.outlier_idx + (size_t)h * 32;
+    uint32_t zmask = 0;
+    bool bad = false;
+    int prev = -1;
+#pragma unroll 4
+    for (int s2 = 0; s2 < 32; ++s2) {  // strictly increasing inside [0, D), as every kernel checks it
+      const int ch = idx[s2];
+      const bool okc = ch >= 0 && ch < D && (s2 == 0 || prev < ch);
+      prev = ch;
+      bad |= !okc;
+      if (okc && ch / 32 == sub) zmask |= 1u << (ch % 32);
+    }
+#pragma unroll
+    for (int k = 0; k < SL; ++k) {
+      const int s2 = sub * SL + k;
+      const int ch = idx[s2];
+      const bool okc = ch >= 0 && ch < D && (s2 == 0 || idx[s2 - 1] < ch);
+      ov[k] = okc ? raw[ch] : 0.0f;
+    }
+    if (bad && live && sub == 0) atomicOr(&c.status[0], KVQ_DEV_ERR_OUTLIER);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) y[j] = ((zmask >> j) & 1u) ? 0.0f : y[j];
+  }
   // rotation: the R lanes of a vector rotate together (a warp may mix K and V
   // vectors, which rotate or not); the shuffles name exactly the rotating lanes
   const bool rot = (which ? rot_v : rot_k) && !prerotated;
@@ -258,6 +295,48 @@ append_rows_kernel(kvq_cache c, int rot_k, int rot_v, const void* __restrict__ k
     uint32_t* qh = static_cast<uint32_t*>(which ? c.v_qh : c.k_qh);
     uint8_t* dp = static_cast<uint8_t*>(which ? c.v_d : c.k_d) + (row * NB + sub) * (type_has_min(qt) ? 4 : 2);
     quantize_lane_block(y, qt, qs, qh ? qh + row * NB + sub : nullptr, dp);
+  }
+  if constexpr (OUTL) {
+    // the slots' q8_0 block: amax over the vector's R lanes, then this lane's SL codes
+    float amax = 0.0f;
+#pragma unroll
+    for (int k = 0; k < SL; ++k) amax = fmaxf(amax, fabsf(ov[k]));
+#pragma unroll
+    for (int m = 1; m < R; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+    const float d = amax / 127.0f;
+    const float id = d != 0.0f ? 1.0f / d : 0.0f;
+    if (store && brow >= 0) {
+      const size_t row = size_t(brow);
+      uint8_t* grp = static_cast<uint8_t*>(c.outl) + (row / 16) * kOutlTile;
+      uint8_t* oqs = grp + which * 512 + (row % 16) * 32 + sub * SL;
+      uint32_t w[SL / 4 > 0 ? SL / 4 : 1];
+#pragma unroll
+      for (int k = 0; k < SL / 4; ++k) {
+        w[k] = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          w[k] |= uint32_t(uint8_t(int8_t(int(roundf(__fmul_rn(ov[4 * k + e], id)))))) << (8 * e);
+      }
+      if constexpr (SL == 16) *reinterpret_cast<uint4*>(oqs) = make_uint4(w[0], w[1], w[2], w[3]);
+      else if constexpr (SL == 8) *reinterpret_cast<uint2*>(oqs) = make_uint2(w[0], w[1]);
+      else *reinterpret_cast<uint32_t*>(oqs) = w[0];
+      if (sub == 0) reinterpret_cast<__half*>(grp + 1024 + which * 32)[row % 16] = __float2half_rn(d);
+    }
+    // the tail keeps the whole vector: rotate the staged raw values again
+    const bool tail_row = store && c.tail_len > 0 && i >= nb - c.tail_len;
+    const unsigned tmask = __ballot_sync(0xffffffffu, tail_row && rot);
+    if (tail_row) {
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const float4 x = *reinterpret_cast<const float4*>(raw + 32 * sub + 4 * t);
+        y[4 * t] = x.x; y[4 * t + 1] = x.y; y[4 * t + 2] = x.z; y[4 * t + 3] = x.w;
+      }
+      if (rot) {
+        lane_fwht<R>(y, lane, tmask);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) y[j] *= inv_sqrt_group<D>();
+      }
+    }
   }
   if (store && c.tail_len > 0 && i >= nb - c.tail_len) {
     uint16_t* tail = static_cast<uint16_t*>(which ? c.v_tail : c.k_tail) +
@@ -367,10 +446,13 @@ cudaError_t append_d(const kvq_cache& c, Rot rot, const void* k, const void* v, 
   if constexpr (D == 64 || D == 128 || D == 256) {
     // one block per lane (32 / (D/32) vectors per warp) for bulk appends; a few
     // vectors (a decode step) finish sooner spread one per warp
-    if (!c.n_outlier && warps >= kRowsMinVectors) {
+    if (warps >= kRowsMinVectors) {
       const long long per_cta = (long long)kAppendWarps * (32 / (D / 32));
-      append_rows_kernel<D><<<unsigned((warps + per_cta - 1) / per_cta), kAppendWarps * 32, 0, st>>>(
-          c, rot.k, rot.v, k, v, in_dtype, n_new, nps, pre);
+      const unsigned grid = unsigned((warps + per_cta - 1) / per_cta);
+      if (c.n_outlier)
+        append_rows_kernel<D, true><<<grid, kAppendWarps * 32, 0, st>>>(c, rot.k, rot.v, k, v, in_dtype, n_new, nps, pre);
+      else
+        append_rows_kernel<D, false><<<grid, kAppendWarps * 32, 0, st>>>(c, rot.k, rot.v, k, v, in_dtype, n_new, nps, pre);
       return cudaGetLastError();
     }
   }

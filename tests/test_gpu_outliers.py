@@ -247,3 +247,27 @@ def test_prefill_paged():
     _append(kvq, torch, gc, oc, k, v, [180, 77])
     q = rng.standard_normal((B, 77, H * g, d)).astype(np.float32)
     assert_close(gpu_prefill(gc, q, "f32", torch), ko.prefill_attention(oc, q), what="paged prefill")
+
+
+@pytest.mark.parametrize("d,rot,kt,vt", [(64, True, "q4_0", "q8_0"), (256, True, "q5_0", "q4_0"),
+                                         (128, False, "q8_0", "q5_0")])
+def test_bulk_append_bit_exact(d, rot, kt, vt):
+    """Appends of at least 2,048 vectors (the block-per-lane kernel with the
+    outlier slots staged in shared memory): blocks, outlier planes and tail rows
+    bit-exact after two ragged calls, then decode."""
+    torch = require_gpu()
+    from rotated_bit_kv_kvq_gb300 import kvq
+    rng = np.random.default_rng(89)
+    B, H, g, T = 2, 4, 2, 16
+    oidx = _outliers(rng, H, d)
+    gc, oc = _caches(kvq, B, H, d, 640, T, kt, vt, rot, oidx)
+    for n, nps in ((300, [300, 280]), (290, [250, 290])):
+        if rot:
+            k, v = _dyadic(rng, (B, n, H, d), oidx), _dyadic(rng, (B, n, H, d), oidx)
+        else:
+            k = rng.standard_normal((B, n, H, d)).astype(np.float32)
+            v = rng.standard_normal((B, n, H, d)).astype(np.float32)
+        _append(kvq, torch, gc, oc, k, v, nps)
+    _check_cache(torch, gc, oc, kt, vt, d)
+    q = rng.standard_normal((B, H * g, d)).astype(np.float32)
+    assert_close(gpu_decode(gc, q, "f32", torch), ko.decode_attention(oc, q), what=f"bulk d{d}")
