@@ -95,29 +95,6 @@ append_kernel(kvq_cache c, int rot_k, int rot_v, const void* __restrict__ kin, c
 // by operation.
 // ---------------------------------------------------------------------------
 
-// Unnormalised Sylvester FWHT of a vector held by R consecutive lanes, 32
-// consecutive channels each: the 5 in-lane channel bits in registers, the
-// log2(R) lane bits by shuffles (o + sgn*v: the rounding of the plain sum or
-// difference) among the lanes of `mask`, which holds whole R-lane groups.
-template <int R>
-__device__ __forceinline__ void lane_fwht(float (&r)[32], int lane, unsigned mask) {
-#pragma unroll
-  for (int hh = 1; hh < 32; hh <<= 1)
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if ((j & hh) == 0) {
-        const float a = r[j], bq = r[j + hh];
-        r[j] = a + bq;
-        r[j + hh] = a - bq;
-      }
-#pragma unroll
-  for (int m = 1; m < R; m <<= 1) {
-    const float sgn = (lane & m) ? -1.0f : 1.0f;  // upper partner: o - v, lower: v + o
-#pragma unroll
-    for (int j = 0; j < 32; ++j) r[j] = fmaf(sgn, r[j], __shfl_xor_sync(mask, r[j], m));
-  }
-}
-
 // One 32-value block held by one lane: quantize and store (qs: the block's
 // bytes; qh_word: q5_x high bits or null; d_ptr: fp16 d or the (d, lo) word).
 __device__ __forceinline__ void quantize_lane_block(const float (&y)[32], int qt, uint8_t* qs_blk,

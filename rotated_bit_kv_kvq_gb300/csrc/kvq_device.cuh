@@ -270,6 +270,29 @@ __device__ __forceinline__ void warp_fwht(float (&v)[D / 32], int lane) {
   }
 }
 
+// Unnormalised Sylvester FWHT of a vector held by R consecutive lanes, 32
+// consecutive channels each: the 5 in-lane channel bits in registers, the
+// log2(R) lane bits by shuffles (o + sgn*v: the rounding of the plain sum or
+// difference) among the lanes of `mask`, which holds whole R-lane groups.
+template <int R>
+__device__ __forceinline__ void lane_fwht(float (&r)[32], int lane, unsigned mask) {
+#pragma unroll
+  for (int hh = 1; hh < 32; hh <<= 1)
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if ((j & hh) == 0) {
+        const float a = r[j], bq = r[j + hh];
+        r[j] = a + bq;
+        r[j + hh] = a - bq;
+      }
+#pragma unroll
+  for (int m = 1; m < R; m <<= 1) {
+    const float sgn = (lane & m) ? -1.0f : 1.0f;  // upper partner: o - v, lower: v + o
+#pragma unroll
+    for (int j = 0; j < 32; ++j) r[j] = fmaf(sgn, r[j], __shfl_xor_sync(mask, r[j], m));
+  }
+}
+
 // 1/sqrt(G) correctly rounded to fp32.
 template <int G>
 __host__ __device__ constexpr float inv_sqrt_group() {

@@ -359,30 +359,6 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
-// Unnormalised Sylvester FWHT of D-channel rows, one row per R = D/32
-// consecutive lanes: lane l holds channels 32(l % R) .. 32(l % R) + 31 of row
-// l / R.  The 5 channel bits inside a lane are combined in registers, the
-// remaining log2(R) across lanes (one shuffle per value per bit).
-template <int D>
-__device__ __forceinline__ void row_fwht(float (&v)[32], int lane) {
-  static_assert(D == 64 || D == 128, "rows of 64 or 128 channels");
-#pragma unroll
-  for (int h = 1; h < 32; h <<= 1)
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if ((i & h) == 0) {
-        const float a = v[i], b = v[i + h];
-        v[i] = a + b;
-        v[i + h] = a - b;
-      }
-#pragma unroll
-  for (int m = 1; m < D / 32; m <<= 1) {
-    const float sgn = (lane & m) ? -1.0f : 1.0f;  // upper partner: o - v, lower: v + o
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = fmaf(sgn, v[i], __shfl_xor_sync(0xffffffffu, v[i], m));
-  }
-}
-
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
   using L = PL<D>;
@@ -577,7 +553,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
         else x = __half2float(__ushort_as_half(uint16_t(hb)));
         v[i] = ok ? x : 0.0f;
       }
-      if (p.rot_k) row_fwht<D>(v, lane);
+      if (p.rot_k) lane_fwht<D / 32>(v, lane, 0xffffffffu);  // a row on D/32 lanes
       // the lane's 32 channels = four 16-byte chunks of 8 fp16 in each of the hi / lo tiles
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
