@@ -271,3 +271,21 @@ def test_bulk_append_bit_exact(d, rot, kt, vt):
     _check_cache(torch, gc, oc, kt, vt, d)
     q = rng.standard_normal((B, H * g, d)).astype(np.float32)
     assert_close(gpu_decode(gc, q, "f32", torch), ko.decode_attention(oc, q), what=f"bulk d{d}")
+
+
+def test_decode_two_head_groups():
+    """12 query heads per KV head: two CTAs along the head axis share one KV
+    head's outlier list; the merge finds each query head's list by its KV head."""
+    torch = require_gpu()
+    from rotated_bit_kv_kvq_gb300 import kvq
+    rng = np.random.default_rng(90)
+    B, H, g, d, T = 2, 2, 12, 128, 8
+    oidx = _outliers(rng, H, d)
+    gc, oc = _caches(kvq, B, H, d, 512, T, "q4_0", "q8_0", False, oidx)
+    k = rng.standard_normal((B, 400, H, d)).astype(np.float32)
+    v = rng.standard_normal((B, 400, H, d)).astype(np.float32)
+    for h in range(H):
+        v[:, :, h][..., oidx[h][:2]] *= 15
+    _append(kvq, torch, gc, oc, k, v, [400, 211])
+    q = rng.standard_normal((B, H * g, d)).astype(np.float32)
+    assert_close(gpu_decode(gc, q, "f32", torch), ko.decode_attention(oc, q), what="two head groups")
