@@ -82,6 +82,30 @@ DecodePlan plan_decode(const kvq_cache& c, int n_q_heads, int sm_count) {
   pl.chunk = chunk;
   pl.splits_body = (c.max_ctx + chunk - 1) / chunk;
   pl.splits = pl.splits_body + pl.splits_tail;
+  pl.cls_len[0] = chunk; pl.cls_len[1] = chunk; pl.cls_len[2] = chunk;
+  pl.cls_cnt[0] = pl.splits_body; pl.cls_cnt[1] = 0; pl.cls_cnt[2] = 0;
+  // One wave of three CTAs per SM: the CTAs are dispatched split by split (the kernel reads
+  // its linear block index split-major), so the first sm_count take the first slot of every
+  // SM, the next sm_count the second, the rest the third.  An SM's warp scheduler favours its
+  // oldest warps: measured on the 64k workload, equal chunks end after 96, 105 and 113 us by
+  // slot.  Chunks sized 1/96 : 1/105 : 1/113 by slot let the three end together.
+  const int cps = ctas_per_sm(c.head_dim, c.n_outlier != 0);
+  const long long sms = sm_count > 0 ? sm_count : 148;
+  const long long ctas = (long long)pl.splits * pairs;
+  if (cps == 3 && ctas <= 3 * sms && ctas > 2 * sms && pl.splits_body >= 3) {
+    const double w[3] = {105.0 / 96.0, 1.0, 105.0 / 113.0};
+    int cnt[3] = {0, 0, 0};
+    for (int s = 0; s < pl.splits_body; ++s) {
+      const long long mid = (long long)(s + pl.splits_tail) * pairs + pairs / 2;
+      ++cnt[mid / sms >= 2 ? 2 : int(mid / sms)];
+    }
+    double tot = 0.0;
+    for (int k = 0; k < 3; ++k) tot += cnt[k] * w[k];
+    for (int k = 0; k < 3; ++k) {
+      pl.cls_cnt[k] = cnt[k];
+      pl.cls_len[k] = int(((long long)(c.max_ctx * w[k] / tot) + 64) / 64 * 64);
+    }
+  }
   pl.ws_bytes = (size_t)c.batch * n_q_heads * pl.splits * (c.head_dim + 2 + c.n_outlier) * sizeof(float);
   return pl;
 }

@@ -109,6 +109,9 @@ struct Params {
   int rot_k;
   float scale_log2;                 // softmax scale * log2(e)
   int chunk, tail_chunk, splits_body, splits_tail, splits;
+  // body chunk classes in dispatch order (DecodePlan): class k holds the splits from cls_s0[k],
+  // cls_len[k] tokens each, the first starting at token cls_beg[k]
+  int cls_len[3], cls_s0[3], cls_beg[3];
   // fused step: new tokens written by the tail CTA (fused != 0)
   int fused, rot_v;
   FusedAppend fa;
@@ -155,19 +158,22 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, tig = lane & 3;
-  const int b = blockIdx.z;
-  const int kvh = blockIdx.y / p.head_groups;
-  const int hg = blockIdx.y % p.head_groups;
+  // grid (KV head x head group, sequence, split): all CTAs of split 0 are dispatched first,
+  // then those of split 1, ... (a split's body chunk depends on it)
+  const int split = blockIdx.z;
+  const int yy = blockIdx.x;
+  const int b = blockIdx.y;
+  const int kvh = yy / p.head_groups;
+  const int hg = yy % p.head_groups;
   const int head0 = kvh * p.group + hg * p.heads_per_cta;
   const int nheads = min(p.heads_per_cta, p.group - hg * p.heads_per_cta);
-  const int split = blockIdx.x;
 
   const int n0 = p.seq_len[b];
   int nn = 0;  // tokens this launch appends to sequence b (fused step)
   if (p.fused) {
     bool ok;
     nn = fused_count(p.fa, n0, b, p.max_ctx, ok);
-    if (!ok && tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(p.status, KVQ_DEV_ERR_APPEND_RANGE);
+    if (!ok && tid == 0 && split == 0 && yy == 0) atomicOr(p.status, KVQ_DEV_ERR_APPEND_RANGE);
   }
   const int n = n0 + nn;
   const int T = p.tail_len;
@@ -179,8 +185,10 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     t_begin = split * p.tail_chunk;
     t_end = min(ntail, t_begin + p.tail_chunk);
   } else {
-    t_begin = (split - p.splits_tail) * p.chunk;
-    t_end = min(nbody, t_begin + p.chunk);
+    const int s = split - p.splits_tail;
+    const int k = int(s >= p.cls_s0[1]) + int(s >= p.cls_s0[2]);  // chunk class of this split
+    t_begin = p.cls_beg[k] + (s - p.cls_s0[k]) * p.cls_len[k];
+    t_end = min(nbody, t_begin + p.cls_len[k]);
   }
   float* ml = p.ws_ml + (((size_t)b * p.n_q_heads + head0) * p.splits + split) * 2;
   if (t_begin >= t_end) {  // nothing to read: an empty partial
@@ -994,6 +1002,13 @@ cudaError_t run_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, cons
   p.rows = row_map(c);
   p.scale_log2 = scale * kLog2e;
   p.chunk = plan.chunk; p.tail_chunk = plan.tail_chunk; p.splits_body = plan.splits_body; p.splits_tail = plan.splits_tail; p.splits = plan.splits;
+  for (int k = 0, s0 = 0, beg = 0; k < 3; ++k) {
+    p.cls_len[k] = plan.cls_len[k];
+    p.cls_s0[k] = s0;
+    p.cls_beg[k] = beg;
+    s0 += plan.cls_cnt[k];
+    beg += plan.cls_cnt[k] * plan.cls_len[k];
+  }
 
   alignas(64) CUtensorMap mk, mv, mkt, mvt;
   memset(&mk, 0, sizeof(mk)); memset(&mv, 0, sizeof(mv)); memset(&mkt, 0, sizeof(mkt)); memset(&mvt, 0, sizeof(mvt));
@@ -1009,7 +1024,7 @@ cudaError_t run_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, cons
   auto kern = decode_split_kernel<D, KT, VT, OL>;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), Cf::smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(plan.splits, c.n_kv_heads * plan.head_groups, c.batch);
+  dim3 grid(c.n_kv_heads * plan.head_groups, c.batch, plan.splits);
   kern<<<grid, kThreads, Cf::smem, st>>>(p, mk, mv, mkt, mvt);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

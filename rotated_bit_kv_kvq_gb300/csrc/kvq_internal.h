@@ -65,6 +65,10 @@ struct DecodePlan {
   int splits;          // splits_body + splits_tail
   size_t ws_bytes;     // workspace bytes: acc [B][Hq][splits][D], (m, l) [B][Hq][splits][2],
                        // then, with outlier channels, their acc [B][Hq][splits][32]
+  // body splits in dispatch order come in up to three classes of cls_cnt[c] splits of
+  // cls_len[c] tokens (a multiple of 64); a uniform plan has one class of `chunk`
+  int cls_len[3];
+  int cls_cnt[3];
 };
 // n_outlier > 0: the q4_0 / q5_0 / q8_0 pairs at head_dim 64, 128 and 256.
 bool decode_supported(int d, int kt, int vt, int n_outlier);
