@@ -95,6 +95,7 @@ struct Cfg {
   static constexpr int off_bar = OL ? off_qof + 2 * 32 * 16 : off_qsum + NB * kMaxHeads * 4;  // mbarriers [kWarps][NS]
   static constexpr int off_ml = off_bar + kWarps * NS * 8;          // [kWarps][8] m and l
   static constexpr int smem = off_ml + 2 * kWarps * kMaxHeads * 4 + 1024;  // + alignment slack
+  static_assert(NB % 2 == 0, "V block headers are read in pairs of blocks");
   static_assert(kWarps * kMaxHeads * (D + (OL ? 32 : 0)) * 4 <= kWarps * NS * stage,
                 "merge buffer must fit in the stages");
 };
@@ -134,6 +135,13 @@ __device__ __forceinline__ void split_h2(float a, float b, uint32_t& hi, uint32_
   hi = pack_h2(a, b);
   const float2 f = __half22float2(u32_as_h2(hi));
   lo = pack_h2(a - f.x, b - f.y);
+}
+
+// two adjacent fp16 values of shared memory (4-byte aligned) in one load
+__device__ __forceinline__ uint32_t ld_h2(const __half* p) { return *reinterpret_cast<const uint32_t*>(p); }
+// half i of such a pair (0: the lower address) as fp32
+__device__ __forceinline__ float h2f(uint32_t w, int i) {
+  return i ? __high2float(u32_as_h2(w)) : __low2float(u32_as_h2(w));
 }
 
 // q5_0 high bits of a K row word h = qh >> (4*tig), placed at bits 4 / 20 (with the 0x6400 magic).
@@ -579,23 +587,32 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
       const __half* vd = reinterpret_cast<const __half*>(st + C::off_vd);
       const float pz[4] = {vt0 ? pt[0] : 0.0f, vt1 ? pt[1] : 0.0f, vt8 ? pt[2] : 0.0f, vt9 ? pt[3] : 0.0f};
       constexpr int VHH = C::VH / 2;  // halves per block header
-      // P times the V scale (part 0) or the V minimum (part 1) of block blk, as fp16 hi + lo
-      auto pscaled = [&](int blk, int part, uint32_t& bh0, uint32_t& bl0, uint32_t& bh1, uint32_t& bl1) {
-        const int o = blk * VHH + part;
-        split_h2(pz[0] * __half2float(vd[(2 * tig) * NB * VHH + o]), pz[1] * __half2float(vd[(2 * tig + 1) * NB * VHH + o]),
-                 bh0, bl0);
-        split_h2(pz[2] * __half2float(vd[(2 * tig + 8) * NB * VHH + o]),
-                 pz[3] * __half2float(vd[(2 * tig + 9) * NB * VHH + o]), bh1, bl1);
+      // headers of the lane's four transposed tokens: d of blocks blk, blk+1 (one pair per token,
+      // loaded at even blk; NB is even) or, for q4_1 / q5_1, (d, minimum) of block blk
+      uint32_t vw[4] = {0u, 0u, 0u, 0u};
+      auto load_vh = [&](int blk) {
+        if (VHH == 2 || (blk & 1) == 0) {
+          const int b0 = VHH == 2 ? blk : blk & ~1;
+          vw[0] = ld_h2(vd + ((2 * tig) * NB + b0) * VHH);
+          vw[1] = ld_h2(vd + ((2 * tig + 1) * NB + b0) * VHH);
+          vw[2] = ld_h2(vd + ((2 * tig + 8) * NB + b0) * VHH);
+          vw[3] = ld_h2(vd + ((2 * tig + 9) * NB + b0) * VHH);
+        }
+      };
+      // P times the V scale of block blk, as fp16 hi + lo
+      auto pscaled = [&](int blk, uint32_t& bh0, uint32_t& bl0, uint32_t& bh1, uint32_t& bl1) {
+        const int i = VHH == 2 ? 0 : (blk & 1);
+        split_h2(pz[0] * h2f(vw[0], i), pz[1] * h2f(vw[1], i), bh0, bl0);
+        split_h2(pz[2] * h2f(vw[2], i), pz[3] * h2f(vw[3], i), bh1, bl1);
       };
       // the minimum adds sum_t P[t][h] * lo[t][blk] to every channel of the block: the
       // lane's share for head g is summed here in fp32 and spread over the channels at the end
       auto add_min = [&](int blk) {
         if constexpr (C::V1) {
-          const int o = blk * VHH + 1;
-          vmin[blk] = fmaf(pz[0], __half2float(vd[(2 * tig) * NB * VHH + o]), vmin[blk]);
-          vmin[blk] = fmaf(pz[1], __half2float(vd[(2 * tig + 1) * NB * VHH + o]), vmin[blk]);
-          vmin[blk] = fmaf(pz[2], __half2float(vd[(2 * tig + 8) * NB * VHH + o]), vmin[blk]);
-          vmin[blk] = fmaf(pz[3], __half2float(vd[(2 * tig + 9) * NB * VHH + o]), vmin[blk]);
+          vmin[blk] = fmaf(pz[0], h2f(vw[0], 1), vmin[blk]);
+          vmin[blk] = fmaf(pz[1], h2f(vw[1], 1), vmin[blk]);
+          vmin[blk] = fmaf(pz[2], h2f(vw[2], 1), vmin[blk]);
+          vmin[blk] = fmaf(pz[3], h2f(vw[3], 1), vmin[blk]);
         }
       };
       const uint32_t vbase = smem_u32(st + C::off_vqs);
@@ -604,7 +621,8 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
 #pragma unroll
         for (int blk = 0; blk < NB; ++blk) {
           uint32_t bh0, bl0, bh1, bl1;
-          pscaled(blk, 0, bh0, bl0, bh1, bl1);
+          load_vh(blk);
+          pscaled(blk, bh0, bl0, bh1, bl1);
           uint32_t r0, r1, r2, r3;
           ldsm_x4_t(vbase + swz_off<C::WV>(rr, 32 * blk + 16 * (mi >> 1), 16), r0, r1, r2, r3);
           r0 ^= 0x80808080u; r1 ^= 0x80808080u; r2 ^= 0x80808080u; r3 ^= 0x80808080u;
@@ -625,7 +643,8 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
           for (int e = 0; e < 2; ++e) {
             const int blk = bp + e;
             uint32_t bh0, bl0, bh1, bl1;
-            pscaled(blk, 0, bh0, bl0, bh1, bl1);
+            load_vh(blk);
+            pscaled(blk, bh0, bl0, bh1, bl1);
             add_min(blk);
             const uint32_t ra = rr4[2 * e], rb = rr4[2 * e + 1];  // tokens 0-7, 8-15
             uint32_t ma0 = 0x64006400u, ma1 = 0x64006400u, ma2 = 0x64006400u, ma3 = 0x64006400u;
@@ -656,8 +675,9 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
       if constexpr (OL) {  // outlier slots += codes_O^T . (P * d_O), as one more q8_0 block
         const __half* vod = reinterpret_cast<const __half*>(st + C::off_vod);
         uint32_t bh0, bl0, bh1, bl1;
-        split_h2(pz[0] * __half2float(vod[2 * tig]), pz[1] * __half2float(vod[2 * tig + 1]), bh0, bl0);
-        split_h2(pz[2] * __half2float(vod[2 * tig + 8]), pz[3] * __half2float(vod[2 * tig + 9]), bh1, bl1);
+        const uint32_t o01 = ld_h2(vod + 2 * tig), o89 = ld_h2(vod + 2 * tig + 8);
+        split_h2(pz[0] * h2f(o01, 0), pz[1] * h2f(o01, 1), bh0, bl0);
+        split_h2(pz[2] * h2f(o89, 0), pz[3] * h2f(o89, 1), bh1, bl1);
         uint32_t r0, r1, r2, r3;
         ldsm_x4_t(smem_u32(st + C::off_vo) + rr * 32 + 16 * (mi >> 1), r0, r1, r2, r3);
         r0 ^= 0x80808080u; r1 ^= 0x80808080u; r2 ^= 0x80808080u; r3 ^= 0x80808080u;
