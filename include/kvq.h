@@ -119,8 +119,9 @@ typedef int32_t kvq_status;
  * payload; kvq_dequant_debug can export them in GGUF array-of-structs order.
  *
  * Requirements (checked by every call): head_dim % 32 == 0 and
- * 32 <= head_dim <= 256; max_ctx % 64 == 0; tail_len >= 0; every non-NULL
- * plane 16-byte aligned; k_qh / v_qh non-NULL only for q5_0 (required then);
+ * 32 <= head_dim <= 256; max_ctx % 64 == 0 and max_ctx <= 2^30; tail_len >= 0;
+ * every non-NULL plane 16-byte aligned; k_qh / v_qh non-NULL only for q5_0 and
+ * q5_1 (required then);
  * k_tail / v_tail non-NULL iff tail_len > 0.  Decode supports head_dim in
  * {64, 128, 256} (plus 192 for q4_0/q4_0); prefill supports head_dim 64 and
  * 128 with up to 128 query heads per KV head; append and debug support every
@@ -131,7 +132,7 @@ typedef struct kvq_cache {
   int32_t batch;        /* sequences                                   */
   int32_t n_kv_heads;   /* KV heads per sequence                       */
   int32_t head_dim;     /* d                                           */
-  int32_t max_ctx;      /* token capacity per sequence (multiple of 64)*/
+  int32_t max_ctx;      /* token capacity per sequence (multiple of 64, at most 2^30) */
   int32_t tail_len;     /* T: recent tokens also kept in bf16 (0 = off)*/
   int32_t k_type;       /* KVQ_TYPE_*                                  */
   int32_t v_type;       /* KVQ_TYPE_*                                  */

@@ -23,7 +23,8 @@ bool shape_ok(const kvq_cache* c) {
   if (!c) return false;
   if (c->batch <= 0 || c->batch > 65535 || c->n_kv_heads <= 0 || c->n_kv_heads > 4096) return false;
   if (c->head_dim < 32 || c->head_dim > 256 || c->head_dim % 32) return false;
-  if (c->max_ctx <= 0 || c->max_ctx % 64) return false;
+  // positions, chunk ends and seq_len + n_new stay below 2^31 in the kernels' int arithmetic
+  if (c->max_ctx <= 0 || c->max_ctx % 64 || c->max_ctx > (1 << 30)) return false;
   if (c->tail_len < 0 || c->tail_len > (1 << 24)) return false;
   if (!valid_type(c->k_type) || !valid_type(c->v_type)) return false;
   if (c->flags & ~(KVQ_ROT_AUTO | KVQ_ROT_K_OFF | KVQ_ROT_V_OFF)) return false;

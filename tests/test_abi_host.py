@@ -129,7 +129,8 @@ def test_cache_check_rejections(built_lib_path):
     assert L.kvq_cache_check(ctypes.byref(c)) == 0
     c = _full_desc(); c.page_table = FAKE                        # a page table without pages
     assert L.kvq_cache_check(ctypes.byref(c)) == kvq.KVQ_ERR_INVALID_ARG
-    for bad in (dict(head_dim=48), dict(head_dim=512), dict(max_ctx=100), dict(batch=0), dict(tail_len=-1),
+    for bad in (dict(head_dim=48), dict(head_dim=512), dict(max_ctx=100), dict(max_ctx=(1 << 30) + 64),
+                dict(batch=0), dict(tail_len=-1),
                 dict(k_type=7), dict(v_type=5), dict(flags=8)):
         assert L.kvq_cache_check(ctypes.byref(_full_desc(**bad))) == kvq.KVQ_ERR_INVALID_ARG, bad
 
