@@ -187,8 +187,8 @@ KVQ_API const char* kvq_status_string(kvq_status s);
 
 /* Bytes the caller must allocate for plane `plane` (KVQ_PLANE_*) of a cache
  * with the given sizes and types; pointers in `c` are ignored.  Returns 0 for
- * an absent plane (qh of a non-q5_0 type, tail of tail_len 0) or an invalid
- * descriptor. */
+ * an absent plane (qh of a type other than q5_0 / q5_1, tail of tail_len 0,
+ * outlier planes of n_outlier 0) or an invalid descriptor. */
 KVQ_API size_t kvq_plane_bytes(const kvq_cache* c, int32_t plane);
 
 /* Host-side check of a descriptor (sizes, types, pointers, alignment). */
@@ -329,8 +329,9 @@ KVQ_API kvq_status kvq_prefill_attention(const kvq_cache* c, const void* q, int3
  *                  must lie below max_ctx; tail reads slot p % tail_len
  *   original_basis non-zero: rotate the values back when that side is rotated
  *   out            device float [count][head_dim] (NULL allowed)
- *   blocks_ggml    device bytes [count][head_dim/32][18|22|34] or NULL: the
- *                  body blocks in GGUF array-of-structs byte order (body only)
+ *   blocks_ggml    device bytes [count][head_dim/32][block bytes] or NULL: the
+ *                  body blocks in GGUF array-of-structs byte order (body only;
+ *                  18, 20, 22, 24, 34 bytes for q4_0, q4_1, q5_0, q5_1, q8_0)
  * No range check against seq_len: positions that were never written return
  * whatever the planes hold.
  */
