@@ -16,7 +16,6 @@ bool valid_type(int t) { return t >= KVQ_TYPE_Q4_0 && t <= KVQ_TYPE_Q5_1; }
 bool has_qh(int t) { return t == KVQ_TYPE_Q5_0 || t == KVQ_TYPE_Q5_1; }
 bool has_min(int t) { return t == KVQ_TYPE_Q4_1 || t == KVQ_TYPE_Q5_1; }
 bool valid_dtype(int t) { return t == KVQ_F32 || t == KVQ_BF16 || t == KVQ_F16; }
-size_t dtype_bytes(int t) { return t == KVQ_F32 ? 4 : 2; }
 
 // sizes and types only (no pointers)
 bool shape_ok(const kvq_cache* c) {
