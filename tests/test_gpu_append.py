@@ -8,7 +8,7 @@ import pytest
 
 from oracle import kvq_oracle as ko
 from conftest import golden_path
-from kvq_testlib import append_both, gpu_blocks, gpu_values, prerotate, require_gpu, to_dev
+from kvq_testlib import append_both, gpu_blocks, gpu_values, require_gpu, to_dev
 
 pytestmark = pytest.mark.gpu
 
