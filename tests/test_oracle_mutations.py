@@ -172,6 +172,79 @@ def _ovals_negated(d_bits, codes, chans, head_dim):
     return -_ORIG_OVALS(d_bits, codes, chans, head_dim)
 
 
+# -- the cache and the attention functions -----------------------------------
+_ORIG_STORED = ko.OracleCache.stored
+_ORIG_APPEND = ko.OracleCache.append
+_ORIG_DECODE = ko.decode_attention
+_ORIG_PREFILL = ko.prefill_attention
+
+
+def _stored_tail_one_short(self, which, b, h):
+    """Body / tail boundary one position late: position n - T read from the body."""
+    n = int(self.seq_len[b])
+    split = min(n, max(0, n - self.T + 1))
+    out = np.empty((n, self.d), dtype=np.float64)
+    out[:split] = self.body_values(which, b, h, 0, split)
+    if n > split:
+        out[split:] = self.tail_values(which, b, h, np.arange(split, n))
+    return out
+
+
+def _tail_slot_shifted(self, which, b, h, positions):
+    """Ring slot off by one: (pos + 1) % T."""
+    slots = (np.asarray(positions, dtype=np.int64) + 1) % self.T
+    return ko.bf16_value(self.tail[which][b, h, slots])
+
+
+def _append_not_write_through(self, k, v, n_new_per_seq=None, prerotated=False):
+    """Tokens that go to the tail are not quantized into the body."""
+    n_before = self.seq_len.copy()
+    _ORIG_APPEND(self, k, v, n_new_per_seq, prerotated)
+    if self.T == 0:
+        return
+    for b in range(self.B):
+        n0, n1 = int(n_before[b]), int(self.seq_len[b])
+        first = max(n0, n1 - self.T)
+        for w in ("k", "v"):
+            self.codes[w][b, :, first:n1] = 0
+            self.dbits[w][b, :, first:n1] = 0
+
+
+def _decode_heads_interleaved(cache, q, scale=None, pairs=None):
+    """Query head h reads KV head h % Hkv instead of h // (Hq / Hkv)."""
+    q = np.asarray(q, dtype=np.float64)
+    B, Hq, d = q.shape
+    perm = np.array([(h % cache.H) * (Hq // cache.H) + h // cache.H for h in range(Hq)])
+    out = _ORIG_DECODE(cache, q[:, perm], scale, pairs)
+    inv = np.empty_like(perm)
+    inv[perm] = np.arange(Hq)
+    return out[:, inv]
+
+
+def _decode_not_rotated_back(cache, q, scale=None, pairs=None):
+    """The output is left in the rotated basis."""
+    out = _ORIG_DECODE(cache, q, scale, pairs)
+    if cache.rot["v"]:
+        out = out @ ko.rotation_matrix(out.shape[-1])   # H is its own inverse: undoes the back-rotation
+    return out
+
+
+def _prefill_strictly_causal(cache, q, q_pos0=None, causal=True, scale=None, heads=None):
+    """A query does not see the key at its own position (t < p)."""
+    B, n_tok = np.asarray(q).shape[:2]
+    if not causal:
+        return _ORIG_PREFILL(cache, q, q_pos0, causal, scale, heads)
+    p0 = cache.seq_len - n_tok if q_pos0 is None else np.asarray(q_pos0)
+    return _ORIG_PREFILL(cache, q, p0 - 1, causal, scale, heads)
+
+
+def _prefill_positions_shifted(cache, q, q_pos0=None, causal=True, scale=None, heads=None):
+    """Default query positions one too far: n - n_tok + 1."""
+    n_tok = np.asarray(q).shape[1]
+    p0 = cache.seq_len - n_tok + 1 if q_pos0 is None else np.asarray(q_pos0)
+    return _ORIG_PREFILL(cache, q, p0, causal, scale, heads)
+
+
 MUTANTS = [
     ("fwht", _fwht_transposed_pairs, [pins.test_rotate_golden_vectors]),
     ("pack_q4_0", _pack_q4_swapped, [pins.test_packing_golden]),
@@ -193,6 +266,17 @@ MUTANTS = [
     ("split_outliers", _split_slots_reversed, [lambda: opins.test_exact_reconstruction_through_rotation(False)]),
     ("outlier_values", _ovals_shifted, [opins.test_outlier_only_vectors_are_q8_0_alone]),
     ("outlier_values", _ovals_negated, [lambda: opins.test_reconstruction_error_within_the_two_quantizations("q4_0")]),
+    ("decode_attention", _decode_heads_interleaved, [pins.test_decode_gqa_bruteforce]),
+    ("decode_attention", _decode_not_rotated_back, [pins.test_decode_gqa_bruteforce]),
+    ("prefill_attention", _prefill_strictly_causal, [pins.test_prefill_causal_bruteforce_and_decode_consistency]),
+    ("prefill_attention", _prefill_positions_shifted, [pins.test_prefill_causal_bruteforce_and_decode_consistency]),
+]
+
+# mutants of OracleCache methods: (method name, replacement, pins)
+CACHE_MUTANTS = [
+    ("stored", _stored_tail_one_short, [pins.test_tail_ring_wraparound_many_appends]),
+    ("tail_values", _tail_slot_shifted, [pins.test_tail_ring_wraparound_many_appends]),
+    ("append", _append_not_write_through, [pins.test_tail_ring_wraparound_many_appends]),
 ]
 
 
@@ -207,3 +291,16 @@ def test_pins_catch_planted_mistake(monkeypatch, i):
         except (AssertionError, ValueError):
             failed += 1
     assert failed >= 1, f"mutant of {name} ({fn.__name__}) passed every pin"
+
+
+@pytest.mark.parametrize("i", range(len(CACHE_MUTANTS)))
+def test_pins_catch_planted_cache_mistake(monkeypatch, i):
+    name, fn, checks = CACHE_MUTANTS[i]
+    monkeypatch.setattr(ko.OracleCache, name, fn)
+    failed = 0
+    for chk in checks:
+        try:
+            chk()
+        except (AssertionError, ValueError):
+            failed += 1
+    assert failed >= 1, f"mutant of OracleCache.{name} ({fn.__name__}) passed every pin"
