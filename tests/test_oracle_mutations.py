@@ -172,6 +172,31 @@ def _ovals_negated(d_bits, codes, chans, head_dim):
     return -_ORIG_OVALS(d_bits, codes, chans, head_dim)
 
 
+_ORIG_GGML = ko.to_ggml_bytes
+
+
+def _f16_truncating(x):
+    """float32 -> fp16 by truncating the mantissa instead of rounding to nearest even."""
+    x = np.asarray(x, dtype=F32)
+    t = x.astype(np.float16)
+    up = np.abs(t.astype(F32)) > np.abs(x)            # RNE rounded away from zero: step back one ulp
+    bits = t.view(np.uint16).copy()
+    bits[up & (x != 0)] -= 1
+    return bits
+
+
+def _q5_divisor_15(y):
+    """q5_0 scale m / -15 instead of m / -16."""
+    return ko._quantize_offset(y, -15.0, 16.5, 31)
+
+
+def _ggml_qs_before_d(qtype, d_bits, codes):
+    """Block fields in the wrong order: quants first, then the scale."""
+    img = _ORIG_GGML(qtype, d_bits, codes)
+    hd = 4 if qtype in ko.MIN_TYPES else 2
+    return np.concatenate([img[..., hd:], img[..., :hd]], axis=-1)
+
+
 # -- the cache and the attention functions -----------------------------------
 _ORIG_STORED = ko.OracleCache.stored
 _ORIG_APPEND = ko.OracleCache.append
@@ -266,6 +291,9 @@ MUTANTS = [
     ("split_outliers", _split_slots_reversed, [lambda: opins.test_exact_reconstruction_through_rotation(False)]),
     ("outlier_values", _ovals_shifted, [opins.test_outlier_only_vectors_are_q8_0_alone]),
     ("outlier_values", _ovals_negated, [lambda: opins.test_reconstruction_error_within_the_two_quantizations("q4_0")]),
+    ("f16_bits", _f16_truncating, [pins.test_golden_blocks]),
+    ("quantize_q5_0", _q5_divisor_15, [pins.test_golden_blocks]),
+    ("to_ggml_bytes", _ggml_qs_before_d, [pins.test_packing_golden]),
     ("decode_attention", _decode_heads_interleaved, [pins.test_decode_gqa_bruteforce]),
     ("decode_attention", _decode_not_rotated_back, [pins.test_decode_gqa_bruteforce]),
     ("prefill_attention", _prefill_strictly_causal, [pins.test_prefill_causal_bruteforce_and_decode_consistency]),
