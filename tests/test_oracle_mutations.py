@@ -197,6 +197,17 @@ def _ggml_qs_before_d(qtype, d_bits, codes):
     return np.concatenate([img[..., hd:], img[..., :hd]], axis=-1)
 
 
+def _enable_rule_32(head_dim):
+    """Rotation enabled from head_dim 32 in steps of 32."""
+    return head_dim >= 32 and head_dim % 32 == 0
+
+
+def _inverse_unguarded(d):
+    """1/d without the d == 0 case (an all-zero block then divides by zero)."""
+    with np.errstate(divide="ignore", invalid="ignore"):
+        return (F32(1.0) / np.asarray(d, dtype=F32)).astype(F32)
+
+
 # -- the cache and the attention functions -----------------------------------
 _ORIG_STORED = ko.OracleCache.stored
 _ORIG_APPEND = ko.OracleCache.append
@@ -292,6 +303,8 @@ MUTANTS = [
     ("outlier_values", _ovals_shifted, [opins.test_outlier_only_vectors_are_q8_0_alone]),
     ("outlier_values", _ovals_negated, [lambda: opins.test_reconstruction_error_within_the_two_quantizations("q4_0")]),
     ("f16_bits", _f16_truncating, [pins.test_golden_blocks]),
+    ("rotation_enabled", _enable_rule_32, [pins.test_enable_rule]),
+    ("_inverse", _inverse_unguarded, [lambda: pins.test_all_zero_block("q4_0", 0x8000, 8)]),
     ("quantize_q5_0", _q5_divisor_15, [pins.test_golden_blocks]),
     ("to_ggml_bytes", _ggml_qs_before_d, [pins.test_packing_golden]),
     ("decode_attention", _decode_heads_interleaved, [pins.test_decode_gqa_bruteforce]),
@@ -315,7 +328,8 @@ def test_pins_catch_planted_mistake(monkeypatch, i):
     failed = 0
     for chk in checks:
         try:
-            chk()
+            with np.errstate(all="ignore"):   # a planted mistake may divide by zero
+                chk()
         except (AssertionError, ValueError):
             failed += 1
     assert failed >= 1, f"mutant of {name} ({fn.__name__}) passed every pin"
@@ -328,7 +342,8 @@ def test_pins_catch_planted_cache_mistake(monkeypatch, i):
     failed = 0
     for chk in checks:
         try:
-            chk()
+            with np.errstate(all="ignore"):   # a planted mistake may divide by zero
+                chk()
         except (AssertionError, ValueError):
             failed += 1
     assert failed >= 1, f"mutant of OracleCache.{name} ({fn.__name__}) passed every pin"
