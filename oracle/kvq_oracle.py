@@ -47,9 +47,10 @@ Precision: rotation and attention in float64; quantizer arithmetic in IEEE
 float32 exactly as the block definition states (one rounding per operation,
 no fused multiply-add); fp16 and bf16 round-to-nearest-even.
 
-Parity pins (see tests/test_oracle_pins.py and tests/test_oracle_outliers.py):
+Parity pins (tests/test_oracle_pins.py and tests/test_oracle_outliers.py):
 every function below is pinned by closed forms, invariants, brute force or
-hand-worked golden values.  No
+hand-worked golden values; tests/test_oracle_mutations.py plants plausible
+mistakes in these functions and checks that a pin fails for each.  No
 function is "parity unpinned".
 """
 
