@@ -33,6 +33,7 @@ KVQ_INPUT_PREROTATED = 1
 (KVQ_PLANE_K_QS, KVQ_PLANE_K_QH, KVQ_PLANE_K_D, KVQ_PLANE_V_QS, KVQ_PLANE_V_QH, KVQ_PLANE_V_D,
  KVQ_PLANE_K_TAIL, KVQ_PLANE_V_TAIL, KVQ_PLANE_SEQ_LEN, KVQ_PLANE_STATUS, KVQ_PLANE_OUTLIER,
  KVQ_PLANE_OUTLIER_IDX) = range(12)
+KVQ_NUM_PLANES = 12
 KVQ_DEV_ERR_APPEND_RANGE, KVQ_DEV_ERR_PREFILL_RANGE, KVQ_DEV_ERR_TIMEOUT, KVQ_DEV_ERR_PAGE = 1, 2, 4, 8
 KVQ_DEV_ERR_OUTLIER = 16
 

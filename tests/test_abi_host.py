@@ -29,6 +29,31 @@ def test_library_exports_every_declared_symbol(built_lib_path):
     assert kvq.lib().kvq_version() == 1
 
 
+def _header_defines():
+    """Integer #defines of include/kvq.h (name -> value)."""
+    src = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    out = {}
+    for name, val in re.findall(r"^#define\s+(KVQ_[A-Z0-9_]+)\s+(-?\d+)u?\b", src, flags=re.M):
+        out[name] = int(val)
+    return out
+
+
+def test_binding_constants_match_header():
+    """Every integer constant of the header that the binding mirrors has the same value."""
+    defs = _header_defines()
+    assert len(defs) >= 30
+    mirrored = [n for n in defs if hasattr(kvq, n)]
+    assert len(mirrored) >= 30, sorted(set(defs) - set(mirrored))
+    for n in mirrored:
+        assert getattr(kvq, n) == defs[n], n
+    # the binding's kvq_cache has the header's fields in the header's order
+    src = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    body = re.search(r"typedef struct kvq_cache \{(.*?)\} kvq_cache;", src, flags=re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = re.findall(r"\b([a-z_][a-z0-9_]*)\s*[;,]", body)
+    assert fields == [f for f, _ in kvq.kvq_cache._fields_]
+
+
 def test_status_strings(built_lib_path):
     for s in (0, -1, -2, -3, -4, -5, -6):
         assert kvq.lib().kvq_status_string(s)
