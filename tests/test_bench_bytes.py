@@ -1,0 +1,36 @@
+"""The bench's algorithmic byte counts against the per-unit figures (no GPU).
+
+Per body token-head: (d/32) blocks of K and V (34 + 18 bytes for q8_0 / q4_0);
+per tail token-head: bf16 K and V (4 d bytes); per query head: bf16 q in and
+out (4 d bytes).  Per appended token-head: bf16 K and V in (4 d), packed blocks
+out, and bf16 tail rows out (4 d) for the last tail_len tokens of a call."""
+
+import bench
+from rotated_bit_kv_kvq_gb300 import workloads as wl
+
+
+def test_headline_decode_bytes():
+    w = wl.WORKLOADS[wl.HEADLINE]
+    assert (w.batch, w.n_kv_heads, w.n_q_heads, w.head_dim, w.tail_len) == (4, 4, 24, 256, 1024)
+    assert (w.k_type, w.v_type) == ("q8_0", "q4_0")
+    per_body = (256 // 32) * (34 + 18)            # 416 B per token-head
+    per_tail = 4 * 256
+    n = 65536
+    exp = 4 * 4 * ((n - 1024) * per_body + 1024 * per_tail) + 4 * 24 * 4 * 256
+    assert exp == 446_267_392
+    assert bench.decode_bytes(w, [n] * 4) == exp
+
+
+def test_decode_bytes_short_and_ragged():
+    w = wl.WORKLOADS[wl.HEADLINE]
+    # shorter than the tail: every token from the tail; empty sequences still read q / write out
+    assert bench.decode_bytes(w, [10, 0]) == 4 * 10 * 4 * 256 + 2 * 24 * 4 * 256
+    assert bench.decode_bytes(w, [1025]) == 4 * (416 + 1024 * 1024) + 24 * 4 * 256
+
+
+def test_append_bytes():
+    w = wl.WORKLOADS[wl.HEADLINE]
+    heads = 4 * 4
+    assert bench.append_bytes(w, 1) == heads * (4 * 256 + 416 + 4 * 256)
+    # a long append writes only its last tail_len tokens to the ring
+    assert bench.append_bytes(w, 5000) == heads * (5000 * (4 * 256 + 416) + 1024 * 4 * 256)
