@@ -34,3 +34,23 @@ def test_append_bytes():
     assert bench.append_bytes(w, 1) == heads * (4 * 256 + 416 + 4 * 256)
     # a long append writes only its last tail_len tokens to the ring
     assert bench.append_bytes(w, 5000) == heads * (5000 * (4 * 256 + 416) + 1024 * 4 * 256)
+
+
+def test_recorded_traffic_only_for_the_source_it_was_taken_on(tmp_path, monkeypatch):
+    """The ncu DRAM bytes in profiles/ count only while the kernel source hashes the same."""
+    import hashlib
+    import json
+    import os
+    src_dir = tmp_path / "rotated_bit_kv_kvq_gb300" / "csrc"
+    src_dir.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    src = src_dir / "k.cuh"
+    src.write_bytes(b"kernel v1")
+    rec = {"bytes_per_launch": 123, "source_sha256": hashlib.sha256(b"kernel v1").hexdigest()}
+    (tmp_path / "profiles" / "decode_b4_ctx64k_traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.recorded_traffic("k.cuh") == 123
+    src.write_bytes(b"kernel v2")
+    assert bench.recorded_traffic("k.cuh") is None
+    os.remove(tmp_path / "profiles" / "decode_b4_ctx64k_traffic.json")
+    assert bench.recorded_traffic("k.cuh") is None
