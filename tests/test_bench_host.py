@@ -1,4 +1,5 @@
-"""The bench's algorithmic byte counts against the per-unit figures (no GPU).
+"""Host logic of the bench (no GPU): algorithmic byte counts against the per-unit
+figures, the recorded-traffic hash check and the clock-sample parsing.
 
 Per body token-head: (d/32) blocks of K and V (34 + 18 bytes for q8_0 / q4_0);
 per tail token-head: bf16 K and V (4 d bytes); per query head: bf16 q in and
@@ -54,3 +55,32 @@ def test_recorded_traffic_only_for_the_source_it_was_taken_on(tmp_path, monkeypa
     assert bench.recorded_traffic("k.cuh") is None
     os.remove(tmp_path / "profiles" / "decode_b4_ctx64k_traffic.json")
     assert bench.recorded_traffic("k.cuh") is None
+
+
+def test_clock_sampler_parses_clocks_and_throttle_reasons(tmp_path):
+    """nvidia-smi CSV rows -> median SM clock, max clock and the active throttle reasons."""
+    class _Proc:
+        def terminate(self):
+            pass
+
+        def wait(self, timeout=None):
+            return 0
+
+    cs = bench.ClockSampler(0)
+    cs.path = str(tmp_path / "clocks.csv")
+    rows = [
+        "0, 2070, 2070, 900.1, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "0, 1980, 2070, 1350.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "0, 2070, 2070, 1000.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "garbage line",
+    ]
+    with open(cs.path, "w") as f:
+        f.write("\n".join(rows) + "\n")
+    cs.f = open(cs.path, "a")
+    cs.proc = _Proc()
+    r = cs.stop()
+    assert r["sm_mhz"] == 2070.0 and r["sm_max_mhz"] == 2070.0 and r["samples"] == 3
+    assert r["reasons"] == ["sw_power_cap"]
+    # without nvidia-smi the line says so instead of inventing clocks
+    none = bench.ClockSampler(0)
+    assert none.stop()["reasons"] == ["nvidia-smi unavailable"]
