@@ -183,7 +183,7 @@ kvq_status kvq_decode_attention(const kvq_cache* c, const void* q, int32_t q_dty
   if (!kvq::decode_supported(c->head_dim, c->k_type, c->v_type, c->n_outlier)) return KVQ_ERR_UNSUPPORTED;
   const kvq::DecodePlan plan = kvq::plan_decode(*c, n_q_heads, sm_count());
   if (!workspace || !aligned16(workspace) || ws_bytes < plan.ws_bytes) return KVQ_ERR_WORKSPACE;
-  if (plan.splits > 65535 || (long long)c->n_kv_heads * plan.head_groups > 0x7fffffff) return KVQ_ERR_UNSUPPORTED;
+  if (!kvq::decode_grid_ok(*c, plan)) return KVQ_ERR_UNSUPPORTED;
   const float sc = scale == 0.0f ? 1.0f / sqrtf(float(c->head_dim)) : scale;
   return from_cuda(kvq::launch_decode(*c, r, plan, q, q_dtype, n_q_heads, sc, out, out_dtype, workspace,
                                       static_cast<cudaStream_t>(stream)));
@@ -210,7 +210,7 @@ kvq_status kvq_append_decode(const kvq_cache* c, const void* k, const void* v, i
   if (!kvq::decode_supported(c->head_dim, c->k_type, c->v_type, c->n_outlier)) return KVQ_ERR_UNSUPPORTED;
   const kvq::DecodePlan plan = kvq::plan_decode(*c, n_q_heads, sm_count());
   if (!workspace || !aligned16(workspace) || ws_bytes < plan.ws_bytes) return KVQ_ERR_WORKSPACE;
-  if (plan.splits > 65535 || (long long)c->n_kv_heads * plan.head_groups > 0x7fffffff) return KVQ_ERR_UNSUPPORTED;
+  if (!kvq::decode_grid_ok(*c, plan)) return KVQ_ERR_UNSUPPORTED;
   const float sc = scale == 0.0f ? 1.0f / sqrtf(float(c->head_dim)) : scale;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (n_new > 0 && kvq::fused_step_ok(*c, plan, n_new)) {
@@ -238,7 +238,7 @@ kvq_status kvq_decode_attention_noalloc(const kvq_cache* c, const void* q, int32
   if (!kvq::decode_supported(c->head_dim, c->k_type, c->v_type, c->n_outlier)) return KVQ_ERR_UNSUPPORTED;
   const kvq::DecodePlan plan = kvq::plan_decode(*c, n_q_heads, sm_count());
   if (plan.ws_bytes > KVQ_NOALLOC_SCRATCH_BYTES) return KVQ_ERR_WORKSPACE;
-  if (plan.splits > 65535 || (long long)c->n_kv_heads * plan.head_groups > 0x7fffffff) return KVQ_ERR_UNSUPPORTED;
+  if (!kvq::decode_grid_ok(*c, plan)) return KVQ_ERR_UNSUPPORTED;
   void* ws = nullptr;
   size_t ws_bytes = 0;
   if (kvq::decode_noalloc_scratch(&ws, &ws_bytes) != cudaSuccess || ws_bytes < plan.ws_bytes) return KVQ_ERR_CUDA;

@@ -2,6 +2,7 @@
 // of the allocation-free entry point.  The kernels are in kvq_decode_impl.cuh
 // (compiled once per head_dim in kvq_decode_d*.cu).
 
+#include <algorithm>
 #include <mutex>
 
 #include "kvq_decode_impl.cuh"
@@ -68,50 +69,33 @@ DecodePlan plan_decode(const kvq_cache& c, int n_q_heads, int sm_count) {
   const int g = n_q_heads / c.n_kv_heads;
   pl.head_groups = (g + kMaxHeads - 1) / kMaxHeads;
   pl.heads_per_cta = (g + pl.head_groups - 1) / pl.head_groups;
-  const long long pairs = (long long)c.batch * c.n_kv_heads * pl.head_groups;
-  // tail: one CTA per (sequence, head group) for tails up to 4096 slots
-  pl.tail_chunk = c.tail_len > 0 ? (c.tail_len < kTailChunkMax ? (c.tail_len + 63) / 64 * 64 : kTailChunkMax) : 64;
-  pl.splits_tail = c.tail_len > 0 ? (c.tail_len + pl.tail_chunk - 1) / pl.tail_chunk : 0;
-  // body: size the chunks so that all CTAs of a full cache fit in one wave of
-  // kCtasPerSm CTAs per SM (shorter sequences leave their last splits empty)
+  pl.planes = c.n_kv_heads * pl.head_groups;
+  // one wave: as many pieces per plane as the SMs hold CTAs of this kernel
   const long long slots = (long long)ctas_per_sm(c.head_dim, c.n_outlier != 0) * (sm_count > 0 ? sm_count : 148);
-  long long per_pair = slots / pairs - pl.splits_tail;
-  if (per_pair < 1) per_pair = 1;
-  int chunk = int(((c.max_ctx + per_pair - 1) / per_pair + 63) / 64 * 64);
-  if (chunk < 512) chunk = 512;
-  pl.chunk = chunk;
-  pl.splits_body = (c.max_ctx + chunk - 1) / chunk;
-  pl.splits = pl.splits_body + pl.splits_tail;
-  pl.cls_len[0] = chunk; pl.cls_len[1] = chunk; pl.cls_len[2] = chunk;
-  pl.cls_cnt[0] = pl.splits_body; pl.cls_cnt[1] = 0; pl.cls_cnt[2] = 0;
-  // One wave of three CTAs per SM: the CTAs are dispatched split by split (the kernel reads
-  // its linear block index split-major), so the first sm_count take the first slot of every
-  // SM, the next sm_count the second, the rest the third.  An SM's warp scheduler favours its
-  // oldest warps: measured on the 64k workload, equal chunks end after 96, 105 and 113 us by
-  // slot.  Chunks sized 1/96 : 1/105 : 1/113 by slot let the three end together.
-  const int cps = ctas_per_sm(c.head_dim, c.n_outlier != 0);
-  const long long sms = sm_count > 0 ? sm_count : 148;
-  const long long ctas = (long long)pl.splits * pairs;
-  if (cps == 3 && ctas <= 3 * sms && ctas > 2 * sms && pl.splits_body >= 3) {
-    const double w[3] = {105.0 / 96.0, 1.0, 105.0 / 113.0};
-    int cnt[3] = {0, 0, 0};
-    for (int s = 0; s < pl.splits_body; ++s) {
-      const long long mid = (long long)(s + pl.splits_tail) * pairs + pairs / 2;
-      ++cnt[mid / sms >= 2 ? 2 : int(mid / sms)];
-    }
-    double tot = 0.0;
-    for (int k = 0; k < 3; ++k) tot += cnt[k] * w[k];
-    for (int k = 0; k < 3; ++k) {
-      pl.cls_cnt[k] = cnt[k];
-      pl.cls_len[k] = int(((long long)(c.max_ctx * w[k] / tot) + 64) / 64 * 64);
-    }
-  }
-  pl.ws_bytes = (size_t)c.batch * n_q_heads * pl.splits * (c.head_dim + 2 + c.n_outlier) * sizeof(float);
+  pl.pieces = int(std::max<long long>(1, slots / pl.planes));
+  pl.pieces_fused = std::max(1, pl.pieces - c.batch);
+  // a piece of the stream touches one more segment than it covers whole at each end:
+  // slot = piece + segment index (or batch + piece + sequence with a fused step)
+  pl.slots = std::max(pl.pieces, c.batch + pl.pieces_fused) + 2 * c.batch;
+  const int nb = c.head_dim / 32;
+  pl.cost_body = (long long)nb * (type_block_bytes(c.k_type) + type_block_bytes(c.v_type)) +
+                 (c.n_outlier ? 2 * 34 : 0);
+  pl.cost_tail = 4LL * c.head_dim;           // bf16 K and V
+  pl.cost_min = 128 * pl.cost_body;          // 8 tiles: 2 per warp
+  pl.hdr_bytes = ((size_t)(1 + 2 * c.batch) * sizeof(long long) + 255) / 256 * 256;
+  const size_t rows = (size_t)pl.planes * pl.slots * pl.heads_per_cta;
+  pl.ws_bytes = pl.hdr_bytes + rows * (c.head_dim + 2 + c.n_outlier) * sizeof(float);
   return pl;
 }
 
 bool fused_step_ok(const kvq_cache& c, const DecodePlan& plan, int n_new) {
-  return c.tail_len > 0 && n_new >= 0 && n_new <= c.tail_len && plan.head_groups == 1 && plan.splits_tail == 1;
+  return c.tail_len > 0 && n_new >= 0 && n_new <= c.tail_len && c.tail_len <= kTailChunkMax &&
+         plan.head_groups == 1;
+}
+
+bool decode_grid_ok(const kvq_cache& c, const DecodePlan& plan) {
+  return (long long)c.batch + plan.pieces_fused <= 65535 && plan.pieces <= 65535 &&
+         (long long)c.batch * c.n_kv_heads * plan.head_groups * kMaxHeads <= 0x7fffffffLL;
 }
 
 cudaError_t launch_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, const void* q, int q_dtype,

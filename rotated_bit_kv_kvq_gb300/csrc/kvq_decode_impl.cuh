@@ -109,16 +109,19 @@ struct Params {
   int q_dtype, n_q_heads, group, heads_per_cta, head_groups;
   int rot_k;
   float scale_log2;                 // softmax scale * log2(e)
-  int chunk, tail_chunk, splits_body, splits_tail, splits;
-  // body chunk classes in dispatch order (DecodePlan): class k holds the splits from cls_s0[k],
-  // cls_len[k] tokens each, the first starting at token cls_beg[k]
-  int cls_len[3], cls_s0[3], cls_beg[3];
+  // Cost partition (DecodePlan): per plane (KV head x head group) the work of all
+  // sequences -- each sequence's tail (unless the step is fused) and body, in
+  // sequence order -- is one stream cut into `pieces` pieces of equal cost (bytes
+  // read), at least cost_min each.  A fused step gives every tail a CTA of its own.
+  int batch, pieces, slots;         // stream pieces and partial slots per plane
+  long long cost_body, cost_tail, cost_min;
+  long long* ws_hdr;                // [0] piece cost, then per sequence: stream offset, tokens
   // fused step: new tokens written by the tail CTA (fused != 0)
   int fused, rot_v;
   FusedAppend fa;
   kvq_cache cache;
   RowMap rows;   // body row of (sequence, KV head, position): contiguous or paged
-  float* ws_acco;  // outlier channels: their partial acc [B][Hq][splits][32]
+  float* ws_acco;  // outlier channels: their partials [plane][slot][head][32]
 };
 
 // New tokens of sequence b in a fused step: the requested count if it fits, else 0.
@@ -130,6 +133,51 @@ __device__ __forceinline__ int fused_count(const FusedAppend& fa, int n0, int b,
 
 __device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
 
+// Tokens of sequence b when the split kernel reads it (after the fused step's
+// append); `flag` reports an append that does not fit.
+__device__ __forceinline__ int seq_tokens(const Params& p, int b, bool flag) {
+  const int n0 = p.seq_len[b];
+  if (!p.fused) return n0;
+  bool ok;
+  const int nn = fused_count(p.fa, n0, b, p.max_ctx, ok);
+  if (!ok && flag) atomicOr(p.status, KVQ_DEV_ERR_APPEND_RANGE);
+  return n0 + nn;
+}
+// cost of sequence b's part of the stream: its tail (not with a fused step) and body
+__device__ __forceinline__ long long stream_cost(int n, int T, int fused, long long cb, long long ct) {
+  return (fused ? 0LL : (long long)min(n, T) * ct) + (long long)max(0, n - T) * cb;
+}
+// first token of a segment (ntok tokens of cost c from stream offset P) at or past
+// stream offset x, rounded up to whole tiles; piece boundaries map to the same token
+// in both pieces, so the pieces of a segment tile it without gaps or overlaps
+__device__ __forceinline__ int seg_token(long long x, long long P, long long c, int ntok, int tile) {
+  if (x <= P) return 0;
+  const long long t = (x - P + c - 1) / c;
+  const long long ta = (t + tile - 1) / tile * tile;
+  return ta >= ntok ? ntok : int(ta);
+}
+// exclusive prefix sum over the CTA's threads (kThreads); *total = the sum of all
+__device__ __forceinline__ long long cta_excl_scan(long long v, long long* total, long long* s_warp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  long long before = 0, all = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    before += w < warp ? s_warp[w] : 0LL;
+    all += s_warp[w];
+  }
+  *total = all;
+  return before + x - v;
+}
+
+
 // a, b -> fp16 pairs hi = fp16(a, b) and lo = fp16(a - hi, b - hi): hi + lo keeps ~22 bits.
 __device__ __forceinline__ void split_h2(float a, float b, uint32_t& hi, uint32_t& lo) {
   hi = pack_h2(a, b);
@@ -139,9 +187,39 @@ __device__ __forceinline__ void split_h2(float a, float b, uint32_t& hi, uint32_
 
 // two adjacent fp16 values of shared memory (4-byte aligned) in one load
 __device__ __forceinline__ uint32_t ld_h2(const __half* p) { return *reinterpret_cast<const uint32_t*>(p); }
+
+// BYTES of shared memory as 32-bit words, in the widest loads the row alignment
+// allows (rows of BYTES bytes from a 16-byte aligned base)
+template <int BYTES>
+__device__ __forceinline__ void lds_words(const uint8_t* p, uint32_t (&w)[BYTES / 4]) {
+  if constexpr (BYTES % 16 == 0) {
+#pragma unroll
+    for (int i = 0; i < BYTES / 16; ++i) {
+      const uint4 v = reinterpret_cast<const uint4*>(p)[i];
+      w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+    }
+  } else if constexpr (BYTES % 8 == 0) {
+#pragma unroll
+    for (int i = 0; i < BYTES / 8; ++i) {
+      const uint2 v = reinterpret_cast<const uint2*>(p)[i];
+      w[2 * i] = v.x; w[2 * i + 1] = v.y;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < BYTES / 4; ++i) w[i] = reinterpret_cast<const uint32_t*>(p)[i];
+  }
+}
+
 // half i of such a pair (0: the lower address) as fp32
 __device__ __forceinline__ float h2f(uint32_t w, int i) {
   return i ? __high2float(u32_as_h2(w)) : __low2float(u32_as_h2(w));
+}
+
+// fp16 scale of block blk from a token's header words: scales only (KHH = 1, two
+// blocks per word) or (scale, minimum) pairs (KHH = 2, one block per word)
+template <int KHH>
+__device__ __forceinline__ float hdr_scale(const uint32_t* w, int blk) {
+  return KHH == 1 ? h2f(w[blk >> 1], blk & 1) : h2f(w[blk], 0);
 }
 
 // q5_0 high bits of a K row word h = qh >> (4*tig), placed at bits 4 / 20 (with the 0x6400 magic).
@@ -166,58 +244,128 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, tig = lane & 3;
-  // grid (KV head x head group, sequence, split): all CTAs of split 0 are dispatched first,
-  // then those of split 1, ... (a split's body chunk depends on it)
-  const int split = blockIdx.z;
-  const int yy = blockIdx.x;
-  const int b = blockIdx.y;
-  const int kvh = yy / p.head_groups;
-  const int hg = yy % p.head_groups;
+  // grid (plane = KV head x head group, piece): piece y of every plane is dispatched
+  // before piece y + 1
+  const int plane = blockIdx.x;
+  const int kvh = plane / p.head_groups;
+  const int hg = plane % p.head_groups;
   const int head0 = kvh * p.group + hg * p.heads_per_cta;
   const int nheads = min(p.heads_per_cta, p.group - hg * p.heads_per_cta);
-
-  const int n0 = p.seq_len[b];
-  int nn = 0;  // tokens this launch appends to sequence b (fused step)
-  if (p.fused) {
-    bool ok;
-    nn = fused_count(p.fa, n0, b, p.max_ctx, ok);
-    if (!ok && tid == 0 && split == 0 && yy == 0) atomicOr(p.status, KVQ_DEV_ERR_APPEND_RANGE);
-  }
-  const int n = n0 + nn;
   const int T = p.tail_len;
-  const int nbody = max(0, n - T);
-  const int ntail = min(n, T);
-  const bool is_tail = split < p.splits_tail;
-  int t_begin, t_end;
-  if (is_tail) {
-    t_begin = split * p.tail_chunk;
-    t_end = min(ntail, t_begin + p.tail_chunk);
-  } else {
-    const int s = split - p.splits_tail;
-    const int k = int(s >= p.cls_s0[1]) + int(s >= p.cls_s0[2]);  // chunk class of this split
-    t_begin = p.cls_beg[k] + (s - p.cls_s0[k]) * p.cls_len[k];
-    t_end = min(nbody, t_begin + p.cls_len[k]);
-  }
-  float* ml = p.ws_ml + (((size_t)b * p.n_q_heads + head0) * p.splits + split) * 2;
-  if (t_begin >= t_end) {  // nothing to read: an empty partial
-    if (tid < nheads) {
-      ml[(size_t)tid * p.splits * 2] = -INFINITY;
-      ml[(size_t)tid * p.splits * 2 + 1] = 0.0f;
-    }
-    return;
-  }
+  const int B = p.batch;
+  const bool cta0 = blockIdx.x == 0 && blockIdx.y == 0;
+  const bool own_tail = p.fused && int(blockIdx.y) < B;  // fused step: the tail of sequence y
+  const long long piece = own_tail ? -1LL : (long long)blockIdx.y - (p.fused ? B : 0);
 
   float* sq = reinterpret_cast<float*>(smem + C::off_q);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::off_bar);
   float* sm_m = reinterpret_cast<float*>(smem + C::off_ml);
   float* sm_l = sm_m + kWarps * kMaxHeads;
+  __shared__ long long s_scan[kWarps];
+  __shared__ long long s_part[3];  // piece cost; stream offset and index of the piece's first sequence
 
   if (tid == 0) {
     for (int i = 0; i < kWarps * NS; ++i) mbar_init(&bars[i], 1);
     fence_barrier_init();
-    if (is_tail) { prefetch_tmap(&tmKt); prefetch_tmap(&tmVt); }
-    else { prefetch_tmap(&tmK); prefetch_tmap(&tmV); }
+    prefetch_tmap(&tmK); prefetch_tmap(&tmV);
+    if (T > 0) { prefetch_tmap(&tmKt); prefetch_tmap(&tmVt); }
   }
+
+  // ---- the partition: every CTA computes the same cut from seq_len ----------
+  // (CTA 0 also records it for the merge kernel, and flags appends that do not fit)
+  {
+    const int per = (B + kThreads - 1) / kThreads;
+    const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
+    long long mine = 0;
+    for (int bb = b0; bb < b1; ++bb)
+      mine += stream_cost(seq_tokens(p, bb, cta0), T, p.fused, p.cost_body, p.cost_tail);
+    long long total;
+    long long P = cta_excl_scan(mine, &total, s_scan);
+    const long long ch = max((total + p.pieces - 1) / p.pieces, p.cost_min);
+    if (tid == 0) { s_part[0] = ch; s_part[1] = 0; s_part[2] = -1; }
+    __syncthreads();
+    const long long x0 = piece * ch;
+    for (int bb = b0; bb < b1; ++bb) {
+      const int n = seq_tokens(p, bb, false);
+      const long long c = stream_cost(n, T, p.fused, p.cost_body, p.cost_tail);
+      if (piece >= 0 && c > 0 && P <= x0 && x0 < P + c) { s_part[1] = P; s_part[2] = bb; }
+      if (cta0) { p.ws_hdr[1 + 2 * bb] = P; p.ws_hdr[2 + 2 * bb] = n; }
+      P += c;
+    }
+    if (cta0 && tid == 0) p.ws_hdr[0] = ch;
+  }
+  __syncthreads();
+
+  // ---- the piece's sub-ranges, one (sequence, tail or body) segment each ------
+  // The cursor (stream offset, sequence, segment kind, staged queries' sequence) lives
+  // in shared memory between sub-ranges; every thread advances a copy identically.
+  __shared__ long long s_cur_P;
+  __shared__ int s_cur[5];  // sequence, next segment kind (0 tail, 1 body), staged sequence, slot, last
+  if (tid == 0) {
+    s_cur_P = s_part[1];
+    s_cur[0] = own_tail ? int(blockIdx.y) : int(s_part[2]);
+    s_cur[1] = (p.fused && !own_tail) ? 1 : 0;
+    s_cur[2] = -1;
+  }
+  __syncthreads();
+  uint32_t kk = 0;  // tiles this warp consumed (ring phases)
+  bool timed_out = false;
+  for (;;) {
+    // find the next non-empty sub-range of this piece (empty ones get an empty partial)
+    int b = 0, n0 = 0, nn = 0, t_begin = 0, t_end = 0, slot = 0, cur_b;
+    bool is_tail = false, last = true, found = false;
+    {
+      const long long x0 = piece * s_part[0], x1 = x0 + s_part[0];
+      long long Pseg = s_cur_P;
+      int sb = s_cur[0], kind = s_cur[1];
+      cur_b = s_cur[2];
+      while (sb >= 0 && sb < B) {
+        b = sb;
+        n0 = p.seq_len[b];
+        nn = 0;  // tokens this launch appends to sequence b (fused step)
+        if (p.fused) {
+          bool ok;
+          nn = fused_count(p.fa, n0, b, p.max_ctx, ok);
+        }
+        const int n = n0 + nn;
+        is_tail = kind == 0;
+        bool use = false;
+        if (own_tail) {
+          t_begin = 0;
+          t_end = min(n, T);
+          slot = b;
+          use = true;
+          sb = B;  // nothing after it
+        } else {
+          const int ntok = is_tail ? min(n, T) : max(0, n - T);
+          const long long c = is_tail ? p.cost_tail : p.cost_body;
+          const long long cs = (long long)ntok * c;
+          if (cs > 0 && Pseg + cs > x0) {  // (Pseg < x1 holds while the loop runs)
+            use = true;
+            const int tile = is_tail ? C::TT : 16;
+            t_begin = seg_token(x0, Pseg, c, ntok, tile);
+            t_end = seg_token(x1, Pseg, c, ntok, tile);
+            slot = p.fused ? B + int(piece) + b : int(piece) + 2 * b + kind;
+          }
+          Pseg += cs;
+          if (p.fused || kind == 1) { kind = p.fused ? 1 : 0; ++sb; } else { kind = 1; }
+          if (Pseg >= x1) sb = B;
+        }
+        last = sb >= B;
+        if (use && t_begin < t_end) { found = true; break; }
+        if (use && tid < nheads) {  // nothing to read: an empty partial
+          float* ml = p.ws_ml + ((size_t)plane * p.slots + slot) * p.heads_per_cta * 2;
+          ml[2 * tid] = -INFINITY;
+          ml[2 * tid + 1] = 0.0f;
+        }
+      }
+      __syncthreads();  // every thread has read the cursor
+      if (tid == 0) {
+        s_cur_P = Pseg; s_cur[0] = sb; s_cur[1] = kind; s_cur[2] = found ? b : cur_b;
+        s_cur[3] = slot; s_cur[4] = last;
+      }
+    }
+    if (!found) break;
 
   // ---- this warp's tiles, and the producer (lane 0) --------------------
   const int TR = is_tail ? C::TT : 16;                       // rows per tile
@@ -229,8 +377,8 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
   const bool paged = p.rows.page_tokens != 0;
   uint32_t bad_stage = 0;  // lane 0: bit s set when the tile in stage s came from a page outside the pool
 
-  auto issue = [&](int k) {  // tile k of this warp -> stage k % NS (lane 0 only)
-    const int s = k % NS;
+  auto issue = [&](int k) {  // tile k of this warp's sub-range -> stage (kk + k) % NS (lane 0 only)
+    const int s = (kk + k) % NS;
     uint8_t* st = wstage + s * C::stage;
     const int t0 = t_begin + (warp + k * kWarps) * TR;
     if (is_tail) {
@@ -293,6 +441,16 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
   }
 
   // ---- queries: load, rotate, scale, split into fp16 hi/lo fragments ----
+  // (once per sequence the piece touches)
+  float* qo = reinterpret_cast<float*>(smem + C::off_qo);  // OL: [8][32] unrotated, scaled
+  // B fragments: k-step (blk, half) covers channels 32*blk + 16*half + 4*tig + {0,2 | 1,3}.
+  // They are the same in every warp: warp 0 builds them once and leaves them in
+  // shared memory over the q staging ([blk][half][lane] x {hi b0b1, hi b2b3, lo b0b1,
+  // lo b2b3}, 32*D bytes = the staging's size), so no warp holds them in registers.
+  const uint4* qfs = reinterpret_cast<const uint4*>(sq);
+  float* qsum = reinterpret_cast<float*>(smem + C::off_qsum);  // [blk][head]: sum of the block's q values
+  if (b != cur_b) {
+
   for (int i = tid; i < kMaxHeads * D; i += kThreads) {
     const int hh = i / D, c = i % D;
     float v = 0.0f;
@@ -305,7 +463,6 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     sq[i] = v;
   }
   __syncthreads();
-  float* qo = reinterpret_cast<float*>(smem + C::off_qo);  // OL: [8][32] unrotated, scaled
   if constexpr (OL) {
     if (warp == 0) {
       const int ch = outlier_channel<D>(p.cache, kvh, lane);
@@ -330,12 +487,6 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     }
   }
   __syncthreads();
-  // B fragments: k-step (blk, half) covers channels 32*blk + 16*half + 4*tig + {0,2 | 1,3}.
-  // They are the same in every warp: warp 0 builds them once and leaves them in
-  // shared memory over the q staging ([blk][half][lane] x {hi b0b1, hi b2b3, lo b0b1,
-  // lo b2b3}, 32*D bytes = the staging's size), so no warp holds them in registers.
-  const uint4* qfs = reinterpret_cast<const uint4*>(sq);
-  float* qsum = reinterpret_cast<float*>(smem + C::off_qsum);  // [blk][head]: sum of the block's q values
   if (warp == 0) {
     if constexpr (C::K1) {
       for (int i = lane; i < NB * kMaxHeads; i += 32) {
@@ -383,6 +534,7 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     }
   }
   __syncthreads();
+  }  // queries of sequence b staged
   const uint4* qofs = reinterpret_cast<const uint4*>(smem + C::off_qof);
 
   // ---- main loop ------------------------------------------------------------
@@ -404,12 +556,16 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
 #pragma unroll
   for (int i = 0; i < (C::V1 ? NB : 1); ++i) vmin[i] = 0.0f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
-  bool timed_out = false;
   int k_stop = my_tiles;
+  // per-lane ldmatrix row and swizzle constants of the body tiles
+  const int mi = lane >> 3, rr = (lane & 7) + 8 * (mi & 1);
+  uint32_t lbK[C::WK / 32], lbV[C::WV / 32];
+  swz_lane<C::WK>(rr, mi >> 1, lbK);
+  swz_lane<C::WV>(rr, mi >> 1, lbV);
 
   for (int k = 0; k < my_tiles; ++k) {
-    const int s = k % NS;
-    const bool arrived = mbar_wait_bounded(&wbar[s], (k / NS) & 1, kWaitCycles);
+    const int s = (kk + k) % NS;
+    const bool arrived = mbar_wait_bounded(&wbar[s], ((kk + k) / NS) & 1, kWaitCycles);
     if (!__all_sync(0xffffffffu, arrived)) { timed_out = true; k_stop = k; break; }
     const uint8_t* st = wstage + s * C::stage;
     const int t0 = t_begin + (warp + k * kWarps) * TR;
@@ -421,14 +577,17 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     float S[4] = {0.f, 0.f, 0.f, 0.f};
     if (!is_tail) {
       // ------------------------------- body: scores
-      const __half* kd = reinterpret_cast<const __half*>(st + C::off_kd);
+      // block headers of this lane's tokens g and g+8, all blocks
+      constexpr int KHH = C::KH / 2;
+      uint32_t kw0[NB * KHH / 2], kw8[NB * KHH / 2];
+      lds_words<NB * C::KH>(st + C::off_kd + g * NB * C::KH, kw0);
+      lds_words<NB * C::KH>(st + C::off_kd + (g + 8) * NB * C::KH, kw8);
       const uint32_t kbase = smem_u32(st + C::off_kqs);
-      const int mi = lane >> 3, rr = (lane & 7) + 8 * (mi & 1);
       if constexpr (KT == KVQ_TYPE_Q8_0) {
 #pragma unroll
         for (int blk = 0; blk < NB; ++blk) {
           uint32_t r0, r1, r2, r3;
-          ldsm_x4(kbase + swz_off<C::WK>(rr, 32 * blk + 16 * (mi >> 1), 16), r0, r1, r2, r3);
+          ldsm_x4(kbase + lbK[swz_lane_idx<C::WK>(2 * blk)] + swz_box_off<C::WK>(2 * blk), r0, r1, r2, r3);
           r0 ^= 0x80808080u; r1 ^= 0x80808080u; r2 ^= 0x80808080u; r3 ^= 0x80808080u;
           const uint32_t alo[4] = {i8_pair<0, 2>(r0), i8_pair<0, 2>(r1), i8_pair<1, 3>(r0), i8_pair<1, 3>(r1)};
           const uint32_t ahi[4] = {i8_pair<0, 2>(r2), i8_pair<0, 2>(r3), i8_pair<1, 3>(r2), i8_pair<1, 3>(r3)};
@@ -438,18 +597,16 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
           mma16816(cc, alo, qa.z, qa.w);
           mma16816(cc, ahi, qb.x, qb.y);
           mma16816(cc, ahi, qb.z, qb.w);
-          const float dk0 = __half2float(kd[g * NB + blk]), dk8 = __half2float(kd[(g + 8) * NB + blk]);
+          const float dk0 = hdr_scale<KHH>(kw0, blk), dk8 = hdr_scale<KHH>(kw8, blk);
           S[0] += dk0 * cc[0]; S[1] += dk0 * cc[1];
           S[2] += dk8 * cc[2]; S[3] += dk8 * cc[3];
         }
       } else {
-        // header of token t, block blk: d (and, for q4_1 / q5_1, the minimum right after it)
-        constexpr int KHH = C::KH / 2;
         constexpr uint32_t OFF = (0x6400u + uint32_t(type_code_offset(KT))) * 0x10001u;
 #pragma unroll
         for (int bp = 0; bp < NB; bp += 2) {
           uint32_t rr4[4];
-          ldsm_x4(kbase + swz_off<C::WK>(rr, 16 * (bp + (mi >> 1)), 16), rr4[0], rr4[1], rr4[2], rr4[3]);
+          ldsm_x4(kbase + lbK[swz_lane_idx<C::WK>(bp)] + swz_box_off<C::WK>(bp), rr4[0], rr4[1], rr4[2], rr4[3]);
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int blk = bp + e;
@@ -472,13 +629,11 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
             mma16816(cc, alo, qa.z, qa.w);
             mma16816(cc, ahi, qb.x, qb.y);
             mma16816(cc, ahi, qb.z, qb.w);
-            const float dk0 = __half2float(kd[(g * NB + blk) * KHH]);
-            const float dk8 = __half2float(kd[((g + 8) * NB + blk) * KHH]);
+            const float dk0 = hdr_scale<KHH>(kw0, blk), dk8 = hdr_scale<KHH>(kw8, blk);
             S[0] += dk0 * cc[0]; S[1] += dk0 * cc[1];
             S[2] += dk8 * cc[2]; S[3] += dk8 * cc[3];
             if constexpr (C::K1) {  // + lo * (sum of the block's q), per token and head
-              const float mk0 = __half2float(kd[(g * NB + blk) * KHH + 1]);
-              const float mk8 = __half2float(kd[((g + 8) * NB + blk) * KHH + 1]);
+              const float mk0 = h2f(kw0[blk], 1), mk8 = h2f(kw8[blk], 1);
               const float2 qs2 = *reinterpret_cast<const float2*>(qsum + blk * kMaxHeads + 2 * tig);
               S[0] += mk0 * qs2.x; S[1] += mk0 * qs2.y;
               S[2] += mk8 * qs2.x; S[3] += mk8 * qs2.y;
@@ -528,16 +683,25 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     }
 
     // ---- online softmax (base 2); rows g, g+8 = tokens, cols 2tig, 2tig+1 = heads
-    if (!v0) { S[0] = -INFINITY; S[1] = -INFINITY; }
-    if (!v8) { S[2] = -INFINITY; S[3] = -INFINITY; }
-    float mx0 = fmaxf(S[0], S[2]), mx1 = fmaxf(S[1], S[3]);
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    // Rows past the end exist only in a warp's last tile (and in tiles of a page
+    // outside the pool): a warp-uniform branch.  8-row tail tiles leave the mma's
+    // rows g+8 empty in every tile.
+    const bool partial = t0 + TR > t_lim;
+    if (partial || TR < 16) {
+      if (!v0) { S[0] = -INFINITY; S[1] = -INFINITY; }
+      if (!v8) { S[2] = -INFINITY; S[3] = -INFINITY; }
     }
-    const float nm0 = fmaxf(m0, mx0), nm1 = fmaxf(m1, mx1);
-    if (__any_sync(0xffffffffu, nm0 > m0 || nm1 > m1)) {
+    float mx0 = fmaxf(S[0], S[2]), mx1 = fmaxf(S[1], S[3]);
+    // The running maximum changes only when some score of the tile exceeds it; for
+    // long contexts that is rare, and the reduction over the tile's rows and the
+    // rescale run only then.
+    if (__any_sync(0xffffffffu, mx0 > m0 || mx1 > m1)) {
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+      }
+      const float nm0 = fmaxf(m0, mx0), nm1 = fmaxf(m1, mx1);
       const float a0 = m0 == -INFINITY ? 0.0f : fast_exp2(m0 - nm0);
       const float a1 = m1 == -INFINITY ? 0.0f : fast_exp2(m1 - nm1);
       l0 *= a0; l1 *= a1;
@@ -566,65 +730,72 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     const float p2 = fast_exp2(S[2] - ms0), p3 = fast_exp2(S[3] - ms1);
     l0 += p0 + p2; l1 += p1 + p3;
 
-    // ---- P.V.  P is transposed once per tile (movmatrix on fp16 hi + lo parts)
-    // into the B-fragment layout: tokens 2tig, 2tig+1, 2tig+8, 2tig+9 of head g.
-    // Each block then scales it by its V scale (fp32) and splits it again into
-    // fp16 hi + lo, so the products keep ~22 bits; the codes are exact.
-    float pt[4];
+    // ---- P.V.  P is split into fp16 hi + lo parts and transposed once per tile
+    // (movmatrix) into the B-fragment layout: tokens 2tig, 2tig+1 (ph0, pl0) and
+    // 2tig+8, 2tig+9 (ph1, pl1) of head g.  Each block scales both parts by the
+    // tokens' V scales in fp16 arithmetic (hscale_split: ~22 bits, like P itself);
+    // the codes are exact.
+    uint32_t ph0, pl0, ph1, pl1;
     {
       const uint32_t h0 = pack_h2(p0, p1), h1 = pack_h2(p2, p3);
       const float2 f0 = __half22float2(u32_as_h2(h0)), f1 = __half22float2(u32_as_h2(h1));
       const uint32_t r0 = pack_h2(p0 - f0.x, p1 - f0.y), r1 = pack_h2(p2 - f1.x, p3 - f1.y);
-      const float2 th0 = __half22float2(u32_as_h2(movm_t(h0))), tr0 = __half22float2(u32_as_h2(movm_t(r0)));
-      const float2 th1 = __half22float2(u32_as_h2(movm_t(h1))), tr1 = __half22float2(u32_as_h2(movm_t(r1)));
-      pt[0] = th0.x + tr0.x; pt[1] = th0.y + tr0.y; pt[2] = th1.x + tr1.x; pt[3] = th1.y + tr1.y;
+      ph0 = movm_t(h0); pl0 = movm_t(r0); ph1 = movm_t(h1); pl1 = movm_t(r1);
     }
     const int tt = t0 + 2 * tig;  // first token of this lane's transposed rows
     const bool vt0 = tt < t_lim, vt1 = tt + 1 < t_lim;
     const bool vt8 = TR == 16 && tt + 8 < t_lim, vt9 = TR == 16 && tt + 9 < t_lim;
     if (!is_tail) {
-      // V scales of the transposed tokens, read per block (0 for rows past the end)
-      const __half* vd = reinterpret_cast<const __half*>(st + C::off_vd);
-      const float pz[4] = {vt0 ? pt[0] : 0.0f, vt1 ? pt[1] : 0.0f, vt8 ? pt[2] : 0.0f, vt9 ? pt[3] : 0.0f};
-      constexpr int VHH = C::VH / 2;  // halves per block header
-      // headers of the lane's four transposed tokens: d of blocks blk, blk+1 (one pair per token,
-      // loaded at even blk; NB is even) or, for q4_1 / q5_1, (d, minimum) of block blk
-      uint32_t vw[4] = {0u, 0u, 0u, 0u};
-      auto load_vh = [&](int blk) {
-        if (VHH == 2 || (blk & 1) == 0) {
-          const int b0 = VHH == 2 ? blk : blk & ~1;
-          vw[0] = ld_h2(vd + ((2 * tig) * NB + b0) * VHH);
-          vw[1] = ld_h2(vd + ((2 * tig + 1) * NB + b0) * VHH);
-          vw[2] = ld_h2(vd + ((2 * tig + 8) * NB + b0) * VHH);
-          vw[3] = ld_h2(vd + ((2 * tig + 9) * NB + b0) * VHH);
+      // V block headers of the lane's four transposed tokens, all blocks; zero for rows
+      // past the end (their bytes may be anything, and 0 * Inf would poison the sum)
+      constexpr int VHH = C::VH / 2;              // halves per block header
+      constexpr int VW = NB * VHH / 2;            // header words per token
+      uint32_t vh[4][VW];
+      {
+        const uint8_t* vd = st + C::off_vd;
+        const int trow[4] = {2 * tig, 2 * tig + 1, 2 * tig + 8, 2 * tig + 9};
+        const bool tok_ok[4] = {vt0, vt1, vt8, vt9};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) lds_words<NB * C::VH>(vd + trow[i] * NB * C::VH, vh[i]);
+        if (partial) {  // full tiles hold written body rows only
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < VW; ++j) vh[i][j] = tok_ok[i] ? vh[i][j] : 0u;
         }
+      }
+      // scale pair of block blk for tokens (ta, tb) of the four
+      auto dvpair = [&](int blk, int ta, int tb) -> uint32_t {
+        if constexpr (VHH == 1) return __byte_perm(vh[ta][blk >> 1], vh[tb][blk >> 1], (blk & 1) ? 0x7632 : 0x5410);
+        else return __byte_perm(vh[ta][blk], vh[tb][blk], 0x5410);
       };
-      // P times the V scale of block blk, as fp16 hi + lo
+      // P times the V scale of block blk, as fp16 hi + lo B fragments
       auto pscaled = [&](int blk, uint32_t& bh0, uint32_t& bl0, uint32_t& bh1, uint32_t& bl1) {
-        const int i = VHH == 2 ? 0 : (blk & 1);
-        split_h2(pz[0] * h2f(vw[0], i), pz[1] * h2f(vw[1], i), bh0, bl0);
-        split_h2(pz[2] * h2f(vw[2], i), pz[3] * h2f(vw[3], i), bh1, bl1);
+        hscale_split(ph0, pl0, dvpair(blk, 0, 1), bh0, bl0);
+        hscale_split(ph1, pl1, dvpair(blk, 2, 3), bh1, bl1);
       };
       // the minimum adds sum_t P[t][h] * lo[t][blk] to every channel of the block: the
       // lane's share for head g is summed here in fp32 and spread over the channels at the end
+      float pz[4] = {0.f, 0.f, 0.f, 0.f};
+      if constexpr (C::V1) {
+        const float2 a0 = __half22float2(u32_as_h2(ph0)), b0 = __half22float2(u32_as_h2(pl0));
+        const float2 a1 = __half22float2(u32_as_h2(ph1)), b1 = __half22float2(u32_as_h2(pl1));
+        pz[0] = a0.x + b0.x; pz[1] = a0.y + b0.y; pz[2] = a1.x + b1.x; pz[3] = a1.y + b1.y;
+      }
       auto add_min = [&](int blk) {
         if constexpr (C::V1) {
-          vmin[blk] = fmaf(pz[0], h2f(vw[0], 1), vmin[blk]);
-          vmin[blk] = fmaf(pz[1], h2f(vw[1], 1), vmin[blk]);
-          vmin[blk] = fmaf(pz[2], h2f(vw[2], 1), vmin[blk]);
-          vmin[blk] = fmaf(pz[3], h2f(vw[3], 1), vmin[blk]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) vmin[blk] = fmaf(pz[i], h2f(vh[i][blk], 1), vmin[blk]);
         }
       };
       const uint32_t vbase = smem_u32(st + C::off_vqs);
-      const int mi = lane >> 3, rr = (lane & 7) + 8 * (mi & 1);
       if constexpr (VT == KVQ_TYPE_Q8_0) {
 #pragma unroll
         for (int blk = 0; blk < NB; ++blk) {
           uint32_t bh0, bl0, bh1, bl1;
-          load_vh(blk);
           pscaled(blk, bh0, bl0, bh1, bl1);
           uint32_t r0, r1, r2, r3;
-          ldsm_x4_t(vbase + swz_off<C::WV>(rr, 32 * blk + 16 * (mi >> 1), 16), r0, r1, r2, r3);
+          ldsm_x4_t(vbase + lbV[swz_lane_idx<C::WV>(2 * blk)] + swz_box_off<C::WV>(2 * blk), r0, r1, r2, r3);
           r0 ^= 0x80808080u; r1 ^= 0x80808080u; r2 ^= 0x80808080u; r3 ^= 0x80808080u;
           const uint32_t a0[4] = {i8_pair<0, 2>(r0), i8_pair<1, 3>(r0), i8_pair<0, 2>(r1), i8_pair<1, 3>(r1)};
           const uint32_t a1[4] = {i8_pair<0, 2>(r2), i8_pair<1, 3>(r2), i8_pair<0, 2>(r3), i8_pair<1, 3>(r3)};
@@ -635,18 +806,20 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
         }
       } else {
         constexpr uint32_t OFF = (0x6400u + uint32_t(type_code_offset(VT))) * 0x10001u;
+        constexpr uint32_t OFF16 = neg_off_x16_bits(type_code_offset(VT));
 #pragma unroll
         for (int bp = 0; bp < NB; bp += 2) {
           uint32_t rr4[4];
-          ldsm_x4_t(vbase + swz_off<C::WV>(rr, 16 * (bp + (mi >> 1)), 16), rr4[0], rr4[1], rr4[2], rr4[3]);
+          ldsm_x4_t(vbase + lbV[swz_lane_idx<C::WV>(bp)] + swz_box_off<C::WV>(bp), rr4[0], rr4[1], rr4[2], rr4[3]);
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int blk = bp + e;
             uint32_t bh0, bl0, bh1, bl1;
-            load_vh(blk);
             pscaled(blk, bh0, bl0, bh1, bl1);
             add_min(blk);
             const uint32_t ra = rr4[2 * e], rb = rr4[2 * e + 1];  // tokens 0-7, 8-15
+            const uint32_t ra8 = ra >> 8, rb8 = rb >> 8;
+            // high bits: at bit 4 / 20 for the low nibbles, bit 8 / 24 for the x16 high nibbles
             uint32_t ma0 = 0x64006400u, ma1 = 0x64006400u, ma2 = 0x64006400u, ma3 = 0x64006400u;
             uint32_t mb0 = 0x64006400u, mb1 = 0x64006400u, mb2 = 0x64006400u, mb3 = 0x64006400u;
             if constexpr (C::V5) {
@@ -657,14 +830,14 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
               const uint32_t wa = __byte_perm(h0, h1, 0x5410), wa2 = __byte_perm(h0, h1, 0x7632);
               const uint32_t wb = __byte_perm(h8, h9, 0x5410), wb2 = __byte_perm(h8, h9, 0x7632);
               ma0 = ((wa << 4) & 0x00100010u) | 0x64006400u;  ma1 = ((wa << 3) & 0x00100010u) | 0x64006400u;
-              ma2 = ((wa2 << 4) & 0x00100010u) | 0x64006400u; ma3 = ((wa2 << 3) & 0x00100010u) | 0x64006400u;
+              ma2 = ((wa2 << 8) & 0x01000100u) | 0x64006400u; ma3 = ((wa2 << 7) & 0x01000100u) | 0x64006400u;
               mb0 = ((wb << 4) & 0x00100010u) | 0x64006400u;  mb1 = ((wb << 3) & 0x00100010u) | 0x64006400u;
-              mb2 = ((wb2 << 4) & 0x00100010u) | 0x64006400u; mb3 = ((wb2 << 3) & 0x00100010u) | 0x64006400u;
+              mb2 = ((wb2 << 8) & 0x01000100u) | 0x64006400u; mb3 = ((wb2 << 7) & 0x01000100u) | 0x64006400u;
             }
-            const uint32_t a0[4] = {nib_pair(ra, 0, ma0, OFF), nib_pair(ra, 8, ma1, OFF),
-                                    nib_pair(rb, 0, mb0, OFF), nib_pair(rb, 8, mb1, OFF)};
-            const uint32_t a1[4] = {nib_pair(ra, 4, ma2, OFF), nib_pair(ra, 12, ma3, OFF),
-                                    nib_pair(rb, 4, mb2, OFF), nib_pair(rb, 12, mb3, OFF)};
+            const uint32_t a0[4] = {nib_pair(ra, 0, ma0, OFF), nib_pair(ra8, 0, ma1, OFF),
+                                    nib_pair(rb, 0, mb0, OFF), nib_pair(rb8, 0, mb1, OFF)};
+            const uint32_t a1[4] = {nib_pair_x16(ra, ma2, OFF16), nib_pair_x16(ra8, ma3, OFF16),
+                                    nib_pair_x16(rb, mb2, OFF16), nib_pair_x16(rb8, mb3, OFF16)};
             mma16816(acc[blk][0], a0, bh0, bh1);
             mma16816(acc[blk][0], a0, bl0, bl1);
             mma16816(acc[blk][1], a1, bh0, bh1);
@@ -674,10 +847,11 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
       }
       if constexpr (OL) {  // outlier slots += codes_O^T . (P * d_O), as one more q8_0 block
         const __half* vod = reinterpret_cast<const __half*>(st + C::off_vod);
+        const uint32_t mlo = (vt0 ? 0x0000FFFFu : 0u) | (vt1 ? 0xFFFF0000u : 0u);
+        const uint32_t mhi = (vt8 ? 0x0000FFFFu : 0u) | (vt9 ? 0xFFFF0000u : 0u);
         uint32_t bh0, bl0, bh1, bl1;
-        const uint32_t o01 = ld_h2(vod + 2 * tig), o89 = ld_h2(vod + 2 * tig + 8);
-        split_h2(pz[0] * h2f(o01, 0), pz[1] * h2f(o01, 1), bh0, bl0);
-        split_h2(pz[2] * h2f(o89, 0), pz[3] * h2f(o89, 1), bh1, bl1);
+        hscale_split(ph0, pl0, ld_h2(vod + 2 * tig) & mlo, bh0, bl0);
+        hscale_split(ph1, pl1, ld_h2(vod + 2 * tig + 8) & mhi, bh1, bl1);
         uint32_t r0, r1, r2, r3;
         ldsm_x4_t(smem_u32(st + C::off_vo) + rr * 32 + 16 * (mi >> 1), r0, r1, r2, r3);
         r0 ^= 0x80808080u; r1 ^= 0x80808080u; r2 ^= 0x80808080u; r3 ^= 0x80808080u;
@@ -690,6 +864,12 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
       }
     } else {
       // tail values are stored as fp16 * 2^-8, so P carries the factor 256
+      float pt[4];
+      {
+        const float2 a0 = __half22float2(u32_as_h2(ph0)), b0 = __half22float2(u32_as_h2(pl0));
+        const float2 a1 = __half22float2(u32_as_h2(ph1)), b1 = __half22float2(u32_as_h2(pl1));
+        pt[0] = a0.x + b0.x; pt[1] = a0.y + b0.y; pt[2] = a1.x + b1.x; pt[3] = a1.y + b1.y;
+      }
       uint32_t bh0, bl0, bh1, bl1;
       split_h2(pt[0] * 256.0f, pt[1] * 256.0f, bh0, bl0);
       split_h2(pt[2] * 256.0f, pt[3] * 256.0f, bh1, bl1);
@@ -697,15 +877,14 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
       const uint32_t mlo = (vt0 ? 0x0000FFFFu : 0u) | (vt1 ? 0xFFFF0000u : 0u);
       const uint32_t mhi = (vt8 ? 0x0000FFFFu : 0u) | (vt9 ? 0xFFFF0000u : 0u);
       const uint32_t vbase = smem_u32(st + C::off_vt);
-      const int mi = lane >> 3;
-      const int rr = (lane & 7) + (C::TT == 16 ? 8 * (mi >> 1) : 0);
+      const int rt = (lane & 7) + (C::TT == 16 ? 8 * (mi >> 1) : 0);
 #pragma unroll
       for (int blk = 0; blk < NB; ++blk)
 #pragma unroll
         for (int cc2 = 0; cc2 < 2; ++cc2) {
           const int mt = 2 * blk + cc2;  // 16 channels
           uint32_t r0, r1, r2, r3;
-          ldsm_x4_t(vbase + swz_off<C::WT>(rr, 2 * (16 * mt + 8 * (mi & 1)), C::TT), r0, r1, r2, r3);
+          ldsm_x4_t(vbase + swz_off<C::WT>(rt, 2 * (16 * mt + 8 * (mi & 1)), C::TT), r0, r1, r2, r3);
           const uint32_t a[4] = {bf16x2_to_h2_scaled(r0) & mlo, bf16x2_to_h2_scaled(r1) & mlo,
                                  bf16x2_to_h2_scaled(r2) & mhi, bf16x2_to_h2_scaled(r3) & mhi};
           mma16816(acc[blk][cc2], a, bh0, bh1);
@@ -724,13 +903,16 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     // wait (bounded) for this warp's copies still in flight before leaving:
     // tiles k_stop .. k_stop+NS-1 were issued and not consumed
     for (int k = k_stop; k < my_tiles && k < k_stop + NS; ++k) {
-      const int s = k % NS;
-      mbar_wait_bounded(&wbar[s], (k / NS) & 1, kWaitCycles);
+      const int s = (kk + k) % NS;
+      mbar_wait_bounded(&wbar[s], ((kk + k) / NS) & 1, kWaitCycles);
     }
   }
+  kk += my_tiles;
+  const int slot_w = s_cur[3];
+  const bool last_w = s_cur[4] != 0;
 
   // the merge kernel may start launching (it waits for this grid's completion)
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (last_w) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // ---- merge the 4 warps, write this CTA's partial ---------------------------
 #pragma unroll
@@ -799,7 +981,7 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     float v = 0.0f;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) v += macc[((size_t)w * kMaxHeads + hh) * D + c];
-    p.ws_acc[(((size_t)b * p.n_q_heads + head0 + hh) * p.splits + split) * D + c] = v;
+    p.ws_acc[(((size_t)plane * p.slots + slot_w) * p.heads_per_cta + hh) * D + c] = v;
   }
   if constexpr (OL) {
     for (int i = tid; i < nheads * 32; i += kThreads) {
@@ -807,7 +989,7 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
       float v = 0.0f;
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) v += maco[((size_t)w * kMaxHeads + hh) * 32 + c];
-      p.ws_acco[(((size_t)b * p.n_q_heads + head0 + hh) * p.splits + split) * 32 + c] = v;
+      p.ws_acco[(((size_t)plane * p.slots + slot_w) * p.heads_per_cta + hh) * 32 + c] = v;
     }
   }
   if (tid < nheads) {
@@ -818,49 +1000,84 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
       const float mw = sm_m[w * kMaxHeads + tid];
       if (mw != -INFINITY) L += sm_l[w * kMaxHeads + tid] * fast_exp2(mw - M);
     }
-    ml[(size_t)tid * p.splits * 2] = M;
-    ml[(size_t)tid * p.splits * 2 + 1] = L;
+    float* ml = p.ws_ml + ((size_t)plane * p.slots + slot_w) * p.heads_per_cta * 2;
+    ml[2 * tid] = M;
+    ml[2 * tid + 1] = L;
   }
+  __syncthreads();  // this sub-range's partial written; its stages, q and (m, l) free again
+  if (last_w || timed_out) break;
+  }  // sub-ranges
 }
 
 // ---------------------------------------------------------------------------
 // Split merge + inverse rotation: one CTA of 256 threads per (sequence, query
-// head).  The split weights 2^(m_s - M) go to shared memory; then every thread
-// owns channels (D <= 256: a group of 256 / D threads shares a channel and takes
-// every (256/D)-th split), so all partial loads of a row are independent and
-// coalesced; splits with weight 0 (no keys) are skipped, their rows were never
-// written; warp 0 rotates the merged row back.
+// head).  The partition header (written by the split kernel) gives the sequence's
+// stream offset and length, from which the slots holding its partials follow: for
+// each of its segments, the pieces that intersect it.  The slot weights
+// 2^(m_s - M) go to shared memory; then every thread owns channels (D <= 256: a
+// group of 256 / D threads shares a channel and takes every (256/D)-th slot), so
+// all partial loads of a row are independent and coalesced; warp 0 rotates the
+// merged row back.
 // ---------------------------------------------------------------------------
 constexpr int kCombineThreads = 256;
 
+struct CombineArgs {
+  const float* ws_acc; const float* ws_ml; const float* ws_acco; const long long* hdr;
+  int slots, heads_per_cta, head_groups, group, batch, tail_len, fused, rot_v, out_dtype, n_q_heads;
+  long long cost_body, cost_tail;
+  void* out;
+  int32_t* seq_len;      // fused step: advanced to the header's token count
+  const int32_t* oidx;   // outlier channels [kv_head][32]
+};
+
+// slots of one segment: the stream pieces it intersects, as a first slot and a count
+__device__ __forceinline__ void seg_slots(long long P, long long cs, long long ch, int base, int& s0, int& cnt) {
+  if (cs <= 0) { s0 = 0; cnt = 0; return; }
+  const long long p0 = P / ch, p1 = (P + cs - 1) / ch;
+  s0 = base + int(p0);
+  cnt = int(p1 - p0 + 1);
+}
+
 template <int D, bool OL>
-__global__ void __launch_bounds__(kCombineThreads)
-decode_combine_kernel(const float* __restrict__ ws_acc, const float* __restrict__ ws_ml, int splits,
-                      int rot_v, void* __restrict__ out, int out_dtype, int n_q_heads, int fused,
-                      FusedAppend fa, int32_t* __restrict__ seq_len, int max_ctx,
-                      const float* __restrict__ ws_acco, const int32_t* __restrict__ oidx, int group) {
+__global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(CombineArgs a) {
   constexpr int G = (D >= 64 && D % 64 == 0) ? (((D & (D - 1)) == 0) ? D : 64) : 32;
   constexpr int E = D / 32;
   constexpr int TPC = kCombineThreads / D >= 1 ? kCombineThreads / D : 1;  // threads per channel
-  extern __shared__ float s_w[];                 // [splits] weights
+  extern __shared__ float s_w[];                 // [slots of this sequence] weights
   __shared__ float s_part[kCombineThreads];      // per-thread partial sums, then the merged row
   __shared__ float s_red[2][kCombineThreads / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int row = blockIdx.x;  // b * Hq + h
+  const int b = row / a.n_q_heads, h = row % a.n_q_heads;
+  const int kvh = h / a.group, r = h % a.group;
+  const int plane = kvh * a.head_groups + r / a.heads_per_cta, hh = r % a.heads_per_cta;
   // launched as a programmatic dependent of the split kernel: wait for its completion
   // (and memory) before reading anything it wrote
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  const long long ch = a.hdr[0], P = a.hdr[1 + 2 * b];
+  const int n = int(a.hdr[2 + 2 * b]);
   // fused step: every split CTA has read seq_len; advance it (head 0's CTA of each sequence)
-  if (fused && tid == 0 && row % n_q_heads == 0) {
-    const int b = row / n_q_heads;
-    bool ok;
-    seq_len[b] += fused_count(fa, seq_len[b], b, max_ctx, ok);
+  if (a.fused && tid == 0 && h == 0) a.seq_len[b] = n;
+  // this sequence's slots: two runs (tail pieces, body pieces)
+  const int T = a.tail_len;
+  const long long ct = (long long)min(n, T) * a.cost_tail, cb = (long long)max(0, n - T) * a.cost_body;
+  int r0, c0, r1, c1;
+  if (a.fused) {
+    r0 = b; c0 = min(n, T) > 0 ? 1 : 0;
+    seg_slots(P, cb, ch, a.batch + b, r1, c1);
+  } else {
+    seg_slots(P, ct, ch, 2 * b, r0, c0);
+    seg_slots(P + ct, cb, ch, 2 * b + 1, r1, c1);
   }
-  const float* ml = ws_ml + (size_t)row * splits * 2;
-  // 1. M = max over non-empty splits
+  const int splits = c0 + c1;
+  auto slot_of = [&](int j) { return j < c0 ? r0 + j : r1 + (j - c0); };
+  const size_t base = (size_t)plane * a.slots;  // slot rows of this plane
+  // 1. M = max over non-empty slots
   float M = -INFINITY;
-  for (int s = tid; s < splits; s += kCombineThreads)
-    if (ml[2 * s + 1] > 0.0f) M = fmaxf(M, ml[2 * s]);
+  for (int j = tid; j < splits; j += kCombineThreads) {
+    const float* ml = a.ws_ml + ((base + slot_of(j)) * a.heads_per_cta + hh) * 2;
+    if (ml[1] > 0.0f) M = fmaxf(M, ml[0]);
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   if (lane == 0) s_red[0][warp] = M;
@@ -870,10 +1087,11 @@ decode_combine_kernel(const float* __restrict__ ws_acc, const float* __restrict_
   for (int w = 1; w < kCombineThreads / 32; ++w) M = fmaxf(M, s_red[0][w]);
   // 2. weights and L = sum of l_s * weight
   float L = 0.0f;
-  for (int s = tid; s < splits; s += kCombineThreads) {
-    const float l = ml[2 * s + 1];
-    const float w = l > 0.0f ? exp2f(ml[2 * s] - M) : 0.0f;
-    s_w[s] = w;
+  for (int j = tid; j < splits; j += kCombineThreads) {
+    const float* ml = a.ws_ml + ((base + slot_of(j)) * a.heads_per_cta + hh) * 2;
+    const float l = ml[1];
+    const float w = l > 0.0f ? exp2f(ml[0] - M) : 0.0f;
+    s_w[j] = w;
     L += l * w;
   }
 #pragma unroll
@@ -883,20 +1101,20 @@ decode_combine_kernel(const float* __restrict__ ws_acc, const float* __restrict_
   L = 0.0f;
 #pragma unroll
   for (int w = 0; w < kCombineThreads / 32; ++w) L += s_red[1][w];
-  // 3. channel c of this thread, splits sub, sub + TPC, ...
+  // 3. channel c of this thread, slots sub, sub + TPC, ...
   const int c = tid % D, sub = tid / D;
   float v = 0.0f;
   if (tid < D * TPC) {
-    // 8 partials in flight per thread; rows of empty splits (weight 0) were never
-    // written: whatever they hold is read but selected away, never multiplied
-    const float* a = ws_acc + (size_t)row * splits * D + c;
+    // 8 partials in flight per thread.  A slot whose sub-range was empty holds only its
+    // (m, l) = (-inf, 0); its acc row is whatever an earlier call left there, so it is
+    // read but selected away by its weight 0 and must never be multiplied.
     for (int s0 = sub; s0 < splits; s0 += 8 * TPC) {
       float x[8], wv[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int s = s0 + u * TPC;
-        wv[u] = s < splits ? s_w[s] : 0.0f;
-        x[u] = s < splits ? a[(size_t)s * D] : 0.0f;
+        const int j = s0 + u * TPC;
+        wv[u] = j < splits ? s_w[j] : 0.0f;
+        x[u] = j < splits ? a.ws_acc[((base + slot_of(j)) * a.heads_per_cta + hh) * D + c] : 0.0f;
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) v += wv[u] != 0.0f ? wv[u] * x[u] : 0.0f;
@@ -906,14 +1124,14 @@ decode_combine_kernel(const float* __restrict__ ws_acc, const float* __restrict_
   // outlier channels: merged partial of slot tid
   __shared__ float s_o[32];
   if (OL && tid < 32) {
-    const float* a = ws_acco + (size_t)row * splits * 32 + tid;
     float t = 0.0f;
     for (int s0 = 0; s0 < splits; s0 += 8) {
       float x[8], wv[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        wv[u] = s0 + u < splits ? s_w[s0 + u] : 0.0f;
-        x[u] = s0 + u < splits ? a[(size_t)(s0 + u) * 32] : 0.0f;
+        const int j = s0 + u;
+        wv[u] = j < splits ? s_w[j] : 0.0f;
+        x[u] = j < splits ? a.ws_acco[((base + slot_of(j)) * a.heads_per_cta + hh) * 32 + tid] : 0.0f;
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) t += wv[u] != 0.0f ? wv[u] * x[u] : 0.0f;
@@ -933,14 +1151,13 @@ decode_combine_kernel(const float* __restrict__ ws_acc, const float* __restrict_
     for (int u = 0; u < TPC; ++u) t += s_part[u * D + ch];
     x[j] = t * inv;
   }
-  if (rot_v) {
+  if (a.rot_v) {
     warp_fwht<D, G>(x, lane);
 #pragma unroll
     for (int j = 0; j < E; ++j) x[j] *= inv_sqrt_group<G>();
   }
   if constexpr (OL) {  // slot i's merged value goes to its channel, in the original basis
-    const int kvh = (row % n_q_heads) / group;
-    const int ch = oidx[(size_t)kvh * 32 + lane];
+    const int ch = a.oidx[(size_t)kvh * 32 + lane];
     const int prev = __shfl_up_sync(0xffffffffu, ch, 1);
     const bool ok = ch >= 0 && ch < D && (lane == 0 || prev < ch);
     const float val = s_o[lane] * inv;
@@ -956,9 +1173,9 @@ decode_combine_kernel(const float* __restrict__ ws_acc, const float* __restrict_
 #pragma unroll
   for (int j = 0; j < E; ++j) {
     const size_t e = (size_t)row * D + fwht_channel<D, G>(lane, j);
-    if (out_dtype == KVQ_F32) static_cast<float*>(out)[e] = x[j];
-    else if (out_dtype == KVQ_BF16) static_cast<__nv_bfloat16*>(out)[e] = __float2bfloat16_rn(x[j]);
-    else static_cast<__half*>(out)[e] = __float2half_rn(x[j]);
+    if (a.out_dtype == KVQ_F32) static_cast<float*>(a.out)[e] = x[j];
+    else if (a.out_dtype == KVQ_BF16) static_cast<__nv_bfloat16*>(a.out)[e] = __float2bfloat16_rn(x[j]);
+    else static_cast<__half*>(a.out)[e] = __float2half_rn(x[j]);
   }
 }
 
@@ -1007,10 +1224,13 @@ cudaError_t run_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, cons
   p.k_d = static_cast<const uint8_t*>(c.k_d); p.v_d = static_cast<const uint8_t*>(c.v_d);
   p.k_qh = static_cast<const uint32_t*>(c.k_qh); p.v_qh = static_cast<const uint32_t*>(c.v_qh);
   p.seq_len = c.seq_len; p.status = c.status; p.q = q;
-  const size_t nacc = (size_t)c.batch * n_q_heads * plan.splits * D;
-  p.ws_acc = static_cast<float*>(ws);
-  p.ws_ml = p.ws_acc + nacc;
-  p.ws_acco = OL ? p.ws_ml + (size_t)c.batch * n_q_heads * plan.splits * 2 : nullptr;
+  // workspace: partition header, then acc [plane][slot][head][D], (m, l) [plane][slot][head][2],
+  // outlier acc [plane][slot][head][32]
+  const size_t nrow = (size_t)plan.planes * plan.slots * plan.heads_per_cta;
+  p.ws_hdr = static_cast<long long*>(ws);
+  p.ws_acc = reinterpret_cast<float*>(static_cast<char*>(ws) + plan.hdr_bytes);
+  p.ws_ml = p.ws_acc + nrow * D;
+  p.ws_acco = OL ? p.ws_ml + nrow * 2 : nullptr;
   p.n_kv_heads = c.n_kv_heads; p.max_ctx = c.max_ctx; p.tail_len = c.tail_len;
   p.q_dtype = q_dtype; p.n_q_heads = n_q_heads; p.group = n_q_heads / c.n_kv_heads;
   p.heads_per_cta = plan.heads_per_cta; p.head_groups = plan.head_groups;
@@ -1021,14 +1241,10 @@ cudaError_t run_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, cons
   p.cache = c;
   p.rows = row_map(c);
   p.scale_log2 = scale * kLog2e;
-  p.chunk = plan.chunk; p.tail_chunk = plan.tail_chunk; p.splits_body = plan.splits_body; p.splits_tail = plan.splits_tail; p.splits = plan.splits;
-  for (int k = 0, s0 = 0, beg = 0; k < 3; ++k) {
-    p.cls_len[k] = plan.cls_len[k];
-    p.cls_s0[k] = s0;
-    p.cls_beg[k] = beg;
-    s0 += plan.cls_cnt[k];
-    beg += plan.cls_cnt[k] * plan.cls_len[k];
-  }
+  p.batch = c.batch;
+  p.pieces = fa ? plan.pieces_fused : plan.pieces;
+  p.slots = plan.slots;
+  p.cost_body = plan.cost_body; p.cost_tail = plan.cost_tail; p.cost_min = plan.cost_min;
 
   alignas(64) CUtensorMap mk, mv, mkt, mvt;
   memset(&mk, 0, sizeof(mk)); memset(&mv, 0, sizeof(mv)); memset(&mkt, 0, sizeof(mkt)); memset(&mvt, 0, sizeof(mvt));
@@ -1044,19 +1260,25 @@ cudaError_t run_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, cons
   auto kern = decode_split_kernel<D, KT, VT, OL>;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), Cf::smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(c.n_kv_heads * plan.head_groups, c.batch, plan.splits);
+  dim3 grid(plan.planes, fa ? c.batch + plan.pieces_fused : plan.pieces);
   kern<<<grid, kThreads, Cf::smem, st>>>(p, mk, mv, mkt, mvt);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int total = c.batch * n_q_heads;
-  const size_t wbytes = (size_t)plan.splits * sizeof(float);
+  CombineArgs ca{};
+  ca.ws_acc = p.ws_acc; ca.ws_ml = p.ws_ml; ca.ws_acco = p.ws_acco; ca.hdr = p.ws_hdr;
+  ca.slots = plan.slots; ca.heads_per_cta = plan.heads_per_cta; ca.head_groups = plan.head_groups;
+  ca.group = p.group; ca.batch = c.batch; ca.tail_len = c.tail_len; ca.fused = p.fused; ca.rot_v = rot.v;
+  ca.out_dtype = out_dtype; ca.n_q_heads = n_q_heads;
+  ca.cost_body = plan.cost_body; ca.cost_tail = plan.cost_tail;
+  ca.out = out; ca.seq_len = c.seq_len; ca.oidx = c.outlier_idx;
+  const size_t wbytes = (size_t)plan.slots * sizeof(float);
   if (wbytes > 48 * 1024) {
     e = ensure_dynamic_smem(reinterpret_cast<const void*>(decode_combine_kernel<D, OL>), (int)wbytes);
     if (e != cudaSuccess) return e;
   }
   // programmatic dependent launch: the merge grid's launch overlaps the split grid's end
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(total);
+  cfg.gridDim = dim3(c.batch * n_q_heads);
   cfg.blockDim = dim3(kCombineThreads);
   cfg.dynamicSmemBytes = wbytes;
   cfg.stream = st;
@@ -1065,9 +1287,7 @@ cudaError_t run_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, cons
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, OL>, (const float*)p.ws_acc, (const float*)p.ws_ml,
-                            (int)plan.splits, (int)rot.v, out, out_dtype, n_q_heads, p.fused, p.fa, c.seq_len,
-                            c.max_ctx, (const float*)p.ws_acco, c.outlier_idx, p.group);
+  return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, OL>, ca);
 }
 
 template <int D>

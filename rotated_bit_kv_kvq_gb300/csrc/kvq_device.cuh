@@ -86,6 +86,31 @@ __device__ __forceinline__ uint32_t hsub2_bits(uint32_t a, uint32_t b) {
   return r;
 }
 
+// fp16x2 a * b and a * b + c, each rounded once to nearest even (never contracted
+// or reassociated by the compiler).
+__device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t hfma2_bits(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
+
+// P * d for an fp16 pair P = hi + lo (lo the rounding residue of hi) and an fp16
+// pair d, as a new hi + lo pair: hi = RN(P_hi * d); the residue P_hi * d - hi is
+// exact in one fused operation (a product of two 11-bit significands rounded to 11
+// bits leaves at most 11 bits), and lo = RN(P_lo * d + residue).
+__device__ __forceinline__ void hscale_split(uint32_t p_hi, uint32_t p_lo, uint32_t d, uint32_t& hi, uint32_t& lo) {
+  hi = hmul2_bits(p_hi, d);
+  uint32_t r;
+  asm("{\n\t.reg .b32 nh;\n\tneg.f16x2 nh, %3;\n\tfma.rn.f16x2 %0, %1, %2, nh;\n\t}"
+      : "=r"(r) : "r"(p_hi), "r"(d), "r"(hi));
+  lo = hfma2_bits(p_lo, d, r);
+}
+
 // pack two floats into fp16x2 (round to nearest even); lo goes to bits 0..15.
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   uint32_t r;
@@ -104,6 +129,18 @@ __device__ __forceinline__ uint32_t nib_pair(uint32_t r, int s, uint32_t hb_or_m
   uint32_t t = ((r >> s) & 0x000F000Fu) | hb_or_magic;
   return hsub2_bits(t, off_bits);
 }
+// The same for nibbles at bit offsets 4 and 20 (high bits already at bit 8 / bit 24
+// in `hb16`): the half is 1024 + 16 * code exactly; one fused x / 16 - (64 + off)
+// gives code - off exactly.  Saves the shift of the plain form.
+__device__ __forceinline__ uint32_t nib_pair_x16(uint32_t r, uint32_t hb16_or_magic, uint32_t neg_off_bits) {
+  const uint32_t t = (r & 0x00F000F0u) | hb16_or_magic;
+  return hfma2_bits(t, 0x2C002C00u, neg_off_bits);  // 0x2C00 = 1/16
+}
+// -(64 + off) as an fp16 pair for nib_pair_x16 (off = 0, 8 or 16)
+__host__ __device__ constexpr uint32_t neg_off_x16_bits(int off) {
+  return (off == 8 ? 0xD480u : off == 16 ? 0xD500u : 0xD400u) * 0x10001u;
+}
+
 // Signed bytes i0, i1 (0..3) of r -> fp16 pair (code).  `ru` = r ^ 0x80808080.
 template <int I0, int I1>
 __device__ __forceinline__ uint32_t i8_pair(uint32_t ru) {
@@ -232,6 +269,22 @@ __device__ __forceinline__ uint32_t swz_off(int r, int x, int rows) {
   else if (W == 32) chunk ^= ((r >> 2) & 1);  // W == 16: no swizzle
   return box * rows * W + r * W + (chunk << 4) + (xi & 15);
 }
+
+// ldmatrix rows of a 16-row tile written as W-byte boxes with their swizzle, read
+// at 16-byte chunk j + h of row r, j even (compile-time), h in {0, 1} (per lane):
+// j + h stays in j's box and chunk (j + h) mod (W/16) = (j mod (W/16)) ^ h, so the
+// swizzled offset is a per-lane constant (one per even chunk of a box, W/32 of
+// them) plus a compile-time box offset.
+template <int W>
+__device__ __forceinline__ void swz_lane(int r, int h, uint32_t (&lb)[W / 32]) {
+  const int key = W == 128 ? (r & 7) : W == 64 ? ((r >> 1) & 3) : ((r >> 2) & 1);
+#pragma unroll
+  for (int i = 0; i < W / 32; ++i) lb[i] = r * W + (((2 * i) ^ (h ^ key)) << 4);
+}
+template <int W>
+__host__ __device__ constexpr int swz_box_off(int j) { return (16 * j / W) * 16 * W; }
+template <int W>
+__host__ __device__ constexpr int swz_lane_idx(int j) { return (j % (W / 16)) / 2; }
 
 // ---------------------------------------------------------------------------
 // Warp FWHT: a head vector of D values, lane l holding E = D/32 of them.

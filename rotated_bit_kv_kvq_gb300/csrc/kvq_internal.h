@@ -54,21 +54,24 @@ cudaError_t launch_debug(const kvq_cache& c, Rot rot, int seq, int kv_head, int 
 // One CTA waiting (bounded) on a barrier that never completes: the failure path.
 cudaError_t launch_wait_timeout(uint32_t* status, long long limit_cycles, cudaStream_t st);
 
-// Decode: split plan shared by the workspace query and the launch.
+// Decode: split plan shared by the workspace query and the launch.  The work is cut
+// on the device, from seq_len, by cost: per plane (KV head x head group) every
+// sequence's tail and body form one stream of bytes to read, cut into `pieces`
+// equal pieces, one CTA each (with a fused step every tail gets a CTA of its own,
+// which also writes the new tokens, and the bodies form the stream).
 struct DecodePlan {
   int heads_per_cta;   // query heads handled by one CTA (<= 8)
   int head_groups;     // CTAs along the head axis per KV head
-  int chunk;           // body tokens per CTA (multiple of 64)
-  int splits_body;     // CTAs per (seq, head group) over the body
-  int tail_chunk;      // tail slots per CTA
-  int splits_tail;     // CTAs per (seq, head group) over the tail
-  int splits;          // splits_body + splits_tail
-  size_t ws_bytes;     // workspace bytes: acc [B][Hq][splits][D], (m, l) [B][Hq][splits][2],
-                       // then, with outlier channels, their acc [B][Hq][splits][32]
-  // body splits in dispatch order come in up to three classes of cls_cnt[c] splits of
-  // cls_len[c] tokens (a multiple of 64); a uniform plan has one class of `chunk`
-  int cls_len[3];
-  int cls_cnt[3];
+  int planes;          // n_kv_heads * head_groups
+  int pieces;          // stream pieces per plane (one wave of CTAs)
+  int pieces_fused;    // stream pieces per plane beside the batch's tail CTAs (fused step)
+  int slots;           // partial slots per plane (pieces plus the cuts at segment ends)
+  long long cost_body; // bytes of one body token of one (sequence, KV head)
+  long long cost_tail; // bytes of one tail token
+  long long cost_min;  // smallest piece
+  size_t hdr_bytes;    // partition header at the start of the workspace
+  size_t ws_bytes;     // header, then acc [planes][slots][heads_per_cta][D], (m, l) [..][2],
+                       // with outlier channels their acc [..][32]
 };
 // n_outlier > 0: the q4_0 / q5_0 / q8_0 pairs at head_dim 64, 128 and 256.
 bool decode_supported(int d, int kt, int vt, int n_outlier);
@@ -89,6 +92,8 @@ struct FusedAppend {
   int prerotated;
 };
 bool fused_step_ok(const kvq_cache& c, const DecodePlan& plan, int n_new);
+// grid dimensions within the launch limits
+bool decode_grid_ok(const kvq_cache& c, const DecodePlan& plan);
 cudaError_t launch_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, const void* q,
                           int q_dtype, int n_q_heads, float scale, void* out, int out_dtype,
                           void* ws, cudaStream_t st, const FusedAppend* fa = nullptr);
