@@ -71,7 +71,8 @@ DecodePlan plan_decode(const kvq_cache& c, int n_q_heads, int sm_count) {
   pl.heads_per_cta = (g + pl.head_groups - 1) / pl.head_groups;
   pl.planes = c.n_kv_heads * pl.head_groups;
   // one wave: as many pieces per plane as the SMs hold CTAs of this kernel
-  const long long slots = (long long)ctas_per_sm(c.head_dim, c.n_outlier != 0) * (sm_count > 0 ? sm_count : 148);
+  const long long sms = sm_count > 0 ? sm_count : 148;
+  const long long slots = (long long)ctas_per_sm(c.head_dim, c.n_outlier != 0) * sms;
   pl.pieces = int(std::max<long long>(1, slots / pl.planes));
   pl.pieces_fused = std::max(1, pl.pieces - c.batch);
   // a piece of the stream touches one more segment than it covers whole at each end:
@@ -82,6 +83,14 @@ DecodePlan plan_decode(const kvq_cache& c, int n_q_heads, int sm_count) {
                  (c.n_outlier ? 2 * 34 : 0);
   pl.cost_tail = 4LL * c.head_dim;           // bf16 K and V
   pl.cost_min = 128 * pl.cost_body;          // 8 tiles: 2 per warp
+  // Measured on the 64k-context workload with equal pieces: an SM's first, second and third
+  // CTA ended after 94, 99 and 105 us.  Pieces weighted 1/94 : 1/99 : 1/105 end together.
+  pl.sms = int(sms);
+  pl.slot_weight[0] = 112; pl.slot_weight[1] = 106; pl.slot_weight[2] = 100;
+  const int cps = ctas_per_sm(c.head_dim, c.n_outlier != 0);
+  auto one_wave = [&](long long ctas) { return cps == 3 && ctas > 2 * sms && ctas <= 3 * sms; };
+  pl.weighted = one_wave((long long)pl.planes * pl.pieces);
+  pl.weighted_fused = one_wave((long long)pl.planes * (c.batch + pl.pieces_fused));
   pl.hdr_bytes = ((size_t)(1 + 2 * c.batch) * sizeof(long long) + 255) / 256 * 256;
   const size_t rows = (size_t)pl.planes * pl.slots * pl.heads_per_cta;
   pl.ws_bytes = pl.hdr_bytes + rows * (c.head_dim + 2 + c.n_outlier) * sizeof(float);

@@ -115,7 +115,8 @@ struct Params {
   // read), at least cost_min each.  A fused step gives every tail a CTA of its own.
   int batch, pieces, slots;         // stream pieces and partial slots per plane
   long long cost_body, cost_tail, cost_min;
-  long long* ws_hdr;                // [0] piece cost, then per sequence: stream offset, tokens
+  int sms, wt[3];                   // piece weights by dispatch slot (Cuts), wt[0] = 0: uniform
+  long long* ws_hdr;                // [0] stream cost per plane, then per sequence: stream offset, tokens
   // fused step: new tokens written by the tail CTA (fused != 0)
   int fused, rot_v;
   FusedAppend fa;
@@ -156,6 +157,56 @@ __device__ __forceinline__ int seg_token(long long x, long long P, long long c, 
   const long long ta = (t + tile - 1) / tile * tile;
   return ta >= ntok ? ntok : int(ta);
 }
+// Cut points of one plane's stream into `pieces` pieces: [cut(p), cut(p + 1)).
+// Uniform pieces of max(total / pieces, cost_min) bytes; or, when the grid is one
+// full wave of three CTAs per SM, pieces weighted by their CTA's dispatch slot
+// (the SM's first, second or third CTA: the warp scheduler favours the oldest
+// warps, so equal pieces end at different times) so that an SM's CTAs end together:
+// cut(p) = min(total, W(p) * unit), W(p) the weight of pieces [0, p), unit =
+// ceil(total / W(pieces)).  One division per set-up; cut() is a few integer ops.
+struct Cuts {
+  long long total, step;  // step: bytes per piece (uniform) or per unit of weight
+  int pieces, e0, e1;     // pieces below e0 run in slot 0, below e1 in slots 0-1
+  int wt[3];              // wt[0] == 0: uniform
+  __device__ long long wsum(int q) const {
+    const int c0 = min(max(e0, 0), q), c1 = min(max(e1, 0), q);
+    return (long long)wt[0] * c0 + (long long)wt[1] * (c1 - c0) + (long long)wt[2] * (q - c1);
+  }
+  __device__ long long cut(int q) const {
+    if (q >= pieces) return total;
+    return min(total, (wt[0] == 0 ? (long long)q : wsum(q)) * step);
+  }
+  // the last piece starting at or before stream offset pos
+  __device__ int piece_of(long long pos) const {
+    int lo = 0, hi = pieces - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (cut(mid) <= pos) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+  }
+};
+// piece p of plane x runs as CTA x + (y0 + p) * planes of a grid dispatched in order
+__device__ __forceinline__ Cuts make_cuts(long long total, int pieces, long long cost_min, int planes, int y0,
+                                          int sms, const int (&wt)[3], int x) {
+  Cuts c;
+  c.total = total;
+  c.pieces = pieces;
+  c.e0 = (sms - x + planes - 1) / planes - y0;
+  c.e1 = (2 * sms - x + planes - 1) / planes - y0;
+  const bool weighted = wt[0] != 0 && total >= (long long)pieces * cost_min;
+  c.wt[0] = weighted ? wt[0] : 0;
+  c.wt[1] = wt[1];
+  c.wt[2] = wt[2];
+  if (weighted) {
+    const long long W = c.wsum(pieces);
+    c.step = (total + W - 1) / W;
+  } else {
+    c.step = max((total + pieces - 1) / pieces, cost_min);
+  }
+  return c;
+}
+
 // exclusive prefix sum over the CTA's threads (kThreads); *total = the sum of all
 __device__ __forceinline__ long long cta_excl_scan(long long v, long long* total, long long* s_warp) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -207,6 +258,62 @@ __device__ __forceinline__ void lds_words(const uint8_t* p, uint32_t (&w)[BYTES 
   } else {
 #pragma unroll
     for (int i = 0; i < BYTES / 4; ++i) w[i] = reinterpret_cast<const uint32_t*>(p)[i];
+  }
+}
+
+// The query row `row` (of D values, f32 / bf16 / f16) as lane `lane`'s values in
+// the warp FWHT layout (P = G/32 consecutive channels per group and lane): one
+// vector load per group, all issued before any is used; zeros when !valid.
+template <int D, int G>
+__device__ __forceinline__ void load_q_fwht(const void* q, int dtype, size_t row, bool valid, int lane,
+                                            float (&v)[D / 32]) {
+  constexpr int P = G / 32, NG = D / G;
+#pragma unroll
+  for (int j = 0; j < D / 32; ++j) v[j] = 0.0f;
+  if (!valid) return;
+  if (dtype == KVQ_F32) {
+    const float* base = static_cast<const float*>(q) + row * D + lane * P;
+#pragma unroll
+    for (int gi = 0; gi < NG; ++gi) {
+      const float* src = base + gi * G;
+      if constexpr (P % 4 == 0) {
+#pragma unroll
+        for (int k = 0; k < P; k += 4) {
+          const float4 x = *reinterpret_cast<const float4*>(src + k);
+          v[gi * P + k] = x.x; v[gi * P + k + 1] = x.y; v[gi * P + k + 2] = x.z; v[gi * P + k + 3] = x.w;
+        }
+      } else if constexpr (P == 2) {
+        const float2 x = *reinterpret_cast<const float2*>(src);
+        v[gi * P] = x.x; v[gi * P + 1] = x.y;
+      } else {
+        v[gi * P] = src[0];
+      }
+    }
+  } else {
+    const uint16_t* base = static_cast<const uint16_t*>(q) + row * D + lane * P;
+    uint32_t w[NG][(P + 1) / 2];
+#pragma unroll
+    for (int gi = 0; gi < NG; ++gi) {
+      const uint16_t* src = base + gi * G;
+      if constexpr (P == 8) {
+        const uint4 x = *reinterpret_cast<const uint4*>(src);
+        w[gi][0] = x.x; w[gi][1] = x.y; w[gi][2] = x.z; w[gi][3] = x.w;
+      } else if constexpr (P == 4) {
+        const uint2 x = *reinterpret_cast<const uint2*>(src);
+        w[gi][0] = x.x; w[gi][1] = x.y;
+      } else if constexpr (P == 2) {
+        w[gi][0] = *reinterpret_cast<const uint32_t*>(src);
+      } else {
+        w[gi][0] = src[0];
+      }
+    }
+#pragma unroll
+    for (int gi = 0; gi < NG; ++gi)
+#pragma unroll
+      for (int k = 0; k < P; ++k) {
+        const uint32_t h = (w[gi][k / 2] >> (16 * (k & 1))) & 0xFFFFu;
+        v[gi * P + k] = dtype == KVQ_BF16 ? bf16_bits_to_f32(h) : __half2float(__ushort_as_half((unsigned short)h));
+      }
   }
 }
 
@@ -262,13 +369,21 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
   float* sm_m = reinterpret_cast<float*>(smem + C::off_ml);
   float* sm_l = sm_m + kWarps * kMaxHeads;
   __shared__ long long s_scan[kWarps];
-  __shared__ long long s_part[3];  // piece cost; stream offset and index of the piece's first sequence
 
+  // The piece's cursor (stream offset, sequence, segment kind, staged queries'
+  // sequence) lives in shared memory between sub-ranges; every thread advances a
+  // copy identically.
+  __shared__ long long s_cur_P, s_x[2];  // cursor offset; the piece's [x0, x1)
+  __shared__ int s_cur[5];  // sequence, next segment kind (0 tail, 1 body), staged sequence, slot, last
   if (tid == 0) {
     for (int i = 0; i < kWarps * NS; ++i) mbar_init(&bars[i], 1);
     fence_barrier_init();
     prefetch_tmap(&tmK); prefetch_tmap(&tmV);
     if (T > 0) { prefetch_tmap(&tmKt); prefetch_tmap(&tmVt); }
+    s_cur_P = 0;
+    s_cur[0] = own_tail ? int(blockIdx.y) : -1;
+    s_cur[1] = (p.fused && !own_tail) ? 1 : 0;
+    s_cur[2] = -1;
   }
 
   // ---- the partition: every CTA computes the same cut from seq_len ----------
@@ -280,34 +395,23 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     for (int bb = b0; bb < b1; ++bb)
       mine += stream_cost(seq_tokens(p, bb, cta0), T, p.fused, p.cost_body, p.cost_tail);
     long long total;
-    long long P = cta_excl_scan(mine, &total, s_scan);
-    const long long ch = max((total + p.pieces - 1) / p.pieces, p.cost_min);
-    if (tid == 0) { s_part[0] = ch; s_part[1] = 0; s_part[2] = -1; }
-    __syncthreads();
-    const long long x0 = piece * ch;
+    long long P = cta_excl_scan(mine, &total, s_scan);  // (its barrier orders the cursor set-up above)
+    const Cuts cu = make_cuts(total, p.pieces, p.cost_min, p.head_groups * p.n_kv_heads, p.fused ? B : 0, p.sms,
+                              p.wt, plane);
+    const long long x0 = piece >= 0 ? cu.cut(int(piece)) : 0;
+    if (tid == 0) { s_x[0] = x0; s_x[1] = piece >= 0 ? cu.cut(int(piece) + 1) : 0; }
     for (int bb = b0; bb < b1; ++bb) {
       const int n = seq_tokens(p, bb, false);
       const long long c = stream_cost(n, T, p.fused, p.cost_body, p.cost_tail);
-      if (piece >= 0 && c > 0 && P <= x0 && x0 < P + c) { s_part[1] = P; s_part[2] = bb; }
+      if (piece >= 0 && c > 0 && P <= x0 && x0 < P + c) { s_cur_P = P; s_cur[0] = bb; }
       if (cta0) { p.ws_hdr[1 + 2 * bb] = P; p.ws_hdr[2 + 2 * bb] = n; }
       P += c;
     }
-    if (cta0 && tid == 0) p.ws_hdr[0] = ch;
+    if (cta0 && tid == 0) p.ws_hdr[0] = total;
   }
   __syncthreads();
 
   // ---- the piece's sub-ranges, one (sequence, tail or body) segment each ------
-  // The cursor (stream offset, sequence, segment kind, staged queries' sequence) lives
-  // in shared memory between sub-ranges; every thread advances a copy identically.
-  __shared__ long long s_cur_P;
-  __shared__ int s_cur[5];  // sequence, next segment kind (0 tail, 1 body), staged sequence, slot, last
-  if (tid == 0) {
-    s_cur_P = s_part[1];
-    s_cur[0] = own_tail ? int(blockIdx.y) : int(s_part[2]);
-    s_cur[1] = (p.fused && !own_tail) ? 1 : 0;
-    s_cur[2] = -1;
-  }
-  __syncthreads();
   uint32_t kk = 0;  // tiles this warp consumed (ring phases)
   bool timed_out = false;
   for (;;) {
@@ -315,7 +419,7 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     int b = 0, n0 = 0, nn = 0, t_begin = 0, t_end = 0, slot = 0, cur_b;
     bool is_tail = false, last = true, found = false;
     {
-      const long long x0 = piece * s_part[0], x1 = x0 + s_part[0];
+      const long long x0 = s_x[0], x1 = s_x[1];
       long long Pseg = s_cur_P;
       int sb = s_cur[0], kind = s_cur[1];
       cur_b = s_cur[2];
@@ -421,6 +525,18 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     }
   };
 
+  // the query rows of a newly touched sequence: loads issued before the tile copies,
+  // which would otherwise queue ahead of them
+  constexpr int GQR = (D >= 64 && D % 64 == 0) ? (((D & (D - 1)) == 0) ? D : 64) : 32;
+  float qv[2][D / 32];  // warp w: heads w and w + 4 in the FWHT layout
+  if (b != cur_b) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int hh = warp + kWarps * i;
+      load_q_fwht<D, GQR>(p.q, p.q_dtype, (size_t)b * p.n_q_heads + head0 + hh, hh < nheads, lane, qv[i]);
+    }
+  }
+
   // Fused step: this (sequence, KV head)'s only tail CTA writes the new tokens
   // (body blocks and bf16 tail rows) before any tail tile is fetched.  Body CTAs
   // never treat those positions as valid: they are >= n - T.  The proxy fence
@@ -450,90 +566,89 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
   const uint4* qfs = reinterpret_cast<const uint4*>(sq);
   float* qsum = reinterpret_cast<float*>(smem + C::off_qsum);  // [blk][head]: sum of the block's q values
   if (b != cur_b) {
-
-  for (int i = tid; i < kMaxHeads * D; i += kThreads) {
-    const int hh = i / D, c = i % D;
-    float v = 0.0f;
-    if (hh < nheads) {
-      const size_t e = ((size_t)b * p.n_q_heads + head0 + hh) * D + c;
-      if (p.q_dtype == KVQ_F32) v = static_cast<const float*>(p.q)[e];
-      else if (p.q_dtype == KVQ_BF16) v = bf16_bits_to_f32(static_cast<const uint16_t*>(p.q)[e]);
-      else v = __half2float(static_cast<const __half*>(p.q)[e]);
-    }
-    sq[i] = v;
-  }
-  __syncthreads();
-  if constexpr (OL) {
-    if (warp == 0) {
-      const int ch = outlier_channel<D>(p.cache, kvh, lane);
+    constexpr int G = GQR;
+    if constexpr (OL) {  // the outlier slots take the unrotated values
 #pragma unroll
-      for (int hh = 0; hh < kMaxHeads; ++hh) qo[hh * 32 + lane] = ch >= 0 ? sq[hh * D + ch] * p.scale_log2 : 0.0f;
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < D / 32; ++j) sq[(warp + kWarps * i) * D + fwht_channel<D, G>(lane, j)] = qv[i][j];
+      __syncthreads();
+      if (warp == 0) {
+        const int ch = outlier_channel<D>(p.cache, kvh, lane);
+#pragma unroll
+        for (int hh = 0; hh < kMaxHeads; ++hh) qo[hh * 32 + lane] = ch >= 0 ? sq[hh * D + ch] * p.scale_log2 : 0.0f;
+      }
+      __syncthreads();
+    }
+    {
+      float sc = p.scale_log2;
+      if (p.rot_k) sc *= inv_sqrt_group<G>();
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        if (p.rot_k) warp_fwht<D, G>(qv[i], lane);
+#pragma unroll
+        for (int j = 0; j < D / 32; ++j) sq[(warp + kWarps * i) * D + fwht_channel<D, G>(lane, j)] = qv[i][j] * sc;
+      }
     }
     __syncthreads();
-  }
-  {
-    constexpr int G = (D >= 64 && D % 64 == 0) ? (((D & (D - 1)) == 0) ? D : 64) : 32;
-    for (int hh = warp; hh < kMaxHeads; hh += kWarps) {
-      float v[D / 32];
+    // fragments: warp w builds blocks w, w + 4, ... from the staged values, then (after
+    // every warp has read them) writes them over the staging
+    constexpr int BPW = (NB + kWarps - 1) / kWarps;
+    uint4 qf[BPW][2];
 #pragma unroll
-      for (int j = 0; j < D / 32; ++j) v[j] = sq[hh * D + fwht_channel<D, G>(lane, j)];
-      float s = p.scale_log2;
-      if (p.rot_k) {
-        warp_fwht<D, G>(v, lane);
-        s *= inv_sqrt_group<G>();
+    for (int u = 0; u < BPW; ++u) {
+      const int blk = warp + kWarps * u;
+      if (blk < NB) {
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const float4 q4 = *reinterpret_cast<const float4*>(sq + g * D + 32 * blk + 16 * hf + 4 * tig);
+          const float qx[4] = {q4.x, q4.y, q4.z, q4.w};
+          float hi[4], lo[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            hi[j] = __half2float(__float2half_rn(qx[j]));
+            lo[j] = qx[j] - hi[j];
+          }
+          qf[u][hf] = make_uint4(pack_h2(hi[0], hi[2]), pack_h2(hi[1], hi[3]), pack_h2(lo[0], lo[2]),
+                                 pack_h2(lo[1], lo[3]));
+        }
       }
-#pragma unroll
-      for (int j = 0; j < D / 32; ++j) sq[hh * D + fwht_channel<D, G>(lane, j)] = v[j] * s;
     }
-  }
-  __syncthreads();
-  if (warp == 0) {
-    if constexpr (C::K1) {
-      for (int i = lane; i < NB * kMaxHeads; i += 32) {
+    if constexpr (C::K1) {  // the block sums of q (for the K minimum), one (block, head) per thread
+      for (int i = tid; i < NB * kMaxHeads; i += kThreads) {
         const int blk = i / kMaxHeads, hh = i % kMaxHeads;
         float t = 0.0f;
         for (int c = 0; c < 32; ++c) t += sq[hh * D + blk * 32 + c];
         qsum[i] = t;
       }
     }
-    uint4 qf[NB][2];
-#pragma unroll
-    for (int blk = 0; blk < NB; ++blk)
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const float4 q4 = *reinterpret_cast<const float4*>(sq + g * D + 32 * blk + 16 * hf + 4 * tig);
-        const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
-        float hi[4], lo[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          hi[j] = __half2float(__float2half_rn(qv[j]));
-          lo[j] = qv[j] - hi[j];
-        }
-        qf[blk][hf] = make_uint4(pack_h2(hi[0], hi[2]), pack_h2(hi[1], hi[3]), pack_h2(lo[0], lo[2]),
-                                 pack_h2(lo[1], lo[3]));
-      }
-    __syncwarp();
-#pragma unroll
-    for (int blk = 0; blk < NB; ++blk)
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) reinterpret_cast<uint4*>(sq)[(blk * 2 + hf) * 32 + lane] = qf[blk][hf];
     if constexpr (OL) {  // the outlier slots' B fragments, same layout as one block of qf
+      if (warp == 0) {
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const float4 q4 = *reinterpret_cast<const float4*>(qo + g * 32 + 16 * hf + 4 * tig);
-        const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
-        float hi[4], lo[4];
+        for (int hf = 0; hf < 2; ++hf) {
+          const float4 q4 = *reinterpret_cast<const float4*>(qo + g * 32 + 16 * hf + 4 * tig);
+          const float qx[4] = {q4.x, q4.y, q4.z, q4.w};
+          float hi[4], lo[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          hi[j] = __half2float(__float2half_rn(qv[j]));
-          lo[j] = qv[j] - hi[j];
+          for (int j = 0; j < 4; ++j) {
+            hi[j] = __half2float(__float2half_rn(qx[j]));
+            lo[j] = qx[j] - hi[j];
+          }
+          reinterpret_cast<uint4*>(smem + C::off_qof)[hf * 32 + lane] =
+              make_uint4(pack_h2(hi[0], hi[2]), pack_h2(hi[1], hi[3]), pack_h2(lo[0], lo[2]), pack_h2(lo[1], lo[3]));
         }
-        reinterpret_cast<uint4*>(smem + C::off_qof)[hf * 32 + lane] =
-            make_uint4(pack_h2(hi[0], hi[2]), pack_h2(hi[1], hi[3]), pack_h2(lo[0], lo[2]), pack_h2(lo[1], lo[3]));
       }
     }
-  }
-  __syncthreads();
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < BPW; ++u) {
+      const int blk = warp + kWarps * u;
+      if (blk < NB) {
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) reinterpret_cast<uint4*>(sq)[(blk * 2 + hf) * 32 + lane] = qf[u][hf];
+      }
+    }
+    __syncthreads();
   }  // queries of sequence b staged
   const uint4* qofs = reinterpret_cast<const uint4*>(smem + C::off_qof);
 
@@ -1024,18 +1139,19 @@ constexpr int kCombineThreads = 256;
 struct CombineArgs {
   const float* ws_acc; const float* ws_ml; const float* ws_acco; const long long* hdr;
   int slots, heads_per_cta, head_groups, group, batch, tail_len, fused, rot_v, out_dtype, n_q_heads;
-  long long cost_body, cost_tail;
+  int pieces, planes, sms, wt[3];
+  long long cost_body, cost_tail, cost_min;
   void* out;
   int32_t* seq_len;      // fused step: advanced to the header's token count
   const int32_t* oidx;   // outlier channels [kv_head][32]
 };
 
 // slots of one segment: the stream pieces it intersects, as a first slot and a count
-__device__ __forceinline__ void seg_slots(long long P, long long cs, long long ch, int base, int& s0, int& cnt) {
+__device__ __forceinline__ void seg_slots(const Cuts& cu, long long P, long long cs, int base, int& s0, int& cnt) {
   if (cs <= 0) { s0 = 0; cnt = 0; return; }
-  const long long p0 = P / ch, p1 = (P + cs - 1) / ch;
-  s0 = base + int(p0);
-  cnt = int(p1 - p0 + 1);
+  const int p0 = cu.piece_of(P), p1 = cu.piece_of(P + cs - 1);
+  s0 = base + p0;
+  cnt = p1 - p0 + 1;
 }
 
 template <int D, bool OL>
@@ -1054,7 +1170,8 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(Combine
   // launched as a programmatic dependent of the split kernel: wait for its completion
   // (and memory) before reading anything it wrote
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const long long ch = a.hdr[0], P = a.hdr[1 + 2 * b];
+  const Cuts cu = make_cuts(a.hdr[0], a.pieces, a.cost_min, a.planes, a.fused ? a.batch : 0, a.sms, a.wt, plane);
+  const long long P = a.hdr[1 + 2 * b];
   const int n = int(a.hdr[2 + 2 * b]);
   // fused step: every split CTA has read seq_len; advance it (head 0's CTA of each sequence)
   if (a.fused && tid == 0 && h == 0) a.seq_len[b] = n;
@@ -1064,10 +1181,10 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(Combine
   int r0, c0, r1, c1;
   if (a.fused) {
     r0 = b; c0 = min(n, T) > 0 ? 1 : 0;
-    seg_slots(P, cb, ch, a.batch + b, r1, c1);
+    seg_slots(cu, P, cb, a.batch + b, r1, c1);
   } else {
-    seg_slots(P, ct, ch, 2 * b, r0, c0);
-    seg_slots(P + ct, cb, ch, 2 * b + 1, r1, c1);
+    seg_slots(cu, P, ct, 2 * b, r0, c0);
+    seg_slots(cu, P + ct, cb, 2 * b + 1, r1, c1);
   }
   const int splits = c0 + c1;
   auto slot_of = [&](int j) { return j < c0 ? r0 + j : r1 + (j - c0); };
@@ -1245,6 +1362,9 @@ cudaError_t run_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, cons
   p.pieces = fa ? plan.pieces_fused : plan.pieces;
   p.slots = plan.slots;
   p.cost_body = plan.cost_body; p.cost_tail = plan.cost_tail; p.cost_min = plan.cost_min;
+  p.sms = plan.sms;
+  const bool wave = fa ? plan.weighted_fused : plan.weighted;
+  for (int k = 0; k < 3; ++k) p.wt[k] = wave ? plan.slot_weight[k] : 0;
 
   alignas(64) CUtensorMap mk, mv, mkt, mvt;
   memset(&mk, 0, sizeof(mk)); memset(&mv, 0, sizeof(mv)); memset(&mkt, 0, sizeof(mkt)); memset(&mvt, 0, sizeof(mvt));
@@ -1269,7 +1389,9 @@ cudaError_t run_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, cons
   ca.slots = plan.slots; ca.heads_per_cta = plan.heads_per_cta; ca.head_groups = plan.head_groups;
   ca.group = p.group; ca.batch = c.batch; ca.tail_len = c.tail_len; ca.fused = p.fused; ca.rot_v = rot.v;
   ca.out_dtype = out_dtype; ca.n_q_heads = n_q_heads;
-  ca.cost_body = plan.cost_body; ca.cost_tail = plan.cost_tail;
+  ca.cost_body = plan.cost_body; ca.cost_tail = plan.cost_tail; ca.cost_min = plan.cost_min;
+  ca.pieces = p.pieces; ca.planes = plan.planes; ca.sms = plan.sms;
+  for (int k = 0; k < 3; ++k) ca.wt[k] = p.wt[k];
   ca.out = out; ca.seq_len = c.seq_len; ca.oidx = c.outlier_idx;
   const size_t wbytes = (size_t)plan.slots * sizeof(float);
   if (wbytes > 48 * 1024) {

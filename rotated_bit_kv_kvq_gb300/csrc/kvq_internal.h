@@ -69,6 +69,11 @@ struct DecodePlan {
   long long cost_body; // bytes of one body token of one (sequence, KV head)
   long long cost_tail; // bytes of one tail token
   long long cost_min;  // smallest piece
+  int sms;             // SMs the plan fills
+  // With one full wave of three CTAs per SM the pieces are weighted by dispatch slot
+  // (an SM's first, second, third CTA), so that the SM's CTAs end together.
+  int slot_weight[3];
+  bool weighted, weighted_fused;
   size_t hdr_bytes;    // partition header at the start of the workspace
   size_t ws_bytes;     // header, then acc [planes][slots][heads_per_cta][D], (m, l) [..][2],
                        // with outlier channels their acc [..][32]
