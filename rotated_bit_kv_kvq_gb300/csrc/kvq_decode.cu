@@ -83,10 +83,12 @@ DecodePlan plan_decode(const kvq_cache& c, int n_q_heads, int sm_count) {
                  (c.n_outlier ? 2 * 34 : 0);
   pl.cost_tail = 4LL * c.head_dim;           // bf16 K and V
   pl.cost_min = 128 * pl.cost_body;          // 8 tiles: 2 per warp
-  // Measured on the 64k-context workload with equal pieces: an SM's first, second and third
-  // CTA ended after 94, 99 and 105 us.  Pieces weighted 1/94 : 1/99 : 1/105 end together.
+  pl.cost_gap = 160 * pl.cost_body;          // ~4 us of a CTA's streaming time
+  // Measured on the 64k-context workload: with equal pieces an SM's first, second and third
+  // CTA ended after 94, 99 and 105 us; with pieces weighted 112 : 106 : 100 after 93, 95
+  // and 98 us; with 118 : 109 : 100 after 92.6, 93.2 and 94.7 us.
   pl.sms = int(sms);
-  pl.slot_weight[0] = 112; pl.slot_weight[1] = 106; pl.slot_weight[2] = 100;
+  pl.slot_weight[0] = 118; pl.slot_weight[1] = 109; pl.slot_weight[2] = 98;
   const int cps = ctas_per_sm(c.head_dim, c.n_outlier != 0);
   auto one_wave = [&](long long ctas) { return cps == 3 && ctas > 2 * sms && ctas <= 3 * sms; };
   pl.weighted = one_wave((long long)pl.planes * pl.pieces);

@@ -113,8 +113,12 @@ struct Params {
   // sequences -- each sequence's tail (unless the step is fused) and body, in
   // sequence order -- is one stream cut into `pieces` pieces of equal cost (bytes
   // read), at least cost_min each.  A fused step gives every tail a CTA of its own.
+  // Every non-empty segment starts with a gap of cost_gap bytes that holds no data:
+  // the cost of a CTA switching segments (partials, pipeline refill, queries), so a
+  // piece that crosses a segment boundary carries less data, and cut points that
+  // fall inside a gap move to the segment's start.
   int batch, pieces, slots;         // stream pieces and partial slots per plane
-  long long cost_body, cost_tail, cost_min;
+  long long cost_body, cost_tail, cost_min, cost_gap;
   int sms, wt[3];                   // piece weights by dispatch slot (Cuts), wt[0] = 0: uniform
   long long* ws_hdr;                // [0] stream cost per plane, then per sequence: stream offset, tokens
   // fused step: new tokens written by the tail CTA (fused != 0)
@@ -132,21 +136,27 @@ __device__ __forceinline__ int fused_count(const FusedAppend& fa, int n0, int b,
   return ok ? req : 0;
 }
 
-__device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
+// 2^x on the special-function unit (relative error about 2^-22; results below
+// 2^-126, far under any weight that matters, flush to zero)
+__device__ __forceinline__ float fast_exp2(float x) { return ex2_approx(x); }
 
-// Tokens of sequence b when the split kernel reads it (after the fused step's
-// append); `flag` reports an append that does not fit.
-__device__ __forceinline__ int seq_tokens(const Params& p, int b, bool flag) {
-  const int n0 = p.seq_len[b];
-  if (!p.fused) return n0;
+// Tokens of sequence b when the split kernel reads it (n0) and those this launch
+// appends to it (nn, fused step); `flag` reports an append that does not fit.
+__device__ __forceinline__ void seq_tokens(const Params& p, int b, bool flag, int& n0, int& nn) {
+  n0 = p.seq_len[b];
+  nn = 0;
+  if (!p.fused) return;
   bool ok;
-  const int nn = fused_count(p.fa, n0, b, p.max_ctx, ok);
+  nn = fused_count(p.fa, n0, b, p.max_ctx, ok);
   if (!ok && flag) atomicOr(p.status, KVQ_DEV_ERR_APPEND_RANGE);
-  return n0 + nn;
+}
+// cost of a segment of ntok tokens of c bytes: its gap and data, nothing when empty
+__device__ __forceinline__ long long seg_cost(int ntok, long long c, long long gap) {
+  return ntok > 0 ? gap + (long long)ntok * c : 0LL;
 }
 // cost of sequence b's part of the stream: its tail (not with a fused step) and body
-__device__ __forceinline__ long long stream_cost(int n, int T, int fused, long long cb, long long ct) {
-  return (fused ? 0LL : (long long)min(n, T) * ct) + (long long)max(0, n - T) * cb;
+__device__ __forceinline__ long long stream_cost(int n, int T, int fused, long long cb, long long ct, long long gap) {
+  return (fused ? 0LL : seg_cost(min(n, T), ct, gap)) + seg_cost(max(0, n - T), cb, gap);
 }
 // first token of a segment (ntok tokens of cost c from stream offset P) at or past
 // stream offset x, rounded up to whole tiles; piece boundaries map to the same token
@@ -375,6 +385,7 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
   // copy identically.
   __shared__ long long s_cur_P, s_x[2];  // cursor offset; the piece's [x0, x1)
   __shared__ int s_cur[5];  // sequence, next segment kind (0 tail, 1 body), staged sequence, slot, last
+  __shared__ int s_first[3];  // the piece's first sequence and its tokens (read, appended)
   if (tid == 0) {
     for (int i = 0; i < kWarps * NS; ++i) mbar_init(&bars[i], 1);
     fence_barrier_init();
@@ -384,16 +395,28 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     s_cur[0] = own_tail ? int(blockIdx.y) : -1;
     s_cur[1] = (p.fused && !own_tail) ? 1 : 0;
     s_cur[2] = -1;
+    s_first[0] = -1;
   }
 
   // ---- the partition: every CTA computes the same cut from seq_len ----------
   // (CTA 0 also records it for the merge kernel, and flags appends that do not fit)
   {
+    constexpr int kCache = 4;  // sequences per thread kept in registers (batch <= 512)
     const int per = (B + kThreads - 1) / kThreads;
     const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
+    int c0[kCache], cn[kCache];
     long long mine = 0;
-    for (int bb = b0; bb < b1; ++bb)
-      mine += stream_cost(seq_tokens(p, bb, cta0), T, p.fused, p.cost_body, p.cost_tail);
+#pragma unroll
+    for (int i = 0; i < kCache; ++i) {
+      c0[i] = cn[i] = 0;
+      if (b0 + i < b1) seq_tokens(p, b0 + i, cta0, c0[i], cn[i]);
+      mine += stream_cost(c0[i] + cn[i], T, p.fused, p.cost_body, p.cost_tail, p.cost_gap);
+    }
+    for (int bb = b0 + kCache; bb < b1; ++bb) {
+      int n0, nn;
+      seq_tokens(p, bb, cta0, n0, nn);
+      mine += stream_cost(n0 + nn, T, p.fused, p.cost_body, p.cost_tail, p.cost_gap);
+    }
     long long total;
     long long P = cta_excl_scan(mine, &total, s_scan);  // (its barrier orders the cursor set-up above)
     const Cuts cu = make_cuts(total, p.pieces, p.cost_min, p.head_groups * p.n_kv_heads, p.fused ? B : 0, p.sms,
@@ -401,15 +424,33 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     const long long x0 = piece >= 0 ? cu.cut(int(piece)) : 0;
     if (tid == 0) { s_x[0] = x0; s_x[1] = piece >= 0 ? cu.cut(int(piece) + 1) : 0; }
     for (int bb = b0; bb < b1; ++bb) {
-      const int n = seq_tokens(p, bb, false);
-      const long long c = stream_cost(n, T, p.fused, p.cost_body, p.cost_tail);
-      if (piece >= 0 && c > 0 && P <= x0 && x0 < P + c) { s_cur_P = P; s_cur[0] = bb; }
+      int n0, nn;
+      if (bb - b0 < kCache) {
+#pragma unroll
+        for (int i = 0; i < kCache; ++i)
+          if (bb - b0 == i) { n0 = c0[i]; nn = cn[i]; }
+      } else {
+        seq_tokens(p, bb, false, n0, nn);
+      }
+      const int n = n0 + nn;
+      const long long c = stream_cost(n, T, p.fused, p.cost_body, p.cost_tail, p.cost_gap);
+      const bool first = own_tail ? bb == int(blockIdx.y) : (piece >= 0 && c > 0 && P <= x0 && x0 < P + c);
+      if (first) {
+        s_cur_P = P;
+        s_cur[0] = bb;
+        s_first[0] = bb; s_first[1] = n0; s_first[2] = nn;
+      }
       if (cta0) { p.ws_hdr[1 + 2 * bb] = P; p.ws_hdr[2 + 2 * bb] = n; }
       P += c;
     }
     if (cta0 && tid == 0) p.ws_hdr[0] = total;
   }
   __syncthreads();
+
+  // The merge kernel may launch now: its CTAs take the SM slots that this grid's
+  // CTAs free as they finish and wait there for this grid's completion.  (It
+  // launches only after every CTA of this grid has started and reached this point.)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // ---- the piece's sub-ranges, one (sequence, tail or body) segment each ------
   uint32_t kk = 0;  // tiles this warp consumed (ring phases)
@@ -425,11 +466,11 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
       cur_b = s_cur[2];
       while (sb >= 0 && sb < B) {
         b = sb;
-        n0 = p.seq_len[b];
-        nn = 0;  // tokens this launch appends to sequence b (fused step)
-        if (p.fused) {
-          bool ok;
-          nn = fused_count(p.fa, n0, b, p.max_ctx, ok);
+        if (b == s_first[0]) {
+          n0 = s_first[1];
+          nn = s_first[2];
+        } else {
+          seq_tokens(p, b, false, n0, nn);
         }
         const int n = n0 + nn;
         is_tail = kind == 0;
@@ -444,14 +485,17 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
           const int ntok = is_tail ? min(n, T) : max(0, n - T);
           const long long c = is_tail ? p.cost_tail : p.cost_body;
           const long long cs = (long long)ntok * c;
-          if (cs > 0 && Pseg + cs > x0) {  // (Pseg < x1 holds while the loop runs)
-            use = true;
-            const int tile = is_tail ? C::TT : 16;
-            t_begin = seg_token(x0, Pseg, c, ntok, tile);
-            t_end = seg_token(x1, Pseg, c, ntok, tile);
-            slot = p.fused ? B + int(piece) + b : int(piece) + 2 * b + kind;
+          if (cs > 0) {
+            const long long D = Pseg + p.cost_gap;  // the segment's data starts after its gap
+            if (D < x1 && D + cs > x0) {
+              use = true;
+              const int tile = is_tail ? C::TT : 16;
+              t_begin = seg_token(x0, D, c, ntok, tile);
+              t_end = seg_token(x1, D, c, ntok, tile);
+              slot = p.fused ? B + int(piece) + b : int(piece) + 2 * b + kind;
+            }
+            Pseg = D + cs;
           }
-          Pseg += cs;
           if (p.fused || kind == 1) { kind = p.fused ? 1 : 0; ++sb; } else { kind = 1; }
           if (Pseg >= x1) sb = B;
         }
@@ -1026,8 +1070,6 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
   const int slot_w = s_cur[3];
   const bool last_w = s_cur[4] != 0;
 
-  // the merge kernel may start launching (it waits for this grid's completion)
-  if (last_w) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // ---- merge the 4 warps, write this CTA's partial ---------------------------
 #pragma unroll
@@ -1134,13 +1176,12 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
 // all partial loads of a row are independent and coalesced; warp 0 rotates the
 // merged row back.
 // ---------------------------------------------------------------------------
-constexpr int kCombineThreads = 256;
 
 struct CombineArgs {
   const float* ws_acc; const float* ws_ml; const float* ws_acco; const long long* hdr;
   int slots, heads_per_cta, head_groups, group, batch, tail_len, fused, rot_v, out_dtype, n_q_heads;
   int pieces, planes, sms, wt[3];
-  long long cost_body, cost_tail, cost_min;
+  long long cost_body, cost_tail, cost_min, cost_gap;
   void* out;
   int32_t* seq_len;      // fused step: advanced to the header's token count
   const int32_t* oidx;   // outlier channels [kv_head][32]
@@ -1154,7 +1195,7 @@ __device__ __forceinline__ void seg_slots(const Cuts& cu, long long P, long long
   cnt = p1 - p0 + 1;
 }
 
-template <int D, bool OL>
+template <int D, bool OL, int kCombineThreads>
 __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(CombineArgs a) {
   constexpr int G = (D >= 64 && D % 64 == 0) ? (((D & (D - 1)) == 0) ? D : 64) : 32;
   constexpr int E = D / 32;
@@ -1178,22 +1219,53 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(Combine
   // this sequence's slots: two runs (tail pieces, body pieces)
   const int T = a.tail_len;
   const long long ct = (long long)min(n, T) * a.cost_tail, cb = (long long)max(0, n - T) * a.cost_body;
+  const long long gap = a.cost_gap;  // every non-empty segment's data follows a gap
   int r0, c0, r1, c1;
   if (a.fused) {
     r0 = b; c0 = min(n, T) > 0 ? 1 : 0;
-    seg_slots(cu, P, cb, a.batch + b, r1, c1);
+    seg_slots(cu, P + gap, cb, a.batch + b, r1, c1);
   } else {
-    seg_slots(cu, P, ct, 2 * b, r0, c0);
-    seg_slots(cu, P + ct, cb, 2 * b + 1, r1, c1);
+    seg_slots(cu, P + gap, ct, 2 * b, r0, c0);
+    seg_slots(cu, P + (ct > 0 ? gap + ct : 0) + gap, cb, 2 * b + 1, r1, c1);
   }
   const int splits = c0 + c1;
   auto slot_of = [&](int j) { return j < c0 ? r0 + j : r1 + (j - c0); };
   const size_t base = (size_t)plane * a.slots;  // slot rows of this plane
+  // 0. channel c of this thread takes slots sub, sub + TPC, ...: the first kAhead of
+  // its partials are loaded now, while the weights are worked out.  A slot whose
+  // sub-range was empty holds only its (m, l) = (-inf, 0); its acc row is whatever an
+  // earlier call left there, so it is read but selected away by its weight 0 and
+  // must never be multiplied.
+  constexpr int kAhead = 8;
+  const int c = tid % D, sub = tid / D;
+  const bool has_ch = tid < D * TPC;
+  float xa[kAhead];
+#pragma unroll
+  for (int u = 0; u < kAhead; ++u) {
+    const int j = sub + u * TPC;
+    xa[u] = has_ch && j < splits ? a.ws_acc[((base + slot_of(j)) * a.heads_per_cta + hh) * D + c] : 0.0f;
+  }
   // 1. M = max over non-empty slots
   float M = -INFINITY;
+  float mlm[2] = {-INFINITY, -INFINITY}, mll[2] = {0.0f, 0.0f};  // this thread's first two (m, l)
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int j = tid + u * kCombineThreads;
+    if (j < splits) {
+      const float2 ml = *reinterpret_cast<const float2*>(a.ws_ml + ((base + slot_of(j)) * a.heads_per_cta + hh) * 2);
+      mlm[u] = ml.x;
+      mll[u] = ml.y;
+    }
+  }
   for (int j = tid; j < splits; j += kCombineThreads) {
-    const float* ml = a.ws_ml + ((base + slot_of(j)) * a.heads_per_cta + hh) * 2;
-    if (ml[1] > 0.0f) M = fmaxf(M, ml[0]);
+    const int u = (j - tid) / kCombineThreads;
+    float m, l;
+    if (u < 2) { m = mlm[u]; l = mll[u]; }
+    else {
+      const float2 ml = *reinterpret_cast<const float2*>(a.ws_ml + ((base + slot_of(j)) * a.heads_per_cta + hh) * 2);
+      m = ml.x; l = ml.y;
+    }
+    if (l > 0.0f) M = fmaxf(M, m);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
@@ -1205,9 +1277,14 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(Combine
   // 2. weights and L = sum of l_s * weight
   float L = 0.0f;
   for (int j = tid; j < splits; j += kCombineThreads) {
-    const float* ml = a.ws_ml + ((base + slot_of(j)) * a.heads_per_cta + hh) * 2;
-    const float l = ml[1];
-    const float w = l > 0.0f ? exp2f(ml[0] - M) : 0.0f;
+    const int u = (j - tid) / kCombineThreads;
+    float m, l;
+    if (u < 2) { m = mlm[u]; l = mll[u]; }
+    else {
+      const float2 ml = *reinterpret_cast<const float2*>(a.ws_ml + ((base + slot_of(j)) * a.heads_per_cta + hh) * 2);
+      m = ml.x; l = ml.y;
+    }
+    const float w = l > 0.0f ? exp2f(m - M) : 0.0f;
     s_w[j] = w;
     L += l * w;
   }
@@ -1218,23 +1295,25 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(Combine
   L = 0.0f;
 #pragma unroll
   for (int w = 0; w < kCombineThreads / 32; ++w) L += s_red[1][w];
-  // 3. channel c of this thread, slots sub, sub + TPC, ...
-  const int c = tid % D, sub = tid / D;
+  // 3. the weighted sum of this thread's partials
   float v = 0.0f;
-  if (tid < D * TPC) {
-    // 8 partials in flight per thread.  A slot whose sub-range was empty holds only its
-    // (m, l) = (-inf, 0); its acc row is whatever an earlier call left there, so it is
-    // read but selected away by its weight 0 and must never be multiplied.
-    for (int s0 = sub; s0 < splits; s0 += 8 * TPC) {
-      float x[8], wv[8];
+  if (has_ch) {
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < kAhead; ++u) {
+      const int j = sub + u * TPC;
+      const float wv = j < splits ? s_w[j] : 0.0f;
+      v += wv != 0.0f ? wv * xa[u] : 0.0f;
+    }
+    for (int s0 = sub + kAhead * TPC; s0 < splits; s0 += kAhead * TPC) {
+      float y[kAhead], wv[kAhead];
+#pragma unroll
+      for (int u = 0; u < kAhead; ++u) {
         const int j = s0 + u * TPC;
         wv[u] = j < splits ? s_w[j] : 0.0f;
-        x[u] = j < splits ? a.ws_acc[((base + slot_of(j)) * a.heads_per_cta + hh) * D + c] : 0.0f;
+        y[u] = j < splits ? a.ws_acc[((base + slot_of(j)) * a.heads_per_cta + hh) * D + c] : 0.0f;
       }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) v += wv[u] != 0.0f ? wv[u] * x[u] : 0.0f;
+      for (int u = 0; u < kAhead; ++u) v += wv[u] != 0.0f ? wv[u] * y[u] : 0.0f;
     }
   }
   s_part[tid] = v;
@@ -1362,6 +1441,7 @@ cudaError_t run_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, cons
   p.pieces = fa ? plan.pieces_fused : plan.pieces;
   p.slots = plan.slots;
   p.cost_body = plan.cost_body; p.cost_tail = plan.cost_tail; p.cost_min = plan.cost_min;
+  p.cost_gap = plan.cost_gap;
   p.sms = plan.sms;
   const bool wave = fa ? plan.weighted_fused : plan.weighted;
   for (int k = 0; k < 3; ++k) p.wt[k] = wave ? plan.slot_weight[k] : 0;
@@ -1390,18 +1470,23 @@ cudaError_t run_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, cons
   ca.group = p.group; ca.batch = c.batch; ca.tail_len = c.tail_len; ca.fused = p.fused; ca.rot_v = rot.v;
   ca.out_dtype = out_dtype; ca.n_q_heads = n_q_heads;
   ca.cost_body = plan.cost_body; ca.cost_tail = plan.cost_tail; ca.cost_min = plan.cost_min;
+  ca.cost_gap = plan.cost_gap;
   ca.pieces = p.pieces; ca.planes = plan.planes; ca.sms = plan.sms;
   for (int k = 0; k < 3; ++k) ca.wt[k] = p.wt[k];
   ca.out = out; ca.seq_len = c.seq_len; ca.oidx = c.outlier_idx;
+  // a row merges many partials when the batch is small: 512 threads keep them all in flight;
+  // with many rows, 256-thread CTAs fit twice as many rows on the GPU at once
+  const bool wide = (long long)c.batch * n_q_heads <= 2LL * plan.sms;
+  auto ckern = wide ? decode_combine_kernel<D, OL, 512> : decode_combine_kernel<D, OL, 256>;
   const size_t wbytes = (size_t)plan.slots * sizeof(float);
   if (wbytes > 48 * 1024) {
-    e = ensure_dynamic_smem(reinterpret_cast<const void*>(decode_combine_kernel<D, OL>), (int)wbytes);
+    e = ensure_dynamic_smem(reinterpret_cast<const void*>(ckern), (int)wbytes);
     if (e != cudaSuccess) return e;
   }
   // programmatic dependent launch: the merge grid's launch overlaps the split grid's end
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(c.batch * n_q_heads);
-  cfg.blockDim = dim3(kCombineThreads);
+  cfg.blockDim = dim3(wide ? 512 : 256);
   cfg.dynamicSmemBytes = wbytes;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -1409,7 +1494,7 @@ cudaError_t run_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, cons
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, OL>, ca);
+  return cudaLaunchKernelEx(&cfg, ckern, ca);
 }
 
 template <int D>

@@ -69,6 +69,7 @@ struct DecodePlan {
   long long cost_body; // bytes of one body token of one (sequence, KV head)
   long long cost_tail; // bytes of one tail token
   long long cost_min;  // smallest piece
+  long long cost_gap;  // virtual bytes before each segment: a CTA's cost of switching segments
   int sms;             // SMs the plan fills
   // With one full wave of three CTAs per SM the pieces are weighted by dispatch slot
   // (an SM's first, second, third CTA), so that the SM's CTAs end together.
