@@ -486,15 +486,15 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
           const long long c = is_tail ? p.cost_tail : p.cost_body;
           const long long cs = (long long)ntok * c;
           if (cs > 0) {
-            const long long D = Pseg + p.cost_gap;  // the segment's data starts after its gap
-            if (D < x1 && D + cs > x0) {
+            const long long dstart = Pseg + p.cost_gap;  // the segment's data starts after its gap
+            if (dstart < x1 && dstart + cs > x0) {
               use = true;
               const int tile = is_tail ? C::TT : 16;
-              t_begin = seg_token(x0, D, c, ntok, tile);
-              t_end = seg_token(x1, D, c, ntok, tile);
+              t_begin = seg_token(x0, dstart, c, ntok, tile);
+              t_end = seg_token(x1, dstart, c, ntok, tile);
               slot = p.fused ? B + int(piece) + b : int(piece) + 2 * b + kind;
             }
-            Pseg = D + cs;
+            Pseg = dstart + cs;
           }
           if (p.fused || kind == 1) { kind = p.fused ? 1 : 0; ++sb; } else { kind = 1; }
           if (Pseg >= x1) sb = B;
