@@ -97,7 +97,7 @@ def recorded_traffic(kernel_file: str):
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,utilization.gpu")
 
     def __init__(self, gpu_index: int):
         self.proc = None
@@ -122,23 +122,31 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.f.close()
-        sm, mx, reasons = [], [], set()
+        sm, mx, loaded, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
+                clk, cmax = float(parts[1]), float(parts[2])
             except ValueError:
                 continue
+            sm.append(clk)
+            mx.append(cmax)
+            try:
+                util = float(parts[9]) if len(parts) > 9 else None
+            except ValueError:
+                util = None
+            if util is not None and util >= 50.0:  # a sample taken while the GPU ran our kernels
+                loaded.append(clk)
             for nm, val in zip(names, parts[5:9]):
                 if val.lower().startswith("active"):
                     reasons.add(nm)
         os.unlink(self.path)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        pick = loaded if loaded else sm
+        return {"sm_mhz": statistics.median(pick) if pick else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm), "samples_under_load": len(loaded)}
 
 
 # ---------------------------------------------------------------------------
@@ -253,8 +261,19 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    clk = clocks.stop()
     step_ms = e0.elapsed_time(e1) / K
+    # keep the GPU under the same decode load for a while longer, so that the clock
+    # samples (every 100 ms) are taken under load; the metric is not timed here
+    t_load = time.perf_counter()
+    n_load = 0
+    while time.perf_counter() - t_load < args.load_s:
+        for _ in range(50):
+            kvq.kvq_decode_attention(cache.desc, qs[n_load % P], out, ws, stream=stream)
+            n_load += 1
+        torch.cuda.synchronize()
+    clk = clocks.stop()
+    clk["load_s"] = round(time.perf_counter() - t_load, 2)
+    clk["load_calls"] = n_load
     st, bits = kvq.kvq_sync_status(cache.desc)
     assert st == 0, (st, bits)
     total_bytes = 0
@@ -399,7 +418,7 @@ def run_ours(args):
             "config": {"workload": w.name, "batch": w.batch, "ctx": w.ctx, "q_heads": w.n_q_heads,
                        "kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "k_type": w.k_type, "v_type": w.v_type,
                        "tail_len": w.tail_len, "append_per_step": n_new,
-                       "l2": f"inputs larger than L2 ({per_step_bytes / 1e6:.1f} MB per step), no flush",
+                       "l2": config_l2_note(w),
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "roofline": {"bound": "hbm", "kernel": "decode (split-K + combine) at ctx "
                          f"{int(dec_lens.max())}", "achieved": round(achieved, 1), "peak": peak,
@@ -421,6 +440,8 @@ def run_ours(args):
             "step_call": "kvq_append_decode" + (" (append fused into the decode launch)" if fused else ""),
             "clocks": clk,
         }
+        if not args.no_configs:
+            line["configs"] = run_config_legs(torch, kvq, peak)
         if not args.no_prefill:
             line["prefill"] = run_prefill_bench(torch, kvq, max(5, K // 5), 3)
         if not args.no_format_pairs:
@@ -436,6 +457,111 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def config_l2_note(w: wl.Workload) -> str:
+    """How the timed region keeps the cache out of L2 (same words for both arms)."""
+    return "inputs larger than L2 (446 MB per step), no flush" if w.name == wl.HEADLINE else \
+        "L2 flushed (256 MB written) before each timed call when the call's bytes fit in L2"
+
+
+# ---------------------------------------------------------------------------
+# the other decode workloads: decode call alone, per-call device time
+# ---------------------------------------------------------------------------
+CONFIG_LEGS = ("decode_d64_ctx256", "decode_gqa16x8_ctx4k", "decode_b32_ragged8k")
+
+
+def fill_cache_ragged(torch, kvq, cache, w: wl.Workload, lens, seed: int = 0):
+    """Seeded synthetic history (as fill_cache) appended to each sequence up to its own
+    length, through the library's write path (per-sequence counts)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    k_chan = wl.outlier_channels(rng, w.n_kv_heads, w.head_dim, w.n_outliers)
+    v_chan = wl.outlier_channels(rng, w.n_kv_heads, w.head_dim, w.n_outliers)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    kmask = torch.ones(w.n_kv_heads, w.head_dim, device="cuda")
+    vmask = torch.ones(w.n_kv_heads, w.head_dim, device="cuda")
+    for h in range(w.n_kv_heads):
+        kmask[h, torch.tensor(k_chan[h])] = 20.0
+        vmask[h, torch.tensor(v_chan[h])] = 20.0
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    lens = np.asarray(lens, dtype=np.int64)
+    chunk, done = 8192, 0
+    while done < int(lens.max()):
+        n = min(chunk, int(lens.max()) - done)
+        per = torch.tensor(np.clip(lens - done, 0, n), dtype=torch.int32, device="cuda")
+        k = (torch.randn(w.batch, n, w.n_kv_heads, w.head_dim, generator=gen, device="cuda") * kmask).to(dt)
+        v = (torch.randn(w.batch, n, w.n_kv_heads, w.head_dim, generator=gen, device="cuda") * vmask).to(dt)
+        kvq.kvq_rotate_quantize_append(cache.desc, k, v, n_new_per_seq=per)
+        done += n
+    torch.cuda.synchronize()
+    st, bits = kvq.kvq_sync_status(cache.desc)
+    assert st == 0, (st, bits)
+    assert np.array_equal(cache.seq_len.cpu().numpy(), lens)
+    return gen
+
+
+def run_config_legs(torch, kvq, peak: float, iters: int = 40):
+    """The decode call alone on the other workloads, each at its own shapes, formats,
+    dtypes and (ragged) lengths.  Calls whose bytes fit in L2 are timed one by one with
+    L2 flushed (a 256 MB buffer written) before each; larger ones back to back."""
+    res = []
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    for name in CONFIG_LEGS:
+        w = wl.WORKLOADS[name]
+        rng = np.random.Generator(np.random.PCG64(0))
+        if w.ragged_min is not None:
+            lens = rng.integers(w.ragged_min, w.ctx + 1, size=w.batch).astype(np.int64)
+        else:
+            lens = np.full(w.batch, w.ctx, dtype=np.int64)
+        cache = kvq.KVCache(w.batch, w.n_kv_heads, w.head_dim, w.max_ctx(64), w.tail_len, w.k_type, w.v_type)
+        gen = fill_cache_ragged(torch, kvq, cache, w, lens)
+        dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+        qs = [torch.randn(w.batch, w.n_q_heads, w.head_dim, generator=gen, device="cuda").to(dt) for _ in range(4)]
+        out = torch.empty(w.batch, w.n_q_heads, w.head_dim, dtype=dt, device="cuda")
+        ws = torch.empty(kvq.kvq_decode_workspace_bytes(cache.desc, w.n_q_heads), dtype=torch.uint8, device="cuda")
+        esz = 2 if w.dtype == "bf16" else 4
+        nbytes = decode_bytes(w, lens, q_bytes=esz, out_bytes=esz)
+        fits = nbytes < 100e6
+        for i in range(3):
+            kvq.kvq_decode_attention(cache.desc, qs[i % 4], out, ws, stream=stream)
+        torch.cuda.synchronize()
+        times = []
+        if fits:
+            for i in range(iters):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                kvq.kvq_decode_attention(cache.desc, qs[i % 4], out, ws, stream=stream)
+                e1.record(stream)
+                e1.synchronize()
+                times.append(e0.elapsed_time(e1))
+            ms = statistics.median(times)
+        else:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(iters):
+                kvq.kvq_decode_attention(cache.desc, qs[i % 4], out, ws, stream=stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / iters
+        st, bits = kvq.kvq_sync_status(cache.desc)
+        assert st == 0, (st, bits)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res.append({"workload": name, "batch": w.batch, "ctx": w.ctx,
+                    "lengths": "uniform %d..%d (seed 0), total %d" % (w.ragged_min, w.ctx, int(lens.sum()))
+                    if w.ragged_min is not None else "all %d" % w.ctx,
+                    "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads, "head_dim": w.head_dim,
+                    "k_type": w.k_type, "v_type": w.v_type, "tail_len": w.tail_len, "q_dtype": w.dtype,
+                    "ms_per_call": round(ms, 5), "bytes_per_call": int(nbytes), "gbs": round(gbs, 1),
+                    "frac": round(gbs / peak, 4),
+                    "l2": "flushed before each call (bytes fit in L2)" if fits else "larger than L2, back to back"})
+        del cache, ws, qs, out
+        torch.cuda.empty_cache()
+    del flush
+    torch.cuda.empty_cache()
+    return res
 
 
 # ---------------------------------------------------------------------------
@@ -683,7 +809,9 @@ def run_reference(args):
             "data": "synthetic", "config": {"workload": w.name, "batch": w.batch, "ctx": w.ctx,
                                             "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads,
                                             "head_dim": w.head_dim, "k_type": w.k_type, "v_type": w.v_type,
-                                            "tail_len": w.tail_len},
+                                            "tail_len": w.tail_len, "append_per_step": max(1, w.append_per_step),
+                                            "l2": config_l2_note(w),
+                                            "parallelism": "single GPU"},
             "cpu_baseline": {"value": val, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -705,6 +833,11 @@ def main():
     ap.add_argument("--no-format-pairs", action="store_true",
                     help="skip the decode measurement with the q4_1 / q5_1 format pairs")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the decode measurement of the other workloads (d=64 ctx 256, GQA 16/8 ctx 4k, "
+                         "ragged batch of 32)")
+    ap.add_argument("--load-s", type=float, default=1.2,
+                    help="seconds of extra decode load inside the clock-sampling window")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -69,9 +69,10 @@ def test_clock_sampler_parses_clocks_and_throttle_reasons(tmp_path):
     cs = bench.ClockSampler(0)
     cs.path = str(tmp_path / "clocks.csv")
     rows = [
-        "0, 2070, 2070, 900.1, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
-        "0, 1980, 2070, 1350.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
-        "0, 2070, 2070, 1000.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "0, 2070, 2070, 900.1, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active, 0",
+        "0, 1980, 2070, 1350.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active, 100",
+        "0, 2070, 2070, 1000.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active, 97",
+        "0, 1950, 2070, 1380.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active, 100",
         "garbage line",
     ]
     with open(cs.path, "w") as f:
@@ -79,7 +80,9 @@ def test_clock_sampler_parses_clocks_and_throttle_reasons(tmp_path):
     cs.f = open(cs.path, "a")
     cs.proc = _Proc()
     r = cs.stop()
-    assert r["sm_mhz"] == 2070.0 and r["sm_max_mhz"] == 2070.0 and r["samples"] == 3
+    # the median SM clock is that of the samples taken under load (utilization >= 50%)
+    assert r["sm_mhz"] == 1980.0 and r["sm_max_mhz"] == 2070.0 and r["samples"] == 4
+    assert r["samples_under_load"] == 3
     assert r["reasons"] == ["sw_power_cap"]
     # without nvidia-smi the line says so instead of inventing clocks
     none = bench.ClockSampler(0)
