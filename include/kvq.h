@@ -254,16 +254,22 @@ KVQ_API kvq_status kvq_decode_attention(const kvq_cache* c, const void* q, int32
  * The split partials go to one scratch array of KVQ_NOALLOC_SCRATCH_BYTES
  * that the library defines statically in device memory: every GPU that loads
  * the library holds it until the process exits.  The call allocates nothing
- * (no cudaMalloc, no allocating library routine).  The first call on each
- * device looks up the array's device address (cudaGetSymbolAddress) with
- * that device current; make that first call before any stream capture.
+ * (no cudaMalloc, no allocating library routine).  Every call looks up the
+ * array's device address (cudaGetSymbolAddress, a host-side lookup that
+ * allocates nothing) with the caller's device current, so a call after a
+ * reset of that device's context finds the array wherever it now lives.  The
+ * first call in a process may load the library's device code: make it
+ * before any stream capture.
  * Arguments, results and errors are those of kvq_decode_attention, except:
  * KVQ_ERR_WORKSPACE when kvq_decode_workspace_bytes(c, n_q_heads) exceeds
  * KVQ_NOALLOC_SCRATCH_BYTES (nothing is launched then).  All calls share the
- * one array and it keeps the last call's contents; every call writes all
- * scratch it reads, so nothing needs clearing.  Calls that overlap on the
- * GPU (for example on two streams at once) race on the array and must not
- * be issued.
+ * one array and it keeps the last call's contents.  A call writes the
+ * partition header and every (m, l) pair its merge reads; the partial rows of
+ * a split whose token range came out empty are not written and may hold an
+ * earlier call's values (even Inf or NaN): the merge reads them but drops them
+ * by their weight 0, never multiplying them.  Calls that overlap on the GPU
+ * (for example on two streams at once) race on the array and must not be
+ * issued.
  */
 #define KVQ_NOALLOC_SCRATCH_BYTES (16u << 20)
 KVQ_API kvq_status kvq_decode_attention_noalloc(const kvq_cache* c, const void* q, int32_t q_dtype,

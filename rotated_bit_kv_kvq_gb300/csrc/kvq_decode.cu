@@ -3,7 +3,6 @@
 // (compiled once per head_dim in kvq_decode_d*.cu).
 
 #include <algorithm>
-#include <mutex>
 
 #include "kvq_decode_impl.cuh"
 
@@ -19,21 +18,13 @@ static __device__ __align__(256) unsigned char g_decode_scratch[KVQ_NOALLOC_SCRA
 }  // namespace
 
 cudaError_t decode_noalloc_scratch(void** ptr, size_t* bytes) {
-  constexpr int kMaxDevices = 64;
-  static std::mutex mu;
-  static void* addr[kMaxDevices] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  // Looked up on every call with the caller's device current: a host-side lookup that
+  // allocates nothing, and that follows the array if the device's context was reset and
+  // the module reloaded at another address since an earlier call.
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {  // once per device, with that device current
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_decode_scratch);
-    if (e != cudaSuccess) return e;
-    addr[dev] = p;
-  }
-  *ptr = addr[dev];
+  *ptr = p;
   *bytes = sizeof(g_decode_scratch);
   return cudaSuccess;
 }

@@ -30,11 +30,14 @@ def test_library_exports_every_declared_symbol(built_lib_path):
 
 
 def _header_defines():
-    """Integer #defines of include/kvq.h (name -> value)."""
+    """Integer #defines of include/kvq.h (name -> value): plain integers and
+    shifted ones of the form (Nu << M)."""
     src = open(os.path.join(ROOT, "include", "kvq.h")).read()
     out = {}
     for name, val in re.findall(r"^#define\s+(KVQ_[A-Z0-9_]+)\s+(-?\d+)u?\b", src, flags=re.M):
         out[name] = int(val)
+    for name, a, sh in re.findall(r"^#define\s+(KVQ_[A-Z0-9_]+)\s+\(\s*(\d+)u?\s*<<\s*(\d+)\s*\)", src, flags=re.M):
+        out[name] = int(a) << int(sh)
     return out
 
 
@@ -46,6 +49,8 @@ def test_binding_constants_match_header():
     assert len(mirrored) >= 30, sorted(set(defs) - set(mirrored))
     for n in mirrored:
         assert getattr(kvq, n) == defs[n], n
+    # the scratch size of the allocation-free entry point is written as a shift
+    assert defs["KVQ_NOALLOC_SCRATCH_BYTES"] == kvq.KVQ_NOALLOC_SCRATCH_BYTES == 16 << 20
     # the binding's kvq_cache has the header's fields in the header's order
     src = open(os.path.join(ROOT, "include", "kvq.h")).read()
     body = re.search(r"typedef struct kvq_cache \{(.*?)\} kvq_cache;", src, flags=re.S).group(1)
