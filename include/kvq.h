@@ -201,7 +201,12 @@ KVQ_API kvq_status kvq_cache_check(const kvq_cache* c);
 KVQ_API kvq_status kvq_resolve_rotation(const kvq_cache* c, int32_t* rot_k, int32_t* rot_v);
 
 /*
- * Rotate, quantize and append new tokens (write path).
+ * Rotate, quantize and append new tokens (write path).  The rotation is
+ * applied where the cache is stored, so the stored K and V are rotated (velog
+ * "fix-kv-cache-quantization-outliers", section 아다마르 회전); the blocks are
+ * the GGUF formats, unchanged (section 적용 및 배경 기술); the most recent
+ * tokens also stay in bf16 (aitrends.kr "KVarN과 Precision Tail", section
+ * 용어 해설).
  *   k, v          device [batch][n_new][n_kv_heads][head_dim] of in_dtype
  *   n_new         rows per sequence in k / v (>= 0; 0 is a no-op; batch * n_new *
  *                 n_kv_heads * 2 must stay below 2^31, else KVQ_ERR_INVALID_ARG)
@@ -227,7 +232,12 @@ KVQ_API kvq_status kvq_rotate_quantize_append(const kvq_cache* c, const void* k,
 KVQ_API size_t kvq_decode_workspace_bytes(const kvq_cache* c, int32_t n_q_heads);
 
 /*
- * One decode step of attention for every sequence (read path).
+ * One decode step of attention for every sequence (read path).  The query is
+ * rotated like the keys, the scores are the rotated dot products, and the
+ * weighted sum of the rotated values is rotated back (velog
+ * "fix-kv-cache-quantization-outliers", section 아다마르 회전); the latest
+ * tail_len tokens are read from the bf16 tail (aitrends.kr "KVarN과 Precision
+ * Tail", section 용어 해설).
  *   q      device [batch][n_q_heads][head_dim] of q_dtype (unrotated)
  *   out    device [batch][n_q_heads][head_dim] of out_dtype (original basis)
  *   scale  softmax scale; 0 means 1/sqrt(head_dim)
@@ -306,7 +316,11 @@ KVQ_API size_t kvq_prefill_workspace_bytes(const kvq_cache* c, int32_t n_q_heads
 
 /*
  * Chunked attention of a block of queries per sequence over the cache
- * (prompt processing), after their K/V have been appended.
+ * (prompt processing), after their K/V have been appended: the prompt-side
+ * use of the same rotated cache (velog "fix-kv-cache-quantization-outliers",
+ * section 트레이드오프, reports its cost apart from token generation), with
+ * the bf16 tail as in decode (aitrends.kr "KVarN과 Precision Tail", section
+ * 용어 해설).
  *   q       device [batch][n_tokens][n_q_heads][head_dim] of q_dtype
  *   q_pos0  device int32 [batch] or NULL: absolute position of query 0 of
  *           sequence b; NULL means seq_len[b] - n_tokens (the just-appended
@@ -329,7 +343,10 @@ KVQ_API kvq_status kvq_prefill_attention(const kvq_cache* c, const void* q, int3
                                  void* stream);
 
 /*
- * Inspection of stored tokens (test aid).
+ * Inspection of stored tokens (test aid): the stored blocks in the GGUF
+ * array-of-structs byte order, which rotation leaves unchanged (velog
+ * "fix-kv-cache-quantization-outliers", section 적용 및 배경 기술), and their
+ * dequantized values, optionally rotated back (section 아다마르 회전).
  *   which          0 = K body, 1 = V body, 2 = K tail, 3 = V tail
  *   t0, count      positions [t0, t0+count) of (seq, kv_head); body positions
  *                  must lie below max_ctx; tail reads slot p % tail_len

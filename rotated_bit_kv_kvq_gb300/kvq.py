@@ -233,6 +233,22 @@ def kvq_resolve_rotation(cache: kvq_cache):
     return st, rk.value, rv.value
 
 
+def default_flags(env=None) -> int:
+    """Cache flags when the caller gives none: the automatic enable rule, with K and
+    V rotation switched off by the environment variables KVQ_ROT_K_DISABLE /
+    KVQ_ROT_V_DISABLE (any value other than empty or "0"), as the patch's own
+    per-side switches allow (velog "fix-kv-cache-quantization-outliers", section
+    적용 및 배경 기술)."""
+    env = os.environ if env is None else env
+    on = lambda name: env.get(name, "") not in ("", "0")
+    f = KVQ_ROT_AUTO
+    if on("KVQ_ROT_K_DISABLE"):
+        f |= KVQ_ROT_K_OFF
+    if on("KVQ_ROT_V_DISABLE"):
+        f |= KVQ_ROT_V_OFF
+    return f
+
+
 def descriptor(batch, n_kv_heads, head_dim, max_ctx, tail_len, k_type, v_type, flags=KVQ_ROT_AUTO,
                page_tokens=0, n_pages=0, n_outlier=0) -> kvq_cache:
     """A descriptor with sizes and types only (pointers NULL)."""
@@ -250,13 +266,16 @@ class KVCache:
     """The planes of one cache, allocated with torch on the current device."""
 
     def __init__(self, batch, n_kv_heads, head_dim, max_ctx, tail_len, k_type, v_type,
-                 flags=KVQ_ROT_AUTO, device="cuda", page_tokens=0, n_pages=0, page_table=None,
+                 flags=None, device="cuda", page_tokens=0, n_pages=0, page_table=None,
                  outliers=None):
-        """page_tokens > 0: paged body planes, a pool of n_pages pages (default: batch *
+        """flags None: default_flags() (the automatic rule, unless the environment
+        switches K or V rotation off).  page_tokens > 0: paged body planes, a pool of n_pages pages (default: batch *
         max_ctx / page_tokens) and a page table (device int32 [batch][max_ctx / page_tokens];
         default: sequence b owns pages b * per_seq ...).  outliers: int [n_kv_heads][32],
         each row the strictly increasing channels kept at 8 bits (None: off)."""
         import torch
+        if flags is None:
+            flags = default_flags()
         if page_tokens and not n_pages:
             n_pages = batch * (max_ctx // page_tokens)
         n_outlier = 0 if outliers is None else len(outliers[0])

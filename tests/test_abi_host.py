@@ -249,3 +249,17 @@ def test_selftest_wait_timeout_argument_checks(built_lib_path):
     assert L.kvq_selftest_wait_timeout(None, 1000, None) == kvq.KVQ_ERR_INVALID_ARG
     c.status = FAKE + 4
     assert L.kvq_selftest_wait_timeout(ctypes.byref(c), 1000, None) == kvq.KVQ_ERR_INVALID_ARG
+
+
+def test_rotation_switches_from_the_environment(built_lib_path):
+    """KVQ_ROT_K_DISABLE / KVQ_ROT_V_DISABLE switch each side off in the default flags;
+    the enable rule then reports that side off (and leaves the other on)."""
+    assert kvq.default_flags({}) == kvq.KVQ_ROT_AUTO
+    assert kvq.default_flags({"KVQ_ROT_K_DISABLE": "0", "KVQ_ROT_V_DISABLE": ""}) == kvq.KVQ_ROT_AUTO
+    fk = kvq.default_flags({"KVQ_ROT_K_DISABLE": "1"})
+    fv = kvq.default_flags({"KVQ_ROT_V_DISABLE": "yes"})
+    fb = kvq.default_flags({"KVQ_ROT_K_DISABLE": "1", "KVQ_ROT_V_DISABLE": "1"})
+    assert fk == kvq.KVQ_ROT_AUTO | kvq.KVQ_ROT_K_OFF and fv == kvq.KVQ_ROT_AUTO | kvq.KVQ_ROT_V_OFF
+    for f, want in ((kvq.default_flags({}), (1, 1)), (fk, (0, 1)), (fv, (1, 0)), (fb, (0, 0))):
+        st, rk, rv = kvq.kvq_resolve_rotation(kvq.descriptor(1, 1, 128, 64, 0, "q4_0", "q4_0", flags=f))
+        assert st == 0 and (rk, rv) == want, (f, rk, rv)
