@@ -119,14 +119,15 @@ typedef int32_t kvq_status;
  * payload; kvq_dequant_debug can export them in GGUF array-of-structs order.
  *
  * Requirements (checked by every call): head_dim % 32 == 0 and
- * 32 <= head_dim <= 256; max_ctx % 64 == 0 and max_ctx <= 2^30; tail_len >= 0;
+ * 32 <= head_dim <= 512; max_ctx % 64 == 0 and max_ctx <= 2^30; tail_len >= 0;
  * every non-NULL plane 16-byte aligned; k_qh / v_qh non-NULL only for q5_0 and
  * q5_1 (required then);
  * k_tail / v_tail non-NULL iff tail_len > 0.  Decode supports head_dim in
- * {64, 128, 256} (plus 192 for q4_0/q4_0); prefill supports head_dim 64 and
- * 128 with up to 128 query heads per KV head; append and debug support every
- * multiple of 32 up to 256.  Prefill stores keys and values internally as
- * fp16 x 2^-8, so it needs |rotated value| < 1.6e7.
+ * {64, 128, 192, 256, 320} for every K / V format pair (192 and 320 rotate in
+ * 64-wide blocks; with outlier channels: 64, 128, 256); prefill supports
+ * head_dim 64 and 128 with up to 128 query heads per KV head; append and debug
+ * support every multiple of 32 up to 512.  Prefill stores keys and values
+ * internally as fp16 x 2^-8, so it needs |rotated value| < 1.6e7.
  */
 typedef struct kvq_cache {
   int32_t batch;        /* sequences                                   */

@@ -21,7 +21,7 @@ bool valid_dtype(int t) { return t == KVQ_F32 || t == KVQ_BF16 || t == KVQ_F16; 
 bool shape_ok(const kvq_cache* c) {
   if (!c) return false;
   if (c->batch <= 0 || c->batch > 65535 || c->n_kv_heads <= 0 || c->n_kv_heads > 4096) return false;
-  if (c->head_dim < 32 || c->head_dim > 256 || c->head_dim % 32) return false;
+  if (c->head_dim < 32 || c->head_dim > 512 || c->head_dim % 32) return false;
   // positions, chunk ends and seq_len + n_new stay below 2^31 in the kernels' int arithmetic
   if (c->max_ctx <= 0 || c->max_ctx % 64 || c->max_ctx > (1 << 30)) return false;
   if (c->tail_len < 0 || c->tail_len > (1 << 24)) return false;

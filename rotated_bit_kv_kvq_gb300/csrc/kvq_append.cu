@@ -460,6 +460,14 @@ cudaError_t launch_append(const kvq_cache& c, Rot rot, const void* k, const void
     case 192: return append_d<192>(c, rot, k, v, in_dtype, n_new, nps, flags, st);
     case 224: return append_d<224>(c, rot, k, v, in_dtype, n_new, nps, flags, st);
     case 256: return append_d<256>(c, rot, k, v, in_dtype, n_new, nps, flags, st);
+    case 288: return append_d<288>(c, rot, k, v, in_dtype, n_new, nps, flags, st);
+    case 320: return append_d<320>(c, rot, k, v, in_dtype, n_new, nps, flags, st);
+    case 352: return append_d<352>(c, rot, k, v, in_dtype, n_new, nps, flags, st);
+    case 384: return append_d<384>(c, rot, k, v, in_dtype, n_new, nps, flags, st);
+    case 416: return append_d<416>(c, rot, k, v, in_dtype, n_new, nps, flags, st);
+    case 448: return append_d<448>(c, rot, k, v, in_dtype, n_new, nps, flags, st);
+    case 480: return append_d<480>(c, rot, k, v, in_dtype, n_new, nps, flags, st);
+    case 512: return append_d<512>(c, rot, k, v, in_dtype, n_new, nps, flags, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -475,6 +483,14 @@ cudaError_t launch_debug(const kvq_cache& c, Rot rot, int seq, int kv_head, int 
     case 192: return debug_d<192>(c, rot, seq, kv_head, which, t0, count, original_basis, out, blocks, st);
     case 224: return debug_d<224>(c, rot, seq, kv_head, which, t0, count, original_basis, out, blocks, st);
     case 256: return debug_d<256>(c, rot, seq, kv_head, which, t0, count, original_basis, out, blocks, st);
+    case 288: return debug_d<288>(c, rot, seq, kv_head, which, t0, count, original_basis, out, blocks, st);
+    case 320: return debug_d<320>(c, rot, seq, kv_head, which, t0, count, original_basis, out, blocks, st);
+    case 352: return debug_d<352>(c, rot, seq, kv_head, which, t0, count, original_basis, out, blocks, st);
+    case 384: return debug_d<384>(c, rot, seq, kv_head, which, t0, count, original_basis, out, blocks, st);
+    case 416: return debug_d<416>(c, rot, seq, kv_head, which, t0, count, original_basis, out, blocks, st);
+    case 448: return debug_d<448>(c, rot, seq, kv_head, which, t0, count, original_basis, out, blocks, st);
+    case 480: return debug_d<480>(c, rot, seq, kv_head, which, t0, count, original_basis, out, blocks, st);
+    case 512: return debug_d<512>(c, rot, seq, kv_head, which, t0, count, original_basis, out, blocks, st);
     default: return cudaErrorInvalidValue;
   }
 }

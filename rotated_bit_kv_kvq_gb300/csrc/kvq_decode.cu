@@ -51,8 +51,7 @@ cudaError_t launch_wait_timeout(uint32_t* status, long long limit_cycles, cudaSt
 bool decode_supported(int d, int kt, int vt, int n_outlier) {
   if (n_outlier)
     return (d == 64 || d == 128 || d == 256) && kt <= KVQ_TYPE_Q8_0 && vt <= KVQ_TYPE_Q8_0 && n_outlier == 32;
-  if (d == 64 || d == 128 || d == 256) return true;  // every K / V format pair
-  return d == 192 && kt == KVQ_TYPE_Q4_0 && vt == KVQ_TYPE_Q4_0;
+  return d == 64 || d == 128 || d == 192 || d == 256 || d == 320;  // every K / V format pair
 }
 
 DecodePlan plan_decode(const kvq_cache& c, int n_q_heads, int sm_count) {
@@ -113,6 +112,7 @@ cudaError_t launch_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, c
     case 128: return launch_decode_d128(c, rot, plan, q, q_dtype, n_q_heads, scale, out, out_dtype, ws, st, fa);
     case 256: return launch_decode_d256(c, rot, plan, q, q_dtype, n_q_heads, scale, out, out_dtype, ws, st, fa);
     case 192: return launch_decode_d192(c, rot, plan, q, q_dtype, n_q_heads, scale, out, out_dtype, ws, st, fa);
+    case 320: return launch_decode_d320(c, rot, plan, q, q_dtype, n_q_heads, scale, out, out_dtype, ws, st, fa);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -47,7 +47,8 @@ constexpr int kSmemBudget = 64 * 1024;       // stages; leaves room for 3 CTAs p
 constexpr int kCtasPerSm = 3;
 // Outlier-channel kernels at head_dim 256 run 2 CTAs per SM: at 3 the extra
 // block's registers spill inside the tile loop.
-constexpr int ctas_per_sm(int d, bool outl) { return outl && d >= 256 ? 2 : kCtasPerSm; }
+// Above head_dim 256 the accumulators alone take 80+ registers: 2 CTAs per SM as well.
+constexpr int ctas_per_sm(int d, bool outl) { return (outl && d >= 256) || d > 256 ? 2 : kCtasPerSm; }
 
 constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 // widest TMA swizzle box (128, 64 or 32 bytes) that tiles a row exactly
@@ -1508,9 +1509,13 @@ cudaError_t run_decode_d(const kvq_cache& c, Rot rot, const DecodePlan& plan, co
                         KVQ_CASE(KT, KVQ_TYPE_Q5_1, false)
 #define KVQ_CASES_K_OL(KT) KVQ_CASE(KT, KVQ_TYPE_Q4_0, true) KVQ_CASE(KT, KVQ_TYPE_Q5_0, true) \
                            KVQ_CASE(KT, KVQ_TYPE_Q8_0, true)
-  if (c.n_outlier) {  // outlier channels: the q4_0 / q5_0 / q8_0 pairs
-    KVQ_CASES_K_OL(KVQ_TYPE_Q4_0) KVQ_CASES_K_OL(KVQ_TYPE_Q5_0) KVQ_CASES_K_OL(KVQ_TYPE_Q8_0)
-    return cudaErrorInvalidValue;
+  if constexpr (D == 64 || D == 128 || D == 256) {
+    if (c.n_outlier) {  // outlier channels: the q4_0 / q5_0 / q8_0 pairs
+      KVQ_CASES_K_OL(KVQ_TYPE_Q4_0) KVQ_CASES_K_OL(KVQ_TYPE_Q5_0) KVQ_CASES_K_OL(KVQ_TYPE_Q8_0)
+      return cudaErrorInvalidValue;
+    }
+  } else {
+    if (c.n_outlier) return cudaErrorInvalidValue;
   }
   KVQ_CASES_K(KVQ_TYPE_Q4_0) KVQ_CASES_K(KVQ_TYPE_Q5_0) KVQ_CASES_K(KVQ_TYPE_Q8_0)
   KVQ_CASES_K(KVQ_TYPE_Q4_1) KVQ_CASES_K(KVQ_TYPE_Q5_1)

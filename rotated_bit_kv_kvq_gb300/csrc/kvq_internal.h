@@ -103,7 +103,7 @@ bool decode_grid_ok(const kvq_cache& c, const DecodePlan& plan);
 cudaError_t launch_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, const void* q,
                           int q_dtype, int n_q_heads, float scale, void* out, int out_dtype,
                           void* ws, cudaStream_t st, const FusedAppend* fa = nullptr);
-// per-head_dim launchers (one translation unit each); 192 supports q4_0 / q4_0 only
+// per-head_dim launchers (one translation unit each)
 #define KVQ_DECODE_LAUNCHER(NAME)                                                                     \
   cudaError_t NAME(const kvq_cache& c, Rot rot, const DecodePlan& plan, const void* q, int q_dtype,  \
                    int n_q_heads, float scale, void* out, int out_dtype, void* ws, cudaStream_t st,  \
@@ -112,6 +112,7 @@ KVQ_DECODE_LAUNCHER(launch_decode_d64)
 KVQ_DECODE_LAUNCHER(launch_decode_d128)
 KVQ_DECODE_LAUNCHER(launch_decode_d192)
 KVQ_DECODE_LAUNCHER(launch_decode_d256)
+KVQ_DECODE_LAUNCHER(launch_decode_d320)
 #undef KVQ_DECODE_LAUNCHER
 
 // Prefill (tcgen05): head_dim 64 or 128, GQA group up to 128.  The workspace

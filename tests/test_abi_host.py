@@ -159,7 +159,7 @@ def test_cache_check_rejections(built_lib_path):
     assert L.kvq_cache_check(ctypes.byref(c)) == 0
     c = _full_desc(); c.page_table = FAKE                        # a page table without pages
     assert L.kvq_cache_check(ctypes.byref(c)) == kvq.KVQ_ERR_INVALID_ARG
-    for bad in (dict(head_dim=48), dict(head_dim=512), dict(max_ctx=100), dict(max_ctx=(1 << 30) + 64),
+    for bad in (dict(head_dim=48), dict(head_dim=544), dict(max_ctx=100), dict(max_ctx=(1 << 30) + 64),
                 dict(batch=0), dict(tail_len=-1),
                 dict(k_type=7), dict(v_type=5), dict(flags=8)):
         assert L.kvq_cache_check(ctypes.byref(_full_desc(**bad))) == kvq.KVQ_ERR_INVALID_ARG, bad
@@ -186,9 +186,11 @@ def test_call_rejections_before_launch(built_lib_path):
     assert L.kvq_decode_attention(ref, FAKE, 0, 8, -1.0, FAKE, 0, FAKE, 1 << 30, None) == kvq.KVQ_ERR_INVALID_ARG
     assert L.kvq_decode_attention(ref, FAKE, 0, 8, 0.0, FAKE, 0, None, 1 << 30, None) == kvq.KVQ_ERR_WORKSPACE
     assert L.kvq_decode_attention(ref, FAKE, 0, 8, 0.0, FAKE, 0, FAKE, 16, None) == kvq.KVQ_ERR_WORKSPACE
-    c160 = _full_desc(head_dim=160)
-    assert L.kvq_decode_attention(ctypes.byref(c160), FAKE, 0, 8, 0.0, FAKE, 0, FAKE, 1 << 30, None) == \
-        kvq.KVQ_ERR_UNSUPPORTED
+    for dd in (160, 384, 512):  # head dims with no decode kernel
+        cdd = _full_desc(head_dim=dd)
+        assert L.kvq_cache_check(ctypes.byref(cdd)) == 0
+        assert L.kvq_decode_attention(ctypes.byref(cdd), FAKE, 0, 8, 0.0, FAKE, 0, FAKE, 1 << 30, None) == \
+            kvq.KVQ_ERR_UNSUPPORTED
     # debug: out-of-range sequence / head / which / positions
     assert L.kvq_dequant_debug(ref, 2, 0, 0, 0, 1, 0, FAKE, None, None) == kvq.KVQ_ERR_INVALID_ARG
     assert L.kvq_dequant_debug(ref, 0, 4, 0, 0, 1, 0, FAKE, None, None) == kvq.KVQ_ERR_INVALID_ARG

@@ -41,7 +41,7 @@ def _inputs(rng, B, n, H, d, scale=1.0):
 
 
 @pytest.mark.parametrize("qt", ["q4_0", "q5_0", "q8_0", "q4_1", "q5_1"])
-@pytest.mark.parametrize("d", [32, 64, 96, 128, 192, 256])
+@pytest.mark.parametrize("d", [32, 64, 96, 128, 192, 256, 320, 384, 512])
 def test_blocks_bit_exact_prerotated(qt, d):
     torch = require_gpu()
     from rotated_bit_kv_kvq_gb300 import kvq
@@ -126,7 +126,8 @@ def test_overflow_sets_status_and_leaves_sequence_untouched():
 
 
 @pytest.mark.parametrize("in_dtype", ["f32", "bf16", "f16"])
-@pytest.mark.parametrize("d,n", [(64, 64), (128, 64), (256, 64), (192, 64), (64, 320), (128, 320), (256, 320)])
+@pytest.mark.parametrize("d,n", [(64, 64), (128, 64), (256, 64), (192, 64), (64, 320), (128, 320), (256, 320),
+                                 (320, 64), (384, 64), (512, 64)])
 def test_gpu_rotation_against_oracle(in_dtype, d, n):
     """The GPU rotates in fp32 (warp FWHT); the oracle in fp64.  Codes may flip
     only where the rotated value sits within float rounding of a code boundary:

@@ -81,7 +81,11 @@ def test_every_format_pair(kt, vt):
 @pytest.mark.parametrize("d,kt,vt", [(64, "q8_0", "q4_0"), (64, "q5_0", "q5_0"), (256, "q8_0", "q4_0"),
                                      (256, "q4_0", "q5_0"), (256, "q8_0", "q8_0"), (192, "q4_0", "q4_0"),
                                      (64, "q4_1", "q5_1"), (256, "q5_1", "q4_1"), (256, "q8_0", "q5_1"),
-                                     (256, "q5_0", "q4_1")])
+                                     (256, "q5_0", "q4_1"),
+                                     # block-diagonal H_64 head dims, every format on each side
+                                     (192, "q8_0", "q4_0"), (192, "q5_0", "q5_1"), (192, "q4_1", "q8_0"),
+                                     (320, "q8_0", "q4_0"), (320, "q4_0", "q4_0"), (320, "q5_0", "q5_1"),
+                                     (320, "q4_1", "q8_0"), (320, "q5_1", "q5_0")])
 def test_head_dims(d, kt, vt):
     rng = np.random.default_rng(22)
     B, H, g, T = 2, 2, 3, 40
