@@ -836,6 +836,9 @@ def main():
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the decode measurement of the other workloads (d=64 ctx 256, GQA 16/8 ctx 4k, "
                          "ragged batch of 32)")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="run only the prompt-workload measurement (bulk append + prefill attention) and print "
+                         "its record; for profiling the bulk write and prefill kernels")
     ap.add_argument("--load-s", type=float, default=1.2,
                     help="seconds of extra decode load inside the clock-sampling window")
     args = ap.parse_args()
@@ -843,6 +846,10 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.prefill_only:
+        import torch
+        from rotated_bit_kv_kvq_gb300 import kvq
+        print(json.dumps({"prefill": run_prefill_bench(torch, kvq, args.steps, args.warmup)}), flush=True)
     else:
         run_ours(args)
 

@@ -102,17 +102,19 @@ kvq_status resolve(const kvq_cache* c, kvq::Rot* r) {
 
 kvq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
 
-int sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  return n;
-}
+int sm_count() { return kvq::device_sm_count(); }
 
 }  // namespace
 
 namespace kvq {
 size_t qs_row_bytes_host(int qt, int d) { return qt == KVQ_TYPE_Q8_0 ? size_t(d) : size_t(d) / 2; }
+
+int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
 }  // namespace kvq
 
 extern "C" {

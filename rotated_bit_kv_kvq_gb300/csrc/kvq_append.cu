@@ -16,6 +16,9 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
+#include <type_traits>
+
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
 #include "kvq_quant.cuh"
@@ -85,20 +88,24 @@ append_kernel(kvq_cache c, int rot_k, int rot_v, const void* __restrict__ kin, c
 }
 
 // ---------------------------------------------------------------------------
-// Block-per-lane variant for power-of-two head_dim 64 / 128 / 256 without
-// outlier channels: a vector is held by R = D/32 consecutive lanes and lane
-// l % R holds exactly block l % R (32 consecutive channels).  The rotation
-// combines the 5 channel bits inside a lane in registers and the log2(R)
-// block bits across lanes (one shuffle per value per bit); each lane then
-// quantizes and stores its own block with no cross-lane reduction, 16-byte
-// loads and stores throughout.  Same arithmetic as quantize_block, operation
-// by operation.
+// Block-per-lane variant for power-of-two head_dim 64 / 128 / 256 (bulk
+// appends): a vector is held by R = D/32 consecutive lanes and lane l % R
+// holds exactly block l % R (32 consecutive channels).  The rotation combines
+// the 5 channel bits inside a lane in registers and the log2(R) block bits
+// across lanes (one shuffle per value per bit); each lane then quantizes and
+// stores its own block with no cross-lane reduction, 16-byte loads and stores
+// throughout.  Same arithmetic as quantize_block, operation by operation.
+// The grid is persistent (a few CTAs per SM, grid-stride over warp tasks) and
+// each warp loads its next task's input while it works on the current one, so
+// that HBM reads overlap the arithmetic and the seq_len hand-off counts one
+// arrival per resident CTA.
 // ---------------------------------------------------------------------------
 
 // One 32-value block held by one lane: quantize and store (qs: the block's
 // bytes; qh_word: q5_x high bits or null; d_ptr: fp16 d or the (d, lo) word).
-__device__ __forceinline__ void quantize_lane_block(const float (&y)[32], int qt, uint8_t* qs_blk,
-                                                    uint32_t* qh_word, void* d_ptr) {
+// Every type, one value at a time (the general path).
+__device__ __forceinline__ void quantize_lane_block_scalar(const float (&y)[32], int qt, uint8_t* qs_blk,
+                                                        uint32_t* qh_word, void* d_ptr) {
   // block parameters, then each code computed once straight into its packed byte
   float lo = 0.0f, id = 0.0f, off = 0.0f;
   int top = 0;
@@ -164,54 +171,157 @@ __device__ __forceinline__ void quantize_lane_block(const float (&y)[32], int qt
   if (type_has_qh(qt)) *qh_word = h;
 }
 
+// trunc(x * id + off) for two values x (the code before the clamp): the
+// product and the sum rounded to nearest one at a time in scalar instructions
+// with explicit rounding modifiers (the compiler keeps those apart; a packed
+// multiply followed by a packed add was seen contracted into a fused
+// multiply-add, which rounds once), then, with 0 <= u < 2^23, a packed add of
+// 2^23 rounded toward zero: the sum lands on the unit grid, so its low mantissa
+// bits hold floor(u) = trunc(u).
+__device__ __forceinline__ void code_bits2(float x0, float x1, float id, float off, uint32_t& c0, uint32_t& c1) {
+  asm("{\n\t.reg .f32 a, b;\n\t.reg .b64 x, m;\n\t"
+      "mul.rn.f32 a, %2, %4;\n\tadd.rn.f32 a, a, %5;\n\t"
+      "mul.rn.f32 b, %3, %4;\n\tadd.rn.f32 b, b, %5;\n\t"
+      "mov.b64 x, {a, b};\n\tmov.b64 m, {%6, %6};\n\tadd.rz.f32x2 x, x, m;\n\t"
+      "mov.b64 {%0, %1}, x;\n\t}"
+      : "=r"(c0), "=r"(c1)
+      : "f"(x0), "f"(x1), "f"(id), "f"(off), "r"(0x4B000000u));
+}
+
+// quantize_lane_block_scalar for q4_0 / q5_0, the same operations in another
+// order of evaluation: the signed value of largest magnitude from a max / min
+// tree (a block holding +a and -a, or no nonzero value, takes the scalar scan,
+// which resolves the first-index rule); codes min(top, trunc(x*id + off)) two
+// at a time with packed multiply and add (one rounding each, as before), the
+// truncation by code_bits2 (u > 0 here), then four codes per word: clamp to
+// top, nibble pack (byte k = code_k | code_{k+16} << 4) and for q5_0 bit 4 of
+// each code into the high-bit word.  q8_0, the scale + minimum types and blocks
+// whose scale or inverse is not finite take the scalar path.
+__device__ __forceinline__ void quantize_lane_block(float (&y)[32], int qt, uint8_t* qs_blk, uint32_t* qh_word,
+                                                    void* d_ptr) {
+  if (qt != KVQ_TYPE_Q4_0 && qt != KVQ_TYPE_Q5_0) {
+    quantize_lane_block_scalar(y, qt, qs_blk, qh_word, d_ptr);
+    return;
+  }
+  float mx[16], mn[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    mx[j] = fmaxf(y[2 * j], y[2 * j + 1]);
+    mn[j] = fminf(y[2 * j], y[2 * j + 1]);
+  }
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int j = 0; j < w; ++j) {
+      mx[j] = fmaxf(mx[j], mx[j + w]);
+      mn[j] = fminf(mn[j], mn[j + w]);
+    }
+  const float hi = mx[0], lo = mn[0];
+  const bool q5 = qt == KVQ_TYPE_Q5_0;
+  const float best_m = hi > -lo ? hi : lo;
+  const float d = q5 ? best_m / -16.0f : best_m / -8.0f;
+  const float id = d != 0.0f ? 1.0f / d : 0.0f;
+  if (!(hi > -lo || -lo > hi) || !(fabsf(best_m) <= 3.0e38f) || !(fabsf(id) <= 3.0e38f)) {
+    quantize_lane_block_scalar(y, qt, qs_blk, qh_word, d_ptr);
+    return;
+  }
+  *static_cast<__half*>(d_ptr) = __float2half_rn(d);
+  const float off = q5 ? 16.5f : 8.5f;
+  uint32_t fb[32];
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) code_bits2(y[j], y[j + 1], id, off, fb[j], fb[j + 1]);
+  const int sh = q5 ? 5 : 4;  // codes reach top + 1 at most: subtract bit log2(top + 1)
+  uint32_t half16[8], h = 0;
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const uint32_t a = __byte_perm(fb[2 * m], fb[2 * m + 1], 0x0040);        // codes 2m, 2m+1
+    const uint32_t b = __byte_perm(fb[2 * m + 16], fb[2 * m + 17], 0x0040);  // codes 2m+16, 2m+17
+    uint32_t x = __byte_perm(a, b, 0x5410);
+    x -= (x >> sh) & 0x01010101u;
+    half16[m] = (x & 0x0F0Fu) | ((x >> 12) & 0xF0F0u);  // qs bytes 2m, 2m+1
+    if (q5) {
+      const uint32_t g = (((x >> 4) & 0x01010101u) * 0x00204081u) >> 21;  // bit 4 of the four codes
+      h |= ((g & 3u) << (2 * m)) | (((g >> 2) & 3u) << (2 * m + 16));
+    }
+  }
+  *reinterpret_cast<uint4*>(qs_blk) =
+      make_uint4(__byte_perm(half16[0], half16[1], 0x5410), __byte_perm(half16[2], half16[3], 0x5410),
+                 __byte_perm(half16[4], half16[5], 0x5410), __byte_perm(half16[6], half16[7], 0x5410));
+  if (q5) *qh_word = h;
+}
+
+// Input kinds of the bulk kernel (a template parameter: no per-value select).
+enum RowIn { kInBf16 = 0, kInF16 = 1, kInF32 = 2 };
+
+// One lane's 32 input channels as raw 16-byte words (16-bit inputs: 4, fp32: 8).
+template <int IN>
+struct RowRaw {
+  uint4 w[IN == kInF32 ? 8 : 4];
+};
+
+// Task tu = 2 * vec + which: vector vec = (b * n_new + i) * H + h of K (which = 0)
+// or V; lane sub of its R lanes reads channels 32*sub .. 32*sub+31 (read once:
+// streaming loads).
+template <int D, int IN>
+__device__ __forceinline__ void rows_load(RowRaw<IN>& r, const void* kin, const void* vin, unsigned tu, int sub) {
+  constexpr bool IN32 = IN == kInF32;
+  const size_t e0 = size_t(tu >> 1) * D + 32 * sub;
+  const void* base = (tu & 1u) ? vin : kin;
+  const uint4* src = IN32 ? reinterpret_cast<const uint4*>(static_cast<const float*>(base) + e0)
+                          : reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + e0);
+#pragma unroll
+  for (int t = 0; t < (IN32 ? 8 : 4); ++t) r.w[t] = __ldcs(src + t);
+}
+
+template <int IN>
+__device__ __forceinline__ void rows_unpack(const RowRaw<IN>& r, float (&y)[32]) {
+  if constexpr (IN == kInF32) {
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      y[4 * t] = __uint_as_float(r.w[t].x); y[4 * t + 1] = __uint_as_float(r.w[t].y);
+      y[4 * t + 2] = __uint_as_float(r.w[t].z); y[4 * t + 3] = __uint_as_float(r.w[t].w);
+    }
+  } else {
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const uint32_t w[4] = {r.w[t].x, r.w[t].y, r.w[t].z, r.w[t].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if constexpr (IN == kInBf16) {
+          y[8 * t + 2 * e] = __uint_as_float(w[e] << 16);
+          y[8 * t + 2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+        } else {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+          y[8 * t + 2 * e] = f.x;
+          y[8 * t + 2 * e + 1] = f.y;
+        }
+      }
+    }
+  }
+}
+
+// Rotate, quantize and store one lane block of task tu (its values in y); `live`
+// false: a lane past the end, which computes a copy and stores nothing.
 template <int D, bool OUTL>
-__global__ void __launch_bounds__(kAppendWarps * 32)
-append_rows_kernel(kvq_cache c, int rot_k, int rot_v, const void* __restrict__ kin, const void* __restrict__ vin,
-                   int in_dtype, int n_new, const int32_t* __restrict__ n_new_per_seq, int prerotated) {
-  static_assert(D == 64 || D == 128 || D == 256, "power-of-two head_dim of 64 to 256");
+__device__ __forceinline__ void rows_task(const kvq_cache& c, int rot_k, int rot_v, int n_new, const DivU32& div_h,
+                                          const DivU32& div_n, const int32_t* __restrict__ n_new_per_seq,
+                                          int prerotated, bool live, unsigned tu, float (&y)[32], int lane) {
   constexpr int R = D / 32;   // lanes per vector
   constexpr int NB = D / kQK;
-  const int lane = threadIdx.x & 31, sub = lane % R;
+  const int sub = lane % R;
   const int H = c.n_kv_heads;
-  const unsigned tasks = unsigned(c.batch) * unsigned(n_new) * unsigned(H) * 2u;
-  const unsigned task = (blockIdx.x * unsigned(kAppendWarps) + (threadIdx.x >> 5)) * (32u / R) + unsigned(lane / R);
-  const bool live = task < tasks;
-  const unsigned tu = live ? task : tasks - 1;   // lanes past the end compute a copy and store nothing
   const int which = int(tu & 1u);
   const unsigned vec = tu >> 1;                  // (b * n_new + i) * H + h
-  const int h = int(vec % unsigned(H));
-  const unsigned bi = vec / unsigned(H);
-  const int i = int(bi % unsigned(n_new));
-  const int b = int(bi / unsigned(n_new));
+  const unsigned bi = div_u32(vec, div_h);
+  const int h = int(vec - bi * unsigned(H));
+  const unsigned bu = div_u32(bi, div_n);
+  const int i = int(bi - bu * unsigned(n_new));
+  const int b = int(bu);
   const int n0 = c.seq_len[b];
   const int nb = n_new_per_seq ? n_new_per_seq[b] : n_new;
   const bool ok = nb >= 0 && nb <= n_new && n0 >= 0 && (long long)n0 + nb <= c.max_ctx;
   if (live && !ok && i == 0 && h == 0 && which == 0 && sub == 0) atomicOr(&c.status[0], KVQ_DEV_ERR_APPEND_RANGE);
 
-  // this lane's block: channels 32*sub .. 32*sub+31
-  float y[32];
-  const size_t e0 = size_t(vec) * D + 32 * sub;
-  if (in_dtype == KVQ_F32) {
-    const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(which ? vin : kin) + e0);
-#pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      const float4 x = src[t];
-      y[4 * t] = x.x; y[4 * t + 1] = x.y; y[4 * t + 2] = x.z; y[4 * t + 3] = x.w;
-    }
-  } else {
-    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(which ? vin : kin) + e0);
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const uint4 x = src[t];
-      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint16_t l16 = uint16_t(w[e] & 0xFFFFu), h16 = uint16_t(w[e] >> 16);
-        y[8 * t + 2 * e] = in_dtype == KVQ_BF16 ? bf16_bits_to_f32(l16) : __half2float(__ushort_as_half(l16));
-        y[8 * t + 2 * e + 1] = in_dtype == KVQ_BF16 ? bf16_bits_to_f32(h16) : __half2float(__ushort_as_half(h16));
-      }
-    }
-  }
   // Outlier channels (OUTL): the raw vector is staged in shared memory; lane sub
   // takes slots sub*SL .. sub*SL+SL-1 of the head's list (their unrotated values
   // become one q8_0 block, written below), and zeroes its own block's channels
@@ -222,6 +332,7 @@ append_rows_kernel(kvq_cache c, int rot_k, int rot_v, const void* __restrict__ k
   if constexpr (OUTL) {
     __shared__ __align__(16) float s_raw[kAppendWarps][32 * 32];
     raw = &s_raw[threadIdx.x >> 5][(lane / R) * D];
+    __syncwarp();  // the warp's previous task has read its staged values
 #pragma unroll
     for (int t = 0; t < 8; ++t)
       *reinterpret_cast<float4*>(raw + 32 * sub + 4 * t) = make_float4(y[4 * t], y[4 * t + 1], y[4 * t + 2], y[4 * t + 3]);
@@ -253,13 +364,19 @@ append_rows_kernel(kvq_cache c, int rot_k, int rot_v, const void* __restrict__ k
   // vectors, which rotate or not); the shuffles name exactly the rotating lanes
   const bool rot = (which ? rot_v : rot_k) && !prerotated;
   const unsigned rmask = __ballot_sync(0xffffffffu, rot);
+  const int qt = which ? c.v_type : c.k_type;
   if (rot) {
     lane_fwht<R>(y, lane, rmask);
+    // packed scaling, except where the next operation is a subtraction (x - lo
+    // of the scale + minimum types), which must not be contracted with it
+    if (type_has_min(qt)) {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) y[j] *= inv_sqrt_group<D>();
+      for (int j = 0; j < 32; ++j) y[j] = __fmul_rn(y[j], inv_sqrt_group<D>());
+    } else {
+      scale32(y, inv_sqrt_group<D>());
+    }
   }
   const int pos = n0 + i;
-  const int qt = which ? c.v_type : c.k_type;
   const bool store = live && ok && i < nb;
   const long long brow = store ? body_row(row_map(c), b, h, pos) : 0;
   if (!store) {
@@ -310,8 +427,7 @@ append_rows_kernel(kvq_cache c, int rot_k, int rot_v, const void* __restrict__ k
       }
       if (rot) {
         lane_fwht<R>(y, lane, tmask);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) y[j] *= inv_sqrt_group<D>();
+        scale32(y, inv_sqrt_group<D>());
       }
     }
   }
@@ -327,6 +443,40 @@ append_rows_kernel(kvq_cache c, int rot_k, int rot_v, const void* __restrict__ k
                (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(y[8 * t + 2 * e + 1]))) << 16);
       reinterpret_cast<uint4*>(tail)[t] = make_uint4(w[0], w[1], w[2], w[3]);
     }
+  }
+}
+
+constexpr int kRowsCtasPerSm = 2;
+
+template <int D, bool OUTL, int IN>
+__global__ void __launch_bounds__(kAppendWarps * 32, kRowsCtasPerSm)
+append_rows_kernel(kvq_cache c, int rot_k, int rot_v, const void* __restrict__ kin, const void* __restrict__ vin,
+                   int n_new, DivU32 div_h, DivU32 div_n, const int32_t* __restrict__ n_new_per_seq, int prerotated) {
+  static_assert(D == 64 || D == 128 || D == 256, "power-of-two head_dim of 64 to 256");
+  constexpr int R = D / 32;   // lanes per vector
+  constexpr unsigned VPW = 32u / R;  // vectors per warp task
+  const int lane = threadIdx.x & 31, sub = lane % R;
+  const unsigned tasks = unsigned(c.batch) * unsigned(n_new) * unsigned(c.n_kv_heads) * 2u;
+  const unsigned wtasks = (tasks + VPW - 1) / VPW;
+  const unsigned stride = gridDim.x * unsigned(kAppendWarps);
+  const unsigned lt = unsigned(lane / R);
+  unsigned wt = blockIdx.x * unsigned(kAppendWarps) + (threadIdx.x >> 5);
+  // 16-bit inputs: the next task's 64 bytes are loaded before the current task's
+  // arithmetic (fp32 inputs would need 32 more registers: loaded in turn)
+  constexpr bool kAhead = IN != kInF32;
+  RowRaw<IN> cur;
+  if (kAhead && wt < wtasks) rows_load<D, IN>(cur, kin, vin, min(wt * VPW + lt, tasks - 1), sub);
+  for (; wt < wtasks; wt += stride) {  // warp-uniform trip count
+    const bool more = kAhead && wt + stride < wtasks;
+    RowRaw<IN> nxt;
+    if (!kAhead) rows_load<D, IN>(cur, kin, vin, min(wt * VPW + lt, tasks - 1), sub);
+    if (more) rows_load<D, IN>(nxt, kin, vin, min((wt + stride) * VPW + lt, tasks - 1), sub);
+    float y[32];
+    rows_unpack<IN>(cur, y);
+    const unsigned task = wt * VPW + lt;
+    rows_task<D, OUTL>(c, rot_k, rot_v, n_new, div_h, div_n, n_new_per_seq, prerotated, task < tasks,
+                       min(task, tasks - 1), y, lane);
+    if (more) cur = nxt;
   }
   finish_append(c, n_new, n_new_per_seq);
 }
@@ -425,11 +575,20 @@ cudaError_t append_d(const kvq_cache& c, Rot rot, const void* k, const void* v, 
     // vectors (a decode step) finish sooner spread one per warp
     if (warps >= kRowsMinVectors) {
       const long long per_cta = (long long)kAppendWarps * (32 / (D / 32));
-      const unsigned grid = unsigned((warps + per_cta - 1) / per_cta);
-      if (c.n_outlier)
-        append_rows_kernel<D, true><<<grid, kAppendWarps * 32, 0, st>>>(c, rot.k, rot.v, k, v, in_dtype, n_new, nps, pre);
-      else
-        append_rows_kernel<D, false><<<grid, kAppendWarps * 32, 0, st>>>(c, rot.k, rot.v, k, v, in_dtype, n_new, nps, pre);
+      const long long full = (warps + per_cta - 1) / per_cta;
+      const int sms = device_sm_count();
+      const unsigned grid = unsigned(std::min<long long>(full, (long long)(sms > 0 ? sms : 148) * kRowsCtasPerSm));
+      const DivU32 div_h = make_divu32(uint32_t(c.n_kv_heads)), div_n = make_divu32(uint32_t(n_new));
+      auto go = [&](auto kern) {
+        kern<<<grid, kAppendWarps * 32, 0, st>>>(c, rot.k, rot.v, k, v, n_new, div_h, div_n, nps, pre);
+      };
+      auto by_input = [&](auto outl) {
+        constexpr bool O = decltype(outl)::value;
+        if (in_dtype == KVQ_F32) go(append_rows_kernel<D, O, kInF32>);
+        else if (in_dtype == KVQ_F16) go(append_rows_kernel<D, O, kInF16>);
+        else go(append_rows_kernel<D, O, kInBf16>);
+      };
+      if (c.n_outlier) by_input(std::true_type{}); else by_input(std::false_type{});
       return cudaGetLastError();
     }
   }

@@ -68,6 +68,27 @@ __device__ __forceinline__ long long body_row(const RowMap& m, int b, int h, int
 }
 
 // ---------------------------------------------------------------------------
+// Unsigned 32-bit division by a run-time invariant divisor d >= 1 with one
+// high multiply (Granlund and Montgomery, "Division by invariant integers
+// using multiplication", 1994, section 4): l = ceil(log2 d),
+// m = floor(2^32 (2^l - d) / d) + 1, q = (t + ((n - t) >> min(l, 1))) >>
+// max(l - 1, 0) with t = mulhi(m, n); exact for every 32-bit n.
+// ---------------------------------------------------------------------------
+struct DivU32 {
+  uint32_t d, m, s1, s2;
+};
+inline DivU32 make_divu32(uint32_t d) {
+  uint32_t l = 0;
+  while (l < 32 && (uint64_t(1) << l) < d) ++l;
+  const uint32_t m = uint32_t(((uint64_t(1) << 32) * ((uint64_t(1) << l) - d)) / d + 1);
+  return DivU32{d, m, l < 1 ? l : 1u, l > 1 ? l - 1 : 0u};
+}
+__device__ __forceinline__ uint32_t div_u32(uint32_t n, const DivU32& v) {
+  const uint32_t t = __umulhi(v.m, n);
+  return (t + ((n - t) >> v.s1)) >> v.s2;
+}
+
+// ---------------------------------------------------------------------------
 // small utilities
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -325,33 +346,66 @@ __device__ __forceinline__ void warp_fwht(float (&v)[D / 32], int lane) {
 
 // Unnormalised Sylvester FWHT of a vector held by R consecutive lanes, 32
 // consecutive channels each: the 5 in-lane channel bits in registers, the
-// log2(R) lane bits by shuffles (o + sgn*v: the rounding of the plain sum or
-// difference) among the lanes of `mask`, which holds whole R-lane groups.
+// log2(R) lane bits by shuffles among the lanes of `mask`, which holds whole
+// R-lane groups.  Every output is one rounding of a plain sum or difference:
+// a - b is taken as fma(b, -1, a) (the product is exact), and the channel-bit
+// stages above bit 0 use the packed fp32x2 forms, two channels per
+// instruction with the same per-channel rounding.
 template <int R>
 __device__ __forceinline__ void lane_fwht(float (&r)[32], int lane, unsigned mask) {
+  const float2 m1 = make_float2(-1.0f, -1.0f);
 #pragma unroll
-  for (int hh = 1; hh < 32; hh <<= 1)
+  for (int j = 0; j < 32; j += 2) {  // channel bit 0: the two halves of a pair
+    const float a = r[j], b = r[j + 1];
+    r[j] = a + b;
+    r[j + 1] = a - b;
+  }
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
+  for (int hh = 2; hh < 32; hh <<= 1)
+#pragma unroll
+    for (int j = 0; j < 32; j += 2)
       if ((j & hh) == 0) {
-        const float a = r[j], bq = r[j + hh];
-        r[j] = a + bq;
-        r[j + hh] = a - bq;
+        const float2 a = make_float2(r[j], r[j + 1]), b = make_float2(r[j + hh], r[j + hh + 1]);
+        const float2 s2 = __fadd2_rn(a, b), d2 = __ffma2_rn(b, m1, a);
+        r[j] = s2.x; r[j + 1] = s2.y;
+        r[j + hh] = d2.x; r[j + hh + 1] = d2.y;
       }
 #pragma unroll
   for (int m = 1; m < R; m <<= 1) {
     const float sgn = (lane & m) ? -1.0f : 1.0f;  // upper partner: o - v, lower: v + o
+    const float2 sg = make_float2(sgn, sgn);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) r[j] = fmaf(sgn, r[j], __shfl_xor_sync(mask, r[j], m));
+    for (int j = 0; j < 32; j += 2) {
+      const float2 o = make_float2(__shfl_xor_sync(mask, r[j], m), __shfl_xor_sync(mask, r[j + 1], m));
+      const float2 t = __ffma2_rn(sg, make_float2(r[j], r[j + 1]), o);
+      r[j] = t.x; r[j + 1] = t.y;
+    }
+  }
+}
+
+// y[j] *= s for the 32 values of a lane block (packed: the same rounding per value).
+__device__ __forceinline__ void scale32(float (&y)[32], float s) {
+  const float2 s2 = make_float2(s, s);
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    const float2 t = __fmul2_rn(make_float2(y[j], y[j + 1]), s2);
+    y[j] = t.x; y[j + 1] = t.y;
   }
 }
 
 // 1/sqrt(G) correctly rounded to fp32.
 template <int G>
 __host__ __device__ constexpr float inv_sqrt_group() {
-  return G == 32 ? 0.17677669529663688f : G == 64 ? 0.125f : G == 128 ? 0.088388347648318440f : 0.0625f;
+  static_assert(G == 32 || G == 64 || G == 128 || G == 256 || G == 512, "Hadamard group of 32 to 512");
+  return G == 32    ? 0.17677669529663688f
+         : G == 64  ? 0.125f
+         : G == 128 ? 0.088388347648318440f
+         : G == 256 ? 0.0625f
+                    : 0.044194173824159216f;
 }
-static_assert(inv_sqrt_group<256>() == 0.0625f, "");
+static_assert(inv_sqrt_group<256>() == 0.0625f && inv_sqrt_group<512>() * inv_sqrt_group<512>() < 0.001954f &&
+                  inv_sqrt_group<512>() * inv_sqrt_group<512>() > 0.001952f,
+              "");
 
 // Channel held in slot j of lane l for the FWHT layout above.
 template <int D, int G>

@@ -46,6 +46,9 @@ inline cudaError_t ensure_dynamic_smem(const void* kernel, int bytes) {
 }
 
 // Launchers (arguments already validated by the API layer).
+// SMs of the current device (0 when the query fails).
+int device_sm_count();
+
 cudaError_t launch_append(const kvq_cache& c, Rot rot, const void* k, const void* v, int in_dtype,
                           int n_new, const int32_t* n_new_per_seq, uint32_t flags, cudaStream_t st);
 cudaError_t launch_debug(const kvq_cache& c, Rot rot, int seq, int kv_head, int which, int t0,

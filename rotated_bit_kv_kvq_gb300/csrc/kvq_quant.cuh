@@ -44,7 +44,18 @@ __device__ __forceinline__ void load_vals(const void* base, int in_dtype, size_t
 
 template <int P>
 __device__ __forceinline__ void store_bytes(uint8_t* dst, const uint8_t* src) {
-  if constexpr (P == 8) {
+  static_assert(P == 1 || P == 2 || P == 4 || P % 8 == 0, "lane width");
+  if constexpr (P > 8) {  // 16-byte pieces (P = 16 at head_dim 512)
+#pragma unroll
+    for (int i = 0; i < P; i += 16) {
+      uint32_t w[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        w[k] = src[i + 4 * k] | (src[i + 4 * k + 1] << 8) | (src[i + 4 * k + 2] << 16) |
+               (uint32_t(src[i + 4 * k + 3]) << 24);
+      *reinterpret_cast<uint4*>(dst + i) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  } else if constexpr (P == 8) {
     uint2 t; uint8_t* tb = reinterpret_cast<uint8_t*>(&t);
 #pragma unroll
     for (int i = 0; i < 8; ++i) tb[i] = src[i];
@@ -64,8 +75,10 @@ __device__ __forceinline__ void store_bf16(uint16_t* dst, const float* v) {
   uint16_t t[P];
 #pragma unroll
   for (int i = 0; i < P; ++i) t[i] = __bfloat16_as_ushort(__float2bfloat16_rn(v[i]));
-  if constexpr (P == 8) {
-    *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<uint4*>(t);
+  static_assert(P == 1 || P == 2 || P == 4 || P % 8 == 0, "lane width");
+  if constexpr (P % 8 == 0) {
+#pragma unroll
+    for (int i = 0; i < P; i += 8) *reinterpret_cast<uint4*>(dst + i) = *reinterpret_cast<uint4*>(t + i);
   } else if constexpr (P == 4) {
     *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<uint2*>(t);
   } else if constexpr (P == 2) {
