@@ -95,10 +95,10 @@ append_kernel(kvq_cache c, int rot_k, int rot_v, const void* __restrict__ kin, c
 // across lanes (one shuffle per value per bit); each lane then quantizes and
 // stores its own block with no cross-lane reduction, 16-byte loads and stores
 // throughout.  Same arithmetic as quantize_block, operation by operation.
-// The grid is persistent (a few CTAs per SM, grid-stride over warp tasks) and
-// each warp loads its next task's input while it works on the current one, so
-// that HBM reads overlap the arithmetic and the seq_len hand-off counts one
-// arrival per resident CTA.
+// The grid is persistent (three CTAs per SM, grid-stride over warp tasks): the
+// other resident warps' arithmetic covers a warp's loads (measured faster than
+// a register prefetch of the next task, which spills at this occupancy), and
+// the seq_len hand-off counts one arrival per resident CTA.
 // ---------------------------------------------------------------------------
 
 // One 32-value block held by one lane: quantize and store (qs: the block's
@@ -203,19 +203,17 @@ __device__ __forceinline__ void quantize_lane_block(float (&y)[32], int qt, uint
     quantize_lane_block_scalar(y, qt, qs_blk, qh_word, d_ptr);
     return;
   }
-  float mx[16], mn[16];
+  // four interleaved partial maxima / minima (short dependency chains, few registers)
+  float mx[4], mn[4];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    mx[j] = fmaxf(y[2 * j], y[2 * j + 1]);
-    mn[j] = fminf(y[2 * j], y[2 * j + 1]);
+  for (int j = 0; j < 4; ++j) { mx[j] = y[j]; mn[j] = y[j]; }
+#pragma unroll
+  for (int j = 4; j < 32; ++j) {
+    mx[j & 3] = fmaxf(mx[j & 3], y[j]);
+    mn[j & 3] = fminf(mn[j & 3], y[j]);
   }
-#pragma unroll
-  for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-    for (int j = 0; j < w; ++j) {
-      mx[j] = fmaxf(mx[j], mx[j + w]);
-      mn[j] = fminf(mn[j], mn[j + w]);
-    }
+  mx[0] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+  mn[0] = fminf(fminf(mn[0], mn[1]), fminf(mn[2], mn[3]));
   const float hi = mx[0], lo = mn[0];
   const bool q5 = qt == KVQ_TYPE_Q5_0;
   const float best_m = hi > -lo ? hi : lo;
@@ -227,15 +225,15 @@ __device__ __forceinline__ void quantize_lane_block(float (&y)[32], int qt, uint
   }
   *static_cast<__half*>(d_ptr) = __float2half_rn(d);
   const float off = q5 ? 16.5f : 8.5f;
-  uint32_t fb[32];
-#pragma unroll
-  for (int j = 0; j < 32; j += 2) code_bits2(y[j], y[j + 1], id, off, fb[j], fb[j + 1]);
   const int sh = q5 ? 5 : 4;  // codes reach top + 1 at most: subtract bit log2(top + 1)
   uint32_t half16[8], h = 0;
 #pragma unroll
-  for (int m = 0; m < 8; ++m) {
-    const uint32_t a = __byte_perm(fb[2 * m], fb[2 * m + 1], 0x0040);        // codes 2m, 2m+1
-    const uint32_t b = __byte_perm(fb[2 * m + 16], fb[2 * m + 17], 0x0040);  // codes 2m+16, 2m+17
+  for (int m = 0; m < 8; ++m) {  // codes 2m, 2m+1, 2m+16, 2m+17
+    uint32_t f0, f1, f16, f17;
+    code_bits2(y[2 * m], y[2 * m + 1], id, off, f0, f1);
+    code_bits2(y[2 * m + 16], y[2 * m + 17], id, off, f16, f17);
+    const uint32_t a = __byte_perm(f0, f1, 0x0040);
+    const uint32_t b = __byte_perm(f16, f17, 0x0040);
     uint32_t x = __byte_perm(a, b, 0x5410);
     x -= (x >> sh) & 0x01010101u;
     half16[m] = (x & 0x0F0Fu) | ((x >> 12) & 0xF0F0u);  // qs bytes 2m, 2m+1
@@ -446,7 +444,7 @@ __device__ __forceinline__ void rows_task(const kvq_cache& c, int rot_k, int rot
   }
 }
 
-constexpr int kRowsCtasPerSm = 2;
+constexpr int kRowsCtasPerSm = 3;  // 80 registers; 24 warps per SM hide the loads
 
 template <int D, bool OUTL, int IN>
 __global__ void __launch_bounds__(kAppendWarps * 32, kRowsCtasPerSm)
@@ -461,22 +459,14 @@ append_rows_kernel(kvq_cache c, int rot_k, int rot_v, const void* __restrict__ k
   const unsigned stride = gridDim.x * unsigned(kAppendWarps);
   const unsigned lt = unsigned(lane / R);
   unsigned wt = blockIdx.x * unsigned(kAppendWarps) + (threadIdx.x >> 5);
-  // 16-bit inputs: the next task's 64 bytes are loaded before the current task's
-  // arithmetic (fp32 inputs would need 32 more registers: loaded in turn)
-  constexpr bool kAhead = IN != kInF32;
-  RowRaw<IN> cur;
-  if (kAhead && wt < wtasks) rows_load<D, IN>(cur, kin, vin, min(wt * VPW + lt, tasks - 1), sub);
   for (; wt < wtasks; wt += stride) {  // warp-uniform trip count
-    const bool more = kAhead && wt + stride < wtasks;
-    RowRaw<IN> nxt;
-    if (!kAhead) rows_load<D, IN>(cur, kin, vin, min(wt * VPW + lt, tasks - 1), sub);
-    if (more) rows_load<D, IN>(nxt, kin, vin, min((wt + stride) * VPW + lt, tasks - 1), sub);
+    RowRaw<IN> raw;
+    rows_load<D, IN>(raw, kin, vin, min(wt * VPW + lt, tasks - 1), sub);
     float y[32];
-    rows_unpack<IN>(cur, y);
+    rows_unpack<IN>(raw, y);
     const unsigned task = wt * VPW + lt;
     rows_task<D, OUTL>(c, rot_k, rot_v, n_new, div_h, div_n, n_new_per_seq, prerotated, task < tasks,
                        min(task, tasks - 1), y, lane);
-    if (more) cur = nxt;
   }
   finish_append(c, n_new, n_new_per_seq);
 }
