@@ -340,14 +340,11 @@ __device__ __forceinline__ float hdr_scale(const uint32_t* w, int blk) {
   return KHH == 1 ? h2f(w[blk >> 1], blk & 1) : h2f(w[blk], 0);
 }
 
-// q5_0 high bits of a K row word h = qh >> (4*tig), placed at bits 4 / 20 (with the 0x6400 magic).
-__device__ __forceinline__ uint32_t khb(uint32_t h, int which) {
-  switch (which) {
-    case 0: return (((h << 4) & 0x10u) | ((h << 18) & 0x100000u)) | 0x64006400u;   // channels +0, +2
-    case 1: return (((h << 3) & 0x10u) | ((h << 17) & 0x100000u)) | 0x64006400u;   // +1, +3
-    case 2: return (((h >> 12) & 0x10u) | ((h << 2) & 0x100000u)) | 0x64006400u;   // 16+0, 16+2
-    default: return (((h >> 13) & 0x10u) | ((h << 1) & 0x100000u)) | 0x64006400u;  // 16+1, 16+3
-  }
+// q5 high bits of a K row word (the K plane's bit order: channels c and c + 2 of
+// a score pair 16 bits apart) for one fp16 pair, at bits 4 / 20 with the 0x6400
+// magic: a rotation by the lane's amount r and one mask.
+__device__ __forceinline__ uint32_t khb(uint32_t h, uint32_t r) {
+  return (__funnelshift_r(h, h, r) & 0x00100010u) | 0x64006400u;
 }
 
 template <int D, int KT, int VT, bool OL>
@@ -719,6 +716,11 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
   int k_stop = my_tiles;
   // per-lane ldmatrix row and swizzle constants of the body tiles
   const int mi = lane >> 3, rr = (lane & 7) + 8 * (mi & 1);
+  // q5 K: rotation bringing the lane's channel pairs (4tig, 4tig+2), (+1, +3),
+  // (16+4tig, 18+4tig), (17+4tig, 19+4tig) of a stored high-bit word to bits 4 / 20
+  uint32_t kr[4];
+#pragma unroll
+  for (int w = 0; w < 4; ++w) kr[w] = uint32_t(2 * tig + (w & 1) + 8 * (w >> 1) - 4) & 31u;
   uint32_t lbK[C::WK / 32], lbV[C::WV / 32];
   swz_lane<C::WK>(rr, mi >> 1, lbK);
   swz_lane<C::WV>(rr, mi >> 1, lbV);
@@ -775,9 +777,9 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
             uint32_t m10 = 0x64006400u, m11 = 0x64006400u, m12 = 0x64006400u, m13 = 0x64006400u;
             if constexpr (C::K5) {
               const uint32_t* kqh = reinterpret_cast<const uint32_t*>(st + C::off_kqh);
-              const uint32_t ha = kqh[g * NB + blk] >> (4 * tig), hb = kqh[(g + 8) * NB + blk] >> (4 * tig);
-              m00 = khb(ha, 0); m01 = khb(ha, 1); m02 = khb(ha, 2); m03 = khb(ha, 3);
-              m10 = khb(hb, 0); m11 = khb(hb, 1); m12 = khb(hb, 2); m13 = khb(hb, 3);
+              const uint32_t ha = kqh[g * NB + blk], hb = kqh[(g + 8) * NB + blk];
+              m00 = khb(ha, kr[0]); m01 = khb(ha, kr[1]); m02 = khb(ha, kr[2]); m03 = khb(ha, kr[3]);
+              m10 = khb(hb, kr[0]); m11 = khb(hb, kr[1]); m12 = khb(hb, kr[2]); m13 = khb(hb, kr[3]);
             }
             const uint32_t alo[4] = {nib_pair(ra, 0, m00, OFF), nib_pair(rb, 0, m10, OFF),
                                      nib_pair(ra, 8, m01, OFF), nib_pair(rb, 8, m11, OFF)};

@@ -68,6 +68,30 @@ __device__ __forceinline__ long long body_row(const RowMap& m, int b, int h, int
 }
 
 // ---------------------------------------------------------------------------
+// Bit order of the K high-bit plane (q5_0 / q5_1 K).  A block's 32-bit word
+// holds bit 4 of code c at bit c in GGUF order; the K plane stores the bit of
+// channel c = 4t + 2b + e (t < 8, b and e single bits) at bit 16b + 2t + e, so
+// that channels c and c + 2 (one fp16 pair of the decode's score operand) sit
+// 16 bits apart.  Three delta swaps of the bit index (bits 1<->2, 2<->3,
+// 3<->4) rotate index bits 1-4; the inverse applies them in reverse order.
+// The V plane keeps GGUF order.
+// ---------------------------------------------------------------------------
+__host__ __device__ inline uint32_t delta_swap(uint32_t x, int d, uint32_t m) {
+  const uint32_t t = ((x >> d) ^ x) & m;
+  return x ^ t ^ (t << d);
+}
+__host__ __device__ inline uint32_t qh_k_from_gguf(uint32_t x) {
+  x = delta_swap(x, 2, 0x0C0C0C0Cu);
+  x = delta_swap(x, 4, 0x00F000F0u);
+  return delta_swap(x, 8, 0x0000FF00u);
+}
+__host__ __device__ inline uint32_t qh_k_to_gguf(uint32_t x) {
+  x = delta_swap(x, 8, 0x0000FF00u);
+  x = delta_swap(x, 4, 0x00F000F0u);
+  return delta_swap(x, 2, 0x0C0C0C0Cu);
+}
+
+// ---------------------------------------------------------------------------
 // Unsigned 32-bit division by a run-time invariant divisor d >= 1 with one
 // high multiply (Granlund and Montgomery, "Division by invariant integers
 // using multiplication", 1994, section 4): l = ceil(log2 d),

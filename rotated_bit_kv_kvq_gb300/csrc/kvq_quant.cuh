@@ -93,7 +93,7 @@ __device__ __forceinline__ void store_bf16(uint16_t* dst, const float* v) {
 // d_ptr: the block's fp16 scale, or for q4_1 / q5_1 its 32-bit (d, lo) word.
 template <int P>
 __device__ __forceinline__ void quantize_block(const float* y, int qt, int r, uint8_t* qs_blk,
-                                               uint32_t* qh_word, void* d_ptr) {
+                                               uint32_t* qh_word, void* d_ptr, bool k_plane = false) {
   constexpr int L = 32 / P;
   uint8_t code[P];
   if (type_has_min(qt)) {
@@ -173,7 +173,7 @@ __device__ __forceinline__ void quantize_block(const float* y, int qt, int r, ui
     for (int j = 0; j < P; ++j) w |= uint32_t((code[j] >> 4) & 1) << (r * P + j);
 #pragma unroll
     for (int m = 1; m < L; m <<= 1) w |= __shfl_xor_sync(0xffffffffu, w, m);
-    if (r == 0) *qh_word = w;
+    if (r == 0) *qh_word = k_plane ? qh_k_from_gguf(w) : w;
   }
 }
 
@@ -260,7 +260,7 @@ __device__ __forceinline__ void store_vector(const kvq_cache& c, int which, int 
       const int blk = gi * P + lane / L;
       const int blk_bytes = qt == KVQ_TYPE_Q8_0 ? 32 : 16;
       quantize_block<P>(v + gi * P, qt, r, qs + blk * blk_bytes, qh ? qh + row * NB + blk : nullptr,
-                        dp + blk * (type_has_min(qt) ? 4 : 2));
+                        dp + blk * (type_has_min(qt) ? 4 : 2), which == 0);
     }
     if (outl) {  // one q8_0 block, slot = lane
       uint8_t* grp = static_cast<uint8_t*>(c.outl) + (row / 16) * kOutlTile;
