@@ -96,7 +96,9 @@ typedef int32_t kvq_status;
 #define KVQ_PLANE_K_D     2  /* fp16 [batch][kv_heads][max_ctx][d/32]       block scales; q4_1 / q5_1: fp16 pairs
                                 (d, lo) [..][d/32][2], i.e. the GGUF block header                                   */
 #define KVQ_PLANE_V_QS    3
-#define KVQ_PLANE_V_QH    4
+#define KVQ_PLANE_V_QH    4  /* uint32, as K_QH in size, GGUF bit order within each word, rows in pairs: for rows
+                                (2r, 2r + 1) and block j, word 2(r*d/32 + j) holds the two rows' bits 0-15 (row 2r in
+                                its low half) and word 2(r*d/32 + j) + 1 their bits 16-31 */
 #define KVQ_PLANE_V_D     5
 #define KVQ_PLANE_K_TAIL  6  /* bf16 [batch][kv_heads][tail_len][d]          rotated values, slot = pos % tail_len */
 #define KVQ_PLANE_V_TAIL  7

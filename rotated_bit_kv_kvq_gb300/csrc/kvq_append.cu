@@ -102,10 +102,10 @@ append_kernel(kvq_cache c, int rot_k, int rot_v, const void* __restrict__ kin, c
 // ---------------------------------------------------------------------------
 
 // One 32-value block held by one lane: quantize and store (qs: the block's
-// bytes; qh_word: q5_x high bits or null; d_ptr: fp16 d or the (d, lo) word).
+// bytes; qh: where the q5_x high-bit word goes; d_ptr: fp16 d or the (d, lo) word).
 // Every type, one value at a time (the general path).
 __device__ __forceinline__ void quantize_lane_block_scalar(const float (&y)[32], int qt, uint8_t* qs_blk,
-                                                        uint32_t* qh_word, void* d_ptr, bool k_plane) {
+                                                        const QhDst& qh, void* d_ptr) {
   // block parameters, then each code computed once straight into its packed byte
   float lo = 0.0f, id = 0.0f, off = 0.0f;
   int top = 0;
@@ -168,7 +168,7 @@ __device__ __forceinline__ void quantize_lane_block_scalar(const float (&y)[32],
     h |= ((c1 >> 4) & 1u) << (k + 16);
   }
   *reinterpret_cast<uint4*>(qs_blk) = make_uint4(w[0], w[1], w[2], w[3]);
-  if (type_has_qh(qt)) *qh_word = k_plane ? qh_k_from_gguf(h) : h;
+  if (type_has_qh(qt)) qh_put(qh, h);
 }
 
 // trunc(x * id + off) for two values x (the code before the clamp): the
@@ -197,10 +197,10 @@ __device__ __forceinline__ void code_bits2(float x0, float x1, float id, float o
 // top, nibble pack (byte k = code_k | code_{k+16} << 4) and for q5_0 bit 4 of
 // each code into the high-bit word.  q8_0, the scale + minimum types and blocks
 // whose scale or inverse is not finite take the scalar path.
-__device__ __forceinline__ void quantize_lane_block(float (&y)[32], int qt, uint8_t* qs_blk, uint32_t* qh_word,
-                                                    void* d_ptr, bool k_plane) {
+__device__ __forceinline__ void quantize_lane_block(float (&y)[32], int qt, uint8_t* qs_blk, const QhDst& qh,
+                                                    void* d_ptr) {
   if (qt != KVQ_TYPE_Q4_0 && qt != KVQ_TYPE_Q5_0) {
-    quantize_lane_block_scalar(y, qt, qs_blk, qh_word, d_ptr, k_plane);
+    quantize_lane_block_scalar(y, qt, qs_blk, qh, d_ptr);
     return;
   }
   // four interleaved partial maxima / minima (short dependency chains, few registers)
@@ -220,7 +220,7 @@ __device__ __forceinline__ void quantize_lane_block(float (&y)[32], int qt, uint
   const float d = q5 ? best_m / -16.0f : best_m / -8.0f;
   const float id = d != 0.0f ? 1.0f / d : 0.0f;
   if (!(hi > -lo || -lo > hi) || !(fabsf(best_m) <= 3.0e38f) || !(fabsf(id) <= 3.0e38f)) {
-    quantize_lane_block_scalar(y, qt, qs_blk, qh_word, d_ptr, k_plane);
+    quantize_lane_block_scalar(y, qt, qs_blk, qh, d_ptr);
     return;
   }
   *static_cast<__half*>(d_ptr) = __float2half_rn(d);
@@ -245,7 +245,7 @@ __device__ __forceinline__ void quantize_lane_block(float (&y)[32], int qt, uint
   *reinterpret_cast<uint4*>(qs_blk) =
       make_uint4(__byte_perm(half16[0], half16[1], 0x5410), __byte_perm(half16[2], half16[3], 0x5410),
                  __byte_perm(half16[4], half16[5], 0x5410), __byte_perm(half16[6], half16[7], 0x5410));
-  if (q5) *qh_word = k_plane ? qh_k_from_gguf(h) : h;
+  if (q5) qh_put(qh, h);
 }
 
 // Input kinds of the bulk kernel (a template parameter: no per-value select).
@@ -384,9 +384,9 @@ __device__ __forceinline__ void rows_task(const kvq_cache& c, int rot_k, int rot
     const size_t row = size_t(brow);
     uint8_t* qs = static_cast<uint8_t*>(which ? c.v_qs : c.k_qs) + row * qs_row_bytes(qt, D) +
                   sub * (qt == KVQ_TYPE_Q8_0 ? 32 : 16);
-    uint32_t* qh = static_cast<uint32_t*>(which ? c.v_qh : c.k_qh);
+    void* qh = which ? c.v_qh : c.k_qh;
     uint8_t* dp = static_cast<uint8_t*>(which ? c.v_d : c.k_d) + (row * NB + sub) * (type_has_min(qt) ? 4 : 2);
-    quantize_lane_block(y, qt, qs, qh ? qh + row * NB + sub : nullptr, dp, which == 0);
+    quantize_lane_block(y, qt, qs, qh_dst(qh, which == 0, row, NB, sub), dp);
   }
   if constexpr (OUTL) {
     // the slots' q8_0 block: amax over the vector's R lanes, then this lane's SL codes
@@ -474,8 +474,6 @@ append_rows_kernel(kvq_cache c, int rot_k, int rot_v, const void* __restrict__ k
 // ---------------------------------------------------------------------------
 // kvq_dequant_debug: one warp per position.
 // ---------------------------------------------------------------------------
-// a stored high-bit word in GGUF order (the K plane keeps another bit order)
-__device__ __forceinline__ uint32_t qh_gguf(uint32_t w, bool is_v) { return is_v ? w : qh_k_to_gguf(w); }
 
 template <int D, int G>
 __global__ void __launch_bounds__(128)
@@ -502,7 +500,7 @@ debug_kernel(kvq_cache c, int rot_side, int seq, int kv_head, int which, int t0,
     if (brow < 0 && lane == 0) atomicOr(&c.status[0], KVQ_DEV_ERR_PAGE);
     const size_t row = brow < 0 ? 0 : size_t(brow);  // an invalid page reads as row 0 (status set)
     const uint8_t* qs = static_cast<const uint8_t*>(is_v ? c.v_qs : c.k_qs) + row * qs_row_bytes(qt, D);
-    const uint32_t* qh = static_cast<const uint32_t*>(is_v ? c.v_qh : c.k_qh);
+    const void* qh = is_v ? c.v_qh : c.k_qh;
     // block header: fp16 d, or for q4_1 / q5_1 the (d, lo) pair, as bytes
     const int hb = type_has_min(qt) ? 4 : 2;
     const uint8_t* dp = static_cast<const uint8_t*>(is_v ? c.v_d : c.k_d) + row * NB * hb;
@@ -518,7 +516,7 @@ debug_kernel(kvq_cache c, int rot_side, int seq, int kv_head, int which, int t0,
       } else {
         const uint8_t byte = qs[blk * 16 + (k & 15)];
         code = k < 16 ? (byte & 15) : (byte >> 4);
-        if (type_has_qh(qt)) code |= int((qh_gguf(qh[row * NB + blk], is_v) >> k) & 1u) << 4;
+        if (type_has_qh(qt)) code |= int((qh_get(qh, !is_v, row, NB, blk) >> k) & 1u) << 4;
         code -= type_code_offset(qt);
       }
       v[j] = float(code) * dv + mv;
@@ -535,7 +533,7 @@ debug_kernel(kvq_cache c, int rot_side, int seq, int kv_head, int which, int t0,
         if (o < hb) {
           val = dp[blk * hb + o];
         } else if (o < hb + qhb) {
-          val = uint8_t(qh_gguf(qh[row * NB + blk], is_v) >> (8 * (o - hb)));
+          val = uint8_t(qh_get(qh, !is_v, row, NB, blk) >> (8 * (o - hb)));
         } else {
           val = qs[blk * qsb + (o - hb - qhb)];
         }

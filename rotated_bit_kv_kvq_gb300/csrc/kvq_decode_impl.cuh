@@ -346,6 +346,10 @@ __device__ __forceinline__ float hdr_scale(const uint32_t* w, int blk) {
 __device__ __forceinline__ uint32_t khb(uint32_t h, uint32_t r) {
   return (__funnelshift_r(h, h, r) & 0x00100010u) | 0x64006400u;
 }
+// q5 V high bits of a row-pair word (two tokens, 16 bits apart) at the mask's bits
+__device__ __forceinline__ uint32_t vhb(uint32_t w, uint32_t r, uint32_t mask) {
+  return (__funnelshift_r(w, w, r) & mask) | 0x64006400u;
+}
 
 template <int D, int KT, int VT, bool OL>
 __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, OL))
@@ -721,6 +725,11 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
   uint32_t kr[4];
 #pragma unroll
   for (int w = 0; w < 4; ++w) kr[w] = uint32_t(2 * tig + (w & 1) + 8 * (w >> 1) - 4) & 31u;
+  // q5 V: rotation bringing channel 2g (+1) of a row pair's low-half word to bits 4 / 20,
+  // and channel 2g + 16 (+17) of its high-half word to bits 8 / 24
+  uint32_t vr[4];
+#pragma unroll
+  for (int w = 0; w < 4; ++w) vr[w] = uint32_t(2 * g + (w & 1) - 4 - 4 * (w >> 1)) & 31u;
   uint32_t lbK[C::WK / 32], lbV[C::WV / 32];
   swz_lane<C::WK>(rr, mi >> 1, lbK);
   swz_lane<C::WV>(rr, mi >> 1, lbV);
@@ -985,16 +994,14 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
             uint32_t ma0 = 0x64006400u, ma1 = 0x64006400u, ma2 = 0x64006400u, ma3 = 0x64006400u;
             uint32_t mb0 = 0x64006400u, mb1 = 0x64006400u, mb2 = 0x64006400u, mb3 = 0x64006400u;
             if constexpr (C::V5) {
-              const uint32_t* vqh = reinterpret_cast<const uint32_t*>(st + C::off_vqh);
-              const int t = 2 * tig;
-              const uint32_t h0 = vqh[t * NB + blk] >> (2 * g), h1 = vqh[(t + 1) * NB + blk] >> (2 * g);
-              const uint32_t h8 = vqh[(t + 8) * NB + blk] >> (2 * g), h9 = vqh[(t + 9) * NB + blk] >> (2 * g);
-              const uint32_t wa = __byte_perm(h0, h1, 0x5410), wa2 = __byte_perm(h0, h1, 0x7632);
-              const uint32_t wb = __byte_perm(h8, h9, 0x5410), wb2 = __byte_perm(h8, h9, 0x7632);
-              ma0 = ((wa << 4) & 0x00100010u) | 0x64006400u;  ma1 = ((wa << 3) & 0x00100010u) | 0x64006400u;
-              ma2 = ((wa2 << 8) & 0x01000100u) | 0x64006400u; ma3 = ((wa2 << 7) & 0x01000100u) | 0x64006400u;
-              mb0 = ((wb << 4) & 0x00100010u) | 0x64006400u;  mb1 = ((wb << 3) & 0x00100010u) | 0x64006400u;
-              mb2 = ((wb2 << 8) & 0x01000100u) | 0x64006400u; mb3 = ((wb2 << 7) & 0x01000100u) | 0x64006400u;
+              // the V plane's row pairs: words [low halves of rows 2tig, 2tig+1], [high halves]
+              // (pair tig) and the same for rows 2tig+8, 2tig+9 (pair tig + 4)
+              const uint2 wa = *reinterpret_cast<const uint2*>(st + C::off_vqh + ((tig * NB + blk) * 2) * 4);
+              const uint2 wb = *reinterpret_cast<const uint2*>(st + C::off_vqh + (((tig + 4) * NB + blk) * 2) * 4);
+              ma0 = vhb(wa.x, vr[0], 0x00100010u); ma1 = vhb(wa.x, vr[1], 0x00100010u);
+              ma2 = vhb(wa.y, vr[2], 0x01000100u); ma3 = vhb(wa.y, vr[3], 0x01000100u);
+              mb0 = vhb(wb.x, vr[0], 0x00100010u); mb1 = vhb(wb.x, vr[1], 0x00100010u);
+              mb2 = vhb(wb.y, vr[2], 0x01000100u); mb3 = vhb(wb.y, vr[3], 0x01000100u);
             }
             const uint32_t a0[4] = {nib_pair(ra, 0, ma0, OFF), nib_pair(ra8, 0, ma1, OFF),
                                     nib_pair(rb, 0, mb0, OFF), nib_pair(rb8, 0, mb1, OFF)};

@@ -74,7 +74,10 @@ __device__ __forceinline__ long long body_row(const RowMap& m, int b, int h, int
 // that channels c and c + 2 (one fp16 pair of the decode's score operand) sit
 // 16 bits apart.  Three delta swaps of the bit index (bits 1<->2, 2<->3,
 // 3<->4) rotate index bits 1-4; the inverse applies them in reverse order.
-// The V plane keeps GGUF order.
+// The V plane keeps GGUF order within each word, but stores rows in pairs
+// (2r, 2r + 1): per (pair, block) one 32-bit word of the two rows' low 16 bits
+// [row 2r | row 2r + 1 << 16], then one of their high 16 bits, so that the two
+// consecutive tokens of one transposed P.V operand arrive in one word.
 // ---------------------------------------------------------------------------
 __host__ __device__ inline uint32_t delta_swap(uint32_t x, int d, uint32_t m) {
   const uint32_t t = ((x >> d) ^ x) & m;
@@ -89,6 +92,38 @@ __host__ __device__ inline uint32_t qh_k_to_gguf(uint32_t x) {
   x = delta_swap(x, 8, 0x0000FF00u);
   x = delta_swap(x, 4, 0x00F000F0u);
   return delta_swap(x, 2, 0x0C0C0C0Cu);
+}
+// 16-bit element index of half h (0: bits 0-15, 1: bits 16-31) of the V word of
+// (row, block); nb blocks per row.
+__host__ __device__ inline size_t qh_v_half(size_t row, int nb, int blk, int h) {
+  return ((((row >> 1) * size_t(nb) + size_t(blk)) * 2 + size_t(h)) * 2) + (row & 1);
+}
+// Where one block's high-bit word goes: its two 16-bit halves (lo == nullptr: none).
+struct QhDst {
+  uint16_t* lo;
+  uint16_t* hi;
+  bool k;
+};
+__device__ __forceinline__ QhDst qh_dst(void* plane, bool k_plane, size_t row, int nb, int blk) {
+  if (!plane) return QhDst{nullptr, nullptr, k_plane};
+  uint16_t* p = static_cast<uint16_t*>(plane);
+  if (k_plane) {
+    uint16_t* w = p + 2 * (row * size_t(nb) + size_t(blk));
+    return QhDst{w, w + 1, true};
+  }
+  return QhDst{p + qh_v_half(row, nb, blk, 0), p + qh_v_half(row, nb, blk, 1), false};
+}
+// store a high-bit word given in GGUF order
+__device__ __forceinline__ void qh_put(const QhDst& d, uint32_t gguf) {
+  const uint32_t w = d.k ? qh_k_from_gguf(gguf) : gguf;
+  *d.lo = uint16_t(w & 0xFFFFu);
+  *d.hi = uint16_t(w >> 16);
+}
+// a stored high-bit word, in GGUF order
+__device__ __forceinline__ uint32_t qh_get(const void* plane, bool k_plane, size_t row, int nb, int blk) {
+  if (k_plane) return qh_k_to_gguf(static_cast<const uint32_t*>(plane)[row * size_t(nb) + size_t(blk)]);
+  const uint16_t* p = static_cast<const uint16_t*>(plane);
+  return uint32_t(p[qh_v_half(row, nb, blk, 0)]) | (uint32_t(p[qh_v_half(row, nb, blk, 1)]) << 16);
 }
 
 // ---------------------------------------------------------------------------

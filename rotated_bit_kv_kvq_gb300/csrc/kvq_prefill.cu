@@ -164,7 +164,7 @@ __device__ __forceinline__ Raw8 fetch8(const SParams& p, bool is_v, int qt, bool
                                       : *reinterpret_cast<const uint2*>(qs + body_row * (D / 2) + blk * 16 + (w & 15));
   r.w.x = a.x;
   r.w.y = a.y;
-  if (type_has_qh(qt)) r.qh = is_v ? p.v_qh[body_row * NB + blk] : qh_k_to_gguf(p.k_qh[body_row * NB + blk]);
+  if (type_has_qh(qt)) r.qh = qh_get(is_v ? p.v_qh : p.k_qh, !is_v, body_row, NB, blk);
   return r;
 }
 

@@ -92,8 +92,8 @@ __device__ __forceinline__ void store_bf16(uint16_t* dst, const float* v) {
 // lanes (lane r of the block holds channels r*P .. r*P+P-1 in y[0..P-1]).
 // d_ptr: the block's fp16 scale, or for q4_1 / q5_1 its 32-bit (d, lo) word.
 template <int P>
-__device__ __forceinline__ void quantize_block(const float* y, int qt, int r, uint8_t* qs_blk,
-                                               uint32_t* qh_word, void* d_ptr, bool k_plane = false) {
+__device__ __forceinline__ void quantize_block(const float* y, int qt, int r, uint8_t* qs_blk, const QhDst& qh,
+                                               void* d_ptr) {
   constexpr int L = 32 / P;
   uint8_t code[P];
   if (type_has_min(qt)) {
@@ -173,7 +173,7 @@ __device__ __forceinline__ void quantize_block(const float* y, int qt, int r, ui
     for (int j = 0; j < P; ++j) w |= uint32_t((code[j] >> 4) & 1) << (r * P + j);
 #pragma unroll
     for (int m = 1; m < L; m <<= 1) w |= __shfl_xor_sync(0xffffffffu, w, m);
-    if (r == 0) *qh_word = k_plane ? qh_k_from_gguf(w) : w;
+    if (r == 0) qh_put(qh, w);
   }
 }
 
@@ -251,7 +251,7 @@ __device__ __forceinline__ void store_vector(const kvq_cache& c, int which, int 
   } else {
     const size_t row = size_t(brow);
     uint8_t* qs = static_cast<uint8_t*>(which ? c.v_qs : c.k_qs) + row * qs_row_bytes(qt, D);
-    uint32_t* qh = static_cast<uint32_t*>(which ? c.v_qh : c.k_qh);
+    void* qh = which ? c.v_qh : c.k_qh;
     uint8_t* dp = static_cast<uint8_t*>(which ? c.v_d : c.k_d) + row * NB * (type_has_min(qt) ? 4 : 2);
     constexpr int L = 32 / P;
     const int r = lane % L;
@@ -259,14 +259,14 @@ __device__ __forceinline__ void store_vector(const kvq_cache& c, int which, int 
     for (int gi = 0; gi < D / G; ++gi) {
       const int blk = gi * P + lane / L;
       const int blk_bytes = qt == KVQ_TYPE_Q8_0 ? 32 : 16;
-      quantize_block<P>(v + gi * P, qt, r, qs + blk * blk_bytes, qh ? qh + row * NB + blk : nullptr,
-                        dp + blk * (type_has_min(qt) ? 4 : 2), which == 0);
+      quantize_block<P>(v + gi * P, qt, r, qs + blk * blk_bytes, qh_dst(qh, which == 0, row, NB, blk),
+                        dp + blk * (type_has_min(qt) ? 4 : 2));
     }
     if (outl) {  // one q8_0 block, slot = lane
       uint8_t* grp = static_cast<uint8_t*>(c.outl) + (row / 16) * kOutlTile;
       uint8_t* oqs = grp + which * 512 + (row % 16) * 32;
       uint16_t* od = reinterpret_cast<uint16_t*>(grp + 1024 + which * 32) + row % 16;
-      quantize_block<1>(&ov, KVQ_TYPE_Q8_0, lane, oqs, nullptr, od);
+      quantize_block<1>(&ov, KVQ_TYPE_Q8_0, lane, oqs, QhDst{nullptr, nullptr, false}, od);
     }
   }
   if (to_tail) {
