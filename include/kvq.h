@@ -88,7 +88,9 @@ typedef int32_t kvq_status;
 
 /* ---- planes of a cache (kvq_plane_bytes) --------------------------------- */
 /* body planes: rows [batch][kv_heads][max_ctx], or [n_pages][kv_heads][page_tokens] when paged */
-#define KVQ_PLANE_K_QS    0  /* uint8 [batch][kv_heads][max_ctx][qs_row]    qs_row = d (q8_0) or d/2 (the others) */
+#define KVQ_PLANE_K_QS    0  /* uint8 [batch][kv_heads][max_ctx][qs_row]    qs_row = d (q8_0) or d/2 (the others);
+                                the GGUF qs bytes of the token's blocks, except that q8_0 codes are stored offset
+                                binary (code + 128, the GGUF byte XOR 0x80); kvq_dequant_debug returns GGUF bytes */
 #define KVQ_PLANE_K_QH    1  /* uint32 [batch][kv_heads][max_ctx][d/32]     q5_0 / q5_1 only (0 bytes otherwise);
                                 the bit of channel c = 4t + 2b + e of a block sits at bit 16b + 2t + e (t < 8; b, e
                                 in {0, 1}), a permutation of the GGUF word, whose bit c is bit 4 of code c; the V

@@ -145,7 +145,7 @@ __device__ __forceinline__ void quantize_lane_block_scalar(const float (&y)[32],
   }
   // code of value j, operation by operation as the block definitions state
   auto code_of = [&](int j) -> uint32_t {
-    if (q8) return uint32_t(uint8_t(int8_t(int(roundf(__fmul_rn(y[j], id))))));
+    if (q8) return uint32_t(uint8_t(int8_t(int(roundf(__fmul_rn(y[j], id)))))) ^ 0x80u;  // stored offset binary
     if (mn) return uint32_t(min(top, __float2int_rz(__fadd_rn(__fmul_rn(__fsub_rn(y[j], lo), id), off))));
     return uint32_t(min(top, __float2int_rz(__fadd_rn(__fmul_rn(y[j], id), off))));
   };
@@ -512,7 +512,7 @@ debug_kernel(kvq_cache c, int rot_side, int seq, int kv_head, int which, int t0,
       const float mv = type_has_min(qt) ? __half2float(reinterpret_cast<const __half*>(dp + blk * hb)[1]) : 0.0f;
       int code;
       if (qt == KVQ_TYPE_Q8_0) {
-        code = int(int8_t(qs[blk * 32 + k]));
+        code = int(qs[blk * 32 + k]) - 128;  // stored offset binary
       } else {
         const uint8_t byte = qs[blk * 16 + (k & 15)];
         code = k < 16 ? (byte & 15) : (byte >> 4);
@@ -535,7 +535,7 @@ debug_kernel(kvq_cache c, int rot_side, int seq, int kv_head, int which, int t0,
         } else if (o < hb + qhb) {
           val = uint8_t(qh_get(qh, !is_v, row, NB, blk) >> (8 * (o - hb)));
         } else {
-          val = qs[blk * qsb + (o - hb - qhb)];
+          val = qs[blk * qsb + (o - hb - qhb)] ^ (qt == KVQ_TYPE_Q8_0 ? 0x80u : 0u);  // q8_0: back to GGUF bytes
         }
         ob[idx] = val;
       }

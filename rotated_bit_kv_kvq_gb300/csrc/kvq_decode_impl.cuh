@@ -759,7 +759,6 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
         for (int blk = 0; blk < NB; ++blk) {
           uint32_t r0, r1, r2, r3;
           ldsm_x4(kbase + lbK[swz_lane_idx<C::WK>(2 * blk)] + swz_box_off<C::WK>(2 * blk), r0, r1, r2, r3);
-          r0 ^= 0x80808080u; r1 ^= 0x80808080u; r2 ^= 0x80808080u; r3 ^= 0x80808080u;
           const uint32_t alo[4] = {i8_pair<0, 2>(r0), i8_pair<0, 2>(r1), i8_pair<1, 3>(r0), i8_pair<1, 3>(r1)};
           const uint32_t ahi[4] = {i8_pair<0, 2>(r2), i8_pair<0, 2>(r3), i8_pair<1, 3>(r2), i8_pair<1, 3>(r3)};
           const uint4 qa = qfs[(blk * 2) * 32 + lane], qb = qfs[(blk * 2 + 1) * 32 + lane];
@@ -967,7 +966,6 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
           pscaled(blk, bh0, bl0, bh1, bl1);
           uint32_t r0, r1, r2, r3;
           ldsm_x4_t(vbase + lbV[swz_lane_idx<C::WV>(2 * blk)] + swz_box_off<C::WV>(2 * blk), r0, r1, r2, r3);
-          r0 ^= 0x80808080u; r1 ^= 0x80808080u; r2 ^= 0x80808080u; r3 ^= 0x80808080u;
           const uint32_t a0[4] = {i8_pair<0, 2>(r0), i8_pair<1, 3>(r0), i8_pair<0, 2>(r1), i8_pair<1, 3>(r1)};
           const uint32_t a1[4] = {i8_pair<0, 2>(r2), i8_pair<1, 3>(r2), i8_pair<0, 2>(r3), i8_pair<1, 3>(r3)};
           mma16816(acc[blk][0], a0, bh0, bh1);

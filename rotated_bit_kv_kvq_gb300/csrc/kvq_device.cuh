@@ -221,7 +221,9 @@ __host__ __device__ constexpr uint32_t neg_off_x16_bits(int off) {
   return (off == 8 ? 0xD480u : off == 16 ? 0xD500u : 0xD400u) * 0x10001u;
 }
 
-// Signed bytes i0, i1 (0..3) of r -> fp16 pair (code).  `ru` = r ^ 0x80808080.
+// Offset-binary bytes i0, i1 (0..3) of ru (code + 128: the body planes store q8_0
+// codes so; the outlier plane's signed bytes are XORed with 0x80 first) -> fp16
+// pair (code).
 template <int I0, int I1>
 __device__ __forceinline__ uint32_t i8_pair(uint32_t ru) {
   uint32_t t = __byte_perm(ru, 0x64646464u, I0 | (4 << 4) | (I1 << 8) | (4 << 12));

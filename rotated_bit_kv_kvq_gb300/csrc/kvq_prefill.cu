@@ -189,7 +189,8 @@ __device__ __forceinline__ void decode8(const Raw8& r, int qt, bool valid, bool 
   const float mn = type_has_min(qt) ? __half2float(__ushort_as_half(uint16_t(r.hdr >> 16))) * kInvScale : 0.0f;
   if (qt == KVQ_TYPE_Q8_0) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) x[e] = float(int8_t((e < 4 ? r.w.x : r.w.y) >> (8 * (e & 3)))) * sc;
+    for (int e = 0; e < 8; ++e)  // stored offset binary: code + 128
+      x[e] = float(int(((e < 4 ? r.w.x : r.w.y) >> (8 * (e & 3))) & 0xFFu) - 128) * sc;
   } else {
     // byte i of a block holds element i (low nibble) and element i + 16 (high nibble)
     const int shift = w < 16 ? 0 : 4;

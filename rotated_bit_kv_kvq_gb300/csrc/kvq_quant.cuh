@@ -91,9 +91,12 @@ __device__ __forceinline__ void store_bf16(uint16_t* dst, const float* v) {
 // Quantize and store one 32-value block whose values are spread over L = 32/P
 // lanes (lane r of the block holds channels r*P .. r*P+P-1 in y[0..P-1]).
 // d_ptr: the block's fp16 scale, or for q4_1 / q5_1 its 32-bit (d, lo) word.
+// q8_0 codes go out as stored in the body planes, offset binary (code + 128,
+// i.e. the GGUF byte XOR 0x80), unless `q8_signed` (the outlier plane keeps the
+// GGUF bytes).
 template <int P>
 __device__ __forceinline__ void quantize_block(const float* y, int qt, int r, uint8_t* qs_blk, const QhDst& qh,
-                                               void* d_ptr) {
+                                               void* d_ptr, bool q8_signed = false) {
   constexpr int L = 32 / P;
   uint8_t code[P];
   if (type_has_min(qt)) {
@@ -143,7 +146,8 @@ __device__ __forceinline__ void quantize_block(const float* y, int qt, int r, ui
       d = best_a / 127.0f;
       const float id = d != 0.0f ? 1.0f / d : 0.0f;
 #pragma unroll
-      for (int j = 0; j < P; ++j) code[j] = uint8_t(int8_t(int(roundf(__fmul_rn(y[j], id)))));
+      for (int j = 0; j < P; ++j)
+        code[j] = uint8_t(int8_t(int(roundf(__fmul_rn(y[j], id))))) ^ (q8_signed ? 0u : 0x80u);
     } else {
       const bool q5 = qt == KVQ_TYPE_Q5_0;
       d = q5 ? best_m / -16.0f : best_m / -8.0f;
@@ -266,7 +270,7 @@ __device__ __forceinline__ void store_vector(const kvq_cache& c, int which, int 
       uint8_t* grp = static_cast<uint8_t*>(c.outl) + (row / 16) * kOutlTile;
       uint8_t* oqs = grp + which * 512 + (row % 16) * 32;
       uint16_t* od = reinterpret_cast<uint16_t*>(grp + 1024 + which * 32) + row % 16;
-      quantize_block<1>(&ov, KVQ_TYPE_Q8_0, lane, oqs, QhDst{nullptr, nullptr, false}, od);
+      quantize_block<1>(&ov, KVQ_TYPE_Q8_0, lane, oqs, QhDst{nullptr, nullptr, false}, od, true);
     }
   }
   if (to_tail) {
