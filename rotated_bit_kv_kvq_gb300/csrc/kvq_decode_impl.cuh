@@ -63,27 +63,33 @@ struct Cfg {
   static constexpr bool K5 = type_has_qh(KT), V5 = type_has_qh(VT);
   static constexpr bool K1 = type_has_min(KT), V1 = type_has_min(VT);   // scale + minimum blocks
   static constexpr int KH = K1 ? 4 : 2, VH = V1 ? 4 : 2;                // block header bytes
-  // body stage: 16 tokens
-  static constexpr int off_kqs = 0;
-  static constexpr int off_vqs = align_up(16 * rowK, 1024);
-  static constexpr int off_kd = off_vqs + align_up(16 * rowV, 16);
-  static constexpr int off_vd = off_kd + 16 * NB * KH;
-  static constexpr int off_kqh = off_vd + 16 * NB * VH;
-  static constexpr int off_vqh = off_kqh + (K5 ? 16 * NB * 4 : 0);
-  // outlier channels (OL): one 16-row group of the outlier plane (K codes, V codes, K scales, V scales)
-  static constexpr int off_ko = align_up(off_vqh + (V5 ? 16 * NB * 4 : 0), 16);
-  static constexpr int off_vo = off_ko + 16 * 32;
-  static constexpr int off_kod = off_vo + 16 * 32;
-  static constexpr int off_vod = off_kod + 16 * 2;
-  static constexpr int body_bytes = OL ? off_vod + 16 * 2 : off_vqh + (V5 ? 16 * NB * 4 : 0);
-  static constexpr uint32_t body_tx =
-      16 * rowK + 16 * rowV + 16 * NB * (KH + VH) + (K5 ? 64 * NB : 0) + (V5 ? 64 * NB : 0) + (OL ? 2 * 16 * 34 : 0);
   // tail stage: TT tokens of bf16 K and V
   static constexpr int TT = D >= 256 ? 8 : 16;
   static constexpr int WT = box_w(2 * D);
   static constexpr int off_kt = 0;
   static constexpr int off_vt = align_up(TT * 2 * D, 1024);
   static constexpr int tail_bytes = off_vt + TT * 2 * D;
+  // body stage: RB tokens.  Up to head_dim 128 (no outlier channels) a body tile holds
+  // 32 tokens, two 16-row halves, when that fits the tail stage's size: twice the
+  // independent work per tile and half the per-tile overhead per token.
+  static constexpr int body32 = align_up(32 * rowK, 1024) + align_up(32 * rowV, 16) + 32 * NB * (KH + VH) +
+                                (K5 ? 32 * NB * 4 : 0) + (V5 ? 32 * NB * 4 : 0);
+  static constexpr int RB = (D <= 128 && !OL && body32 <= tail_bytes) ? 32 : 16;
+  static constexpr int HB = RB / 16;  // 16-row halves of a body tile
+  static constexpr int off_kqs = 0;
+  static constexpr int off_vqs = align_up(RB * rowK, 1024);
+  static constexpr int off_kd = off_vqs + align_up(RB * rowV, 16);
+  static constexpr int off_vd = off_kd + RB * NB * KH;
+  static constexpr int off_kqh = off_vd + RB * NB * VH;
+  static constexpr int off_vqh = off_kqh + (K5 ? RB * NB * 4 : 0);
+  // outlier channels (OL): one 16-row group of the outlier plane (K codes, V codes, K scales, V scales)
+  static constexpr int off_ko = align_up(off_vqh + (V5 ? 16 * NB * 4 : 0), 16);
+  static constexpr int off_vo = off_ko + 16 * 32;
+  static constexpr int off_kod = off_vo + 16 * 32;
+  static constexpr int off_vod = off_kod + 16 * 2;
+  static constexpr int body_bytes = OL ? off_vod + 16 * 2 : off_vqh + (V5 ? RB * NB * 4 : 0);
+  static constexpr uint32_t body_tx = RB * rowK + RB * rowV + RB * NB * (KH + VH) + (K5 ? 4 * RB * NB : 0) +
+                                      (V5 ? 4 * RB * NB : 0) + (OL ? 2 * 16 * 34 : 0);
   static constexpr uint32_t tail_tx = 2 * TT * 2 * D;
   static constexpr int stage = align_up(body_bytes > tail_bytes ? body_bytes : tail_bytes, 1024);
   static constexpr int NS_raw = kSmemBudget / (kWarps * stage);
@@ -491,7 +497,7 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
             const long long dstart = Pseg + p.cost_gap;  // the segment's data starts after its gap
             if (dstart < x1 && dstart + cs > x0) {
               use = true;
-              const int tile = is_tail ? C::TT : 16;
+              const int tile = is_tail ? C::TT : C::RB;
               t_begin = seg_token(x0, dstart, c, ntok, tile);
               t_end = seg_token(x1, dstart, c, ntok, tile);
               slot = p.fused ? B + int(piece) + b : int(piece) + 2 * b + kind;
@@ -518,7 +524,7 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     if (!found) break;
 
   // ---- this warp's tiles, and the producer (lane 0) --------------------
-  const int TR = is_tail ? C::TT : 16;                       // rows per tile
+  const int TR = is_tail ? C::TT : C::RB;                    // rows per tile
   const int ntiles = (t_end - t_begin + TR - 1) / TR;
   const int my_tiles = ntiles > warp ? (ntiles - warp + kWarps - 1) / kWarps : 0;
   uint8_t* wstage = smem + warp * NS * C::stage;
@@ -541,7 +547,7 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
       }
     } else {
       size_t row = bh * p.max_ctx + t0;
-      if (paged) {  // a 16-token tile never crosses a page
+      if (paged) {  // a body tile (16 or 32 tokens, aligned) never crosses a page (a multiple of 64)
         const int pg = p.rows.page_table[(size_t)b * (p.max_ctx / p.rows.page_tokens) + t0 / p.rows.page_tokens];
         const bool bad = pg < 0 || pg >= p.rows.n_pages;
         bad_stage = (bad_stage & ~(1u << s)) | (bad ? (1u << s) : 0u);
@@ -553,16 +559,22 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
         }
       }
       mbar_arrive_expect_tx(&wbar[s], C::body_tx);
+      // per box column of W bytes: RB rows, as RB / 16 stacked 16-row boxes
 #pragma unroll
-      for (int x = 0; x < C::rowK; x += C::WK)
-        tma_2d_g2s(st + C::off_kqs + (x / C::WK) * 16 * C::WK, &tmK, x, int(row), &wbar[s]);
+      for (int hb = 0; hb < C::HB; ++hb) {
 #pragma unroll
-      for (int x = 0; x < C::rowV; x += C::WV)
-        tma_2d_g2s(st + C::off_vqs + (x / C::WV) * 16 * C::WV, &tmV, x, int(row), &wbar[s]);
-      bulk_g2s(st + C::off_kd, p.k_d + row * NB * C::KH, 16 * NB * C::KH, &wbar[s]);
-      bulk_g2s(st + C::off_vd, p.v_d + row * NB * C::VH, 16 * NB * C::VH, &wbar[s]);
-      if constexpr (C::K5) bulk_g2s(st + C::off_kqh, p.k_qh + row * NB, 16 * NB * 4, &wbar[s]);
-      if constexpr (C::V5) bulk_g2s(st + C::off_vqh, p.v_qh + row * NB, 16 * NB * 4, &wbar[s]);
+        for (int x = 0; x < C::rowK; x += C::WK)
+          tma_2d_g2s(st + C::off_kqs + (x / C::WK) * C::RB * C::WK + hb * 16 * C::WK, &tmK, x, int(row) + 16 * hb,
+                     &wbar[s]);
+#pragma unroll
+        for (int x = 0; x < C::rowV; x += C::WV)
+          tma_2d_g2s(st + C::off_vqs + (x / C::WV) * C::RB * C::WV + hb * 16 * C::WV, &tmV, x, int(row) + 16 * hb,
+                     &wbar[s]);
+      }
+      bulk_g2s(st + C::off_kd, p.k_d + row * NB * C::KH, C::RB * NB * C::KH, &wbar[s]);
+      bulk_g2s(st + C::off_vd, p.v_d + row * NB * C::VH, C::RB * NB * C::VH, &wbar[s]);
+      if constexpr (C::K5) bulk_g2s(st + C::off_kqh, p.k_qh + row * NB, C::RB * NB * 4, &wbar[s]);
+      if constexpr (C::V5) bulk_g2s(st + C::off_vqh, p.v_qh + row * NB, C::RB * NB * 4, &wbar[s]);
       if constexpr (OL) {  // outlier rows: 32 codes + one fp16 scale per token, K and V
         // the tile's 16-row group of the outlier plane has the stage's layout: one copy
         bulk_g2s(st + C::off_ko, static_cast<const uint8_t*>(p.cache.outl) + (row / 16) * kOutlTile, kOutlTile,
@@ -743,22 +755,34 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     // positions past the end, or a whole tile whose page id lies outside the pool, are masked
     int t_lim = t_end;
     if (paged && ((__shfl_sync(0xffffffffu, bad_stage, 0) >> s) & 1u)) t_lim = t0;
-    const bool v0 = t0 + g < t_lim, v8 = (TR == 16) && (t0 + g + 8 < t_lim);
+    // validity of the lane's rows 16hh + g and 16hh + g + 8 of the tile (a tail tile is
+    // one half of 16 or 8 rows)
+    constexpr int HB = C::HB;
+    bool vv[HB][2];
+#pragma unroll
+    for (int hh = 0; hh < HB; ++hh) {
+      vv[hh][0] = 16 * hh < TR && t0 + 16 * hh + g < t_lim;
+      vv[hh][1] = 16 * hh + 8 < TR && t0 + 16 * hh + g + 8 < t_lim;
+    }
 
-    float S[4] = {0.f, 0.f, 0.f, 0.f};
+    float S[HB][4];
+#pragma unroll
+    for (int hh = 0; hh < HB; ++hh) S[hh][0] = S[hh][1] = S[hh][2] = S[hh][3] = 0.f;
     if (!is_tail) {
-      // ------------------------------- body: scores
-      // block headers of this lane's tokens g and g+8, all blocks
+#pragma unroll
+      for (int hh = 0; hh < HB; ++hh) {
+      // ------------------------------- body: scores of rows 16hh .. 16hh + 15
+      // block headers of this lane's tokens 16hh + g and 16hh + g + 8, all blocks
       constexpr int KHH = C::KH / 2;
       uint32_t kw0[NB * KHH / 2], kw8[NB * KHH / 2];
-      lds_words<NB * C::KH>(st + C::off_kd + g * NB * C::KH, kw0);
-      lds_words<NB * C::KH>(st + C::off_kd + (g + 8) * NB * C::KH, kw8);
-      const uint32_t kbase = smem_u32(st + C::off_kqs);
+      lds_words<NB * C::KH>(st + C::off_kd + (16 * hh + g) * NB * C::KH, kw0);
+      lds_words<NB * C::KH>(st + C::off_kd + (16 * hh + g + 8) * NB * C::KH, kw8);
+      const uint32_t kbase = smem_u32(st + C::off_kqs) + hh * 16 * C::WK;
       if constexpr (KT == KVQ_TYPE_Q8_0) {
 #pragma unroll
         for (int blk = 0; blk < NB; ++blk) {
           uint32_t r0, r1, r2, r3;
-          ldsm_x4(kbase + lbK[swz_lane_idx<C::WK>(2 * blk)] + swz_box_off<C::WK>(2 * blk), r0, r1, r2, r3);
+          ldsm_x4(kbase + lbK[swz_lane_idx<C::WK>(2 * blk)] + swz_box_off<C::WK, C::RB>(2 * blk), r0, r1, r2, r3);
           const uint32_t alo[4] = {i8_pair<0, 2>(r0), i8_pair<0, 2>(r1), i8_pair<1, 3>(r0), i8_pair<1, 3>(r1)};
           const uint32_t ahi[4] = {i8_pair<0, 2>(r2), i8_pair<0, 2>(r3), i8_pair<1, 3>(r2), i8_pair<1, 3>(r3)};
           const uint4 qa = qfs[(blk * 2) * 32 + lane], qb = qfs[(blk * 2 + 1) * 32 + lane];
@@ -768,15 +792,15 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
           mma16816(cc, ahi, qb.x, qb.y);
           mma16816(cc, ahi, qb.z, qb.w);
           const float dk0 = hdr_scale<KHH>(kw0, blk), dk8 = hdr_scale<KHH>(kw8, blk);
-          S[0] += dk0 * cc[0]; S[1] += dk0 * cc[1];
-          S[2] += dk8 * cc[2]; S[3] += dk8 * cc[3];
+          S[hh][0] += dk0 * cc[0]; S[hh][1] += dk0 * cc[1];
+          S[hh][2] += dk8 * cc[2]; S[hh][3] += dk8 * cc[3];
         }
       } else {
         constexpr uint32_t OFF = (0x6400u + uint32_t(type_code_offset(KT))) * 0x10001u;
 #pragma unroll
         for (int bp = 0; bp < NB; bp += 2) {
           uint32_t rr4[4];
-          ldsm_x4(kbase + lbK[swz_lane_idx<C::WK>(bp)] + swz_box_off<C::WK>(bp), rr4[0], rr4[1], rr4[2], rr4[3]);
+          ldsm_x4(kbase + lbK[swz_lane_idx<C::WK>(bp)] + swz_box_off<C::WK, C::RB>(bp), rr4[0], rr4[1], rr4[2], rr4[3]);
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int blk = bp + e;
@@ -785,7 +809,7 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
             uint32_t m10 = 0x64006400u, m11 = 0x64006400u, m12 = 0x64006400u, m13 = 0x64006400u;
             if constexpr (C::K5) {
               const uint32_t* kqh = reinterpret_cast<const uint32_t*>(st + C::off_kqh);
-              const uint32_t ha = kqh[g * NB + blk], hb = kqh[(g + 8) * NB + blk];
+              const uint32_t ha = kqh[(16 * hh + g) * NB + blk], hb = kqh[(16 * hh + g + 8) * NB + blk];
               m00 = khb(ha, kr[0]); m01 = khb(ha, kr[1]); m02 = khb(ha, kr[2]); m03 = khb(ha, kr[3]);
               m10 = khb(hb, kr[0]); m11 = khb(hb, kr[1]); m12 = khb(hb, kr[2]); m13 = khb(hb, kr[3]);
             }
@@ -800,17 +824,18 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
             mma16816(cc, ahi, qb.x, qb.y);
             mma16816(cc, ahi, qb.z, qb.w);
             const float dk0 = hdr_scale<KHH>(kw0, blk), dk8 = hdr_scale<KHH>(kw8, blk);
-            S[0] += dk0 * cc[0]; S[1] += dk0 * cc[1];
-            S[2] += dk8 * cc[2]; S[3] += dk8 * cc[3];
+            S[hh][0] += dk0 * cc[0]; S[hh][1] += dk0 * cc[1];
+            S[hh][2] += dk8 * cc[2]; S[hh][3] += dk8 * cc[3];
             if constexpr (C::K1) {  // + lo * (sum of the block's q), per token and head
               const float mk0 = h2f(kw0[blk], 1), mk8 = h2f(kw8[blk], 1);
               const float2 qs2 = *reinterpret_cast<const float2*>(qsum + blk * kMaxHeads + 2 * tig);
-              S[0] += mk0 * qs2.x; S[1] += mk0 * qs2.y;
-              S[2] += mk8 * qs2.x; S[3] += mk8 * qs2.y;
+              S[hh][0] += mk0 * qs2.x; S[hh][1] += mk0 * qs2.y;
+              S[hh][2] += mk8 * qs2.x; S[hh][3] += mk8 * qs2.y;
             }
           }
         }
       }
+      }  // halves
       if constexpr (OL) {  // + d_O[t] * (codes_O[t] . q_O[h]): one q8_0 block in plain 32-byte rows
         uint32_t r0, r1, r2, r3;
         ldsm_x4(smem_u32(st + C::off_ko) + rr * 32 + 16 * (mi >> 1), r0, r1, r2, r3);
@@ -823,10 +848,11 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
         mma16816(cc, alo, qa.z, qa.w);
         mma16816(cc, ahi, qb.x, qb.y);
         mma16816(cc, ahi, qb.z, qb.w);
+        static_assert(HB == 1, "outlier-channel tiles are 16 rows");
         const __half* kod = reinterpret_cast<const __half*>(st + C::off_kod);
         const float dk0 = __half2float(kod[g]), dk8 = __half2float(kod[g + 8]);
-        S[0] += dk0 * cc[0]; S[1] += dk0 * cc[1];
-        S[2] += dk8 * cc[2]; S[3] += dk8 * cc[3];
+        S[0][0] += dk0 * cc[0]; S[0][1] += dk0 * cc[1];
+        S[0][2] += dk8 * cc[2]; S[0][3] += dk8 * cc[3];
       }
     } else {
       // ------------------------------- tail (bf16, stored as fp16 * 2^-8): scores
@@ -849,7 +875,7 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
           mma16816(cc, a, qa.z, qa.w);
         }
 #pragma unroll
-      for (int r = 0; r < 4; ++r) S[r] = 256.0f * cc[r];
+      for (int r = 0; r < 4; ++r) S[0][r] = 256.0f * cc[r];
     }
 
     // ---- online softmax (base 2); rows g, g+8 = tokens, cols 2tig, 2tig+1 = heads
@@ -857,11 +883,19 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     // outside the pool): a warp-uniform branch.  8-row tail tiles leave the mma's
     // rows g+8 empty in every tile.
     const bool partial = t0 + TR > t_lim;
-    if (partial || TR < 16) {
-      if (!v0) { S[0] = -INFINITY; S[1] = -INFINITY; }
-      if (!v8) { S[2] = -INFINITY; S[3] = -INFINITY; }
+    if (partial || TR < 16 * HB) {
+#pragma unroll
+      for (int hh = 0; hh < HB; ++hh) {
+        if (!vv[hh][0]) { S[hh][0] = -INFINITY; S[hh][1] = -INFINITY; }
+        if (!vv[hh][1]) { S[hh][2] = -INFINITY; S[hh][3] = -INFINITY; }
+      }
     }
-    float mx0 = fmaxf(S[0], S[2]), mx1 = fmaxf(S[1], S[3]);
+    float mx0 = fmaxf(S[0][0], S[0][2]), mx1 = fmaxf(S[0][1], S[0][3]);
+#pragma unroll
+    for (int hh = 1; hh < HB; ++hh) {
+      mx0 = fmaxf(mx0, fmaxf(S[hh][0], S[hh][2]));
+      mx1 = fmaxf(mx1, fmaxf(S[hh][1], S[hh][3]));
+    }
     // The running maximum changes only when some score of the tile exceeds it; for
     // long contexts that is rare, and the reduction over the tile's rows and the
     // rescale run only then.
@@ -896,35 +930,46 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
       m0 = nm0; m1 = nm1;
     }
     const float ms0 = m0 == -INFINITY ? 0.0f : m0, ms1 = m1 == -INFINITY ? 0.0f : m1;
-    const float p0 = fast_exp2(S[0] - ms0), p1 = fast_exp2(S[1] - ms1);
-    const float p2 = fast_exp2(S[2] - ms0), p3 = fast_exp2(S[3] - ms1);
-    l0 += p0 + p2; l1 += p1 + p3;
+    float pp[HB][4];
+#pragma unroll
+    for (int hh = 0; hh < HB; ++hh) {
+      pp[hh][0] = fast_exp2(S[hh][0] - ms0); pp[hh][1] = fast_exp2(S[hh][1] - ms1);
+      pp[hh][2] = fast_exp2(S[hh][2] - ms0); pp[hh][3] = fast_exp2(S[hh][3] - ms1);
+      l0 += pp[hh][0] + pp[hh][2]; l1 += pp[hh][1] + pp[hh][3];
+    }
 
     // ---- P.V.  P is split into fp16 hi + lo parts and transposed once per tile
     // (movmatrix) into the B-fragment layout: tokens 2tig, 2tig+1 (ph0, pl0) and
     // 2tig+8, 2tig+9 (ph1, pl1) of head g.  Each block scales both parts by the
     // tokens' V scales in fp16 arithmetic (hscale_split: ~22 bits, like P itself);
     // the codes are exact.
-    uint32_t ph0, pl0, ph1, pl1;
-    {
+    uint32_t ph0[HB], pl0[HB], ph1[HB], pl1[HB];
+    bool vt0[HB], vt1[HB], vt8[HB], vt9[HB];  // validity of the lane's transposed rows
+#pragma unroll
+    for (int hh = 0; hh < HB; ++hh) {
+      const float p0 = pp[hh][0], p1 = pp[hh][1], p2 = pp[hh][2], p3 = pp[hh][3];
       const uint32_t h0 = pack_h2(p0, p1), h1 = pack_h2(p2, p3);
       const float2 f0 = __half22float2(u32_as_h2(h0)), f1 = __half22float2(u32_as_h2(h1));
       const uint32_t r0 = pack_h2(p0 - f0.x, p1 - f0.y), r1 = pack_h2(p2 - f1.x, p3 - f1.y);
-      ph0 = movm_t(h0); pl0 = movm_t(r0); ph1 = movm_t(h1); pl1 = movm_t(r1);
+      ph0[hh] = movm_t(h0); pl0[hh] = movm_t(r0); ph1[hh] = movm_t(h1); pl1[hh] = movm_t(r1);
+      const int tt = t0 + 16 * hh + 2 * tig;  // first token of this lane's transposed rows
+      vt0[hh] = 16 * hh < TR && tt < t_lim;
+      vt1[hh] = 16 * hh < TR && tt + 1 < t_lim;
+      vt8[hh] = 16 * hh + 8 < TR && tt + 8 < t_lim;
+      vt9[hh] = 16 * hh + 8 < TR && tt + 9 < t_lim;
     }
-    const int tt = t0 + 2 * tig;  // first token of this lane's transposed rows
-    const bool vt0 = tt < t_lim, vt1 = tt + 1 < t_lim;
-    const bool vt8 = TR == 16 && tt + 8 < t_lim, vt9 = TR == 16 && tt + 9 < t_lim;
     if (!is_tail) {
-      // V block headers of the lane's four transposed tokens, all blocks; zero for rows
-      // past the end (their bytes may be anything, and 0 * Inf would poison the sum)
+#pragma unroll
+      for (int hh = 0; hh < HB; ++hh) {
+      // V block headers of the lane's four transposed tokens (rows 16hh + ...), all blocks;
+      // zero for rows past the end (their bytes may be anything, and 0 * Inf would poison the sum)
       constexpr int VHH = C::VH / 2;              // halves per block header
       constexpr int VW = NB * VHH / 2;            // header words per token
       uint32_t vh[4][VW];
       {
         const uint8_t* vd = st + C::off_vd;
-        const int trow[4] = {2 * tig, 2 * tig + 1, 2 * tig + 8, 2 * tig + 9};
-        const bool tok_ok[4] = {vt0, vt1, vt8, vt9};
+        const int trow[4] = {16 * hh + 2 * tig, 16 * hh + 2 * tig + 1, 16 * hh + 2 * tig + 8, 16 * hh + 2 * tig + 9};
+        const bool tok_ok[4] = {vt0[hh], vt1[hh], vt8[hh], vt9[hh]};
 #pragma unroll
         for (int i = 0; i < 4; ++i) lds_words<NB * C::VH>(vd + trow[i] * NB * C::VH, vh[i]);
         if (partial) {  // full tiles hold written body rows only
@@ -941,15 +986,15 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
       };
       // P times the V scale of block blk, as fp16 hi + lo B fragments
       auto pscaled = [&](int blk, uint32_t& bh0, uint32_t& bl0, uint32_t& bh1, uint32_t& bl1) {
-        hscale_split(ph0, pl0, dvpair(blk, 0, 1), bh0, bl0);
-        hscale_split(ph1, pl1, dvpair(blk, 2, 3), bh1, bl1);
+        hscale_split(ph0[hh], pl0[hh], dvpair(blk, 0, 1), bh0, bl0);
+        hscale_split(ph1[hh], pl1[hh], dvpair(blk, 2, 3), bh1, bl1);
       };
       // the minimum adds sum_t P[t][h] * lo[t][blk] to every channel of the block: the
       // lane's share for head g is summed here in fp32 and spread over the channels at the end
       float pz[4] = {0.f, 0.f, 0.f, 0.f};
       if constexpr (C::V1) {
-        const float2 a0 = __half22float2(u32_as_h2(ph0)), b0 = __half22float2(u32_as_h2(pl0));
-        const float2 a1 = __half22float2(u32_as_h2(ph1)), b1 = __half22float2(u32_as_h2(pl1));
+        const float2 a0 = __half22float2(u32_as_h2(ph0[hh])), b0 = __half22float2(u32_as_h2(pl0[hh]));
+        const float2 a1 = __half22float2(u32_as_h2(ph1[hh])), b1 = __half22float2(u32_as_h2(pl1[hh]));
         pz[0] = a0.x + b0.x; pz[1] = a0.y + b0.y; pz[2] = a1.x + b1.x; pz[3] = a1.y + b1.y;
       }
       auto add_min = [&](int blk) {
@@ -958,14 +1003,14 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
           for (int i = 0; i < 4; ++i) vmin[blk] = fmaf(pz[i], h2f(vh[i][blk], 1), vmin[blk]);
         }
       };
-      const uint32_t vbase = smem_u32(st + C::off_vqs);
+      const uint32_t vbase = smem_u32(st + C::off_vqs) + hh * 16 * C::WV;
       if constexpr (VT == KVQ_TYPE_Q8_0) {
 #pragma unroll
         for (int blk = 0; blk < NB; ++blk) {
           uint32_t bh0, bl0, bh1, bl1;
           pscaled(blk, bh0, bl0, bh1, bl1);
           uint32_t r0, r1, r2, r3;
-          ldsm_x4_t(vbase + lbV[swz_lane_idx<C::WV>(2 * blk)] + swz_box_off<C::WV>(2 * blk), r0, r1, r2, r3);
+          ldsm_x4_t(vbase + lbV[swz_lane_idx<C::WV>(2 * blk)] + swz_box_off<C::WV, C::RB>(2 * blk), r0, r1, r2, r3);
           const uint32_t a0[4] = {i8_pair<0, 2>(r0), i8_pair<1, 3>(r0), i8_pair<0, 2>(r1), i8_pair<1, 3>(r1)};
           const uint32_t a1[4] = {i8_pair<0, 2>(r2), i8_pair<1, 3>(r2), i8_pair<0, 2>(r3), i8_pair<1, 3>(r3)};
           mma16816(acc[blk][0], a0, bh0, bh1);
@@ -979,7 +1024,7 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
 #pragma unroll
         for (int bp = 0; bp < NB; bp += 2) {
           uint32_t rr4[4];
-          ldsm_x4_t(vbase + lbV[swz_lane_idx<C::WV>(bp)] + swz_box_off<C::WV>(bp), rr4[0], rr4[1], rr4[2], rr4[3]);
+          ldsm_x4_t(vbase + lbV[swz_lane_idx<C::WV>(bp)] + swz_box_off<C::WV, C::RB>(bp), rr4[0], rr4[1], rr4[2], rr4[3]);
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int blk = bp + e;
@@ -994,8 +1039,9 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
             if constexpr (C::V5) {
               // the V plane's row pairs: words [low halves of rows 2tig, 2tig+1], [high halves]
               // (pair tig) and the same for rows 2tig+8, 2tig+9 (pair tig + 4)
-              const uint2 wa = *reinterpret_cast<const uint2*>(st + C::off_vqh + ((tig * NB + blk) * 2) * 4);
-              const uint2 wb = *reinterpret_cast<const uint2*>(st + C::off_vqh + (((tig + 4) * NB + blk) * 2) * 4);
+              const uint2 wa = *reinterpret_cast<const uint2*>(st + C::off_vqh + (((8 * hh + tig) * NB + blk) * 2) * 4);
+              const uint2 wb =
+                  *reinterpret_cast<const uint2*>(st + C::off_vqh + (((8 * hh + tig + 4) * NB + blk) * 2) * 4);
               ma0 = vhb(wa.x, vr[0], 0x00100010u); ma1 = vhb(wa.x, vr[1], 0x00100010u);
               ma2 = vhb(wa.y, vr[2], 0x01000100u); ma3 = vhb(wa.y, vr[3], 0x01000100u);
               mb0 = vhb(wb.x, vr[0], 0x00100010u); mb1 = vhb(wb.x, vr[1], 0x00100010u);
@@ -1012,13 +1058,14 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
           }
         }
       }
+      }  // halves
       if constexpr (OL) {  // outlier slots += codes_O^T . (P * d_O), as one more q8_0 block
         const __half* vod = reinterpret_cast<const __half*>(st + C::off_vod);
-        const uint32_t mlo = (vt0 ? 0x0000FFFFu : 0u) | (vt1 ? 0xFFFF0000u : 0u);
-        const uint32_t mhi = (vt8 ? 0x0000FFFFu : 0u) | (vt9 ? 0xFFFF0000u : 0u);
+        const uint32_t mlo = (vt0[0] ? 0x0000FFFFu : 0u) | (vt1[0] ? 0xFFFF0000u : 0u);
+        const uint32_t mhi = (vt8[0] ? 0x0000FFFFu : 0u) | (vt9[0] ? 0xFFFF0000u : 0u);
         uint32_t bh0, bl0, bh1, bl1;
-        hscale_split(ph0, pl0, ld_h2(vod + 2 * tig) & mlo, bh0, bl0);
-        hscale_split(ph1, pl1, ld_h2(vod + 2 * tig + 8) & mhi, bh1, bl1);
+        hscale_split(ph0[0], pl0[0], ld_h2(vod + 2 * tig) & mlo, bh0, bl0);
+        hscale_split(ph1[0], pl1[0], ld_h2(vod + 2 * tig + 8) & mhi, bh1, bl1);
         uint32_t r0, r1, r2, r3;
         ldsm_x4_t(smem_u32(st + C::off_vo) + rr * 32 + 16 * (mi >> 1), r0, r1, r2, r3);
         r0 ^= 0x80808080u; r1 ^= 0x80808080u; r2 ^= 0x80808080u; r3 ^= 0x80808080u;
@@ -1033,16 +1080,16 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
       // tail values are stored as fp16 * 2^-8, so P carries the factor 256
       float pt[4];
       {
-        const float2 a0 = __half22float2(u32_as_h2(ph0)), b0 = __half22float2(u32_as_h2(pl0));
-        const float2 a1 = __half22float2(u32_as_h2(ph1)), b1 = __half22float2(u32_as_h2(pl1));
+        const float2 a0 = __half22float2(u32_as_h2(ph0[0])), b0 = __half22float2(u32_as_h2(pl0[0]));
+        const float2 a1 = __half22float2(u32_as_h2(ph1[0])), b1 = __half22float2(u32_as_h2(pl1[0]));
         pt[0] = a0.x + b0.x; pt[1] = a0.y + b0.y; pt[2] = a1.x + b1.x; pt[3] = a1.y + b1.y;
       }
       uint32_t bh0, bl0, bh1, bl1;
       split_h2(pt[0] * 256.0f, pt[1] * 256.0f, bh0, bl0);
       split_h2(pt[2] * 256.0f, pt[3] * 256.0f, bh1, bl1);
       // token validity of the rows this lane reads from the transposed tile
-      const uint32_t mlo = (vt0 ? 0x0000FFFFu : 0u) | (vt1 ? 0xFFFF0000u : 0u);
-      const uint32_t mhi = (vt8 ? 0x0000FFFFu : 0u) | (vt9 ? 0xFFFF0000u : 0u);
+      const uint32_t mlo = (vt0[0] ? 0x0000FFFFu : 0u) | (vt1[0] ? 0xFFFF0000u : 0u);
+      const uint32_t mhi = (vt8[0] ? 0x0000FFFFu : 0u) | (vt9[0] ? 0xFFFF0000u : 0u);
       const uint32_t vbase = smem_u32(st + C::off_vt);
       const int rt = (lane & 7) + (C::TT == 16 ? 8 * (mi >> 1) : 0);
 #pragma unroll

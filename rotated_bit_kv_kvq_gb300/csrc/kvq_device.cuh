@@ -363,8 +363,9 @@ __device__ __forceinline__ void swz_lane(int r, int h, uint32_t (&lb)[W / 32]) {
 #pragma unroll
   for (int i = 0; i < W / 32; ++i) lb[i] = r * W + (((2 * i) ^ (h ^ key)) << 4);
 }
-template <int W>
-__host__ __device__ constexpr int swz_box_off(int j) { return (16 * j / W) * 16 * W; }
+// byte offset of the W-byte box column holding 16-byte chunk j, R rows per column
+template <int W, int R = 16>
+__host__ __device__ constexpr int swz_box_off(int j) { return (16 * j / W) * R * W; }
 template <int W>
 __host__ __device__ constexpr int swz_lane_idx(int j) { return (j % (W / 16)) / 2; }
 
