@@ -68,22 +68,22 @@ DecodePlan plan_decode(const kvq_cache& c, int n_q_heads, int sm_count) {
   // a piece of the stream touches one more segment than it covers whole at each end:
   // slot = piece + segment index (or batch + piece + sequence with a fused step)
   pl.slots = std::max(pl.pieces, c.batch + pl.pieces_fused) + 2 * c.batch;
-  // Costs in time, per token of one (sequence, KV head).  Below head_dim 256 a tail token
-  // (16-token bf16 tiles) costs about what a body token costs (per-CTA timing of the ragged
-  // 32-sequence batch at head_dim 128: 0.0226 against 0.0255 us); at head_dim 256 the
-  // 8-token tail tiles make a tail token about 2.5 body tokens (the bytes ratio, 1024 : 416;
-  // a ratio of 2 measured 1.8% slower on the 64k workload).
+  // Costs in time, per token of one (sequence, KV head).  At head_dim 256 the 8-token tail
+  // tiles make a tail token about 2.5 body tokens (the bytes ratio, 1024 : 416; a ratio of 2
+  // measured 1.8% slower on the 64k workload).  Below it a tail token (16-token bf16 tiles)
+  // costs 1.25 body tokens since body tiles hold 32 tokens (ragged 32-sequence batch at head_dim
+  // 128: 16 : 16 took 108.5 us, 20 : 16 107.0 us, 24 : 16 109.0 us).
   pl.cost_body = 16;
-  pl.cost_tail = c.head_dim >= 256 ? 40 : 16;
+  pl.cost_tail = c.head_dim >= 256 ? 40 : 20;
   pl.cost_min = 128 * pl.cost_body;          // 8 tiles: 2 per warp
   pl.cost_gap = 160 * pl.cost_body;          // ~4 us of a CTA's streaming time
   // Measured on the 64k-context workload: with equal pieces an SM's first, second and third
   // CTA ended after 94, 99 and 105 us; with pieces weighted 112 : 106 : 100 after 93, 95
-  // and 98 us; with 118 : 109 : 100 after 92.6, 93.2 and 94.7 us.  At head_dim 128 (the
-  // ragged batch) the second and third CTAs run relatively slower still.
+  // and 98 us; with 118 : 109 : 100 after 92.6, 93.2 and 94.7 us.  The same weights serve
+  // head_dim 128 with its 32-token body tiles (ragged 32-sequence batch 108.5 -> 107.0 us,
+  // 4 x 64k at head_dim 128 155.8 -> 148.2 us against 118 : 102 : 83).
   pl.sms = int(sms);
-  if (c.head_dim >= 256) { pl.slot_weight[0] = 118; pl.slot_weight[1] = 109; pl.slot_weight[2] = 98; }
-  else { pl.slot_weight[0] = 118; pl.slot_weight[1] = 102; pl.slot_weight[2] = 83; }
+  pl.slot_weight[0] = 118; pl.slot_weight[1] = 109; pl.slot_weight[2] = 98;
   const int cps = ctas_per_sm(c.head_dim, c.n_outlier != 0);
   auto one_wave = [&](long long ctas) { return cps == 3 && ctas > 2 * sms && ctas <= 3 * sms; };
   pl.weighted = one_wave((long long)pl.planes * pl.pieces);
