@@ -1266,23 +1266,31 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(Combine
   // launched as a programmatic dependent of the split kernel: wait for its completion
   // (and memory) before reading anything it wrote
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const Cuts cu = make_cuts(a.hdr[0], a.pieces, a.cost_min, a.planes, a.fused ? a.batch : 0, a.sms, a.wt, plane);
-  const long long P = a.hdr[1 + 2 * b];
-  const int n = int(a.hdr[2 + 2 * b]);
-  // fused step: every split CTA has read seq_len; advance it (head 0's CTA of each sequence)
-  if (a.fused && tid == 0 && h == 0) a.seq_len[b] = n;
-  // this sequence's slots: two runs (tail pieces, body pieces)
-  const int T = a.tail_len;
-  const long long ct = (long long)min(n, T) * a.cost_tail, cb = (long long)max(0, n - T) * a.cost_body;
-  const long long gap = a.cost_gap;  // every non-empty segment's data follows a gap
-  int r0, c0, r1, c1;
-  if (a.fused) {
-    r0 = b; c0 = min(n, T) > 0 ? 1 : 0;
-    seg_slots(cu, P + gap, cb, a.batch + b, r1, c1);
-  } else {
-    seg_slots(cu, P + gap, ct, 2 * b, r0, c0);
-    seg_slots(cu, P + (ct > 0 ? gap + ct : 0) + gap, cb, 2 * b + 1, r1, c1);
+  // this row's slots (two runs), worked out once by lane 0 from the partition header
+  // (every thread repeating the cut arithmetic was a large part of the merge's time)
+  __shared__ int s_runs[4];
+  if (tid == 0) {
+    const Cuts cu = make_cuts(a.hdr[0], a.pieces, a.cost_min, a.planes, a.fused ? a.batch : 0, a.sms, a.wt, plane);
+    const long long P = a.hdr[1 + 2 * b];
+    const int n = int(a.hdr[2 + 2 * b]);
+    // fused step: every split CTA has read seq_len; advance it (head 0's CTA of each sequence)
+    if (a.fused && h == 0) a.seq_len[b] = n;
+    // this sequence's slots: two runs (tail pieces, body pieces)
+    const int T = a.tail_len;
+    const long long ct = (long long)min(n, T) * a.cost_tail, cb = (long long)max(0, n - T) * a.cost_body;
+    const long long gap = a.cost_gap;  // every non-empty segment's data follows a gap
+    int q0, k0, q1, k1;
+    if (a.fused) {
+      q0 = b; k0 = min(n, T) > 0 ? 1 : 0;
+      seg_slots(cu, P + gap, cb, a.batch + b, q1, k1);
+    } else {
+      seg_slots(cu, P + gap, ct, 2 * b, q0, k0);
+      seg_slots(cu, P + (ct > 0 ? gap + ct : 0) + gap, cb, 2 * b + 1, q1, k1);
+    }
+    s_runs[0] = q0; s_runs[1] = k0; s_runs[2] = q1; s_runs[3] = k1;
   }
+  __syncthreads();
+  const int r0 = s_runs[0], c0 = s_runs[1], r1 = s_runs[2], c1 = s_runs[3];
   const int splits = c0 + c1;
   auto slot_of = [&](int j) { return j < c0 ? r0 + j : r1 + (j - c0); };
   const size_t base = (size_t)plane * a.slots;  // slot rows of this plane
