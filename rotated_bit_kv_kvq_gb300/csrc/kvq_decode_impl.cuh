@@ -1255,9 +1255,7 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(Combine
   constexpr int G = (D >= 64 && D % 64 == 0) ? (((D & (D - 1)) == 0) ? D : 64) : 32;
   constexpr int E = D / 32;
   constexpr int TPC = kCombineThreads / D >= 1 ? kCombineThreads / D : 1;  // threads per channel
-  extern __shared__ float s_w[];                 // [slots of this sequence] weights
-  __shared__ float s_part[kCombineThreads];      // per-thread partial sums, then the merged row
-  __shared__ float s_red[2][kCombineThreads / 32];
+  __shared__ float s_part[kCombineThreads];      // per-thread partial sums
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int row = blockIdx.x;  // b * Hq + h
   const int b = row / a.n_q_heads, h = row % a.n_q_heads;
@@ -1294,120 +1292,71 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(Combine
   const int splits = c0 + c1;
   auto slot_of = [&](int j) { return j < c0 ? r0 + j : r1 + (j - c0); };
   const size_t base = (size_t)plane * a.slots;  // slot rows of this plane
-  // 0. channel c of this thread takes slots sub, sub + TPC, ...: the first kAhead of
-  // its partials are loaded now, while the weights are worked out.  A slot whose
-  // sub-range was empty holds only its (m, l) = (-inf, 0); its acc row is whatever an
-  // earlier call left there, so it is read but selected away by its weight 0 and
-  // must never be multiplied.
-  constexpr int kAhead = 8;
+  // Thread (channel c, sub) merges slots sub, sub + TPC, ... in batches of kBatch, every
+  // load of a batch issued before any is used: the batch's maximum M, then the weight
+  // sum L and the channel's weighted sum v, the running values rescaled when M grows.
+  // A slot whose sub-range was empty holds only (m, l) = (-inf, 0); its acc row is
+  // whatever an earlier call left there: read, but selected away by its weight 0 and
+  // never multiplied.
+  constexpr int kBatch = kCombineThreads >= 512 ? 16 : 8;  // wide CTAs serve rows with many slots
   const int c = tid % D, sub = tid / D;
   const bool has_ch = tid < D * TPC;
-  float xa[kAhead];
+  float M = -INFINITY, L = 0.0f, v = 0.0f;
+  for (int s0 = sub; has_ch && s0 < splits; s0 += kBatch * TPC) {
+    float bm[kBatch], bl[kBatch], bx[kBatch];
 #pragma unroll
-  for (int u = 0; u < kAhead; ++u) {
-    const int j = sub + u * TPC;
-    xa[u] = has_ch && j < splits ? a.ws_acc[((base + slot_of(j)) * a.heads_per_cta + hh) * D + c] : 0.0f;
-  }
-  // 1. M = max over non-empty slots
-  float M = -INFINITY;
-  float mlm[2] = {-INFINITY, -INFINITY}, mll[2] = {0.0f, 0.0f};  // this thread's first two (m, l)
-#pragma unroll
-  for (int u = 0; u < 2; ++u) {
-    const int j = tid + u * kCombineThreads;
-    if (j < splits) {
-      const float2 ml = *reinterpret_cast<const float2*>(a.ws_ml + ((base + slot_of(j)) * a.heads_per_cta + hh) * 2);
-      mlm[u] = ml.x;
-      mll[u] = ml.y;
-    }
-  }
-  for (int j = tid; j < splits; j += kCombineThreads) {
-    const int u = (j - tid) / kCombineThreads;
-    float m, l;
-    if (u < 2) { m = mlm[u]; l = mll[u]; }
-    else {
-      const float2 ml = *reinterpret_cast<const float2*>(a.ws_ml + ((base + slot_of(j)) * a.heads_per_cta + hh) * 2);
-      m = ml.x; l = ml.y;
-    }
-    if (l > 0.0f) M = fmaxf(M, m);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  if (lane == 0) s_red[0][warp] = M;
-  __syncthreads();
-  M = s_red[0][0];
-#pragma unroll
-  for (int w = 1; w < kCombineThreads / 32; ++w) M = fmaxf(M, s_red[0][w]);
-  // 2. weights and L = sum of l_s * weight
-  float L = 0.0f;
-  for (int j = tid; j < splits; j += kCombineThreads) {
-    const int u = (j - tid) / kCombineThreads;
-    float m, l;
-    if (u < 2) { m = mlm[u]; l = mll[u]; }
-    else {
-      const float2 ml = *reinterpret_cast<const float2*>(a.ws_ml + ((base + slot_of(j)) * a.heads_per_cta + hh) * 2);
-      m = ml.x; l = ml.y;
-    }
-    const float w = l > 0.0f ? exp2f(m - M) : 0.0f;
-    s_w[j] = w;
-    L += l * w;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-  if (lane == 0) s_red[1][warp] = L;
-  __syncthreads();
-  L = 0.0f;
-#pragma unroll
-  for (int w = 0; w < kCombineThreads / 32; ++w) L += s_red[1][w];
-  // 3. the weighted sum of this thread's partials
-  float v = 0.0f;
-  if (has_ch) {
-#pragma unroll
-    for (int u = 0; u < kAhead; ++u) {
-      const int j = sub + u * TPC;
-      const float wv = j < splits ? s_w[j] : 0.0f;
-      v += wv != 0.0f ? wv * xa[u] : 0.0f;
-    }
-    for (int s0 = sub + kAhead * TPC; s0 < splits; s0 += kAhead * TPC) {
-      float y[kAhead], wv[kAhead];
-#pragma unroll
-      for (int u = 0; u < kAhead; ++u) {
-        const int j = s0 + u * TPC;
-        wv[u] = j < splits ? s_w[j] : 0.0f;
-        y[u] = j < splits ? a.ws_acc[((base + slot_of(j)) * a.heads_per_cta + hh) * D + c] : 0.0f;
+    for (int u = 0; u < kBatch; ++u) {
+      const int j = s0 + u * TPC;
+      bm[u] = -INFINITY; bl[u] = 0.0f; bx[u] = 0.0f;
+      if (j < splits) {
+        const size_t ri = (base + slot_of(j)) * a.heads_per_cta + hh;
+        const float2 ml = *reinterpret_cast<const float2*>(a.ws_ml + ri * 2);
+        bm[u] = ml.x; bl[u] = ml.y;
+        bx[u] = a.ws_acc[ri * D + c];
       }
-#pragma unroll
-      for (int u = 0; u < kAhead; ++u) v += wv[u] != 0.0f ? wv[u] * y[u] : 0.0f;
     }
+    // (slot j is warp-uniform: a warp's threads share sub; absent slots cost nothing)
+    float mb = M;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u)
+      if (s0 + u * TPC < splits) mb = fmaxf(mb, bl[u] > 0.0f ? bm[u] : -INFINITY);
+    const float fo = M == -INFINITY ? 0.0f : fast_exp2(M - mb);
+    L *= fo;
+    v *= fo;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      if (s0 + u * TPC < splits) {
+        const float w = bl[u] > 0.0f ? fast_exp2(bm[u] - mb) : 0.0f;
+        L = fmaf(bl[u], w, L);
+        v += w != 0.0f ? w * bx[u] : 0.0f;
+      }
+    }
+    M = mb;
   }
+  // the TPC threads of a channel: their sums, and each sub's (M, L) (the same in all its threads)
+  __shared__ float s_m[TPC], s_l[TPC];
   s_part[tid] = v;
-  // outlier channels: merged partial of slot tid
-  __shared__ float s_o[32];
-  if (OL && tid < 32) {
-    float t = 0.0f;
-    for (int s0 = 0; s0 < splits; s0 += 8) {
-      float x[8], wv[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int j = s0 + u;
-        wv[u] = j < splits ? s_w[j] : 0.0f;
-        x[u] = j < splits ? a.ws_acco[((base + slot_of(j)) * a.heads_per_cta + hh) * 32 + tid] : 0.0f;
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) t += wv[u] != 0.0f ? wv[u] * x[u] : 0.0f;
-    }
-    s_o[tid] = t;
-  }
+  if (has_ch && c == 0) { s_m[sub] = M; s_l[sub] = L; }
   __syncthreads();
-  // 4. warp 0: merged row / L, inverse rotation, (+ outlier channels), store
+  // 4. warp 0: the subs combined, / L, inverse rotation, (+ outlier channels), store
   if (warp != 0) return;
-  const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+  float Mg = -INFINITY;
+#pragma unroll
+  for (int u = 0; u < TPC; ++u) Mg = fmaxf(Mg, s_m[u]);
+  float fu[TPC], Lg = 0.0f;
+#pragma unroll
+  for (int u = 0; u < TPC; ++u) {
+    fu[u] = s_m[u] == -INFINITY ? 0.0f : fast_exp2(s_m[u] - Mg);
+    Lg = fmaf(s_l[u], fu[u], Lg);
+  }
+  const float inv = Lg > 0.0f ? 1.0f / Lg : 0.0f;
   float x[E];
 #pragma unroll
   for (int j = 0; j < E; ++j) {
     const int ch = fwht_channel<D, G>(lane, j);
     float t = 0.0f;
 #pragma unroll
-    for (int u = 0; u < TPC; ++u) t += s_part[u * D + ch];
+    for (int u = 0; u < TPC; ++u) t += fu[u] != 0.0f ? s_part[u * D + ch] * fu[u] : 0.0f;
     x[j] = t * inv;
   }
   if (a.rot_v) {
@@ -1415,11 +1364,28 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(Combine
 #pragma unroll
     for (int j = 0; j < E; ++j) x[j] *= inv_sqrt_group<G>();
   }
-  if constexpr (OL) {  // slot i's merged value goes to its channel, in the original basis
+  if constexpr (OL) {  // outlier slot `lane`: its merged value (same weights), to its channel in the original basis
+    float t = 0.0f;
+    for (int s0 = 0; s0 < splits; s0 += 8) {
+      float xo[8], wv[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = s0 + u;
+        xo[u] = 0.0f; wv[u] = 0.0f;
+        if (j < splits) {
+          const size_t ri = (base + slot_of(j)) * a.heads_per_cta + hh;
+          const float2 ml = *reinterpret_cast<const float2*>(a.ws_ml + ri * 2);
+          wv[u] = ml.y > 0.0f ? fast_exp2(ml.x - Mg) : 0.0f;
+          xo[u] = a.ws_acco[ri * 32 + lane];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) t += wv[u] != 0.0f ? wv[u] * xo[u] : 0.0f;
+    }
     const int ch = a.oidx[(size_t)kvh * 32 + lane];
     const int prev = __shfl_up_sync(0xffffffffu, ch, 1);
     const bool ok = ch >= 0 && ch < D && (lane == 0 || prev < ch);
-    const float val = s_o[lane] * inv;
+    const float val = t * inv;
 #pragma unroll 4
     for (int sl = 0; sl < 32; ++sl) {
       const int cs = __shfl_sync(0xffffffffu, ok ? ch : -1, sl);
@@ -1541,16 +1507,11 @@ cudaError_t run_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, cons
   // with many rows, 256-thread CTAs fit twice as many rows on the GPU at once
   const bool wide = (long long)c.batch * n_q_heads <= 2LL * plan.sms;
   auto ckern = wide ? decode_combine_kernel<D, OL, 512> : decode_combine_kernel<D, OL, 256>;
-  const size_t wbytes = (size_t)plan.slots * sizeof(float);
-  if (wbytes > 48 * 1024) {
-    e = ensure_dynamic_smem(reinterpret_cast<const void*>(ckern), (int)wbytes);
-    if (e != cudaSuccess) return e;
-  }
   // programmatic dependent launch: the merge grid's launch overlaps the split grid's end
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(c.batch * n_q_heads);
   cfg.blockDim = dim3(wide ? 512 : 256);
-  cfg.dynamicSmemBytes = wbytes;
+  cfg.dynamicSmemBytes = 0;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
