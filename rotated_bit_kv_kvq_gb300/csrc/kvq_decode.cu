@@ -88,8 +88,8 @@ DecodePlan plan_decode(const kvq_cache& c, int n_q_heads, int sm_count) {
   auto one_wave = [&](long long ctas) { return cps == 3 && ctas > 2 * sms && ctas <= 3 * sms; };
   pl.weighted = one_wave((long long)pl.planes * pl.pieces);
   pl.weighted_fused = one_wave((long long)pl.planes * (c.batch + pl.pieces_fused));
-  pl.hdr_bytes = ((size_t)(1 + 2 * c.batch) * sizeof(long long) + 255) / 256 * 256;
   const size_t rows = (size_t)pl.planes * pl.slots * pl.heads_per_cta;
+  pl.hdr_bytes = ((size_t)(1 + 2 * c.batch) * sizeof(long long) + 255) / 256 * 256;
   pl.ws_bytes = pl.hdr_bytes + rows * (c.head_dim + 2 + c.n_outlier) * sizeof(float);
   return pl;
 }

@@ -127,13 +127,13 @@ struct Params {
   int batch, pieces, slots;         // stream pieces and partial slots per plane
   long long cost_body, cost_tail, cost_min, cost_gap;
   int sms, wt[3];                   // piece weights by dispatch slot (Cuts), wt[0] = 0: uniform
-  long long* ws_hdr;                // [0] stream cost per plane, then per sequence: stream offset, tokens
   // fused step: new tokens written by the tail CTA (fused != 0)
   int fused, rot_v;
   FusedAppend fa;
   kvq_cache cache;
   RowMap rows;   // body row of (sequence, KV head, position): contiguous or paged
   float* ws_acco;  // outlier channels: their partials [plane][slot][head][32]
+  long long* ws_hdr;  // fused step: [0] stream cost per plane, then per sequence: stream offset, tokens
 };
 
 // New tokens of sequence b in a fused step: the requested count if it fits, else 0.
@@ -407,7 +407,8 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
   }
 
   // ---- the partition: every CTA computes the same cut from seq_len ----------
-  // (CTA 0 also records it for the merge kernel, and flags appends that do not fit)
+  // (the merge kernel works out the same numbers, or with a fused step reads the ones CTA 0
+  // records; CTA 0 also flags appends that do not fit)
   {
     constexpr int kCache = 4;  // sequences per thread kept in registers (batch <= 512)
     const int per = (B + kThreads - 1) / kThreads;
@@ -442,16 +443,16 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
       }
       const int n = n0 + nn;
       const long long c = stream_cost(n, T, p.fused, p.cost_body, p.cost_tail, p.cost_gap);
+      if (cta0 && p.fused) { p.ws_hdr[1 + 2 * bb] = P; p.ws_hdr[2 + 2 * bb] = n; }
       const bool first = own_tail ? bb == int(blockIdx.y) : (piece >= 0 && c > 0 && P <= x0 && x0 < P + c);
       if (first) {
         s_cur_P = P;
         s_cur[0] = bb;
         s_first[0] = bb; s_first[1] = n0; s_first[2] = nn;
       }
-      if (cta0) { p.ws_hdr[1 + 2 * bb] = P; p.ws_hdr[2 + 2 * bb] = n; }
       P += c;
     }
-    if (cta0 && tid == 0) p.ws_hdr[0] = total;
+    if (cta0 && p.fused && tid == 0) p.ws_hdr[0] = total;
   }
   __syncthreads();
 
@@ -1238,7 +1239,7 @@ struct CombineArgs {
   int pieces, planes, sms, wt[3];
   long long cost_body, cost_tail, cost_min, cost_gap;
   void* out;
-  int32_t* seq_len;      // fused step: advanced to the header's token count
+  int32_t* seq_len;      // fused step: advanced to the recorded token count
   const int32_t* oidx;   // outlier channels [kv_head][32]
 };
 
@@ -1261,19 +1262,16 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(Combine
   const int b = row / a.n_q_heads, h = row % a.n_q_heads;
   const int kvh = h / a.group, r = h % a.group;
   const int plane = kvh * a.head_groups + r / a.heads_per_cta, hh = r % a.heads_per_cta;
-  // launched as a programmatic dependent of the split kernel: wait for its completion
-  // (and memory) before reading anything it wrote
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  // this row's slots (two runs), worked out once by lane 0 from the partition header
-  // (every thread repeating the cut arithmetic was a large part of the merge's time)
-  __shared__ int s_runs[4];
-  if (tid == 0) {
-    const Cuts cu = make_cuts(a.hdr[0], a.pieces, a.cost_min, a.planes, a.fused ? a.batch : 0, a.sms, a.wt, plane);
-    const long long P = a.hdr[1 + 2 * b];
-    const int n = int(a.hdr[2 + 2 * b]);
-    // fused step: every split CTA has read seq_len; advance it (head 0's CTA of each sequence)
-    if (a.fused && h == 0) a.seq_len[b] = n;
-    // this sequence's slots: two runs (tail pieces, body pieces)
+  // This row's slots (two runs), from the partition; lane 0 of the CTA does the cut
+  // arithmetic once.  Decode alone: worked out before waiting for the split grid, from
+  // seq_len (which the split kernel reads too and nobody writes; the same integer sums,
+  // so the same cuts).  A fused step advances seq_len after the wait, and a merge CTA
+  // that becomes resident late could read an advanced length there: it reads the
+  // sequence offsets and token counts the split's CTA 0 recorded, after the wait.
+  __shared__ long long s_sum[2][kCombineThreads / 32];
+  __shared__ int s_runs[4], s_n;
+  auto runs = [&](long long total, long long P, int n) {
+    const Cuts cu = make_cuts(total, a.pieces, a.cost_min, a.planes, a.fused ? a.batch : 0, a.sms, a.wt, plane);
     const int T = a.tail_len;
     const long long ct = (long long)min(n, T) * a.cost_tail, cb = (long long)max(0, n - T) * a.cost_body;
     const long long gap = a.cost_gap;  // every non-empty segment's data follows a gap
@@ -1286,6 +1284,37 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(Combine
       seg_slots(cu, P + (ct > 0 ? gap + ct : 0) + gap, cb, 2 * b + 1, q1, k1);
     }
     s_runs[0] = q0; s_runs[1] = k0; s_runs[2] = q1; s_runs[3] = k1;
+  };
+  if (!a.fused) {
+    long long mine = 0, pre = 0;
+    for (int bb = tid; bb < a.batch; bb += kCombineThreads) {
+      const int n = a.seq_len[bb];
+      const long long cst = stream_cost(n, a.tail_len, 0, a.cost_body, a.cost_tail, a.cost_gap);
+      mine += cst;
+      if (bb < b) pre += cst;
+      if (bb == b) s_n = n;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mine += __shfl_xor_sync(0xffffffffu, mine, o);
+      pre += __shfl_xor_sync(0xffffffffu, pre, o);
+    }
+    if (lane == 0) { s_sum[0][warp] = mine; s_sum[1][warp] = pre; }
+    __syncthreads();
+    if (tid == 0) {
+      long long total = 0, P = 0;
+#pragma unroll
+      for (int w = 0; w < kCombineThreads / 32; ++w) { total += s_sum[0][w]; P += s_sum[1][w]; }
+      runs(total, P, s_n);
+    }
+  }
+  // launched as a programmatic dependent of the split kernel: wait for its completion
+  // (and memory) before reading anything it wrote
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (a.fused && tid == 0) {
+    const int n = int(a.hdr[2 + 2 * b]);
+    runs(a.hdr[0], a.hdr[1 + 2 * b], n);
+    if (h == 0) a.seq_len[b] = n;  // every split CTA has read seq_len: advance it (head 0's CTA)
   }
   __syncthreads();
   const int r0 = s_runs[0], c0 = s_runs[1], r1 = s_runs[2], c1 = s_runs[3];

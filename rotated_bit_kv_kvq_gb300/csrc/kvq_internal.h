@@ -78,7 +78,7 @@ struct DecodePlan {
   // (an SM's first, second, third CTA), so that the SM's CTAs end together.
   int slot_weight[3];
   bool weighted, weighted_fused;
-  size_t hdr_bytes;    // partition header at the start of the workspace
+  size_t hdr_bytes;    // fused-step partition header at the start of the workspace
   size_t ws_bytes;     // header, then acc [planes][slots][heads_per_cta][D], (m, l) [..][2],
                        // with outlier channels their acc [..][32]
 };
