@@ -92,8 +92,8 @@ typedef int32_t kvq_status;
                                 the GGUF qs bytes of the token's blocks, except that q8_0 codes are stored offset
                                 binary (code + 128, the GGUF byte XOR 0x80); kvq_dequant_debug returns GGUF bytes */
 #define KVQ_PLANE_K_QH    1  /* uint32 [batch][kv_heads][max_ctx][d/32]     q5_0 / q5_1 only (0 bytes otherwise);
-                                the bit of channel c = 4t + 2b + e of a block sits at bit 16b + 2t + e (t < 8; b, e
-                                in {0, 1}), a permutation of the GGUF word, whose bit c is bit 4 of code c; the V
+                                the bit of channel c (index bits c4..c0) of a block sits at bit 16*c1 + 8*c3 +
+                                4*c4 + 2*c2 + c0, a permutation of the GGUF word, whose bit c is bit 4 of code c; the V
                                 plane (KVQ_PLANE_V_QH) keeps GGUF order, and kvq_dequant_debug returns GGUF bytes */
 #define KVQ_PLANE_K_D     2  /* fp16 [batch][kv_heads][max_ctx][d/32]       block scales; q4_1 / q5_1: fp16 pairs
                                 (d, lo) [..][d/32][2], i.e. the GGUF block header                                   */

@@ -42,6 +42,9 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kMaxHeads = 8;                 // query heads per CTA (mma N)
 constexpr long long kWaitCycles = 1000000000LL;  // ~0.5 s at 2 GHz; a TMA tile lands in microseconds
 constexpr float kLog2e = 1.4426950408889634f;
+// Lazy softmax reference (log2 units): the weight of a tile's largest score is at
+// least 2^-kLazyMax, so P's fp16 hi / lo split keeps its relative precision.
+constexpr float kLazyMax = 2.0f;
 constexpr int kTailChunkMax = 4096;  // tail slots per CTA
 constexpr int kSmemBudget = 64 * 1024;       // stages; leaves room for 3 CTAs per SM
 constexpr int kCtasPerSm = 3;
@@ -346,12 +349,10 @@ __device__ __forceinline__ float hdr_scale(const uint32_t* w, int blk) {
   return KHH == 1 ? h2f(w[blk >> 1], blk & 1) : h2f(w[blk], 0);
 }
 
-// q5 high bits of a K row word (the K plane's bit order: channels c and c + 2 of
-// a score pair 16 bits apart) for one fp16 pair, at bits 4 / 20 with the 0x6400
-// magic: a rotation by the lane's amount r and one mask.
-__device__ __forceinline__ uint32_t khb(uint32_t h, uint32_t r) {
-  return (__funnelshift_r(h, h, r) & 0x00100010u) | 0x64006400u;
-}
+// q5 high bits of one fp16 pair of K codes from a K row word already rotated by
+// the lane's amount (the K plane's bit order puts the pair's two bits 16 apart):
+// the mask's bits (4 / 20 or 8 / 24) with the 0x6400 magic.
+__device__ __forceinline__ uint32_t khb(uint32_t h_rot, uint32_t mask) { return (h_rot & mask) | 0x64006400u; }
 // q5 V high bits of a row-pair word (two tokens, 16 bits apart) at the mask's bits
 __device__ __forceinline__ uint32_t vhb(uint32_t w, uint32_t r, uint32_t mask) {
   return (__funnelshift_r(w, w, r) & mask) | 0x64006400u;
@@ -733,11 +734,13 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
   int k_stop = my_tiles;
   // per-lane ldmatrix row and swizzle constants of the body tiles
   const int mi = lane >> 3, rr = (lane & 7) + 8 * (mi & 1);
-  // q5 K: rotation bringing the lane's channel pairs (4tig, 4tig+2), (+1, +3),
-  // (16+4tig, 18+4tig), (17+4tig, 19+4tig) of a stored high-bit word to bits 4 / 20
-  uint32_t kr[4];
+  // q5 K: rotations of a stored high-bit word bringing the lane's channel pairs
+  // (4tig, 4tig+2) [kr[0]] and (4tig+1, 4tig+3) [kr[1]] to bits 4 / 20, and with the
+  // same rotations (16+4tig, 18+4tig) and (17+4tig, 19+4tig) to bits 8 / 24 (their
+  // nibbles are read in place, x16)
+  uint32_t kr[2];
 #pragma unroll
-  for (int w = 0; w < 4; ++w) kr[w] = uint32_t(2 * tig + (w & 1) + 8 * (w >> 1) - 4) & 31u;
+  for (int w = 0; w < 2; ++w) kr[w] = uint32_t(8 * (tig >> 1) + 2 * (tig & 1) + w - 4) & 31u;
   // q5 V: rotation bringing channel 2g (+1) of a row pair's low-half word to bits 4 / 20,
   // and channel 2g + 16 (+17) of its high-half word to bits 8 / 24
   uint32_t vr[4];
@@ -798,6 +801,7 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
         }
       } else {
         constexpr uint32_t OFF = (0x6400u + uint32_t(type_code_offset(KT))) * 0x10001u;
+        constexpr uint32_t OFF16 = neg_off_x16_bits(type_code_offset(KT));
 #pragma unroll
         for (int bp = 0; bp < NB; bp += 2) {
           uint32_t rr4[4];
@@ -806,18 +810,24 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
           for (int e = 0; e < 2; ++e) {
             const int blk = bp + e;
             const uint32_t ra = rr4[2 * e], rb = rr4[2 * e + 1];  // token g, token g+8
+            const uint32_t ra8 = ra >> 8, rb8 = rb >> 8;
+            // high bits: at bit 4 / 20 for the low nibbles, bit 8 / 24 for the x16 high nibbles
             uint32_t m00 = 0x64006400u, m01 = 0x64006400u, m02 = 0x64006400u, m03 = 0x64006400u;
             uint32_t m10 = 0x64006400u, m11 = 0x64006400u, m12 = 0x64006400u, m13 = 0x64006400u;
             if constexpr (C::K5) {
               const uint32_t* kqh = reinterpret_cast<const uint32_t*>(st + C::off_kqh);
               const uint32_t ha = kqh[(16 * hh + g) * NB + blk], hb = kqh[(16 * hh + g + 8) * NB + blk];
-              m00 = khb(ha, kr[0]); m01 = khb(ha, kr[1]); m02 = khb(ha, kr[2]); m03 = khb(ha, kr[3]);
-              m10 = khb(hb, kr[0]); m11 = khb(hb, kr[1]); m12 = khb(hb, kr[2]); m13 = khb(hb, kr[3]);
+              const uint32_t ha0 = __funnelshift_r(ha, ha, kr[0]), ha1 = __funnelshift_r(ha, ha, kr[1]);
+              const uint32_t hb0 = __funnelshift_r(hb, hb, kr[0]), hb1 = __funnelshift_r(hb, hb, kr[1]);
+              m00 = khb(ha0, 0x00100010u); m01 = khb(ha1, 0x00100010u);
+              m02 = khb(ha0, 0x01000100u); m03 = khb(ha1, 0x01000100u);
+              m10 = khb(hb0, 0x00100010u); m11 = khb(hb1, 0x00100010u);
+              m12 = khb(hb0, 0x01000100u); m13 = khb(hb1, 0x01000100u);
             }
             const uint32_t alo[4] = {nib_pair(ra, 0, m00, OFF), nib_pair(rb, 0, m10, OFF),
-                                     nib_pair(ra, 8, m01, OFF), nib_pair(rb, 8, m11, OFF)};
-            const uint32_t ahi[4] = {nib_pair(ra, 4, m02, OFF), nib_pair(rb, 4, m12, OFF),
-                                     nib_pair(ra, 12, m03, OFF), nib_pair(rb, 12, m13, OFF)};
+                                     nib_pair(ra8, 0, m01, OFF), nib_pair(rb8, 0, m11, OFF)};
+            const uint32_t ahi[4] = {nib_pair_x16(ra, m02, OFF16), nib_pair_x16(rb, m12, OFF16),
+                                     nib_pair_x16(ra8, m03, OFF16), nib_pair_x16(rb8, m13, OFF16)};
             const uint4 qa = qfs[(blk * 2) * 32 + lane], qb = qfs[(blk * 2 + 1) * 32 + lane];
             float cc[4] = {0.f, 0.f, 0.f, 0.f};
             mma16816(cc, alo, qa.x, qa.y);
@@ -897,16 +907,17 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
       mx0 = fmaxf(mx0, fmaxf(S[hh][0], S[hh][2]));
       mx1 = fmaxf(mx1, fmaxf(S[hh][1], S[hh][3]));
     }
-    // The running maximum changes only when some score of the tile exceeds it; for
-    // long contexts that is rare, and the reduction over the tile's rows and the
-    // rescale run only then.
+    // m0 / m1 are reference points, not the running maxima: kLazyMax above the
+    // maximum seen at the last rescale.  Weights 2^(S - m) stay <= 1, and the
+    // reduction over the tile's rows and the rescale run only when a score passes
+    // the reference -- a few times per head and sub-range, not at every new maximum.
     if (__any_sync(0xffffffffu, mx0 > m0 || mx1 > m1)) {
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) {
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
       }
-      const float nm0 = fmaxf(m0, mx0), nm1 = fmaxf(m1, mx1);
+      const float nm0 = fmaxf(m0, mx0 + kLazyMax), nm1 = fmaxf(m1, mx1 + kLazyMax);
       const float a0 = m0 == -INFINITY ? 0.0f : fast_exp2(m0 - nm0);
       const float a1 = m1 == -INFINITY ? 0.0f : fast_exp2(m1 - nm1);
       l0 *= a0; l1 *= a1;

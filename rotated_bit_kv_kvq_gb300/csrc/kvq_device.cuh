@@ -69,11 +69,13 @@ __device__ __forceinline__ long long body_row(const RowMap& m, int b, int h, int
 
 // ---------------------------------------------------------------------------
 // Bit order of the K high-bit plane (q5_0 / q5_1 K).  A block's 32-bit word
-// holds bit 4 of code c at bit c in GGUF order; the K plane stores the bit of
-// channel c = 4t + 2b + e (t < 8, b and e single bits) at bit 16b + 2t + e, so
-// that channels c and c + 2 (one fp16 pair of the decode's score operand) sit
-// 16 bits apart.  Three delta swaps of the bit index (bits 1<->2, 2<->3,
-// 3<->4) rotate index bits 1-4; the inverse applies them in reverse order.
+// holds bit 4 of code c at bit c in GGUF order.  The K plane stores the bit of
+// channel c (index bits c4..c0) at bit 16*c1 + 8*c3 + 4*c4 + 2*c2 + c0: channels
+// c and c + 2 (one fp16 pair of the decode's score operand) sit 16 bits apart,
+// and the pairs (c, c + 2) and (c + 16, c + 18) that one lane converts sit 4 bits
+// apart, so one rotation serves both.  Four delta swaps of the bit index (bits
+// 1<->2, 2<->3, 3<->4, then 2<->3 again) give the order; the inverse applies them
+// in reverse.
 // The V plane keeps GGUF order within each word, but stores rows in pairs
 // (2r, 2r + 1): per (pair, block) one 32-bit word of the two rows' low 16 bits
 // [row 2r | row 2r + 1 << 16], then one of their high 16 bits, so that the two
@@ -86,9 +88,11 @@ __host__ __device__ inline uint32_t delta_swap(uint32_t x, int d, uint32_t m) {
 __host__ __device__ inline uint32_t qh_k_from_gguf(uint32_t x) {
   x = delta_swap(x, 2, 0x0C0C0C0Cu);
   x = delta_swap(x, 4, 0x00F000F0u);
-  return delta_swap(x, 8, 0x0000FF00u);
+  x = delta_swap(x, 8, 0x0000FF00u);
+  return delta_swap(x, 4, 0x00F000F0u);
 }
 __host__ __device__ inline uint32_t qh_k_to_gguf(uint32_t x) {
+  x = delta_swap(x, 4, 0x00F000F0u);
   x = delta_swap(x, 8, 0x0000FF00u);
   x = delta_swap(x, 4, 0x00F000F0u);
   return delta_swap(x, 2, 0x0C0C0C0Cu);
