@@ -368,7 +368,9 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // the warp index through a shuffle from lane 0: visibly the same in every lane, so
+  // the copy addresses derived from it can stay warp-uniform
+  const int tid = threadIdx.x, lane = tid & 31, warp = __shfl_sync(0xffffffffu, tid >> 5, 0);
   const int g = lane >> 2, tig = lane & 3;
   // grid (plane = KV head x head group, piece): piece y of every plane is dispatched
   // before piece y + 1
@@ -524,8 +526,14 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
       }
     }
     if (!found) break;
+  // (every thread found the same sub-range; taken from lane 0 so that the compiler
+  // sees warp-uniform values in the copy addressing)
+  b = __shfl_sync(0xffffffffu, b, 0);
+  t_begin = __shfl_sync(0xffffffffu, t_begin, 0);
+  t_end = __shfl_sync(0xffffffffu, t_end, 0);
+  is_tail = __shfl_sync(0xffffffffu, int(is_tail), 0) != 0;
 
-  // ---- this warp's tiles, and the producer (lane 0) --------------------
+  // ---- this warp's tiles, and the producer (one lane) --------------------
   const int TR = is_tail ? C::TT : C::RB;                    // rows per tile
   const int ntiles = (t_end - t_begin + TR - 1) / TR;
   const int my_tiles = ntiles > warp ? (ntiles - warp + kWarps - 1) / kWarps : 0;
@@ -612,7 +620,7 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     asm volatile("fence.proxy.async.global;" ::: "memory");
   }
   __syncthreads();  // barriers initialised (and the fused step's tokens stored)
-  if (lane == 0) {
+  if (elect_one()) {
     for (int k = 0; k < NS && k < my_tiles; ++k) issue(k);
   }
 
@@ -1118,7 +1126,7 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
         }
     }
     __syncwarp();
-    if (lane == 0 && k + NS < my_tiles) {
+    if (k + NS < my_tiles && elect_one()) {
       fence_proxy_async_smem();
       issue(k + NS);
     }
