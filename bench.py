@@ -839,6 +839,9 @@ def main():
     ap.add_argument("--prefill-only", action="store_true",
                     help="run only the prompt-workload measurement (bulk append + prefill attention) and print "
                          "its record; for profiling the bulk write and prefill kernels")
+    ap.add_argument("--configs-only", action="store_true",
+                    help="run only the decode measurement of the other workloads (d=64 ctx 256, GQA 16/8 ctx "
+                         "4k, ragged batch of 32) and print their records; for profiling those launches")
     ap.add_argument("--load-s", type=float, default=1.2,
                     help="seconds of extra decode load inside the clock-sampling window")
     args = ap.parse_args()
@@ -850,6 +853,10 @@ def main():
         import torch
         from rotated_bit_kv_kvq_gb300 import kvq
         print(json.dumps({"prefill": run_prefill_bench(torch, kvq, args.steps, args.warmup)}), flush=True)
+    elif args.configs_only:
+        import torch
+        from rotated_bit_kv_kvq_gb300 import kvq
+        print(json.dumps({"configs": run_config_legs(torch, kvq, measured_peaks()[0])}), flush=True)
     else:
         run_ours(args)
 

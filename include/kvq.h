@@ -93,14 +93,15 @@ typedef int32_t kvq_status;
                                 binary (code + 128, the GGUF byte XOR 0x80); kvq_dequant_debug returns GGUF bytes */
 #define KVQ_PLANE_K_QH    1  /* uint32 [batch][kv_heads][max_ctx][d/32]     q5_0 / q5_1 only (0 bytes otherwise);
                                 the bit of channel c (index bits c4..c0) of a block sits at bit 16*c1 + 8*c3 +
-                                4*c4 + 2*c2 + c0, a permutation of the GGUF word, whose bit c is bit 4 of code c; the V
-                                plane (KVQ_PLANE_V_QH) keeps GGUF order, and kvq_dequant_debug returns GGUF bytes */
+                                4*c4 + 2*c2 + c0, a permutation of the GGUF word, whose bit c is bit 4 of code c;
+                                kvq_dequant_debug returns GGUF bytes                                                 */
 #define KVQ_PLANE_K_D     2  /* fp16 [batch][kv_heads][max_ctx][d/32]       block scales; q4_1 / q5_1: fp16 pairs
                                 (d, lo) [..][d/32][2], i.e. the GGUF block header                                   */
 #define KVQ_PLANE_V_QS    3
-#define KVQ_PLANE_V_QH    4  /* uint32, as K_QH in size, GGUF bit order within each word, rows in pairs: for rows
-                                (2r, 2r + 1) and block j, word 2(r*d/32 + j) holds the two rows' bits 0-15 (row 2r in
-                                its low half) and word 2(r*d/32 + j) + 1 their bits 16-31 */
+#define KVQ_PLANE_V_QH    4  /* uint32, as K_QH in size, rows in pairs: a row's bits split in two 16-bit parts, the
+                                bit of channel c (index bits c4..c0) in part c3 at bit 8*c2 + 4*c4 + 2*c1 + c0; for
+                                rows (2r, 2r + 1) and block j, word 2(r*d/32 + j) holds the two rows' parts 0 (row 2r
+                                in its low half) and word 2(r*d/32 + j) + 1 their parts 1 */
 #define KVQ_PLANE_V_D     5
 #define KVQ_PLANE_K_TAIL  6  /* bf16 [batch][kv_heads][tail_len][d]          rotated values, slot = pos % tail_len */
 #define KVQ_PLANE_V_TAIL  7

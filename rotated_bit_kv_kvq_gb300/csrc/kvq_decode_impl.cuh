@@ -353,10 +353,9 @@ __device__ __forceinline__ float hdr_scale(const uint32_t* w, int blk) {
 // the lane's amount (the K plane's bit order puts the pair's two bits 16 apart):
 // the mask's bits (4 / 20 or 8 / 24) with the 0x6400 magic.
 __device__ __forceinline__ uint32_t khb(uint32_t h_rot, uint32_t mask) { return (h_rot & mask) | 0x64006400u; }
-// q5 V high bits of a row-pair word (two tokens, 16 bits apart) at the mask's bits
-__device__ __forceinline__ uint32_t vhb(uint32_t w, uint32_t r, uint32_t mask) {
-  return (__funnelshift_r(w, w, r) & mask) | 0x64006400u;
-}
+// q5 V high bits of one fp16 pair (two tokens, 16 bits apart) from a row-pair part
+// word already rotated by the lane's amount, at the mask's bits with the 0x6400 magic
+__device__ __forceinline__ uint32_t vhb(uint32_t w_rot, uint32_t mask) { return (w_rot & mask) | 0x64006400u; }
 
 template <int D, int KT, int VT, bool OL>
 __global__ void __launch_bounds__(kThreads, ctas_per_sm(D, OL))
@@ -735,9 +734,9 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     for (int r = 0; r < 4; ++r) acco[j][r] = 0.0f;
   // V1 (scale + minimum V blocks): sum over this lane's transposed tokens of P * lo per
   // block, for head g, in the running-max frame; added to the block's channels at the end
-  float vmin[C::V1 ? NB : 1];
-#pragma unroll
-  for (int i = 0; i < (C::V1 ? NB : 1); ++i) vmin[i] = 0.0f;
+  // V1: sum_t P[t][h] * lo[t][blk] as one more mma accumulator, rows = blocks g, g + 8
+  // (A = the tile's block minima, blocks x tokens), columns = heads 2tig, 2tig + 1
+  float dmin[4] = {0.f, 0.f, 0.f, 0.f};
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
   int k_stop = my_tiles;
   // per-lane ldmatrix row and swizzle constants of the body tiles
@@ -749,11 +748,12 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
   uint32_t kr[2];
 #pragma unroll
   for (int w = 0; w < 2; ++w) kr[w] = uint32_t(8 * (tig >> 1) + 2 * (tig & 1) + w - 4) & 31u;
-  // q5 V: rotation bringing channel 2g (+1) of a row pair's low-half word to bits 4 / 20,
-  // and channel 2g + 16 (+17) of its high-half word to bits 8 / 24
-  uint32_t vr[4];
+  // q5 V: rotations of the lane's part word (part g / 4) of a row pair bringing channel
+  // 2g [vr[0]] and 2g + 1 [vr[1]] to bits 4 / 20, and with the same rotations channels
+  // 2g + 16 and 2g + 17 to bits 8 / 24
+  uint32_t vr[2];
 #pragma unroll
-  for (int w = 0; w < 4; ++w) vr[w] = uint32_t(2 * g + (w & 1) - 4 - 4 * (w >> 1)) & 31u;
+  for (int w = 0; w < 2; ++w) vr[w] = uint32_t(8 * ((g & 3) >> 1) + 2 * (g & 1) + w - 4) & 31u;
   uint32_t lbK[C::WK / 32], lbV[C::WV / 32];
   swz_lane<C::WK>(rr, mi >> 1, lbK);
   swz_lane<C::WV>(rr, mi >> 1, lbV);
@@ -941,11 +941,8 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
           acco[j][0] *= a0; acco[j][1] *= a1; acco[j][2] *= a0; acco[j][3] *= a1;
         }
       }
-      if constexpr (C::V1) {  // head g's factor lives in lane tig = g / 2
-        const float x0 = __shfl_sync(0xffffffffu, a0, g >> 1), x1 = __shfl_sync(0xffffffffu, a1, g >> 1);
-        const float ag = (g & 1) ? x1 : x0;
-#pragma unroll
-        for (int i = 0; i < NB; ++i) vmin[i] *= ag;
+      if constexpr (C::V1) {
+        dmin[0] *= a0; dmin[1] *= a1; dmin[2] *= a0; dmin[3] *= a1;
       }
       m0 = nm0; m1 = nm1;
     }
@@ -1009,20 +1006,25 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
         hscale_split(ph0[hh], pl0[hh], dvpair(blk, 0, 1), bh0, bl0);
         hscale_split(ph1[hh], pl1[hh], dvpair(blk, 2, 3), bh1, bl1);
       };
-      // the minimum adds sum_t P[t][h] * lo[t][blk] to every channel of the block: the
-      // lane's share for head g is summed here in fp32 and spread over the channels at the end
-      float pz[4] = {0.f, 0.f, 0.f, 0.f};
+      // the minimum adds sum_t P[t][h] * lo[t][blk] to every channel of the block: one mma
+      // per P part with A = the minima of blocks g (and g + 8) at the lane's four transposed
+      // tokens (zero for rows past the end: their bytes may be anything)
       if constexpr (C::V1) {
-        const float2 a0 = __half22float2(u32_as_h2(ph0[hh])), b0 = __half22float2(u32_as_h2(pl0[hh]));
-        const float2 a1 = __half22float2(u32_as_h2(ph1[hh])), b1 = __half22float2(u32_as_h2(pl1[hh]));
-        pz[0] = a0.x + b0.x; pz[1] = a0.y + b0.y; pz[2] = a1.x + b1.x; pz[3] = a1.y + b1.y;
+        const uint8_t* vd = st + C::off_vd;
+        const int tr[4] = {16 * hh + 2 * tig, 16 * hh + 2 * tig + 1, 16 * hh + 2 * tig + 8, 16 * hh + 2 * tig + 9};
+        const bool ok[4] = {vt0[hh], vt1[hh], vt8[hh], vt9[hh]};
+        auto lo2 = [&](int blk, int i0, int i1) -> uint32_t {  // (d, lo) words -> the two lo halves
+          const int bb = blk < NB ? blk : NB - 1;
+          uint32_t w0 = *reinterpret_cast<const uint32_t*>(vd + (tr[i0] * NB + bb) * 4);
+          uint32_t w1 = *reinterpret_cast<const uint32_t*>(vd + (tr[i1] * NB + bb) * 4);
+          if (partial) { w0 = ok[i0] ? w0 : 0u; w1 = ok[i1] ? w1 : 0u; }
+          return blk < NB ? __byte_perm(w0, w1, 0x7632) : 0u;
+        };
+        const uint32_t al[4] = {lo2(g, 0, 1), NB > 8 ? lo2(g + 8, 0, 1) : 0u, lo2(g, 2, 3),
+                                NB > 8 ? lo2(g + 8, 2, 3) : 0u};
+        mma16816(dmin, al, ph0[hh], ph1[hh]);
+        mma16816(dmin, al, pl0[hh], pl1[hh]);
       }
-      auto add_min = [&](int blk) {
-        if constexpr (C::V1) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) vmin[blk] = fmaf(pz[i], h2f(vh[i][blk], 1), vmin[blk]);
-        }
-      };
       const uint32_t vbase = smem_u32(st + C::off_vqs) + hh * 16 * C::WV;
       if constexpr (VT == KVQ_TYPE_Q8_0) {
 #pragma unroll
@@ -1050,22 +1052,24 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
             const int blk = bp + e;
             uint32_t bh0, bl0, bh1, bl1;
             pscaled(blk, bh0, bl0, bh1, bl1);
-            add_min(blk);
             const uint32_t ra = rr4[2 * e], rb = rr4[2 * e + 1];  // tokens 0-7, 8-15
             const uint32_t ra8 = ra >> 8, rb8 = rb >> 8;
             // high bits: at bit 4 / 20 for the low nibbles, bit 8 / 24 for the x16 high nibbles
             uint32_t ma0 = 0x64006400u, ma1 = 0x64006400u, ma2 = 0x64006400u, ma3 = 0x64006400u;
             uint32_t mb0 = 0x64006400u, mb1 = 0x64006400u, mb2 = 0x64006400u, mb3 = 0x64006400u;
             if constexpr (C::V5) {
-              // the V plane's row pairs: words [low halves of rows 2tig, 2tig+1], [high halves]
-              // (pair tig) and the same for rows 2tig+8, 2tig+9 (pair tig + 4)
-              const uint2 wa = *reinterpret_cast<const uint2*>(st + C::off_vqh + (((8 * hh + tig) * NB + blk) * 2) * 4);
-              const uint2 wb =
-                  *reinterpret_cast<const uint2*>(st + C::off_vqh + (((8 * hh + tig + 4) * NB + blk) * 2) * 4);
-              ma0 = vhb(wa.x, vr[0], 0x00100010u); ma1 = vhb(wa.x, vr[1], 0x00100010u);
-              ma2 = vhb(wa.y, vr[2], 0x01000100u); ma3 = vhb(wa.y, vr[3], 0x01000100u);
-              mb0 = vhb(wb.x, vr[0], 0x00100010u); mb1 = vhb(wb.x, vr[1], 0x00100010u);
-              mb2 = vhb(wb.y, vr[2], 0x01000100u); mb3 = vhb(wb.y, vr[3], 0x01000100u);
+              // the V plane's row pairs: the lane's part word of rows 2tig, 2tig+1 (pair tig)
+              // and of rows 2tig+8, 2tig+9 (pair tig + 4)
+              const uint32_t wa =
+                  *reinterpret_cast<const uint32_t*>(st + C::off_vqh + (((8 * hh + tig) * NB + blk) * 2 + (g >> 2)) * 4);
+              const uint32_t wb = *reinterpret_cast<const uint32_t*>(
+                  st + C::off_vqh + (((8 * hh + tig + 4) * NB + blk) * 2 + (g >> 2)) * 4);
+              const uint32_t wa0 = __funnelshift_r(wa, wa, vr[0]), wa1 = __funnelshift_r(wa, wa, vr[1]);
+              const uint32_t wb0 = __funnelshift_r(wb, wb, vr[0]), wb1 = __funnelshift_r(wb, wb, vr[1]);
+              ma0 = vhb(wa0, 0x00100010u); ma1 = vhb(wa1, 0x00100010u);
+              ma2 = vhb(wa0, 0x01000100u); ma3 = vhb(wa1, 0x01000100u);
+              mb0 = vhb(wb0, 0x00100010u); mb1 = vhb(wb1, 0x00100010u);
+              mb2 = vhb(wb0, 0x01000100u); mb3 = vhb(wb1, 0x01000100u);
             }
             const uint32_t a0[4] = {nib_pair(ra, 0, ma0, OFF), nib_pair(ra8, 0, ma1, OFF),
                                     nib_pair(rb, 0, mb0, OFF), nib_pair(rb8, 0, mb1, OFF)};
@@ -1181,18 +1185,20 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
       base[(2 * tig) * D + cg8] = acc[blk][cc2][2] * f0;
       base[(2 * tig + 1) * D + cg8] = acc[blk][cc2][3] * f1;
     }
-  if constexpr (C::V1) {  // head g: the 4 tig lanes' sums, in this warp's merge frame, on every channel
-    const float x0 = __shfl_sync(0xffffffffu, f0, g >> 1), x1 = __shfl_sync(0xffffffffu, f1, g >> 1);
-    const float fg = (g & 1) ? x1 : x0;
+  if constexpr (C::V1) {  // blocks g, g + 8 for heads 2tig, 2tig + 1, in this warp's merge frame
     __syncwarp();
 #pragma unroll
-    for (int blk = 0; blk < NB; ++blk) {
-      float t = vmin[blk];
-      t += __shfl_xor_sync(0xffffffffu, t, 1);
-      t += __shfl_xor_sync(0xffffffffu, t, 2);
-      float* row = macc + ((size_t)warp * kMaxHeads + g) * D + 32 * blk + 8 * tig;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) row[c] += t * fg;
+    for (int half = 0; half < 2; ++half) {
+      const int blk = g + 8 * half;
+      if (blk < NB) {
+        const float v0 = dmin[2 * half] * f0, v1 = dmin[2 * half + 1] * f1;
+        float* r0 = macc + ((size_t)warp * kMaxHeads + 2 * tig) * D + 32 * blk;
+#pragma unroll 8
+        for (int c = 0; c < 32; ++c) {
+          r0[c] += v0;
+          r0[D + c] += v1;
+        }
+      }
     }
   }
   float* maco = macc + (size_t)kWarps * kMaxHeads * D;  // OL: [kWarps][8][32]

@@ -76,10 +76,14 @@ __device__ __forceinline__ long long body_row(const RowMap& m, int b, int h, int
 // apart, so one rotation serves both.  Four delta swaps of the bit index (bits
 // 1<->2, 2<->3, 3<->4, then 2<->3 again) give the order; the inverse applies them
 // in reverse.
-// The V plane keeps GGUF order within each word, but stores rows in pairs
-// (2r, 2r + 1): per (pair, block) one 32-bit word of the two rows' low 16 bits
-// [row 2r | row 2r + 1 << 16], then one of their high 16 bits, so that the two
-// consecutive tokens of one transposed P.V operand arrive in one word.
+// The V plane stores rows in pairs (2r, 2r + 1) and a row's bits in two 16-bit
+// parts: per (pair, block) one 32-bit word [part 0 of row 2r | part 0 of row
+// 2r + 1 << 16], then one of their parts 1, so that the two consecutive tokens of
+// one transposed P.V operand arrive in one word.  Part c3 of a row holds channel c
+// (index bits c4..c0) at bit 8*c2 + 4*c4 + 2*c1 + c0: the four channels 2g, 2g + 1,
+// 2g + 16, 2g + 17 that one lane converts sit in one part, the pairs 4 bits apart,
+// so two rotations serve them.  Two delta swaps of the bit index (bits 3<->4, then
+// 2<->3) give the order.
 // ---------------------------------------------------------------------------
 __host__ __device__ inline uint32_t delta_swap(uint32_t x, int d, uint32_t m) {
   const uint32_t t = ((x >> d) ^ x) & m;
@@ -97,8 +101,16 @@ __host__ __device__ inline uint32_t qh_k_to_gguf(uint32_t x) {
   x = delta_swap(x, 4, 0x00F000F0u);
   return delta_swap(x, 2, 0x0C0C0C0Cu);
 }
-// 16-bit element index of half h (0: bits 0-15, 1: bits 16-31) of the V word of
-// (row, block); nb blocks per row.
+__host__ __device__ inline uint32_t qh_v_from_gguf(uint32_t x) {
+  x = delta_swap(x, 8, 0x0000FF00u);
+  return delta_swap(x, 4, 0x00F000F0u);
+}
+__host__ __device__ inline uint32_t qh_v_to_gguf(uint32_t x) {
+  x = delta_swap(x, 4, 0x00F000F0u);
+  return delta_swap(x, 8, 0x0000FF00u);
+}
+// 16-bit element index of part h (0: bits 0-15, 1: bits 16-31 of the word
+// qh_v_from_gguf gives) of the V word of (row, block); nb blocks per row.
 __host__ __device__ inline size_t qh_v_half(size_t row, int nb, int blk, int h) {
   return ((((row >> 1) * size_t(nb) + size_t(blk)) * 2 + size_t(h)) * 2) + (row & 1);
 }
@@ -119,7 +131,7 @@ __device__ __forceinline__ QhDst qh_dst(void* plane, bool k_plane, size_t row, i
 }
 // store a high-bit word given in GGUF order
 __device__ __forceinline__ void qh_put(const QhDst& d, uint32_t gguf) {
-  const uint32_t w = d.k ? qh_k_from_gguf(gguf) : gguf;
+  const uint32_t w = d.k ? qh_k_from_gguf(gguf) : qh_v_from_gguf(gguf);
   *d.lo = uint16_t(w & 0xFFFFu);
   *d.hi = uint16_t(w >> 16);
 }
@@ -127,7 +139,7 @@ __device__ __forceinline__ void qh_put(const QhDst& d, uint32_t gguf) {
 __device__ __forceinline__ uint32_t qh_get(const void* plane, bool k_plane, size_t row, int nb, int blk) {
   if (k_plane) return qh_k_to_gguf(static_cast<const uint32_t*>(plane)[row * size_t(nb) + size_t(blk)]);
   const uint16_t* p = static_cast<const uint16_t*>(plane);
-  return uint32_t(p[qh_v_half(row, nb, blk, 0)]) | (uint32_t(p[qh_v_half(row, nb, blk, 1)]) << 16);
+  return qh_v_to_gguf(uint32_t(p[qh_v_half(row, nb, blk, 0)]) | (uint32_t(p[qh_v_half(row, nb, blk, 1)]) << 16));
 }
 
 // ---------------------------------------------------------------------------
