@@ -75,7 +75,8 @@ struct PL {
   static constexpr int off_k = 2 * q;           // two slots of [hi | lo]
   static constexpr int off_v = off_k + 4 * kt;  // two slots of [hi | lo]
   static constexpr int off_xl = off_v + 4 * vt;  // [2][128] floats: the halves' row sums
-  static constexpr int off_bar = off_xl + 2 * kPM * 4;
+  static constexpr int off_xm = off_xl + 2 * kPM * 4;  // [2 tiles][2 halves][128] (max, tile) words
+  static constexpr int off_bar = off_xm + 2 * 2 * kPM * 8;
   static constexpr int smem = off_bar + 256 + 1024;
   static constexpr int stage_stride = D + 4;    // epilogue fp32 rows (reuse Q and K slots), 16-byte rows
   static_assert(kPM * stage_stride * 4 <= off_v, "epilogue staging must fit below the V slots");
@@ -573,6 +574,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
 
   // ---- softmax: row = TMEM lane (tid % 128), half h of the 64 keys ---------
   const int row = tid & (kPM - 1), h = tid / kPM;
+  // The two halves of a row swap their maxima through shared memory: slot [j & 1][h][row]
+  // holds (maximum, tile j), written by half h, polled (bounded) by the other half.
+  // A slot is rewritten for tile j + 2 only after its writer has seen the other
+  // half's tile j + 1 value, which comes after that half read tile j's.
+  unsigned long long* xm = reinterpret_cast<unsigned long long*>(sm + L::off_xm);
+  xm[(0 * 2 + h) * kPM + row] = ~0ull;
+  xm[(1 * 2 + h) * kPM + row] = ~0ull;
+  named_sync(1, kSoftmax);
   const int li = row / g;
   const int qi = tile * p.ppt + li;
   const bool row_ok = li < p.ppt && qi < p.n_tokens && p0 >= 0;
@@ -588,7 +597,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
     ok = __all_sync(0xffffffffu, role_wait(&sy->sfull[s], (j >> 1) & 1, sy, p.status));
     if (!ok) break;
     tc::fence_after_sync();
-    float sv[HN], so[HN];  // own half, other half
+    float sv[HN];  // this half's 32 scores
     {
       float t[HN];
       const uint32_t sa = lane_taddr + s * L::s_cols;
@@ -599,29 +608,42 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
       tc::wait_ld();
 #pragma unroll
       for (int c = 0; c < HN; ++c) sv[c] += t[c];
-      tc::ld_x16(sa + (1 - h) * HN, *reinterpret_cast<float(*)[16]>(&so[0]));
-      tc::ld_x16(sa + (1 - h) * HN + 16, *reinterpret_cast<float(*)[16]>(&so[16]));
-      tc::ld_x16(sa + kPN + (1 - h) * HN, *reinterpret_cast<float(*)[16]>(&t[0]));
-      tc::ld_x16(sa + kPN + (1 - h) * HN + 16, *reinterpret_cast<float(*)[16]>(&t[16]));
-      tc::wait_ld();
-#pragma unroll
-      for (int c = 0; c < HN; ++c) so[c] += t[c];
     }
     tc::fence_before_sync();
     mbar_arrive(&sy->sfree[s]);
     // mask keys past this row's end (partial tiles only)
     if (j * kPN + kPN > kv_end_row) {
-      const int own0 = j * kPN + h * HN, oth0 = j * kPN + (1 - h) * HN;
+      const int own0 = j * kPN + h * HN;
 #pragma unroll
-      for (int c = 0; c < HN; ++c) {
+      for (int c = 0; c < HN; ++c)
         if (own0 + c >= kv_end_row) sv[c] = -INFINITY;
-        if (oth0 + c >= kv_end_row) so[c] = -INFINITY;
-      }
     }
-    float mx[4] = {fmaxf(sv[0], so[0]), fmaxf(sv[1], so[1]), fmaxf(sv[2], so[2]), fmaxf(sv[3], so[3])};
+    float mx[4] = {sv[0], sv[1], sv[2], sv[3]};
 #pragma unroll
-    for (int c = 4; c < HN; ++c) mx[c & 3] = fmaxf(mx[c & 3], fmaxf(sv[c], so[c]));
-    const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * 256.0f;  // keys were staged x 2^-8
+    for (int c = 4; c < HN; ++c) mx[c & 3] = fmaxf(mx[c & 3], sv[c]);
+    const float mo = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+    // the row's maximum: this half's and the other half's
+    float mp;
+    {
+      volatile unsigned long long* mine = xm + ((j & 1) * 2 + h) * kPM + row;
+      volatile unsigned long long* other = xm + ((j & 1) * 2 + 1 - h) * kPM + row;
+      *mine = (static_cast<unsigned long long>(uint32_t(j)) << 32) | __float_as_uint(mo);
+      unsigned long long w = *other;
+      if (uint32_t(w >> 32) != uint32_t(j)) {
+        const long long t0 = clock64();
+        while (uint32_t((w = *other) >> 32) != uint32_t(j)) {
+          if (*reinterpret_cast<volatile int*>(&sy->abort) || clock64() - t0 > kPWait) {
+            *reinterpret_cast<volatile int*>(&sy->abort) = 1;
+            atomicOr(p.status, KVQ_DEV_ERR_TIMEOUT);
+            break;
+          }
+        }
+      }
+      mp = __uint_as_float(uint32_t(w));
+    }
+    ok = __all_sync(0xffffffffu, !*reinterpret_cast<volatile int*>(&sy->abort));
+    if (!ok) break;
+    const float mt = fmaxf(mo, mp) * 256.0f;  // keys were staged x 2^-8
     // lazy rescale: move the reference maximum only when it grew by more than 2^4
     float alpha = 1.0f;
     const bool move = mt > m_used + kLazyRescale || (m_used == -INFINITY && mt > -INFINITY);
