@@ -465,6 +465,9 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
 
   // ---- the piece's sub-ranges, one (sequence, tail or body) segment each ------
   uint32_t kk = 0;  // tiles this warp consumed (ring phases)
+  // K1 (scale + minimum K blocks): B fragment of the minimum's mma, the block sums of q
+  // as fp16 hi / lo for blocks 2tig, 2tig + 1 (and + 8, + 9) of head g
+  uint32_t bqh[2] = {0u, 0u}, bql[2] = {0u, 0u};
   bool timed_out = false;
   for (;;) {
     // find the next non-empty sub-range of this piece (empty ones get an empty partial)
@@ -716,6 +719,15 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
       }
     }
     __syncthreads();
+    if constexpr (C::K1) {
+#pragma unroll
+      for (int e = 0; e < (NB > 8 ? 2 : 1); ++e) {
+        const int b0 = 2 * tig + 8 * e;
+        const float x0 = b0 < NB ? qsum[b0 * kMaxHeads + g] : 0.0f;
+        const float x1 = b0 + 1 < NB ? qsum[(b0 + 1) * kMaxHeads + g] : 0.0f;
+        split_h2(x0, x1, bqh[e], bql[e]);
+      }
+    }
   }  // queries of sequence b staged
   const uint4* qofs = reinterpret_cast<const uint4*>(smem + C::off_qof);
 
@@ -845,13 +857,19 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
             const float dk0 = hdr_scale<KHH>(kw0, blk), dk8 = hdr_scale<KHH>(kw8, blk);
             S[hh][0] += dk0 * cc[0]; S[hh][1] += dk0 * cc[1];
             S[hh][2] += dk8 * cc[2]; S[hh][3] += dk8 * cc[3];
-            if constexpr (C::K1) {  // + lo * (sum of the block's q), per token and head
-              const float mk0 = h2f(kw0[blk], 1), mk8 = h2f(kw8[blk], 1);
-              const float2 qs2 = *reinterpret_cast<const float2*>(qsum + blk * kMaxHeads + 2 * tig);
-              S[hh][0] += mk0 * qs2.x; S[hh][1] += mk0 * qs2.y;
-              S[hh][2] += mk8 * qs2.x; S[hh][3] += mk8 * qs2.y;
-            }
           }
+        }
+        if constexpr (C::K1) {  // + sum_blk lo[t][blk] * (sum of block blk's q)[h]: one mma per q part
+          const uint8_t* kd = st + C::off_kd;
+          auto lo2 = [&](int t, int b0) -> uint32_t {  // minima of blocks b0, b0 + 1 of row t
+            if (b0 >= NB) return 0u;
+            const uint2 w = *reinterpret_cast<const uint2*>(kd + ((16 * hh + t) * NB + b0) * 4);
+            return __byte_perm(w.x, w.y, 0x7632);
+          };
+          const uint32_t am[4] = {lo2(g, 2 * tig), lo2(g + 8, 2 * tig), NB > 8 ? lo2(g, 2 * tig + 8) : 0u,
+                                  NB > 8 ? lo2(g + 8, 2 * tig + 8) : 0u};
+          mma16816(S[hh], am, bqh[0], bqh[1]);
+          mma16816(S[hh], am, bql[0], bql[1]);
         }
       }
       }  // halves
