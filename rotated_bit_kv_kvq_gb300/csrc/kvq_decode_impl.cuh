@@ -37,6 +37,8 @@
 namespace kvq {
 namespace {
 
+template <bool B>
+struct BoolTag { static constexpr bool value = B; };
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxHeads = 8;                 // query heads per CTA (mma N)
@@ -770,6 +772,11 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
   swz_lane<C::WK>(rr, mi >> 1, lbK);
   swz_lane<C::WV>(rr, mi >> 1, lbV);
 
+  // The tile loop, compiled once for tail and once for body sub-ranges: each copy holds
+  // only its own kind's code, which keeps the body loop compact in the instruction cache.
+  auto tile_loop = [&](auto tail_tag) {
+  constexpr bool kTail = decltype(tail_tag)::value;
+  const int TR = kTail ? C::TT : C::RB;  // rows per tile (a constant in each copy)
   for (int k = 0; k < my_tiles; ++k) {
     const int s = (kk + k) % NS;
     const bool arrived = mbar_wait_bounded(&wbar[s], ((kk + k) / NS) & 1, kWaitCycles);
@@ -792,7 +799,7 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     float S[HB][4];
 #pragma unroll
     for (int hh = 0; hh < HB; ++hh) S[hh][0] = S[hh][1] = S[hh][2] = S[hh][3] = 0.f;
-    if (!is_tail) {
+    if constexpr (!kTail) {
 #pragma unroll
       for (int hh = 0; hh < HB; ++hh) {
       // ------------------------------- body: scores of rows 16hh .. 16hh + 15
@@ -993,7 +1000,7 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
       vt8[hh] = 16 * hh + 8 < TR && tt + 8 < t_lim;
       vt9[hh] = 16 * hh + 8 < TR && tt + 9 < t_lim;
     }
-    if (!is_tail) {
+    if constexpr (!kTail) {
 #pragma unroll
       for (int hh = 0; hh < HB; ++hh) {
       // V block headers of the lane's four transposed tokens (rows 16hh + ...), all blocks;
@@ -1153,6 +1160,9 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
       issue(k + NS);
     }
   }
+  };
+  if (is_tail) tile_loop(BoolTag<true>{});
+  else tile_loop(BoolTag<false>{});
 
   if (timed_out) {
     if (lane == 0) atomicOr(p.status, KVQ_DEV_ERR_TIMEOUT);
