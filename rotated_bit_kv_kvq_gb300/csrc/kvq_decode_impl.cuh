@@ -15,7 +15,7 @@
 //
 // Kernel 1 (split-K): CTA = (split, KV head x head group, sequence), 4 warps.
 // Every warp streams its own 16-token tiles through a ring of shared-memory
-// stages filled by TMA (2-D tensor copies with hardware swizzle for the packed
+// stages filled by TMA (tensor copies with hardware swizzle, one per plane, for the packed
 // codes and bf16 rows, 1-D bulk copies for scales and q5_0 high bits).  Codes
 // are turned into exact fp16 integers in registers and multiplied on the
 // tensor cores (mma.m16n8k16, fp32 accumulate):
@@ -554,11 +554,8 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
     if (is_tail) {
       const int row = int(bh * T + t0);
       mbar_arrive_expect_tx(&wbar[s], C::tail_tx);
-#pragma unroll
-      for (int x = 0; x < 2 * D; x += C::WT) {
-        tma_2d_g2s(st + C::off_kt + (x / C::WT) * C::TT * C::WT, &tmKt, x / 2, row, &wbar[s]);
-        tma_2d_g2s(st + C::off_vt + (x / C::WT) * C::TT * C::WT, &tmVt, x / 2, row, &wbar[s]);
-      }
+      tma_3d_g2s(st + C::off_kt, &tmKt, row, &wbar[s]);  // [column][TT rows][WT bytes]
+      tma_3d_g2s(st + C::off_vt, &tmVt, row, &wbar[s]);
     } else {
       size_t row = bh * p.max_ctx + t0;
       if (paged) {  // a body tile (16 or 32 tokens, aligned) never crosses a page (a multiple of 64)
@@ -573,18 +570,9 @@ decode_split_kernel(Params p, const __grid_constant__ CUtensorMap tmK, const __g
         }
       }
       mbar_arrive_expect_tx(&wbar[s], C::body_tx);
-      // per box column of W bytes: RB rows, as RB / 16 stacked 16-row boxes
-#pragma unroll
-      for (int hb = 0; hb < C::HB; ++hb) {
-#pragma unroll
-        for (int x = 0; x < C::rowK; x += C::WK)
-          tma_2d_g2s(st + C::off_kqs + (x / C::WK) * C::RB * C::WK + hb * 16 * C::WK, &tmK, x, int(row) + 16 * hb,
-                     &wbar[s]);
-#pragma unroll
-        for (int x = 0; x < C::rowV; x += C::WV)
-          tma_2d_g2s(st + C::off_vqs + (x / C::WV) * C::RB * C::WV + hb * 16 * C::WV, &tmV, x, int(row) + 16 * hb,
-                     &wbar[s]);
-      }
+      // one copy per plane: [box column of W bytes][RB rows][W bytes]
+      tma_3d_g2s(st + C::off_kqs, &tmK, int(row), &wbar[s]);
+      tma_3d_g2s(st + C::off_vqs, &tmV, int(row), &wbar[s]);
       bulk_g2s(st + C::off_kd, p.k_d + row * NB * C::KH, C::RB * NB * C::KH, &wbar[s]);
       bulk_g2s(st + C::off_vd, p.v_d + row * NB * C::VH, C::RB * NB * C::VH, &wbar[s]);
       if constexpr (C::K5) bulk_g2s(st + C::off_kqh, p.k_qh + row * NB, C::RB * NB * 4, &wbar[s]);
@@ -1509,16 +1497,19 @@ CUtensorMapSwizzle swizzle_for(int w) {
   return w == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : (w == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
 }
 
-// rows x row_bytes plane of `elem` sized elements, boxes of box_w bytes x box_rows.
+// rows x row_bytes plane of `elem` sized elements, seen as three dimensions (elements
+// within a box column of box_w bytes, row, box column) so that one copy of box_rows
+// rows brings every column: shared memory [column][box_rows rows][box_w bytes].
 bool make_map(CUtensorMap* m, void* base, CUtensorMapDataType dt, int elem, long long rows, int row_bytes,
               int box_w_bytes, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {cuuint64_t(row_bytes / elem), cuuint64_t(rows)};
-  cuuint64_t strides[1] = {cuuint64_t(row_bytes)};
-  cuuint32_t box[2] = {cuuint32_t(box_w_bytes / elem), cuuint32_t(box_rows)};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(box_w_bytes),
+  const int cols = row_bytes / box_w_bytes;
+  cuuint64_t dims[3] = {cuuint64_t(box_w_bytes / elem), cuuint64_t(rows), cuuint64_t(cols)};
+  cuuint64_t strides[2] = {cuuint64_t(row_bytes), cuuint64_t(box_w_bytes)};
+  cuuint32_t box[3] = {cuuint32_t(box_w_bytes / elem), cuuint32_t(box_rows), cuuint32_t(cols)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, dt, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(box_w_bytes),
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1560,8 +1551,8 @@ cudaError_t run_decode(const kvq_cache& c, Rot rot, const DecodePlan& plan, cons
   alignas(64) CUtensorMap mk, mv, mkt, mvt;
   memset(&mk, 0, sizeof(mk)); memset(&mv, 0, sizeof(mv)); memset(&mkt, 0, sizeof(mkt)); memset(&mvt, 0, sizeof(mvt));
   const long long rows = body_rows(c);
-  if (!make_map(&mk, c.k_qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, rows, Cf::rowK, Cf::WK, 16)) return cudaErrorInvalidValue;
-  if (!make_map(&mv, c.v_qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, rows, Cf::rowV, Cf::WV, 16)) return cudaErrorInvalidValue;
+  if (!make_map(&mk, c.k_qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, rows, Cf::rowK, Cf::WK, Cf::RB)) return cudaErrorInvalidValue;
+  if (!make_map(&mv, c.v_qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, rows, Cf::rowV, Cf::WV, Cf::RB)) return cudaErrorInvalidValue;
   if (c.tail_len > 0) {
     const long long trows = (long long)c.batch * c.n_kv_heads * c.tail_len;
     if (!make_map(&mkt, c.k_tail, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, trows, 2 * D, Cf::WT, Cf::TT) ||

@@ -351,11 +351,12 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return r;
 }
 
-// 2-D tiled tensor copy global -> shared (coordinates: x = inner element, y = row).
-__device__ __forceinline__ void tma_2d_g2s(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+// 3-D tiled tensor copy global -> shared: a row-major plane seen as (x: bytes within a
+// box column, y: row, z: box column), so that one copy fills [column][row][box width].
+__device__ __forceinline__ void tma_3d_g2s(void* dst, const CUtensorMap* map, int y, uint64_t* bar) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(y), "r"(0), "r"(smem_u32(bar))
       : "memory");
 }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
