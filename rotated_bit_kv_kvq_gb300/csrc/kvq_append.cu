@@ -174,8 +174,9 @@ __device__ __forceinline__ void quantize_lane_block_scalar(const float (&y)[32],
 // trunc(x * id + off) for two values x (the code before the clamp): the
 // product and the sum rounded to nearest one at a time in scalar instructions
 // with explicit rounding modifiers (the compiler keeps those apart; a packed
-// multiply followed by a packed add was seen contracted into a fused
-// multiply-add, which rounds once), then, with 0 <= u < 2^23, a packed add of
+// multiply followed by a packed add -- fp32x2 instructions, even with .rn on
+// both -- came out as one fused multiply-add, which rounds once, and failed the
+// bit-exact block test), then, with 0 <= u < 2^23, a packed add of
 // 2^23 rounded toward zero: the sum lands on the unit grid, so its low mantissa
 // bits hold floor(u) = trunc(u).
 __device__ __forceinline__ void code_bits2(float x0, float x1, float id, float off, uint32_t& c0, uint32_t& c1) {
@@ -192,8 +193,8 @@ __device__ __forceinline__ void code_bits2(float x0, float x1, float id, float o
 // order of evaluation: the signed value of largest magnitude from a max / min
 // tree (a block holding +a and -a, or no nonzero value, takes the scalar scan,
 // which resolves the first-index rule); codes min(top, trunc(x*id + off)) two
-// at a time with packed multiply and add (one rounding each, as before), the
-// truncation by code_bits2 (u > 0 here), then four codes per word: clamp to
+// at a time by code_bits2 (scalar multiply and add, one rounding each, as
+// before; the truncation packed, u > 0 here), then four codes per word: clamp to
 // top, nibble pack (byte k = code_k | code_{k+16} << 4) and for q5_0 bit 4 of
 // each code into the high-bit word.  q8_0, the scale + minimum types and blocks
 // whose scale or inverse is not finite take the scalar path.
@@ -458,6 +459,9 @@ append_rows_kernel(kvq_cache c, int rot_k, int rot_v, const void* __restrict__ k
   const unsigned wtasks = (tasks + VPW - 1) / VPW;
   const unsigned stride = gridDim.x * unsigned(kAppendWarps);
   const unsigned lt = unsigned(lane / R);
+  // strided: the warps work on neighbouring tasks at any one time, so the partial
+  // sectors of the body planes they write (one token row each) meet in L2 (contiguous
+  // per-warp task ranges, which balance the warps' task counts, were 18% slower)
   unsigned wt = blockIdx.x * unsigned(kAppendWarps) + (threadIdx.x >> 5);
   for (; wt < wtasks; wt += stride) {  // warp-uniform trip count
     RowRaw<IN> raw;
