@@ -258,14 +258,14 @@ struct RowRaw {
   uint4 w[IN == kInF32 ? 8 : 4];
 };
 
-// Task tu = 2 * vec + which: vector vec = (b * n_new + i) * H + h of K (which = 0)
-// or V; lane sub of its R lanes reads channels 32*sub .. 32*sub+31 (read once:
-// streaming loads).
+// Vector vec = (b * n_new + i) * H + h of K (which = 0) or V; lane sub of its R
+// lanes reads channels 32*sub .. 32*sub+31 (read once: streaming loads).
 template <int D, int IN>
-__device__ __forceinline__ void rows_load(RowRaw<IN>& r, const void* kin, const void* vin, unsigned tu, int sub) {
+__device__ __forceinline__ void rows_load(RowRaw<IN>& r, const void* kin, const void* vin, size_t vec, int which,
+                                          int sub) {
   constexpr bool IN32 = IN == kInF32;
-  const size_t e0 = size_t(tu >> 1) * D + 32 * sub;
-  const void* base = (tu & 1u) ? vin : kin;
+  const size_t e0 = vec * D + 32 * sub;
+  const void* base = which ? vin : kin;
   const uint4* src = IN32 ? reinterpret_cast<const uint4*>(static_cast<const float*>(base) + e0)
                           : reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + e0);
 #pragma unroll
@@ -299,23 +299,17 @@ __device__ __forceinline__ void rows_unpack(const RowRaw<IN>& r, float (&y)[32])
   }
 }
 
-// Rotate, quantize and store one lane block of task tu (its values in y); `live`
-// false: a lane past the end, which computes a copy and stores nothing.
+// Rotate, quantize and store one lane block of new token i of (sequence b, KV
+// head h), K (which = 0) or V (its values in y); `live` false: a lane past the
+// end, which computes a copy and stores nothing.
 template <int D, bool OUTL>
-__device__ __forceinline__ void rows_task(const kvq_cache& c, int rot_k, int rot_v, int n_new, const DivU32& div_h,
-                                          const DivU32& div_n, const int32_t* __restrict__ n_new_per_seq,
-                                          int prerotated, bool live, unsigned tu, float (&y)[32], int lane) {
+__device__ __forceinline__ void rows_task(const kvq_cache& c, int rot_k, int rot_v, int n_new,
+                                          const int32_t* __restrict__ n_new_per_seq, int prerotated, bool live,
+                                          int b, int i, int h, int which, float (&y)[32], int lane) {
   constexpr int R = D / 32;   // lanes per vector
   constexpr int NB = D / kQK;
   const int sub = lane % R;
   const int H = c.n_kv_heads;
-  const int which = int(tu & 1u);
-  const unsigned vec = tu >> 1;                  // (b * n_new + i) * H + h
-  const unsigned bi = div_u32(vec, div_h);
-  const int h = int(vec - bi * unsigned(H));
-  const unsigned bu = div_u32(bi, div_n);
-  const int i = int(bi - bu * unsigned(n_new));
-  const int b = int(bu);
   const int n0 = c.seq_len[b];
   const int nb = n_new_per_seq ? n_new_per_seq[b] : n_new;
   const bool ok = nb >= 0 && nb <= n_new && n0 >= 0 && (long long)n0 + nb <= c.max_ctx;
@@ -455,22 +449,34 @@ append_rows_kernel(kvq_cache c, int rot_k, int rot_v, const void* __restrict__ k
   constexpr int R = D / 32;   // lanes per vector
   constexpr unsigned VPW = 32u / R;  // vectors per warp task
   const int lane = threadIdx.x & 31, sub = lane % R;
-  const unsigned tasks = unsigned(c.batch) * unsigned(n_new) * unsigned(c.n_kv_heads) * 2u;
-  const unsigned wtasks = (tasks + VPW - 1) / VPW;
+  // Warp tasks hold only K vectors (tasks below Wv) or only V vectors, so every lane
+  // of a warp takes the same quantizer path even when K and V formats differ: task
+  // wt = which * Wv + u holds vectors u*VPW .. u*VPW+VPW-1, vector vec = (b * n_new
+  // + i) * H + h (one token's heads, then the next token's: contiguous input rows).
+  const unsigned nvec = unsigned(c.batch) * unsigned(n_new) * unsigned(c.n_kv_heads);
+  const unsigned Wv = (nvec + VPW - 1) / VPW;
+  const unsigned wtasks = 2u * Wv;
   const unsigned stride = gridDim.x * unsigned(kAppendWarps);
+  const int H = c.n_kv_heads;
   const unsigned lt = unsigned(lane / R);
   // strided: the warps work on neighbouring tasks at any one time, so the partial
   // sectors of the body planes they write (one token row each) meet in L2 (contiguous
   // per-warp task ranges, which balance the warps' task counts, were 18% slower)
   unsigned wt = blockIdx.x * unsigned(kAppendWarps) + (threadIdx.x >> 5);
   for (; wt < wtasks; wt += stride) {  // warp-uniform trip count
+    const int which = wt >= Wv ? 1 : 0;
+    const unsigned v0 = (wt - (which ? Wv : 0u)) * VPW + lt;
+    const bool live = v0 < nvec;
+    const unsigned vec = live ? v0 : nvec - 1;  // a lane past the end loads a valid row
+    const unsigned bi = div_u32(vec, div_h);
+    const int h = int(vec - bi * unsigned(H));
+    const unsigned bu = div_u32(bi, div_n);
+    const int i = int(bi - bu * unsigned(n_new)), b = int(bu);
     RowRaw<IN> raw;
-    rows_load<D, IN>(raw, kin, vin, min(wt * VPW + lt, tasks - 1), sub);
+    rows_load<D, IN>(raw, kin, vin, vec, which, sub);
     float y[32];
     rows_unpack<IN>(raw, y);
-    const unsigned task = wt * VPW + lt;
-    rows_task<D, OUTL>(c, rot_k, rot_v, n_new, div_h, div_n, n_new_per_seq, prerotated, task < tasks,
-                       min(task, tasks - 1), y, lane);
+    rows_task<D, OUTL>(c, rot_k, rot_v, n_new, n_new_per_seq, prerotated, live, b, i, h, which, y, lane);
   }
   finish_append(c, n_new, n_new_per_seq);
 }
