@@ -205,10 +205,41 @@ def test_bulk_blocks_bit_exact_prerotated(qt, d):
                 assert np.array_equal(got, oc.tail_values(w, b, h, np.arange(n - T, n)))
 
 
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_bulk_partial_last_task(d):
+    """Bulk appends whose vector count (batch x tokens x KV heads = 3 x 229 x 3) is
+    no multiple of the vectors a warp task holds (32 / (d / 32)): the last K task
+    and the last V task each have lanes past the end, which must store nothing,
+    and the first V task follows a partly filled K task.  Mixed K/V formats,
+    ragged counts, two calls; blocks and tail rows bit-exact."""
+    torch = require_gpu()
+    from rotated_bit_kv_kvq_gb300 import kvq
+    rng = np.random.default_rng(300 + d)
+    B, H, T = 3, 3, 8
+    gc = kvq.KVCache(B, H, d, 512, T, "q8_0", "q5_0")
+    oc = ko.OracleCache(B, H, d, 512, T, "q8_0", "q5_0", True, True)
+    for n, nps in ((229, [229, 200, 3]), (229, [1, 229, 228])):
+        assert (B * n * H) % (32 // (d // 32)) != 0
+        k = _inputs(rng, B, n, H, d)
+        v = _inputs(rng, B, n, H, d, scale=2.0)
+        append_both(gc, oc, k, v, n_new_per_seq=nps, torch=torch)
+    lens = gc.seq_len.cpu().numpy()
+    assert np.array_equal(lens, oc.seq_len)
+    for b in range(B):
+        n = int(lens[b])
+        for h in range(H):
+            for which, w, t in ((0, "k", "q8_0"), (1, "v", "q5_0")):
+                assert np.array_equal(gpu_blocks(gc, b, h, which, 0, n, t, d, torch), oc.ggml_blocks(w, b, h, 0, n))
+            for which, w in ((2, "k"), (3, "v")):
+                got = gpu_values(gc, b, h, which, n - T, T, d, torch)
+                assert np.array_equal(got, oc.tail_values(w, b, h, np.arange(n - T, n)))
+
+
 def test_bulk_k_rotated_v_not():
-    """K rotated in the kernel, V stored as given (KVQ_ROT_V_OFF): in the bulk
-    kernel a warp mixes both kinds of vectors.  V blocks are bit-exact; K within
-    the rotation tolerance (exact here: dyadic inputs at head_dim 64)."""
+    """K rotated in the kernel, V stored as given (KVQ_ROT_V_OFF), through the
+    bulk kernel (its warp tasks hold K vectors or V vectors, each side with its
+    own switch).  V blocks are bit-exact; K within the rotation tolerance (exact
+    here: dyadic inputs at head_dim 64)."""
     torch = require_gpu()
     from rotated_bit_kv_kvq_gb300 import kvq
     rng = np.random.default_rng(203)
