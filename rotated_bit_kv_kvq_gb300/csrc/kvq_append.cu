@@ -353,8 +353,9 @@ __device__ __forceinline__ void rows_task(const kvq_cache& c, int rot_k, int rot
 #pragma unroll
     for (int j = 0; j < 32; ++j) y[j] = ((zmask >> j) & 1u) ? 0.0f : y[j];
   }
-  // rotation: the R lanes of a vector rotate together (a warp may mix K and V
-  // vectors, which rotate or not); the shuffles name exactly the rotating lanes
+  // rotation: the R lanes of a vector rotate together; the shuffles name exactly
+  // the rotating lanes (all of a bulk warp task's lanes, whose vectors are all K or
+  // all V; the outlier path's second rotation covers only the tail rows)
   const bool rot = (which ? rot_v : rot_k) && !prerotated;
   const unsigned rmask = __ballot_sync(0xffffffffu, rot);
   const int qt = which ? c.v_type : c.k_type;
