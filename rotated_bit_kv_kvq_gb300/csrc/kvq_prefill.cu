@@ -36,7 +36,7 @@
 //                           halves take the row maximum over all 64 scores,
 //                           so they agree without exchanging it), rescale O
 //                           in TMEM when a row's maximum grew by more than
-//                           2^4, write P_j, and finish with O / l, the
+//                           2^7, write P_j, and finish with O / l, the
 //                           inverse rotation and the output cast.
 // Every wait is bounded: a wait that gives up sets the status word's timeout
 // bit and a shared abort flag that ends the other roles' loops; the CTA then
@@ -62,7 +62,7 @@ constexpr int kStageThreads = 256;
 constexpr long long kPWait = 2000000000LL;  // ~1 s at 2 GHz per wait
 constexpr float kPLog2e = 1.4426950408889634f;
 constexpr float kInvScale = 0.00390625f;    // staged K/V values are x * 2^-8
-constexpr float kLazyRescale = 4.0f;        // log2 units: P*256 stays <= 2^12
+constexpr float kLazyRescale = 7.0f;        // log2 units: P*256 stays <= 2^15 (fp16 max 65504)
 
 template <int D>
 struct PL {
@@ -644,7 +644,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(AParams p) {
     ok = __all_sync(0xffffffffu, !*reinterpret_cast<volatile int*>(&sy->abort));
     if (!ok) break;
     const float mt = fmaxf(mo, mp) * 256.0f;  // keys were staged x 2^-8
-    // lazy rescale: move the reference maximum only when it grew by more than 2^4
+    // lazy rescale: move the reference maximum only when it grew by more than 2^7
     float alpha = 1.0f;
     const bool move = mt > m_used + kLazyRescale || (m_used == -INFINITY && mt > -INFINITY);
     if (move) {
