@@ -1,5 +1,6 @@
 """Host logic of the bench (no GPU): algorithmic byte counts against the per-unit
-figures, the recorded-traffic hash check and the clock-sample parsing.
+figures, the recorded-traffic hash check, the clock-sample parsing and the
+device-side wait ahead of a timed region.
 
 Per body token-head: (d/32) blocks of K and V (34 + 18 bytes for q8_0 / q4_0);
 per tail token-head: bf16 K and V (4 d bytes); per query head: bf16 q in and
@@ -87,3 +88,17 @@ def test_clock_sampler_parses_clocks_and_throttle_reasons(tmp_path):
     # without nvidia-smi the line says so instead of inventing clocks
     none = bench.ClockSampler(0)
     assert none.stop()["reasons"] == ["nvidia-smi unavailable"]
+
+
+def test_hold_device_uses_the_device_wait_when_present():
+    """The device-side wait ahead of a timed region's start event: called on the
+    current stream through torch's wait kernel when the torch build has one, a
+    no-op otherwise (never an error that would stop the bench)."""
+    import types
+    calls = []
+    fake = types.SimpleNamespace(cuda=types.SimpleNamespace(_sleep=lambda cycles: calls.append(cycles)))
+    bench.hold_device(fake)
+    assert calls == [200_000]
+    bench.hold_device(fake, cycles=1000)
+    assert calls == [200_000, 1000]
+    bench.hold_device(types.SimpleNamespace(cuda=types.SimpleNamespace()))  # no wait kernel: nothing happens
