@@ -755,8 +755,9 @@ def run_prefill_bench(torch, kvq, steps: int, warmup: int, seed: int = 0):
 # ---------------------------------------------------------------------------
 # the CPU oracle (cpu_baseline leg and --impl reference)
 # ---------------------------------------------------------------------------
-def oracle_pair_sample(w: wl.Workload, seed: int = 0):
-    """One (sequence, KV head) pair of the workload at full context, in the oracle."""
+def oracle_pair_sample(w: wl.Workload, seed: int = 0, extra: int = 0):
+    """One (sequence, KV head) pair of the workload at full context, in the oracle
+    (with room for `extra` more tokens)."""
     from oracle import kvq_oracle as ko
     rng = np.random.Generator(np.random.PCG64(seed))
     n = w.ctx
@@ -767,7 +768,7 @@ def oracle_pair_sample(w: wl.Workload, seed: int = 0):
     k = wl.round_bf16(k) if w.dtype == "bf16" else k
     v = wl.round_bf16(v) if w.dtype == "bf16" else v
     rot = ko.rotation_enabled(w.head_dim)
-    oc = ko.OracleCache(1, 1, w.head_dim, w.max_ctx(), w.tail_len, w.k_type, w.v_type, rot, rot)
+    oc = ko.OracleCache(1, 1, w.head_dim, w.max_ctx(extra), w.tail_len, w.k_type, w.v_type, rot, rot)
     oc.append(k, v)
     q = rng.standard_normal((1, w.group, w.head_dim)).astype(np.float32)
     # one KV head's share: packed body + bf16 tail + q/out (bf16) of its query heads
@@ -816,16 +817,38 @@ def run_reference(args):
         return
     from oracle import kvq_oracle as ko
     w = wl.WORKLOADS[args.workload]
-    oc, q, nbytes = oracle_pair_sample(w)
-    for _ in range(args.warmup):
+    n_new = max(1, w.append_per_step)
+    W, K = args.warmup, args.steps
+    oc, q, _ = oracle_pair_sample(w, extra=(W + K) * n_new)
+    # the step's new tokens of the sampled pair, drawn ahead of the timed region
+    rng = np.random.Generator(np.random.PCG64(11))
+    new = []
+    for _ in range(W + K):
+        kv = rng.standard_normal((2, 1, n_new, 1, w.head_dim), dtype=np.float32)
+        new.append(wl.round_bf16(kv) if w.dtype == "bf16" else kv)
+    # one pair's share of a step's bytes: its decode at the current length, and its append
+    pairs = w.batch * w.n_kv_heads
+
+    def pair_bytes(n):  # packed body + bf16 tail + q / out of its query heads, + its append
+        return (max(0, n - w.tail_len) * token_bytes(w) + min(n, w.tail_len) * 4 * w.head_dim
+                + w.group * w.head_dim * 4 + append_bytes(w, n_new) // pairs)
+
+    def step(i):
+        oc.append(new[i][0], new[i][1])
         ko.decode_attention(oc, q)
+
+    for i in range(W):
+        step(i)
+    n_first = int(oc.seq_len[0]) + n_new
     t0 = time.perf_counter()
-    for _ in range(args.steps):
-        ko.decode_attention(oc, q)
-    dt = (time.perf_counter() - t0) / args.steps
+    for i in range(K):
+        step(W + i)
+    dt = (time.perf_counter() - t0) / K
+    nbytes = sum(pair_bytes(n_first + i * n_new) for i in range(K)) / K
     val = round(nbytes / dt / 1e9, 4)
-    sample = (f"each step: decode attention of 1 of {w.batch * w.n_kv_heads} (sequence, KV head) pairs at "
-              f"{w.ctx} tokens, float64 numpy oracle")
+    sample = (f"each step: the append of {n_new} new token(s) and decode attention of 1 of {pairs} "
+              f"(sequence, KV head) pairs at {w.ctx}+ tokens (its share of the step's bytes), float64 / "
+              f"float32 numpy oracle")
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
