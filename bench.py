@@ -777,6 +777,16 @@ def oracle_pair_sample(w: wl.Workload, seed: int = 0, extra: int = 0):
     return oc, q, nbytes
 
 
+def pair_step_bytes(w: wl.Workload, n: int, n_new: int) -> int:
+    """One (sequence, KV head) pair's share of a step's algorithmic bytes: its decode
+    at n tokens (packed body, bf16 tail, q / out of its query heads) and its append of
+    n_new tokens.  For a batch whose sequences all hold n tokens, the pairs' shares add
+    up to decode_bytes + append_bytes."""
+    pairs = w.batch * w.n_kv_heads
+    return (max(0, n - w.tail_len) * token_bytes(w) + min(n, w.tail_len) * 4 * w.head_dim
+            + w.group * w.head_dim * 4 + append_bytes(w, n_new) // pairs)
+
+
 def cpu_baseline(w: wl.Workload, budget_s: float = 15.0):
     from oracle import kvq_oracle as ko
     oc, q, nbytes = oracle_pair_sample(w)
@@ -826,13 +836,7 @@ def run_reference(args):
     for _ in range(W + K):
         kv = rng.standard_normal((2, 1, n_new, 1, w.head_dim), dtype=np.float32)
         new.append(wl.round_bf16(kv) if w.dtype == "bf16" else kv)
-    # one pair's share of a step's bytes: its decode at the current length, and its append
     pairs = w.batch * w.n_kv_heads
-
-    def pair_bytes(n):  # packed body + bf16 tail + q / out of its query heads, + its append
-        return (max(0, n - w.tail_len) * token_bytes(w) + min(n, w.tail_len) * 4 * w.head_dim
-                + w.group * w.head_dim * 4 + append_bytes(w, n_new) // pairs)
-
     def step(i):
         oc.append(new[i][0], new[i][1])
         ko.decode_attention(oc, q)
@@ -844,7 +848,7 @@ def run_reference(args):
     for i in range(K):
         step(W + i)
     dt = (time.perf_counter() - t0) / K
-    nbytes = sum(pair_bytes(n_first + i * n_new) for i in range(K)) / K
+    nbytes = sum(pair_step_bytes(w, n_first + i * n_new, n_new) for i in range(K)) / K
     val = round(nbytes / dt / 1e9, 4)
     sample = (f"each step: the append of {n_new} new token(s) and decode attention of 1 of {pairs} "
               f"(sequence, KV head) pairs at {w.ctx}+ tokens (its share of the step's bytes), float64 / "

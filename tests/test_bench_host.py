@@ -102,3 +102,12 @@ def test_hold_device_uses_the_device_wait_when_present():
     bench.hold_device(fake, cycles=1000)
     assert calls == [200_000, 1000]
     bench.hold_device(types.SimpleNamespace(cuda=types.SimpleNamespace()))  # no wait kernel: nothing happens
+
+
+def test_reference_step_bytes_are_a_pairs_share():
+    """The reference arm's per-step bytes (one pair's append and decode) times the
+    number of (sequence, KV head) pairs equal the repo arm's step bytes."""
+    w = wl.WORKLOADS[wl.HEADLINE]
+    pairs = w.batch * w.n_kv_heads
+    for n in (65536, 65555, 500, 1024, 1025):
+        assert pairs * bench.pair_step_bytes(w, n, 1) == bench.decode_bytes(w, [n] * w.batch) + bench.append_bytes(w, 1)
